@@ -1,0 +1,303 @@
+"""Seeded synthetic inputs for FP8 paged decode attention.
+
+This module only draws numbers and lays them out; it computes no part of the
+attention.  Both the CUDA path and the fp64 oracle consume what it returns,
+byte for byte.
+
+Recipe (shapes follow the workloads on the FlashMLA "update fp8 support" page,
+the aiter sparse_mla_fwd page and the InfiniCore paged-attention page):
+
+* random numbers: a counter-based splitmix64 stream per (seed, purpose),
+  mapped to (0, 1] and then to N(0, 1) by Box-Muller, all in float64;
+* Q: N(0, 1) rounded to bf16;
+* KV: N(0, 1) over the valid token slots, one per-tensor scale
+  ``amax / 448`` (stored as float32), then E4M3 ("fn" encoding) of
+  ``x / scale`` clamped to +-448 -- the cast itself is torch's
+  ``float8_e4m3fn`` conversion, a library routine;
+* paging: the used pages are placed at a seeded random permutation of the
+  physical pool; spare pages and every slot past a sequence's length hold
+  the byte 0x7F (an E4M3 NaN), so any read that should not happen shows up.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+E4M3_MAX = 448.0
+POISON_BYTE = 0x7F
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def u64_stream(seed: int, purpose: int, n: int) -> np.ndarray:
+    """n splitmix64 outputs for the stream keyed by (seed, purpose)."""
+    key = _mix64(np.array([(seed * 1_000_003 + purpose) & 0xFFFFFFFFFFFFFFFF],
+                          dtype=np.uint64))[0]
+    idx = np.arange(1, n + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        return _mix64(key + idx * _GOLDEN)
+
+
+def uniform(seed: int, purpose: int, n: int) -> np.ndarray:
+    """Uniform float64 in (0, 1]."""
+    u = u64_stream(seed, purpose, n) >> np.uint64(11)
+    return (u.astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
+
+
+def normal(seed: int, purpose: int, shape) -> np.ndarray:
+    """N(0, 1) float64 by Box-Muller."""
+    n = int(np.prod(shape))
+    m = (n + 1) // 2
+    u1 = uniform(seed, 2 * purpose, m)
+    u2 = uniform(seed, 2 * purpose + 1, m)
+    r = np.sqrt(-2.0 * np.log(u1))
+    z = np.concatenate([r * np.cos(2.0 * math.pi * u2), r * np.sin(2.0 * math.pi * u2)])
+    return z[:n].reshape(shape)
+
+
+def permutation(seed: int, purpose: int, n: int) -> np.ndarray:
+    keys = u64_stream(seed, purpose, n)
+    return np.argsort(keys, kind="stable").astype(np.int64)
+
+
+def randint(seed: int, purpose: int, n: int, lo: int, hi: int) -> np.ndarray:
+    """Integers uniform in [lo, hi] (inclusive)."""
+    span = hi - lo + 1
+    u = uniform(seed, purpose, n)
+    return np.minimum(lo + np.floor(u * span).astype(np.int64), hi)
+
+
+def to_bf16(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def per_tensor_scale(values: np.ndarray) -> float:
+    """amax / 448 as the float32 value both sides use (1.0 for an all-zero tensor)."""
+    amax = float(np.max(np.abs(values))) if values.size else 0.0
+    return float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+
+
+def to_e4m3_bytes(x: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 bytes of x / scale (torch's float8_e4m3fn cast after clamping)."""
+    y = np.clip(np.asarray(x, dtype=np.float64) / scale, -E4M3_MAX, E4M3_MAX)
+    t = torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+# --------------------------------------------------------------------------
+# Dense MLA (d = 576 = 512 latent + 64 RoPE, dv = 512, one KV head, page 64)
+# --------------------------------------------------------------------------
+
+MLA_D = 576
+MLA_DV = 512
+MLA_PAGE = 64
+
+
+@dataclass
+class MLAInputs:
+    q: torch.Tensor            # bf16 [b, s_q, h_q, 576]
+    kv_cache: torch.Tensor     # uint8 (E4M3 bytes) [num_pages, 64, 576]
+    block_table: torch.Tensor  # int32 [b, max_pages]
+    seqlens: torch.Tensor      # int32 [b]
+    kv_scale: float            # float32 value
+    softmax_scale: float
+    causal: bool
+
+    @property
+    def b(self):
+        return self.q.shape[0]
+
+    @property
+    def s_q(self):
+        return self.q.shape[1]
+
+    @property
+    def h_q(self):
+        return self.q.shape[2]
+
+
+def mla_inputs(seed: int, b: int, s_q: int, h_q: int, seqlens, causal: bool = True,
+               spare_pages: int = 0, softmax_scale: float | None = None,
+               page_order: np.ndarray | None = None) -> MLAInputs:
+    """Paged MLA decode inputs.  ``seqlens`` is a list of cache lengths."""
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    assert seqlens.shape == (b,)
+    n_pages = (seqlens + MLA_PAGE - 1) // MLA_PAGE
+    used = int(n_pages.sum())
+    num_pages = max(used + spare_pages, 1)
+    perm = permutation(seed, 1, num_pages) if page_order is None else np.asarray(page_order)
+    max_pages = max(int(n_pages.max()) if b else 1, 1)
+    fill = int(perm[used]) if num_pages > used else 0
+    block_table = np.full((b, max_pages), fill, dtype=np.int32)
+    cache = np.full((num_pages, MLA_PAGE, MLA_D), POISON_BYTE, dtype=np.uint8)
+
+    vals = normal(seed, 2, (max(used, 1) * MLA_PAGE, MLA_D))[: used * MLA_PAGE]
+    valid = np.zeros(used * MLA_PAGE, dtype=bool)
+    k = 0
+    for i in range(b):
+        for p in range(int(n_pages[i])):
+            block_table[i, p] = perm[k + p]
+        lo = k * MLA_PAGE
+        valid[lo: lo + int(seqlens[i])] = True
+        k += int(n_pages[i])
+    scale = per_tensor_scale(vals[valid])
+    enc = to_e4m3_bytes(vals, scale)
+    enc[~valid] = POISON_BYTE
+    enc = enc.reshape(used, MLA_PAGE, MLA_D)
+    k = 0
+    for i in range(b):
+        for p in range(int(n_pages[i])):
+            cache[block_table[i, p]] = enc[k + p]
+        k += int(n_pages[i])
+
+    q = to_bf16(normal(seed, 3, (b, s_q, h_q, MLA_D)))
+    if softmax_scale is None:
+        softmax_scale = float(np.float32(1.0 / math.sqrt(MLA_D)))
+    return MLAInputs(q=q, kv_cache=torch.from_numpy(cache),
+                     block_table=torch.from_numpy(block_table),
+                     seqlens=torch.from_numpy(seqlens.astype(np.int32)),
+                     kv_scale=scale, softmax_scale=softmax_scale, causal=causal)
+
+
+def uniform_seqlens(seed: int, b: int, lo: int, hi: int) -> list[int]:
+    return [int(x) for x in randint(seed, 7, b, lo, hi)]
+
+
+# --------------------------------------------------------------------------
+# Sparse top-k MLA (rope-free d = dv = 512, one flat cache of rows)
+# --------------------------------------------------------------------------
+
+SPARSE_D = 512
+
+
+@dataclass
+class SparseInputs:
+    q: torch.Tensor          # bf16 [s_q, h_q, 512]
+    kv_cache: torch.Tensor   # uint8 [num_tokens, 512]
+    topk_idx: torch.Tensor   # int32 [s_q, topk]; -1 = skip
+    kv_scale: float
+    softmax_scale: float
+
+
+def sparse_inputs(seed: int, s_q: int, h_q: int = 16, num_tokens: int = 131072,
+                  topk: int = 2048) -> SparseInputs:
+    vals = normal(seed, 2, (num_tokens, SPARSE_D))
+    scale = per_tensor_scale(vals)
+    cache = to_e4m3_bytes(vals, scale)
+    idx = np.empty((s_q, topk), dtype=np.int32)
+    for t in range(s_q):
+        idx[t] = permutation(seed, 100 + t, num_tokens)[:topk]
+    q = to_bf16(normal(seed, 3, (s_q, h_q, SPARSE_D)))
+    return SparseInputs(q=q, kv_cache=torch.from_numpy(cache), topk_idx=torch.from_numpy(idx),
+                        kv_scale=scale,
+                        softmax_scale=float(np.float32(1.0 / math.sqrt(SPARSE_D))))
+
+
+PEAKY_Q0 = 7.0          # 1.75 * 2**2: exact in bf16 and, after a power-of-two row scale, in E4M3
+PEAKY_MARGIN = 9.0      # key 0 scores this much above every other key
+
+
+def sparse_peaky_inputs(seed: int, s_q: int = 2, h_q: int = 16, num_tokens: int = 131072,
+                        topk: int = 2048) -> SparseInputs:
+    """One key per query token scores +9 above 2047 keys that score exactly 0.
+
+    Dims [0, 256) carry the score, dims [256, 512) carry the values: Q is 0
+    there, the tail keys hold w + 0.1 N(0, 1) and key 0 holds z, so the output
+    on those dims is about 0.8 z + 0.2 w.  Key 0's dim 0 is the cache's
+    largest magnitude, so it encodes to exactly 448 and its score is
+    softmax_scale * 7 * 448 * kv_scale = 9 up to float32 rounding of the scales.
+    """
+    softmax_scale = float(np.float32(1.0 / math.sqrt(SPARSE_D)))
+    kappa = PEAKY_MARGIN / (softmax_scale * PEAKY_Q0)     # true value of key 0's dim 0
+    kv_scale = float(np.float32(kappa / E4M3_MAX))
+    half = SPARSE_D // 2
+    w = normal(seed, 11, (half,))
+    z = normal(seed, 12, (half,))
+    vals = np.zeros((num_tokens, SPARSE_D))
+    idx = np.empty((s_q, topk), dtype=np.int32)
+    perm = permutation(seed, 13, num_tokens)
+    for t in range(s_q):
+        rows = perm[t * topk:(t + 1) * topk]
+        key0 = rows[int(randint(seed, 14 + t, 1, 0, topk - 1)[0])]
+        vals[rows, half:] = w[None, :] + 0.1 * normal(seed, 20 + t, (topk, half))
+        vals[key0, :] = 0.0
+        vals[key0, 0] = E4M3_MAX * kv_scale
+        vals[key0, half:] = z
+        idx[t] = rows
+    cache = to_e4m3_bytes(vals, kv_scale)
+    q = np.zeros((s_q, h_q, SPARSE_D))
+    q[:, :, 0] = PEAKY_Q0
+    q[:, :, 1:half] = normal(seed, 30, (s_q, h_q, half - 1))
+    return SparseInputs(q=to_bf16(q), kv_cache=torch.from_numpy(cache),
+                        topk_idx=torch.from_numpy(idx), kv_scale=kv_scale,
+                        softmax_scale=softmax_scale)
+
+
+# --------------------------------------------------------------------------
+# GQA paged decode (separate K / V caches [num_blocks, h_kv, page, head_dim])
+# --------------------------------------------------------------------------
+
+
+@dataclass
+class GQAInputs:
+    q: torch.Tensor           # bf16 [bs, h_q, hd]
+    k_cache: torch.Tensor     # uint8 [num_blocks, h_kv, page, hd]
+    v_cache: torch.Tensor     # uint8 [num_blocks, h_kv, page, hd]
+    block_table: torch.Tensor # int32 [bs, max_blocks]
+    seqlens: torch.Tensor     # int32 [bs]
+    k_scale: float
+    v_scale: float
+    softmax_scale: float
+
+
+def gqa_inputs(seed: int, bs: int, seqlens, h_q: int = 32, h_kv: int = 8, hd: int = 128,
+               page: int = 16, spare_blocks: int = 0) -> GQAInputs:
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    n_blocks = (seqlens + page - 1) // page
+    used = int(n_blocks.sum())
+    num_blocks = max(used + spare_blocks, 1)
+    perm = permutation(seed, 1, num_blocks)
+    max_blocks = max(int(n_blocks.max()) if bs else 1, 1)
+    fill = int(perm[used]) if num_blocks > used else 0
+    block_table = np.full((bs, max_blocks), fill, dtype=np.int32)
+    valid = np.zeros((used, page), dtype=bool)
+    k = 0
+    for i in range(bs):
+        for p in range(int(n_blocks[i])):
+            block_table[i, p] = perm[k + p]
+            valid[k + p, : min(page, int(seqlens[i]) - p * page)] = True
+        k += int(n_blocks[i])
+    caches, scales = [], []
+    for purpose in (2, 4):
+        vals = normal(seed, purpose, (max(used, 1), h_kv, page, hd))[:used]
+        vmask = np.broadcast_to(valid[:, None, :, None], vals.shape)
+        scale = per_tensor_scale(vals[vmask])
+        enc = to_e4m3_bytes(vals, scale)
+        enc[~vmask] = POISON_BYTE
+        cache = np.full((num_blocks, h_kv, page, hd), POISON_BYTE, dtype=np.uint8)
+        k = 0
+        for i in range(bs):
+            for p in range(int(n_blocks[i])):
+                cache[block_table[i, p]] = enc[k + p]
+            k += int(n_blocks[i])
+        caches.append(torch.from_numpy(cache))
+        scales.append(scale)
+    q = to_bf16(normal(seed, 3, (bs, h_q, hd)))
+    return GQAInputs(q=q, k_cache=caches[0], v_cache=caches[1],
+                     block_table=torch.from_numpy(block_table),
+                     seqlens=torch.from_numpy(seqlens.astype(np.int32)),
+                     k_scale=scales[0], v_scale=scales[1],
+                     softmax_scale=float(np.float32(1.0 / math.sqrt(hd))))

@@ -1,0 +1,88 @@
+"""Properties of the restated page-range scheduler (pins that do not use the GPU).
+
+The partition rule is this library's own (the pages describe split-KV
+flash-decoding -- InfiniCore "FP8(E4M3) KV cache support in paged
+attention", split-kv commit -- but no scheduler), so it is pinned by what any
+correct partition must satisfy: every (sequence, page) is covered exactly
+once, in order; split counts and split indices agree with the coverage; the
+balanced rule keeps units within budget; the forced rule cuts near-equal
+chunks.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.attention import SCHED_FIXED_COST, unit_segments
+
+
+def _coverage(sched, seqlens, num_splits):
+    n = [(int(s) + 63) // 64 for s in seqlens]
+    seen = {}
+    order = []
+    split_ids = {}
+    for u in range(sched.shape[0]):
+        for (b, lo, hi, k) in unit_segments(sched[u], seqlens):
+            assert k == split_ids.get(b, 0)
+            split_ids[b] = k + 1
+            for p in range(lo, hi):
+                assert (b, p) not in seen
+                seen[(b, p)] = u
+                order.append((b, p))
+    expect = [(b, p) for b in range(len(n)) for p in range(n[b])]
+    assert order == expect
+    for b in range(len(n)):
+        assert num_splits[b + 1] - num_splits[b] == split_ids.get(b, 0)
+    return seen
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_balanced_partition_covers_each_page_once(seed):
+    rng = np.random.default_rng(seed)
+    b = int(rng.integers(1, 130))
+    seqlens = rng.integers(0, 9000, size=b)
+    seqlens[rng.random(b) < 0.1] = 0
+    units = int(rng.integers(1, 80))
+    sched, splits = oracle.schedule(seqlens, units)
+    _coverage(sched, seqlens, splits)
+    n = [(int(s) + 63) // 64 for s in seqlens]
+    total = sum(x + SCHED_FIXED_COST for x in n if x > 0)
+    budget = -(-total // units) + SCHED_FIXED_COST if total else 0
+    for u in range(units - 1):
+        cost = sum(hi - lo + SCHED_FIXED_COST for (_, lo, hi, _) in unit_segments(sched[u], seqlens))
+        assert cost <= budget
+
+
+def test_headline_batch_is_balanced():
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    seqlens = syn.uniform_seqlens(2, 64, 2048, 6144)
+    units = 76
+    sched, splits = oracle.schedule(seqlens, units)
+    _coverage(sched, seqlens, splits)
+    costs = [sum(hi - lo + SCHED_FIXED_COST for (_, lo, hi, _) in unit_segments(sched[u], seqlens))
+             for u in range(units)]
+    assert max(costs) <= 1.15 * (sum(costs) / units) + SCHED_FIXED_COST
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 8])
+def test_forced_splits(k):
+    seqlens = np.array([256, 300, 0, 1, 64 * 9])
+    units = 40
+    sched, splits = oracle.schedule(seqlens, units, force_splits=k)
+    _coverage(sched, seqlens, splits)
+    for b, s in enumerate(seqlens):
+        n = (int(s) + 63) // 64
+        assert splits[b + 1] - splits[b] == min(k, n)
+    sizes = {}
+    for u in range(units):
+        for (b, lo, hi, _) in unit_segments(sched[u], seqlens):
+            sizes.setdefault(b, []).append(hi - lo)
+    for b, sz in sizes.items():
+        assert max(sz) - min(sz) <= 1
+
+
+def test_all_empty_batch():
+    sched, splits = oracle.schedule([0, 0, 0], 5)
+    assert np.all(splits == 0)
+    for u in range(5):
+        assert unit_segments(sched[u], [0, 0, 0]) == []
