@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of FP8 paged MLA decode on one GB300 (or N replicas).
+
+Workload (default): the MTP decode shape of the FlashMLA "update fp8
+support" page -- b=64, s_q=2 (causal), h_q=64, d=576 (512 latent + 64 RoPE),
+dv=512, one KV head, page 64, seeded synthetic inputs with cache lengths
+uniform in [2048, 6144] (mean 4096), E4M3 KV with a per-tensor scale, FP8
+Q/P dots.  One step = the whole hot path over one batch: the tile
+scheduler (metadata), the decode kernel and the split-KV combine.
+
+Metric: TFLOPS with FLOPs = 2 * b * s_q * h_q * s_k * (576 + 512) summed
+over sequences (the convention that reproduces the page's TFLOPS column);
+the JSON line also carries us/call, KV GB/s and the roofline fraction.
+
+Timing: CUDA events on the launching stream around exactly K steps after W
+warm-up steps, a barrier and a synchronize on both sides, max over ranks.
+Three copies of the inputs (3 x ~165 MB, more than twice the 129 MB L2)
+rotate between steps, so every step reads its KV from HBM.
+
+Multi-GPU: the batch is data-parallel and needs no exchange, so N GPUs run
+N independent replicas of the per-GPU batch ("scaling": "weak").
+
+``--impl reference`` times the fp64 CPU oracle on the same workload (a
+bounded sample of sequences per step) on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+MLA_D, MLA_DV = 576, 512
+METRIC = "FP8-KV MLA decode µs/call, TFLOPS, KV GB/s and % roofline (b=64,s_q=2,s_k=4096)"
+WORKLOAD = dict(workload="mla_mtp_decode", b=64, s_q=2, h_q=64, h_kv=1, d=576, dv=512, page=64,
+                seqlens="uniform[2048,6144] seed 2", causal=True)
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "mla_decode_fp8_b64_sq2_traffic.txt")
+KERNEL_SOURCE = os.path.join(ROOT, "paged_decode_attention_fp8_gb300", "csrc", "mla_decode.cu")
+
+
+# ----------------------------------------------------------- accounting ----
+
+
+def mla_flops(seqlens, s_q, h_q, d=MLA_D, dv=MLA_DV):
+    """2 * s_q * h_q * s_k * (d + dv) per sequence (causal mask not discounted)."""
+    return sum(2.0 * s_q * h_q * int(s) * (d + dv) for s in seqlens)
+
+
+def mla_split_flops(seqlens, s_q, h_q):
+    """(FP8 flops, bf16 flops): latent Q.K and P.V run in E4M3, the 64-wide RoPE chunk in bf16."""
+    keys = sum(int(s) for s in seqlens)
+    return 2.0 * s_q * h_q * keys * (512 + MLA_DV), 2.0 * s_q * h_q * keys * 64
+
+
+def mla_bytes(seqlens, b, s_q, h_q):
+    """Algorithmic bytes: valid KV rows (576 B each), Q (bf16), out (bf16), lse (f32),
+    the block-table entries of the used pages and the seqlens."""
+    kv = sum(int(s) for s in seqlens) * MLA_D
+    pages = sum((int(s) + 63) // 64 for s in seqlens)
+    rows = b * s_q * h_q
+    return kv + rows * MLA_D * 2 + rows * MLA_DV * 2 + rows * 4 + pages * 4 + b * 4
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+def traffic_from_profile():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(KERNEL_SOURCE, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    vals = {}
+    with open(PROFILE_TRAFFIC) as f:
+        for line in f:
+            m = re.match(r"^(\w+):\s*(\S+)", line.strip())
+            if m:
+                vals[m.group(1)] = m.group(2)
+    if vals.get("kernel_source_sha256_16") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------- clocks ----
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["no samples"], samples=0)
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(smax), reasons=sorted(reasons), samples=len(sm))
+
+
+# ---------------------------------------------------------- our arm ----
+
+
+def build_inputs(seed, device, copies=3):
+    import torch
+
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    w = WORKLOAD
+    seqlens = syn.uniform_seqlens(2, w["b"], 2048, 6144)
+    inp = syn.mla_inputs(seed, w["b"], w["s_q"], w["h_q"], seqlens, causal=True, spare_pages=64)
+    sets = []
+    for c in range(copies):
+        q = inp.q.to(device)
+        kv = inp.kv_cache.to(device)
+        sets.append((q, kv))
+    bt = inp.block_table.to(device)
+    sl = inp.seqlens.to(device)
+    scale = torch.tensor([inp.kv_scale], dtype=torch.float32, device=device)
+    return inp, seqlens, sets, bt, sl, scale
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_decode_attention_fp8_gb300 as fm
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOAD
+    b, s_q, h_q = w["b"], w["s_q"], w["h_q"]
+    inp, seqlens, sets, bt, sl, scale = build_inputs(2 + 1000 * rank, dev)
+    units = fm.metadata_units()
+    tile_sched = torch.empty((units, 8), dtype=torch.int32, device=dev)
+    num_splits = torch.empty((b + 1,), dtype=torch.int32, device=dev)
+    out = torch.empty((b, s_q, h_q, MLA_DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=dev)
+    ws = torch.empty((fm.workspace_bytes(b, s_q, h_q, units),), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dot = args.dot
+
+    def step(i, ev=None):
+        q, kv = sets[i % len(sets)]
+        fm.get_metadata(sl, h_q, s_q, num_units=units, tile_sched=tile_sched, num_splits=num_splits)
+        if ev is not None:
+            ev[0].record(stream)
+        fm.decode(q, kv, bt, sl, scale, inp.softmax_scale, True, tile_sched, num_splits, dot_mode=dot,
+                  out=out, lse=lse, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert fm.last_device_error() == 0
+
+    kernel_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i, kernel_events[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    dec_ms = [a.elapsed_time(b_) for a, b_ in kernel_events]
+    assert fm.last_device_error() == 0
+
+    ms_per_step = total_ms / args.steps
+    flops = mla_flops(seqlens, s_q, h_q)
+    nbytes = mla_bytes(seqlens, b, s_q, h_q)
+    kv_bytes = sum(seqlens) * MLA_D
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    peaks = measured_peaks()
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    achieved = nbytes / (dec_avg_ms * 1e-3) / 1e9
+    f8, f16 = mla_split_flops(seqlens, s_q, h_q)
+    fp8_peak = 2.0 * peaks["bf16"]        # nominal E4M3 / bf16 dense ratio (4.5 / 2.25)
+    t_hbm = nbytes / (peaks["hbm"] * 1e9)
+    t_tensor = f8 / (fp8_peak * 1e12) + f16 / (peaks["bf16"] * 1e12)
+    roofline = dict(bound="hbm" if t_hbm >= t_tensor else "tensor", achieved=round(achieved, 1),
+                    peak=peaks["hbm"], unit="GB/s", frac=round(achieved / peaks["hbm"], 4),
+                    traffic=traffic_from_profile(),
+                    kernel="fp8mla_decode (decode + combine kernels)",
+                    algorithmic_bytes_per_launch=nbytes,
+                    t_hbm_us=round(t_hbm * 1e6, 2), t_tensor_us=round(t_tensor * 1e6, 2),
+                    roofline_frac_of_time=round(max(t_hbm, t_tensor) / (dec_avg_ms * 1e-3), 4),
+                    peak_source=f"{peaks['src']} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)")
+
+    e2e = measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, world)
+
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3" if dot == "fp8" else "bf16",
+        "data": "synthetic (seeded N(0,1) Q/KV, E4M3 per-tensor scale)",
+        "config": dict(WORKLOAD, dot=dot, l2="3 rotating input copies (~495 MB) > 2x L2",
+                       parallelism=f"replicas x{world}"),
+        "us_per_call": round(dec_avg_ms * 1e3, 2),
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "tflops_decode_call": round(flops / (dec_avg_ms * 1e-3) / 1e12, 1),
+        "kv_gbs": round(kv_bytes / (dec_avg_ms * 1e-3) / 1e9, 1),
+        "roofline": roofline,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(inp, seqlens, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, world):
+    """Same metric through the public API with host buffers: each step copies Q, the block
+    table and the seqlens from pinned host memory, runs metadata + decode, and reads out + lse
+    back.  The KV cache is the model's resident state (like weights) and stays in HBM."""
+    import torch
+
+    import paged_decode_attention_fp8_gb300 as fm
+    w = WORKLOAD
+    b, s_q, h_q = w["b"], w["s_q"], w["h_q"]
+    q_h = inp.q.pin_memory()
+    bt_h = inp.block_table.pin_memory()
+    sl_h = inp.seqlens.pin_memory()
+    out_h = torch.empty((b, s_q, h_q, MLA_DV), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((b, s_q, h_q), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(inp.q, device=dev)
+    bt_d = torch.empty_like(inp.block_table, device=dev)
+    sl_d = torch.empty_like(inp.seqlens, device=dev)
+    ts = torch.empty((units, 8), dtype=torch.int32, device=dev)
+    ns = torch.empty((b + 1,), dtype=torch.int32, device=dev)
+    out = torch.empty((b, s_q, h_q, MLA_DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=dev)
+    ws = torch.empty((fm.workspace_bytes(b, s_q, h_q, units),), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = max(args.steps // 10, 20)
+
+    def step(i):
+        _, kv = sets[i % len(sets)]
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        fm.get_metadata(sl_d, h_q, s_q, num_units=units, tile_sched=ts, num_splits=ns)
+        fm.decode(q_d, kv, bt_d, sl_d, scale, inp.softmax_scale, True, ts, ns, dot_mode=args.dot,
+                  out=out, lse=lse, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    return dict(value=round(world * flops / (ms * 1e-3) / 1e12, 2), unit="TFLOPS", ms_per_step=round(ms, 5),
+                h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h), steps=steps,
+                note="KV cache resident in HBM; per-step Q/block table/seqlens in, out/lse back")
+
+
+# ------------------------------------------------------ oracle baseline ----
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, seqlens, budget_s=15.0):
+    """The fp64 oracle as it stands, timed on a bounded sample of the batch's sequences."""
+    import oracle
+    w = WORKLOAD
+    done, t_used, flops = [], 0.0, 0.0
+    order = list(range(w["b"]))
+    t_start = time.perf_counter()
+    for bi in order:
+        t0 = time.perf_counter()
+        oracle.mla_decode(inp.q, inp.kv_cache, inp.block_table, inp.seqlens, inp.kv_scale, inp.softmax_scale,
+                          True, batches=[bi])
+        t_used += time.perf_counter() - t0
+        done.append(bi)
+        flops += mla_flops([seqlens[bi]], w["s_q"], w["h_q"])
+        if time.perf_counter() - t_start > budget_s:
+            break
+    tflops = flops / t_used / 1e12
+    full_ms = mla_flops(seqlens, w["s_q"], w["h_q"]) / (tflops * 1e12) * 1e3
+    return dict(value=round(tflops, 6), unit="TFLOPS", cores=cpu_cores(), kind="oracle",
+                sample=f"{len(done)} of {w['b']} sequences ({t_used:.1f} s); full batch ~{full_ms:.0f} ms/call",
+                threads_note="numpy fp64 (BLAS matmul may use up to `cores` threads)")
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    import oracle
+    w = WORKLOAD
+    seqlens = syn.uniform_seqlens(2, w["b"], 2048, 6144)
+    inp = syn.mla_inputs(2, w["b"], w["s_q"], w["h_q"], seqlens, causal=True, spare_pages=64)
+    per_step = max(1, int(args.ref_seqs))
+
+    def step(i):
+        picks = [(i * per_step + k) % w["b"] for k in range(per_step)]
+        oracle.mla_decode(inp.q, inp.kv_cache, inp.block_table, inp.seqlens, inp.kv_scale, inp.softmax_scale,
+                          True, batches=picks)
+        return mla_flops([seqlens[p] for p in picks], w["s_q"], w["h_q"])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for i in range(args.steps):
+        flops += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    tflops = flops / dt / 1e12
+    ms_per_step = dt / args.steps * 1e3
+    res = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(tflops, 6),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) Q/KV, E4M3 per-tensor scale)",
+        "config": dict(WORKLOAD, dot="exact fp64", sample=f"{per_step} of {w['b']} sequences per step"),
+        "cpu_baseline": dict(value=round(tflops, 6), unit="TFLOPS", cores=cpu_cores(), kind="oracle",
+                             sample=f"{per_step} of {w['b']} sequences per step, {args.steps} steps"),
+        "e2e": dict(value=round(tflops, 6), unit="TFLOPS", h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--dot", choices=["fp8", "bf16"], default="fp8")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-seqs", type=int, default=2, help="sequences of the batch per reference step")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        args.steps = 5 if args.steps is None else args.steps
+        args.warmup = 1 if args.warmup is None else args.warmup
+        run_reference(args)
+        return
+    args.steps = 20000 if args.steps is None else args.steps
+    args.warmup = 50 if args.warmup is None else max(args.warmup, 3)
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,222 @@
+/*
+ * fp8mla.h -- C ABI of libfp8mla.so: decode-phase attention over an FP8
+ * (E4M3, OCP "fn" encoding) paged KV cache on sm_103a.
+ *
+ * Three variants of one operation, all "softmax(scale * q . k) @ v over the
+ * keys of a paged cache", plus the bookkeeping around them:
+ *
+ *   fp8mla_get_metadata / fp8mla_decode  -- dense MLA decode: d = 576
+ *       (512 latent + 64 RoPE), dv = 512 (V is the first 512 dims of the
+ *       same cached row), one shared KV head, s_q = 1..2 query tokens with a
+ *       bottom-right causal mask.  FlashMLA "update fp8 support":
+ *       Improvements (FP8 Q and KV, Q.K over nine 64-wide K chunks with the
+ *       RoPE chunk kept at 16 bit) and the H800 test shape (b, s_q, h_q,
+ *       h_kv = 1, d = 576, dv = 512, causal).
+ *   sparse_mla_decode -- top-k sparse MLA: each query token attends to the
+ *       rows listed in its top-k index list of one flat cache (rope-free
+ *       d = dv = 512).  aiter "Support fp8 KV caches and fp8 dots in
+ *       sparse_mla_fwd on gfx942": Technical details (in-kernel Q
+ *       quantisation, P quantised as p * 128 with the factor divided out in
+ *       the epilogue) and Results (16 heads, top-k 2048).
+ *   paged_gqa_decode -- grouped-query paged decode with separate K and V
+ *       caches and split-KV flash-decoding.  InfiniCore "add FP8 blockwise
+ *       dequantize/GEMM operators and FP8(E4M3) KV cache support in paged
+ *       attention": Summary (FP8 decode kernel, split-kv with a combine
+ *       kernel, the "auto" waves heuristic) and the split-kv commit
+ *       (partial (max, sum_exp, weighted sum) triples, empty shards publish
+ *       m = -inf, l = 0, acc = 0).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument that names a tensor is a DEVICE pointer unless
+ *    stated otherwise; the caller owns all memory (inputs, outputs,
+ *    workspace, metadata).  The library allocates nothing on these calls;
+ *    it keeps only a small host-side cache of encoded TMA descriptors.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and returns as soon as its kernels are enqueued.
+ *  - Arguments are checked on the host before anything is launched; a bad
+ *    argument returns a status and launches nothing.  Device-side problems
+ *    (an index out of range, a bounded wait that ran out) never trap: the
+ *    kernel records a bit in a device status word and skips the work;
+ *    fp8mla_get_last_device_error() reads and clears it.
+ *  - Values: the cache holds E4M3 bytes; true value = kv_scale * decode(byte)
+ *    with one float32 per-tensor scale (amax / 448 on the InfiniCore page)
+ *    passed as a DEVICE pointer to one float.  Q is bf16.  Outputs: bf16
+ *    `out` and float32 `lse` = natural log of sum_j exp(scale * q . k_j).
+ *  - A row that sees no key (empty cache, causal cut, all indices -1) gets
+ *    out = 0 and lse = -inf (InfiniCore zero-length-row commit; FlashInfer
+ *    "add xqa fp8 mha and fp8 kv cache", review of fully masked rows).
+ *  - Cache bytes past a sequence's length and pages the block table does not
+ *    reference are never read and may hold anything (NaN included).
+ */
+#ifndef FP8MLA_H
+#define FP8MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FP8MLA_API __attribute__((visibility("default")))
+#else
+#define FP8MLA_API
+#endif
+
+typedef struct CUstream_st* fp8mla_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  FP8MLA_OK = 0,
+  FP8MLA_ERR_INVALID_ARG = 1,       /* null pointer, bad shape, missing kv scale, ... */
+  FP8MLA_ERR_UNSUPPORTED_DTYPE = 2, /* cache encoding other than OCP E4M3 */
+  FP8MLA_ERR_WORKSPACE_TOO_SMALL = 3,
+  FP8MLA_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
+  FP8MLA_ERR_DEVICE = 5             /* not a launch failure: see fp8mla_get_last_device_error */
+} fp8mla_status_t;
+
+/* Precision of the two dot products (Q.K and P.V).
+ *  FP8MLA_DOT_16BIT: Q, K, P and V enter the tensor cores as 16-bit values
+ *    (the E4M3 cache converts exactly); "bf16 dots" on the aiter page.
+ *  FP8MLA_DOT_FP8:   the latent part of Q is quantised in-kernel to E4M3
+ *    with a per-row power-of-two scale, the RoPE part of Q.K stays bf16
+ *    (FlashMLA page, Improvements), and P is quantised as E4M3(128 * p)
+ *    (aiter page, Technical details). */
+typedef enum { FP8MLA_DOT_16BIT = 0, FP8MLA_DOT_FP8 = 1 } fp8mla_dot_mode_t;
+
+/* Encoding of the cache bytes.  Only FP8MLA_KV_E4M3 (OCP e4m3 "fn", or a
+ * uint8 view of it) is accepted; the others are refused with
+ * FP8MLA_ERR_UNSUPPORTED_DTYPE instead of being misread (aiter page,
+ * Technical details: "a typed cache in the other arch's encoding is
+ * refused"). */
+typedef enum {
+  FP8MLA_KV_E4M3 = 0,
+  FP8MLA_KV_E4M3FNUZ = 1,
+  FP8MLA_KV_E5M2 = 2,
+  FP8MLA_KV_OTHER = 3
+} fp8mla_kv_dtype_t;
+
+/* Device status bits reported by fp8mla_get_last_device_error. */
+#define FP8MLA_DEV_WAIT_TIMEOUT 0x1u   /* a bounded mbarrier wait ran out; the CTA stopped */
+#define FP8MLA_DEV_BAD_PAGE 0x2u       /* block-table entry outside [0, num_pages) */
+#define FP8MLA_DEV_BAD_SEQLEN 0x4u     /* seqlen < 0 or more pages than the block table row */
+#define FP8MLA_DEV_BAD_INDEX 0x8u      /* top-k index outside [-1, num_tokens) */
+
+/* ------------------------------------------------------------------ MLA ---
+ * Work units.  The dense MLA kernel runs one work unit per pair of SMs (the
+ * two CTAs of a unit each own one half of dv).  fp8mla_metadata_units(n)
+ * is the number of units for a GPU with n SMs: max(1, n / 2). */
+FP8MLA_API int fp8mla_metadata_units(int num_sms);
+
+/* fp8mla_get_metadata -- split the batch's (sequence, 64-token page) work
+ * list into `num_units` contiguous page ranges of balanced cost (each page
+ * costs 1, each (sequence, unit) segment a fixed 4 more).  Computed once per
+ * decode step on the device, reused by every layer.
+ *   cache_seqlens  int32 [b] (device)
+ *   h_q, s_q       query heads and tokens (h_q * s_q <= 128)
+ *   num_units      fp8mla_metadata_units(num_sms)
+ *   force_splits   0 = balanced; k > 0 = cut every sequence into min(k,
+ *                  pages) near-equal chunks, one unit each (needs
+ *                  b * k <= num_units) -- for split-KV tests
+ *   tile_sched     int32 [num_units][8] (device, written): {b_begin,
+ *                  page_begin, b_end, page_end, split index of the first
+ *                  segment, 0, 0, 0}; the range ends before (b_end, page_end)
+ *   num_splits     int32 [b + 1] (device, written): prefix sum of the number
+ *                  of units touching each sequence (0 for an empty one). */
+FP8MLA_API fp8mla_status_t fp8mla_get_metadata(const int32_t* cache_seqlens, int b, int h_q, int s_q, int num_units,
+                                    int force_splits, int32_t* tile_sched, int32_t* num_splits,
+                                    fp8mla_stream_t stream);
+
+/* Workspace for split-KV partials of fp8mla_decode: (b + num_units)
+ * partial slots of 128 x 512 float32 accumulators plus 128 (m, l) pairs. */
+FP8MLA_API size_t fp8mla_workspace_bytes(int b, int s_q, int h_q, int num_units);
+
+/* fp8mla_decode -- dense MLA decode over the paged E4M3 cache.
+ *   q              bf16 [b, s_q, h_q, 576]
+ *   kv_cache       E4M3 bytes [num_pages, 64, 576]; row = 512 latent || 64 RoPE
+ *   kv_dtype       must be FP8MLA_KV_E4M3
+ *   block_table    int32 [b, max_pages]; logical page p of sequence i lives at
+ *                  physical page block_table[i * max_pages + p]
+ *   cache_seqlens  int32 [b]; keys per sequence (0 allowed)
+ *   kv_scale       float32 [1] (device): per-tensor dequantisation scale; NULL
+ *                  is refused (InfiniCore "F8 cache without scales fails
+ *                  loudly (Bad Parameter)")
+ *   softmax_scale  multiplier of q . k (e.g. 1/sqrt(576))
+ *   causal         1: query token i of s_q sees keys j < s_k - s_q + i + 1
+ *   tile_sched, num_splits, num_units -- from fp8mla_get_metadata on the same
+ *                  cache_seqlens
+ *   workspace      >= fp8mla_workspace_bytes(b, s_q, h_q, num_units) bytes,
+ *                  256-byte aligned; contents need not be initialised
+ *   out            bf16 [b, s_q, h_q, 512] (written)
+ *   lse            float32 [b, s_q, h_q] (written)
+ *   dot_mode       FP8MLA_DOT_FP8 or FP8MLA_DOT_16BIT
+ * Requires h_q * s_q <= 128, kv_cache / q / out 16-byte aligned. */
+FP8MLA_API fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype, int num_pages,
+                              const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                              const float* kv_scale, float softmax_scale, int causal, const int32_t* tile_sched,
+                              const int32_t* num_splits, int num_units, void* workspace, size_t workspace_bytes,
+                              void* out, float* lse, fp8mla_dot_mode_t dot_mode, int b, int s_q, int h_q,
+                              fp8mla_stream_t stream);
+
+/* ----------------------------------------------------------- sparse MLA ---
+ * sparse_mla_decode -- query token t attends to the cache rows
+ * topk_idx[t][0..topk) (an index of -1 is skipped), d = dv = 512 rope-free.
+ *   q            bf16 [s_q, h_q, 512], h_q <= 16... multiple of 1, h_q <= 64
+ *   kv_cache     E4M3 bytes [num_tokens, 512]
+ *   topk_idx     int32 [s_q, topk]
+ *   kv_scale     float32 [1] (device), NULL refused
+ *   num_splits   0 = auto, 1 = no split-K (one pass over all keys), k > 1 =
+ *                keys cut into k contiguous shards merged by the combine step
+ *   workspace    >= sparse_mla_workspace_bytes(s_q, h_q, topk, num_splits)
+ *   out          bf16 [s_q, h_q, 512]; lse float32 [s_q, h_q]
+ *   dot_mode     FP8MLA_DOT_FP8 (Q quantised per row, P as E4M3(128 p)) or
+ *                FP8MLA_DOT_16BIT */
+FP8MLA_API fp8mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype,
+                                  int64_t num_tokens, const int32_t* topk_idx, int topk, const float* kv_scale,
+                                  float softmax_scale, int num_splits, void* workspace, size_t workspace_bytes,
+                                  void* out, float* lse, fp8mla_dot_mode_t dot_mode, int s_q, int h_q,
+                                  fp8mla_stream_t stream);
+
+FP8MLA_API size_t sparse_mla_workspace_bytes(int s_q, int h_q, int topk, int num_splits);
+
+/* ------------------------------------------------------------------ GQA ---
+ * paged_gqa_decode -- grouped-query decode; q head h reads KV head
+ * h / (h_q / h_kv).
+ *   q            bf16 [bs, h_q, head_dim]
+ *   k_cache      E4M3 bytes [num_blocks, h_kv, page_size, head_dim]
+ *   v_cache      E4M3 bytes [num_blocks, h_kv, page_size, head_dim]
+ *   k_scale, v_scale  float32 [1] each (device), NULL refused
+ *   block_table  int32 [bs, max_blocks]; seqlens int32 [bs]
+ *   num_splits   0 = auto (no split while bs * h_kv fills the GPU, else
+ *                enough key shards to fill it, at most 16); k >= 1 forced
+ *   workspace    >= paged_gqa_workspace_bytes(bs, h_q, head_dim, splits)
+ *   out          bf16 [bs, h_q, head_dim]; lse float32 [bs, h_q]
+ * Requires head_dim == 128, page_size == 16, h_q % h_kv == 0, h_q / h_kv <= 16. */
+FP8MLA_API fp8mla_status_t paged_gqa_decode(const void* q, const void* k_cache, const void* v_cache,
+                                 fp8mla_kv_dtype_t kv_dtype, int num_blocks, const float* k_scale,
+                                 const float* v_scale, const int32_t* block_table, int max_blocks,
+                                 const int32_t* seqlens, float softmax_scale, int num_splits, void* workspace,
+                                 size_t workspace_bytes, void* out, float* lse, int bs, int h_q, int h_kv,
+                                 int head_dim, int page_size, fp8mla_stream_t stream);
+
+FP8MLA_API size_t paged_gqa_workspace_bytes(int bs, int h_q, int head_dim, int max_splits);
+
+/* Number of key shards paged_gqa_decode will use for these arguments
+ * (num_splits as passed: 0 = auto).  Host-only, no device access. */
+FP8MLA_API int paged_gqa_num_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_splits);
+
+/* ------------------------------------------------------------- status ---- */
+
+/* Synchronises `stream`, returns in *code_out the OR of the FP8MLA_DEV_* bits
+ * recorded since the last call on the current device, and clears them. */
+FP8MLA_API fp8mla_status_t fp8mla_get_last_device_error(fp8mla_stream_t stream, uint32_t* code_out);
+
+/* Static string naming a status code. */
+FP8MLA_API const char* fp8mla_status_string(fp8mla_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8MLA_H */

@@ -1,0 +1,55 @@
+// Shared constants and the bounded mbarrier wait used by every kernel.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fp8mla.h"
+#include "ptx.cuh"
+
+namespace fp8mla {
+
+// A wait that has not completed after this long is treated as a hang: the
+// kernel records FP8MLA_DEV_WAIT_TIMEOUT and stops instead of spinning on.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint32_t kWaitMinPolls = 1u << 16;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Bounded wait on an mbarrier phase.  Returns false (without waiting further)
+// once *abort_flag is set by any thread of the CTA, or after the limit, in
+// which case it sets the flag and the status bit itself.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                             uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (it > kWaitMinPolls && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (abort_flag != nullptr) *abort_flag = 1u;
+        atomicOr(status, FP8MLA_DEV_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Pages of a sequence; 0 (and a status bit) for a length the block table cannot hold.
+__device__ __forceinline__ int seq_pages(int s_k, int page, int max_pages, uint32_t* status) {
+  if (s_k <= 0) {
+    if (s_k < 0) atomicOr(status, FP8MLA_DEV_BAD_SEQLEN);
+    return 0;
+  }
+  const int n = (s_k + page - 1) / page;
+  if (n > max_pages) {
+    atomicOr(status, FP8MLA_DEV_BAD_SEQLEN);
+    return 0;
+  }
+  return n;
+}
+
+}  // namespace fp8mla

@@ -1,0 +1,611 @@
+// Paged GQA decode over separate E4M3 K / V caches, tcgen05 + TMA, sm_103a.
+//
+// The operation (InfiniCore "add FP8 blockwise dequantize/GEMM operators and
+// FP8(E4M3) KV cache support in paged attention": Summary, the FP8 paged
+// attention decode kernel with split-kv): for batch b and query head h,
+//   out[b, h] = softmax_j(scale * q[b, h] . k_j) @ v_j
+// with k_j = k_scale * E4M3(K[block_table[b][j / 16], kvh, j % 16]) and v_j
+// likewise from V, kvh = h / (h_q / h_kv).
+//
+// GB300 design (swap-AB, one CTA per (sequence, KV head, split)):
+//   * 128 tokens (8 pages of 16) per step; each page's K and V tile
+//     [16 tokens x 128 B] arrives by one TMA each (128-byte swizzle).
+//   * 16-bit dots: converter threads turn the E4M3 tiles into f16 (exact)
+//     in 128-byte-swizzled tiles; Q (the head group, <= 16 heads) is f16
+//     with a per-head power-of-two scale.
+//   * S^T = K Q^T: M = 128 tokens, N = 16, K = 128 (8 f16 MMAs); softmax
+//     across TMEM lanes (per-head max by shuffles + a 4-warp exchange; each
+//     thread keeps partial sums), P^T (f16) to shared memory, then
+//     O^T = V^T P^T with V^T read MN-major straight from the converted tile.
+//   * Split-KV over the token dimension with a combine kernel; the split
+//     count follows the FA2-style "waves" rule: none while the grid already
+//     fills the GPU, else the smallest count within 85% of the best wave
+//     efficiency (InfiniCore page, Summary: the "auto" heuristic).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "gqa_decode.h"
+#include "mla_decode.h"
+
+namespace fp8mla {
+
+__device__ uint32_t g_status_gqa;
+
+namespace gqa {
+
+constexpr int kHd = 128;
+constexpr int kPage = 16;
+constexpr int kTok = 128;               // tokens per step (MMA M)
+constexpr int kPagesPerStep = kTok / kPage;
+constexpr int kN = 16;                  // head group, padded (MMA N)
+constexpr int kThreads = 256;
+constexpr int kStages = 2;
+constexpr int kRawTile = kTok * kHd;    // 16 KB of E4M3 per operand per step
+constexpr int kCvtAtom = kTok * 128;    // one 64-dim f16 atom (16 KB)
+constexpr int kOffRawK = 0, kOffRawV = kRawTile, kOffK16 = 2 * kRawTile, kOffV16 = kOffK16 + 2 * kCvtAtom;
+constexpr int kStageBytes = kOffV16 + 2 * kCvtAtom;   // 96 KB
+constexpr int kQBytes = 2 * kN * 128;
+constexpr int kPBytes = 2 * kN * 128;
+constexpr float kTau = 8.0f;
+constexpr uint32_t kTmemCols = 32, kTS = 0, kTO = 16;
+
+struct Params {
+  const uint16_t* q;           // bf16 [bs, h_q, 128]
+  const int32_t* block_table;  // [bs, max_blocks]
+  const int32_t* seqlens;      // [bs]
+  const float* k_scale;
+  const float* v_scale;
+  uint16_t* out;               // bf16 [bs, h_q, 128]
+  float* lse;                  // [bs, h_q]
+  float* ws_o;                 // [bs * h_kv * splits, 16, 128]  -- indexed per (b, kv head) sequence
+  float2* ws_ml;
+  int num_blocks, max_blocks, bs, h_q, h_kv, group, splits;
+  float softmax_scale;
+};
+
+struct Smem {
+  uint64_t kv_full[kStages], kv_empty[kStages], cvt_ready[kStages];
+  uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma;
+  uint32_t tmem_base, abort_flag, prod_ok;
+  float qs[kN];
+  float red[4][kN];
+  float red2[4][kN];
+};
+
+constexpr size_t kSmemBytes = kStages * kStageBytes + kQBytes + kPBytes + sizeof(Smem) + 1024;
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  const bool ok = wait_bounded(bar, parity, abort_flag, &g_status_gqa);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+// Smallest e with amax <= 2^14 * 2^e: keeps f16 products of Q and E4M3 values far from overflow.
+__device__ __forceinline__ int pow2_exp_f16(float amax) {
+  const uint32_t bits = __float_as_uint(amax);
+  const int expo = static_cast<int>((bits >> 23) & 0xFFu);
+  if (expo == 0) return 0;
+  const int e = (expo - 127) + ((bits & 0x7FFFFFu) ? 1 : 0) - 14;
+  return max(min(e, 100), -100);
+}
+
+__device__ __forceinline__ uint32_t f16x2_of_e4m3x2(uint32_t two_bytes) { return e4m3x2_to_f16x2(two_bytes); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const Params prm) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* q_tile = smem + kStages * kStageBytes;
+  uint8_t* p_tile = q_tile + kQBytes;
+  Smem* sm = reinterpret_cast<Smem*>(p_tile + kPBytes);
+  volatile uint32_t* abort_flag = &sm->abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int split = blockIdx.x % prm.splits;
+  const int seq = blockIdx.x / prm.splits;      // (b, kv head)
+  const int b = seq / prm.h_kv;
+  const int kvh = seq % prm.h_kv;
+
+  int s_k = prm.seqlens[b];
+  int n_pages = s_k > 0 ? (s_k + kPage - 1) / kPage : 0;
+  if (s_k < 0 || n_pages > prm.max_blocks) {
+    if (threadIdx.x == 0) atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_SEQLEN);
+    s_k = 0;
+    n_pages = 0;
+  }
+  const int n_steps_all = (n_pages + kPagesPerStep - 1) / kPagesPerStep;
+  const int st0 = static_cast<int>((static_cast<long long>(split) * n_steps_all) / prm.splits);
+  const int st1 = static_cast<int>((static_cast<long long>(split + 1) * n_steps_all) / prm.splits);
+  const int nsteps = st1 - st0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm->kv_full[s], 1);
+      mbar_init(&sm->kv_empty[s], 1);
+      mbar_init(&sm->cvt_ready[s], 1);
+    }
+    mbar_init(&sm->s_full, 1);
+    mbar_init(&sm->s_free, 128);
+    mbar_init(&sm->p_full, 128);
+    mbar_init(&sm->pv_done, 1);
+    mbar_init(&sm->q_full, 128);
+    mbar_init(&sm->final_mma, 1);
+    sm->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int i = 0;
+      for (; i < nsteps; ++i) {
+        const int st = i % kStages, use = i / kStages;
+        if (use > 0 && !wait_bounded(&sm->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa)) break;
+        const int p0 = (st0 + i) * kPagesPerStep;
+        const int np = min(kPagesPerStep, n_pages - p0);
+        mbar_arrive_expect_tx(&sm->kv_full[st], 2u * np * kPage * kHd);
+        uint8_t* sb = smem + st * kStageBytes;
+        for (int p = 0; p < np; ++p) {
+          int blk = prm.block_table[static_cast<size_t>(b) * prm.max_blocks + p0 + p];
+          if (blk < 0 || blk >= prm.num_blocks) {
+            atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_PAGE);
+            blk = 0;
+          }
+          const int row = (blk * prm.h_kv + kvh) * kPage;
+          tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->kv_full[st], 0, row, 0);
+          tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->kv_full[st], 0, row, 0);
+        }
+      }
+      for (int j = max(0, i - kStages); j < i; ++j)
+        wait_bounded(&sm->kv_full[j % kStages], (j / kStages) & 1, nullptr, &g_status_gqa);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, kN, 128);  // f16: K (K-major) x Q (K-major)
+      constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, 0, kN, 128);  // f16: V^T (MN-major) x P^T (K-major)
+      const uint32_t qb = smem_u32(q_tile), pb = smem_u32(p_tile);
+      bool ok = wait_bounded(&sm->q_full, 0, abort_flag, &g_status_gqa);
+      auto issue_pv = [&](int j) -> bool {
+        if (!wait_bounded(&sm->p_full, j & 1, abort_flag, &g_status_gqa)) return false;
+        tc_fence_after();
+        const int st = j % kStages;
+        const uint32_t vb = smem_u32(smem + st * kStageBytes + kOffV16);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ss(tmem + kTO, make_sdesc(vb + kk * 2048, kCvtAtom, 1024, SWIZZLE_128B),
+                     make_sdesc(pb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_pv,
+                     (j == 0 && kk == 0) ? 0u : 1u);
+        tc_commit(&sm->pv_done);
+        tc_commit(&sm->kv_empty[st]);
+        return true;
+      };
+      for (int i = 0; ok && i < nsteps; ++i) {
+        const int st = i % kStages, use = i / kStages;
+        if (!wait_bounded(&sm->cvt_ready[st], use & 1, abort_flag, &g_status_gqa) ||
+            (i > 0 && !wait_bounded(&sm->s_free, (i - 1) & 1, abort_flag, &g_status_gqa))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kb = smem_u32(smem + st * kStageBytes + kOffK16);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ss(tmem + kTS, make_sdesc(kb + (kk >> 2) * kCvtAtom + (kk & 3) * 32, 16, 1024, SWIZZLE_128B),
+                     make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
+                     kk > 0 ? 1u : 0u);
+        tc_commit(&sm->s_full);
+        if (i > 0 && !issue_pv(i - 1)) ok = false;
+      }
+      if (ok && nsteps > 0) issue_pv(nsteps - 1);
+      tc_commit(&sm->final_mma);
+      wait_bounded(&sm->final_mma, 0, nullptr, &g_status_gqa);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------ Q prep, conversion, softmax, epilogue ----
+    const int r = threadIdx.x - 128;   // token row of a step / TMEM lane / output dim
+    const int w = warp - 4;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(w * 32) << 16);
+    const float k_scale = *prm.k_scale, v_scale = *prm.v_scale;
+    const uint16_t* qgrp = prm.q + (static_cast<size_t>(b) * prm.h_q + kvh * prm.group) * kHd;
+    {
+      // Q tile: thread (head qh, eighth qj) converts dims [16 qj, 16 qj + 16) to f16 / qs
+      const int qh = r / 8, qj = r % 8;
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (qh < prm.group) {
+        v0 = __ldg(reinterpret_cast<const uint4*>(qgrp + qh * kHd + qj * 16));
+        v1 = __ldg(reinterpret_cast<const uint4*>(qgrp + qh * kHd + qj * 16 + 8));
+      }
+      float amax = 0.f;
+      const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(wd[k])), fabsf(bf16_hi(wd[k]))));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+      const int e = pow2_exp_f16(amax);
+      const float inv = exp2i(-e);
+      if (qj == 0) sm->qs[qh] = exp2i(e);
+      uint32_t h16[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) h16[k] = pack_f16x2(bf16_lo(wd[k]) * inv, bf16_hi(wd[k]) * inv);
+      // dims [16 qj, 16 qj + 16) = atom qj / 4, chunks 2 (qj % 4), 2 (qj % 4) + 1
+      uint8_t* row = q_tile + (qj / 4) * (kN * 128) + (qh / 8) * 1024 + (qh % 8) * 128;
+      *reinterpret_cast<uint4*>(row + (((2 * (qj % 4)) ^ (qh % 8)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+      *reinterpret_cast<uint4*>(row + (((2 * (qj % 4) + 1) ^ (qh % 8)) << 4)) =
+          make_uint4(h16[4], h16[5], h16[6], h16[7]);
+      fence_proxy_async_smem();
+      named_bar_sync(2, 128);
+      mbar_arrive(&sm->q_full);
+    }
+    float c_h[kN], m_h[kN], l_h[kN];
+#pragma unroll
+    for (int h = 0; h < kN; ++h) {
+      c_h[h] = prm.softmax_scale * kLog2e * sm->qs[h] * k_scale;
+      m_h[h] = kNegInf;
+      l_h[h] = 0.f;
+    }
+    bool ok = true;
+    for (int i = 0; i < nsteps; ++i) {
+      const int st = i % kStages, use = i / kStages;
+      const int tok = (st0 + i) * kTok + r;
+      const bool live = tok < s_k;
+      // ---- convert K and V rows of token r to f16 ----
+      if (!warp_wait(&sm->kv_full[st], use & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint8_t* sb = smem + st * kStageBytes;
+      {
+        const int sw = r & 7;
+        const uint8_t* srck = sb + kOffRawK + r * 128;
+        const uint8_t* srcv = sb + kOffRawV + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {   // 16 E4M3 -> 16 f16 (two 16-byte chunks)
+          uint4 ko = make_uint4(0, 0, 0, 0), ko2 = ko, vo = ko, vo2 = ko;
+          if (live) {
+            const uint4 kv = *reinterpret_cast<const uint4*>(srck + ((c ^ sw) << 4));
+            const uint4 vv = *reinterpret_cast<const uint4*>(srcv + ((c ^ sw) << 4));
+            ko = make_uint4(f16x2_of_e4m3x2(kv.x & 0xFFFFu), f16x2_of_e4m3x2(kv.x >> 16), f16x2_of_e4m3x2(kv.y & 0xFFFFu),
+                            f16x2_of_e4m3x2(kv.y >> 16));
+            ko2 = make_uint4(f16x2_of_e4m3x2(kv.z & 0xFFFFu), f16x2_of_e4m3x2(kv.z >> 16),
+                             f16x2_of_e4m3x2(kv.w & 0xFFFFu), f16x2_of_e4m3x2(kv.w >> 16));
+            vo = make_uint4(f16x2_of_e4m3x2(vv.x & 0xFFFFu), f16x2_of_e4m3x2(vv.x >> 16), f16x2_of_e4m3x2(vv.y & 0xFFFFu),
+                            f16x2_of_e4m3x2(vv.y >> 16));
+            vo2 = make_uint4(f16x2_of_e4m3x2(vv.z & 0xFFFFu), f16x2_of_e4m3x2(vv.z >> 16),
+                             f16x2_of_e4m3x2(vv.w & 0xFFFFu), f16x2_of_e4m3x2(vv.w >> 16));
+          }
+          // dims [16 c, 16 c + 16): f16 atom c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1
+          uint8_t* dk = sb + kOffK16 + (c / 4) * kCvtAtom + r * 128;
+          uint8_t* dv = sb + kOffV16 + (c / 4) * kCvtAtom + r * 128;
+          *reinterpret_cast<uint4*>(dk + (((2 * (c % 4)) ^ sw) << 4)) = ko;
+          *reinterpret_cast<uint4*>(dk + (((2 * (c % 4) + 1) ^ sw) << 4)) = ko2;
+          *reinterpret_cast<uint4*>(dv + (((2 * (c % 4)) ^ sw) << 4)) = vo;
+          *reinterpret_cast<uint4*>(dv + (((2 * (c % 4) + 1) ^ sw) << 4)) = vo2;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (r == 0) mbar_arrive(&sm->cvt_ready[st]);
+      }
+      // ---- softmax over this step's tokens ----
+      if (!warp_wait(&sm->s_full, i & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t s[kN];
+      tmem_ld16(lane_base + kTS, s);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sm->s_free);
+      float v[kN];
+#pragma unroll
+      for (int h = 0; h < kN; ++h) v[h] = live ? __uint_as_float(s[h]) * c_h[h] : kNegInf;
+#pragma unroll
+      for (int h = 0; h < kN; ++h) {
+        float x = v[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        if (lane == 0) sm->red[w][h] = x;
+      }
+      named_bar_sync(2, 128);
+      float alpha[kN];
+      bool any_rescale = false;
+#pragma unroll
+      for (int h = 0; h < kN; ++h) {
+        const float mx = fmaxf(fmaxf(sm->red[0][h], sm->red[1][h]), fmaxf(sm->red[2][h], sm->red[3][h]));
+        alpha[h] = 1.f;
+        if (mx > m_h[h] + kTau) {
+          alpha[h] = ex2_approx(m_h[h] - mx);
+          any_rescale |= (i > 0);
+          m_h[h] = mx;
+        }
+      }
+      named_bar_sync(2, 128);
+      uint32_t ph[kN / 2];
+#pragma unroll
+      for (int h = 0; h < kN; h += 2) {
+        const float p0 = ex2_approx(v[h] - (m_h[h] == kNegInf ? 0.f : m_h[h]));
+        const float p1 = ex2_approx(v[h + 1] - (m_h[h + 1] == kNegInf ? 0.f : m_h[h + 1]));
+        l_h[h] = l_h[h] * alpha[h] + p0;
+        l_h[h + 1] = l_h[h + 1] * alpha[h + 1] + p1;
+        ph[h / 2] = pack_f16x2(p0, p1);
+      }
+      if (i > 0 && !warp_wait(&sm->pv_done, (i - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (any_rescale) {
+        uint32_t o[kN];
+        tmem_ld16(lane_base + kTO, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < kN; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+        tmem_st16(lane_base + kTO, o);
+        tmem_st_wait();
+      }
+      // P^T (K-major, f16): row h, token r -> atom r / 64, chunk (r % 64) / 8, element r % 8
+      {
+        const int a = r / 64, ch = (r % 64) / 8, el = r % 8;
+#pragma unroll
+        for (int h = 0; h < kN; ++h) {
+          const uint16_t val = static_cast<uint16_t>((h & 1) ? (ph[h / 2] >> 16) : (ph[h / 2] & 0xFFFFu));
+          *reinterpret_cast<uint16_t*>(p_tile + a * (kN * 128) + (h / 8) * 1024 + (h % 8) * 128 +
+                                       ((ch ^ (h % 8)) << 4) + el * 2) = val;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm->p_full);
+    }
+
+    const bool whole = prm.splits == 1;
+    const size_t slot = static_cast<size_t>(seq) * prm.splits + split;
+    if (ok && nsteps > 0 && warp_wait(&sm->pv_done, (nsteps - 1) & 1, abort_flag)) {
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < kN; ++h) {
+        float x = l_h[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) sm->red2[w][h] = x;
+      }
+      named_bar_sync(2, 128);
+      uint32_t o[kN];
+      tmem_ld16(lane_base + kTO, o);
+      tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < kN; ++h) {
+        if (h >= prm.group) break;
+        const float lsum = (sm->red2[0][h] + sm->red2[1][h]) + (sm->red2[2][h] + sm->red2[3][h]);
+        const int hq = kvh * prm.group + h;
+        if (whole) {
+          const float f = lsum > 0.f ? v_scale / lsum : 0.f;
+          prm.out[(static_cast<size_t>(b) * prm.h_q + hq) * kHd + r] =
+              static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[h]) * f, 0.f));
+          if (r == 0)
+            prm.lse[static_cast<size_t>(b) * prm.h_q + hq] =
+                lsum > 0.f ? (m_h[h] + lg2_approx(lsum)) * kLn2 : kNegInf;
+        } else {
+          prm.ws_o[(slot * kN + h) * kHd + r] = __uint_as_float(o[h]) * v_scale;
+          if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(lsum > 0.f ? m_h[h] : kNegInf, lsum);
+        }
+      }
+    } else if (ok && nsteps == 0) {
+      for (int h = 0; h < prm.group; ++h) {
+        const int hq = kvh * prm.group + h;
+        if (whole) {
+          prm.out[(static_cast<size_t>(b) * prm.h_q + hq) * kHd + r] = 0;
+          if (r == 0) prm.lse[static_cast<size_t>(b) * prm.h_q + hq] = kNegInf;
+        } else {
+          prm.ws_o[(slot * kN + h) * kHd + r] = 0.f;
+          if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(kNegInf, 0.f);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Merge of split partials: one warp per (sequence = (b, kv head), head), lane l owns 4 dims.
+__global__ void gqa_combine_kernel(const float* __restrict__ ws_o, const float2* __restrict__ ws_ml, int splits,
+                                   int group, int h_q, int h_kv, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  const int seq = blockIdx.x;
+  const int h = blockIdx.y * 4 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (h >= group) return;
+  const int b = seq / h_kv, kvh = seq % h_kv;
+  const size_t row = static_cast<size_t>(b) * h_q + kvh * group + h;
+  float big_m = kNegInf;
+  for (int s = 0; s < splits; ++s) big_m = fmaxf(big_m, ws_ml[(static_cast<size_t>(seq) * splits + s) * kN + h].x);
+  uint16_t* orow = out + row * kHd + lane * 4;
+  if (big_m == kNegInf) {
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0, 0);
+    if (lane == 0) lse[row] = kNegInf;
+    return;
+  }
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, big_l = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const size_t slot = (static_cast<size_t>(seq) * splits + s) * kN + h;
+    const float2 ml = ws_ml[slot];
+    if (ml.x == kNegInf) continue;
+    const float wgt = ex2_approx(ml.x - big_m);
+    big_l += ml.y * wgt;
+    const float4 v = *reinterpret_cast<const float4*>(ws_o + slot * kHd + lane * 4);
+    acc[0] += wgt * v.x;
+    acc[1] += wgt * v.y;
+    acc[2] += wgt * v.z;
+    acc[3] += wgt * v.w;
+  }
+  const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
+  *reinterpret_cast<uint2*>(orow) =
+      make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  if (lane == 0) lse[row] = big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 : kNegInf;
+}
+
+// ---------------------------------------------------------------- host ----
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 3-D view {128 B, rows, 1} of a cache as [num_blocks * h_kv * 16] rows of 128 bytes, box = one page.
+bool encode_pages(CUtensorMap* map, const void* base, long long rows) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHd), static_cast<cuuint64_t>(rows), 1};
+  const cuuint64_t strides[2] = {kHd, static_cast<cuuint64_t>(rows) * kHd};
+  const cuuint32_t box[3] = {128, kPage, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace gqa
+
+int gqa_choose_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_splits) {
+  const int max_steps = std::max(1, (max_seqlen + gqa::kTok - 1) / gqa::kTok);
+  if (num_splits > 0) return std::max(1, std::min(num_splits, max_steps));
+  const long long ctas = static_cast<long long>(std::max(bs, 1)) * std::max(h_kv, 1);
+  if (num_sms < 1 || ctas * 5 >= static_cast<long long>(num_sms) * 4) return 1;  // grid already ~fills the GPU
+  const int cap = std::min(16, max_steps);
+  double eff[17] = {0}, best = 0;
+  for (int s = 1; s <= cap; ++s) {
+    const long long n = ctas * s;
+    const long long waves = (n + num_sms - 1) / num_sms;
+    eff[s] = static_cast<double>(n) / static_cast<double>(waves * num_sms);
+    best = std::max(best, eff[s]);
+  }
+  for (int s = 1; s <= cap; ++s)
+    if (eff[s] >= 0.85 * best) return s;
+  return 1;
+}
+
+size_t gqa_workspace_bytes(int bs, int h_q, int head_dim, int max_splits) {
+  (void)h_q;
+  if (bs < 1 || max_splits < 2 || head_dim != gqa::kHd) return 0;
+  // slots: every (b, kv head) pair needs max_splits slots of 16 heads; h_kv <= h_q bounds the pairs
+  const size_t slots = static_cast<size_t>(bs) * std::max(h_q, 1) * max_splits;
+  return gqa::round_up(slots * gqa::kN * gqa::kHd * sizeof(float), 256) +
+         gqa::round_up(slots * gqa::kN * sizeof(float2), 256);
+}
+
+fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                 const float* k_scale, const float* v_scale, const int32_t* block_table,
+                                 int max_blocks, const int32_t* seqlens, float softmax_scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, void* out, float* lse, int bs, int h_q,
+                                 int h_kv, int head_dim, int page_size, cudaStream_t stream) {
+  if (head_dim != gqa::kHd || page_size != gqa::kPage || bs < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 ||
+      h_q / h_kv > gqa::kN || num_blocks < 1 || max_blocks < 1 || num_splits < 0 || !(softmax_scale > 0.f))
+    return FP8MLA_ERR_INVALID_ARG;
+  if (bs == 0) return FP8MLA_OK;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seqlens == nullptr ||
+      out == nullptr || lse == nullptr)
+    return FP8MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) & 15u)
+    return FP8MLA_ERR_INVALID_ARG;
+  int splits = std::min(num_splits, 1 << 16);
+  if (splits == 0) {  // auto: the waves rule for this GPU, with the block table's capacity as the longest context
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+      return FP8MLA_ERR_CUDA;
+    splits = gqa_choose_splits(bs, h_kv, max_blocks * gqa::kPage, sms, 0);
+  }
+  if (splits > 1) {
+    const size_t need = gqa_workspace_bytes(bs, h_q, head_dim, splits);
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FP8MLA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return FP8MLA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  const long long rows = static_cast<long long>(num_blocks) * h_kv * gqa::kPage;
+  CUtensorMap tk, tv;
+  if (!gqa::encode_pages(&tk, k_cache, rows) || !gqa::encode_pages(&tv, v_cache, rows)) return FP8MLA_ERR_CUDA;
+  gqa::Params prm;
+  prm.q = static_cast<const uint16_t*>(q);
+  prm.block_table = block_table;
+  prm.seqlens = seqlens;
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
+  prm.out = static_cast<uint16_t*>(out);
+  prm.lse = lse;
+  const size_t slots = static_cast<size_t>(bs) * h_kv * splits;
+  prm.ws_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  prm.ws_ml = splits > 1 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                                     gqa::round_up(slots * gqa::kN * gqa::kHd * sizeof(float), 256))
+                         : nullptr;
+  prm.num_blocks = num_blocks;
+  prm.max_blocks = max_blocks;
+  prm.bs = bs;
+  prm.h_q = h_q;
+  prm.h_kv = h_kv;
+  prm.group = h_q / h_kv;
+  prm.splits = splits;
+  prm.softmax_scale = softmax_scale;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(gqa::gqa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(gqa::kSmemBytes)) != cudaSuccess)
+      return FP8MLA_ERR_CUDA;
+    configured = true;
+  }
+  const long long grid = static_cast<long long>(bs) * h_kv * splits;
+  if (grid > 0x7FFFFFFFll) return FP8MLA_ERR_INVALID_ARG;
+  gqa::gqa_decode_kernel<<<static_cast<unsigned>(grid), gqa::kThreads, gqa::kSmemBytes, stream>>>(tk, tv, prm);
+  if (cudaGetLastError() != cudaSuccess) return FP8MLA_ERR_CUDA;
+  if (splits > 1) {
+    dim3 cg(static_cast<unsigned>(bs * h_kv), (prm.group + 3) / 4);
+    gqa::gqa_combine_kernel<<<cg, 128, 0, stream>>>(prm.ws_o, prm.ws_ml, splits, prm.group, h_q, h_kv, prm.out, lse);
+    if (cudaGetLastError() != cudaSuccess) return FP8MLA_ERR_CUDA;
+  }
+  return FP8MLA_OK;
+}
+
+uint32_t gqa_read_and_clear_status() {
+  uint32_t v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_status_gqa, sizeof(v));
+  cudaMemcpyToSymbol(g_status_gqa, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fp8mla

@@ -1,0 +1,22 @@
+// Paged GQA decode with split-KV (gqa_decode.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "fp8mla.h"
+
+namespace fp8mla {
+
+size_t gqa_workspace_bytes(int bs, int h_q, int head_dim, int max_splits);
+int gqa_choose_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_splits);
+fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
+                                 const float* k_scale, const float* v_scale, const int32_t* block_table,
+                                 int max_blocks, const int32_t* seqlens, float softmax_scale, int num_splits,
+                                 void* workspace, size_t workspace_bytes, void* out, float* lse, int bs, int h_q,
+                                 int h_kv, int head_dim, int page_size, cudaStream_t stream);
+uint32_t gqa_read_and_clear_status();
+
+}  // namespace fp8mla

@@ -1,0 +1,674 @@
+// Dense MLA decode over an E4M3 paged KV cache, tcgen05 + TMA, sm_103a.
+//
+// The operation (FlashMLA "update fp8 support", Improvements; test shape
+// d = 576, dv = 512, h_kv = 1, s_q <= 2, causal) per sequence b:
+//   S = Q K^T (Q: R = s_q * h_q rows x 576; K: the sequence's cached rows),
+//   P = softmax(softmax_scale * S) under the causal mask, O = P V with V the
+//   first 512 dims of the same rows; lse = log sum exp.
+//
+// GB300 design (one work unit = 2 CTAs (FP8 dots) or 4 CTAs (16-bit dots),
+// each owning one slice of dv):
+//   * TMEM (512 columns x 128 lanes) holds everything the tensor core
+//     touches besides K/V: O (this CTA's dv slice), S (64 columns), P, and
+//     Q itself, so Q.K^T runs with A read from TMEM and shared memory holds
+//     only a ring of KV pages.  FP8 dots: O 256 + S 64 + P 16 (E4M3) + Q
+//     latent 128 (E4M3) + Q RoPE 32 (bf16) columns.  16-bit dots: O 128 +
+//     S 64 + P 32 (bf16) + Q 288 (bf16) columns.
+//   * TMA loads a whole 64-token page through the block table: four
+//     128-byte-swizzled boxes of the 512 latent bytes (usable as K-major B
+//     for Q.K^T and as MN-major B for P.V without any transpose) and one
+//     plain box of the 64 RoPE bytes.
+//   * FP8 dots: Q.K^T = 16 E4M3 MMAs (K = 32) over the latent part plus 4
+//     bf16 MMAs (K = 16) over the RoPE part into one f32 accumulator -- the
+//     RoPE chunk stays 16-bit (FlashMLA page, Improvements: the nine 64-wide
+//     K chunks let RoPE run in BF16).  Q's latent part is quantised in-kernel
+//     with a per-row power-of-two scale qs, so the RoPE part divides by qs
+//     exactly (aiter sparse_mla_fwd page, Technical details: in-kernel Q
+//     quantisation).  16-bit dots: converter warps turn each page into bf16
+//     (exact) and both products run as bf16 MMAs.
+//   * Online softmax in the log2 domain (InfiniCore page, Summary) with the
+//     per-tensor kv_scale and qs folded into one per-row constant; in FP8
+//     mode P is stored as E4M3(128 p) so long tails do not flush to zero and
+//     the epilogue divides the 128 back out with the V scale (aiter page,
+//     Technical details and Accuracy).  The running max is only raised when
+//     a tile's max exceeds it by more than 1 (log2 units), which keeps
+//     128 p <= 256 < 448 and makes O rescales rare.
+//   * Rows of the sequence's last page past its length are zeroed once per
+//     sequence before P.V reads them (FlashMLA page, TODO: fill_oob_KV per
+//     tile was the stated limiter); scores there are masked by a select.
+//   * A unit may cover a piece of a sequence; pieces publish (m, l, O) to a
+//     workspace and a combine kernel merges them (InfiniCore split-kv commit).
+//   * FP8 dots perturb the LSE by softmax_scale * (q_hat - q) . k_mean, where
+//     k_mean = sum_j p_j k_j; its latent part is exactly the output row, so
+//     the epilogue publishes -softmax_scale * (q_hat - q) . out per dv slice
+//     and the combine step subtracts that first-order term from the LSE.
+//
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// owner, warps 2-3 page conversion (RoPE or whole page to bf16) and tail
+// zeroing, warps 4-7 softmax, Q preparation and epilogue (thread r owns
+// query row r = TMEM lane r).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "mla_decode.h"
+
+namespace fp8mla {
+
+__device__ uint32_t g_status_mla;
+
+namespace mla {
+
+constexpr int kPage = 64;
+constexpr int kD = 576;
+constexpr int kDLat = 512;
+constexpr int kDV = 512;
+constexpr int kRows = 128;
+constexpr int kThreads = 256;
+constexpr int kLatBox = kPage * 128;                 // one 128-byte column slice of a page (8 KB)
+constexpr uint32_t kPageTxBytes = kPage * kD;        // bytes one page's TMA loads deliver
+
+template <bool kFp8>
+struct Cfg;
+
+template <>
+struct Cfg<true> {  // FP8 Q/P dots
+  static constexpr int kParts = 2, kDvPart = 256, kStages = 4;
+  static constexpr float kPScale = 128.0f, kTau = 1.0f;
+  static constexpr int kOffRope8 = 4 * kLatBox;      // 64 tokens x 64 E4M3 bytes, no swizzle
+  static constexpr int kOffCvt = kOffRope8 + kPage * 64;   // RoPE as bf16, 128 B swizzle
+  static constexpr int kStageBytes = kOffCvt + kLatBox;
+  static constexpr uint32_t kTO = 0, kTS = 256, kTP = 320, kTQ = 352, kTQR = 480;
+};
+
+template <>
+struct Cfg<false> {  // 16-bit dots
+  static constexpr int kParts = 4, kDvPart = 128, kStages = 2;
+  static constexpr float kPScale = 1.0f, kTau = 8.0f;
+  static constexpr int kOffRope8 = 4 * kLatBox;
+  static constexpr int kOffCvt = kOffRope8 + kPage * 64;  // 9 bf16 boxes: 8 latent + RoPE
+  static constexpr int kStageBytes = kOffCvt + 9 * kLatBox;
+  static constexpr uint32_t kTO = 0, kTS = 128, kTP = 192, kTQ = 224, kTQR = 224 + 256;
+};
+
+static_assert(Cfg<true>::kOffCvt % 1024 == 0 && Cfg<true>::kStageBytes % 1024 == 0, "1 KB aligned tiles");
+static_assert(Cfg<false>::kOffCvt % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0, "1 KB aligned tiles");
+
+template <bool kFp8>
+struct Barriers {
+  uint64_t kv_full[Cfg<kFp8>::kStages];
+  uint64_t kv_empty[Cfg<kFp8>::kStages];
+  uint64_t cvt_ready[Cfg<kFp8>::kStages];
+  uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+  uint32_t cvt_ok;
+};
+
+template <bool kFp8>
+constexpr size_t smem_bytes() {
+  return Cfg<kFp8>::kStages * Cfg<kFp8>::kStageBytes + sizeof(Barriers<kFp8>) + 1024;
+}
+
+// One (sequence, page range) piece of a unit's work.
+struct Segment {
+  int b, lo, hi, split, s_k, n;
+};
+
+// Walks the segments of one unit: sequences b_begin .. b_end of the tile
+// schedule, clipped to the unit's page range, skipping empty pieces.
+struct SegmentWalker {
+  int b, b0, p0, b1, p1, k0;
+  const MlaParams* prm;
+  __device__ SegmentWalker(const MlaParams& p, int unit) : prm(&p) {
+    const int32_t* row = p.tile_sched + unit * 8;
+    b0 = row[0];
+    p0 = row[1];
+    b1 = row[2];
+    p1 = row[3];
+    k0 = row[4];
+    b = b0;
+  }
+  __device__ bool next(Segment& s) {
+    while (b <= b1 && b < prm->b) {
+      const int bb = b++;
+      const int s_k = prm->seqlens[bb];
+      const int n = seq_pages(s_k, kPage, prm->max_pages, &g_status_mla);
+      const int lo = (bb == b0) ? p0 : 0;
+      int hi = (bb == b1) ? p1 : n;
+      hi = min(hi, n);
+      if (hi <= lo) continue;
+      s = Segment{bb, lo, hi, (bb == b0) ? k0 : 0, s_k, n};
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  const bool ok = wait_bounded(bar, parity, abort_flag, &g_status_mla);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Smallest e with amax <= 448 * 2^e (exact, from the float's exponent and mantissa).
+__device__ __forceinline__ int pow2_scale_exponent(float amax) {
+  const uint32_t bits = __float_as_uint(amax);
+  const int expo = static_cast<int>((bits >> 23) & 0xFFu);
+  if (expo == 0) return -126;  // zero or subnormal: any scale in range works
+  const uint32_t mant = bits & 0x7FFFFFu;
+  const int e = (expo - 127) - (mant <= 0x600000u ? 8 : 7);  // 448 = 1.75 * 2^8
+  return max(e, -126);
+}
+
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+// x -> E4M3(x * inv_qs) * qs - x: the in-kernel quantisation error of one Q element.
+__device__ __forceinline__ float2 q_quant_error(uint32_t bf16x2, float inv_qs, float qs) {
+  const float x0 = bf16_lo(bf16x2), x1 = bf16_hi(bf16x2);
+  const uint32_t h = e4m3x2_to_f16x2(pack_e4m3x2(x0 * inv_qs, x1 * inv_qs));
+  return make_float2(f16_lo(h) * qs - x0, f16_hi(h) * qs - x1);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                      const MlaParams prm) {
+  using C = Cfg<kFp8>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  Barriers<kFp8>* bars = reinterpret_cast<Barriers<kFp8>*>(smem + C::kStages * C::kStageBytes);
+  volatile uint32_t* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int unit = blockIdx.x / C::kParts;
+  const int part = blockIdx.x % C::kParts;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->cvt_ready[s], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, kRows);
+    mbar_init(&bars->p_full, kRows);
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->q_full, kRows);
+    mbar_init(&bars->final_mma, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_lat);
+      tma_prefetch_desc(&tm_rope);
+      SegmentWalker walk(prm, unit);
+      Segment sg;
+      int i = 0;
+      bool ok = true;
+      while (ok && walk.next(sg)) {
+        for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+          const int st = i % C::kStages;
+          const int use = i / C::kStages;
+          if (use > 0 && !wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla)) {
+            ok = false;
+            break;
+          }
+          int phys = prm.block_table[static_cast<size_t>(sg.b) * prm.max_pages + pg];
+          if (phys < 0 || phys >= prm.num_pages) {
+            atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
+            phys = 0;
+          }
+          uint8_t* sb = smem + st * C::kStageBytes;
+          mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * kLatBox, &tm_lat, &bars->kv_full[st], j * 128, 0, phys);
+          tma_load_3d(sb + C::kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
+        }
+      }
+      // Never leave with copies in flight: wait for the last loads issued.
+      for (int j = max(0, i - C::kStages); j < i; ++j)
+        wait_bounded(&bars->kv_full[j % C::kStages], (j / C::kStages) & 1, nullptr, &g_status_mla);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer ----
+    if (lane == 0) {
+      const uint32_t t_s = tmem + C::kTS, t_o = tmem + C::kTO;
+      SegmentWalker walk(prm, unit);
+      Segment sg;
+      int i = 0, seg_i = 0;
+      bool ok = true;
+
+      auto issue_qk = [&](uint32_t sb) {
+        if constexpr (kFp8) {
+          constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);   // e4m3 x e4m3, both K-major
+          constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);  // bf16 x bf16
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            const uint64_t bd = make_sdesc(sb + (kk >> 2) * kLatBox + (kk & 3) * 32, 16, 1024, SWIZZLE_128B);
+            mma_f8_ts(t_s, tmem + C::kTQ + kk * 8, bd, idesc8, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = make_sdesc(sb + C::kOffCvt + kk * 32, 16, 1024, SWIZZLE_128B);
+            mma_f16_ts(t_s, tmem + C::kTQR + kk * 8, bd, idesc16, 1u);
+          }
+        } else {
+          constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);
+#pragma unroll
+          for (int kk = 0; kk < 36; ++kk) {
+            const uint64_t bd =
+                make_sdesc(sb + C::kOffCvt + (kk >> 2) * kLatBox + (kk & 3) * 32, 16, 1024, SWIZZLE_128B);
+            mma_f16_ts(t_s, tmem + C::kTQ + kk * 8, bd, idesc16, kk > 0 ? 1u : 0u);
+          }
+        }
+      };
+
+      auto issue_pv = [&](int j, bool first_in_seg) -> bool {
+        if (!wait_bounded(&bars->p_full, j & 1, abort_flag, &g_status_mla)) return false;
+        tc_fence_after();
+        const int st = j % C::kStages;
+        const uint32_t sb = smem_u32(smem + st * C::kStageBytes);
+        if constexpr (kFp8) {
+          constexpr uint32_t idesc = make_idesc(0, 0, 0, 1, 256, 128);   // e4m3, B MN-major, N = 256
+          const uint32_t v_base = sb + part * 2 * kLatBox;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t bd = make_sdesc(v_base + kk * 4096, kLatBox, 1024, SWIZZLE_128B);
+            mma_f8_ts(t_o, tmem + C::kTP + kk * 8, bd, idesc, (first_in_seg && kk == 0) ? 0u : 1u);
+          }
+        } else {
+          constexpr uint32_t idesc = make_idesc(1, 1, 0, 1, 128, 128);   // bf16, B MN-major, N = 128
+          const uint32_t v_base = sb + C::kOffCvt + part * 2 * kLatBox;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = make_sdesc(v_base + kk * 2048, kLatBox, 1024, SWIZZLE_128B);
+            mma_f16_ts(t_o, tmem + C::kTP + kk * 8, bd, idesc, (first_in_seg && kk == 0) ? 0u : 1u);
+          }
+        }
+        tc_commit(&bars->pv_done);
+        tc_commit(&bars->kv_empty[st]);
+        return true;
+      };
+
+      while (ok && walk.next(sg)) {
+        if (!wait_bounded(&bars->q_full, seg_i & 1, abort_flag, &g_status_mla)) break;
+        const int first_i = i;
+        for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+          const int st = i % C::kStages;
+          const int use = i / C::kStages;
+          if (!wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla) ||
+              !wait_bounded(&bars->cvt_ready[st], use & 1, abort_flag, &g_status_mla) ||
+              (i > 0 && !wait_bounded(&bars->s_free, (i - 1) & 1, abort_flag, &g_status_mla))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_qk(smem_u32(smem + st * C::kStageBytes));
+          tc_commit(&bars->s_full);
+          if (i > first_i && !issue_pv(i - 1, i - 1 == first_i)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        if (!issue_pv(i - 1, i - 1 == first_i)) break;
+        ++seg_i;
+      }
+      tc_commit(&bars->final_mma);
+      wait_bounded(&bars->final_mma, 0, nullptr, &g_status_mla);
+    }
+    __syncwarp();
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------- page conversion, tail zeroing ----
+    const int t = threadIdx.x - 64;  // token row of the page
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int i = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+        const int st = i % C::kStages;
+        const int use = i / C::kStages;
+        if (t == 0) bars->cvt_ok = wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla) ? 1u : 0u;
+        named_bar_sync(1, 64);
+        if (!bars->cvt_ok) {
+          ok = false;
+          break;
+        }
+        uint8_t* sb = smem + st * C::kStageBytes;
+        const bool dead = (pg == sg.n - 1) && (t >= sg.s_k - pg * kPage);  // slot past the sequence end
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        const int sw = t & 7;
+        // RoPE bytes -> bf16 (box C::kOffCvt + (kFp8 ? 0 : 8 boxes))
+        {
+          const uint4* src = reinterpret_cast<const uint4*>(sb + C::kOffRope8 + t * 64);
+          uint8_t* dst = sb + C::kOffCvt + (kFp8 ? 0 : 8 * kLatBox) + t * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4 lo = z, hi = z;
+            if (!dead) {
+              const uint4 v = src[c];
+              e4m3x4_to_bf16x4(v.x, lo.x, lo.y);
+              e4m3x4_to_bf16x4(v.y, lo.z, lo.w);
+              e4m3x4_to_bf16x4(v.z, hi.x, hi.y);
+              e4m3x4_to_bf16x4(v.w, hi.z, hi.w);
+            }
+            *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
+            *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
+          }
+        }
+        if constexpr (kFp8) {
+          if (dead) {  // zero the slot's V row (all four 128-byte slices)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint4* row = reinterpret_cast<uint4*>(sb + j * kLatBox + t * 128);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) row[c] = z;
+            }
+          }
+        } else {
+          // latent: raw box j chunk c (16 E4M3) -> bf16 box 2j + c/4, chunks 2(c%4), 2(c%4)+1
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            const uint8_t* src = sb + j * kLatBox + t * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint4 lo = z, hi = z;
+              if (!dead) {
+                const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+                e4m3x4_to_bf16x4(v.x, lo.x, lo.y);
+                e4m3x4_to_bf16x4(v.y, lo.z, lo.w);
+                e4m3x4_to_bf16x4(v.z, hi.x, hi.y);
+                e4m3x4_to_bf16x4(v.w, hi.z, hi.w);
+              }
+              uint8_t* dst = sb + C::kOffCvt + (2 * j + c / 4) * kLatBox + t * 128;
+              *reinterpret_cast<uint4*>(dst + (((2 * (c % 4)) ^ sw) << 4)) = lo;
+              *reinterpret_cast<uint4*>(dst + (((2 * (c % 4) + 1) ^ sw) << 4)) = hi;
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 64);
+        if (t == 0) mbar_arrive(&bars->cvt_ready[st]);
+      }
+    }
+  } else {
+    // -------------------------------- softmax / Q prep / epilogue ----
+    const int r = threadIdx.x - 128;                       // query row = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
+    const float kv_scale = *prm.kv_scale;
+    const int R = prm.s_q * prm.h_q;
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int i = 0;
+    while (walk.next(sg)) {
+      const uint16_t* qrow = prm.q + (static_cast<size_t>(sg.b) * R + r) * kD;
+      float c_row, qs = 1.f, inv_qs = 1.f;
+      if constexpr (kFp8) {
+        // ---- Q preparation: latent -> E4M3(q / qs), RoPE -> bf16(q / qs) ----
+        float amax = 0.f;
+        if (r < R) {
+          const uint4* q4 = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll 8
+          for (int c = 0; c < kD / 8; ++c) {
+            const uint4 v = __ldg(q4 + c);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                                     fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
+                                     fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+          }
+        }
+        const int qe = pow2_scale_exponent(amax);
+        qs = exp2i(qe);
+        inv_qs = exp2i(-qe);
+        c_row = prm.softmax_scale * kLog2e * qs * kv_scale;
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {  // 8 chunks of 64 latent values -> 16 columns each
+          uint32_t pk[16];
+          const uint4* q4 = reinterpret_cast<const uint4*>(qrow + ch * 64);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < R) v = __ldg(q4 + c);
+            pk[2 * c] = pack_e4m3x4(bf16_lo(v.x) * inv_qs, bf16_hi(v.x) * inv_qs, bf16_lo(v.y) * inv_qs,
+                                    bf16_hi(v.y) * inv_qs);
+            pk[2 * c + 1] = pack_e4m3x4(bf16_lo(v.z) * inv_qs, bf16_hi(v.z) * inv_qs, bf16_lo(v.w) * inv_qs,
+                                        bf16_hi(v.w) * inv_qs);
+          }
+          tmem_st16(lane_base + C::kTQ + ch * 16, pk);
+        }
+        uint32_t pk[32];
+        const uint4* q4 = reinterpret_cast<const uint4*>(qrow + kDLat);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (r < R) v = __ldg(q4 + c);
+          pk[4 * c + 0] = pack_bf16x2(bf16_lo(v.x) * inv_qs, bf16_hi(v.x) * inv_qs);
+          pk[4 * c + 1] = pack_bf16x2(bf16_lo(v.y) * inv_qs, bf16_hi(v.y) * inv_qs);
+          pk[4 * c + 2] = pack_bf16x2(bf16_lo(v.z) * inv_qs, bf16_hi(v.z) * inv_qs);
+          pk[4 * c + 3] = pack_bf16x2(bf16_lo(v.w) * inv_qs, bf16_hi(v.w) * inv_qs);
+        }
+        tmem_st32(lane_base + C::kTQR, pk);
+      } else {
+        // ---- Q preparation: bf16 as is, 576 values -> 288 columns ----
+        c_row = prm.softmax_scale * kLog2e * kv_scale;
+#pragma unroll 1
+        for (int ch = 0; ch < 9; ++ch) {
+          uint32_t pk[32];
+          const uint4* q4 = reinterpret_cast<const uint4*>(qrow + ch * 64);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < R) v = __ldg(q4 + c);
+            pk[4 * c + 0] = v.x;
+            pk[4 * c + 1] = v.y;
+            pk[4 * c + 2] = v.z;
+            pk[4 * c + 3] = v.w;
+          }
+          tmem_st32(lane_base + C::kTQ + ch * 32, pk);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->q_full);
+
+      // keys visible to this row (bottom-right causal alignment)
+      const int qtok = (r < R) ? r / prm.h_q : 0;
+      const int visible = prm.causal ? (sg.s_k - prm.s_q + qtok + 1) : sg.s_k;
+      float m_run = kNegInf, l_run = 0.f;
+      bool ok = true;
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+        if (!warp_wait(&bars->s_full, i & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[64];
+        tmem_ld32(lane_base + C::kTS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(lane_base + C::kTS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->s_free);
+
+        const int base = pg * kPage;
+        float mx = kNegInf;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float v = (base + c < visible) ? __uint_as_float(s[c]) * c_row : kNegInf;
+          s[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_run + C::kTau) {
+          alpha = ex2_approx(m_run - mx);
+          rescale = (pg != sg.lo);
+          m_run = mx;
+        }
+        const float msub = (m_run == kNegInf) ? 0.f : m_run;
+        float sum = 0.f;
+        uint32_t pk[kFp8 ? 16 : 32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float p0 = ex2_approx(__uint_as_float(s[c]) - msub);
+          const float p1 = ex2_approx(__uint_as_float(s[c + 1]) - msub);
+          const float p2 = ex2_approx(__uint_as_float(s[c + 2]) - msub);
+          const float p3 = ex2_approx(__uint_as_float(s[c + 3]) - msub);
+          sum += (p0 + p1) + (p2 + p3);
+          if constexpr (kFp8) {
+            pk[c / 4] = pack_e4m3x4(p0 * C::kPScale, p1 * C::kPScale, p2 * C::kPScale, p3 * C::kPScale);
+          } else {
+            pk[c / 2] = pack_bf16x2(p0, p1);
+            pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+          }
+        }
+        l_run = l_run * alpha + sum;
+
+        if (i > 0 && !warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+          for (int ch = 0; ch < C::kDvPart / 32; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + C::kTO + ch * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+            tmem_st32(lane_base + C::kTO + ch * 32, o);
+          }
+        }
+        if constexpr (kFp8)
+          tmem_st16(lane_base + C::kTP, pk);
+        else
+          tmem_st32(lane_base + C::kTP, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);
+      }
+      if (!ok) break;
+
+      // ---- epilogue: O is final once the segment's last P.V completes ----
+      if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      const bool whole = (sg.lo == 0 && sg.hi == sg.n);
+      const float o_scale = kv_scale / C::kPScale;  // tensor-core units -> true units
+      const float f = whole ? ((l_run > 0.f) ? o_scale / l_run : 0.f) : o_scale;
+      const int col0 = part * C::kDvPart;
+      const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
+      float dq_dot = 0.f;  // sum over this slice of (q_hat - q) * O (FP8 dots only)
+#pragma unroll 1
+      for (int ch = 0; ch < C::kDvPart / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + C::kTO + ch * 32, o);
+        tmem_ld_wait();
+        if (r >= R) continue;
+        if constexpr (kFp8) {
+          const uint4* q4 = reinterpret_cast<const uint4*>(qrow + col0 + ch * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = __ldg(q4 + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 e = q_quant_error(w[k], inv_qs, qs);
+              dq_dot += e.x * __uint_as_float(o[8 * c + 2 * k]) + e.y * __uint_as_float(o[8 * c + 2 * k + 1]);
+            }
+          }
+        }
+        if (whole) {
+          uint4* dst = reinterpret_cast<uint4*>(prm.out + (static_cast<size_t>(sg.b) * R + r) * kDV + col0 + ch * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
+            dst[c] = w;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(prm.ws_o + (static_cast<size_t>(slot) * kRows + r) * kDV + col0 +
+                                                  ch * 32);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            dst[c] = make_float4(__uint_as_float(o[4 * c]) * f, __uint_as_float(o[4 * c + 1]) * f,
+                                 __uint_as_float(o[4 * c + 2]) * f, __uint_as_float(o[4 * c + 3]) * f);
+        }
+      }
+      if (r < R) {
+        const size_t row = static_cast<size_t>(sg.b) * R + r;
+        if (whole) {
+          if (part == 0) prm.lse[row] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * kLn2 : kNegInf;
+          if constexpr (kFp8) prm.ws_corr[row * 2 + part] = -prm.softmax_scale * dq_dot * f;
+        } else {
+          const size_t srow = static_cast<size_t>(slot) * kRows + r;
+          if (part == 0) prm.ws_ml[srow] = make_float2((l_run > 0.f) ? m_run : kNegInf, l_run);
+          if constexpr (kFp8) prm.ws_d[srow * 2 + part] = dq_dot * f;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool kFp8>
+cudaError_t launch(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
+                   cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<kFp8>()));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  mla_decode_kernel<kFp8><<<num_units * Cfg<kFp8>::kParts, kThreads, smem_bytes<kFp8>(), stream>>>(tm_lat, tm_rope,
+                                                                                                   prm);
+  return cudaGetLastError();
+}
+
+}  // namespace mla
+
+cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
+                                  int num_units, cudaStream_t stream) {
+  return mla::launch<true>(tm_lat, tm_rope, prm, num_units, stream);
+}
+
+cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
+                                    int num_units, cudaStream_t stream) {
+  return mla::launch<false>(tm_lat, tm_rope, prm, num_units, stream);
+}
+
+uint32_t mla_read_and_clear_status() {
+  uint32_t v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_status_mla, sizeof(v));
+  cudaMemcpyToSymbol(g_status_mla, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace fp8mla

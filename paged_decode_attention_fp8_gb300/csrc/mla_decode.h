@@ -1,0 +1,58 @@
+// Host-side declarations shared by the C ABI and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fp8mla {
+
+struct MlaParams {
+  const uint16_t* q;           // bf16 [b, s_q, h_q, 576]
+  const int32_t* block_table;  // [b, max_pages]
+  const int32_t* seqlens;      // [b]
+  const float* kv_scale;       // [1]
+  const int32_t* tile_sched;   // [num_units, 8]
+  const int32_t* num_splits;   // [b + 1]
+  float* ws_o;                 // [slots, 128, 512] partial accumulators (true units)
+  float2* ws_ml;               // [slots, 128] (m in log2 units, l)
+  float* ws_d;                 // [slots, 128, parts<=2] sum of (q_hat - q) * O_partial per dv slice (FP8 dots)
+  float* ws_corr;              // [b, 128, 2] -softmax_scale * (q_hat - q) . out per dv slice (FP8 dots)
+  uint16_t* out;               // bf16 [b, s_q, h_q, 512]
+  float* lse;                  // [b, s_q, h_q]
+  float softmax_scale;
+  int causal;
+  int max_pages;
+  int num_pages;
+  int b, s_q, h_q;
+};
+
+constexpr int kMlaRows = 128;
+constexpr int kMlaDV = 512;
+constexpr int kMlaPage = 64;
+constexpr int kMlaD = 576;
+constexpr int kSchedFixedCost = 4;
+
+// dense MLA decode kernels (mla_decode.cu)
+cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
+                                  int num_units, cudaStream_t stream);
+cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
+                                    int num_units, cudaStream_t stream);
+uint32_t mla_read_and_clear_status();
+
+// metadata + combine (metadata.cu)
+cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, int force_splits, int32_t* tile_sched,
+                                int32_t* num_splits, cudaStream_t stream);
+// Merges split partials into out / lse, and (FP8 dots, apply_corr) applies the
+// first-order Q-quantisation correction to every row's LSE.
+cudaError_t launch_mla_combine(const int32_t* num_splits, const float* ws_o, const float2* ws_ml, const float* ws_d,
+                               const float* ws_corr, int apply_corr, float softmax_scale, uint16_t* out, float* lse,
+                               int b, int rows, cudaStream_t stream);
+// The same merge for any variant whose partial slots hold slot_rows rows of dv = 512.
+cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const float* ws_o, const float2* ws_ml,
+                                 const float* ws_d, const float* ws_corr, int apply_corr, float softmax_scale,
+                                 uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream);
+uint32_t metadata_read_and_clear_status();
+
+}  // namespace fp8mla

@@ -1,0 +1,61 @@
+"""Comparison metrics shared by the GPU parity tests.
+
+Tolerances (from the target stated for this path): relative L2 <= 1e-2 with
+16-bit dots, <= 5e-2 with FP8 Q/P dots and cosine >= 0.999; |delta lse| <=
+2e-3 over rows with a finite reference LSE; rows whose reference LSE is
+-inf must come back exactly 0 with LSE -inf.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+
+TOL = {
+    "fp8": dict(rel_l2=5e-2, cos=0.999, lse=2e-3),
+    "bf16": dict(rel_l2=1e-2, cos=0.9999, lse=2e-3),
+}
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, mode, mask=None):
+    """Returns a dict of metrics; ``mask`` selects rows (leading dims) to compare."""
+    o = to_np(out_gpu)
+    l = to_np(lse_gpu)
+    if mask is not None:
+        o, l, out_ref, lse_ref = o[mask], l[mask], out_ref[mask], lse_ref[mask]
+    empty = np.isneginf(lse_ref)
+    res = {}
+    res["empty_rows_ok"] = bool(np.all(np.isneginf(l[empty])) and np.all(o[empty] == 0))
+    live = ~empty
+    ol, rl = o[live], out_ref[live]
+    num = np.linalg.norm((ol - rl).ravel())
+    den = np.linalg.norm(rl.ravel())
+    res["rel_l2"] = float(num / den) if den > 0 else float(num)
+    nrm = np.linalg.norm(ol.ravel()) * den
+    res["cos"] = float(np.dot(ol.ravel(), rl.ravel()) / nrm) if nrm > 0 else 1.0
+    res["lse_max_abs"] = float(np.max(np.abs(l[live] - lse_ref[live]))) if live.any() else 0.0
+    res["finite"] = bool(np.all(np.isfinite(o)) and np.all(np.isfinite(l[live])))
+    return res
+
+
+def assert_close(metrics, mode):
+    tol = TOL[mode]
+    assert metrics["finite"], metrics
+    assert metrics["empty_rows_ok"], metrics
+    assert metrics["rel_l2"] <= tol["rel_l2"], metrics
+    assert metrics["cos"] >= tol["cos"], metrics
+    assert metrics["lse_max_abs"] <= tol["lse"], metrics
+
+
+def record(name, metrics):
+    """Appends a parity result to gpurun_out/parity_metrics.jsonl when that folder exists."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = os.path.join(root, "gpurun_out")
+    if os.path.isdir(out):
+        with open(os.path.join(out, "parity_metrics.jsonl"), "a") as f:
+            f.write(json.dumps(dict(name=name, **metrics)) + "\n")

@@ -1,0 +1,117 @@
+"""The C-ABI library loads without a GPU, exports every function declared in
+include/*.h, and refuses bad arguments on the host before launching anything
+(no compute call is made here)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import paged_decode_attention_fp8_gb300 as fm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"FP8MLA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = fm.lib()
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert names == set(fm.EXPORTED_SYMBOLS)
+
+
+def test_exported_symbols_are_only_the_c_abi():
+    out = os.popen(f"nm -D --defined-only {fm.LIB_PATH}").read()
+    text_syms = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert text_syms == declared_functions()
+
+
+def test_status_strings_and_units():
+    lib = fm.lib()
+    assert lib.fp8mla_status_string(0) == b"ok"
+    assert b"E4M3" in lib.fp8mla_status_string(2)
+    assert lib.fp8mla_metadata_units(148) == 74
+    assert lib.fp8mla_metadata_units(152) == 76
+    assert lib.fp8mla_metadata_units(1) == 1
+
+
+def test_workspace_sizes_grow_with_batch():
+    lib = fm.lib()
+    a = lib.fp8mla_workspace_bytes(64, 2, 64, 76)
+    b = lib.fp8mla_workspace_bytes(128, 2, 64, 76)
+    assert b > a > 140 * 128 * 512 * 4
+    assert a % 256 == 0
+
+
+def _decode(**over):
+    args = dict(q=1 << 20, kv=1 << 20, kv_dtype=fm.KV_E4M3, num_pages=16, bt=1 << 20, max_pages=8, sl=1 << 20,
+                scale=1 << 20, softmax_scale=0.04, causal=1, ts=1 << 20, ns=1 << 20, units=76, ws=1 << 20,
+                ws_bytes=1 << 40, out=1 << 20, lse=1 << 20, dot=fm.DOT_FP8, b=2, s_q=2, h_q=64)
+    args.update(over)
+    a = args
+    return fm.lib().fp8mla_decode(a["q"], a["kv"], a["kv_dtype"], a["num_pages"], a["bt"], a["max_pages"], a["sl"],
+                                  a["scale"], a["softmax_scale"], a["causal"], a["ts"], a["ns"], a["units"], a["ws"],
+                                  a["ws_bytes"], a["out"], a["lse"], a["dot"], a["b"], a["s_q"], a["h_q"], None)
+
+
+@pytest.mark.parametrize("code", [fm.KV_E4M3FNUZ, fm.KV_E5M2, fm.KV_OTHER])
+def test_foreign_encodings_refused(code):
+    assert _decode(kv_dtype=code) == 2
+
+
+def test_missing_scale_refused():
+    # an FP8 cache without its scale fails loudly (InfiniCore page: "Bad Parameter")
+    assert _decode(scale=None) == 1
+
+
+@pytest.mark.parametrize("over", [dict(h_q=128), dict(s_q=0), dict(q=None), dict(out=None), dict(units=0),
+                                  dict(dot=7), dict(softmax_scale=0.0), dict(q=(1 << 20) + 2),
+                                  dict(num_pages=0)])
+def test_bad_arguments_refused(over):
+    assert _decode(**over) == 1
+
+
+def test_small_workspace_refused():
+    assert _decode(ws_bytes=1024) == 3
+
+
+def test_metadata_argument_checks():
+    lib = fm.lib()
+    # force_splits * b > units
+    assert lib.fp8mla_get_metadata(1 << 20, 64, 64, 2, 76, 2, 1 << 20, 1 << 20, None) == 1
+    assert lib.fp8mla_get_metadata(1 << 20, 4, 128, 2, 76, 0, 1 << 20, 1 << 20, None) == 1
+    assert lib.fp8mla_get_metadata(None, 4, 64, 2, 76, 0, 1 << 20, 1 << 20, None) == 1
+
+
+def test_sparse_and_gqa_refuse_foreign_encodings_and_missing_scales():
+    lib = fm.lib()
+    assert lib.sparse_mla_decode(1 << 20, 1 << 20, fm.KV_E5M2, 1024, 1 << 20, 2048, 1 << 20, 0.04, 0, 1 << 20,
+                                 1 << 40, 1 << 20, 1 << 20, fm.DOT_FP8, 2, 16, None) == 2
+    assert lib.sparse_mla_decode(1 << 20, 1 << 20, fm.KV_E4M3, 1024, 1 << 20, 2048, None, 0.04, 0, 1 << 20,
+                                 1 << 40, 1 << 20, 1 << 20, fm.DOT_FP8, 2, 16, None) == 1
+    assert lib.paged_gqa_decode(1 << 20, 1 << 20, 1 << 20, fm.KV_E4M3FNUZ, 64, 1 << 20, 1 << 20, 1 << 20, 8,
+                                1 << 20, 0.08, 0, 1 << 20, 1 << 40, 1 << 20, 1 << 20, 1, 32, 8, 128, 16, None) == 2
+    assert lib.paged_gqa_decode(1 << 20, 1 << 20, 1 << 20, fm.KV_E4M3, 64, None, 1 << 20, 1 << 20, 8,
+                                1 << 20, 0.08, 0, 1 << 20, 1 << 40, 1 << 20, 1 << 20, 1, 32, 8, 128, 16, None) == 1
+
+
+def test_python_dtype_mapping():
+    import torch
+    assert fm.kv_dtype_code(torch.empty(1, dtype=torch.float8_e4m3fn)) == fm.KV_E4M3
+    assert fm.kv_dtype_code(torch.empty(1, dtype=torch.uint8)) == fm.KV_E4M3
+    assert fm.kv_dtype_code(torch.empty(1, dtype=torch.float8_e5m2)) == fm.KV_E5M2
+    assert fm.kv_dtype_code(torch.empty(1, dtype=torch.int8)) == fm.KV_OTHER
+    assert fm.kv_dtype_code(torch.empty(1, dtype=torch.bool)) == fm.KV_OTHER
