@@ -39,79 +39,81 @@ __device__ __forceinline__ void put_row(int32_t* row, int a, int b, int c, int d
   row[7] = 0;
 }
 
-// One thread: the rule is sequential and touches b + num_units items.
+// One warp stages the page counts in shared memory; lane 0 then runs the
+// sequential rule (it touches b + num_units items) at shared-memory latency.
 __global__ void mla_metadata_kernel(const int32_t* __restrict__ seqlens, int B, int U, int force,
                                     int32_t* __restrict__ sched, int32_t* __restrict__ num_splits) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  int32_t* count = num_splits + 1;  // count[i] = splits of sequence i, prefix-summed at the end
-  for (int i = 0; i < B; ++i) count[i] = 0;
-  num_splits[0] = 0;
-
-  if (force > 0) {
-    int u = 0;
-    for (int bi = 0; bi < B; ++bi) {
-      const int n = pages_of(seqlens[bi]);
-      const int c = min(force, n);
-      for (int j = 0; j < c; ++j, ++u) {
-        if (u >= U) continue;  // the host refuses b * force > num_units
-        const int p0 = static_cast<int>((static_cast<long long>(j) * n) / c);
-        const int p1 = static_cast<int>((static_cast<long long>(j + 1) * n) / c);
-        if (p1 == n)
-          put_row(sched + 8 * u, bi, p0, bi + 1, 0, j);
-        else
-          put_row(sched + 8 * u, bi, p0, bi, p1, j);
-        count[bi] += 1;
-      }
-    }
-    for (; u < U; ++u) put_row(sched + 8 * u, B, 0, B, 0, 0);
-  } else {
-    long long total = 0;
-    for (int bi = 0; bi < B; ++bi) {
-      const int n = pages_of(seqlens[bi]);
-      if (n > 0) total += n + kSchedFixedCost;
-    }
-    const long long budget = total > 0 ? (total + U - 1) / U + kSchedFixedCost : 0;
-    int bi = 0, p = 0;
-    for (int u = 0; u < U; ++u) {
-      while (bi < B && pages_of(seqlens[bi]) == 0) ++bi;
-      const int sb = bi, sp = p;
-      const int first = bi < B ? count[bi] : 0;
-      long long left = budget;
-      while (bi < B) {
-        const int n = pages_of(seqlens[bi]);
-        if (n == 0) {
-          ++bi;
-          continue;
-        }
-        const int rest = n - p;
-        if (u == U - 1 || rest + kSchedFixedCost <= left) {
-          left -= rest + kSchedFixedCost;
-          count[bi] += 1;
-          ++bi;
-          p = 0;
-          continue;
-        }
-        const long long take = left - kSchedFixedCost;
-        if (take >= 1) {
-          p += static_cast<int>(take);
-          count[bi] += 1;
-        }
-        break;
-      }
-      put_row(sched + 8 * u, sb, sp, bi, p, first);
-    }
+  extern __shared__ int32_t meta_smem[];
+  int32_t* n = meta_smem;        // pages per sequence
+  int32_t* count = n + B;        // splits per sequence
+  if (blockIdx.x != 0) return;
+  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+    n[i] = pages_of(seqlens[i]);
+    count[i] = 0;
   }
-  int run = 0;
-  for (int i = 0; i < B; ++i) {
-    run += count[i];
-    count[i] = run;
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    if (force > 0) {
+      int u = 0;
+      for (int bi = 0; bi < B; ++bi) {
+        const int nb = n[bi];
+        const int c = min(force, nb);
+        for (int j = 0; j < c; ++j, ++u) {
+          if (u >= U) continue;  // the host refuses b * force > num_units
+          const int p0 = static_cast<int>((static_cast<long long>(j) * nb) / c);
+          const int p1 = static_cast<int>((static_cast<long long>(j + 1) * nb) / c);
+          if (p1 == nb)
+            put_row(sched + 8 * u, bi, p0, bi + 1, 0, j);
+          else
+            put_row(sched + 8 * u, bi, p0, bi, p1, j);
+          count[bi] += 1;
+        }
+      }
+      for (; u < U; ++u) put_row(sched + 8 * u, B, 0, B, 0, 0);
+    } else {
+      long long total = 0;
+      for (int bi = 0; bi < B; ++bi)
+        if (n[bi] > 0) total += n[bi] + kSchedFixedCost;
+      const long long budget = total > 0 ? (total + U - 1) / U + kSchedFixedCost : 0;
+      int bi = 0, p = 0;
+      for (int u = 0; u < U; ++u) {
+        while (bi < B && n[bi] == 0) ++bi;
+        const int sb = bi, sp = p;
+        const int first = bi < B ? count[bi] : 0;
+        long long left = budget;
+        while (bi < B) {
+          const int nb = n[bi];
+          if (nb == 0) {
+            ++bi;
+            continue;
+          }
+          const int rest = nb - p;
+          if (u == U - 1 || rest + kSchedFixedCost <= left) {
+            left -= rest + kSchedFixedCost;
+            count[bi] += 1;
+            ++bi;
+            p = 0;
+            continue;
+          }
+          const long long take = left - kSchedFixedCost;
+          if (take >= 1) {
+            p += static_cast<int>(take);
+            count[bi] += 1;
+          }
+          break;
+        }
+        put_row(sched + 8 * u, sb, sp, bi, p, first);
+      }
+    }
+    int run = 0;
+    num_splits[0] = 0;
+    for (int i = 0; i < B; ++i) {
+      run += count[i];
+      num_splits[i + 1] = run;
+    }
   }
 }
 
-// Grid (sequence, 16-row block), 4 warps.  A sequence with exactly one split
-// was finished by the decode kernel: only its LSE correction (FP8 dots) is
-// left, one thread per row.  Otherwise one warp per row merges the splits;
-// lane l owns dv columns [16 l, 16 l + 16).
 // Partial slots are [slot][slot_rows] rows of dv = 512; with uniform_splits > 0
 // sequence bi owns slots [bi * uniform_splits, (bi + 1) * uniform_splits).
 __global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int uniform_splits,
@@ -185,7 +187,16 @@ __global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int
 
 cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, int force_splits, int32_t* tile_sched,
                                 int32_t* num_splits, cudaStream_t stream) {
-  mla_metadata_kernel<<<1, 32, 0, stream>>>(seqlens, b, num_units, force_splits, tile_sched, num_splits);
+  const size_t smem = static_cast<size_t>(b) * 2 * sizeof(int32_t);
+  if (smem > kMetadataMaxSmem) return cudaErrorInvalidValue;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kMetadataMaxSmem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  mla_metadata_kernel<<<1, 32, smem, stream>>>(seqlens, b, num_units, force_splits, tile_sched, num_splits);
   return cudaGetLastError();
 }
 
