@@ -206,6 +206,36 @@ FP8MLA_API size_t paged_gqa_workspace_bytes(int bs, int h_q, int head_dim, int m
  * (num_splits as passed: 0 = auto).  Host-only, no device access. */
 FP8MLA_API int paged_gqa_num_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_splits);
 
+/* ------------------------------------------------------ no allocation ---
+ * fp8mla_decode_no_alloc -- the dense MLA decode for callers that cannot
+ * allocate device memory: code running where cudaMalloc is not allowed or
+ * not available (inside a host runtime that only hands out fixed input and
+ * output buffers, a plugin without access to an allocator, a process with
+ * a hard memory budget fixed at start-up).  The pages have no counterpart:
+ * this is a deployment convenience of this library.
+ *
+ * Same arguments and results as fp8mla_decode without the schedule and the
+ * workspace: the call schedules one work unit per sequence (no split-KV) and
+ * keeps its schedule, split counts and LSE-correction terms in a fixed
+ * device array compiled into this library (73 KB, held by every GPU that
+ * loads the library until the process exits).  It calls no allocator.
+ *   b <= FP8MLA_NO_ALLOC_MAX_BATCH; a larger batch returns
+ *   FP8MLA_ERR_WORKSPACE_TOO_SMALL and launches nothing.
+ *   All calls on a device share the array and it keeps the last call's
+ *   contents (every call rewrites what it reads, so nothing needs clearing);
+ *   calls that overlap on the GPU (other streams, other host threads) race on
+ *   it, so the caller must serialise them.
+ *   The first call on each device looks up the array's device address with
+ *   that device current (cudaGetSymbolAddress); make that first call before
+ *   capturing a stream into a graph. */
+#define FP8MLA_NO_ALLOC_MAX_BATCH 64
+FP8MLA_API fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype,
+                                                  int num_pages, const int32_t* block_table, int max_pages,
+                                                  const int32_t* cache_seqlens, const float* kv_scale,
+                                                  float softmax_scale, int causal, void* out, float* lse,
+                                                  fp8mla_dot_mode_t dot_mode, int b, int s_q, int h_q,
+                                                  fp8mla_stream_t stream);
+
 /* ------------------------------------------------------------- status ---- */
 
 /* Synchronises `stream`, returns in *code_out the OR of the FP8MLA_DEV_* bits

@@ -59,6 +59,7 @@ _SIGNATURES = {
                               _P]),
     "paged_gqa_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "paged_gqa_num_splits": (_I, [_I, _I, _I, _I, _I]),
+    "fp8mla_decode_no_alloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _F, _I, _P, _P, _I, _I, _I, _I, _P]),
     "fp8mla_get_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "fp8mla_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -193,6 +194,41 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
                                units, _ptr(workspace), workspace.numel() * workspace.element_size(),
                                _ptr(out), _ptr(lse), _dot(dot_mode), b, s_q, h_q, _stream(q.device)),
            "fp8mla_decode")
+    return out, lse
+
+
+NO_ALLOC_MAX_BATCH = 64
+
+
+def decode_no_alloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                    cache_seqlens: torch.Tensor, kv_scale: torch.Tensor, softmax_scale: float | None = None,
+                    causal: bool = True, dot_mode="fp8", out: torch.Tensor | None = None,
+                    lse: torch.Tensor | None = None):
+    """Dense MLA decode that needs no schedule or workspace from the caller.
+
+    For callers that cannot allocate device memory: the library keeps the
+    scratch in a fixed array of its own (one work unit per sequence, no
+    split-KV), so only inputs and outputs are passed; b <= 64.  Calls that
+    overlap on the GPU share that array and race.  Returns (out, lse) like
+    ``decode`` (out / lse are allocated here only when not given).
+    """
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv_cache, "kv_cache", None, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, 1)
+    _need(kv_scale, "kv_scale", torch.float32)
+    b, s_q, h_q, d = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(MLA_D)
+    if out is None:
+        out = torch.empty((b, s_q, h_q, MLA_DV), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=q.device)
+    _check(lib().fp8mla_decode_no_alloc(_ptr(q), _ptr(kv_cache), kv_dtype_code(kv_cache), kv_cache.shape[0],
+                                        _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens),
+                                        _ptr(kv_scale), float(softmax_scale), 1 if causal else 0, _ptr(out),
+                                        _ptr(lse), _dot(dot_mode), b, s_q, h_q, _stream(q.device)),
+           "fp8mla_decode_no_alloc")
     return out, lse
 
 
