@@ -259,7 +259,7 @@ def run_ours(args):
                     roofline_frac_of_time=round(max(t_hbm, t_tensor) / (dec_avg_ms * 1e-3), 4),
                     peak_source=f"{peaks['src']} (MEASURED_PEAKS.json hbm_gbs; fp8 = 2 x bf16_tflops)")
 
-    e2e = measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, world)
+    e2e = None if args.no_e2e else measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, world)
 
     res = {
         "metric": METRIC,
@@ -345,6 +345,105 @@ def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, worl
     return dict(value=round(world * flops / (ms * 1e-3) / 1e12, 2), unit="TFLOPS", ms_per_step=round(ms, 5),
                 h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h), steps=steps,
                 note="KV cache resident in HBM; per-step Q/block table/seqlens in, out/lse back")
+
+
+# ------------------------------------------- sparse / GQA measurement legs ----
+
+
+def run_secondary(args):
+    """µs/call and roofline of the sparse top-k MLA or the paged GQA variant (one GPU).
+
+    Sparse: 16 heads, d = dv = 512, 131072-token E4M3 cache, top-k 2048, s_q query
+    tokens, FP8 dots, auto split; three cache copies rotate (3 x 64 MiB > L2).
+    GQA: 32/8 heads, hd 128, page 16, bs 32 with contexts uniform in [1024, 16384],
+    16-bit dots, auto split; two copies of the ~570 MB caches rotate.
+    """
+    import torch
+
+    import paged_decode_attention_fp8_gb300 as fm
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks = measured_peaks()
+    if args.workload == "sparse":
+        inp = syn.sparse_inputs(4, args.sq)
+        sets = [(inp.q.to(dev), inp.kv_cache.to(dev)) for _ in range(3)]
+        idx = inp.topk_idx.to(dev)
+        scale = torch.tensor([inp.kv_scale], dtype=torch.float32, device=dev)
+        s_q, h_q, topk = inp.q.shape[0], inp.q.shape[1], idx.shape[1]
+        ws = torch.empty((max(fm.sparse_workspace_bytes(s_q, h_q, topk, 0), 256),), dtype=torch.uint8, device=dev)
+        out = torch.empty((s_q, h_q, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=dev)
+
+        def call(i):
+            q, kv = sets[i % len(sets)]
+            fm.sparse_mla_decode(q, kv, idx, scale, inp.softmax_scale, out=out, lse=lse, workspace=ws)
+
+        nbytes = s_q * topk * 512 + 2 * s_q * h_q * 512 * 2 + s_q * h_q * 4 + s_q * topk * 4
+        flops = 2.0 * s_q * h_q * topk * 1024
+        t_tensor = flops / (2.0 * peaks["bf16"] * 1e12)
+        cfg = dict(workload="sparse_topk_mla_decode", s_q=s_q, h_q=h_q, d=512, topk=topk, num_tokens=131072,
+                   dot="fp8", splits="auto", l2="3 rotating cache copies (192 MiB) > L2")
+        metric = f"sparse top-k MLA decode us/call (s_q={s_q}, 16 heads, top-k 2048)"
+        launches = 2
+    else:
+        seqlens = syn.uniform_seqlens(5, 32, 1024, 16384)
+        inp = syn.gqa_inputs(5, 32, seqlens)
+        sets = [(inp.k_cache.to(dev), inp.v_cache.to(dev)) for _ in range(2)]
+        q, bt, sl = inp.q.to(dev), inp.block_table.to(dev), inp.seqlens.to(dev)
+        ks = torch.tensor([inp.k_scale], dtype=torch.float32, device=dev)
+        vs = torch.tensor([inp.v_scale], dtype=torch.float32, device=dev)
+        bs, h_q, hd = inp.q.shape
+        h_kv = inp.k_cache.shape[1]
+        splits = fm.gqa_num_splits(bs, h_kv, bt.shape[1] * 16)
+        ws = torch.empty((max(fm.gqa_workspace_bytes(bs, h_q, hd, splits), 256),), dtype=torch.uint8, device=dev)
+        out = torch.empty((bs, h_q, hd), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((bs, h_q), dtype=torch.float32, device=dev)
+
+        def call(i):
+            kc, vc = sets[i % len(sets)]
+            fm.paged_gqa_decode(q, kc, vc, bt, sl, ks, vs, inp.softmax_scale, num_splits=0, out=out, lse=lse,
+                                workspace=ws)
+
+        keys = sum(seqlens)
+        nbytes = keys * h_kv * hd * 2 + 2 * bs * h_q * hd * 2 + bs * h_q * 4 + sum((x + 15) // 16 for x in seqlens) * 4
+        flops = 2.0 * keys * h_q * hd * 2
+        t_tensor = flops / (peaks["bf16"] * 1e12)
+        cfg = dict(workload="paged_gqa_decode", bs=bs, h_q=h_q, h_kv=h_kv, head_dim=hd, page=16,
+                   seqlens="uniform[1024,16384] seed 5", dot="f16", splits=splits,
+                   l2="2 rotating cache copies (~1.1 GB) > L2")
+        metric = "paged GQA decode us/call (bs=32, 32/8 heads, hd 128, ctx U[1024,16384])"
+        launches = 1 if splits == 1 else 2
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    assert fm.last_device_error() == 0
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        call(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert fm.last_device_error() == 0
+    ms = sorted(a.elapsed_time(b) for a, b in evs)
+    avg = sum(ms) / len(ms)
+    t_hbm = nbytes / (peaks["hbm"] * 1e9)
+    res = {
+        "metric": metric, "value": round(avg * 1e3, 2), "unit": "us/call", "higher_is_better": False,
+        "steps": args.steps, "warmup": args.warmup, "n_gpus": 1, "data": "synthetic", "config": cfg,
+        "p10_us": round(ms[len(ms) // 10] * 1e3, 2), "p90_us": round(ms[(9 * len(ms)) // 10] * 1e3, 2),
+        "tflops": round(flops / (avg * 1e-3) / 1e12, 2),
+        "roofline": dict(bound="hbm" if t_hbm >= t_tensor else "tensor",
+                         achieved=round(nbytes / (avg * 1e-3) / 1e9, 1), peak=peaks["hbm"], unit="GB/s",
+                         frac=round(nbytes / (avg * 1e-3) / 1e9 / peaks["hbm"], 4),
+                         algorithmic_bytes_per_launch=int(nbytes), t_hbm_us=round(t_hbm * 1e6, 2),
+                         t_tensor_us=round(t_tensor * 1e6, 2),
+                         roofline_frac_of_time=round(max(t_hbm, t_tensor) / (avg * 1e-3), 4)),
+        "gpu_launches_per_call": launches,
+    }
+    print(json.dumps(res), flush=True)
 
 
 # ------------------------------------------------------ oracle baseline ----
@@ -436,7 +535,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--dot", choices=["fp8", "bf16"], default="fp8")
+    ap.add_argument("--workload", choices=["mla", "sparse", "gqa"], default="mla",
+                    help="mla = the headline line; sparse / gqa = measurement legs of the other variants")
+    ap.add_argument("--sq", type=int, default=2, help="query tokens of the sparse leg (2 or 16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (short runs under a profiler)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-seqs", type=int, default=2, help="sequences of the batch per reference step")
     args = ap.parse_args()
@@ -447,6 +550,10 @@ def main():
         return
     args.steps = 20000 if args.steps is None else args.steps
     args.warmup = 50 if args.warmup is None else max(args.warmup, 3)
+    if args.workload != "mla":
+        args.steps = min(args.steps, 2000)
+        run_secondary(args)
+        return
     run_ours(args)
 
 

@@ -260,16 +260,17 @@ def schedule(seqlens, num_units: int, force_splits: int = 0, page: int = SCHED_P
     Returns (tile_sched [num_units, 8] int32, num_splits [b + 1] int32).
     Unit u covers the flattened (sequence, page) positions from
     (b_begin, page_begin) up to but excluding (b_end, page_end); field 4 is
-    the split index, within sequence b_begin, of the unit's first segment.
-    num_splits is the prefix sum of how many units touch each sequence.
+    the index, among the pieces sequence b_begin is cut into, of the unit's
+    first piece.  num_splits is the prefix sum of the number of pieces of
+    each sequence.
 
-    Balanced rule (force_splits == 0): every non-empty sequence costs its
-    pages plus ``fixed_cost``; each unit gets a budget of
-    ceil(total / num_units) + fixed_cost and takes whole remainders of
-    sequences while they fit, else ``budget_left - fixed_cost`` pages of the
-    current one (when that is at least one page) and stops; the last unit
-    takes whatever is left.  Forced rule (force_splits = k): sequence i is
-    cut into c = min(k, n_i) chunks, chunk j being pages
+    Balanced rule (force_splits == 0): lay the sequences on one cost line,
+    each non-empty sequence taking (pages + fixed_cost) positions; unit u
+    gets positions [floor(u W / U), floor((u + 1) W / U)) of the W in all.
+    A position maps to page max(0, offset - fixed_cost) of its sequence, so
+    a sequence's first fixed_cost positions stand for its page 0.  Units
+    whose interval holds no page are empty.  Forced rule (force_splits = k):
+    sequence i is cut into c = min(k, n_i) chunks, chunk j being pages
     [floor(j n_i / c), floor((j + 1) n_i / c)), one unit per chunk in order.
     """
     sl = as_int64(seqlens)
@@ -296,31 +297,33 @@ def schedule(seqlens, num_units: int, force_splits: int = 0, page: int = SCHED_P
             else:
                 sched[u] = [b, 0, b, 0, 0, 0, 0, 0]
     else:
-        total = sum(x + fixed_cost for x in n if x > 0)
-        budget = -(-total // num_units) + fixed_cost if total > 0 else 0
-        bi, p = 0, 0
+        cost = [x + fixed_cost if x > 0 else 0 for x in n]
+        begin = [0] * (b + 1)
+        for i in range(b):
+            begin[i + 1] = begin[i] + cost[i]
+        total = begin[b]
+
+        def position(x):
+            for i in range(b):
+                if cost[i] > 0 and begin[i] <= x < begin[i] + cost[i]:
+                    return (i, max(0, x - begin[i] - fixed_cost))
+            return (b, 0)
+
+        starts = [position(u * total // num_units) for u in range(num_units)] + [(b, 0)]
         for u in range(num_units):
-            while bi < b and n[bi] == 0:
-                bi += 1
-            start = (bi, p)
-            first = count[bi] if bi < b else 0
-            left = budget
-            while bi < b:
-                if n[bi] == 0:
-                    bi += 1
-                    continue
-                rest = n[bi] - p
-                if u == num_units - 1 or rest + fixed_cost <= left:
-                    left -= rest + fixed_cost
-                    count[bi] += 1
-                    bi, p = bi + 1, 0
-                    continue
-                take = left - fixed_cost
-                if take >= 1:
-                    p += take
-                    count[bi] += 1
-                break
-            sched[u] = [start[0], start[1], bi, p, first, 0, 0, 0]
+            (bs, ps), (be, pe) = starts[u], starts[u + 1]
+            nonempty = (bs, ps) < (be, pe)
+            first = 0
+            if nonempty and ps > 0:
+                first = sum(1 for v in range(u + 1)
+                            if starts[v][0] == bs and starts[v][1] > 0 and starts[v] < starts[v + 1])
+            sched[u] = [bs, ps, be, pe, first, 0, 0, 0]
+            if nonempty:
+                for i in range(bs, min(be, b - 1) + 1):
+                    lo = ps if i == bs else 0
+                    hi = pe if i == be else n[i]
+                    if hi > lo:
+                        count[i] += 1
 
     num_splits = np.zeros(b + 1, dtype=np.int32)
     num_splits[1:] = np.cumsum(count)

@@ -142,7 +142,7 @@ fp8mla_status_t fp8mla_get_metadata(const int32_t* cache_seqlens, int b, int h_q
   if ((b > 0 && cache_seqlens == nullptr) || tile_sched == nullptr || num_splits == nullptr)
     return FP8MLA_ERR_INVALID_ARG;
   if (force_splits > 0 && static_cast<long long>(b) * force_splits > num_units) return FP8MLA_ERR_INVALID_ARG;
-  if (static_cast<size_t>(b) * 8 > kMetadataMaxSmem) return FP8MLA_ERR_INVALID_ARG;
+  if (metadata_smem_bytes(b, num_units) > kMetadataMaxSmem) return FP8MLA_ERR_INVALID_ARG;
   if (launch_mla_metadata(cache_seqlens, b, num_units, force_splits, tile_sched, num_splits,
                           reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FP8MLA_ERR_CUDA;

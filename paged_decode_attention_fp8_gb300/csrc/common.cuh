@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <utility>
 
 #include "fp8mla.h"
 #include "ptx.cuh"
@@ -50,6 +51,34 @@ __device__ __forceinline__ int seq_pages(int s_k, int page, int max_pages, uint3
     return 0;
   }
   return n;
+}
+
+// One arrival per warp: every lane's earlier work (shared-memory writes,
+// completed tcgen05 loads/stores followed by tcgen05.fence::before_thread_sync)
+// is ordered before lane 0's release-arrive by the warp barrier.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Launches `kernel` on `stream` as a programmatic dependent of the previous
+// work in the stream: its CTAs may start while that work finishes, so the
+// kernel must call griddep_wait() before touching memory the predecessor
+// writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace fp8mla

@@ -70,10 +70,10 @@ struct Params {
 
 struct Smem {
   uint64_t kv_full[kStages], kv_empty[kStages], cvt_ready[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma;
+  uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma, xchg;
   uint32_t tmem_base, abort_flag, prod_ok;
   float qs[kN];
-  float red[4][kN];
+  float red[2][4][kN];   // per-warp partial maxima, double-buffered by step parity
   float red2[4][kN];
 };
 
@@ -97,6 +97,8 @@ __device__ __forceinline__ int pow2_exp_f16(float amax) {
 
 __device__ __forceinline__ uint32_t f16x2_of_e4m3x2(uint32_t two_bytes) { return e4m3x2_to_f16x2(two_bytes); }
 
+// kG: the softmax handles heads [0, kG) of the N = 16 MMA columns (kG >= the head group).
+template <int kG>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const Params prm) {
@@ -131,14 +133,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm->kv_full[s], 1);
       mbar_init(&sm->kv_empty[s], 1);
-      mbar_init(&sm->cvt_ready[s], 1);
+      mbar_init(&sm->cvt_ready[s], 4);
     }
     mbar_init(&sm->s_full, 1);
-    mbar_init(&sm->s_free, 128);
-    mbar_init(&sm->p_full, 128);
+    mbar_init(&sm->s_free, 4);
+    mbar_init(&sm->p_full, 4);
     mbar_init(&sm->pv_done, 1);
-    mbar_init(&sm->q_full, 128);
+    mbar_init(&sm->q_full, 4);
     mbar_init(&sm->final_mma, 1);
+    mbar_init(&sm->xchg, 4);
     sm->abort_flag = 0;
     fence_barrier_init();
   }
@@ -146,38 +149,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sm->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  griddep_wait();  // inputs may come from the previous kernel in the stream
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();
   const uint32_t tmem = sm->tmem_base;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
+    // lanes 0..7 fetch the step's block-table entries at once; lane 0 issues the loads
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int i = 0;
-      for (; i < nsteps; ++i) {
-        const int st = i % kStages, use = i / kStages;
-        if (use > 0 && !wait_bounded(&sm->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa)) break;
-        const int p0 = (st0 + i) * kPagesPerStep;
-        const int np = min(kPagesPerStep, n_pages - p0);
-        mbar_arrive_expect_tx(&sm->kv_full[st], 2u * np * kPage * kHd);
-        uint8_t* sb = smem + st * kStageBytes;
-        for (int p = 0; p < np; ++p) {
-          int blk = prm.block_table[static_cast<size_t>(b) * prm.max_blocks + p0 + p];
-          if (blk < 0 || blk >= prm.num_blocks) {
-            atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_PAGE);
-            blk = 0;
-          }
-          const int row = (blk * prm.h_kv + kvh) * kPage;
-          tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->kv_full[st], 0, row, 0);
-          tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->kv_full[st], 0, row, 0);
+    }
+    int i = 0;
+    for (; i < nsteps; ++i) {
+      const int st = i % kStages, use = i / kStages;
+      const int p0 = (st0 + i) * kPagesPerStep;
+      const int np = min(kPagesPerStep, n_pages - p0);
+      int mine = 0;
+      if (lane < np) {
+        mine = __ldg(prm.block_table + static_cast<size_t>(b) * prm.max_blocks + p0 + lane);
+        if (mine < 0 || mine >= prm.num_blocks) {
+          atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_PAGE);
+          mine = 0;
         }
       }
+      int rows[kPagesPerStep];
+#pragma unroll
+      for (int p = 0; p < kPagesPerStep; ++p) rows[p] = (__shfl_sync(0xffffffffu, mine, p) * prm.h_kv + kvh) * kPage;
+      bool ok = true;
+      if (lane == 0) {
+        ok = use == 0 || wait_bounded(&sm->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm->kv_full[st], 2u * np * kPage * kHd);
+          uint8_t* sb = smem + st * kStageBytes;
+#pragma unroll
+          for (int p = 0; p < kPagesPerStep; ++p) {
+            if (p >= np) break;
+            tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->kv_full[st], 0, rows[p], 0);
+            tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->kv_full[st], 0, rows[p], 0);
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    }
+    if (lane == 0)
       for (int j = max(0, i - kStages); j < i; ++j)
         wait_bounded(&sm->kv_full[j % kStages], (j / kStages) & 1, nullptr, &g_status_gqa);
-    }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
@@ -227,6 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x - 128;   // token row of a step / TMEM lane / output dim
     const int w = warp - 4;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(w * 32) << 16);
+    // exchange point of the 128 softmax threads: bounded, abort-aware mbarrier waits
+    uint32_t xphase = 0;
+    auto xsync = [&]() -> bool {
+      warp_arrive(&sm->xchg);
+      const bool ok = warp_wait(&sm->xchg, xphase & 1, abort_flag);
+      ++xphase;
+      return ok;
+    };
     const float k_scale = *prm.k_scale, v_scale = *prm.v_scale;
     const uint16_t* qgrp = prm.q + (static_cast<size_t>(b) * prm.h_q + kvh * prm.group) * kHd;
     {
@@ -256,18 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4*>(row + (((2 * (qj % 4) + 1) ^ (qh % 8)) << 4)) =
           make_uint4(h16[4], h16[5], h16[6], h16[7]);
       fence_proxy_async_smem();
-      named_bar_sync(2, 128);
-      mbar_arrive(&sm->q_full);
+      warp_arrive(&sm->q_full);
     }
-    float c_h[kN], m_h[kN], l_h[kN];
+    for (int i = r; i < kPBytes / 16; i += 128) reinterpret_cast<uint4*>(p_tile)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    bool ok = xsync();  // qs[] and the zeroed P tile complete
+    float c_h[kG], m_h[kG], l_h[kG];
 #pragma unroll
-    for (int h = 0; h < kN; ++h) {
+    for (int h = 0; h < kG; ++h) {
       c_h[h] = prm.softmax_scale * kLog2e * sm->qs[h] * k_scale;
       m_h[h] = kNegInf;
       l_h[h] = 0.f;
     }
-    bool ok = true;
-    for (int i = 0; i < nsteps; ++i) {
+    for (int i = 0; ok && i < nsteps; ++i) {
       const int st = i % kStages, use = i / kStages;
       const int tok = (st0 + i) * kTok + r;
       const bool live = tok < s_k;
@@ -305,8 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dv + (((2 * (c % 4) + 1) ^ sw) << 4)) = vo2;
         }
         fence_proxy_async_smem();
-        named_bar_sync(2, 128);
-        if (r == 0) mbar_arrive(&sm->cvt_ready[st]);
+        warp_arrive(&sm->cvt_ready[st]);  // one arrival per converting warp
       }
       // ---- softmax over this step's tokens ----
       if (!warp_wait(&sm->s_full, i & 1, abort_flag)) {
@@ -318,23 +346,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld16(lane_base + kTS, s);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&sm->s_free);
-      float v[kN];
+      warp_arrive(&sm->s_free);
+      float v[kG];
 #pragma unroll
-      for (int h = 0; h < kN; ++h) v[h] = live ? __uint_as_float(s[h]) * c_h[h] : kNegInf;
+      for (int h = 0; h < kG; ++h) v[h] = live ? __uint_as_float(s[h]) * c_h[h] : kNegInf;
 #pragma unroll
-      for (int h = 0; h < kN; ++h) {
+      for (int h = 0; h < kG; ++h) {
         float x = v[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (lane == 0) sm->red[w][h] = x;
+        if (lane == 0) sm->red[i & 1][w][h] = x;
       }
-      named_bar_sync(2, 128);
-      float alpha[kN];
+      if (!xsync()) {
+        ok = false;
+        break;
+      }
+      float alpha[kG];
       bool any_rescale = false;
 #pragma unroll
-      for (int h = 0; h < kN; ++h) {
-        const float mx = fmaxf(fmaxf(sm->red[0][h], sm->red[1][h]), fmaxf(sm->red[2][h], sm->red[3][h]));
+      for (int h = 0; h < kG; ++h) {
+        const float* rm = &sm->red[i & 1][0][0];
+        const float mx = fmaxf(fmaxf(rm[h], rm[kN + h]), fmaxf(rm[2 * kN + h], rm[3 * kN + h]));
         alpha[h] = 1.f;
         if (mx > m_h[h] + kTau) {
           alpha[h] = ex2_approx(m_h[h] - mx);
@@ -342,10 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_h[h] = mx;
         }
       }
-      named_bar_sync(2, 128);
-      uint32_t ph[kN / 2];
+      uint32_t ph[kG / 2];
 #pragma unroll
-      for (int h = 0; h < kN; h += 2) {
+      for (int h = 0; h < kG; h += 2) {
         const float p0 = ex2_approx(v[h] - (m_h[h] == kNegInf ? 0.f : m_h[h]));
         const float p1 = ex2_approx(v[h + 1] - (m_h[h + 1] == kNegInf ? 0.f : m_h[h + 1]));
         l_h[h] = l_h[h] * alpha[h] + p0;
@@ -362,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(lane_base + kTO, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < kN; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+        for (int h = 0; h < kG; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
         tmem_st16(lane_base + kTO, o);
         tmem_st_wait();
       }
@@ -370,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const int a = r / 64, ch = (r % 64) / 8, el = r % 8;
 #pragma unroll
-        for (int h = 0; h < kN; ++h) {
+        for (int h = 0; h < kG; ++h) {
           const uint16_t val = static_cast<uint16_t>((h & 1) ? (ph[h / 2] >> 16) : (ph[h / 2] & 0xFFFFu));
           *reinterpret_cast<uint16_t*>(p_tile + a * (kN * 128) + (h / 8) * 1024 + (h % 8) * 128 +
                                        ((ch ^ (h % 8)) << 4) + el * 2) = val;
@@ -378,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&sm->p_full);
+      warp_arrive(&sm->p_full);
     }
 
     const bool whole = prm.splits == 1;
@@ -386,18 +417,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && nsteps > 0 && warp_wait(&sm->pv_done, (nsteps - 1) & 1, abort_flag)) {
       tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < kN; ++h) {
+      for (int h = 0; h < kG; ++h) {
         float x = l_h[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
         if (lane == 0) sm->red2[w][h] = x;
       }
-      named_bar_sync(2, 128);
+      ok = xsync();
       uint32_t o[kN];
       tmem_ld16(lane_base + kTO, o);
       tmem_ld_wait();
 #pragma unroll
-      for (int h = 0; h < kN; ++h) {
+      for (int h = 0; h < kG; ++h) {
         if (h >= prm.group) break;
         const float lsum = (sm->red2[0][h] + sm->red2[1][h]) + (sm->red2[2][h] + sm->red2[3][h]);
         const int hq = kvh * prm.group + h;
@@ -438,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merge of split partials: one warp per (sequence = (b, kv head), head), lane l owns 4 dims.
 __global__ void gqa_combine_kernel(const float* __restrict__ ws_o, const float2* __restrict__ ws_ml, int splits,
                                    int group, int h_q, int h_kv, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  griddep_wait();  // launched as a dependent of the decode kernel
   const int seq = blockIdx.x;
   const int h = blockIdx.y * 4 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -584,19 +616,27 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   prm.softmax_scale = softmax_scale;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(gqa::gqa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gqa::gqa_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(gqa::kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(gqa::gqa_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(gqa::kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(gqa::gqa_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(gqa::kSmemBytes)) != cudaSuccess)
       return FP8MLA_ERR_CUDA;
     configured = true;
   }
   const long long grid = static_cast<long long>(bs) * h_kv * splits;
   if (grid > 0x7FFFFFFFll) return FP8MLA_ERR_INVALID_ARG;
-  gqa::gqa_decode_kernel<<<static_cast<unsigned>(grid), gqa::kThreads, gqa::kSmemBytes, stream>>>(tk, tv, prm);
-  if (cudaGetLastError() != cudaSuccess) return FP8MLA_ERR_CUDA;
+  auto kernel = prm.group <= 4 ? gqa::gqa_decode_kernel<4>
+                                : (prm.group <= 8 ? gqa::gqa_decode_kernel<8> : gqa::gqa_decode_kernel<16>);
+  if (launch_dependent(kernel, dim3(static_cast<unsigned>(grid)), dim3(gqa::kThreads), gqa::kSmemBytes, stream, tk,
+                       tv, prm) != cudaSuccess)
+    return FP8MLA_ERR_CUDA;
   if (splits > 1) {
     dim3 cg(static_cast<unsigned>(bs * h_kv), (prm.group + 3) / 4);
-    gqa::gqa_combine_kernel<<<cg, 128, 0, stream>>>(prm.ws_o, prm.ws_ml, splits, prm.group, h_q, h_kv, prm.out, lse);
-    if (cudaGetLastError() != cudaSuccess) return FP8MLA_ERR_CUDA;
+    if (launch_dependent(gqa::gqa_combine_kernel, cg, dim3(128), 0, stream, prm.ws_o, prm.ws_ml, splits, prm.group,
+                         h_q, h_kv, prm.out, lse) != cudaSuccess)
+      return FP8MLA_ERR_CUDA;
   }
   return FP8MLA_OK;
 }

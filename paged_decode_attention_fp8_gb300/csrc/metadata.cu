@@ -1,15 +1,15 @@
 // Tile scheduling for the dense MLA kernel and the split-KV combine kernel.
 //
-// Scheduling: the flattened (sequence, 64-token page) work list is cut into
-// num_units contiguous ranges.  Each page costs 1 and each (sequence, unit)
-// piece a fixed kSchedFixedCost more (Q load + epilogue).  A unit's budget is
-// ceil(total / num_units) + fixed; it takes whole remainders of sequences
-// while they fit, else (budget left - fixed) pages of the current one, and
-// the last unit takes what is left.  A sequence cut across units becomes
-// several splits whose partial (m, l, acc) the combine kernel merges: the
-// split-KV flash-decoding of the InfiniCore "FP8(E4M3) KV cache support in
-// paged attention" page (split-kv commit), with a balanced persistent
-// schedule instead of a fixed split count.
+// Scheduling: every non-empty sequence occupies pages + kSchedFixedCost units
+// of one cost line (the fixed part stands for its Q load and epilogue); unit
+// u takes the cost interval [floor(u W / U), floor((u + 1) W / U)), and a
+// cost position maps to a page of its sequence (its first kSchedFixedCost
+// positions to page 0).  Units whose interval holds no page are empty.  A
+// sequence cut across units becomes several splits whose partial
+// (m, l, acc) the combine kernel merges: the split-KV flash-decoding of the
+// InfiniCore "FP8(E4M3) KV cache support in paged attention" page (split-kv
+// commit), with a balanced persistent schedule instead of a fixed split
+// count.  Every step is a prefix sum or an independent binary search.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -39,81 +39,154 @@ __device__ __forceinline__ void put_row(int32_t* row, int a, int b, int c, int d
   row[7] = 0;
 }
 
-// One warp stages the page counts in shared memory; lane 0 then runs the
-// sequential rule (it touches b + num_units items) at shared-memory latency.
-__global__ void mla_metadata_kernel(const int32_t* __restrict__ seqlens, int B, int U, int force,
-                                    int32_t* __restrict__ sched, int32_t* __restrict__ num_splits) {
-  extern __shared__ int32_t meta_smem[];
-  int32_t* n = meta_smem;        // pages per sequence
-  int32_t* count = n + B;        // splits per sequence
+constexpr int kMetaThreads = 512;
+
+// Exclusive prefix sum of v[0, n) in place (one block); returns the total.
+template <typename T>
+__device__ T block_exclusive_scan(T* v, int n, T* scratch) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int per = (n + nt - 1) / nt;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  T run = 0;
+  for (int i = lo; i < hi; ++i) run += v[i];
+  scratch[tid] = run;
+  __syncthreads();
+  if (tid == 0) {
+    T acc = 0;
+    for (int k = 0; k < nt; ++k) {
+      const T x = scratch[k];
+      scratch[k] = acc;
+      acc += x;
+    }
+    scratch[nt] = acc;
+  }
+  __syncthreads();
+  T acc = scratch[tid];
+  for (int i = lo; i < hi; ++i) {
+    const T x = v[i];
+    v[i] = acc;
+    acc += x;
+  }
+  const T total = scratch[nt];
+  __syncthreads();
+  return total;
+}
+
+// Flattened (sequence, page) position of cost-line position x.
+__device__ __forceinline__ void cost_position(const long long* cost0, const int32_t* n, int B, long long x, int& b,
+                                              int& p) {
+  int lo = 0, hi = B;  // largest b with cost0[b] <= x among non-empty sequences; B if none
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (cost0[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  b = lo;
+  while (b < B && n[b] == 0) ++b;  // cost0 is flat across empty sequences
+  if (b >= B) {
+    b = B;
+    p = 0;
+    return;
+  }
+  const long long off = x - cost0[b] - kSchedFixedCost;
+  p = off > 0 ? static_cast<int>(off) : 0;
+}
+
+__global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_t* __restrict__ seqlens, int B, int U,
+                                                                    int force, int32_t* __restrict__ sched,
+                                                                    int32_t* __restrict__ num_splits) {
+  extern __shared__ __align__(16) uint8_t meta_raw[];
+  long long* cost0 = reinterpret_cast<long long*>(meta_raw);           // [B + 1]
+  long long* lscratch = cost0 + (B + 1);                               // [kMetaThreads + 1]
+  int32_t* n = reinterpret_cast<int32_t*>(lscratch + kMetaThreads + 1);  // [B]
+  int32_t* count = n + B;                                              // [B + 1]
+  int32_t* ustart = count + (B + 1);                                   // [2 (U + 1)]
+  int32_t* iscratch = ustart + 2 * (U + 1);                            // [kMetaThreads + 1]
   if (blockIdx.x != 0) return;
-  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+  griddep_launch_dependents();  // the decode kernel's prologue may overlap this one
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int i = tid; i < B; i += nt) {
     n[i] = pages_of(seqlens[i]);
     count[i] = 0;
   }
-  __syncwarp();
-  if (threadIdx.x == 0) {
-    if (force > 0) {
-      int u = 0;
-      for (int bi = 0; bi < B; ++bi) {
-        const int nb = n[bi];
-        const int c = min(force, nb);
-        for (int j = 0; j < c; ++j, ++u) {
-          if (u >= U) continue;  // the host refuses b * force > num_units
-          const int p0 = static_cast<int>((static_cast<long long>(j) * nb) / c);
-          const int p1 = static_cast<int>((static_cast<long long>(j + 1) * nb) / c);
-          if (p1 == nb)
-            put_row(sched + 8 * u, bi, p0, bi + 1, 0, j);
-          else
-            put_row(sched + 8 * u, bi, p0, bi, p1, j);
-          count[bi] += 1;
-        }
-      }
-      for (; u < U; ++u) put_row(sched + 8 * u, B, 0, B, 0, 0);
-    } else {
-      long long total = 0;
-      for (int bi = 0; bi < B; ++bi)
-        if (n[bi] > 0) total += n[bi] + kSchedFixedCost;
-      const long long budget = total > 0 ? (total + U - 1) / U + kSchedFixedCost : 0;
-      int bi = 0, p = 0;
-      for (int u = 0; u < U; ++u) {
-        while (bi < B && n[bi] == 0) ++bi;
-        const int sb = bi, sp = p;
-        const int first = bi < B ? count[bi] : 0;
-        long long left = budget;
-        while (bi < B) {
-          const int nb = n[bi];
-          if (nb == 0) {
-            ++bi;
-            continue;
-          }
-          const int rest = nb - p;
-          if (u == U - 1 || rest + kSchedFixedCost <= left) {
-            left -= rest + kSchedFixedCost;
-            count[bi] += 1;
-            ++bi;
-            p = 0;
-            continue;
-          }
-          const long long take = left - kSchedFixedCost;
-          if (take >= 1) {
-            p += static_cast<int>(take);
-            count[bi] += 1;
-          }
-          break;
-        }
-        put_row(sched + 8 * u, sb, sp, bi, p, first);
+  __syncthreads();
+
+  if (force > 0) {
+    // chunk j of sequence i (c = min(force, n_i) chunks) goes to unit (number of chunks before i) + j
+    for (int i = tid; i < B; i += nt) count[i] = min(force, n[i]);
+    __syncthreads();
+    block_exclusive_scan<int32_t>(count, B, iscratch);  // count[i] = first unit of sequence i
+    for (int i = tid; i < B; i += nt) {
+      const int nb = n[i], c = min(force, nb), u0 = count[i];
+      for (int j = 0; j < c; ++j) {
+        const int u = u0 + j;
+        if (u >= U) break;  // the host refuses b * force > num_units
+        const int p0 = static_cast<int>((static_cast<long long>(j) * nb) / c);
+        const int p1 = static_cast<int>((static_cast<long long>(j + 1) * nb) / c);
+        if (p1 == nb)
+          put_row(sched + 8 * u, i, p0, i + 1, 0, j);
+        else
+          put_row(sched + 8 * u, i, p0, i, p1, j);
       }
     }
-    int run = 0;
-    num_splits[0] = 0;
-    for (int i = 0; i < B; ++i) {
-      run += count[i];
-      num_splits[i + 1] = run;
+    const int used = B > 0 ? min(U, count[B - 1] + min(force, n[B - 1])) : 0;
+    for (int u = used + tid; u < U; u += nt) put_row(sched + 8 * u, B, 0, B, 0, 0);
+    __syncthreads();
+    for (int i = tid; i < B; i += nt) count[i] = min(force, n[i]);
+  } else {
+    for (int i = tid; i < B; i += nt) cost0[i] = n[i] > 0 ? n[i] + kSchedFixedCost : 0;
+    __syncthreads();
+    const long long W = block_exclusive_scan<long long>(cost0, B, lscratch);
+    if (tid == 0) cost0[B] = W;
+    __syncthreads();
+    // start position of every unit, and of the end (unit U)
+    for (int u = tid; u <= U; u += nt) {
+      int b, p;
+      if (u == U) {
+        b = B;
+        p = 0;
+      } else {
+        cost_position(cost0, n, B, (static_cast<long long>(u) * W) / U, b, p);
+      }
+      ustart[2 * u] = b;
+      ustart[2 * u + 1] = p;
+    }
+    __syncthreads();
+    for (int u = tid; u < U; u += nt) {
+      const int bs = ustart[2 * u], ps = ustart[2 * u + 1];
+      const int be = ustart[2 * u + 2], pe = ustart[2 * u + 3];
+      const bool nonempty = (bs < be) || (bs == be && ps < pe);
+      // piece index inside sequence bs: piece 0 starts at page 0, and every
+      // non-empty unit starting inside it at page > 0 opens the next one
+      int first = 0;
+      if (nonempty && ps > 0)
+        for (int v = u; v >= 0 && ustart[2 * v] == bs; --v) {
+          const int vb = ustart[2 * v], vp = ustart[2 * v + 1];
+          const bool vne = (vb < ustart[2 * v + 2]) || (vb == ustart[2 * v + 2] && vp < ustart[2 * v + 3]);
+          if (vne && vp > 0) ++first;
+        }
+      put_row(sched + 8 * u, bs, ps, be, pe, first);
+      if (nonempty)
+        for (int i = bs; i <= min(be, B - 1); ++i) {
+          const int lo = (i == bs) ? ps : 0;
+          const int hi = (i == be) ? pe : n[i];
+          if (hi > lo) atomicAdd(&count[i], 1);
+        }
     }
   }
+  __syncthreads();
+  const int total = block_exclusive_scan<int32_t>(count, B, iscratch);
+  for (int i = tid; i < B; i += nt) num_splits[i] = count[i];
+  if (tid == 0) num_splits[B] = total;
 }
 
+// Grid (sequence, 4-row block), one warp per row.  A sequence with exactly
+// one split was finished by the decode kernel: only its LSE correction (FP8
+// dots) is left.  Otherwise the lanes first compute the per-split weights
+// 2^(m_s - M) in parallel (split s on lane s % 32), then every lane
+// accumulates its 16 dv columns over the splits.
 // Partial slots are [slot][slot_rows] rows of dv = 512; with uniform_splits > 0
 // sequence bi owns slots [bi * uniform_splits, (bi + 1) * uniform_splits).
 __global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int uniform_splits,
@@ -121,73 +194,95 @@ __global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int
                                      const float* __restrict__ ws_d, const float* __restrict__ ws_corr, int apply_corr,
                                      float softmax_scale, uint16_t* __restrict__ out, float* __restrict__ lse, int rows,
                                      int slot_rows) {
+  griddep_wait();  // launched as a dependent of the decode kernel
   const int bi = blockIdx.x;
-  const int r0 = blockIdx.y * 16;
+  const int r = blockIdx.y * 4 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= rows) return;
   const int s0 = uniform_splits > 0 ? bi * uniform_splits : num_splits[bi];
   const int ns = uniform_splits > 0 ? uniform_splits : num_splits[bi + 1] - s0;
+  const size_t row = static_cast<size_t>(bi) * rows + r;
   if (ns == 1) {
-    const int r = r0 + threadIdx.x;
-    if (!apply_corr || threadIdx.x >= 16 || r >= rows) return;
-    const size_t row = static_cast<size_t>(bi) * rows + r;
-    const float l = lse[row];
-    if (l != kNegInf) lse[row] = l + ws_corr[2 * row] + ws_corr[2 * row + 1];
+    if (apply_corr && lane == 0) {
+      const float l = lse[row];
+      if (l != kNegInf) lse[row] = l + ws_corr[2 * row] + ws_corr[2 * row + 1];
+    }
     return;
   }
-  const int lane = threadIdx.x % 32;
-  for (int r = r0 + threadIdx.x / 32; r < min(r0 + 16, rows); r += 4) {
-    const size_t row = static_cast<size_t>(bi) * rows + r;
-    uint16_t* orow = out + row * kMlaDV + lane * 16;
-    float big_m = kNegInf;
-    for (int s = 0; s < ns; ++s) big_m = fmaxf(big_m, ws_ml[static_cast<size_t>(s0 + s) * slot_rows + r].x);
-    if (ns == 0 || big_m == kNegInf) {  // no visible key: out 0, lse -inf
-      *reinterpret_cast<uint4*>(orow) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(orow + 8) = make_uint4(0, 0, 0, 0);
-      if (lane == 0) lse[row] = kNegInf;
-      continue;
-    }
-    float acc[16];
+  uint16_t* orow = out + row * kMlaDV + lane * 16;
+  float big_m = kNegInf;
+  for (int s = lane; s < ns; s += 32) big_m = fmaxf(big_m, ws_ml[static_cast<size_t>(s0 + s) * slot_rows + r].x);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) acc[c] = 0.f;
-    float big_l = 0.f, dq = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const size_t slot = static_cast<size_t>(s0 + s) * slot_rows + r;
+  for (int o = 16; o > 0; o >>= 1) big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, o));
+  if (ns == 0 || big_m == kNegInf) {  // no visible key: out 0, lse -inf
+    *reinterpret_cast<uint4*>(orow) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(orow + 8) = make_uint4(0, 0, 0, 0);
+    if (lane == 0) lse[row] = kNegInf;
+    return;
+  }
+  float acc[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+  float big_l = 0.f, dq = 0.f;
+  for (int base = 0; base < ns; base += 32) {
+    // this round's splits: lane j holds the weight of split base + j
+    float w = 0.f;
+    if (base + lane < ns) {
+      const size_t slot = static_cast<size_t>(s0 + base + lane) * slot_rows + r;
       const float2 ml = ws_ml[slot];
-      if (ml.x == kNegInf) continue;  // empty shard: the neutral element
-      const float w = ex2_approx(ml.x - big_m);
-      big_l += ml.y * w;
-      if (apply_corr) dq += w * (ws_d[2 * slot] + ws_d[2 * slot + 1]);
+      if (ml.x != kNegInf) {  // empty shard: the neutral element
+        w = ex2_approx(ml.x - big_m);
+        big_l += ml.y * w;
+        if (apply_corr) dq += w * (ws_d[2 * slot] + ws_d[2 * slot + 1]);
+      }
+    }
+    const int cnt = min(32, ns - base);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      const size_t slot = static_cast<size_t>(s0 + base + j) * slot_rows + r;
       const float4* src = reinterpret_cast<const float4*>(ws_o + slot * kMlaDV + lane * 16);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const float4 v = src[c];
-        acc[4 * c + 0] += w * v.x;
-        acc[4 * c + 1] += w * v.y;
-        acc[4 * c + 2] += w * v.z;
-        acc[4 * c + 3] += w * v.w;
+        acc[4 * c + 0] += wj * v.x;
+        acc[4 * c + 1] += wj * v.y;
+        acc[4 * c + 2] += wj * v.z;
+        acc[4 * c + 3] += wj * v.w;
       }
     }
-    const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
-    uint4 w0, w1;
-    w0.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    w0.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    w0.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    w0.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    w1.x = pack_bf16x2(acc[8] * inv, acc[9] * inv);
-    w1.y = pack_bf16x2(acc[10] * inv, acc[11] * inv);
-    w1.z = pack_bf16x2(acc[12] * inv, acc[13] * inv);
-    w1.w = pack_bf16x2(acc[14] * inv, acc[15] * inv);
-    *reinterpret_cast<uint4*>(orow) = w0;
-    *reinterpret_cast<uint4*>(orow + 8) = w1;
-    if (lane == 0)
-      lse[row] = big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 - softmax_scale * dq * inv : kNegInf;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    big_l += __shfl_xor_sync(0xffffffffu, big_l, o);
+    dq += __shfl_xor_sync(0xffffffffu, dq, o);
+  }
+  const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
+  uint4 w0, w1;
+  w0.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  w0.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  w0.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  w0.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  w1.x = pack_bf16x2(acc[8] * inv, acc[9] * inv);
+  w1.y = pack_bf16x2(acc[10] * inv, acc[11] * inv);
+  w1.z = pack_bf16x2(acc[12] * inv, acc[13] * inv);
+  w1.w = pack_bf16x2(acc[14] * inv, acc[15] * inv);
+  *reinterpret_cast<uint4*>(orow) = w0;
+  *reinterpret_cast<uint4*>(orow + 8) = w1;
+  if (lane == 0)
+    lse[row] = big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 - softmax_scale * dq * inv : kNegInf;
 }
 
 }  // namespace
 
+size_t metadata_smem_bytes(int b, int num_units) {
+  return static_cast<size_t>(b + 1 + kMetaThreads + 1) * sizeof(long long) +
+         static_cast<size_t>(b + (b + 1) + 2 * (num_units + 1) + kMetaThreads + 1) * sizeof(int32_t);
+}
+
 cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, int force_splits, int32_t* tile_sched,
                                 int32_t* num_splits, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(b) * 2 * sizeof(int32_t);
+  const size_t smem = metadata_smem_bytes(b, num_units);
   if (smem > kMetadataMaxSmem) return cudaErrorInvalidValue;
   static bool configured = false;
   if (!configured) {
@@ -196,7 +291,8 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  mla_metadata_kernel<<<1, 32, smem, stream>>>(seqlens, b, num_units, force_splits, tile_sched, num_splits);
+  mla_metadata_kernel<<<1, kMetaThreads, smem, stream>>>(seqlens, b, num_units, force_splits, tile_sched,
+                                                         num_splits);
   return cudaGetLastError();
 }
 
@@ -204,10 +300,9 @@ cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, 
                                  const float* ws_d, const float* ws_corr, int apply_corr, float softmax_scale,
                                  uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
-  dim3 grid(b, (rows + 15) / 16);
-  split_combine_kernel<<<grid, 128, 0, stream>>>(num_splits, uniform_splits, ws_o, ws_ml, ws_d, ws_corr, apply_corr,
-                                                 softmax_scale, out, lse, rows, slot_rows);
-  return cudaGetLastError();
+  dim3 grid(b, (rows + 3) / 4);
+  return launch_dependent(split_combine_kernel, grid, dim3(128), 0, stream, num_splits, uniform_splits, ws_o, ws_ml,
+                          ws_d, ws_corr, apply_corr, softmax_scale, out, lse, rows, slot_rows);
 }
 
 cudaError_t launch_mla_combine(const int32_t* num_splits, const float* ws_o, const float2* ws_ml, const float* ws_d,

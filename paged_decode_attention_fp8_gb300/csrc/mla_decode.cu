@@ -43,10 +43,12 @@
 //     the epilogue publishes -softmax_scale * (q_hat - q) . out per dv slice
 //     and the combine step subtracts that first-order term from the LSE.
 //
-// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-3 page conversion (RoPE or whole page to bf16) and tail
-// zeroing, warps 4-7 softmax, Q preparation and epilogue (thread r owns
-// query row r = TMEM lane r).
+// zeroing, warps 4-11 softmax, Q preparation and epilogue: query row r
+// (= TMEM lane r) is shared by two threads, each owning half of the page's
+// score columns, half of the O slice and half of the Q row; the two halves
+// exchange the per-row tile max through shared memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -66,7 +68,7 @@ constexpr int kD = 576;
 constexpr int kDLat = 512;
 constexpr int kDV = 512;
 constexpr int kRows = 128;
-constexpr int kThreads = 256;
+constexpr int kSoftmaxThreads = 256;                // two threads per query row
 constexpr int kLatBox = kPage * 128;                 // one 128-byte column slice of a page (8 KB)
 constexpr uint32_t kPageTxBytes = kPage * kD;        // bytes one page's TMA loads deliver
 
@@ -75,8 +77,10 @@ struct Cfg;
 
 template <>
 struct Cfg<true> {  // FP8 Q/P dots
-  static constexpr int kParts = 2, kDvPart = 256, kStages = 4;
-  static constexpr float kPScale = 128.0f, kTau = 1.0f;
+  static constexpr int kParts = 2, kDvPart = 256, kStages = 3;
+  static constexpr int kThreads = 512;               // + 4 Q-staging warps
+  static constexpr bool kStageQ = true;              // next segment's Q is prepared ahead, in shared memory
+  static constexpr float kPScale = 128.0f, kPLog2 = 7.0f, kTau = 1.0f;
   static constexpr int kOffRope8 = 4 * kLatBox;      // 64 tokens x 64 E4M3 bytes, no swizzle
   static constexpr int kOffCvt = kOffRope8 + kPage * 64;   // RoPE as bf16, 128 B swizzle
   static constexpr int kStageBytes = kOffCvt + kLatBox;
@@ -86,7 +90,9 @@ struct Cfg<true> {  // FP8 Q/P dots
 template <>
 struct Cfg<false> {  // 16-bit dots
   static constexpr int kParts = 4, kDvPart = 128, kStages = 2;
-  static constexpr float kPScale = 1.0f, kTau = 8.0f;
+  static constexpr int kThreads = 384;
+  static constexpr bool kStageQ = false;
+  static constexpr float kPScale = 1.0f, kPLog2 = 0.0f, kTau = 8.0f;
   static constexpr int kOffRope8 = 4 * kLatBox;
   static constexpr int kOffCvt = kOffRope8 + kPage * 64;  // 9 bf16 boxes: 8 latent + RoPE
   static constexpr int kStageBytes = kOffCvt + 9 * kLatBox;
@@ -96,20 +102,34 @@ struct Cfg<false> {  // 16-bit dots
 static_assert(Cfg<true>::kOffCvt % 1024 == 0 && Cfg<true>::kStageBytes % 1024 == 0, "1 KB aligned tiles");
 static_assert(Cfg<false>::kOffCvt % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0, "1 KB aligned tiles");
 
+// Staged Q (FP8 dots): per query row 512 E4M3 latent bytes + 64 bf16 RoPE values
+// (already divided by the row's power-of-two scale), rows padded to 656 bytes
+// so that a warp's 16-byte row reads hit distinct banks; then one float qs per row.
+constexpr int kQStageRow = 656;
+constexpr int kQStageBytes = kRows * kQStageRow + kRows * 4;
+
 template <bool kFp8>
 struct Barriers {
   uint64_t kv_full[Cfg<kFp8>::kStages];
   uint64_t kv_empty[Cfg<kFp8>::kStages];
   uint64_t cvt_ready[Cfg<kFp8>::kStages];
   uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma;
+  uint64_t xchg;            // softmax-group exchange barrier (all 256 softmax threads arrive)
+  uint64_t qst_full;        // staged Q of the next segment is ready (128 Q-staging threads arrive)
+  uint64_t qst_free;        // staged Q was copied into TMEM (256 softmax threads arrive)
   uint32_t tmem_base;
   uint32_t abort_flag;
   uint32_t cvt_ok;
+  float xmax[2][2][kRows];  // per-page tile max of each row half, double-buffered by page parity
+  float xamax[2][kRows];    // Q amax halves
+  float xsum[2][kRows];     // row-sum halves
+  float xdq[2][kRows];      // LSE-correction halves
 };
 
 template <bool kFp8>
 constexpr size_t smem_bytes() {
-  return Cfg<kFp8>::kStages * Cfg<kFp8>::kStageBytes + sizeof(Barriers<kFp8>) + 1024;
+  return Cfg<kFp8>::kStages * Cfg<kFp8>::kStageBytes + (Cfg<kFp8>::kStageQ ? kQStageBytes : 0) +
+         sizeof(Barriers<kFp8>) + 1024;
 }
 
 // One (sequence, page range) piece of a unit's work.
@@ -164,6 +184,11 @@ __device__ __forceinline__ int pow2_scale_exponent(float amax) {
 
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
 
+__device__ __forceinline__ float absmax_bf16x8(uint4 v) {
+  return fmaxf(fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))), fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))),
+               fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))), fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
+}
+
 // x -> E4M3(x * inv_qs) * qs - x: the in-kernel quantisation error of one Q element.
 __device__ __forceinline__ float2 q_quant_error(uint32_t bf16x2, float inv_qs, float qs) {
   const float x0 = bf16_lo(bf16x2), x1 = bf16_hi(bf16x2);
@@ -172,14 +197,16 @@ __device__ __forceinline__ float2 q_quant_error(uint32_t bf16x2, float inv_qs, f
 }
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                       const MlaParams prm) {
   using C = Cfg<kFp8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  Barriers<kFp8>* bars = reinterpret_cast<Barriers<kFp8>*>(smem + C::kStages * C::kStageBytes);
+  uint8_t* qstage = smem + C::kStages * C::kStageBytes;  // FP8 dots only
+  Barriers<kFp8>* bars =
+      reinterpret_cast<Barriers<kFp8>*>(qstage + (C::kStageQ ? kQStageBytes : 0));
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -194,11 +221,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->cvt_ready[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, kRows);
-    mbar_init(&bars->p_full, kRows);
+    mbar_init(&bars->s_free, kSoftmaxThreads / 32);   // one arrival per softmax warp
+    mbar_init(&bars->p_full, kSoftmaxThreads / 32);
     mbar_init(&bars->pv_done, 1);
-    mbar_init(&bars->q_full, kRows);
+    mbar_init(&bars->q_full, kSoftmaxThreads / 32);
     mbar_init(&bars->final_mma, 1);
+    mbar_init(&bars->xchg, kSoftmaxThreads / 32);
+    mbar_init(&bars->qst_full, kRows / 32);
+    mbar_init(&bars->qst_free, kSoftmaxThreads / 32);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -206,44 +236,119 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
+  // Everything above overlaps the previous kernel (launched as its dependent);
+  // from here on this grid reads the schedule and writes outputs.
+  griddep_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
+
+  if constexpr (C::kStageQ) {
+    // The unit's first Q is staged by all 512 threads at once (eight per row,
+    // 72 values each, two rounds of 64 rows) so the first Q.K^T starts early;
+    // the Q-staging warps take over from the second segment on.
+    SegmentWalker first(prm, unit);
+    Segment sg0;
+    if (first.next(sg0)) {
+      const int R = prm.s_q * prm.h_q;
+      const int part = threadIdx.x % 8;  // values [72 part, 72 part + 72) of the row
+#pragma unroll 1
+      for (int round = 0; round < 2; ++round) {
+        const int r = round * 64 + threadIdx.x / 8;
+        const uint16_t* qrow = prm.q + (static_cast<size_t>(sg0.b) * R + r) * kD + part * 72;
+        uint4 v[9];
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < 9; ++c) {
+          v[c] = (r < R) ? __ldg(reinterpret_cast<const uint4*>(qrow) + c) : make_uint4(0, 0, 0, 0);
+          amax = fmaxf(amax, absmax_bf16x8(v[c]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        const int qe = pow2_scale_exponent(amax);
+        const float inv_qs = exp2i(-qe);
+        uint8_t* row = qstage + r * kQStageRow;
+        const int nlat = (part < 7) ? 9 : 1;  // chunks of 8 latent values in this part
+#pragma unroll
+        for (int c = 0; c < 9; ++c) {
+          const uint4 a = v[c];
+          if (c < nlat) {  // 8 latent values -> 8 E4M3 bytes
+            uint2 o;
+            o.x = pack_e4m3x4(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs, bf16_lo(a.y) * inv_qs,
+                              bf16_hi(a.y) * inv_qs);
+            o.y = pack_e4m3x4(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs, bf16_lo(a.w) * inv_qs,
+                              bf16_hi(a.w) * inv_qs);
+            *reinterpret_cast<uint2*>(row + part * 72 + 8 * c) = o;
+          } else {  // RoPE: 8 values -> 16 bytes of bf16 / qs
+            uint4 o;
+            o.x = pack_bf16x2(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs);
+            o.y = pack_bf16x2(bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs);
+            o.z = pack_bf16x2(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs);
+            o.w = pack_bf16x2(bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
+            *reinterpret_cast<uint4*>(row + kDLat + 16 * (c - 1)) = o;
+          }
+        }
+        if (part == 0) reinterpret_cast<float*>(qstage + kRows * kQStageRow)[r] = exp2i(qe);
+      }
+    }
+    __syncthreads();
+    if (warp >= 12) warp_arrive(&bars->qst_full);  // phase 0 of the staging barrier: the first segment
+  }
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
+    // The warp loads 32 block-table entries at a time (one per lane) and lane 0
+    // issues the page loads, so no page waits on its own table lookup.
     if (lane == 0) {
       tma_prefetch_desc(&tm_lat);
       tma_prefetch_desc(&tm_rope);
-      SegmentWalker walk(prm, unit);
-      Segment sg;
-      int i = 0;
-      bool ok = true;
-      while (ok && walk.next(sg)) {
-        for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+    }
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int i = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      const int32_t* bt = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
+      for (int chunk = sg.lo; ok && chunk < sg.hi; chunk += 32) {
+        int mine = 0;
+        if (chunk + lane < sg.hi) {
+          mine = __ldg(bt + chunk + lane);
+          if (mine < 0 || mine >= prm.num_pages) {
+            atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
+            mine = 0;
+          }
+        }
+        const int cnt = min(32, sg.hi - chunk);
+        for (int j = 0; j < cnt; ++j, ++i) {
+          const int phys = __shfl_sync(0xffffffffu, mine, j);
           const int st = i % C::kStages;
           const int use = i / C::kStages;
-          if (use > 0 && !wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla)) {
+          bool waited = true;
+          if (lane == 0) {
+            waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla);
+            if (waited) {
+              uint8_t* sb = smem + st * C::kStageBytes;
+              mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                tma_load_3d(sb + k * kLatBox, &tm_lat, &bars->kv_full[st], k * 128, 0, phys);
+              tma_load_3d(sb + C::kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
             ok = false;
             break;
           }
-          int phys = prm.block_table[static_cast<size_t>(sg.b) * prm.max_pages + pg];
-          if (phys < 0 || phys >= prm.num_pages) {
-            atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
-            phys = 0;
-          }
-          uint8_t* sb = smem + st * C::kStageBytes;
-          mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tma_load_3d(sb + j * kLatBox, &tm_lat, &bars->kv_full[st], j * 128, 0, phys);
-          tma_load_3d(sb + C::kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
         }
       }
-      // Never leave with copies in flight: wait for the last loads issued.
+    }
+    // Never leave with copies in flight: wait for the last loads issued.
+    if (lane == 0)
       for (int j = max(0, i - C::kStages); j < i; ++j)
         wait_bounded(&bars->kv_full[j % C::kStages], (j / C::kStages) & 1, nullptr, &g_status_mla);
-    }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
@@ -408,68 +513,129 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) mbar_arrive(&bars->cvt_ready[st]);
       }
     }
+  } else if (warp >= 12) {
+    // ---------------- Q staging (FP8 dots): one thread per query row ----
+    // Quantises the Q row of every segment, in order, into shared memory
+    // while the previous segment streams: latent -> E4M3(q / qs), RoPE ->
+    // bf16(q / qs), qs = smallest power of two with amax <= 448 qs.
+    if constexpr (C::kStageQ) {
+      const int r = threadIdx.x - 384;
+      const int R = prm.s_q * prm.h_q;
+      uint8_t* row = qstage + r * kQStageRow;
+      float* qs_arr = reinterpret_cast<float*>(qstage + kRows * kQStageRow);
+      SegmentWalker walk(prm, unit);
+      Segment sg;
+      int seg_i = 1;
+      walk.next(sg);  // the first segment was staged by the whole CTA
+      while (walk.next(sg)) {
+        const uint16_t* qrow = prm.q + (static_cast<size_t>(sg.b) * R + r) * kD;
+        float amax = 0.f;
+        if (r < R) {
+          const uint4* q4 = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll 12
+          for (int c = 0; c < kD / 8; ++c) amax = fmaxf(amax, absmax_bf16x8(__ldg(q4 + c)));
+        }
+        const int qe = pow2_scale_exponent(amax);
+        const float inv_qs = exp2i(-qe);
+        // the staging buffer holds one segment: wait until the previous one was copied out
+        if (!warp_wait(&bars->qst_free, (seg_i - 1) & 1, abort_flag)) break;
+        const uint4* q4 = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll 4
+        for (int c = 0; c < kDLat / 16; ++c) {  // 16 latent values -> one 16-byte chunk
+          uint4 a = make_uint4(0, 0, 0, 0), b2 = a;
+          if (r < R) {
+            a = __ldg(q4 + 2 * c);
+            b2 = __ldg(q4 + 2 * c + 1);
+          }
+          uint4 o;
+          o.x = pack_e4m3x4(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs, bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs);
+          o.y = pack_e4m3x4(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs, bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
+          o.z = pack_e4m3x4(bf16_lo(b2.x) * inv_qs, bf16_hi(b2.x) * inv_qs, bf16_lo(b2.y) * inv_qs,
+                            bf16_hi(b2.y) * inv_qs);
+          o.w = pack_e4m3x4(bf16_lo(b2.z) * inv_qs, bf16_hi(b2.z) * inv_qs, bf16_lo(b2.w) * inv_qs,
+                            bf16_hi(b2.w) * inv_qs);
+          *reinterpret_cast<uint4*>(row + 16 * c) = o;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 8 RoPE values -> one 16-byte chunk of bf16
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (r < R) v = __ldg(q4 + kDLat / 8 + c);
+          uint4 o;
+          o.x = pack_bf16x2(bf16_lo(v.x) * inv_qs, bf16_hi(v.x) * inv_qs);
+          o.y = pack_bf16x2(bf16_lo(v.y) * inv_qs, bf16_hi(v.y) * inv_qs);
+          o.z = pack_bf16x2(bf16_lo(v.z) * inv_qs, bf16_hi(v.z) * inv_qs);
+          o.w = pack_bf16x2(bf16_lo(v.w) * inv_qs, bf16_hi(v.w) * inv_qs);
+          *reinterpret_cast<uint4*>(row + kDLat + 16 * c) = o;
+        }
+        qs_arr[r] = exp2i(qe);
+        warp_arrive(&bars->qst_full);  // release: the row is visible to whoever waits on this phase
+        ++seg_i;
+      }
+    }
   } else {
-    // -------------------------------- softmax / Q prep / epilogue ----
-    const int r = threadIdx.x - 128;                       // query row = TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp - 4) * 32) << 16);
+    // ------------------ softmax / Q prep / epilogue (8 warps, 2 per row) ----
+    const int hf = (warp - 4) / 4;                          // which half of the row
+    const int r = (warp % 4) * 32 + lane;                   // query row = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const float kv_scale = *prm.kv_scale;
     const int R = prm.s_q * prm.h_q;
+    constexpr int kOHalf = C::kDvPart / 2;                  // O columns of this thread
+    // Exchange point of the 256 softmax threads: an mbarrier with bounded,
+    // abort-aware waits, so no thread can block forever on a peer that stopped.
+    uint32_t xphase = 0;
+    auto xsync = [&]() -> bool {
+      warp_arrive(&bars->xchg);
+      const bool ok = warp_wait(&bars->xchg, xphase & 1, abort_flag);
+      ++xphase;
+      return ok;
+    };
     SegmentWalker walk(prm, unit);
     Segment sg;
     int i = 0;
+    int seg_ph = 0;  // segments consumed from the Q staging buffer
     while (walk.next(sg)) {
       const uint16_t* qrow = prm.q + (static_cast<size_t>(sg.b) * R + r) * kD;
       float c_row, qs = 1.f, inv_qs = 1.f;
       if constexpr (kFp8) {
-        // ---- Q preparation: latent -> E4M3(q / qs), RoPE -> bf16(q / qs) ----
-        float amax = 0.f;
-        if (r < R) {
-          const uint4* q4 = reinterpret_cast<const uint4*>(qrow);
-#pragma unroll 8
-          for (int c = 0; c < kD / 8; ++c) {
-            const uint4 v = __ldg(q4 + c);
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
-                                     fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))),
-                                     fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
-          }
-        }
-        const int qe = pow2_scale_exponent(amax);
-        qs = exp2i(qe);
-        inv_qs = exp2i(-qe);
+        // ---- Q: copy this half of the staged row into TMEM ----
+        // latent bytes [256 hf, 256 hf + 256) -> columns 64 hf ..; RoPE values [32 hf, 32 hf + 32)
+        if (!warp_wait(&bars->qst_full, seg_ph & 1, abort_flag)) break;
+        const uint8_t* row = qstage + r * kQStageRow;
+        qs = reinterpret_cast<const float*>(qstage + kRows * kQStageRow)[r];
+        inv_qs = 1.0f / qs;  // a power of two: exact
         c_row = prm.softmax_scale * kLog2e * qs * kv_scale;
-#pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {  // 8 chunks of 64 latent values -> 16 columns each
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
           uint32_t pk[16];
-          const uint4* q4 = reinterpret_cast<const uint4*>(qrow + ch * 64);
+          const uint4* src = reinterpret_cast<const uint4*>(row + 256 * hf + 64 * ch);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < R) v = __ldg(q4 + c);
-            pk[2 * c] = pack_e4m3x4(bf16_lo(v.x) * inv_qs, bf16_hi(v.x) * inv_qs, bf16_lo(v.y) * inv_qs,
-                                    bf16_hi(v.y) * inv_qs);
-            pk[2 * c + 1] = pack_e4m3x4(bf16_lo(v.z) * inv_qs, bf16_hi(v.z) * inv_qs, bf16_lo(v.w) * inv_qs,
-                                        bf16_hi(v.w) * inv_qs);
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = src[c];
+            pk[4 * c + 0] = v.x;
+            pk[4 * c + 1] = v.y;
+            pk[4 * c + 2] = v.z;
+            pk[4 * c + 3] = v.w;
           }
-          tmem_st16(lane_base + C::kTQ + ch * 16, pk);
+          tmem_st16(lane_base + C::kTQ + (4 * hf + ch) * 16, pk);
         }
-        uint32_t pk[32];
-        const uint4* q4 = reinterpret_cast<const uint4*>(qrow + kDLat);
+        uint32_t pk[16];
+        const uint4* src = reinterpret_cast<const uint4*>(row + kDLat + 64 * hf);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (r < R) v = __ldg(q4 + c);
-          pk[4 * c + 0] = pack_bf16x2(bf16_lo(v.x) * inv_qs, bf16_hi(v.x) * inv_qs);
-          pk[4 * c + 1] = pack_bf16x2(bf16_lo(v.y) * inv_qs, bf16_hi(v.y) * inv_qs);
-          pk[4 * c + 2] = pack_bf16x2(bf16_lo(v.z) * inv_qs, bf16_hi(v.z) * inv_qs);
-          pk[4 * c + 3] = pack_bf16x2(bf16_lo(v.w) * inv_qs, bf16_hi(v.w) * inv_qs);
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = src[c];
+          pk[4 * c + 0] = v.x;
+          pk[4 * c + 1] = v.y;
+          pk[4 * c + 2] = v.z;
+          pk[4 * c + 3] = v.w;
         }
-        tmem_st32(lane_base + C::kTQR, pk);
+        tmem_st16(lane_base + C::kTQR + 16 * hf, pk);
+        warp_arrive(&bars->qst_free);  // the staging row may be overwritten with the next segment's
+        ++seg_ph;
       } else {
-        // ---- Q preparation: bf16 as is, 576 values -> 288 columns ----
+        // ---- Q preparation: bf16 as is; 64-value chunks 0-4 (hf 0) or 5-8 (hf 1) ----
         c_row = prm.softmax_scale * kLog2e * kv_scale;
 #pragma unroll 1
-        for (int ch = 0; ch < 9; ++ch) {
+        for (int ch = hf ? 5 : 0; ch < (hf ? 9 : 5); ++ch) {
           uint32_t pk[32];
           const uint4* q4 = reinterpret_cast<const uint4*>(qrow + ch * 64);
 #pragma unroll
@@ -486,34 +652,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->q_full);
+      warp_arrive(&bars->q_full);
+      {  // warm L2 with the next segment's Q rows while this one runs
+        SegmentWalker peek = walk;
+        Segment nx;
+        if (peek.next(nx) && r < R) {
+          const char* nq = reinterpret_cast<const char*>(prm.q + (static_cast<size_t>(nx.b) * R + r) * kD);
+          for (int o = hf * (kD * 2 / 2); o < (hf + 1) * (kD * 2 / 2); o += 128) prefetch_l2(nq + o);
+        }
+      }
 
-      // keys visible to this row (bottom-right causal alignment)
+      // keys visible to this row (bottom-right causal alignment); pages wholly
+      // below every row's limit need no mask
       const int qtok = (r < R) ? r / prm.h_q : 0;
       const int visible = prm.causal ? (sg.s_k - prm.s_q + qtok + 1) : sg.s_k;
-      float m_run = kNegInf, l_run = 0.f;
+      const int min_visible = prm.causal ? (sg.s_k - prm.s_q + 1) : sg.s_k;
+      float m_run = kNegInf, l_run = 0.f;  // l_run sums the scaled p (2^kPLog2 p)
       bool ok = true;
       for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+        if constexpr (kFp8) {  // the epilogue's LSE correction re-reads these Q columns
+          if (pg == sg.hi - 1 && r < R) {
+            const char* qc = reinterpret_cast<const char*>(qrow + part * C::kDvPart + hf * kOHalf);
+            prefetch_l2(qc);
+            prefetch_l2(qc + 128);
+          }
+        }
         if (!warp_wait(&bars->s_full, i & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t s[64];
-        tmem_ld32(lane_base + C::kTS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(lane_base + C::kTS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        uint32_t s[32];
+        tmem_ld32(lane_base + C::kTS + 32 * hf, s);
         tmem_ld_wait();
         tc_fence_before();
-        mbar_arrive(&bars->s_free);
+        warp_arrive(&bars->s_free);
 
-        const int base = pg * kPage;
         float mx = kNegInf;
+        if (pg * kPage + kPage > min_visible) {
+          const int base = pg * kPage + 32 * hf;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float v = (base + c < visible) ? __uint_as_float(s[c]) * c_row : kNegInf;
-          s[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int c = 0; c < 32; ++c) {
+            const float v = (base + c < visible) ? __uint_as_float(s[c]) : kNegInf;
+            s[c] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
         }
+        mx *= c_row;  // c_row > 0
+        float* xm = &bars->xmax[i & 1][0][0];
+        xm[hf * kRows + r] = mx;
+        if (!xsync()) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(xm[r], xm[kRows + r]);
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_run + C::kTau) {
@@ -521,18 +716,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = (pg != sg.lo);
           m_run = mx;
         }
-        const float msub = (m_run == kNegInf) ? 0.f : m_run;
+        const float bias = (m_run == kNegInf) ? 0.f : (C::kPLog2 - m_run);
         float sum = 0.f;
-        uint32_t pk[kFp8 ? 16 : 32];
+        uint32_t pk[kFp8 ? 8 : 16];
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float p0 = ex2_approx(__uint_as_float(s[c]) - msub);
-          const float p1 = ex2_approx(__uint_as_float(s[c + 1]) - msub);
-          const float p2 = ex2_approx(__uint_as_float(s[c + 2]) - msub);
-          const float p3 = ex2_approx(__uint_as_float(s[c + 3]) - msub);
+        for (int c = 0; c < 32; c += 4) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c_row, bias));
+          const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
+          const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
           sum += (p0 + p1) + (p2 + p3);
           if constexpr (kFp8) {
-            pk[c / 4] = pack_e4m3x4(p0 * C::kPScale, p1 * C::kPScale, p2 * C::kPScale, p3 * C::kPScale);
+            pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
           } else {
             pk[c / 2] = pack_bf16x2(p0, p1);
             pk[c / 2 + 1] = pack_bf16x2(p2, p3);
@@ -548,45 +743,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, rescale)) {
           const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
-          for (int ch = 0; ch < C::kDvPart / 32; ++ch) {
+          for (int ch = 0; ch < kOHalf / 32; ++ch) {
+            const uint32_t col = C::kTO + hf * kOHalf + ch * 32;
             uint32_t o[32];
-            tmem_ld32(lane_base + C::kTO + ch * 32, o);
+            tmem_ld32(lane_base + col, o);
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
-            tmem_st32(lane_base + C::kTO + ch * 32, o);
+            tmem_st32(lane_base + col, o);
           }
         }
         if constexpr (kFp8)
-          tmem_st16(lane_base + C::kTP, pk);
+          tmem_st8(lane_base + C::kTP + 8 * hf, pk);
         else
-          tmem_st32(lane_base + C::kTP, pk);
+          tmem_st16(lane_base + C::kTP + 16 * hf, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->p_full);
+        warp_arrive(&bars->p_full);
       }
       if (!ok) break;
 
       // ---- epilogue: O is final once the segment's last P.V completes ----
       if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag)) break;
       tc_fence_after();
+      bars->xsum[hf][r] = l_run;
+      if (!xsync()) break;
+      const float l_tot = (bars->xsum[0][r] + bars->xsum[1][r]) * (1.0f / C::kPScale);  // sum of p
       const bool whole = (sg.lo == 0 && sg.hi == sg.n);
       const float o_scale = kv_scale / C::kPScale;  // tensor-core units -> true units
-      const float f = whole ? ((l_run > 0.f) ? o_scale / l_run : 0.f) : o_scale;
-      const int col0 = part * C::kDvPart;
+      const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
+      const int col0 = part * C::kDvPart + hf * kOHalf;
       const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
-      float dq_dot = 0.f;  // sum over this slice of (q_hat - q) * O (FP8 dots only)
+      float dq_dot = 0.f;  // sum over this thread's columns of (q_hat - q) * O (FP8 dots only)
 #pragma unroll 1
-      for (int ch = 0; ch < C::kDvPart / 32; ++ch) {
+      for (int ch = 0; ch < kOHalf / 32; ++ch) {
+        uint4 qv[4];  // this chunk's Q (prefetched into L2 during the last page), loaded beside O
+        if constexpr (kFp8) {
+          if (r < R) {
+            const uint4* q4 = reinterpret_cast<const uint4*>(qrow + col0 + ch * 32);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) qv[c] = __ldg(q4 + c);
+          }
+        }
         uint32_t o[32];
-        tmem_ld32(lane_base + C::kTO + ch * 32, o);
+        tmem_ld32(lane_base + C::kTO + hf * kOHalf + ch * 32, o);
         tmem_ld_wait();
         if (r >= R) continue;
         if constexpr (kFp8) {
-          const uint4* q4 = reinterpret_cast<const uint4*>(qrow + col0 + ch * 32);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 v = __ldg(q4 + c);
+            const uint4 v = qv[c];
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -615,14 +821,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __uint_as_float(o[4 * c + 2]) * f, __uint_as_float(o[4 * c + 3]) * f);
         }
       }
-      if (r < R) {
+      if constexpr (kFp8) {
+        bars->xdq[hf][r] = dq_dot;
+        if (!xsync()) break;
+        dq_dot = bars->xdq[0][r] + bars->xdq[1][r];
+      }
+      if (r < R && hf == 0) {
         const size_t row = static_cast<size_t>(sg.b) * R + r;
         if (whole) {
-          if (part == 0) prm.lse[row] = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * kLn2 : kNegInf;
+          if (part == 0) prm.lse[row] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
           if constexpr (kFp8) prm.ws_corr[row * 2 + part] = -prm.softmax_scale * dq_dot * f;
         } else {
           const size_t srow = static_cast<size_t>(slot) * kRows + r;
-          if (part == 0) prm.ws_ml[srow] = make_float2((l_run > 0.f) ? m_run : kNegInf, l_run);
+          if (part == 0) prm.ws_ml[srow] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
           if constexpr (kFp8) prm.ws_d[srow * 2 + part] = dq_dot * f;
         }
       }
@@ -647,9 +858,8 @@ cudaError_t launch(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const 
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  mla_decode_kernel<kFp8><<<num_units * Cfg<kFp8>::kParts, kThreads, smem_bytes<kFp8>(), stream>>>(tm_lat, tm_rope,
-                                                                                                   prm);
-  return cudaGetLastError();
+  return launch_dependent(mla_decode_kernel<kFp8>, dim3(num_units * Cfg<kFp8>::kParts), dim3(Cfg<kFp8>::kThreads),
+                          smem_bytes<kFp8>(), stream, tm_lat, tm_rope, prm);
 }
 
 }  // namespace mla

@@ -33,7 +33,8 @@ constexpr int kMlaDV = 512;
 constexpr int kMlaPage = 64;
 constexpr int kMlaD = 576;
 constexpr int kSchedFixedCost = 4;
-constexpr size_t kMetadataMaxSmem = 200 * 1024;  // the scheduler stages 8 bytes per sequence: b <= 25600
+constexpr size_t kMetadataMaxSmem = 200 * 1024;  // the scheduler stages ~16 bytes per sequence and unit
+size_t metadata_smem_bytes(int b, int num_units);
 
 // dense MLA decode kernels (mla_decode.cu)
 cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,

@@ -74,10 +74,10 @@ struct Params {
 
 struct Smem {
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma;
+  uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma, xchg;
   uint32_t tmem_base, abort_flag, prod_ok;
   float qs[kN];
-  float red[4][kN];
+  float red[2][4][kN];   // per-warp partial maxima, double-buffered by step parity
   float red2[4][kN];
 };
 
@@ -133,11 +133,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->kv_empty[s], 1);
     }
     mbar_init(&sm->s_full, 1);
-    mbar_init(&sm->s_free, 128);
-    mbar_init(&sm->p_full, 128);
+    mbar_init(&sm->s_free, 4);
+    mbar_init(&sm->p_full, 4);
     mbar_init(&sm->pv_done, 1);
-    mbar_init(&sm->q_full, 128);
+    mbar_init(&sm->q_full, 4);
     mbar_init(&sm->final_mma, 1);
+    mbar_init(&sm->xchg, 4);
     sm->abort_flag = 0;
     fence_barrier_init();
   }
@@ -145,9 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sm->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  griddep_wait();  // inputs may come from the previous kernel in the stream
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();
   const uint32_t tmem = sm->tmem_base;
 
   if (warp == 0) {
@@ -223,6 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = threadIdx.x - 128;
     const int w = warp - 4;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(w * 32) << 16);
+    // exchange point of the 128 softmax threads: bounded, abort-aware mbarrier waits
+    uint32_t xphase = 0;
+    auto xsync = [&]() -> bool {
+      warp_arrive(&sm->xchg);
+      const bool ok = warp_wait(&sm->xchg, xphase & 1, abort_flag);
+      ++xphase;
+      return ok;
+    };
     const float kv_scale = *prm.kv_scale;
     const uint16_t* qtok = prm.q + static_cast<size_t>(t) * prm.h_q * kD;
 
@@ -259,9 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(row + ((chunk ^ (qh % 8)) << 4)) = o;
       }
       fence_proxy_async_smem();
-      named_bar_sync(2, 128);
-      mbar_arrive(&sm->q_full);
+      warp_arrive(&sm->q_full);
     }
+    bool ok = xsync();  // qs[] complete
     float c_h[kN], m_h[kN], l_h[kN];
 #pragma unroll
     for (int h = 0; h < kN; ++h) {
@@ -269,8 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_h[h] = kNegInf;
       l_h[h] = 0.f;
     }
-    bool ok = true;
-    for (int i = 0; i < nchunks; ++i) {
+    for (int i = 0; ok && i < nchunks; ++i) {
       const int kslot = (c0 + i) * kKeys + r;
       const bool valid = key_row(prm, t, kslot) >= 0;
       if (!warp_wait(&sm->s_full, i & 1, abort_flag)) {
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld16(lane_base + kTS, s);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&sm->s_free);
+      warp_arrive(&sm->s_free);
       float v[kN];
 #pragma unroll
       for (int h = 0; h < kN; ++h) v[h] = valid ? __uint_as_float(s[h]) * c_h[h] : kNegInf;
@@ -292,14 +302,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         float x = v[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (lane == 0) sm->red[w][h] = x;
+        if (lane == 0) sm->red[i & 1][w][h] = x;
       }
-      named_bar_sync(2, 128);
+      if (!xsync()) {
+        ok = false;
+        break;
+      }
       float alpha[kN];
       bool any_rescale = false;
 #pragma unroll
       for (int h = 0; h < kN; ++h) {
-        const float mx = fmaxf(fmaxf(sm->red[0][h], sm->red[1][h]), fmaxf(sm->red[2][h], sm->red[3][h]));
+        const float* rm = &sm->red[i & 1][0][0];
+        const float mx = fmaxf(fmaxf(rm[h], rm[kN + h]), fmaxf(rm[2 * kN + h], rm[3 * kN + h]));
         alpha[h] = 1.f;
         if (mx > m_h[h] + kTau) {
           alpha[h] = ex2_approx(m_h[h] - mx);
@@ -307,7 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_h[h] = mx;
         }
       }
-      named_bar_sync(2, 128);  // red[] may be overwritten next step only after everyone read it
       uint8_t pb[kN];
 #pragma unroll
       for (int h = 0; h < kN; ++h) {
@@ -339,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         p_tile[(h / 8) * 1024 + (h % 8) * 128 + ((((r >> 4) ^ (h % 8))) << 4) + (r & 15)] = pb[h];
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&sm->p_full);
+      warp_arrive(&sm->p_full);
     }
 
     if (ok && nchunks > 0 && warp_wait(&sm->pv_done, (nchunks - 1) & 1, abort_flag)) {
@@ -352,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
         if (lane == 0) sm->red2[w][h] = x;
       }
-      named_bar_sync(2, 128);
+      ok = xsync();
       float lsum[kN], dq[kN];
 #pragma unroll
       for (int h = 0; h < kN; ++h) {
@@ -389,12 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float x = dq[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) sm->red[w][h] = x;
+        if (lane == 0) sm->red[0][w][h] = x;   // the per-step slots are no longer in use here
       }
-      named_bar_sync(2, 128);
-      if (r < prm.h_q) {
+      if (xsync() && r < prm.h_q) {
         const int h = r;
-        const float dsum = (sm->red[0][h] + sm->red[1][h]) + (sm->red[2][h] + sm->red[3][h]);
+        const float dsum = (sm->red[0][0][h] + sm->red[0][1][h]) + (sm->red[0][2][h] + sm->red[0][3][h]);
         float mh = kNegInf;
 #pragma unroll
         for (int k = 0; k < kN; ++k)
@@ -543,8 +555,9 @@ fp8mla_status_t sparse_decode_entry(const void* q, const void* kv_cache, int64_t
       return FP8MLA_ERR_CUDA;
     configured = true;
   }
-  sparse::sparse_mla_kernel<<<s_q * splits, sparse::kThreads, sparse::kSmemBytes, stream>>>(tm, prm);
-  if (cudaGetLastError() != cudaSuccess) return FP8MLA_ERR_CUDA;
+  if (launch_dependent(sparse::sparse_mla_kernel, dim3(s_q * splits), dim3(sparse::kThreads), sparse::kSmemBytes,
+                       stream, tm, prm) != cudaSuccess)
+    return FP8MLA_ERR_CUDA;
   if (splits > 1) {
     if (launch_split_combine(nullptr, splits, prm.ws_o, prm.ws_ml, prm.ws_d, nullptr, 1, softmax_scale,
                              static_cast<uint16_t*>(out), lse, s_q, h_q, sparse::kN, stream) != cudaSuccess)
