@@ -189,9 +189,11 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
 // accumulates its 16 dv columns over the splits.
 // Partial slots are [slot][slot_rows] rows of dv = 512; with uniform_splits > 0
 // sequence bi owns slots [bi * uniform_splits, (bi + 1) * uniform_splits).
+// corr_terms (0 = none) is the number of LSE-correction shares each row or
+// slot row carries in ws_corr / ws_d (one per producer of a piece of the row).
 __global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int uniform_splits,
                                      const float* __restrict__ ws_o, const float2* __restrict__ ws_ml,
-                                     const float* __restrict__ ws_d, const float* __restrict__ ws_corr, int apply_corr,
+                                     const float* __restrict__ ws_d, const float* __restrict__ ws_corr, int corr_terms,
                                      float softmax_scale, uint16_t* __restrict__ out, float* __restrict__ lse, int rows,
                                      int slot_rows) {
   griddep_wait();  // launched as a dependent of the decode kernel
@@ -203,9 +205,11 @@ __global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int
   const int ns = uniform_splits > 0 ? uniform_splits : num_splits[bi + 1] - s0;
   const size_t row = static_cast<size_t>(bi) * rows + r;
   if (ns == 1) {
-    if (apply_corr && lane == 0) {
+    if (corr_terms > 0 && lane == 0) {
       const float l = lse[row];
-      if (l != kNegInf) lse[row] = l + ws_corr[2 * row] + ws_corr[2 * row + 1];
+      float c = 0.f;
+      for (int t = 0; t < corr_terms; ++t) c += ws_corr[corr_terms * row + t];
+      if (l != kNegInf) lse[row] = l + c;
     }
     return;
   }
@@ -233,7 +237,11 @@ __global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int
       if (ml.x != kNegInf) {  // empty shard: the neutral element
         w = ex2_approx(ml.x - big_m);
         big_l += ml.y * w;
-        if (apply_corr) dq += w * (ws_d[2 * slot] + ws_d[2 * slot + 1]);
+        if (corr_terms > 0) {
+          float d = 0.f;
+          for (int t = 0; t < corr_terms; ++t) d += ws_d[corr_terms * slot + t];
+          dq += w * d;
+        }
       }
     }
     const int cnt = min(32, ns - base);
@@ -297,19 +305,19 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
 }
 
 cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const float* ws_o, const float2* ws_ml,
-                                 const float* ws_d, const float* ws_corr, int apply_corr, float softmax_scale,
+                                 const float* ws_d, const float* ws_corr, int corr_terms, float softmax_scale,
                                  uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
   dim3 grid(b, (rows + 3) / 4);
   return launch_dependent(split_combine_kernel, grid, dim3(128), 0, stream, num_splits, uniform_splits, ws_o, ws_ml,
-                          ws_d, ws_corr, apply_corr, softmax_scale, out, lse, rows, slot_rows);
+                          ws_d, ws_corr, corr_terms, softmax_scale, out, lse, rows, slot_rows);
 }
 
 cudaError_t launch_mla_combine(const int32_t* num_splits, const float* ws_o, const float2* ws_ml, const float* ws_d,
                                const float* ws_corr, int apply_corr, float softmax_scale, uint16_t* out, float* lse,
                                int b, int rows, cudaStream_t stream) {
-  return launch_split_combine(num_splits, 0, ws_o, ws_ml, ws_d, ws_corr, apply_corr, softmax_scale, out, lse, b, rows,
-                              kMlaRows, stream);
+  return launch_split_combine(num_splits, 0, ws_o, ws_ml, ws_d, ws_corr, apply_corr ? kMlaCorrTerms : 0,
+                              softmax_scale, out, lse, b, rows, kMlaRows, stream);
 }
 
 uint32_t metadata_read_and_clear_status() {

@@ -848,18 +848,747 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   }
 }
 
+// ===========================================================================
+// FP8-dots kernel.
+//
+// Work unit = 2 CTAs, each owning one 256-wide dv slice.  The shared-memory
+// ring of 5 stages carries, in one order that every role walks, two Q slots
+// at the start of each segment (the segment's quantised Q, one row half per
+// slot) followed by the segment's KV pages, so no separate Q buffer competes
+// with the KV pages for shared memory.  TMEM: O 256 + S 64 + two P buffers
+// of 16 + Q latent 128 + Q RoPE 32 columns.
+// ===========================================================================
+namespace f8 {
+constexpr int kStages = 5;
+constexpr int kThreads = 384;
+constexpr int kOffRope8 = 4 * kLatBox;            // 64 tokens x 64 E4M3 RoPE bytes, no swizzle
+constexpr int kOffCvt = kOffRope8 + kPage * 64;   // the RoPE part as bf16, 128-byte swizzle
+constexpr int kStageBytes = kOffCvt + kLatBox;
+constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
+constexpr float kTau = 2.75f;                     // 64 * 2^2.75 = 430.5 < 448
+constexpr uint32_t kTO = 0, kTS = 256, kTP = 320, kTQ = 352, kTQR = 480;
+constexpr int kPCols = 16;                        // one P buffer: 64 E4M3 keys per row
+// Q slot h (h = 0, 1): per row, latent bytes [256 h, 256 h + 256) at a 272-byte
+// pitch, then per row RoPE values [32 h, 32 h + 32) as bf16 at an 80-byte pitch
+// (pitches chosen so a quarter-warp's 16-byte row accesses hit distinct banks).
+constexpr int kQLatPitch = 272;
+constexpr int kQRopeOff = kRows * kQLatPitch;
+constexpr int kQRopePitch = 80;
+static_assert(kQRopeOff + kRows * kQRopePitch <= kStageBytes, "a Q slot fits one stage");
+static_assert(kOffCvt % 1024 == 0 && kStageBytes % 1024 == 0, "1 KB aligned tiles");
+static_assert(kStageBytes == kMlaQSlotBytes, "a quantised-Q half is one ring stage");
+
+struct Bars {
+  uint64_t kv_full[kStages];    // stage holds its page (TMA bytes) or its Q slot (Q warps' arrival)
+  uint64_t kv_empty[kStages];   // stage may be refilled
+  uint64_t cvt_ready[kStages];  // the page's RoPE part is converted and its dead rows zeroed
+  uint64_t p_full[2];           // P buffer b written (one arrival per softmax warp)
+  uint64_t pv_done[2];          // the P.V that read P buffer b completed
+  uint64_t s_full, s_free, q_full, final_mma, xchg;
+  uint32_t tmem_base, abort_flag, cvt_ok;
+  float xsum[2][kRows];         // row-sum halves
+};
+
+constexpr size_t smem_bytes() { return kStages * kStageBytes + sizeof(Bars) + 1024; }
+
+// Quantises the Q rows of sequence b into the two Q slots: latent -> E4M3(q / qs),
+// RoPE -> bf16(q / qs), qs = smallest power of two with amax <= 448 qs.  kTpr
+// threads share a row; thread `part` takes the 8-value chunks c = part (mod kTpr)
+// of the row's 72 (64 latent, 8 RoPE).
+template <int kTpr>
+__device__ __forceinline__ void fill_q_row(const MlaParams& prm, int b, int r, int part, uint8_t* slot0,
+                                           uint8_t* slot1, float* qs_out) {
+  constexpr int kChunks = 72 / kTpr;
+  constexpr bool kHold = kChunks <= 18;  // few enough chunks to keep in registers between the two passes
+  const int R = prm.s_q * prm.h_q;
+  const bool live = r < R;
+  const uint4* q4 = reinterpret_cast<const uint4*>(prm.q + (static_cast<size_t>(b) * R + (live ? r : 0)) * kD);
+  uint4 held[kHold ? kChunks : 1];
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const uint4 v = live ? __ldg(q4 + part + j * kTpr) : make_uint4(0, 0, 0, 0);
+    if constexpr (kHold) held[j] = v;
+    amax = fmaxf(amax, absmax_bf16x8(v));
+  }
+#pragma unroll
+  for (int o = 1; o < kTpr; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int qe = pow2_scale_exponent(amax);
+  const float inv_qs = exp2i(-qe);
+  // chunk c (8 values) -> latent bytes of slot c / 32, or bf16 RoPE of slot (c - 64) / 4
+  auto put = [&](int c, uint4 a) {
+    if (c < 64) {
+      uint2 o;
+      o.x = pack_e4m3x4(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs, bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs);
+      o.y = pack_e4m3x4(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs, bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
+      uint8_t* slot = (c < 32) ? slot0 : slot1;
+      *reinterpret_cast<uint2*>(slot + r * kQLatPitch + (c & 31) * 8) = o;
+    } else {
+      uint4 o;
+      o.x = pack_bf16x2(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs);
+      o.y = pack_bf16x2(bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs);
+      o.z = pack_bf16x2(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs);
+      o.w = pack_bf16x2(bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
+      const int j4 = c - 64;
+      uint8_t* slot = (j4 < 4) ? slot0 : slot1;
+      *reinterpret_cast<uint4*>(slot + kQRopeOff + r * kQRopePitch + (j4 & 3) * 16) = o;
+    }
+  };
+  if constexpr (kHold) {
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) put(part + j * kTpr, held[j]);
+  } else {
+#pragma unroll 6
+    for (int j = 0; j < kChunks; ++j) {
+      const int c = part + j * kTpr;
+      put(c, live ? __ldg(q4 + c) : make_uint4(0, 0, 0, 0));
+    }
+  }
+  if (part == 0) qs_out[r] = exp2i(qe);
+}
+// Quantised Q for FP8 dots in the ring's Q-slot layout, one grid ahead of the
+// decode kernel: grid (b, 4), 256 threads, eight threads per row, 32 rows per
+// CTA.  It lets the decode kernel start its prologue at once, and completes
+// only after the grid it was launched behind (so that the decode kernel's
+// wait on this grid also covers the tile schedule written before it).
+__global__ void __launch_bounds__(256) mla_qprep_kernel(const MlaParams prm) {
+  griddep_launch_dependents();
+  const int b = blockIdx.x;
+  const int r = blockIdx.y * 32 + threadIdx.x / 8;
+  uint8_t* half0 = prm.qbuf + static_cast<size_t>(b) * 2 * kStageBytes;
+  fill_q_row<8>(prm, b, r, threadIdx.x % 8, half0, half0 + kStageBytes, prm.qscale + static_cast<size_t>(b) * kRows);
+  griddep_wait();
+}
+
+// Lanes in groups of N (N = 4 or 8) each hold N 16-byte pieces; afterwards
+// lane q of a group holds piece q of every lane of its group, piece k coming
+// from lane k (an N x N transpose by XOR butterflies).
+template <int N>
+__device__ __forceinline__ void lane_group_transpose(uint4 (&pc)[N], int lane) {
+  const int q = lane & (N - 1);
+#pragma unroll
+  for (int m = N / 2; m >= 1; m >>= 1) {
+    const bool hi = (q & m) != 0;
+#pragma unroll
+    for (int a = 0; a < N; ++a) {
+      if (a & m) continue;
+      const int b = a | m;
+      uint4 t = hi ? pc[a] : pc[b];  // the piece the partner needs
+      t.x = __shfl_xor_sync(0xffffffffu, t.x, m);
+      t.y = __shfl_xor_sync(0xffffffffu, t.y, m);
+      t.z = __shfl_xor_sync(0xffffffffu, t.z, m);
+      t.w = __shfl_xor_sync(0xffffffffu, t.w, m);
+      if (hi)
+        pc[a] = t;
+      else
+        pc[b] = t;
+    }
+  }
+}
+}  // namespace f8
+
+__global__ void __launch_bounds__(f8::kThreads, 1)
+    mla_fp8_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                   const MlaParams prm) {
+  using namespace f8;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kStages * kStageBytes);
+  volatile uint32_t* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int unit = blockIdx.x / 2;
+  const int part = blockIdx.x % 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->cvt_ready[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->p_full[b], kSoftmaxThreads / 32);
+      mbar_init(&bars->pv_done[b], 1);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, kSoftmaxThreads / 32);  // one arrival per softmax warp
+    mbar_init(&bars->q_full, kSoftmaxThreads / 32);
+    mbar_init(&bars->final_mma, 1);
+    mbar_init(&bars->xchg, kSoftmaxThreads / 32);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  // Everything above overlaps the previous kernel (launched as its dependent);
+  // from here on this grid reads the schedule and writes outputs.
+  griddep_wait();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_launch_dependents();
+  const uint32_t tmem = bars->tmem_base;
+
+  // Ring protocol.  Every role walks the same slot sequence: two Q slots at
+  // the start of each segment (the halves of its quantised Q, prepared by
+  // mla_qprep_kernel) and then its pages.  Each stage barrier completes one
+  // phase per occupancy of its stage, and every role that waits on one
+  // observes each of its phases in turn, so a parity wait can never pass on a
+  // phase two behind or two ahead: kv_empty is waited by the producer only;
+  // kv_full by the converter for every occupancy, by the MMA warp for pages
+  // and by the softmax warps for Q slots; each stage is released only after
+  // the converter's cvt_ready for that occupancy.
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ----
+    // The warp loads 32 block-table entries at a time (one per lane); lane 0
+    // issues the loads.
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_lat);
+      tma_prefetch_desc(&tm_rope);
+    }
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int k = 0;
+    uint32_t issued = 0, par = 0;  // per stage: last occupant was loaded here, and its use parity
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      // the segment's quantised Q, one half per slot
+      for (int q = 0; q < 2 && ok; ++q, ++k) {
+        const int st = k % kStages, use = k / kStages;
+        bool waited = true;
+        if (lane == 0) {
+          waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla);
+          if (waited) {
+            mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+            bulk_load(smem + st * kStageBytes, prm.qbuf + (static_cast<size_t>(sg.b) * 2 + q) * kStageBytes,
+                      kStageBytes, &bars->kv_full[st]);
+            issued |= 1u << st;
+            par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0;
+      }
+      if (!ok) break;
+      const int32_t* bt = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
+      for (int chunk = sg.lo; ok && chunk < sg.hi; chunk += 32) {
+        int mine = 0;
+        if (chunk + lane < sg.hi) {
+          mine = __ldg(bt + chunk + lane);
+          if (mine < 0 || mine >= prm.num_pages) {
+            atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
+            mine = 0;
+          }
+        }
+        const int cnt = min(32, sg.hi - chunk);
+        for (int j = 0; j < cnt; ++j, ++k) {
+          const int phys = __shfl_sync(0xffffffffu, mine, j);
+          const int st = k % kStages;
+          const int use = k / kStages;
+          bool waited = true;
+          if (lane == 0) {
+            waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla);
+            if (waited) {
+              uint8_t* sb = smem + st * kStageBytes;
+              mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kLatBox, &tm_lat, &bars->kv_full[st], q * 128, 0, phys);
+              tma_load_3d(sb + kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
+              issued |= 1u << st;
+              par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
+            ok = false;
+            break;
+          }
+        }
+      }
+    }
+    // Never leave with copies in flight: wait for the last load of each stage.
+    if (lane == 0)
+      for (int s = 0; s < kStages; ++s)
+        if ((issued >> s) & 1u) wait_bounded(&bars->kv_full[s], (par >> s) & 1u, nullptr, &g_status_mla);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer ----
+    // The whole warp runs the loop (so descriptors stay warp-uniform) and one
+    // elected lane issues -- from a lone thread each MMA costs about twice as
+    // long to issue.  Per page i: wait until S was read out, Q.K^T as 16 E4M3
+    // MMAs (latent, K = 32) and 4 bf16 MMAs (RoPE, K = 16) back to back, then
+    // the P.V of page i - 2, whose P the softmax warps store while this Q.K^T
+    // runs, so Q.K^T never waits behind a P.V.
+    {
+      constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
+      constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);   // bf16 x bf16
+      constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
+      const uint32_t t_s = tmem + kTS, t_o = tmem + kTO;
+      const bool leader = elect_one();
+      SegmentWalker walk(prm, unit);
+      Segment sg;
+      int i = 0, k = 0, seg = 0;
+      int j = 0;           // next page whose P.V is due (pages j .. i - 1 have their Q.K^T issued)
+      uint32_t pend = 0;   // per pending page p, byte p % 4: its stage | first-of-segment << 3
+      bool ok = true;
+      // the P.V of page j, once its P is written
+      auto issue_pv = [&]() -> bool {
+        const int pb = j & 1;
+        if (!warp_wait(&bars->p_full[pb], (j >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t e = (pend >> (8 * (j & 3))) & 0xFFu;
+        const int st = static_cast<int>(e & 7u);
+        const bool first = ((e >> 3) & 1u) != 0;
+        const uint32_t v_base = smem_u32(smem + st * kStageBytes) + part * 2 * kLatBox;
+        const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          if (leader)
+            mma_f8_ts(t_o, tmem + kTP + pb * kPCols + kk * 8, vd + ((kk * 4096) >> 4), idesc_pv,
+                      (first && kk == 0) ? 0u : 1u);
+          __syncwarp();
+        }
+        if (leader) {
+          tc_commit(&bars->pv_done[pb]);
+          tc_commit(&bars->kv_empty[st]);
+        }
+        __syncwarp();
+        ++j;
+        return true;
+      };
+      while (ok && walk.next(sg)) {
+        const int st0 = k % kStages, st1 = (k + 1) % kStages;
+        // The previous segment's last P.Vs come first: the softmax warps write
+        // their P before they copy this segment's Q.
+        while (ok && j < i) ok = issue_pv();
+        // the softmax warps have copied both Q slots into TMEM (and the converter has seen them)
+        if (!ok || !warp_wait(&bars->q_full, seg & 1, abort_flag) ||
+            !warp_wait(&bars->cvt_ready[st0], (k / kStages) & 1, abort_flag) ||
+            !warp_wait(&bars->cvt_ready[st1], ((k + 1) / kStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          mbar_arrive(&bars->kv_empty[st0]);
+          mbar_arrive(&bars->kv_empty[st1]);
+        }
+        __syncwarp();
+        k += 2;
+        for (int pg = sg.lo; pg < sg.hi; ++pg, ++i, ++k) {
+          const int st = k % kStages;
+          const int use = k / kStages;
+          // cvt_ready follows the converter's own wait for the page's load, so it
+          // also stands for kv_full; the S buffer must have been read out
+          if (!warp_wait(&bars->cvt_ready[st], use & 1, abort_flag) ||
+              (i > 0 && !warp_wait(&bars->s_free, (i - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = smem_u32(smem + st * kStageBytes);
+          const uint64_t kd = make_sdesc(sb, 16, 1024, SWIZZLE_128B);
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk) {
+            if (leader)
+              mma_f8_ts(t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4), idesc8,
+                        kk > 0 ? 1u : 0u);
+            __syncwarp();
+          }
+          const uint64_t rd = make_sdesc(sb + kOffCvt, 16, 1024, SWIZZLE_128B);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (leader) mma_f16_ts(t_s, tmem + kTQR + kk * 8, rd + ((kk * 32) >> 4), idesc16, 1u);
+            __syncwarp();
+          }
+          if (leader) tc_commit(&bars->s_full);
+          __syncwarp();
+          const uint32_t e = static_cast<uint32_t>(st) | ((pg == sg.lo) ? 8u : 0u);
+          pend = (pend & ~(0xFFu << (8 * (i & 3)))) | (e << (8 * (i & 3)));
+          // P.V two pages back (in this segment): its P was written before S(i - 1) was read
+          if (pg - sg.lo >= 2 && !issue_pv()) {  // j == i - 2 here
+            ok = false;
+            break;
+          }
+        }
+        ++seg;
+      }
+      while (ok && j < i) ok = issue_pv();  // the last P.Vs
+      if (leader) tc_commit(&bars->final_mma);
+      __syncwarp();
+      warp_wait(&bars->final_mma, 0, nullptr);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------- RoPE conversion, tail zeroing (64 threads) ----
+    const int t = threadIdx.x - 64;  // token row of the page
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int k = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      // the Q slots need no conversion, but their fills are waited for and
+      // acknowledged like the pages' so that each stage phase is seen in turn
+      if (t == 0) {
+        const bool filled =
+            wait_bounded(&bars->kv_full[k % kStages], (k / kStages) & 1, abort_flag, &g_status_mla) &&
+            wait_bounded(&bars->kv_full[(k + 1) % kStages], ((k + 1) / kStages) & 1, abort_flag, &g_status_mla);
+        if (filled) {
+          mbar_arrive(&bars->cvt_ready[k % kStages]);
+          mbar_arrive(&bars->cvt_ready[(k + 1) % kStages]);
+        }
+        bars->cvt_ok = filled ? 1u : 0u;
+      }
+      named_bar_sync(1, 64);
+      if (!bars->cvt_ok) break;
+      named_bar_sync(1, 64);  // cvt_ok is rewritten below
+      k += 2;
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++k) {
+        const int st = k % kStages;
+        const int use = k / kStages;
+        if (t == 0) bars->cvt_ok = wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla) ? 1u : 0u;
+        named_bar_sync(1, 64);
+        if (!bars->cvt_ok) {
+          ok = false;
+          break;
+        }
+        uint8_t* sb = smem + st * kStageBytes;
+        const bool dead = (pg == sg.n - 1) && (t >= sg.s_k - pg * kPage);  // slot past the sequence end
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        const int sw = t & 7;
+        const uint4* src = reinterpret_cast<const uint4*>(sb + kOffRope8 + t * 64);
+        uint8_t* dst = sb + kOffCvt + t * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint4 lo = z, hi = z;
+          if (!dead) {
+            const uint4 v = src[c];
+            e4m3x4_to_bf16x4(v.x, lo.x, lo.y);
+            e4m3x4_to_bf16x4(v.y, lo.z, lo.w);
+            e4m3x4_to_bf16x4(v.z, hi.x, hi.y);
+            e4m3x4_to_bf16x4(v.w, hi.z, hi.w);
+          }
+          *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
+        }
+        if (dead) {  // zero the slot's V row (all four 128-byte slices)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4* row = reinterpret_cast<uint4*>(sb + j * kLatBox + t * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) row[c] = z;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 64);
+        if (t == 0) mbar_arrive(&bars->cvt_ready[st]);
+      }
+    }
+  } else {
+    // ------------------ softmax / Q copy / epilogue (8 warps, 2 per row) ----
+    const int hf = (warp - 4) / 4;         // which half of the row
+    const int r = (warp % 4) * 32 + lane;  // query row = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    const float kv_scale = *prm.kv_scale;
+    const int R = prm.s_q * prm.h_q;
+    constexpr int kOHalf = 128;  // O columns of this thread
+    uint32_t xphase = 0;
+    auto xsync = [&]() -> bool {  // bounded, abort-aware exchange point of the 256 softmax threads
+      warp_arrive(&bars->xchg);
+      const bool ok = warp_wait(&bars->xchg, xphase & 1, abort_flag);
+      ++xphase;
+      return ok;
+    };
+    // Copies this half of the Q row of the segment whose Q slots start at ring
+    // slot kq into TMEM: latent bytes [256 hf, +256) -> columns kTQ + 64 hf..,
+    // RoPE values [32 hf, +32) -> columns kTQR + 16 hf..
+    auto copy_q = [&](int kq, int b_seq, float& qs_out) -> bool {
+      const int st = (kq + hf) % kStages, use = (kq + hf) / kStages;
+      if (!warp_wait(&bars->kv_full[st], use & 1, abort_flag)) return false;
+      const uint8_t* slot = smem + st * kStageBytes;
+      const uint4* lat = reinterpret_cast<const uint4*>(slot + r * kQLatPitch);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = lat[4 * ch + c];
+          pk[4 * c + 0] = v.x;
+          pk[4 * c + 1] = v.y;
+          pk[4 * c + 2] = v.z;
+          pk[4 * c + 3] = v.w;
+        }
+        tmem_st16(lane_base + kTQ + (4 * hf + ch) * 16, pk);
+      }
+      {
+        uint32_t pk[16];
+        const uint4* rope = reinterpret_cast<const uint4*>(slot + kQRopeOff + r * kQRopePitch);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = rope[c];
+          pk[4 * c + 0] = v.x;
+          pk[4 * c + 1] = v.y;
+          pk[4 * c + 2] = v.z;
+          pk[4 * c + 3] = v.w;
+        }
+        tmem_st16(lane_base + kTQR + 16 * hf, pk);
+      }
+      qs_out = prm.qscale[static_cast<size_t>(b_seq) * kRows + r];
+      fence_proxy_async_smem();  // the slots' next contents arrive by TMA
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(&bars->q_full);
+      return true;
+    };
+
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int i = 0, k = 0, seg = 0;
+    float qs_next = 1.f;
+    bool ok = walk.next(sg) && copy_q(0, sg.b, qs_next);
+    while (ok) {
+      const float qs = qs_next;
+      const float inv_qs = 1.0f / qs;  // a power of two: exact
+      const float c_row = prm.softmax_scale * kLog2e * qs * kv_scale;
+      SegmentWalker peek = walk;
+      Segment nx;
+      const bool has_next = peek.next(nx);
+      const int k_next = k + 2 + (sg.hi - sg.lo);
+      const uint16_t* qrow = prm.q + (static_cast<size_t>(sg.b) * R + (r < R ? r : 0)) * kD;
+      const int col0 = part * 256 + hf * kOHalf;  // this thread's O columns
+      // keys visible to this row (bottom-right causal alignment); pages wholly
+      // below every row's limit need no mask
+      const int qtok = (r < R) ? r / prm.h_q : 0;
+      const int visible = prm.causal ? (sg.s_k - prm.s_q + qtok + 1) : sg.s_k;
+      const int min_visible = prm.causal ? (sg.s_k - prm.s_q + 1) : sg.s_k;
+      float m_run = kNegInf, l_run = 0.f;  // l_run sums the stored-scale p (kPScale p)
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+        if (pg == sg.hi - 1) {  // the epilogue's LSE correction re-reads these Q columns
+          const char* qc = reinterpret_cast<const char*>(qrow + col0);
+          prefetch_l2(qc);
+          prefetch_l2(qc + 128);
+        }
+        if (!warp_wait(&bars->s_full, i & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // Both halves of the row are read: the other half only for the row max,
+        // so each warp takes the max of all 64 keys without waiting on its partner.
+        uint32_t s[32], so[32];
+        tmem_ld32(lane_base + kTS + 32 * hf, s);
+        tmem_ld32(lane_base + kTS + 32 * (1 - hf), so);
+        tmem_ld_wait();
+        tc_fence_before();
+        warp_arrive(&bars->s_free);
+
+        if (pg * kPage + kPage > min_visible) {
+          const int base = pg * kPage + 32 * hf, base_o = pg * kPage + 32 * (1 - hf);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (base + c >= visible) s[c] = __float_as_uint(kNegInf);
+            if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
+          }
+        }
+        // row max of the 64 scores as a tree (short dependency chains)
+        float m16[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          m16[c] = fmaxf(fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
+                         fmaxf(__uint_as_float(so[2 * c]), __uint_as_float(so[2 * c + 1])));
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) m16[c] = fmaxf(m16[c], m16[c + w]);
+        float mx = m16[0] * c_row;  // c_row > 0; both warps of the row get the same value
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_run + kTau) {
+          alpha = ex2_approx(m_run - mx);
+          rescale = (pg != sg.lo);
+          m_run = mx;
+        }
+        const float bias = (m_run == kNegInf) ? 0.f : (kPLog2 - m_run);
+        float sum = 0.f;
+        uint32_t pk[8];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c_row, bias));
+          const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
+          const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
+          sum += (p0 + p1) + (p2 + p3);
+          pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+        }
+        l_run = l_run * alpha + sum;
+
+        const int pb = i & 1;
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O is being accumulated by the previous page's P.V: wait for it, then rescale
+          if (!warp_wait(&bars->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+          for (int ch = 0; ch < kOHalf / 32; ++ch) {
+            const uint32_t col = kTO + hf * kOHalf + ch * 32;
+            uint32_t o[32];
+            tmem_ld32(lane_base + col, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+            tmem_st32(lane_base + col, o);
+          }
+        } else if (i >= 2) {
+          // the P buffer is free once the P.V that last read it has completed
+          if (!warp_wait(&bars->pv_done[pb], ((i - 2) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st8(lane_base + kTP + pb * kPCols + 8 * hf, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&bars->p_full[pb]);
+        // the segment's last Q.K^T is done: the next segment's Q may replace it now
+        if (pg == sg.hi - 1 && has_next && !copy_q(k_next, nx.b, qs_next)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+
+      // ---- epilogue: O is final once the segment's last P.V completes ----
+      // this thread's 128 Q values for the LSE correction (in L2 since the last
+      // page), requested before the row-sum exchange and the last P.V's wait
+      uint4 qv[16];
+      {
+        const uint4* q4e = reinterpret_cast<const uint4*>(qrow + col0);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) qv[c] = (r < R) ? __ldg(q4e + c) : make_uint4(0, 0, 0, 0);
+      }
+      bars->xsum[hf][r] = l_run;
+      if (!xsync()) break;
+      const float l_tot = (bars->xsum[0][r] + bars->xsum[1][r]) * (1.0f / kPScale);  // sum of p
+      const bool whole = (sg.lo == 0 && sg.hi == sg.n);
+      const float o_scale = kv_scale / kPScale;  // tensor-core units -> true units
+      const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
+      const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
+      if (!warp_wait(&bars->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      float dq_dot = 0.f;  // sum over this thread's columns of (q_hat - q) * O
+#pragma unroll
+      for (int ch = 0; ch < kOHalf / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = qv[4 * ch + c];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 e = q_quant_error(w[q], inv_qs, qs);
+            dq_dot += e.x * __uint_as_float(o[8 * c + 2 * q]) + e.y * __uint_as_float(o[8 * c + 2 * q + 1]);
+          }
+        }
+      }
+      // O out, 32 columns at a time.  A thread holds one row; lane groups
+      // transpose their 16-byte pieces so that each store instruction writes
+      // whole runs of a row (64 bytes of bf16, or a 128-byte line of fp32).
+      const int row0 = (warp % 4) * 32;  // first row of this warp
+#pragma unroll 1
+      for (int ch = 0; ch < kOHalf / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
+        tmem_ld_wait();
+        if (whole) {
+          uint4 pc[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            pc[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
+            pc[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
+            pc[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
+            pc[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
+          }
+          lane_group_transpose<4>(pc, lane);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int row = row0 + (lane & ~3) + kk;
+            if (row < R)
+              *reinterpret_cast<uint4*>(prm.out + (static_cast<size_t>(sg.b) * R + row) * kDV + col0 + ch * 32 +
+                                        8 * (lane & 3)) = pc[kk];
+          }
+        } else {
+          uint4 pc[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            pc[c] = make_uint4(__float_as_uint(__uint_as_float(o[4 * c]) * f),
+                               __float_as_uint(__uint_as_float(o[4 * c + 1]) * f),
+                               __float_as_uint(__uint_as_float(o[4 * c + 2]) * f),
+                               __float_as_uint(__uint_as_float(o[4 * c + 3]) * f));
+          lane_group_transpose<8>(pc, lane);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int row = row0 + (lane & ~7) + kk;
+            if (row < R)
+              *reinterpret_cast<uint4*>(prm.ws_o + (static_cast<size_t>(slot) * kRows + row) * kDV + col0 +
+                                        ch * 32 + 4 * (lane & 7)) = pc[kk];
+          }
+        }
+      }
+      if (r < R) {  // each (dv slice, row half) publishes its own share of the correction
+        const size_t row = static_cast<size_t>(sg.b) * R + r;
+        if (whole) {
+          if (part == 0 && hf == 0) prm.lse[row] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
+          prm.ws_corr[row * 4 + part * 2 + hf] = -prm.softmax_scale * dq_dot * f;
+        } else {
+          const size_t srow = static_cast<size_t>(slot) * kRows + r;
+          if (part == 0 && hf == 0) prm.ws_ml[srow] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
+          prm.ws_d[srow * 4 + part * 2 + hf] = dq_dot * f;
+        }
+      }
+      if (!has_next) break;
+      walk.next(sg);
+      k = k_next;
+      ++seg;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 template <bool kFp8>
 cudaError_t launch(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
                    cudaStream_t stream) {
   static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes<kFp8>()));
-    if (e != cudaSuccess) return e;
-    configured = true;
+  if constexpr (kFp8) {
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(f8::smem_bytes()));
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    return launch_dependent(mla_fp8_kernel, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream,
+                            tm_lat, tm_rope, prm);
+  } else {
+    if (!configured) {
+      cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem_bytes<kFp8>()));
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    return launch_dependent(mla_decode_kernel<kFp8>, dim3(num_units * Cfg<kFp8>::kParts), dim3(Cfg<kFp8>::kThreads),
+                            smem_bytes<kFp8>(), stream, tm_lat, tm_rope, prm);
   }
-  return launch_dependent(mla_decode_kernel<kFp8>, dim3(num_units * Cfg<kFp8>::kParts), dim3(Cfg<kFp8>::kThreads),
-                          smem_bytes<kFp8>(), stream, tm_lat, tm_rope, prm);
 }
 
 }  // namespace mla
@@ -872,6 +1601,11 @@ cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& 
 cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                     int num_units, cudaStream_t stream) {
   return mla::launch<false>(tm_lat, tm_rope, prm, num_units, stream);
+}
+
+cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream) {
+  if (prm.b == 0) return cudaSuccess;
+  return launch_dependent(mla::f8::mla_qprep_kernel, dim3(prm.b, mla::kRows / 32), dim3(256), 0, stream, prm);
 }
 
 uint32_t mla_read_and_clear_status() {

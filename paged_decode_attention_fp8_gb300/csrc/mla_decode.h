@@ -17,8 +17,10 @@ struct MlaParams {
   const int32_t* num_splits;   // [b + 1]
   float* ws_o;                 // [slots, 128, 512] partial accumulators (true units)
   float2* ws_ml;               // [slots, 128] (m in log2 units, l)
-  float* ws_d;                 // [slots, 128, parts<=2] sum of (q_hat - q) * O_partial per dv slice (FP8 dots)
-  float* ws_corr;              // [b, 128, 2] -softmax_scale * (q_hat - q) . out per dv slice (FP8 dots)
+  float* ws_d;                 // [slots, 128, 4] sum of (q_hat - q) * O_partial per (dv slice, row half) (FP8 dots)
+  float* ws_corr;              // [b, 128, 4] -softmax_scale * (q_hat - q) . out per (dv slice, row half) (FP8 dots)
+  uint8_t* qbuf;               // [b, 2, kMlaQSlotBytes] Q quantised for FP8 dots, in the kernel's slot layout
+  float* qscale;               // [b, 128] per-row power-of-two Q scale (FP8 dots)
   uint16_t* out;               // bf16 [b, s_q, h_q, 512]
   float* lse;                  // [b, s_q, h_q]
   float softmax_scale;
@@ -33,6 +35,8 @@ constexpr int kMlaDV = 512;
 constexpr int kMlaPage = 64;
 constexpr int kMlaD = 576;
 constexpr int kSchedFixedCost = 4;
+constexpr int kMlaCorrTerms = 4;  // LSE-correction shares per row: 2 dv slices x 2 row halves
+constexpr int kMlaQSlotBytes = 45056;  // one quantised-Q half: 128 rows x (272 latent + 80 RoPE) bytes
 constexpr size_t kMetadataMaxSmem = 200 * 1024;  // the scheduler stages ~16 bytes per sequence and unit
 size_t metadata_smem_bytes(int b, int num_units);
 
@@ -42,6 +46,9 @@ cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& 
 cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                     int num_units, cudaStream_t stream);
 uint32_t mla_read_and_clear_status();
+// Quantises every sequence's Q rows for FP8 dots into prm.qbuf / prm.qscale
+// (launched right before launch_mla_decode_fp8, as a programmatic dependent).
+cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream);
 
 // metadata + combine (metadata.cu)
 cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, int force_splits, int32_t* tile_sched,
@@ -51,9 +58,10 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
 cudaError_t launch_mla_combine(const int32_t* num_splits, const float* ws_o, const float2* ws_ml, const float* ws_d,
                                const float* ws_corr, int apply_corr, float softmax_scale, uint16_t* out, float* lse,
                                int b, int rows, cudaStream_t stream);
-// The same merge for any variant whose partial slots hold slot_rows rows of dv = 512.
+// The same merge for any variant whose partial slots hold slot_rows rows of dv = 512;
+// each row carries corr_terms LSE-correction shares (0: none).
 cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const float* ws_o, const float2* ws_ml,
-                                 const float* ws_d, const float* ws_corr, int apply_corr, float softmax_scale,
+                                 const float* ws_d, const float* ws_corr, int corr_terms, float softmax_scale,
                                  uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream);
 uint32_t metadata_read_and_clear_status();
 

@@ -1,6 +1,7 @@
 // fp8mla_decode_no_alloc: the dense MLA decode for callers that cannot
 // allocate device memory.  It needs the same scratch as fp8mla_decode (a
-// tile schedule, split counts and the per-row LSE-correction terms), but
+// tile schedule, split counts, the per-row LSE-correction terms and, for FP8
+// dots, the quantised Q with its per-row scales), but
 // takes it from a fixed array that lives in this library instead of from the
 // caller.  It schedules one work unit per sequence (no split-KV), so the
 // split partials of fp8mla_decode's workspace are never used.
@@ -19,8 +20,10 @@ namespace {
 constexpr int kNoAllocMaxBatch = FP8MLA_NO_ALLOC_MAX_BATCH;
 constexpr size_t kSchedBytes = 256 * 8 * sizeof(int32_t);                         // tile schedule, <= 256 units
 constexpr size_t kSplitsBytes = 256 * sizeof(int32_t);                            // split prefix, <= 255 sequences
-constexpr size_t kCorrBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaRows * 2 * sizeof(float);
-constexpr size_t kScratchBytes = kSchedBytes + kSplitsBytes + kCorrBytes;         // 73 KB
+constexpr size_t kCorrBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaRows * kMlaCorrTerms * sizeof(float);
+constexpr size_t kQBufBytes = static_cast<size_t>(kNoAllocMaxBatch) * 2 * kMlaQSlotBytes;    // quantised Q
+constexpr size_t kQScaleBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaRows * sizeof(float);
+constexpr size_t kScratchBytes = kSchedBytes + kSplitsBytes + kCorrBytes + kQBufBytes + kQScaleBytes;  // 5.9 MB
 static_assert(kNoAllocMaxBatch <= 255, "the split prefix holds b + 1 entries");
 
 // Held by every GPU that loads the library, for the life of the process.
@@ -97,6 +100,8 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
   int32_t* tile_sched = reinterpret_cast<int32_t*>(scratch);
   int32_t* num_splits = reinterpret_cast<int32_t*>(scratch + kSchedBytes);
   float* corr = reinterpret_cast<float*>(scratch + kSchedBytes + kSplitsBytes);
+  uint8_t* qbuf = reinterpret_cast<uint8_t*>(scratch) + kSchedBytes + kSplitsBytes + kCorrBytes;
+  float* qscale = reinterpret_cast<float*>(qbuf + kQBufBytes);
 
   CUtensorMap tm_lat, tm_rope;
   if (!encode_page_view(&tm_lat, kv_cache, num_pages, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -122,6 +127,8 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
   prm.ws_ml = nullptr;
   prm.ws_d = nullptr;
   prm.ws_corr = corr;
+  prm.qbuf = qbuf;
+  prm.qscale = qscale;
   prm.out = static_cast<uint16_t*>(out);
   prm.lse = lse;
   prm.softmax_scale = softmax_scale;
@@ -131,8 +138,10 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
   prm.b = b;
   prm.s_q = s_q;
   prm.h_q = h_q;
-  const cudaError_t e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_decode_fp8(tm_lat, tm_rope, prm, units, s)
-                                                     : launch_mla_decode_16bit(tm_lat, tm_rope, prm, units, s);
+  cudaError_t e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_qprep(prm, s) : cudaSuccess;
+  if (e == cudaSuccess)
+    e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_decode_fp8(tm_lat, tm_rope, prm, units, s)
+                                     : launch_mla_decode_16bit(tm_lat, tm_rope, prm, units, s);
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
   if (launch_mla_combine(num_splits, nullptr, nullptr, nullptr, corr, dot_mode == FP8MLA_DOT_FP8 ? 1 : 0,
                          softmax_scale, prm.out, lse, b, s_q * h_q, s) != cudaSuccess)
