@@ -96,7 +96,7 @@ MlaWorkspace mla_workspace_layout(int b, int num_units) {
   const size_t slots = static_cast<size_t>(b) + num_units;
   MlaWorkspace w;
   w.o = 0;
-  w.ml = w.o + round_up(slots * kMlaRows * kMlaDV * sizeof(float), 256);
+  w.ml = w.o + round_up(slots * kMlaRows * kMlaDV * sizeof(uint16_t), 256);
   w.d = w.ml + round_up(slots * kMlaRows * sizeof(float2), 256);
   w.corr = w.d + round_up(slots * kMlaRows * kMlaCorrTerms * sizeof(float), 256);
   w.qbuf = w.corr + round_up(static_cast<size_t>(b) * kMlaRows * kMlaCorrTerms * sizeof(float), 256);
@@ -185,7 +185,7 @@ fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dty
   prm.kv_scale = kv_scale;
   prm.tile_sched = tile_sched;
   prm.num_splits = num_splits;
-  prm.ws_o = reinterpret_cast<float*>(ws + wl.o);
+  prm.ws_o = reinterpret_cast<uint16_t*>(ws + wl.o);
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
   prm.ws_d = reinterpret_cast<float*>(ws + wl.d);
   prm.ws_corr = reinterpret_cast<float*>(ws + wl.corr);

@@ -39,6 +39,25 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
   }
 }
 
+// The same contract as wait_bounded, but polling with the non-blocking probe:
+// for waits on the critical path, where a suspended thread wakes up late.
+__device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint32_t* status) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (it > kWaitMinPolls && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (abort_flag != nullptr) *abort_flag = 1u;
+        atomicOr(status, FP8MLA_DEV_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait until a shared-memory counter (published with st_release_cta)
 // reaches target; the same abort and limit rules as wait_bounded.
 __device__ __forceinline__ bool wait_counter_bounded(const uint32_t* ctr, uint32_t target,

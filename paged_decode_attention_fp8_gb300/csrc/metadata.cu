@@ -182,43 +182,47 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
   if (tid == 0) num_splits[B] = total;
 }
 
-// Grid (sequence, 4-row block), one warp per row.  A sequence with exactly
+// Grid (sequence, 8-row block), one warp per row.  A sequence with exactly
 // one split was finished by the decode kernel: only its LSE correction (FP8
-// dots) is left.  Otherwise the lanes first compute the per-split weights
-// 2^(m_s - M) in parallel (split s on lane s % 32), then every lane
-// accumulates its 16 dv columns over the splits.
+// dots) is left.  Otherwise splits are taken 32 at a time: lane j reads split
+// j's (m, l) and correction, the round's max rescales what is accumulated so
+// far, and every lane accumulates its 16 dv columns over the round's splits.
 // Partial slots are [slot][slot_rows] rows of dv = 512; with uniform_splits > 0
 // sequence bi owns slots [bi * uniform_splits, (bi + 1) * uniform_splits).
 // corr_terms (0 = none) is the number of LSE-correction shares each row or
 // slot row carries in ws_corr / ws_d (one per producer of a piece of the row).
-__global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int uniform_splits,
-                                     const float* __restrict__ ws_o, const float2* __restrict__ ws_ml,
-                                     const float* __restrict__ ws_d, const float* __restrict__ ws_corr, int corr_terms,
-                                     float softmax_scale, uint16_t* __restrict__ out, float* __restrict__ lse, int rows,
-                                     int slot_rows) {
+template <bool kBf16>
+__global__ void __launch_bounds__(256) split_combine_kernel(
+    const int32_t* __restrict__ num_splits, int uniform_splits, const void* __restrict__ ws_o_,
+    const float2* __restrict__ ws_ml, const float* __restrict__ ws_d, const float* __restrict__ ws_corr, int corr_terms,
+    float softmax_scale, uint16_t* __restrict__ out, float* __restrict__ lse, int rows, int slot_rows) {
   griddep_wait();  // launched as a dependent of the decode kernel
   const int bi = blockIdx.x;
-  const int r = blockIdx.y * 4 + threadIdx.x / 32;
+  const int r = blockIdx.y * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (r >= rows) return;
-  const int s0 = uniform_splits > 0 ? bi * uniform_splits : num_splits[bi];
-  const int ns = uniform_splits > 0 ? uniform_splits : num_splits[bi + 1] - s0;
+  const int s0 = uniform_splits > 0 ? bi * uniform_splits : __ldg(num_splits + bi);
+  const int ns = uniform_splits > 0 ? uniform_splits : __ldg(num_splits + bi + 1) - s0;
   const size_t row = static_cast<size_t>(bi) * rows + r;
+  auto corr_sum = [&](const float* p) {  // the row's correction shares (4, 2 or 0 of them)
+    if (corr_terms == 4) {
+      const float4 c = __ldg(reinterpret_cast<const float4*>(p));
+      return (c.x + c.y) + (c.z + c.w);
+    }
+    float c = 0.f;
+    for (int t = 0; t < corr_terms; ++t) c += __ldg(p + t);
+    return c;
+  };
   if (ns == 1) {
     if (corr_terms > 0 && lane == 0) {
+      const float c = corr_sum(ws_corr + static_cast<size_t>(corr_terms) * row);
       const float l = lse[row];
-      float c = 0.f;
-      for (int t = 0; t < corr_terms; ++t) c += ws_corr[corr_terms * row + t];
       if (l != kNegInf) lse[row] = l + c;
     }
     return;
   }
   uint16_t* orow = out + row * kMlaDV + lane * 16;
-  float big_m = kNegInf;
-  for (int s = lane; s < ns; s += 32) big_m = fmaxf(big_m, ws_ml[static_cast<size_t>(s0 + s) * slot_rows + r].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, o));
-  if (ns == 0 || big_m == kNegInf) {  // no visible key: out 0, lse -inf
+  if (ns <= 0) {
     *reinterpret_cast<uint4*>(orow) = make_uint4(0, 0, 0, 0);
     *reinterpret_cast<uint4*>(orow + 8) = make_uint4(0, 0, 0, 0);
     if (lane == 0) lse[row] = kNegInf;
@@ -227,36 +231,58 @@ __global__ void split_combine_kernel(const int32_t* __restrict__ num_splits, int
   float acc[16];
 #pragma unroll
   for (int c = 0; c < 16; ++c) acc[c] = 0.f;
-  float big_l = 0.f, dq = 0.f;
+  float big_l = 0.f, dq = 0.f, big_m = kNegInf;
   for (int base = 0; base < ns; base += 32) {
-    // this round's splits: lane j holds the weight of split base + j
-    float w = 0.f;
-    if (base + lane < ns) {
-      const size_t slot = static_cast<size_t>(s0 + base + lane) * slot_rows + r;
-      const float2 ml = ws_ml[slot];
-      if (ml.x != kNegInf) {  // empty shard: the neutral element
-        w = ex2_approx(ml.x - big_m);
-        big_l += ml.y * w;
-        if (corr_terms > 0) {
-          float d = 0.f;
-          for (int t = 0; t < corr_terms; ++t) d += ws_d[corr_terms * slot + t];
-          dq += w * d;
-        }
-      }
-    }
+    // this round's splits: lane j holds split base + j's (m, l) and correction
     const int cnt = min(32, ns - base);
+    float2 ml = make_float2(kNegInf, 0.f);
+    float d = 0.f;
+    if (lane < cnt) {
+      const size_t slot = static_cast<size_t>(s0 + base + lane) * slot_rows + r;
+      ml = __ldg(ws_ml + slot);
+      if (corr_terms > 0) d = corr_sum(ws_d + static_cast<size_t>(corr_terms) * slot);
+    }
+    float m_round = ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m_round = fmaxf(m_round, __shfl_xor_sync(0xffffffffu, m_round, o));
+    if (m_round == kNegInf) continue;  // every split of this round is empty
+    // fold this round into the running (big_m, big_l, acc, dq)
+    const float m_new = fmaxf(big_m, m_round);
+    const float a_old = (big_m == kNegInf) ? 0.f : ex2_approx(big_m - m_new);
+    big_l *= a_old;
+    dq *= a_old;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) acc[c] *= a_old;
+    big_m = m_new;
+    const float w = (ml.x == kNegInf) ? 0.f : ex2_approx(ml.x - big_m);  // an empty split is the neutral element
+    big_l += ml.y * w;
+    dq += w * d;
 #pragma unroll 4
     for (int j = 0; j < cnt; ++j) {
       const float wj = __shfl_sync(0xffffffffu, w, j);
       const size_t slot = static_cast<size_t>(s0 + base + j) * slot_rows + r;
-      const float4* src = reinterpret_cast<const float4*>(ws_o + slot * kMlaDV + lane * 16);
+      if constexpr (kBf16) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(ws_o_) + slot * kMlaDV + lane * 16);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float4 v = src[c];
-        acc[4 * c + 0] += wj * v.x;
-        acc[4 * c + 1] += wj * v.y;
-        acc[4 * c + 2] += wj * v.z;
-        acc[4 * c + 3] += wj * v.w;
+        for (int c = 0; c < 2; ++c) {
+          const uint4 v = __ldg(src + c);
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[8 * c + 2 * q] += wj * bf16_lo(w4[q]);
+            acc[8 * c + 2 * q + 1] += wj * bf16_hi(w4[q]);
+          }
+        }
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(ws_o_) + slot * kMlaDV + lane * 16);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float4 v = __ldg(src + c);
+          acc[4 * c + 0] += wj * v.x;
+          acc[4 * c + 1] += wj * v.y;
+          acc[4 * c + 2] += wj * v.z;
+          acc[4 * c + 3] += wj * v.w;
+        }
       }
     }
   }
@@ -304,19 +330,23 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const float* ws_o, const float2* ws_ml,
+cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const void* ws_o, bool partials_bf16,
+                                 const float2* ws_ml,
                                  const float* ws_d, const float* ws_corr, int corr_terms, float softmax_scale,
                                  uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
-  dim3 grid(b, (rows + 3) / 4);
-  return launch_dependent(split_combine_kernel, grid, dim3(128), 0, stream, num_splits, uniform_splits, ws_o, ws_ml,
-                          ws_d, ws_corr, corr_terms, softmax_scale, out, lse, rows, slot_rows);
+  dim3 grid(b, (rows + 7) / 8);
+  if (partials_bf16)
+    return launch_dependent(split_combine_kernel<true>, grid, dim3(256), 0, stream, num_splits, uniform_splits, ws_o,
+                            ws_ml, ws_d, ws_corr, corr_terms, softmax_scale, out, lse, rows, slot_rows);
+  return launch_dependent(split_combine_kernel<false>, grid, dim3(256), 0, stream, num_splits, uniform_splits, ws_o,
+                          ws_ml, ws_d, ws_corr, corr_terms, softmax_scale, out, lse, rows, slot_rows);
 }
 
-cudaError_t launch_mla_combine(const int32_t* num_splits, const float* ws_o, const float2* ws_ml, const float* ws_d,
+cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml, const float* ws_d,
                                const float* ws_corr, int apply_corr, float softmax_scale, uint16_t* out, float* lse,
                                int b, int rows, cudaStream_t stream) {
-  return launch_split_combine(num_splits, 0, ws_o, ws_ml, ws_d, ws_corr, apply_corr ? kMlaCorrTerms : 0,
+  return launch_split_combine(num_splits, 0, ws_o, true, ws_ml, ws_d, ws_corr, apply_corr ? kMlaCorrTerms : 0,
                               softmax_scale, out, lse, b, rows, kMlaRows, stream);
 }
 

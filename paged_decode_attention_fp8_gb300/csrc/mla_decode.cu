@@ -172,6 +172,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+// warp_wait polling without suspension, for the waits on the per-page critical path
+__device__ __forceinline__ bool warp_spin(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  const bool ok = wait_spin(bar, parity, abort_flag, &g_status_mla);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Smallest e with amax <= 448 * 2^e (exact, from the float's exponent and mantissa).
 __device__ __forceinline__ int pow2_scale_exponent(float amax) {
   const uint32_t bits = __float_as_uint(amax);
@@ -813,12 +819,16 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             dst[c] = w;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(prm.ws_o + (static_cast<size_t>(slot) * kRows + r) * kDV + col0 +
-                                                  ch * 32);
+          uint4* dst = reinterpret_cast<uint4*>(prm.ws_o + (static_cast<size_t>(slot) * kRows + r) * kDV + col0 + ch * 32);
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            dst[c] = make_float4(__uint_as_float(o[4 * c]) * f, __uint_as_float(o[4 * c + 1]) * f,
-                                 __uint_as_float(o[4 * c + 2]) * f, __uint_as_float(o[4 * c + 3]) * f);
+          for (int c = 0; c < 4; ++c) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
+            dst[c] = w;
+          }
         }
       }
       if constexpr (kFp8) {
@@ -1136,7 +1146,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       // the P.V of page j, once its P is written
       auto issue_pv = [&]() -> bool {
         const int pb = j & 1;
-        if (!warp_wait(&bars->p_full[pb], (j >> 1) & 1, abort_flag)) return false;
+        if (!warp_spin(&bars->p_full[pb], (j >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t e = (pend >> (8 * (j & 3))) & 0xFFu;
         const int st = static_cast<int>(e & 7u);
@@ -1181,8 +1191,8 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           const int use = k / kStages;
           // cvt_ready follows the converter's own wait for the page's load, so it
           // also stands for kv_full; the S buffer must have been read out
-          if (!warp_wait(&bars->cvt_ready[st], use & 1, abort_flag) ||
-              (i > 0 && !warp_wait(&bars->s_free, (i - 1) & 1, abort_flag))) {
+          if (!warp_spin(&bars->cvt_ready[st], use & 1, abort_flag) ||
+              (i > 0 && !warp_spin(&bars->s_free, (i - 1) & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -1368,7 +1378,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           prefetch_l2(qc);
           prefetch_l2(qc + 128);
         }
-        if (!warp_wait(&bars->s_full, i & 1, abort_flag)) {
+        if (!warp_spin(&bars->s_full, i & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -1443,7 +1453,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           }
         } else if (i >= 2) {
           // the P buffer is free once the P.V that last read it has completed
-          if (!warp_wait(&bars->pv_done[pb], ((i - 2) >> 1) & 1, abort_flag)) {
+          if (!warp_spin(&bars->pv_done[pb], ((i - 2) >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -1496,48 +1506,33 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           }
         }
       }
-      // O out, 32 columns at a time.  A thread holds one row; lane groups
-      // transpose their 16-byte pieces so that each store instruction writes
-      // whole runs of a row (64 bytes of bf16, or a 128-byte line of fp32).
+      // O out as bf16, 32 columns at a time.  A thread holds one row; groups
+      // of four lanes transpose their 16-byte pieces so that each store
+      // instruction writes 64-byte runs of rows.
       const int row0 = (warp % 4) * 32;  // first row of this warp
 #pragma unroll 1
       for (int ch = 0; ch < kOHalf / 32; ++ch) {
         uint32_t o[32];
         tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
         tmem_ld_wait();
-        if (whole) {
-          uint4 pc[4];
+        uint4 pc[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            pc[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
-            pc[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
-            pc[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
-            pc[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
-          }
-          lane_group_transpose<4>(pc, lane);
+        for (int c = 0; c < 4; ++c) {
+          pc[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
+          pc[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
+          pc[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
+          pc[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
+        }
+        lane_group_transpose<4>(pc, lane);
+        // a whole sequence goes straight to out; a piece to its bf16 partial slot
+        uint16_t* base = whole ? prm.out + static_cast<size_t>(sg.b) * R * kDV
+                               : prm.ws_o + static_cast<size_t>(slot) * kRows * kDV;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int row = row0 + (lane & ~3) + kk;
-            if (row < R)
-              *reinterpret_cast<uint4*>(prm.out + (static_cast<size_t>(sg.b) * R + row) * kDV + col0 + ch * 32 +
-                                        8 * (lane & 3)) = pc[kk];
-          }
-        } else {
-          uint4 pc[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            pc[c] = make_uint4(__float_as_uint(__uint_as_float(o[4 * c]) * f),
-                               __float_as_uint(__uint_as_float(o[4 * c + 1]) * f),
-                               __float_as_uint(__uint_as_float(o[4 * c + 2]) * f),
-                               __float_as_uint(__uint_as_float(o[4 * c + 3]) * f));
-          lane_group_transpose<8>(pc, lane);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const int row = row0 + (lane & ~7) + kk;
-            if (row < R)
-              *reinterpret_cast<uint4*>(prm.ws_o + (static_cast<size_t>(slot) * kRows + row) * kDV + col0 +
-                                        ch * 32 + 4 * (lane & 7)) = pc[kk];
-          }
+        for (int kk = 0; kk < 4; ++kk) {
+          const int row = row0 + (lane & ~3) + kk;
+          if (row < R)
+            *reinterpret_cast<uint4*>(base + static_cast<size_t>(row) * kDV + col0 + ch * 32 + 8 * (lane & 3)) =
+                pc[kk];
         }
       }
       if (r < R) {  // each (dv slice, row half) publishes its own share of the correction

@@ -15,7 +15,7 @@ struct MlaParams {
   const float* kv_scale;       // [1]
   const int32_t* tile_sched;   // [num_units, 8]
   const int32_t* num_splits;   // [b + 1]
-  float* ws_o;                 // [slots, 128, 512] partial accumulators (true units)
+  uint16_t* ws_o;              // [slots, 128, 512] partial accumulators as bf16 (true units)
   float2* ws_ml;               // [slots, 128] (m in log2 units, l)
   float* ws_d;                 // [slots, 128, 4] sum of (q_hat - q) * O_partial per (dv slice, row half) (FP8 dots)
   float* ws_corr;              // [b, 128, 4] -softmax_scale * (q_hat - q) . out per (dv slice, row half) (FP8 dots)
@@ -55,12 +55,14 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
                                 int32_t* num_splits, cudaStream_t stream);
 // Merges split partials into out / lse, and (FP8 dots, apply_corr) applies the
 // first-order Q-quantisation correction to every row's LSE.
-cudaError_t launch_mla_combine(const int32_t* num_splits, const float* ws_o, const float2* ws_ml, const float* ws_d,
+cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml, const float* ws_d,
                                const float* ws_corr, int apply_corr, float softmax_scale, uint16_t* out, float* lse,
                                int b, int rows, cudaStream_t stream);
-// The same merge for any variant whose partial slots hold slot_rows rows of dv = 512;
-// each row carries corr_terms LSE-correction shares (0: none).
-cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const float* ws_o, const float2* ws_ml,
+// The same merge for any variant whose partial slots hold slot_rows rows of dv = 512
+// (fp32, or bf16 when partials_bf16); each row carries corr_terms LSE-correction
+// shares (0: none).
+cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const void* ws_o, bool partials_bf16,
+                                 const float2* ws_ml,
                                  const float* ws_d, const float* ws_corr, int corr_terms, float softmax_scale,
                                  uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream);
 uint32_t metadata_read_and_clear_status();
