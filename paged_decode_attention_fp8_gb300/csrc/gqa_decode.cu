@@ -9,18 +9,22 @@
 //
 // GB300 design (swap-AB, one CTA per (sequence, KV head, split)):
 //   * 128 tokens (8 pages of 16) per step; each page's K and V tile
-//     [16 tokens x 128 B] arrives by one TMA each (128-byte swizzle).
-//   * 16-bit dots: converter threads turn the E4M3 tiles into f16 (exact)
-//     in 128-byte-swizzled tiles; Q (the head group, <= 16 heads) is f16
-//     with a per-head power-of-two scale.
-//   * S^T = K Q^T: M = 128 tokens, N = 16, K = 128 (8 f16 MMAs); softmax
-//     across TMEM lanes (per-head max by shuffles + a 4-warp exchange; each
-//     thread keeps partial sums), P^T (f16) to shared memory, then
-//     O^T = V^T P^T with V^T read MN-major straight from the converted tile.
-//   * Split-KV over the token dimension with a combine kernel; the split
-//     count follows the FA2-style "waves" rule: none while the grid already
-//     fills the GPU, else the smallest count within 85% of the best wave
-//     efficiency (InfiniCore page, Summary: the "auto" heuristic).
+//     [16 tokens x 128 B] arrives by one TMA each (128-byte swizzle) into a
+//     ring of four raw stages, so that several steps are in flight from HBM.
+//   * 16-bit dots: four converter warps turn each step into f16 (exact):
+//     token r's K row goes straight into TMEM lane r, the A operand of
+//     Q.K^T, and its V row into one of two f16 V slots in shared memory;
+//     Q (the head group, <= 16 heads) is f16 with a per-head power-of-two scale.
+//   * S^T = K Q^T: M = 128 tokens, N = 16, K = 128 (8 f16 MMAs, A from
+//     TMEM); softmax across TMEM lanes (per-head max by shuffles + a 4-warp
+//     exchange; each thread keeps partial sums), P^T (f16) to shared memory,
+//     then O^T = V^T P^T with V^T read MN-major from the f16 V slot.  S and P
+//     are double-buffered; a converged warp issues the MMAs (one elected lane).
+//   * Split-KV over the token dimension with a combine kernel; for small
+//     grids the split count follows the FA2-style "waves" rule, the smallest
+//     count within 85% of the best wave efficiency (InfiniCore page,
+//     Summary: the "auto" heuristic); a grid that already fills the GPU is
+//     still cut into about six CTAs per SM so unequal contexts balance.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -43,16 +47,18 @@ constexpr int kPage = 16;
 constexpr int kTok = 128;               // tokens per step (MMA M)
 constexpr int kPagesPerStep = kTok / kPage;
 constexpr int kN = 16;                  // head group, padded (MMA N)
-constexpr int kThreads = 256;
-constexpr int kStages = 2;
+constexpr int kThreads = 384;           // producer, MMA, 2 idle, 4 softmax, 4 converter warps
+constexpr int kRawStages = 4;           // E4M3 K and V of a step, in flight from HBM
+constexpr int kV16Slots = 2;            // f16 V of a step, from conversion until its P.V
 constexpr int kRawTile = kTok * kHd;    // 16 KB of E4M3 per operand per step
 constexpr int kCvtAtom = kTok * 128;    // one 64-dim f16 atom (16 KB)
-constexpr int kOffRawK = 0, kOffRawV = kRawTile, kOffK16 = 2 * kRawTile, kOffV16 = kOffK16 + 2 * kCvtAtom;
-constexpr int kStageBytes = kOffV16 + 2 * kCvtAtom;   // 96 KB
+constexpr int kOffRawK = 0, kOffRawV = kRawTile, kRawStageBytes = 2 * kRawTile;   // 32 KB
+constexpr int kV16Bytes = 2 * kCvtAtom;                                            // 32 KB
 constexpr int kQBytes = 2 * kN * 128;
-constexpr int kPBytes = 2 * kN * 128;
+constexpr int kPBytes = 2 * kN * 128;   // one P^T buffer (two are kept)
 constexpr float kTau = 8.0f;
-constexpr uint32_t kTmemCols = 32, kTS = 0, kTO = 16;
+// TMEM: S (two buffers of 16 columns), O (16), K of a step as f16 (two slots of 64)
+constexpr uint32_t kTmemCols = 256, kTS = 0, kTO = 32, kTK = 64;
 
 struct Params {
   const uint16_t* q;           // bf16 [bs, h_q, 128]
@@ -69,15 +75,18 @@ struct Params {
 };
 
 struct Smem {
-  uint64_t kv_full[kStages], kv_empty[kStages], cvt_ready[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma, xchg;
-  uint32_t tmem_base, abort_flag, prod_ok;
+  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+  uint64_t cvt_ready[kV16Slots], k16_empty[kV16Slots], v16_empty[kV16Slots];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];  // by step parity
+  uint64_t q_full, final_mma, xchg;
+  uint32_t tmem_base, abort_flag;
   float qs[kN];
   float red[2][4][kN];   // per-warp partial maxima, double-buffered by step parity
   float red2[4][kN];
 };
 
-constexpr size_t kSmemBytes = kStages * kStageBytes + kQBytes + kPBytes + sizeof(Smem) + 1024;
+constexpr size_t kSmemBytes =
+    kRawStages * kRawStageBytes + kV16Slots * kV16Bytes + kQBytes + 2 * kPBytes + sizeof(Smem) + 1024;
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
   const bool ok = wait_bounded(bar, parity, abort_flag, &g_status_gqa);
@@ -105,9 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* q_tile = smem + kStages * kStageBytes;
+  uint8_t* v16 = smem + kRawStages * kRawStageBytes;    // f16 V slots
+  uint8_t* q_tile = v16 + kV16Slots * kV16Bytes;
   uint8_t* p_tile = q_tile + kQBytes;
-  Smem* sm = reinterpret_cast<Smem*>(p_tile + kPBytes);
+  Smem* sm = reinterpret_cast<Smem*>(p_tile + 2 * kPBytes);
   volatile uint32_t* abort_flag = &sm->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -130,15 +140,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nsteps = st1 - st0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm->kv_full[s], 1);
-      mbar_init(&sm->kv_empty[s], 1);
-      mbar_init(&sm->cvt_ready[s], 4);
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(&sm->raw_full[s], 1);
+      mbar_init(&sm->raw_empty[s], 4);  // one arrival per converter warp
     }
-    mbar_init(&sm->s_full, 1);
-    mbar_init(&sm->s_free, 4);
-    mbar_init(&sm->p_full, 4);
-    mbar_init(&sm->pv_done, 1);
+    for (int s = 0; s < kV16Slots; ++s) {
+      mbar_init(&sm->cvt_ready[s], 4);
+      mbar_init(&sm->k16_empty[s], 1);
+      mbar_init(&sm->v16_empty[s], 1);
+    }
+    for (int bf = 0; bf < 2; ++bf) {
+      mbar_init(&sm->s_full[bf], 1);
+      mbar_init(&sm->s_free[bf], 4);
+      mbar_init(&sm->p_full[bf], 4);
+      mbar_init(&sm->pv_done[bf], 1);
+    }
     mbar_init(&sm->q_full, 4);
     mbar_init(&sm->final_mma, 1);
     mbar_init(&sm->xchg, 4);
@@ -165,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int i = 0;
     for (; i < nsteps; ++i) {
-      const int st = i % kStages, use = i / kStages;
+      const int st = i % kRawStages, use = i / kRawStages;
       const int p0 = (st0 + i) * kPagesPerStep;
       const int np = min(kPagesPerStep, n_pages - p0);
       int mine = 0;
@@ -181,69 +197,149 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int p = 0; p < kPagesPerStep; ++p) rows[p] = (__shfl_sync(0xffffffffu, mine, p) * prm.h_kv + kvh) * kPage;
       bool ok = true;
       if (lane == 0) {
-        ok = use == 0 || wait_bounded(&sm->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa);
+        ok = use == 0 || wait_bounded(&sm->raw_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa);
         if (ok) {
-          mbar_arrive_expect_tx(&sm->kv_full[st], 2u * np * kPage * kHd);
-          uint8_t* sb = smem + st * kStageBytes;
+          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd);
+          uint8_t* sb = smem + st * kRawStageBytes;
 #pragma unroll
           for (int p = 0; p < kPagesPerStep; ++p) {
             if (p >= np) break;
-            tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->kv_full[st], 0, rows[p], 0);
-            tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->kv_full[st], 0, rows[p], 0);
+            tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->raw_full[st], 0, rows[p], 0);
+            tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->raw_full[st], 0, rows[p], 0);
           }
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
     }
     if (lane == 0)
-      for (int j = max(0, i - kStages); j < i; ++j)
-        wait_bounded(&sm->kv_full[j % kStages], (j / kStages) & 1, nullptr, &g_status_gqa);
+      for (int j = max(0, i - kRawStages); j < i; ++j)
+        wait_bounded(&sm->raw_full[j % kRawStages], (j / kRawStages) & 1, nullptr, &g_status_gqa);
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, kN, 128);  // f16: K (K-major) x Q (K-major)
+    // The whole warp runs the loop and one elected lane issues.  Q.K^T reads
+    // the step's K from TMEM (f16, written there by the converter warps);
+    // P.V reads V^T from the step's f16 slot in shared memory.  S and P are
+    // double-buffered, so Q.K^T of step i runs while the softmax warps work
+    // on step i - 1.
+    {
+      constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, kN, 128);  // f16: K (TMEM) x Q (K-major)
       constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, 0, kN, 128);  // f16: V^T (MN-major) x P^T (K-major)
-      const uint32_t qb = smem_u32(q_tile), pb = smem_u32(p_tile);
-      bool ok = wait_bounded(&sm->q_full, 0, abort_flag, &g_status_gqa);
+      const bool leader = elect_one();
+      const uint32_t qb = smem_u32(q_tile);
+      bool ok = warp_wait(&sm->q_full, 0, abort_flag);
       auto issue_pv = [&](int j) -> bool {
-        if (!wait_bounded(&sm->p_full, j & 1, abort_flag, &g_status_gqa)) return false;
+        const int bf = j & 1, vs = j % kV16Slots;
+        if (!warp_wait(&sm->p_full[bf], (j >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
-        const int st = j % kStages;
-        const uint32_t vb = smem_u32(smem + st * kStageBytes + kOffV16);
+        const uint32_t vb = smem_u32(v16 + vs * kV16Bytes);
+        const uint32_t pb = smem_u32(p_tile + bf * kPBytes);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ss(tmem + kTO, make_sdesc(vb + kk * 2048, kCvtAtom, 1024, SWIZZLE_128B),
-                     make_sdesc(pb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_pv,
-                     (j == 0 && kk == 0) ? 0u : 1u);
-        tc_commit(&sm->pv_done);
-        tc_commit(&sm->kv_empty[st]);
+        for (int kk = 0; kk < 8; ++kk) {
+          if (leader)
+            mma_f16_ss(tmem + kTO, make_sdesc(vb + kk * 2048, kCvtAtom, 1024, SWIZZLE_128B),
+                       make_sdesc(pb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_pv,
+                       (j == 0 && kk == 0) ? 0u : 1u);
+          __syncwarp();
+        }
+        if (leader) {
+          tc_commit(&sm->pv_done[bf]);
+          tc_commit(&sm->v16_empty[vs]);
+        }
+        __syncwarp();
         return true;
       };
       for (int i = 0; ok && i < nsteps; ++i) {
-        const int st = i % kStages, use = i / kStages;
-        if (!wait_bounded(&sm->cvt_ready[st], use & 1, abort_flag, &g_status_gqa) ||
-            (i > 0 && !wait_bounded(&sm->s_free, (i - 1) & 1, abort_flag, &g_status_gqa))) {
+        const int ks = i % kV16Slots, bf = i & 1;
+        if (!warp_wait(&sm->cvt_ready[ks], (i / kV16Slots) & 1, abort_flag) ||
+            (i >= 2 && !warp_wait(&sm->s_free[bf], ((i - 2) >> 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t kb = smem_u32(smem + st * kStageBytes + kOffK16);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ss(tmem + kTS, make_sdesc(kb + (kk >> 2) * kCvtAtom + (kk & 3) * 32, 16, 1024, SWIZZLE_128B),
-                     make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
-                     kk > 0 ? 1u : 0u);
-        tc_commit(&sm->s_full);
+        for (int kk = 0; kk < 8; ++kk) {
+          if (leader)
+            mma_f16_ts(tmem + kTS + bf * kN, tmem + kTK + ks * 64 + kk * 8,
+                       make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
+                       kk > 0 ? 1u : 0u);
+          __syncwarp();
+        }
+        if (leader) {
+          tc_commit(&sm->s_full[bf]);
+          tc_commit(&sm->k16_empty[ks]);
+        }
+        __syncwarp();
         if (i > 0 && !issue_pv(i - 1)) ok = false;
       }
       if (ok && nsteps > 0) issue_pv(nsteps - 1);
-      tc_commit(&sm->final_mma);
-      wait_bounded(&sm->final_mma, 0, nullptr, &g_status_gqa);
+      if (leader) tc_commit(&sm->final_mma);
+      __syncwarp();
+      warp_wait(&sm->final_mma, 0, nullptr);
     }
-    __syncwarp();
+  } else if (warp >= 8) {
+    // ------------------------- K / V conversion to f16 (one token row each) ----
+    // Token r's K row goes to TMEM lane r (the A operand of Q.K^T), its V row
+    // to the step's f16 V slot (128-byte swizzle, read MN-major by P.V).
+    const int r = threadIdx.x - 256;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
+    for (int i = 0; i < nsteps; ++i) {
+      const int st = i % kRawStages, use = i / kRawStages, vs = i % kV16Slots;
+      const bool live = (st0 + i) * kTok + r < s_k;
+      if (!warp_wait(&sm->raw_full[st], use & 1, abort_flag)) break;
+      const uint8_t* sb = smem + st * kRawStageBytes;
+      const int sw = r & 7;
+      uint4 kraw[8], vraw[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        kraw[c] = live ? *reinterpret_cast<const uint4*>(sb + kOffRawK + r * 128 + ((c ^ sw) << 4))
+                       : make_uint4(0, 0, 0, 0);
+        vraw[c] = live ? *reinterpret_cast<const uint4*>(sb + kOffRawV + r * 128 + ((c ^ sw) << 4))
+                       : make_uint4(0, 0, 0, 0);
+      }
+      warp_arrive(&sm->raw_empty[st]);  // the raw stage may be refilled
+      // the K slot and the V slot of this step were last read two steps ago
+      if (i >= kV16Slots && (!warp_wait(&sm->k16_empty[vs], ((i - kV16Slots) / kV16Slots) & 1, abort_flag) ||
+                             !warp_wait(&sm->v16_empty[vs], ((i - kV16Slots) / kV16Slots) & 1, abort_flag)))
+        break;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // K: dims [64 half, 64 half + 64) -> 32 columns of f16 pairs
+        uint32_t kc[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 x = kraw[4 * half + c];
+          kc[8 * c + 0] = f16x2_of_e4m3x2(x.x & 0xFFFFu);
+          kc[8 * c + 1] = f16x2_of_e4m3x2(x.x >> 16);
+          kc[8 * c + 2] = f16x2_of_e4m3x2(x.y & 0xFFFFu);
+          kc[8 * c + 3] = f16x2_of_e4m3x2(x.y >> 16);
+          kc[8 * c + 4] = f16x2_of_e4m3x2(x.z & 0xFFFFu);
+          kc[8 * c + 5] = f16x2_of_e4m3x2(x.z >> 16);
+          kc[8 * c + 6] = f16x2_of_e4m3x2(x.w & 0xFFFFu);
+          kc[8 * c + 7] = f16x2_of_e4m3x2(x.w >> 16);
+        }
+        tmem_st32(lane_base + kTK + vs * 64 + half * 32, kc);
+      }
+      uint8_t* vslot = v16 + vs * kV16Bytes;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {   // V: 16 E4M3 -> 16 f16 (two 16-byte chunks)
+        const uint4 x = vraw[c];
+        const uint4 vo = make_uint4(f16x2_of_e4m3x2(x.x & 0xFFFFu), f16x2_of_e4m3x2(x.x >> 16),
+                                    f16x2_of_e4m3x2(x.y & 0xFFFFu), f16x2_of_e4m3x2(x.y >> 16));
+        const uint4 vo2 = make_uint4(f16x2_of_e4m3x2(x.z & 0xFFFFu), f16x2_of_e4m3x2(x.z >> 16),
+                                     f16x2_of_e4m3x2(x.w & 0xFFFFu), f16x2_of_e4m3x2(x.w >> 16));
+        // dims [16 c, 16 c + 16): f16 atom c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1
+        uint8_t* dv = vslot + (c / 4) * kCvtAtom + r * 128;
+        *reinterpret_cast<uint4*>(dv + (((2 * (c % 4)) ^ sw) << 4)) = vo;
+        *reinterpret_cast<uint4*>(dv + (((2 * (c % 4) + 1) ^ sw) << 4)) = vo2;
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      warp_arrive(&sm->cvt_ready[vs]);  // one arrival per converting warp
+    }
   } else if (warp >= 4) {
-    // ------------------------ Q prep, conversion, softmax, epilogue ----
+    // ------------------------------- Q prep, softmax, epilogue ----
     const int r = threadIdx.x - 128;   // token row of a step / TMEM lane / output dim
     const int w = warp - 4;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(w * 32) << 16);
@@ -286,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       warp_arrive(&sm->q_full);
     }
-    for (int i = r; i < kPBytes / 16; i += 128) reinterpret_cast<uint4*>(p_tile)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = r; i < 2 * kPBytes / 16; i += 128) reinterpret_cast<uint4*>(p_tile)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     bool ok = xsync();  // qs[] and the zeroed P tile complete
     float c_h[kG], m_h[kG], l_h[kG];
@@ -297,56 +393,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_h[h] = 0.f;
     }
     for (int i = 0; ok && i < nsteps; ++i) {
-      const int st = i % kStages, use = i / kStages;
+      const int bf = i & 1;
       const int tok = (st0 + i) * kTok + r;
       const bool live = tok < s_k;
-      // ---- convert K and V rows of token r to f16 ----
-      if (!warp_wait(&sm->kv_full[st], use & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      uint8_t* sb = smem + st * kStageBytes;
-      {
-        const int sw = r & 7;
-        const uint8_t* srck = sb + kOffRawK + r * 128;
-        const uint8_t* srcv = sb + kOffRawV + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {   // 16 E4M3 -> 16 f16 (two 16-byte chunks)
-          uint4 ko = make_uint4(0, 0, 0, 0), ko2 = ko, vo = ko, vo2 = ko;
-          if (live) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(srck + ((c ^ sw) << 4));
-            const uint4 vv = *reinterpret_cast<const uint4*>(srcv + ((c ^ sw) << 4));
-            ko = make_uint4(f16x2_of_e4m3x2(kv.x & 0xFFFFu), f16x2_of_e4m3x2(kv.x >> 16), f16x2_of_e4m3x2(kv.y & 0xFFFFu),
-                            f16x2_of_e4m3x2(kv.y >> 16));
-            ko2 = make_uint4(f16x2_of_e4m3x2(kv.z & 0xFFFFu), f16x2_of_e4m3x2(kv.z >> 16),
-                             f16x2_of_e4m3x2(kv.w & 0xFFFFu), f16x2_of_e4m3x2(kv.w >> 16));
-            vo = make_uint4(f16x2_of_e4m3x2(vv.x & 0xFFFFu), f16x2_of_e4m3x2(vv.x >> 16), f16x2_of_e4m3x2(vv.y & 0xFFFFu),
-                            f16x2_of_e4m3x2(vv.y >> 16));
-            vo2 = make_uint4(f16x2_of_e4m3x2(vv.z & 0xFFFFu), f16x2_of_e4m3x2(vv.z >> 16),
-                             f16x2_of_e4m3x2(vv.w & 0xFFFFu), f16x2_of_e4m3x2(vv.w >> 16));
-          }
-          // dims [16 c, 16 c + 16): f16 atom c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1
-          uint8_t* dk = sb + kOffK16 + (c / 4) * kCvtAtom + r * 128;
-          uint8_t* dv = sb + kOffV16 + (c / 4) * kCvtAtom + r * 128;
-          *reinterpret_cast<uint4*>(dk + (((2 * (c % 4)) ^ sw) << 4)) = ko;
-          *reinterpret_cast<uint4*>(dk + (((2 * (c % 4) + 1) ^ sw) << 4)) = ko2;
-          *reinterpret_cast<uint4*>(dv + (((2 * (c % 4)) ^ sw) << 4)) = vo;
-          *reinterpret_cast<uint4*>(dv + (((2 * (c % 4) + 1) ^ sw) << 4)) = vo2;
-        }
-        fence_proxy_async_smem();
-        warp_arrive(&sm->cvt_ready[st]);  // one arrival per converting warp
-      }
       // ---- softmax over this step's tokens ----
-      if (!warp_wait(&sm->s_full, i & 1, abort_flag)) {
+      if (!warp_wait(&sm->s_full[bf], (i >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t s[kN];
-      tmem_ld16(lane_base + kTS, s);
+      tmem_ld16(lane_base + kTS + bf * kN, s);
       tmem_ld_wait();
       tc_fence_before();
-      warp_arrive(&sm->s_free);
+      warp_arrive(&sm->s_free[bf]);
       float v[kG];
 #pragma unroll
       for (int h = 0; h < kG; ++h) v[h] = live ? __uint_as_float(s[h]) * c_h[h] : kNegInf;
@@ -383,7 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_h[h + 1] = l_h[h + 1] * alpha[h + 1] + p1;
         ph[h / 2] = pack_f16x2(p0, p1);
       }
-      if (i > 0 && !warp_wait(&sm->pv_done, (i - 1) & 1, abort_flag)) {
+      // O is rescaled only after the previous step's P.V; the P buffer is
+      // rewritten only after the P.V that read it two steps ago
+      if (any_rescale) {
+        if (!warp_wait(&sm->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+      } else if (i >= 2 && !warp_wait(&sm->pv_done[bf], ((i - 2) >> 1) & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -403,18 +470,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < kG; ++h) {
           const uint16_t val = static_cast<uint16_t>((h & 1) ? (ph[h / 2] >> 16) : (ph[h / 2] & 0xFFFFu));
-          *reinterpret_cast<uint16_t*>(p_tile + a * (kN * 128) + (h / 8) * 1024 + (h % 8) * 128 +
+          *reinterpret_cast<uint16_t*>(p_tile + bf * kPBytes + a * (kN * 128) + (h / 8) * 1024 + (h % 8) * 128 +
                                        ((ch ^ (h % 8)) << 4) + el * 2) = val;
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      warp_arrive(&sm->p_full);
+      warp_arrive(&sm->p_full[bf]);
     }
 
     const bool whole = prm.splits == 1;
     const size_t slot = static_cast<size_t>(seq) * prm.splits + split;
-    if (ok && nsteps > 0 && warp_wait(&sm->pv_done, (nsteps - 1) & 1, abort_flag)) {
+    if (ok && nsteps > 0 && warp_wait(&sm->pv_done[(nsteps - 1) & 1], ((nsteps - 1) >> 1) & 1, abort_flag)) {
       tc_fence_after();
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
@@ -539,7 +606,14 @@ int gqa_choose_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_spl
   const int max_steps = std::max(1, (max_seqlen + gqa::kTok - 1) / gqa::kTok);
   if (num_splits > 0) return std::max(1, std::min(num_splits, max_steps));
   const long long ctas = static_cast<long long>(std::max(bs, 1)) * std::max(h_kv, 1);
-  if (num_sms < 1 || ctas * 5 >= static_cast<long long>(num_sms) * 4) return 1;  // grid already ~fills the GPU
+  if (num_sms < 1) return 1;
+  if (ctas * 5 >= static_cast<long long>(num_sms) * 4) {
+    // The grid already fills the GPU, but contexts of unequal length leave the
+    // last wave ragged: cut every sequence into a few pieces (about six CTAs
+    // per SM, each of at least 8 steps) so the hardware scheduler can balance.
+    const long long want = (6LL * num_sms + ctas - 1) / ctas;
+    return static_cast<int>(std::max(1LL, std::min({want, 16LL, static_cast<long long>(max_steps / 8)})));
+  }
   const int cap = std::min(16, max_steps);
   double eff[17] = {0}, best = 0;
   for (int s = 1; s <= cap; ++s) {

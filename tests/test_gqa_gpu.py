@@ -68,9 +68,11 @@ def test_ragged_lengths_and_groups(group):
 
 
 def test_auto_split_rule():
-    # large grids take no split; a lone sequence is split to fill the GPU
+    # a full grid is cut into about six CTAs per SM (pieces of >= 8 steps);
+    # a lone sequence is split to fill the GPU
     sms = fm.num_sms()
-    assert fm.gqa_num_splits(32, 8, 16384) == 1
+    assert fm.gqa_num_splits(32, 8, 16384) == min(16, -(-6 * sms // 256))
+    assert fm.gqa_num_splits(256, 8, 1024) == 1   # pieces would be shorter than 8 steps
     assert fm.gqa_num_splits(1, 8, 16384) > 1
     assert fm.gqa_num_splits(1, 8, 16384, num_splits=4) == 4
     assert fm.gqa_num_splits(1, 8, 256, num_splits=8) == 2   # capped at the 128-token steps present
