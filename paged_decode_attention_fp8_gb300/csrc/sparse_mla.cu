@@ -179,48 +179,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform descriptors) and one elected
+    // lane issues: from a lone thread each MMA costs about twice as long.
+    {
       constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, kN, 128);   // K (K-major) x Q (K-major)
       constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, 0, kN, 128);   // V^T (MN-major) x P^T (K-major)
+      const bool leader = elect_one();
       const uint32_t qb = smem_u32(q_tile), pb = smem_u32(p_tile);
-      bool ok = wait_bounded(&sm->q_full, 0, abort_flag, &g_status_sparse);
+      bool ok = warp_wait(&sm->q_full, 0, abort_flag);
       auto issue_pv = [&](int j) -> bool {
-        if (!wait_bounded(&sm->p_full, j & 1, abort_flag, &g_status_sparse)) return false;
+        if (!warp_wait(&sm->p_full, j & 1, abort_flag)) return false;
         tc_fence_after();
         const int st = j % kStages;
         const uint32_t sb = smem_u32(smem + st * kStageBytes);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ss(tmem + kTO + mt * kN, make_sdesc(sb + mt * kAtom + kk * 4096, kAtom, 1024, SWIZZLE_128B),
-                      make_sdesc(pb + kk * 32, 16, 1024, SWIZZLE_128B), idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
-        tc_commit(&sm->pv_done);
-        tc_commit(&sm->kv_empty[st]);
+          for (int kk = 0; kk < 4; ++kk) {
+            if (leader)
+              mma_f8_ss(tmem + kTO + mt * kN, make_sdesc(sb + mt * kAtom + kk * 4096, kAtom, 1024, SWIZZLE_128B),
+                        make_sdesc(pb + kk * 32, 16, 1024, SWIZZLE_128B), idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
+            __syncwarp();
+          }
+        if (leader) {
+          tc_commit(&sm->pv_done);
+          tc_commit(&sm->kv_empty[st]);
+        }
+        __syncwarp();
         return true;
       };
       for (int i = 0; ok && i < nchunks; ++i) {
         const int st = i % kStages, use = i / kStages;
-        if (!wait_bounded(&sm->kv_full[st], use & 1, abort_flag, &g_status_sparse) ||
-            (i > 0 && !wait_bounded(&sm->s_free, (i - 1) & 1, abort_flag, &g_status_sparse))) {
+        if (!warp_wait(&sm->kv_full[st], use & 1, abort_flag) ||
+            (i > 0 && !warp_wait(&sm->s_free, (i - 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t sb = smem_u32(smem + st * kStageBytes);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          mma_f8_ss(tmem + kTS, make_sdesc(sb + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024, SWIZZLE_128B),
-                    make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
-                    kk > 0 ? 1u : 0u);
-        tc_commit(&sm->s_full);
+        for (int kk = 0; kk < 16; ++kk) {
+          if (leader)
+            mma_f8_ss(tmem + kTS, make_sdesc(sb + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024, SWIZZLE_128B),
+                      make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
+                      kk > 0 ? 1u : 0u);
+          __syncwarp();
+        }
+        if (leader) tc_commit(&sm->s_full);
+        __syncwarp();
         if (i > 0 && !issue_pv(i - 1)) ok = false;
       }
       if (ok && nchunks > 0) issue_pv(nchunks - 1);
-      tc_commit(&sm->final_mma);
-      wait_bounded(&sm->final_mma, 0, nullptr, &g_status_sparse);
+      if (leader) tc_commit(&sm->final_mma);
+      __syncwarp();
+      warp_wait(&sm->final_mma, 0, nullptr);
     }
-    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------- Q prep, softmax, epilogue (128) ----
     const int r = threadIdx.x - 128;
