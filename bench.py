@@ -253,7 +253,7 @@ def run_ours(args):
     roofline = dict(bound="hbm" if t_hbm >= t_tensor else "tensor", achieved=round(achieved, 1),
                     peak=peaks["hbm"], unit="GB/s", frac=round(achieved / peaks["hbm"], 4),
                     traffic=traffic_from_profile(),
-                    kernel="fp8mla_decode (decode + combine kernels)",
+                    kernel="fp8mla_decode (Q quantisation + decode + combine kernels)",
                     algorithmic_bytes_per_launch=nbytes,
                     t_hbm_us=round(t_hbm * 1e6, 2), t_tensor_us=round(t_tensor * 1e6, 2),
                     roofline_frac_of_time=round(max(t_hbm, t_tensor) / (dec_avg_ms * 1e-3), 4),
@@ -283,7 +283,8 @@ def run_ours(args):
         "roofline": roofline,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        # per step: schedule, (FP8 dots: Q quantisation,) decode, combine
+        "gpu_launches": (4 if dot == "fp8" else 3) * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(inp, seqlens, budget_s=args.cpu_budget)
