@@ -100,7 +100,7 @@ MlaWorkspace mla_workspace_layout(int b, int num_units) {
   w.d = w.ml + round_up(slots * kMlaRows * sizeof(float2), 256);
   w.corr = w.d + round_up(slots * kMlaRows * kMlaCorrTerms * sizeof(float), 256);
   w.qbuf = w.corr + round_up(static_cast<size_t>(b) * kMlaRows * kMlaCorrTerms * sizeof(float), 256);
-  w.qscale = w.qbuf + round_up(static_cast<size_t>(b) * 2 * kMlaQSlotBytes, 256);
+  w.qscale = w.qbuf + round_up(static_cast<size_t>(b) * kMlaQBytes, 256);
   w.total = w.qscale + round_up(static_cast<size_t>(b) * kMlaRows * sizeof(float), 256);
   return w;
 }

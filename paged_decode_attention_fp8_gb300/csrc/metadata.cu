@@ -42,32 +42,44 @@ __device__ __forceinline__ void put_row(int32_t* row, int a, int b, int c, int d
 constexpr int kMetaThreads = 512;
 
 // Exclusive prefix sum of v[0, n) in place (one block); returns the total.
+// Each thread sums a contiguous run, the runs are scanned with warp shuffles
+// (in-warp, then across the warp totals), and each thread rewrites its run.
+// scratch holds at least blockDim.x / 32 + 1 values.
 template <typename T>
 __device__ T block_exclusive_scan(T* v, int n, T* scratch) {
   const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, wid = tid >> 5, nw = nt >> 5;
   const int per = (n + nt - 1) / nt;
   const int lo = min(n, tid * per), hi = min(n, lo + per);
   T run = 0;
   for (int i = lo; i < hi; ++i) run += v[i];
-  scratch[tid] = run;
+  T inc = run;  // inclusive scan of the runs inside the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) scratch[wid] = inc;
   __syncthreads();
-  if (tid == 0) {
-    T acc = 0;
-    for (int k = 0; k < nt; ++k) {
-      const T x = scratch[k];
-      scratch[k] = acc;
-      acc += x;
+  if (wid == 0) {
+    T w = lane < nw ? scratch[lane] : T(0);
+    T winc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const T y = __shfl_up_sync(0xffffffffu, winc, o);
+      if (lane >= o) winc += y;
     }
-    scratch[nt] = acc;
+    if (lane < nw) scratch[lane] = winc - w;  // exclusive offset of warp `lane`
+    if (lane == 31) scratch[nw] = winc;       // the total
   }
   __syncthreads();
-  T acc = scratch[tid];
+  T acc = scratch[wid] + inc - run;
   for (int i = lo; i < hi; ++i) {
     const T x = v[i];
     v[i] = acc;
     acc += x;
   }
-  const T total = scratch[nt];
+  const T total = scratch[nw];
   __syncthreads();
   return total;
 }
@@ -196,13 +208,15 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
     const int32_t* __restrict__ num_splits, int uniform_splits, const void* __restrict__ ws_o_,
     const float2* __restrict__ ws_ml, const float* __restrict__ ws_d, const float* __restrict__ ws_corr, int corr_terms,
     float softmax_scale, uint16_t* __restrict__ out, float* __restrict__ lse, int rows, int slot_rows) {
-  griddep_wait();  // launched as a dependent of the decode kernel
   const int bi = blockIdx.x;
   const int r = blockIdx.y * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  if (r >= rows) return;
+  // The split counts were written before the decode kernel started (it waited
+  // for them), so they are read before waiting for the decode kernel itself.
   const int s0 = uniform_splits > 0 ? bi * uniform_splits : __ldg(num_splits + bi);
   const int ns = uniform_splits > 0 ? uniform_splits : __ldg(num_splits + bi + 1) - s0;
+  griddep_wait();  // launched as a dependent of the decode kernel
+  if (r >= rows) return;
   const size_t row = static_cast<size_t>(bi) * rows + r;
   auto corr_sum = [&](const float* p) {  // the row's correction shares (4, 2 or 0 of them)
     if (corr_terms == 4) {
@@ -232,6 +246,52 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
 #pragma unroll
   for (int c = 0; c < 16; ++c) acc[c] = 0.f;
   float big_l = 0.f, dq = 0.f, big_m = kNegInf;
+  if (kBf16 && ns <= 4) {
+    // few splits (the usual case): every load is issued before any is used
+    constexpr int kMax = 4;
+    uint4 v[kMax][2];
+    float2 ml = make_float2(kNegInf, 0.f);
+    float d = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMax; ++j) {
+      if (j < ns) {
+        const size_t slot = static_cast<size_t>(s0 + j) * slot_rows + r;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(ws_o_) + slot * kMlaDV + lane * 16);
+        v[j][0] = __ldg(src);
+        v[j][1] = __ldg(src + 1);
+      }
+    }
+    if (lane < ns) {
+      const size_t slot = static_cast<size_t>(s0 + lane) * slot_rows + r;
+      ml = __ldg(ws_ml + slot);
+      if (corr_terms > 0) d = corr_sum(ws_d + static_cast<size_t>(corr_terms) * slot);
+    }
+    float m_all = ml.x;
+#pragma unroll
+    for (int o = 2; o > 0; o >>= 1) m_all = fmaxf(m_all, __shfl_xor_sync(0xffffffffu, m_all, o));
+    m_all = __shfl_sync(0xffffffffu, m_all, 0);
+    if (m_all != kNegInf) {
+      big_m = m_all;
+      const float w = (ml.x == kNegInf) ? 0.f : ex2_approx(ml.x - big_m);  // an empty split adds nothing
+      big_l = ml.y * w;
+      dq = w * d;
+#pragma unroll
+      for (int j = 0; j < kMax; ++j) {
+        if (j < ns) {
+          const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t w4[4] = {v[j][c].x, v[j][c].y, v[j][c].z, v[j][c].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[8 * c + 2 * q] += wj * bf16_lo(w4[q]);
+              acc[8 * c + 2 * q + 1] += wj * bf16_hi(w4[q]);
+            }
+          }
+        }
+      }
+    }
+  } else
   for (int base = 0; base < ns; base += 32) {
     // this round's splits: lane j holds split base + j's (m, l) and correction
     const int cnt = min(32, ns - base);

@@ -871,43 +871,61 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 namespace f8 {
 constexpr int kStages = 5;
 constexpr int kThreads = 384;
-constexpr int kOffRope8 = 4 * kLatBox;            // 64 tokens x 64 E4M3 RoPE bytes, no swizzle
-constexpr int kOffCvt = kOffRope8 + kPage * 64;   // the RoPE part as bf16, 128-byte swizzle
-constexpr int kStageBytes = kOffCvt + kLatBox;
+constexpr int kOffRope8 = 4 * kLatBox;             // 64 tokens x 64 E4M3 RoPE bytes, no swizzle
+constexpr int kStageBytes = kOffRope8 + kPage * 64;
+// Shared memory after the ring: two buffers for a page's RoPE part as f16
+// (64 keys x 128 B, 128-byte swizzle), Q's RoPE part (128 rows x 128 B f16,
+// 128-byte swizzle), and P (128 rows x 64 E4M3 keys) as 8-row x 16-byte core
+// matrices: row group g and 16-byte key chunk c at g * kPSbo + c * kPLbo.
+constexpr int kCvtBytes = kLatBox;
+constexpr int kOffCvt = kStages * kStageBytes;
+constexpr int kOffQRope = kOffCvt + 2 * kCvtBytes;
+constexpr int kOffP = kOffQRope + kRows * 128;
+constexpr int kPLbo = 128, kPSbo = 512;
+constexpr int kSmemData = kOffP + kRows * kPage;
 constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
 constexpr float kTau = 2.75f;                     // 64 * 2^2.75 = 430.5 < 448
-constexpr uint32_t kTO = 0, kTS = 256, kTP = 320, kTQ = 352, kTQR = 480;
-constexpr int kPCols = 16;                        // one P buffer: 64 E4M3 keys per row
-// Q slot h (h = 0, 1): per row, latent bytes [256 h, 256 h + 256) at a 272-byte
-// pitch, then per row RoPE values [32 h, 32 h + 32) as bf16 at an 80-byte pitch
-// (pitches chosen so a quarter-warp's 16-byte row accesses hit distinct banks).
+// TMEM columns: O slice, two S buffers (pages alternate), Q latent (E4M3).
+constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
+// Quantised Q of a sequence, as three ring slots: slot h (h = 0, 1) holds per
+// row latent bytes [256 h, 256 h + 256) at a 272-byte pitch, slot 2 the RoPE
+// values as f16 at a 144-byte pitch (pitches chosen so a quarter-warp's
+// 16-byte row accesses hit distinct banks).
 constexpr int kQLatPitch = 272;
-constexpr int kQRopeOff = kRows * kQLatPitch;
-constexpr int kQRopePitch = 80;
-static_assert(kQRopeOff + kRows * kQRopePitch <= kStageBytes, "a Q slot fits one stage");
-static_assert(kOffCvt % 1024 == 0 && kStageBytes % 1024 == 0, "1 KB aligned tiles");
-static_assert(kStageBytes == kMlaQSlotBytes, "a quantised-Q half is one ring stage");
+constexpr int kQRopePitch = 144;
+constexpr int kQLatSlotBytes = kRows * kQLatPitch;
+constexpr int kQRopeSlotBytes = kRows * kQRopePitch;
+static_assert(kQLatSlotBytes <= kStageBytes && kQRopeSlotBytes <= kStageBytes, "a Q slot fits one stage");
+// After the slots: the latent quantisation error q_hat qs - q, 128 rows x 512
+// bf16, read by the epilogue for the LSE correction.
+constexpr int kQErrOff = 2 * kQLatSlotBytes + kQRopeSlotBytes;
+static_assert(kQErrOff + kRows * kDLat * 2 == kMlaQBytes, "quantised-Q layout");
+static_assert(kStageBytes % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
+              "1 KB aligned tiles");
+static_assert(kStageBytes == static_cast<int>(kPageTxBytes), "a page fills one stage");
 
 struct Bars {
   uint64_t kv_full[kStages];    // stage holds its page (TMA bytes) or its Q slot (Q warps' arrival)
   uint64_t kv_empty[kStages];   // stage may be refilled
   uint64_t cvt_ready[kStages];  // the page's RoPE part is converted and its dead rows zeroed
-  uint64_t p_full[2];           // P buffer b written (one arrival per softmax warp)
-  uint64_t pv_done[2];          // the P.V that read P buffer b completed
-  uint64_t s_full, s_free, q_full, final_mma, xchg;
+  uint64_t s_full[2];           // S buffer b holds a page's scores
+  uint64_t p_full;              // P written (one arrival per softmax warp)
+  uint64_t pv_done;             // the P.V that read P completed
+  uint64_t q_full, final_mma, xchg;
   uint32_t tmem_base, abort_flag, cvt_ok;
   float xsum[2][kRows];         // row-sum halves
 };
 
-constexpr size_t smem_bytes() { return kStages * kStageBytes + sizeof(Bars) + 1024; }
+constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
+static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
 
-// Quantises the Q rows of sequence b into the two Q slots: latent -> E4M3(q / qs),
-// RoPE -> bf16(q / qs), qs = smallest power of two with amax <= 448 qs.  kTpr
+// Quantises the Q rows of sequence b into the three Q slots: latent -> E4M3(q / qs),
+// RoPE -> f16(q / qs), qs = smallest power of two with amax <= 448 qs.  kTpr
 // threads share a row; thread `part` takes the 8-value chunks c = part (mod kTpr)
 // of the row's 72 (64 latent, 8 RoPE).
 template <int kTpr>
 __device__ __forceinline__ void fill_q_row(const MlaParams& prm, int b, int r, int part, uint8_t* slot0,
-                                           uint8_t* slot1, float* qs_out) {
+                                           uint8_t* slot1, uint8_t* slot2, uint8_t* err, float* qs_out) {
   constexpr int kChunks = 72 / kTpr;
   constexpr bool kHold = kChunks <= 18;  // few enough chunks to keep in registers between the two passes
   const int R = prm.s_q * prm.h_q;
@@ -925,7 +943,7 @@ __device__ __forceinline__ void fill_q_row(const MlaParams& prm, int b, int r, i
   for (int o = 1; o < kTpr; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const int qe = pow2_scale_exponent(amax);
   const float inv_qs = exp2i(-qe);
-  // chunk c (8 values) -> latent bytes of slot c / 32, or bf16 RoPE of slot (c - 64) / 4
+  // chunk c (8 values) -> latent bytes of slot c / 32, or f16 RoPE of slot 2
   auto put = [&](int c, uint4 a) {
     if (c < 64) {
       uint2 o;
@@ -933,15 +951,23 @@ __device__ __forceinline__ void fill_q_row(const MlaParams& prm, int b, int r, i
       o.y = pack_e4m3x4(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs, bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
       uint8_t* slot = (c < 32) ? slot0 : slot1;
       *reinterpret_cast<uint2*>(slot + r * kQLatPitch + (c & 31) * 8) = o;
+      const float qs = exp2i(qe);
+      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t hq[4] = {e4m3x2_to_f16x2(o.x & 0xFFFFu), e4m3x2_to_f16x2(o.x >> 16), e4m3x2_to_f16x2(o.y & 0xFFFFu),
+                              e4m3x2_to_f16x2(o.y >> 16)};
+      uint4 ev;
+      uint32_t* e4 = &ev.x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        e4[k] = pack_bf16x2(f16_lo(hq[k]) * qs - bf16_lo(w[k]), f16_hi(hq[k]) * qs - bf16_hi(w[k]));
+      *reinterpret_cast<uint4*>(err + r * kDLat * 2 + c * 16) = ev;
     } else {
       uint4 o;
-      o.x = pack_bf16x2(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs);
-      o.y = pack_bf16x2(bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs);
-      o.z = pack_bf16x2(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs);
-      o.w = pack_bf16x2(bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
-      const int j4 = c - 64;
-      uint8_t* slot = (j4 < 4) ? slot0 : slot1;
-      *reinterpret_cast<uint4*>(slot + kQRopeOff + r * kQRopePitch + (j4 & 3) * 16) = o;
+      o.x = pack_f16x2(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs);
+      o.y = pack_f16x2(bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs);
+      o.z = pack_f16x2(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs);
+      o.w = pack_f16x2(bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
+      *reinterpret_cast<uint4*>(slot2 + r * kQRopePitch + (c - 64) * 16) = o;
     }
   };
   if constexpr (kHold) {
@@ -965,8 +991,9 @@ __global__ void __launch_bounds__(256) mla_qprep_kernel(const MlaParams prm) {
   griddep_launch_dependents();
   const int b = blockIdx.x;
   const int r = blockIdx.y * 32 + threadIdx.x / 8;
-  uint8_t* half0 = prm.qbuf + static_cast<size_t>(b) * 2 * kStageBytes;
-  fill_q_row<8>(prm, b, r, threadIdx.x % 8, half0, half0 + kStageBytes, prm.qscale + static_cast<size_t>(b) * kRows);
+  uint8_t* q = prm.qbuf + static_cast<size_t>(b) * kMlaQBytes;
+  fill_q_row<8>(prm, b, r, threadIdx.x % 8, q, q + kQLatSlotBytes, q + 2 * kQLatSlotBytes, q + kQErrOff,
+                prm.qscale + static_cast<size_t>(b) * kRows);
   griddep_wait();
 }
 
@@ -1004,7 +1031,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  Bars* bars = reinterpret_cast<Bars*>(smem + kStages * kStageBytes);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kSmemData);
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -1018,12 +1045,9 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       mbar_init(&bars->kv_empty[s], 1);
       mbar_init(&bars->cvt_ready[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->p_full[b], kSoftmaxThreads / 32);
-      mbar_init(&bars->pv_done[b], 1);
-    }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, kSoftmaxThreads / 32);  // one arrival per softmax warp
+    for (int b = 0; b < 2; ++b) mbar_init(&bars->s_full[b], 1);
+    mbar_init(&bars->p_full, kSoftmaxThreads / 32);
+    mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->xchg, kSoftmaxThreads / 32);
@@ -1043,9 +1067,9 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
   griddep_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
 
-  // Ring protocol.  Every role walks the same slot sequence: two Q slots at
-  // the start of each segment (the halves of its quantised Q, prepared by
-  // mla_qprep_kernel) and then its pages.  Each stage barrier completes one
+  // Ring protocol.  Every role walks the same slot sequence: three Q slots at
+  // the start of each segment (its quantised Q, prepared by mla_qprep_kernel)
+  // and then its pages.  Each stage barrier completes one
   // phase per occupancy of its stage, and every role that waits on one
   // observes each of its phases in turn, so a parity wait can never pass on a
   // phase two behind or two ahead: kv_empty is waited by the producer only;
@@ -1066,16 +1090,18 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     uint32_t issued = 0, par = 0;  // per stage: last occupant was loaded here, and its use parity
     bool ok = true;
     while (ok && walk.next(sg)) {
-      // the segment's quantised Q, one half per slot
-      for (int q = 0; q < 2 && ok; ++q, ++k) {
+      // the segment's quantised Q: two latent halves and the RoPE part
+      for (int q = 0; q < 3 && ok; ++q, ++k) {
         const int st = k % kStages, use = k / kStages;
+        const uint32_t bytes = (q < 2) ? kQLatSlotBytes : kQRopeSlotBytes;
         bool waited = true;
         if (lane == 0) {
           waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla);
           if (waited) {
-            mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-            bulk_load(smem + st * kStageBytes, prm.qbuf + (static_cast<size_t>(sg.b) * 2 + q) * kStageBytes,
-                      kStageBytes, &bars->kv_full[st]);
+            mbar_arrive_expect_tx(&bars->kv_full[st], bytes);
+            bulk_load(smem + st * kStageBytes,
+                      prm.qbuf + static_cast<size_t>(sg.b) * kMlaQBytes + static_cast<size_t>(q) * kQLatSlotBytes,
+                      bytes, &bars->kv_full[st]);
             issued |= 1u << st;
             par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
           }
@@ -1127,26 +1153,29 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     // ------------------------------------------------- MMA issuer ----
     // The whole warp runs the loop (so descriptors stay warp-uniform) and one
     // elected lane issues -- from a lone thread each MMA costs about twice as
-    // long to issue.  Per page i: wait until S was read out, Q.K^T as 16 E4M3
-    // MMAs (latent, K = 32) and 4 bf16 MMAs (RoPE, K = 16) back to back, then
-    // the P.V of page i - 2, whose P the softmax warps store while this Q.K^T
-    // runs, so Q.K^T never waits behind a P.V.
+    // long to issue.  Pages alternate between two S buffers, so the Q.K^T of
+    // page i runs while the softmax warps work on page i - 1.  Per page i: wait
+    // until S buffer i % 2 was read out (page i - 2), Q.K^T as 16 E4M3 MMAs
+    // (latent, Q from TMEM, K = 32) and 4 f16 MMAs (RoPE, Q from shared
+    // memory, K = 16), then the P.V of page i - 1 (2 E4M3 MMAs, K = 32 keys,
+    // N = 256) once its P is written.
     {
       constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
-      constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);   // bf16 x bf16
+      constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
       constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
-      const uint32_t t_s = tmem + kTS, t_o = tmem + kTO;
+      const uint32_t t_o = tmem + kTO;
       const bool leader = elect_one();
+      const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
+      const uint64_t pd = make_sdesc(smem_u32(smem + kOffP), kPLbo, kPSbo, SWIZZLE_NONE);
       SegmentWalker walk(prm, unit);
       Segment sg;
       int i = 0, k = 0, seg = 0;
       int j = 0;           // next page whose P.V is due (pages j .. i - 1 have their Q.K^T issued)
       uint32_t pend = 0;   // per pending page p, byte p % 4: its stage | first-of-segment << 3
       bool ok = true;
-      // the P.V of page j, once its P is written
+      // the P.V of page j, once its P is written; it releases the page's stage
       auto issue_pv = [&]() -> bool {
-        const int pb = j & 1;
-        if (!warp_spin(&bars->p_full[pb], (j >> 1) & 1, abort_flag)) return false;
+        if (!warp_spin(&bars->p_full, j & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t e = (pend >> (8 * (j & 3))) & 0xFFu;
         const int st = static_cast<int>(e & 7u);
@@ -1156,12 +1185,12 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           if (leader)
-            mma_f8_ts(t_o, tmem + kTP + pb * kPCols + kk * 8, vd + ((kk * 4096) >> 4), idesc_pv,
+            mma_f8_ss(t_o, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
                       (first && kk == 0) ? 0u : 1u);
           __syncwarp();
         }
         if (leader) {
-          tc_commit(&bars->pv_done[pb]);
+          tc_commit(&bars->pv_done);
           tc_commit(&bars->kv_empty[st]);
         }
         __syncwarp();
@@ -1169,36 +1198,35 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         return true;
       };
       while (ok && walk.next(sg)) {
-        const int st0 = k % kStages, st1 = (k + 1) % kStages;
-        // The previous segment's last P.Vs come first: the softmax warps write
-        // their P before they copy this segment's Q.
+        // The previous segment's last P.V comes first: the softmax warps write
+        // its P before they copy this segment's Q.
         while (ok && j < i) ok = issue_pv();
-        // the softmax warps have copied both Q slots into TMEM (and the converter has seen them)
-        if (!ok || !warp_wait(&bars->q_full, seg & 1, abort_flag) ||
-            !warp_wait(&bars->cvt_ready[st0], (k / kStages) & 1, abort_flag) ||
-            !warp_wait(&bars->cvt_ready[st1], ((k + 1) / kStages) & 1, abort_flag)) {
+        // the softmax warps have copied the Q slots (and the converter has seen them)
+        bool qok = ok && warp_wait(&bars->q_full, seg & 1, abort_flag);
+        for (int q = 0; q < 3 && qok; ++q)
+          qok = warp_wait(&bars->cvt_ready[(k + q) % kStages], ((k + q) / kStages) & 1, abort_flag);
+        if (!qok) {
           ok = false;
           break;
         }
-        if (leader) {
-          mbar_arrive(&bars->kv_empty[st0]);
-          mbar_arrive(&bars->kv_empty[st1]);
-        }
+        if (leader)
+          for (int q = 0; q < 3; ++q) mbar_arrive(&bars->kv_empty[(k + q) % kStages]);
         __syncwarp();
-        k += 2;
+        k += 3;
+        // Page i's inputs are waited for before the P.V of page i - 2 (so that
+        // Q.K^T(i) follows that P.V in the tensor pipe without a gap).  S buffer
+        // i % 2 last held page i - 2, whose P (written after its S was read) that
+        // P.V waited for -- or the previous segment's flush did.
+        if (!warp_spin(&bars->cvt_ready[k % kStages], (k / kStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         for (int pg = sg.lo; pg < sg.hi; ++pg, ++i, ++k) {
           const int st = k % kStages;
-          const int use = k / kStages;
-          // cvt_ready follows the converter's own wait for the page's load, so it
-          // also stands for kv_full; the S buffer must have been read out
-          if (!warp_spin(&bars->cvt_ready[st], use & 1, abort_flag) ||
-              (i > 0 && !warp_spin(&bars->s_free, (i - 1) & 1, abort_flag))) {
-            ok = false;
-            break;
-          }
+          const int sbuf = i & 1;
           tc_fence_after();
-          const uint32_t sb = smem_u32(smem + st * kStageBytes);
-          const uint64_t kd = make_sdesc(sb, 16, 1024, SWIZZLE_128B);
+          const uint32_t t_s = tmem + kTS + sbuf * kPage;
+          const uint64_t kd = make_sdesc(smem_u32(smem + st * kStageBytes), 16, 1024, SWIZZLE_128B);
 #pragma unroll
           for (int kk = 0; kk < 16; ++kk) {
             if (leader)
@@ -1206,25 +1234,30 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
                         kk > 0 ? 1u : 0u);
             __syncwarp();
           }
-          const uint64_t rd = make_sdesc(sb + kOffCvt, 16, 1024, SWIZZLE_128B);
+          const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + sbuf * kCvtBytes), 16, 1024, SWIZZLE_128B);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            if (leader) mma_f16_ts(t_s, tmem + kTQR + kk * 8, rd + ((kk * 32) >> 4), idesc16, 1u);
+            if (leader) mma_f16_ss(t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
             __syncwarp();
           }
-          if (leader) tc_commit(&bars->s_full);
+          if (leader) tc_commit(&bars->s_full[sbuf]);
           __syncwarp();
           const uint32_t e = static_cast<uint32_t>(st) | ((pg == sg.lo) ? 8u : 0u);
           pend = (pend & ~(0xFFu << (8 * (i & 3)))) | (e << (8 * (i & 3)));
-          // P.V two pages back (in this segment): its P was written before S(i - 1) was read
-          if (pg - sg.lo >= 2 && !issue_pv()) {  // j == i - 2 here
+          // the next page's conversion, then the P.V of the previous page
+          if (pg + 1 < sg.hi &&
+              !warp_spin(&bars->cvt_ready[(k + 1) % kStages], ((k + 1) / kStages) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (pg > sg.lo && !issue_pv()) {  // j == i - 1 here
             ok = false;
             break;
           }
         }
         ++seg;
       }
-      while (ok && j < i) ok = issue_pv();  // the last P.Vs
+      while (ok && j < i) ok = issue_pv();  // the last P.V
       if (leader) tc_commit(&bars->final_mma);
       __syncwarp();
       warp_wait(&bars->final_mma, 0, nullptr);
@@ -1234,29 +1267,33 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     const int t = threadIdx.x - 64;  // token row of the page
     SegmentWalker walk(prm, unit);
     Segment sg;
-    int k = 0;
+    int k = 0, i = 0;  // ring slots, pages
     bool ok = true;
     while (ok && walk.next(sg)) {
       // the Q slots need no conversion, but their fills are waited for and
       // acknowledged like the pages' so that each stage phase is seen in turn
       if (t == 0) {
-        const bool filled =
-            wait_bounded(&bars->kv_full[k % kStages], (k / kStages) & 1, abort_flag, &g_status_mla) &&
-            wait_bounded(&bars->kv_full[(k + 1) % kStages], ((k + 1) / kStages) & 1, abort_flag, &g_status_mla);
-        if (filled) {
-          mbar_arrive(&bars->cvt_ready[k % kStages]);
-          mbar_arrive(&bars->cvt_ready[(k + 1) % kStages]);
-        }
+        bool filled = true;
+        for (int q = 0; q < 3 && filled; ++q)
+          filled = wait_bounded(&bars->kv_full[(k + q) % kStages], ((k + q) / kStages) & 1, abort_flag,
+                                &g_status_mla);
+        if (filled)
+          for (int q = 0; q < 3; ++q) mbar_arrive(&bars->cvt_ready[(k + q) % kStages]);
         bars->cvt_ok = filled ? 1u : 0u;
       }
       named_bar_sync(1, 64);
       if (!bars->cvt_ok) break;
       named_bar_sync(1, 64);  // cvt_ok is rewritten below
-      k += 2;
-      for (int pg = sg.lo; pg < sg.hi; ++pg, ++k) {
+      k += 3;
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++k, ++i) {
         const int st = k % kStages;
         const int use = k / kStages;
-        if (t == 0) bars->cvt_ok = wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla) ? 1u : 0u;
+        // conversion buffer i % 2 is free once the Q.K^T of page i - 2 completed
+        if (t == 0)
+          bars->cvt_ok = (wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla) &&
+                          (i < 2 || wait_bounded(&bars->s_full[i & 1], ((i - 2) >> 1) & 1, abort_flag, &g_status_mla)))
+                             ? 1u
+                             : 0u;
         named_bar_sync(1, 64);
         if (!bars->cvt_ok) {
           ok = false;
@@ -1267,16 +1304,20 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         const uint4 z = make_uint4(0, 0, 0, 0);
         const int sw = t & 7;
         const uint4* src = reinterpret_cast<const uint4*>(sb + kOffRope8 + t * 64);
-        uint8_t* dst = sb + kOffCvt + t * 128;
+        uint8_t* dst = smem + kOffCvt + (i & 1) * kCvtBytes + t * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint4 lo = z, hi = z;
           if (!dead) {
             const uint4 v = src[c];
-            e4m3x4_to_bf16x4(v.x, lo.x, lo.y);
-            e4m3x4_to_bf16x4(v.y, lo.z, lo.w);
-            e4m3x4_to_bf16x4(v.z, hi.x, hi.y);
-            e4m3x4_to_bf16x4(v.w, hi.z, hi.w);
+            lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
+            lo.y = e4m3x2_to_f16x2(v.x >> 16);
+            lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
+            lo.w = e4m3x2_to_f16x2(v.y >> 16);
+            hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
+            hi.y = e4m3x2_to_f16x2(v.z >> 16);
+            hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
+            hi.w = e4m3x2_to_f16x2(v.w >> 16);
           }
           *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
           *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
@@ -1310,13 +1351,15 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       return ok;
     };
     // Copies this half of the Q row of the segment whose Q slots start at ring
-    // slot kq into TMEM: latent bytes [256 hf, +256) -> columns kTQ + 64 hf..,
-    // RoPE values [32 hf, +32) -> columns kTQR + 16 hf..
+    // slot kq: latent bytes [256 hf, +256) into TMEM columns kTQ + 64 hf..,
+    // RoPE values [32 hf, +32) into the shared Q RoPE tile (128-byte swizzle).
     auto copy_q = [&](int kq, int b_seq, float& qs_out) -> bool {
       const int st = (kq + hf) % kStages, use = (kq + hf) / kStages;
-      if (!warp_wait(&bars->kv_full[st], use & 1, abort_flag)) return false;
-      const uint8_t* slot = smem + st * kStageBytes;
-      const uint4* lat = reinterpret_cast<const uint4*>(slot + r * kQLatPitch);
+      const int st_r = (kq + 2) % kStages, use_r = (kq + 2) / kStages;
+      if (!warp_wait(&bars->kv_full[st], use & 1, abort_flag) ||
+          !warp_wait(&bars->kv_full[st_r], use_r & 1, abort_flag))
+        return false;
+      const uint4* lat = reinterpret_cast<const uint4*>(smem + st * kStageBytes + r * kQLatPitch);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
@@ -1331,20 +1374,13 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         tmem_st16(lane_base + kTQ + (4 * hf + ch) * 16, pk);
       }
       {
-        uint32_t pk[16];
-        const uint4* rope = reinterpret_cast<const uint4*>(slot + kQRopeOff + r * kQRopePitch);
+        const uint4* rope = reinterpret_cast<const uint4*>(smem + st_r * kStageBytes + r * kQRopePitch);
+        uint8_t* dst = smem + kOffQRope + r * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = rope[c];
-          pk[4 * c + 0] = v.x;
-          pk[4 * c + 1] = v.y;
-          pk[4 * c + 2] = v.z;
-          pk[4 * c + 3] = v.w;
-        }
-        tmem_st16(lane_base + kTQR + 16 * hf, pk);
+        for (int c = 4 * hf; c < 4 * hf + 4; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = rope[c];
       }
       qs_out = prm.qscale[static_cast<size_t>(b_seq) * kRows + r];
-      fence_proxy_async_smem();  // the slots' next contents arrive by TMA
+      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs, the slots refilled by TMA
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bars->q_full);
@@ -1358,13 +1394,14 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     bool ok = walk.next(sg) && copy_q(0, sg.b, qs_next);
     while (ok) {
       const float qs = qs_next;
-      const float inv_qs = 1.0f / qs;  // a power of two: exact
       const float c_row = prm.softmax_scale * kLog2e * qs * kv_scale;
       SegmentWalker peek = walk;
       Segment nx;
       const bool has_next = peek.next(nx);
-      const int k_next = k + 2 + (sg.hi - sg.lo);
-      const uint16_t* qrow = prm.q + (static_cast<size_t>(sg.b) * R + (r < R ? r : 0)) * kD;
+      const int k_next = k + 3 + (sg.hi - sg.lo);
+      // the segment's latent quantisation errors (bf16, rows of 512), for the LSE correction
+      const uint16_t* ebase =
+          reinterpret_cast<const uint16_t*>(prm.qbuf + static_cast<size_t>(sg.b) * kMlaQBytes + kQErrOff);
       const int col0 = part * 256 + hf * kOHalf;  // this thread's O columns
       // keys visible to this row (bottom-right causal alignment); pages wholly
       // below every row's limit need no mask
@@ -1374,11 +1411,12 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       float m_run = kNegInf, l_run = 0.f;  // l_run sums the stored-scale p (kPScale p)
       for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
         if (pg == sg.hi - 1) {  // the epilogue's LSE correction re-reads these Q columns
-          const char* qc = reinterpret_cast<const char*>(qrow + col0);
+          const char* qc = reinterpret_cast<const char*>(ebase + static_cast<size_t>(r) * kDLat + col0);
           prefetch_l2(qc);
           prefetch_l2(qc + 128);
         }
-        if (!warp_spin(&bars->s_full, i & 1, abort_flag)) {
+        const int sbuf = i & 1;
+        if (!warp_spin(&bars->s_full[sbuf], (i >> 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
@@ -1386,11 +1424,9 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         // Both halves of the row are read: the other half only for the row max,
         // so each warp takes the max of all 64 keys without waiting on its partner.
         uint32_t s[32], so[32];
-        tmem_ld32(lane_base + kTS + 32 * hf, s);
-        tmem_ld32(lane_base + kTS + 32 * (1 - hf), so);
+        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * hf, s);
+        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * (1 - hf), so);
         tmem_ld_wait();
-        tc_fence_before();
-        warp_arrive(&bars->s_free);
 
         if (pg * kPage + kPage > min_visible) {
           const int base = pg * kPage + 32 * hf, base_o = pg * kPage + 32 * (1 - hf);
@@ -1400,17 +1436,22 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
             if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
           }
         }
-        // row max of the 64 scores as a tree (short dependency chains)
-        float m16[16];
+        // row max of the 64 scores as a tree of three-way maxima
+        float m22[22];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          m16[c] = fmaxf(fmaxf(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
-                         fmaxf(__uint_as_float(so[2 * c]), __uint_as_float(so[2 * c + 1])));
+        for (int c = 0; c < 10; ++c) {
+          m22[c] = fmax3(__uint_as_float(s[3 * c]), __uint_as_float(s[3 * c + 1]), __uint_as_float(s[3 * c + 2]));
+          m22[10 + c] =
+              fmax3(__uint_as_float(so[3 * c]), __uint_as_float(so[3 * c + 1]), __uint_as_float(so[3 * c + 2]));
+        }
+        m22[20] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
+        m22[21] = fmaxf(__uint_as_float(so[30]), __uint_as_float(so[31]));
+        float m8[8];
 #pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-          for (int c = 0; c < w; ++c) m16[c] = fmaxf(m16[c], m16[c + w]);
-        float mx = m16[0] * c_row;  // c_row > 0; both warps of the row get the same value
+        for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
+        m8[7] = m22[21];
+        const float m3a = fmax3(m8[0], m8[1], m8[2]), m3b = fmax3(m8[3], m8[4], m8[5]);
+        const float mx = fmax3(m3a, m3b, fmaxf(m8[6], m8[7])) * c_row;  // c_row > 0; both warps agree
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_run + kTau) {
@@ -1432,14 +1473,14 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         }
         l_run = l_run * alpha + sum;
 
-        const int pb = i & 1;
+        // P has one tile and O one accumulator: the previous page's P.V must
+        // have completed before either is touched
+        if (i >= 1 && !warp_spin(&bars->pv_done, (i - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         if (__any_sync(0xffffffffu, rescale)) {
-          // O is being accumulated by the previous page's P.V: wait for it, then rescale
-          if (!warp_wait(&bars->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
           for (int ch = 0; ch < kOHalf / 32; ++ch) {
@@ -1451,18 +1492,16 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
             tmem_st32(lane_base + col, o);
           }
-        } else if (i >= 2) {
-          // the P buffer is free once the P.V that last read it has completed
-          if (!warp_spin(&bars->pv_done[pb], ((i - 2) >> 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          tmem_st_wait();
         }
-        tmem_st8(lane_base + kTP + pb * kPCols + 8 * hf, pk);
-        tmem_st_wait();
+        {  // this warp's 32 keys of row r: 16-byte chunks 2 hf and 2 hf + 1
+          uint8_t* prow = smem + kOffP + (r >> 3) * kPSbo + (r & 7) * 16;
+          *reinterpret_cast<uint4*>(prow + (2 * hf) * kPLbo) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(prow + (2 * hf + 1) * kPLbo) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        fence_proxy_async_smem();
         tc_fence_before();
-        warp_arrive(&bars->p_full[pb]);
+        warp_arrive(&bars->p_full);
         // the segment's last Q.K^T is done: the next segment's Q may replace it now
         if (pg == sg.hi - 1 && has_next && !copy_q(k_next, nx.b, qs_next)) {
           ok = false;
@@ -1472,14 +1511,21 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       if (!ok) break;
 
       // ---- epilogue: O is final once the segment's last P.V completes ----
-      // this thread's 128 Q values for the LSE correction (in L2 since the last
-      // page), requested before the row-sum exchange and the last P.V's wait
-      uint4 qv[16];
-      {
-        const uint4* q4e = reinterpret_cast<const uint4*>(qrow + col0);
+      // Output pass over this thread's 128 O columns, 32 at a time.  A thread
+      // holds one row; groups of four lanes transpose their 16-byte pieces so
+      // that each store writes 64-byte runs of rows, and in that layout the
+      // same lanes read the matching 16-byte pieces of the quantisation errors
+      // (coalesced) for the LSE correction's dot product with the output.
+      const int row0 = (warp % 4) * 32;  // first row of this warp
+      const int grow = row0 + (lane & ~3);  // the group's first row
+      auto load_err = [&](int ch, uint4 (&ev)[4]) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) qv[c] = (r < R) ? __ldg(q4e + c) : make_uint4(0, 0, 0, 0);
-      }
+        for (int kk = 0; kk < 4; ++kk)
+          ev[kk] = __ldg(reinterpret_cast<const uint4*>(ebase + static_cast<size_t>(grow + kk) * kDLat + col0 + ch * 32 +
+                                                        8 * (lane & 3)));
+      };
+      uint4 ev[4];
+      load_err(0, ev);  // in flight across the row-sum exchange and the last P.V's wait
       bars->xsum[hf][r] = l_run;
       if (!xsync()) break;
       const float l_tot = (bars->xsum[0][r] + bars->xsum[1][r]) * (1.0f / kPScale);  // sum of p
@@ -1487,33 +1533,18 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       const float o_scale = kv_scale / kPScale;  // tensor-core units -> true units
       const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
       const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
-      if (!warp_wait(&bars->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) break;
+      if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag)) break;
       tc_fence_after();
-      float dq_dot = 0.f;  // sum over this thread's columns of (q_hat - q) * O
-#pragma unroll
-      for (int ch = 0; ch < kOHalf / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = qv[4 * ch + c];
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 e = q_quant_error(w[q], inv_qs, qs);
-            dq_dot += e.x * __uint_as_float(o[8 * c + 2 * q]) + e.y * __uint_as_float(o[8 * c + 2 * q + 1]);
-          }
-        }
-      }
-      // O out as bf16, 32 columns at a time.  A thread holds one row; groups
-      // of four lanes transpose their 16-byte pieces so that each store
-      // instruction writes 64-byte runs of rows.
-      const int row0 = (warp % 4) * 32;  // first row of this warp
+      // a whole sequence goes straight to out; a piece to its bf16 partial slot
+      uint16_t* obase = whole ? prm.out + static_cast<size_t>(sg.b) * R * kDV
+                              : prm.ws_o + static_cast<size_t>(slot) * kRows * kDV;
+      float dqk[4] = {0.f, 0.f, 0.f, 0.f};  // (q_hat - q) . O f for rows grow + kk, over this lane's pieces
 #pragma unroll 1
       for (int ch = 0; ch < kOHalf / 32; ++ch) {
         uint32_t o[32];
         tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
+        uint4 en[4];  // the next chunk's errors, in flight while this chunk is processed
+        if (ch + 1 < kOHalf / 32) load_err(ch + 1, en);
         tmem_ld_wait();
         uint4 pc[4];
 #pragma unroll
@@ -1524,26 +1555,39 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           pc[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
         }
         lane_group_transpose<4>(pc, lane);
-        // a whole sequence goes straight to out; a piece to its bf16 partial slot
-        uint16_t* base = whole ? prm.out + static_cast<size_t>(sg.b) * R * kDV
-                               : prm.ws_o + static_cast<size_t>(slot) * kRows * kDV;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const int row = row0 + (lane & ~3) + kk;
-          if (row < R)
-            *reinterpret_cast<uint4*>(base + static_cast<size_t>(row) * kDV + col0 + ch * 32 + 8 * (lane & 3)) =
+          const uint32_t a4[4] = {pc[kk].x, pc[kk].y, pc[kk].z, pc[kk].w};
+          const uint32_t e4[4] = {ev[kk].x, ev[kk].y, ev[kk].z, ev[kk].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dqk[kk] += bf16_lo(e4[q]) * bf16_lo(a4[q]) + bf16_hi(e4[q]) * bf16_hi(a4[q]);
+          if (grow + kk < R)
+            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(grow + kk) * kDV + col0 + ch * 32 + 8 * (lane & 3)) =
                 pc[kk];
         }
+        if (ch + 1 < kOHalf / 32) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) ev[kk] = en[kk];
+        }
       }
+      // sum each row's share over its group's four lanes; lane q keeps row grow + q (its own)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        dqk[kk] += __shfl_xor_sync(0xffffffffu, dqk[kk], 1);
+        dqk[kk] += __shfl_xor_sync(0xffffffffu, dqk[kk], 2);
+      }
+      const int q4 = lane & 3;
+      const float dq_out = q4 == 0 ? dqk[0] : q4 == 1 ? dqk[1] : q4 == 2 ? dqk[2] : dqk[3];
       if (r < R) {  // each (dv slice, row half) publishes its own share of the correction
         const size_t row = static_cast<size_t>(sg.b) * R + r;
         if (whole) {
           if (part == 0 && hf == 0) prm.lse[row] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
-          prm.ws_corr[row * 4 + part * 2 + hf] = -prm.softmax_scale * dq_dot * f;
+          prm.ws_corr[row * 4 + part * 2 + hf] = -prm.softmax_scale * dq_out;
         } else {
           const size_t srow = static_cast<size_t>(slot) * kRows + r;
           if (part == 0 && hf == 0) prm.ws_ml[srow] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
-          prm.ws_d[srow * 4 + part * 2 + hf] = dq_dot * f;
+          prm.ws_d[srow * 4 + part * 2 + hf] = dq_out;
         }
       }
       if (!has_next) break;

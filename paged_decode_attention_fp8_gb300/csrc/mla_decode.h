@@ -19,7 +19,7 @@ struct MlaParams {
   float2* ws_ml;               // [slots, 128] (m in log2 units, l)
   float* ws_d;                 // [slots, 128, 4] sum of (q_hat - q) * O_partial per (dv slice, row half) (FP8 dots)
   float* ws_corr;              // [b, 128, 4] -softmax_scale * (q_hat - q) . out per (dv slice, row half) (FP8 dots)
-  uint8_t* qbuf;               // [b, 2, kMlaQSlotBytes] Q quantised for FP8 dots, in the kernel's slot layout
+  uint8_t* qbuf;               // [b, kMlaQBytes] Q quantised for FP8 dots, in the kernel's slot layout
   float* qscale;               // [b, 128] per-row power-of-two Q scale (FP8 dots)
   uint16_t* out;               // bf16 [b, s_q, h_q, 512]
   float* lse;                  // [b, s_q, h_q]
@@ -36,7 +36,10 @@ constexpr int kMlaPage = 64;
 constexpr int kMlaD = 576;
 constexpr int kSchedFixedCost = 4;
 constexpr int kMlaCorrTerms = 4;  // LSE-correction shares per row: 2 dv slices x 2 row halves
-constexpr int kMlaQSlotBytes = 45056;  // one quantised-Q half: 128 rows x (272 latent + 80 RoPE) bytes
+// One sequence's quantised Q, in the decode kernel's ring-slot layout (two
+// latent slots of 128 x 272 bytes, one RoPE slot of 128 x 144 bytes), then
+// the latent quantisation error (q_hat qs - q) as 128 x 512 bf16.
+constexpr int kMlaQBytes = 219136;
 constexpr size_t kMetadataMaxSmem = 200 * 1024;  // the scheduler stages ~16 bytes per sequence and unit
 size_t metadata_smem_bytes(int b, int num_units);
 

@@ -21,9 +21,9 @@ constexpr int kNoAllocMaxBatch = FP8MLA_NO_ALLOC_MAX_BATCH;
 constexpr size_t kSchedBytes = 256 * 8 * sizeof(int32_t);                         // tile schedule, <= 256 units
 constexpr size_t kSplitsBytes = 256 * sizeof(int32_t);                            // split prefix, <= 255 sequences
 constexpr size_t kCorrBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaRows * kMlaCorrTerms * sizeof(float);
-constexpr size_t kQBufBytes = static_cast<size_t>(kNoAllocMaxBatch) * 2 * kMlaQSlotBytes;    // quantised Q
+constexpr size_t kQBufBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaQBytes;    // quantised Q
 constexpr size_t kQScaleBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaRows * sizeof(float);
-constexpr size_t kScratchBytes = kSchedBytes + kSplitsBytes + kCorrBytes + kQBufBytes + kQScaleBytes;  // 5.9 MB
+constexpr size_t kScratchBytes = kSchedBytes + kSplitsBytes + kCorrBytes + kQBufBytes + kQScaleBytes;  // 14.2 MB
 static_assert(kNoAllocMaxBatch <= 255, "the split prefix holds b + 1 entries");
 
 // Held by every GPU that loads the library, for the life of the process.
