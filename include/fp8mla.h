@@ -217,7 +217,7 @@ FP8MLA_API int paged_gqa_num_splits(int bs, int h_kv, int max_seqlen, int num_sm
  * Same arguments and results as fp8mla_decode without the schedule and the
  * workspace: the call schedules one work unit per sequence (no split-KV) and
  * keeps its schedule, split counts, LSE-correction terms and quantised Q in a fixed
- * device array compiled into this library (14.2 MB, held by every GPU that
+ * device array compiled into this library (14.1 MB, held by every GPU that
  * loads the library until the process exits).  It calls no allocator.
  *   b <= FP8MLA_NO_ALLOC_MAX_BATCH; a larger batch returns
  *   FP8MLA_ERR_WORKSPACE_TOO_SMALL and launches nothing.

@@ -86,10 +86,10 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [partial O | partial (m, l) | partial (q_hat - q) . O | per-row LSE correction |
-//             quantised Q (FP8 dots) | per-row Q scale]
+// Workspace: [partial O | partial (m, l) | quantised Q and its quantisation
+//             error (FP8 dots) | per-row Q scale]
 struct MlaWorkspace {
-  size_t o, ml, d, corr, qbuf, qscale, total;
+  size_t o, ml, qbuf, qscale, total;
 };
 
 MlaWorkspace mla_workspace_layout(int b, int num_units) {
@@ -97,9 +97,7 @@ MlaWorkspace mla_workspace_layout(int b, int num_units) {
   MlaWorkspace w;
   w.o = 0;
   w.ml = w.o + round_up(slots * kMlaRows * kMlaDV * sizeof(uint16_t), 256);
-  w.d = w.ml + round_up(slots * kMlaRows * sizeof(float2), 256);
-  w.corr = w.d + round_up(slots * kMlaRows * kMlaCorrTerms * sizeof(float), 256);
-  w.qbuf = w.corr + round_up(static_cast<size_t>(b) * kMlaRows * kMlaCorrTerms * sizeof(float), 256);
+  w.qbuf = w.ml + round_up(slots * kMlaRows * sizeof(float2), 256);
   w.qscale = w.qbuf + round_up(static_cast<size_t>(b) * kMlaQBytes, 256);
   w.total = w.qscale + round_up(static_cast<size_t>(b) * kMlaRows * sizeof(float), 256);
   return w;
@@ -187,8 +185,6 @@ fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dty
   prm.num_splits = num_splits;
   prm.ws_o = reinterpret_cast<uint16_t*>(ws + wl.o);
   prm.ws_ml = reinterpret_cast<float2*>(ws + wl.ml);
-  prm.ws_d = reinterpret_cast<float*>(ws + wl.d);
-  prm.ws_corr = reinterpret_cast<float*>(ws + wl.corr);
   prm.qbuf = reinterpret_cast<uint8_t*>(ws + wl.qbuf);
   prm.qscale = reinterpret_cast<float*>(ws + wl.qscale);
   prm.out = static_cast<uint16_t*>(out);
@@ -207,7 +203,7 @@ fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dty
     e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_decode_fp8(tm_lat, tm_rope, prm, num_units, s)
                                      : launch_mla_decode_16bit(tm_lat, tm_rope, prm, num_units, s);
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
-  if (launch_mla_combine(num_splits, prm.ws_o, prm.ws_ml, prm.ws_d, prm.ws_corr, dot_mode == FP8MLA_DOT_FP8 ? 1 : 0,
+  if (launch_mla_combine(num_splits, prm.ws_o, prm.ws_ml, dot_mode == FP8MLA_DOT_FP8 ? prm.qbuf : nullptr,
                          softmax_scale, prm.out, lse, b, s_q * h_q, s) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   return FP8MLA_OK;

@@ -201,13 +201,16 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
 // far, and every lane accumulates its 16 dv columns over the round's splits.
 // Partial slots are [slot][slot_rows] rows of dv = 512; with uniform_splits > 0
 // sequence bi owns slots [bi * uniform_splits, (bi + 1) * uniform_splits).
-// corr_terms (0 = none) is the number of LSE-correction shares each row or
-// slot row carries in ws_corr / ws_d (one per producer of a piece of the row).
+// The FP8-dot LSE correction lse -= softmax_scale (q_hat - q) . out comes
+// either from corr_terms shares each row or slot row carries in ws_corr / ws_d
+// (one per producer of a piece of the row; 0 = none), or, with qerr non-null,
+// from the row's stored quantisation error dotted with the finished output.
 template <bool kBf16>
 __global__ void __launch_bounds__(256) split_combine_kernel(
     const int32_t* __restrict__ num_splits, int uniform_splits, const void* __restrict__ ws_o_,
     const float2* __restrict__ ws_ml, const float* __restrict__ ws_d, const float* __restrict__ ws_corr, int corr_terms,
-    float softmax_scale, uint16_t* __restrict__ out, float* __restrict__ lse, int rows, int slot_rows) {
+    const uint8_t* __restrict__ qerr, size_t qerr_stride, float softmax_scale, uint16_t* __restrict__ out,
+    float* __restrict__ lse, int rows, int slot_rows) {
   const int bi = blockIdx.x;
   const int r = blockIdx.y * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -215,6 +218,23 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
   // for them), so they are read before waiting for the decode kernel itself.
   const int s0 = uniform_splits > 0 ? bi * uniform_splits : __ldg(num_splits + bi);
   const int ns = uniform_splits > 0 ? uniform_splits : __ldg(num_splits + bi + 1) - s0;
+  // The row's Q quantisation error (FP8 dots: q_hat qs - q as bf16), also
+  // final before the decode kernel started; this lane's 16 columns.
+  uint4 ev0 = make_uint4(0, 0, 0, 0), ev1 = ev0;
+  if (qerr != nullptr && r < rows) {
+    const uint4* e = reinterpret_cast<const uint4*>(qerr + bi * qerr_stride + static_cast<size_t>(r) * kMlaDV * 2) +
+                     lane * 2;
+    ev0 = __ldg(e);
+    ev1 = __ldg(e + 1);
+  }
+  // (q_hat - q) . o for this lane's 16 columns of an output row o
+  auto err_dot = [&](const float (&o)[16]) {
+    const uint32_t w[8] = {ev0.x, ev0.y, ev0.z, ev0.w, ev1.x, ev1.y, ev1.z, ev1.w};
+    float d = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d += bf16_lo(w[q]) * o[2 * q] + bf16_hi(w[q]) * o[2 * q + 1];
+    return d;
+  };
   griddep_wait();  // launched as a dependent of the decode kernel
   if (r >= rows) return;
   const size_t row = static_cast<size_t>(bi) * rows + r;
@@ -228,7 +248,25 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
     return c;
   };
   if (ns == 1) {
-    if (corr_terms > 0 && lane == 0) {
+    if (qerr != nullptr) {
+      // the LSE correction from the finished output row: lse -= scale (q_hat - q) . out
+      const uint4* orow4 = reinterpret_cast<const uint4*>(out + row * kMlaDV) + lane * 2;
+      const uint4 a = orow4[0], b2 = orow4[1];
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+      float o[16];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        o[2 * q] = bf16_lo(w[q]);
+        o[2 * q + 1] = bf16_hi(w[q]);
+      }
+      float d = err_dot(o);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      if (lane == 0) {
+        const float l = lse[row];
+        if (l != kNegInf) lse[row] = l - softmax_scale * d;
+      }
+    } else if (corr_terms > 0 && lane == 0) {
       const float c = corr_sum(ws_corr + static_cast<size_t>(corr_terms) * row);
       const float l = lse[row];
       if (l != kNegInf) lse[row] = l + c;
@@ -352,6 +390,15 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
     dq += __shfl_xor_sync(0xffffffffu, dq, o);
   }
   const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
+  if (qerr != nullptr) {  // the LSE correction from the merged output row
+    float o[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) o[c] = acc[c] * inv;
+    float d = err_dot(o);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    dq = d * big_l;  // the lse line below divides by big_l
+  }
   uint4 w0, w1;
   w0.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   w0.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
@@ -392,22 +439,26 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
 
 cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const void* ws_o, bool partials_bf16,
                                  const float2* ws_ml,
-                                 const float* ws_d, const float* ws_corr, int corr_terms, float softmax_scale,
+                                 const float* ws_d, const float* ws_corr, int corr_terms, const uint8_t* qerr,
+                                 size_t qerr_stride, float softmax_scale,
                                  uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
   dim3 grid(b, (rows + 7) / 8);
   if (partials_bf16)
     return launch_dependent(split_combine_kernel<true>, grid, dim3(256), 0, stream, num_splits, uniform_splits, ws_o,
-                            ws_ml, ws_d, ws_corr, corr_terms, softmax_scale, out, lse, rows, slot_rows);
+                            ws_ml, ws_d, ws_corr, corr_terms, qerr, qerr_stride, softmax_scale, out, lse, rows,
+                            slot_rows);
   return launch_dependent(split_combine_kernel<false>, grid, dim3(256), 0, stream, num_splits, uniform_splits, ws_o,
-                          ws_ml, ws_d, ws_corr, corr_terms, softmax_scale, out, lse, rows, slot_rows);
+                          ws_ml, ws_d, ws_corr, corr_terms, qerr, qerr_stride, softmax_scale, out, lse, rows,
+                          slot_rows);
 }
 
-cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml, const float* ws_d,
-                               const float* ws_corr, int apply_corr, float softmax_scale, uint16_t* out, float* lse,
-                               int b, int rows, cudaStream_t stream) {
-  return launch_split_combine(num_splits, 0, ws_o, true, ws_ml, ws_d, ws_corr, apply_corr ? kMlaCorrTerms : 0,
-                              softmax_scale, out, lse, b, rows, kMlaRows, stream);
+cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,
+                               const uint8_t* qbuf, float softmax_scale, uint16_t* out, float* lse, int b, int rows,
+                               cudaStream_t stream) {
+  return launch_split_combine(num_splits, 0, ws_o, true, ws_ml, nullptr, nullptr, 0,
+                              qbuf != nullptr ? qbuf + kMlaQErrOff : nullptr, kMlaQBytes, softmax_scale, out, lse, b,
+                              rows, kMlaRows, stream);
 }
 
 uint32_t metadata_read_and_clear_status() {

@@ -72,65 +72,32 @@ constexpr int kSoftmaxThreads = 256;                // two threads per query row
 constexpr int kLatBox = kPage * 128;                 // one 128-byte column slice of a page (8 KB)
 constexpr uint32_t kPageTxBytes = kPage * kD;        // bytes one page's TMA loads deliver
 
-template <bool kFp8>
-struct Cfg;
-
-template <>
-struct Cfg<true> {  // FP8 Q/P dots
-  static constexpr int kParts = 2, kDvPart = 256, kStages = 3;
-  static constexpr int kThreads = 512;               // + 4 Q-staging warps
-  static constexpr bool kStageQ = true;              // next segment's Q is prepared ahead, in shared memory
-  static constexpr float kPScale = 128.0f, kPLog2 = 7.0f, kTau = 1.0f;
-  static constexpr int kOffRope8 = 4 * kLatBox;      // 64 tokens x 64 E4M3 bytes, no swizzle
-  static constexpr int kOffCvt = kOffRope8 + kPage * 64;   // RoPE as bf16, 128 B swizzle
-  static constexpr int kStageBytes = kOffCvt + kLatBox;
-  static constexpr uint32_t kTO = 0, kTS = 256, kTP = 320, kTQ = 352, kTQR = 480;
-};
-
-template <>
-struct Cfg<false> {  // 16-bit dots
+// 16-bit dots (exact): 4 CTAs per unit, each owning a 128-column slice of dv.
+struct Cfg16 {
   static constexpr int kParts = 4, kDvPart = 128, kStages = 2;
   static constexpr int kThreads = 384;
-  static constexpr bool kStageQ = false;
   static constexpr float kPScale = 1.0f, kPLog2 = 0.0f, kTau = 8.0f;
   static constexpr int kOffRope8 = 4 * kLatBox;
   static constexpr int kOffCvt = kOffRope8 + kPage * 64;  // 9 bf16 boxes: 8 latent + RoPE
   static constexpr int kStageBytes = kOffCvt + 9 * kLatBox;
   static constexpr uint32_t kTO = 0, kTS = 128, kTP = 192, kTQ = 224, kTQR = 224 + 256;
 };
+static_assert(Cfg16::kOffCvt % 1024 == 0 && Cfg16::kStageBytes % 1024 == 0, "1 KB aligned tiles");
 
-static_assert(Cfg<true>::kOffCvt % 1024 == 0 && Cfg<true>::kStageBytes % 1024 == 0, "1 KB aligned tiles");
-static_assert(Cfg<false>::kOffCvt % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0, "1 KB aligned tiles");
-
-// Staged Q (FP8 dots): per query row 512 E4M3 latent bytes + 64 bf16 RoPE values
-// (already divided by the row's power-of-two scale), rows padded to 656 bytes
-// so that a warp's 16-byte row reads hit distinct banks; then one float qs per row.
-constexpr int kQStageRow = 656;
-constexpr int kQStageBytes = kRows * kQStageRow + kRows * 4;
-
-template <bool kFp8>
-struct Barriers {
-  uint64_t kv_full[Cfg<kFp8>::kStages];
-  uint64_t kv_empty[Cfg<kFp8>::kStages];
-  uint64_t cvt_ready[Cfg<kFp8>::kStages];
+struct Barriers16 {
+  uint64_t kv_full[Cfg16::kStages];
+  uint64_t kv_empty[Cfg16::kStages];
+  uint64_t cvt_ready[Cfg16::kStages];
   uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma;
   uint64_t xchg;            // softmax-group exchange barrier (all 256 softmax threads arrive)
-  uint64_t qst_full;        // staged Q of the next segment is ready (128 Q-staging threads arrive)
-  uint64_t qst_free;        // staged Q was copied into TMEM (256 softmax threads arrive)
   uint32_t tmem_base;
   uint32_t abort_flag;
   uint32_t cvt_ok;
   float xmax[2][2][kRows];  // per-page tile max of each row half, double-buffered by page parity
-  float xamax[2][kRows];    // Q amax halves
   float xsum[2][kRows];     // row-sum halves
-  float xdq[2][kRows];      // LSE-correction halves
 };
 
-template <bool kFp8>
-constexpr size_t smem_bytes() {
-  return Cfg<kFp8>::kStages * Cfg<kFp8>::kStageBytes + (Cfg<kFp8>::kStageQ ? kQStageBytes : 0) +
-         sizeof(Barriers<kFp8>) + 1024;
-}
+constexpr size_t smem_bytes16() { return Cfg16::kStages * Cfg16::kStageBytes + sizeof(Barriers16) + 1024; }
 
 // One (sequence, page range) piece of a unit's work.
 struct Segment {
@@ -195,24 +162,16 @@ __device__ __forceinline__ float absmax_bf16x8(uint4 v) {
                fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))), fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
 }
 
-// x -> E4M3(x * inv_qs) * qs - x: the in-kernel quantisation error of one Q element.
-__device__ __forceinline__ float2 q_quant_error(uint32_t bf16x2, float inv_qs, float qs) {
-  const float x0 = bf16_lo(bf16x2), x1 = bf16_hi(bf16x2);
-  const uint32_t h = e4m3x2_to_f16x2(pack_e4m3x2(x0 * inv_qs, x1 * inv_qs));
-  return make_float2(f16_lo(h) * qs - x0, f16_hi(h) * qs - x1);
-}
-
-template <bool kFp8>
-__global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
-                      const MlaParams prm) {
-  using C = Cfg<kFp8>;
+// Dense MLA decode with 16-bit dots: Q and every page converted to bf16
+// (exact), bf16 MMAs; the reference for the FP8-dot kernel's rounding.
+__global__ void __launch_bounds__(Cfg16::kThreads, 1)
+    mla_decode_16bit_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                            const MlaParams prm) {
+  using C = Cfg16;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* qstage = smem + C::kStages * C::kStageBytes;  // FP8 dots only
-  Barriers<kFp8>* bars =
-      reinterpret_cast<Barriers<kFp8>*>(qstage + (C::kStageQ ? kQStageBytes : 0));
+  Barriers16* bars = reinterpret_cast<Barriers16*>(smem + C::kStages * C::kStageBytes);
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -233,8 +192,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->xchg, kSoftmaxThreads / 32);
-    mbar_init(&bars->qst_full, kRows / 32);
-    mbar_init(&bars->qst_free, kSoftmaxThreads / 32);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -251,58 +208,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   griddep_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
 
-  if constexpr (C::kStageQ) {
-    // The unit's first Q is staged by all 512 threads at once (eight per row,
-    // 72 values each, two rounds of 64 rows) so the first Q.K^T starts early;
-    // the Q-staging warps take over from the second segment on.
-    SegmentWalker first(prm, unit);
-    Segment sg0;
-    if (first.next(sg0)) {
-      const int R = prm.s_q * prm.h_q;
-      const int part = threadIdx.x % 8;  // values [72 part, 72 part + 72) of the row
-#pragma unroll 1
-      for (int round = 0; round < 2; ++round) {
-        const int r = round * 64 + threadIdx.x / 8;
-        const uint16_t* qrow = prm.q + (static_cast<size_t>(sg0.b) * R + r) * kD + part * 72;
-        uint4 v[9];
-        float amax = 0.f;
-#pragma unroll
-        for (int c = 0; c < 9; ++c) {
-          v[c] = (r < R) ? __ldg(reinterpret_cast<const uint4*>(qrow) + c) : make_uint4(0, 0, 0, 0);
-          amax = fmaxf(amax, absmax_bf16x8(v[c]));
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-        const int qe = pow2_scale_exponent(amax);
-        const float inv_qs = exp2i(-qe);
-        uint8_t* row = qstage + r * kQStageRow;
-        const int nlat = (part < 7) ? 9 : 1;  // chunks of 8 latent values in this part
-#pragma unroll
-        for (int c = 0; c < 9; ++c) {
-          const uint4 a = v[c];
-          if (c < nlat) {  // 8 latent values -> 8 E4M3 bytes
-            uint2 o;
-            o.x = pack_e4m3x4(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs, bf16_lo(a.y) * inv_qs,
-                              bf16_hi(a.y) * inv_qs);
-            o.y = pack_e4m3x4(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs, bf16_lo(a.w) * inv_qs,
-                              bf16_hi(a.w) * inv_qs);
-            *reinterpret_cast<uint2*>(row + part * 72 + 8 * c) = o;
-          } else {  // RoPE: 8 values -> 16 bytes of bf16 / qs
-            uint4 o;
-            o.x = pack_bf16x2(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs);
-            o.y = pack_bf16x2(bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs);
-            o.z = pack_bf16x2(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs);
-            o.w = pack_bf16x2(bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
-            *reinterpret_cast<uint4*>(row + kDLat + 16 * (c - 1)) = o;
-          }
-        }
-        if (part == 0) reinterpret_cast<float*>(qstage + kRows * kQStageRow)[r] = exp2i(qe);
-      }
-    }
-    __syncthreads();
-    if (warp >= 12) warp_arrive(&bars->qst_full);  // phase 0 of the staging barrier: the first segment
-  }
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
@@ -366,20 +271,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       bool ok = true;
 
       auto issue_qk = [&](uint32_t sb) {
-        if constexpr (kFp8) {
-          constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);   // e4m3 x e4m3, both K-major
-          constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);  // bf16 x bf16
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const uint64_t bd = make_sdesc(sb + (kk >> 2) * kLatBox + (kk & 3) * 32, 16, 1024, SWIZZLE_128B);
-            mma_f8_ts(t_s, tmem + C::kTQ + kk * 8, bd, idesc8, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = make_sdesc(sb + C::kOffCvt + kk * 32, 16, 1024, SWIZZLE_128B);
-            mma_f16_ts(t_s, tmem + C::kTQR + kk * 8, bd, idesc16, 1u);
-          }
-        } else {
+        {
           constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);
 #pragma unroll
           for (int kk = 0; kk < 36; ++kk) {
@@ -395,15 +287,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         tc_fence_after();
         const int st = j % C::kStages;
         const uint32_t sb = smem_u32(smem + st * C::kStageBytes);
-        if constexpr (kFp8) {
-          constexpr uint32_t idesc = make_idesc(0, 0, 0, 1, 256, 128);   // e4m3, B MN-major, N = 256
-          const uint32_t v_base = sb + part * 2 * kLatBox;
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t bd = make_sdesc(v_base + kk * 4096, kLatBox, 1024, SWIZZLE_128B);
-            mma_f8_ts(t_o, tmem + C::kTP + kk * 8, bd, idesc, (first_in_seg && kk == 0) ? 0u : 1u);
-          }
-        } else {
+        {
           constexpr uint32_t idesc = make_idesc(1, 1, 0, 1, 128, 128);   // bf16, B MN-major, N = 128
           const uint32_t v_base = sb + C::kOffCvt + part * 2 * kLatBox;
 #pragma unroll
@@ -466,10 +350,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         const bool dead = (pg == sg.n - 1) && (t >= sg.s_k - pg * kPage);  // slot past the sequence end
         const uint4 z = make_uint4(0, 0, 0, 0);
         const int sw = t & 7;
-        // RoPE bytes -> bf16 (box C::kOffCvt + (kFp8 ? 0 : 8 boxes))
+        // RoPE bytes -> bf16 (box C::kOffCvt + (8 boxes))
         {
           const uint4* src = reinterpret_cast<const uint4*>(sb + C::kOffRope8 + t * 64);
-          uint8_t* dst = sb + C::kOffCvt + (kFp8 ? 0 : 8 * kLatBox) + t * 128;
+          uint8_t* dst = sb + C::kOffCvt + 8 * kLatBox + t * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint4 lo = z, hi = z;
@@ -484,16 +368,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
           }
         }
-        if constexpr (kFp8) {
-          if (dead) {  // zero the slot's V row (all four 128-byte slices)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4* row = reinterpret_cast<uint4*>(sb + j * kLatBox + t * 128);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) row[c] = z;
-            }
-          }
-        } else {
+        {
           // latent: raw box j chunk c (16 E4M3) -> bf16 box 2j + c/4, chunks 2(c%4), 2(c%4)+1
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
@@ -519,65 +394,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         if (t == 0) mbar_arrive(&bars->cvt_ready[st]);
       }
     }
-  } else if (warp >= 12) {
-    // ---------------- Q staging (FP8 dots): one thread per query row ----
-    // Quantises the Q row of every segment, in order, into shared memory
-    // while the previous segment streams: latent -> E4M3(q / qs), RoPE ->
-    // bf16(q / qs), qs = smallest power of two with amax <= 448 qs.
-    if constexpr (C::kStageQ) {
-      const int r = threadIdx.x - 384;
-      const int R = prm.s_q * prm.h_q;
-      uint8_t* row = qstage + r * kQStageRow;
-      float* qs_arr = reinterpret_cast<float*>(qstage + kRows * kQStageRow);
-      SegmentWalker walk(prm, unit);
-      Segment sg;
-      int seg_i = 1;
-      walk.next(sg);  // the first segment was staged by the whole CTA
-      while (walk.next(sg)) {
-        const uint16_t* qrow = prm.q + (static_cast<size_t>(sg.b) * R + r) * kD;
-        float amax = 0.f;
-        if (r < R) {
-          const uint4* q4 = reinterpret_cast<const uint4*>(qrow);
-#pragma unroll 12
-          for (int c = 0; c < kD / 8; ++c) amax = fmaxf(amax, absmax_bf16x8(__ldg(q4 + c)));
-        }
-        const int qe = pow2_scale_exponent(amax);
-        const float inv_qs = exp2i(-qe);
-        // the staging buffer holds one segment: wait until the previous one was copied out
-        if (!warp_wait(&bars->qst_free, (seg_i - 1) & 1, abort_flag)) break;
-        const uint4* q4 = reinterpret_cast<const uint4*>(qrow);
-#pragma unroll 4
-        for (int c = 0; c < kDLat / 16; ++c) {  // 16 latent values -> one 16-byte chunk
-          uint4 a = make_uint4(0, 0, 0, 0), b2 = a;
-          if (r < R) {
-            a = __ldg(q4 + 2 * c);
-            b2 = __ldg(q4 + 2 * c + 1);
-          }
-          uint4 o;
-          o.x = pack_e4m3x4(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs, bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs);
-          o.y = pack_e4m3x4(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs, bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
-          o.z = pack_e4m3x4(bf16_lo(b2.x) * inv_qs, bf16_hi(b2.x) * inv_qs, bf16_lo(b2.y) * inv_qs,
-                            bf16_hi(b2.y) * inv_qs);
-          o.w = pack_e4m3x4(bf16_lo(b2.z) * inv_qs, bf16_hi(b2.z) * inv_qs, bf16_lo(b2.w) * inv_qs,
-                            bf16_hi(b2.w) * inv_qs);
-          *reinterpret_cast<uint4*>(row + 16 * c) = o;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {  // 8 RoPE values -> one 16-byte chunk of bf16
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (r < R) v = __ldg(q4 + kDLat / 8 + c);
-          uint4 o;
-          o.x = pack_bf16x2(bf16_lo(v.x) * inv_qs, bf16_hi(v.x) * inv_qs);
-          o.y = pack_bf16x2(bf16_lo(v.y) * inv_qs, bf16_hi(v.y) * inv_qs);
-          o.z = pack_bf16x2(bf16_lo(v.z) * inv_qs, bf16_hi(v.z) * inv_qs);
-          o.w = pack_bf16x2(bf16_lo(v.w) * inv_qs, bf16_hi(v.w) * inv_qs);
-          *reinterpret_cast<uint4*>(row + kDLat + 16 * c) = o;
-        }
-        qs_arr[r] = exp2i(qe);
-        warp_arrive(&bars->qst_full);  // release: the row is visible to whoever waits on this phase
-        ++seg_i;
-      }
-    }
   } else {
     // ------------------ softmax / Q prep / epilogue (8 warps, 2 per row) ----
     const int hf = (warp - 4) / 4;                          // which half of the row
@@ -598,46 +414,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     SegmentWalker walk(prm, unit);
     Segment sg;
     int i = 0;
-    int seg_ph = 0;  // segments consumed from the Q staging buffer
     while (walk.next(sg)) {
       const uint16_t* qrow = prm.q + (static_cast<size_t>(sg.b) * R + r) * kD;
-      float c_row, qs = 1.f, inv_qs = 1.f;
-      if constexpr (kFp8) {
-        // ---- Q: copy this half of the staged row into TMEM ----
-        // latent bytes [256 hf, 256 hf + 256) -> columns 64 hf ..; RoPE values [32 hf, 32 hf + 32)
-        if (!warp_wait(&bars->qst_full, seg_ph & 1, abort_flag)) break;
-        const uint8_t* row = qstage + r * kQStageRow;
-        qs = reinterpret_cast<const float*>(qstage + kRows * kQStageRow)[r];
-        inv_qs = 1.0f / qs;  // a power of two: exact
-        c_row = prm.softmax_scale * kLog2e * qs * kv_scale;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t pk[16];
-          const uint4* src = reinterpret_cast<const uint4*>(row + 256 * hf + 64 * ch);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 v = src[c];
-            pk[4 * c + 0] = v.x;
-            pk[4 * c + 1] = v.y;
-            pk[4 * c + 2] = v.z;
-            pk[4 * c + 3] = v.w;
-          }
-          tmem_st16(lane_base + C::kTQ + (4 * hf + ch) * 16, pk);
-        }
-        uint32_t pk[16];
-        const uint4* src = reinterpret_cast<const uint4*>(row + kDLat + 64 * hf);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = src[c];
-          pk[4 * c + 0] = v.x;
-          pk[4 * c + 1] = v.y;
-          pk[4 * c + 2] = v.z;
-          pk[4 * c + 3] = v.w;
-        }
-        tmem_st16(lane_base + C::kTQR + 16 * hf, pk);
-        warp_arrive(&bars->qst_free);  // the staging row may be overwritten with the next segment's
-        ++seg_ph;
-      } else {
+      float c_row;
+      {
         // ---- Q preparation: bf16 as is; 64-value chunks 0-4 (hf 0) or 5-8 (hf 1) ----
         c_row = prm.softmax_scale * kLog2e * kv_scale;
 #pragma unroll 1
@@ -676,13 +456,6 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       float m_run = kNegInf, l_run = 0.f;  // l_run sums the scaled p (2^kPLog2 p)
       bool ok = true;
       for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
-        if constexpr (kFp8) {  // the epilogue's LSE correction re-reads these Q columns
-          if (pg == sg.hi - 1 && r < R) {
-            const char* qc = reinterpret_cast<const char*>(qrow + part * C::kDvPart + hf * kOHalf);
-            prefetch_l2(qc);
-            prefetch_l2(qc + 128);
-          }
-        }
         if (!warp_wait(&bars->s_full, i & 1, abort_flag)) {
           ok = false;
           break;
@@ -724,7 +497,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         }
         const float bias = (m_run == kNegInf) ? 0.f : (C::kPLog2 - m_run);
         float sum = 0.f;
-        uint32_t pk[kFp8 ? 8 : 16];
+        uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
@@ -732,9 +505,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
           const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
           sum += (p0 + p1) + (p2 + p3);
-          if constexpr (kFp8) {
-            pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
-          } else {
+          {
             pk[c / 2] = pack_bf16x2(p0, p1);
             pk[c / 2 + 1] = pack_bf16x2(p2, p3);
           }
@@ -759,10 +530,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             tmem_st32(lane_base + col, o);
           }
         }
-        if constexpr (kFp8)
-          tmem_st8(lane_base + C::kTP + 8 * hf, pk);
-        else
-          tmem_st16(lane_base + C::kTP + 16 * hf, pk);
+        tmem_st16(lane_base + C::kTP + 16 * hf, pk);
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(&bars->p_full);
@@ -780,33 +548,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
       const int col0 = part * C::kDvPart + hf * kOHalf;
       const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
-      float dq_dot = 0.f;  // sum over this thread's columns of (q_hat - q) * O (FP8 dots only)
 #pragma unroll 1
       for (int ch = 0; ch < kOHalf / 32; ++ch) {
-        uint4 qv[4];  // this chunk's Q (prefetched into L2 during the last page), loaded beside O
-        if constexpr (kFp8) {
-          if (r < R) {
-            const uint4* q4 = reinterpret_cast<const uint4*>(qrow + col0 + ch * 32);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) qv[c] = __ldg(q4 + c);
-          }
-        }
         uint32_t o[32];
         tmem_ld32(lane_base + C::kTO + hf * kOHalf + ch * 32, o);
         tmem_ld_wait();
         if (r >= R) continue;
-        if constexpr (kFp8) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 v = qv[c];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 e = q_quant_error(w[k], inv_qs, qs);
-              dq_dot += e.x * __uint_as_float(o[8 * c + 2 * k]) + e.y * __uint_as_float(o[8 * c + 2 * k + 1]);
-            }
-          }
-        }
         if (whole) {
           uint4* dst = reinterpret_cast<uint4*>(prm.out + (static_cast<size_t>(sg.b) * R + r) * kDV + col0 + ch * 32);
 #pragma unroll
@@ -831,20 +578,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
         }
       }
-      if constexpr (kFp8) {
-        bars->xdq[hf][r] = dq_dot;
-        if (!xsync()) break;
-        dq_dot = bars->xdq[0][r] + bars->xdq[1][r];
-      }
       if (r < R && hf == 0) {
         const size_t row = static_cast<size_t>(sg.b) * R + r;
         if (whole) {
           if (part == 0) prm.lse[row] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
-          if constexpr (kFp8) prm.ws_corr[row * 2 + part] = -prm.softmax_scale * dq_dot * f;
         } else {
           const size_t srow = static_cast<size_t>(slot) * kRows + r;
           if (part == 0) prm.ws_ml[srow] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
-          if constexpr (kFp8) prm.ws_d[srow * 2 + part] = dq_dot * f;
         }
       }
     }
@@ -897,9 +637,9 @@ constexpr int kQLatSlotBytes = kRows * kQLatPitch;
 constexpr int kQRopeSlotBytes = kRows * kQRopePitch;
 static_assert(kQLatSlotBytes <= kStageBytes && kQRopeSlotBytes <= kStageBytes, "a Q slot fits one stage");
 // After the slots: the latent quantisation error q_hat qs - q, 128 rows x 512
-// bf16, read by the epilogue for the LSE correction.
+// bf16, read by the combine kernel for the LSE correction.
 constexpr int kQErrOff = 2 * kQLatSlotBytes + kQRopeSlotBytes;
-static_assert(kQErrOff + kRows * kDLat * 2 == kMlaQBytes, "quantised-Q layout");
+static_assert(kQErrOff == kMlaQErrOff && kQErrOff + kRows * kDLat * 2 == kMlaQBytes, "quantised-Q layout");
 static_assert(kStageBytes % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
               "1 KB aligned tiles");
 static_assert(kStageBytes == static_cast<int>(kPageTxBytes), "a page fills one stage");
@@ -1213,10 +953,10 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           for (int q = 0; q < 3; ++q) mbar_arrive(&bars->kv_empty[(k + q) % kStages]);
         __syncwarp();
         k += 3;
-        // Page i's inputs are waited for before the P.V of page i - 2 (so that
-        // Q.K^T(i) follows that P.V in the tensor pipe without a gap).  S buffer
-        // i % 2 last held page i - 2, whose P (written after its S was read) that
-        // P.V waited for -- or the previous segment's flush did.
+        // Page i's conversion is waited for while the P.V of page i - 2 runs (so
+        // that Q.K^T(i) follows that P.V in the tensor pipe without a gap).  S
+        // buffer i % 2 last held page i - 2, whose P (written after its S was
+        // read) that P.V waited for -- or the previous segment's flush did.
         if (!warp_spin(&bars->cvt_ready[k % kStages], (k / kStages) & 1, abort_flag)) {
           ok = false;
           break;
@@ -1244,13 +984,14 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           __syncwarp();
           const uint32_t e = static_cast<uint32_t>(st) | ((pg == sg.lo) ? 8u : 0u);
           pend = (pend & ~(0xFFu << (8 * (i & 3)))) | (e << (8 * (i & 3)));
-          // the next page's conversion, then the P.V of the previous page
-          if (pg + 1 < sg.hi &&
-              !warp_spin(&bars->cvt_ready[(k + 1) % kStages], ((k + 1) / kStages) & 1, abort_flag)) {
+          // the P.V of the previous page (queued right behind this Q.K^T), then
+          // the next page's conversion while that P.V runs
+          if (pg > sg.lo && !issue_pv()) {  // j == i - 1 here
             ok = false;
             break;
           }
-          if (pg > sg.lo && !issue_pv()) {  // j == i - 1 here
+          if (pg + 1 < sg.hi &&
+              !warp_spin(&bars->cvt_ready[(k + 1) % kStages], ((k + 1) / kStages) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -1399,9 +1140,6 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       Segment nx;
       const bool has_next = peek.next(nx);
       const int k_next = k + 3 + (sg.hi - sg.lo);
-      // the segment's latent quantisation errors (bf16, rows of 512), for the LSE correction
-      const uint16_t* ebase =
-          reinterpret_cast<const uint16_t*>(prm.qbuf + static_cast<size_t>(sg.b) * kMlaQBytes + kQErrOff);
       const int col0 = part * 256 + hf * kOHalf;  // this thread's O columns
       // keys visible to this row (bottom-right causal alignment); pages wholly
       // below every row's limit need no mask
@@ -1410,11 +1148,6 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       const int min_visible = prm.causal ? (sg.s_k - prm.s_q + 1) : sg.s_k;
       float m_run = kNegInf, l_run = 0.f;  // l_run sums the stored-scale p (kPScale p)
       for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
-        if (pg == sg.hi - 1) {  // the epilogue's LSE correction re-reads these Q columns
-          const char* qc = reinterpret_cast<const char*>(ebase + static_cast<size_t>(r) * kDLat + col0);
-          prefetch_l2(qc);
-          prefetch_l2(qc + 128);
-        }
         const int sbuf = i & 1;
         if (!warp_spin(&bars->s_full[sbuf], (i >> 1) & 1, abort_flag)) {
           ok = false;
@@ -1511,21 +1244,6 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       if (!ok) break;
 
       // ---- epilogue: O is final once the segment's last P.V completes ----
-      // Output pass over this thread's 128 O columns, 32 at a time.  A thread
-      // holds one row; groups of four lanes transpose their 16-byte pieces so
-      // that each store writes 64-byte runs of rows, and in that layout the
-      // same lanes read the matching 16-byte pieces of the quantisation errors
-      // (coalesced) for the LSE correction's dot product with the output.
-      const int row0 = (warp % 4) * 32;  // first row of this warp
-      const int grow = row0 + (lane & ~3);  // the group's first row
-      auto load_err = [&](int ch, uint4 (&ev)[4]) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          ev[kk] = __ldg(reinterpret_cast<const uint4*>(ebase + static_cast<size_t>(grow + kk) * kDLat + col0 + ch * 32 +
-                                                        8 * (lane & 3)));
-      };
-      uint4 ev[4];
-      load_err(0, ev);  // in flight across the row-sum exchange and the last P.V's wait
       bars->xsum[hf][r] = l_run;
       if (!xsync()) break;
       const float l_tot = (bars->xsum[0][r] + bars->xsum[1][r]) * (1.0f / kPScale);  // sum of p
@@ -1535,16 +1253,17 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
       if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag)) break;
       tc_fence_after();
-      // a whole sequence goes straight to out; a piece to its bf16 partial slot
+      // O out as bf16, 32 columns at a time.  A thread holds one row; groups of
+      // four lanes transpose their 16-byte pieces so that each store writes
+      // 64-byte runs of rows.  A whole sequence goes straight to out, a piece
+      // to its bf16 partial slot; the combine kernel adds the LSE correction.
+      const int grow = (warp % 4) * 32 + (lane & ~3);  // the lane group's first row
       uint16_t* obase = whole ? prm.out + static_cast<size_t>(sg.b) * R * kDV
                               : prm.ws_o + static_cast<size_t>(slot) * kRows * kDV;
-      float dqk[4] = {0.f, 0.f, 0.f, 0.f};  // (q_hat - q) . O f for rows grow + kk, over this lane's pieces
 #pragma unroll 1
       for (int ch = 0; ch < kOHalf / 32; ++ch) {
         uint32_t o[32];
         tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
-        uint4 en[4];  // the next chunk's errors, in flight while this chunk is processed
-        if (ch + 1 < kOHalf / 32) load_err(ch + 1, en);
         tmem_ld_wait();
         uint4 pc[4];
 #pragma unroll
@@ -1556,38 +1275,16 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         }
         lane_group_transpose<4>(pc, lane);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t a4[4] = {pc[kk].x, pc[kk].y, pc[kk].z, pc[kk].w};
-          const uint32_t e4[4] = {ev[kk].x, ev[kk].y, ev[kk].z, ev[kk].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dqk[kk] += bf16_lo(e4[q]) * bf16_lo(a4[q]) + bf16_hi(e4[q]) * bf16_hi(a4[q]);
+        for (int kk = 0; kk < 4; ++kk)
           if (grow + kk < R)
             *reinterpret_cast<uint4*>(obase + static_cast<size_t>(grow + kk) * kDV + col0 + ch * 32 + 8 * (lane & 3)) =
                 pc[kk];
-        }
-        if (ch + 1 < kOHalf / 32) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) ev[kk] = en[kk];
-        }
       }
-      // sum each row's share over its group's four lanes; lane q keeps row grow + q (its own)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        dqk[kk] += __shfl_xor_sync(0xffffffffu, dqk[kk], 1);
-        dqk[kk] += __shfl_xor_sync(0xffffffffu, dqk[kk], 2);
-      }
-      const int q4 = lane & 3;
-      const float dq_out = q4 == 0 ? dqk[0] : q4 == 1 ? dqk[1] : q4 == 2 ? dqk[2] : dqk[3];
-      if (r < R) {  // each (dv slice, row half) publishes its own share of the correction
-        const size_t row = static_cast<size_t>(sg.b) * R + r;
+      if (r < R && part == 0 && hf == 0) {  // the row's (uncorrected) LSE, or the piece's (m, l)
         if (whole) {
-          if (part == 0 && hf == 0) prm.lse[row] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
-          prm.ws_corr[row * 4 + part * 2 + hf] = -prm.softmax_scale * dq_out;
+          prm.lse[static_cast<size_t>(sg.b) * R + r] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
         } else {
-          const size_t srow = static_cast<size_t>(slot) * kRows + r;
-          if (part == 0 && hf == 0) prm.ws_ml[srow] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
-          prm.ws_d[srow * 4 + part * 2 + hf] = dq_out;
+          prm.ws_ml[static_cast<size_t>(slot) * kRows + r] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
         }
       }
       if (!has_next) break;
@@ -1605,41 +1302,42 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
   }
 }
 
-template <bool kFp8>
-cudaError_t launch(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
-                   cudaStream_t stream) {
+cudaError_t launch_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
+                       cudaStream_t stream) {
   static bool configured = false;
-  if constexpr (kFp8) {
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(f8::smem_bytes()));
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
-    return launch_dependent(mla_fp8_kernel, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream,
-                            tm_lat, tm_rope, prm);
-  } else {
-    if (!configured) {
-      cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem_bytes<kFp8>()));
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
-    return launch_dependent(mla_decode_kernel<kFp8>, dim3(num_units * Cfg<kFp8>::kParts), dim3(Cfg<kFp8>::kThreads),
-                            smem_bytes<kFp8>(), stream, tm_lat, tm_rope, prm);
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(f8::smem_bytes()));
+    if (e != cudaSuccess) return e;
+    configured = true;
   }
+  return launch_dependent(mla_fp8_kernel, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream, tm_lat,
+                          tm_rope, prm);
+}
+
+cudaError_t launch_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
+                         cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_16bit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes16()));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return launch_dependent(mla_decode_16bit_kernel, dim3(num_units * Cfg16::kParts), dim3(Cfg16::kThreads),
+                          smem_bytes16(), stream, tm_lat, tm_rope, prm);
 }
 
 }  // namespace mla
 
 cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                   int num_units, cudaStream_t stream) {
-  return mla::launch<true>(tm_lat, tm_rope, prm, num_units, stream);
+  return mla::launch_fp8(tm_lat, tm_rope, prm, num_units, stream);
 }
 
 cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                     int num_units, cudaStream_t stream) {
-  return mla::launch<false>(tm_lat, tm_rope, prm, num_units, stream);
+  return mla::launch_16bit(tm_lat, tm_rope, prm, num_units, stream);
 }
 
 cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream) {

@@ -17,8 +17,6 @@ struct MlaParams {
   const int32_t* num_splits;   // [b + 1]
   uint16_t* ws_o;              // [slots, 128, 512] partial accumulators as bf16 (true units)
   float2* ws_ml;               // [slots, 128] (m in log2 units, l)
-  float* ws_d;                 // [slots, 128, 4] sum of (q_hat - q) * O_partial per (dv slice, row half) (FP8 dots)
-  float* ws_corr;              // [b, 128, 4] -softmax_scale * (q_hat - q) . out per (dv slice, row half) (FP8 dots)
   uint8_t* qbuf;               // [b, kMlaQBytes] Q quantised for FP8 dots, in the kernel's slot layout
   float* qscale;               // [b, 128] per-row power-of-two Q scale (FP8 dots)
   uint16_t* out;               // bf16 [b, s_q, h_q, 512]
@@ -35,11 +33,11 @@ constexpr int kMlaDV = 512;
 constexpr int kMlaPage = 64;
 constexpr int kMlaD = 576;
 constexpr int kSchedFixedCost = 4;
-constexpr int kMlaCorrTerms = 4;  // LSE-correction shares per row: 2 dv slices x 2 row halves
 // One sequence's quantised Q, in the decode kernel's ring-slot layout (two
 // latent slots of 128 x 272 bytes, one RoPE slot of 128 x 144 bytes), then
 // the latent quantisation error (q_hat qs - q) as 128 x 512 bf16.
 constexpr int kMlaQBytes = 219136;
+constexpr int kMlaQErrOff = 88064;  // offset of the quantisation error inside one sequence's block
 constexpr size_t kMetadataMaxSmem = 200 * 1024;  // the scheduler stages ~16 bytes per sequence and unit
 size_t metadata_smem_bytes(int b, int num_units);
 
@@ -56,17 +54,21 @@ cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream);
 // metadata + combine (metadata.cu)
 cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, int force_splits, int32_t* tile_sched,
                                 int32_t* num_splits, cudaStream_t stream);
-// Merges split partials into out / lse, and (FP8 dots, apply_corr) applies the
-// first-order Q-quantisation correction to every row's LSE.
-cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml, const float* ws_d,
-                               const float* ws_corr, int apply_corr, float softmax_scale, uint16_t* out, float* lse,
-                               int b, int rows, cudaStream_t stream);
+// Merges split partials into out / lse, and (FP8 dots: qbuf, the quantised Q
+// blocks, non-null) applies the first-order Q-quantisation correction to every
+// row's LSE from the finished output row and the stored quantisation error.
+cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,
+                               const uint8_t* qbuf, float softmax_scale, uint16_t* out, float* lse, int b, int rows,
+                               cudaStream_t stream);
 // The same merge for any variant whose partial slots hold slot_rows rows of dv = 512
-// (fp32, or bf16 when partials_bf16); each row carries corr_terms LSE-correction
-// shares (0: none).
+// (fp32, or bf16 when partials_bf16).  The LSE correction comes either from
+// corr_terms shares per row or piece (ws_corr / ws_d; 0: none) or, with qerr
+// non-null, from the quantisation error rows (bf16 x 512) of sequence i at
+// qerr + i * qerr_stride.
 cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const void* ws_o, bool partials_bf16,
                                  const float2* ws_ml,
-                                 const float* ws_d, const float* ws_corr, int corr_terms, float softmax_scale,
+                                 const float* ws_d, const float* ws_corr, int corr_terms, const uint8_t* qerr,
+                                 size_t qerr_stride, float softmax_scale,
                                  uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream);
 uint32_t metadata_read_and_clear_status();
 

@@ -20,10 +20,9 @@ namespace {
 constexpr int kNoAllocMaxBatch = FP8MLA_NO_ALLOC_MAX_BATCH;
 constexpr size_t kSchedBytes = 256 * 8 * sizeof(int32_t);                         // tile schedule, <= 256 units
 constexpr size_t kSplitsBytes = 256 * sizeof(int32_t);                            // split prefix, <= 255 sequences
-constexpr size_t kCorrBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaRows * kMlaCorrTerms * sizeof(float);
 constexpr size_t kQBufBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaQBytes;    // quantised Q
 constexpr size_t kQScaleBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaRows * sizeof(float);
-constexpr size_t kScratchBytes = kSchedBytes + kSplitsBytes + kCorrBytes + kQBufBytes + kQScaleBytes;  // 14.2 MB
+constexpr size_t kScratchBytes = kSchedBytes + kSplitsBytes + kQBufBytes + kQScaleBytes;  // 14.1 MB
 static_assert(kNoAllocMaxBatch <= 255, "the split prefix holds b + 1 entries");
 
 // Held by every GPU that loads the library, for the life of the process.
@@ -99,8 +98,7 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
   if (scratch == nullptr) return FP8MLA_ERR_CUDA;
   int32_t* tile_sched = reinterpret_cast<int32_t*>(scratch);
   int32_t* num_splits = reinterpret_cast<int32_t*>(scratch + kSchedBytes);
-  float* corr = reinterpret_cast<float*>(scratch + kSchedBytes + kSplitsBytes);
-  uint8_t* qbuf = reinterpret_cast<uint8_t*>(scratch) + kSchedBytes + kSplitsBytes + kCorrBytes;
+  uint8_t* qbuf = reinterpret_cast<uint8_t*>(scratch) + kSchedBytes + kSplitsBytes;
   float* qscale = reinterpret_cast<float*>(qbuf + kQBufBytes);
 
   CUtensorMap tm_lat, tm_rope;
@@ -109,9 +107,9 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
     return FP8MLA_ERR_CUDA;
 
   // One unit per sequence: every sequence is one whole piece, so the split
-  // partials (ws_o, ws_ml, ws_d) are never written or read.  The schedule and
-  // the correction terms are rewritten by every call before they are read,
-  // so nothing left in the array by an earlier call needs clearing.
+  // partials (ws_o, ws_ml) are never written or read.  The schedule and the
+  // quantised Q are rewritten by every call before they are read, so nothing
+  // left in the array by an earlier call needs clearing.
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int units = b;
   if (launch_mla_metadata(cache_seqlens, b, units, 1, tile_sched, num_splits, s) != cudaSuccess)
@@ -125,8 +123,6 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
   prm.num_splits = num_splits;
   prm.ws_o = nullptr;
   prm.ws_ml = nullptr;
-  prm.ws_d = nullptr;
-  prm.ws_corr = corr;
   prm.qbuf = qbuf;
   prm.qscale = qscale;
   prm.out = static_cast<uint16_t*>(out);
@@ -143,8 +139,8 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
     e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_decode_fp8(tm_lat, tm_rope, prm, units, s)
                                      : launch_mla_decode_16bit(tm_lat, tm_rope, prm, units, s);
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
-  if (launch_mla_combine(num_splits, nullptr, nullptr, nullptr, corr, dot_mode == FP8MLA_DOT_FP8 ? 1 : 0,
-                         softmax_scale, prm.out, lse, b, s_q * h_q, s) != cudaSuccess)
+  if (launch_mla_combine(num_splits, nullptr, nullptr, dot_mode == FP8MLA_DOT_FP8 ? qbuf : nullptr, softmax_scale,
+                         prm.out, lse, b, s_q * h_q, s) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   return FP8MLA_OK;
 }

@@ -572,7 +572,7 @@ fp8mla_status_t sparse_decode_entry(const void* q, const void* kv_cache, int64_t
                        stream, tm, prm) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   if (splits > 1) {
-    if (launch_split_combine(nullptr, splits, prm.ws_o, false, prm.ws_ml, prm.ws_d, nullptr, 2, softmax_scale,
+    if (launch_split_combine(nullptr, splits, prm.ws_o, false, prm.ws_ml, prm.ws_d, nullptr, 2, nullptr, 0, softmax_scale,
                              static_cast<uint16_t*>(out), lse, s_q, h_q, sparse::kN, stream) != cudaSuccess)
       return FP8MLA_ERR_CUDA;
   }
