@@ -923,17 +923,11 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         const uint32_t v_base = smem_u32(smem + st * kStageBytes) + part * 2 * kLatBox;
         const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          if (leader)
-            mma_f8_ss(t_o, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
-                      (first && kk == 0) ? 0u : 1u);
-          __syncwarp();
-        }
-        if (leader) {
-          tc_commit(&bars->pv_done);
-          tc_commit(&bars->kv_empty[st]);
-        }
-        __syncwarp();
+        for (int kk = 0; kk < 2; ++kk)
+          mma_f8_ss_if(leader, t_o, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
+                       (first && kk == 0) ? 0u : 1u);
+        tc_commit_if(leader, &bars->pv_done);
+        tc_commit_if(leader, &bars->kv_empty[st]);
         ++j;
         return true;
       };
@@ -968,20 +962,14 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           const uint32_t t_s = tmem + kTS + sbuf * kPage;
           const uint64_t kd = make_sdesc(smem_u32(smem + st * kStageBytes), 16, 1024, SWIZZLE_128B);
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            if (leader)
-              mma_f8_ts(t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4), idesc8,
-                        kk > 0 ? 1u : 0u);
-            __syncwarp();
-          }
+          for (int kk = 0; kk < 16; ++kk)
+            mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4),
+                         idesc8, kk > 0 ? 1u : 0u);
           const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + sbuf * kCvtBytes), 16, 1024, SWIZZLE_128B);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            if (leader) mma_f16_ss(t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
-            __syncwarp();
-          }
-          if (leader) tc_commit(&bars->s_full[sbuf]);
-          __syncwarp();
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ss_if(leader, t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
+          tc_commit_if(leader, &bars->s_full[sbuf]);
           const uint32_t e = static_cast<uint32_t>(st) | ((pg == sg.lo) ? 8u : 0u);
           pend = (pend & ~(0xFFu << (8 * (i & 3)))) | (e << (8 * (i & 3)));
           // the P.V of the previous page (queued right behind this Q.K^T), then
