@@ -235,18 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vb = smem_u32(v16 + vs * kV16Bytes);
         const uint32_t pb = smem_u32(p_tile + bf * kPBytes);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          if (leader)
-            mma_f16_ss(tmem + kTO, make_sdesc(vb + kk * 2048, kCvtAtom, 1024, SWIZZLE_128B),
-                       make_sdesc(pb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_pv,
-                       (j == 0 && kk == 0) ? 0u : 1u);
-          __syncwarp();
-        }
-        if (leader) {
-          tc_commit(&sm->pv_done[bf]);
-          tc_commit(&sm->v16_empty[vs]);
-        }
-        __syncwarp();
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ss_if(leader, tmem + kTO, make_sdesc(vb + kk * 2048, kCvtAtom, 1024, SWIZZLE_128B),
+                        make_sdesc(pb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_pv,
+                        (j == 0 && kk == 0) ? 0u : 1u);
+        tc_commit_if(leader, &sm->pv_done[bf]);
+        tc_commit_if(leader, &sm->v16_empty[vs]);
         return true;
       };
       for (int i = 0; ok && i < nsteps; ++i) {
@@ -258,18 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          if (leader)
-            mma_f16_ts(tmem + kTS + bf * kN, tmem + kTK + ks * 64 + kk * 8,
-                       make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
-                       kk > 0 ? 1u : 0u);
-          __syncwarp();
-        }
-        if (leader) {
-          tc_commit(&sm->s_full[bf]);
-          tc_commit(&sm->k16_empty[ks]);
-        }
-        __syncwarp();
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts_if(leader, tmem + kTS + bf * kN, tmem + kTK + ks * 64 + kk * 8,
+                        make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
+                        kk > 0 ? 1u : 0u);
+        tc_commit_if(leader, &sm->s_full[bf]);
+        tc_commit_if(leader, &sm->k16_empty[ks]);
         if (i > 0 && !issue_pv(i - 1)) ok = false;
       }
       if (ok && nsteps > 0) issue_pv(nsteps - 1);

@@ -196,16 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            if (leader)
-              mma_f8_ss(tmem + kTO + mt * kN, make_sdesc(sb + mt * kAtom + kk * 4096, kAtom, 1024, SWIZZLE_128B),
-                        make_sdesc(pb + kk * 32, 16, 1024, SWIZZLE_128B), idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
-            __syncwarp();
+            mma_f8_ss_if(leader, tmem + kTO + mt * kN,
+                         make_sdesc(sb + mt * kAtom + kk * 4096, kAtom, 1024, SWIZZLE_128B),
+                         make_sdesc(pb + kk * 32, 16, 1024, SWIZZLE_128B), idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
           }
-        if (leader) {
-          tc_commit(&sm->pv_done);
-          tc_commit(&sm->kv_empty[st]);
-        }
-        __syncwarp();
+        tc_commit_if(leader, &sm->pv_done);
+        tc_commit_if(leader, &sm->kv_empty[st]);
         return true;
       };
       for (int i = 0; ok && i < nchunks; ++i) {
@@ -219,14 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = smem_u32(smem + st * kStageBytes);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          if (leader)
-            mma_f8_ss(tmem + kTS, make_sdesc(sb + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024, SWIZZLE_128B),
-                      make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
-                      kk > 0 ? 1u : 0u);
-          __syncwarp();
+          mma_f8_ss_if(leader, tmem + kTS, make_sdesc(sb + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024, SWIZZLE_128B),
+                       make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
+                       kk > 0 ? 1u : 0u);
         }
-        if (leader) tc_commit(&sm->s_full);
-        __syncwarp();
+        tc_commit_if(leader, &sm->s_full);
         if (i > 0 && !issue_pv(i - 1)) ok = false;
       }
       if (ok && nchunks > 0) issue_pv(nchunks - 1);
