@@ -492,6 +492,74 @@ Layout layout(int s_q, int splits) {
   return l;
 }
 
+// Merge of the splits of one (token, head) row: grid (s_q, h_q), 128 threads,
+// thread t owns output columns 4t .. 4t + 3.  Split j of token bi holds the
+// row's fp32 partial O (true units, unnormalised) and (m, l) with m in log2
+// units, plus the two LSE-correction shares d_j; the result is
+// out = sum_j w_j O_j / L and lse = ln2 (M + log2 L) - scale sum_j w_j d_j / L,
+// w_j = 2^(m_j - M), M = max_j m_j, L = sum_j w_j l_j.  Every thread recomputes
+// the weights it needs from (m, l) (a broadcast read), and issues the partial
+// loads of 16 splits before using any of them.
+__global__ void __launch_bounds__(128) combine_kernel(int splits, const float* __restrict__ ws_o,
+                                                      const float2* __restrict__ ws_ml,
+                                                      const float* __restrict__ ws_d, float softmax_scale,
+                                                      uint16_t* __restrict__ out, float* __restrict__ lse, int h_q) {
+  griddep_wait();  // launched as a dependent of the decode kernel
+  const int bi = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
+  const size_t slot0 = static_cast<size_t>(bi) * splits;
+  __shared__ float red[4], l_sh;
+  float mx = kNegInf;
+  for (int j = t; j < splits; j += 128) mx = fmaxf(mx, __ldg(ws_ml + (slot0 + j) * kN + h).x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((t & 31) == 0) red[t >> 5] = mx;
+  __syncthreads();
+  const float big_m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  uint16_t* orow = out + (static_cast<size_t>(bi) * h_q + h) * kMlaDV + 4 * t;
+  if (big_m == kNegInf) {  // every split of the row is empty
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0, 0);
+    if (t == 0) lse[static_cast<size_t>(bi) * h_q + h] = kNegInf;
+    return;
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float big_l = 0.f, dq = 0.f;
+  for (int j0 = 0; j0 < splits; j0 += 16) {
+    float4 v[16];
+    float2 ml[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      if (j0 + q < splits) {
+        const size_t slot = (slot0 + j0 + q) * kN + h;
+        v[q] = __ldg(reinterpret_cast<const float4*>(ws_o + slot * kMlaDV) + t);
+        ml[q] = __ldg(ws_ml + slot);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      if (j0 + q < splits) {
+        const float w = (ml[q].x == kNegInf) ? 0.f : ex2_approx(ml[q].x - big_m);  // an empty split adds nothing
+        acc.x += w * v[q].x;
+        acc.y += w * v[q].y;
+        acc.z += w * v[q].z;
+        acc.w += w * v[q].w;
+        if (t == 0) {
+          const size_t slot = (slot0 + j0 + q) * kN + h;
+          big_l += w * ml[q].y;
+          dq += w * (__ldg(ws_d + 2 * slot) + __ldg(ws_d + 2 * slot + 1));
+        }
+      }
+    }
+  }
+  if (t == 0) l_sh = big_l;
+  __syncthreads();
+  big_l = l_sh;
+  const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
+  *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (t == 0)
+    lse[static_cast<size_t>(bi) * h_q + h] =
+        big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 - softmax_scale * dq * inv : kNegInf;
+}
+
 }  // namespace sparse
 
 int sparse_choose_splits(int s_q, int topk, int num_splits) {
@@ -565,8 +633,10 @@ fp8mla_status_t sparse_decode_entry(const void* q, const void* kv_cache, int64_t
                        stream, tm, prm) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   if (splits > 1) {
-    if (launch_split_combine(nullptr, splits, prm.ws_o, false, prm.ws_ml, prm.ws_d, nullptr, 2, nullptr, 0, softmax_scale,
-                             static_cast<uint16_t*>(out), lse, s_q, h_q, sparse::kN, stream) != cudaSuccess)
+    if (launch_dependent(sparse::combine_kernel, dim3(s_q, h_q), dim3(128), 0, stream, splits,
+                         static_cast<const float*>(prm.ws_o), static_cast<const float2*>(prm.ws_ml),
+                         static_cast<const float*>(prm.ws_d), softmax_scale, static_cast<uint16_t*>(out), lse,
+                         h_q) != cudaSuccess)
       return FP8MLA_ERR_CUDA;
   }
   return FP8MLA_OK;
