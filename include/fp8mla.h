@@ -128,8 +128,10 @@ FP8MLA_API fp8mla_status_t fp8mla_get_metadata(const int32_t* cache_seqlens, int
                                     int force_splits, int32_t* tile_sched, int32_t* num_splits,
                                     fp8mla_stream_t stream);
 
-/* Workspace for split-KV partials of fp8mla_decode: (b + num_units)
- * partial slots of 128 x 512 float32 accumulators plus 128 (m, l) pairs. */
+/* Workspace of fp8mla_decode: (b + num_units) split-KV partial slots of
+ * 128 x 512 bf16 accumulators plus 128 (m, l) pairs each, then (FP8 dots) per
+ * sequence its quantised Q (219 136 bytes: the decode kernel's Q slots and the
+ * bf16 quantisation error used for the LSE correction) and 128 Q scales. */
 FP8MLA_API size_t fp8mla_workspace_bytes(int b, int s_q, int h_q, int num_units);
 
 /* fp8mla_decode -- dense MLA decode over the paged E4M3 cache.
@@ -216,7 +218,7 @@ FP8MLA_API int paged_gqa_num_splits(int bs, int h_kv, int max_seqlen, int num_sm
  *
  * Same arguments and results as fp8mla_decode without the schedule and the
  * workspace: the call schedules one work unit per sequence (no split-KV) and
- * keeps its schedule, split counts, LSE-correction terms and quantised Q in a fixed
+ * keeps its schedule, split counts and quantised Q (with its quantisation error) in a fixed
  * device array compiled into this library (14.1 MB, held by every GPU that
  * loads the library until the process exits).  It calls no allocator.
  *   b <= FP8MLA_NO_ALLOC_MAX_BATCH; a larger batch returns
