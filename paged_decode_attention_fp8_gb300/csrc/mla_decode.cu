@@ -6,33 +6,30 @@
 //   P = softmax(softmax_scale * S) under the causal mask, O = P V with V the
 //   first 512 dims of the same rows; lse = log sum exp.
 //
-// GB300 design (one work unit = 2 CTAs (FP8 dots) or 4 CTAs (16-bit dots),
-// each owning one slice of dv):
-//   * TMEM (512 columns x 128 lanes) holds everything the tensor core
-//     touches besides K/V: O (this CTA's dv slice), S (64 columns), P, and
-//     Q itself, so Q.K^T runs with A read from TMEM and shared memory holds
-//     only a ring of KV pages.  FP8 dots: O 256 + S 64 + P 16 (E4M3) + Q
-//     latent 128 (E4M3) + Q RoPE 32 (bf16) columns.  16-bit dots: O 128 +
-//     S 64 + P 32 (bf16) + Q 288 (bf16) columns.
+// GB300 design: one work unit = 2 CTAs (FP8 dots, mla_fp8_kernel) or 4 CTAs
+// (16-bit dots, mla_decode_16bit_kernel), each owning one slice of dv.
 //   * TMA loads a whole 64-token page through the block table: four
 //     128-byte-swizzled boxes of the 512 latent bytes (usable as K-major B
 //     for Q.K^T and as MN-major B for P.V without any transpose) and one
 //     plain box of the 64 RoPE bytes.
-//   * FP8 dots: Q.K^T = 16 E4M3 MMAs (K = 32) over the latent part plus 4
-//     bf16 MMAs (K = 16) over the RoPE part into one f32 accumulator -- the
-//     RoPE chunk stays 16-bit (FlashMLA page, Improvements: the nine 64-wide
-//     K chunks let RoPE run in BF16).  Q's latent part is quantised in-kernel
-//     with a per-row power-of-two scale qs, so the RoPE part divides by qs
-//     exactly (aiter sparse_mla_fwd page, Technical details: in-kernel Q
-//     quantisation).  16-bit dots: converter warps turn each page into bf16
-//     (exact) and both products run as bf16 MMAs.
+//   * FP8 dots: Q is quantised by mla_qprep_kernel one grid ahead (per-row
+//     power-of-two scale qs; latent -> E4M3, RoPE -> f16 divided by qs
+//     exactly; aiter sparse_mla_fwd page, Technical details: Q quantisation)
+//     and carried through the page ring.  TMEM holds O (256 columns), two S
+//     buffers (64 each; pages alternate) and the latent Q (128, the A operand
+//     of the latent Q.K^T); shared memory holds the ring, the page's RoPE part
+//     converted to f16 (exact for E4M3), the Q RoPE tile and the P tile.
+//     Q.K^T = 16 E4M3 MMAs (K = 32) + 4 f16 MMAs (K = 16) into one f32
+//     accumulator -- the RoPE chunk stays 16-bit (FlashMLA page,
+//     Improvements) -- and P.V = 2 E4M3 MMAs with N = 256.
+//   * 16-bit dots: converter warps turn each page into bf16 (exact); Q, S, P
+//     and O live in TMEM and both products run as bf16 MMAs.
 //   * Online softmax in the log2 domain (InfiniCore page, Summary) with the
-//     per-tensor kv_scale and qs folded into one per-row constant; in FP8
-//     mode P is stored as E4M3(128 p) so long tails do not flush to zero and
-//     the epilogue divides the 128 back out with the V scale (aiter page,
-//     Technical details and Accuracy).  The running max is only raised when
-//     a tile's max exceeds it by more than 1 (log2 units), which keeps
-//     128 p <= 256 < 448 and makes O rescales rare.
+//     per-tensor kv_scale and qs folded into one per-row constant; with FP8
+//     dots P is stored as E4M3(64 p) so long tails do not flush to zero, and
+//     the running max is only raised when a page's max exceeds it by more
+//     than 2.75 (log2 units): 64 p <= 64 * 2^2.75 < 448 and O rescales are
+//     rare (aiter page, Technical details and Accuracy).
 //   * Rows of the sequence's last page past its length are zeroed once per
 //     sequence before P.V reads them (FlashMLA page, TODO: fill_oob_KV per
 //     tile was the stated limiter); scores there are masked by a select.
@@ -40,15 +37,14 @@
 //     workspace and a combine kernel merges them (InfiniCore split-kv commit).
 //   * FP8 dots perturb the LSE by softmax_scale * (q_hat - q) . k_mean, where
 //     k_mean = sum_j p_j k_j; its latent part is exactly the output row, so
-//     the epilogue publishes -softmax_scale * (q_hat - q) . out per dv slice
-//     and the combine step subtracts that first-order term from the LSE.
+//     the combine kernel subtracts softmax_scale * (q_hat - q) . out, from the
+//     quantisation error the prep kernel stored and the finished output row.
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-3 page conversion (RoPE or whole page to bf16) and tail
-// zeroing, warps 4-11 softmax, Q preparation and epilogue: query row r
-// (= TMEM lane r) is shared by two threads, each owning half of the page's
-// score columns, half of the O slice and half of the Q row; the two halves
-// exchange the per-row tile max through shared memory.
+// owner, warps 2-3 page conversion (the RoPE part to f16, or the whole page
+// to bf16) and tail zeroing, warps 4-11 softmax, Q copy and epilogue: query
+// row r (= TMEM lane r) is shared by two threads, each owning half of the
+// page's score columns and half of the O slice.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -602,11 +598,11 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
 // FP8-dots kernel.
 //
 // Work unit = 2 CTAs, each owning one 256-wide dv slice.  The shared-memory
-// ring of 5 stages carries, in one order that every role walks, two Q slots
-// at the start of each segment (the segment's quantised Q, one row half per
-// slot) followed by the segment's KV pages, so no separate Q buffer competes
-// with the KV pages for shared memory.  TMEM: O 256 + S 64 + two P buffers
-// of 16 + Q latent 128 + Q RoPE 32 columns.
+// ring of 5 stages carries, in one order that every role walks, three Q slots
+// at the start of each segment (the segment's quantised Q: two latent halves
+// and the RoPE part) followed by the segment's KV pages, so no separate Q
+// buffer competes with the KV pages for shared memory.  TMEM: O 256 + two S
+// buffers of 64 + Q latent 128 columns.
 // ===========================================================================
 namespace f8 {
 constexpr int kStages = 5;
