@@ -79,10 +79,12 @@ typedef enum {
 /* Precision of the two dot products (Q.K and P.V).
  *  FP8MLA_DOT_16BIT: Q, K, P and V enter the tensor cores as 16-bit values
  *    (the E4M3 cache converts exactly); "bf16 dots" on the aiter page.
- *  FP8MLA_DOT_FP8:   the latent part of Q is quantised in-kernel to E4M3
- *    with a per-row power-of-two scale, the RoPE part of Q.K stays bf16
- *    (FlashMLA page, Improvements), and P is quantised as E4M3(128 * p)
- *    (aiter page, Technical details). */
+ *  FP8MLA_DOT_FP8:   the latent part of Q is quantised to E4M3 with a
+ *    per-row power-of-two scale, the RoPE part of Q.K stays 16-bit (f16 in
+ *    dense MLA; FlashMLA page, Improvements), and P is quantised as E4M3
+ *    (64 * p in dense MLA, 128 * p in sparse MLA; aiter page, Technical
+ *    details).  The first-order effect of quantising Q on the LSE is
+ *    corrected (dense and sparse MLA). */
 typedef enum { FP8MLA_DOT_16BIT = 0, FP8MLA_DOT_FP8 = 1 } fp8mla_dot_mode_t;
 
 /* Encoding of the cache bytes.  Only FP8MLA_KV_E4M3 (OCP e4m3 "fn", or a
