@@ -194,32 +194,28 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
   if (tid == 0) num_splits[B] = total;
 }
 
-// Grid (sequence, 8-row block), one warp per row.  A sequence with exactly
-// one split was finished by the decode kernel: only its LSE correction (FP8
-// dots) is left.  Otherwise splits are taken 32 at a time: lane j reads split
-// j's (m, l) and correction, the round's max rescales what is accumulated so
-// far, and every lane accumulates its 16 dv columns over the round's splits.
-// Partial slots are [slot][slot_rows] rows of dv = 512; with uniform_splits > 0
-// sequence bi owns slots [bi * uniform_splits, (bi + 1) * uniform_splits).
-// The FP8-dot LSE correction lse -= softmax_scale (q_hat - q) . out comes
-// either from corr_terms shares each row or slot row carries in ws_corr / ws_d
-// (one per producer of a piece of the row; 0 = none), or, with qerr non-null,
-// from the row's stored quantisation error dotted with the finished output.
-template <bool kBf16>
-__global__ void __launch_bounds__(256) split_combine_kernel(
-    const int32_t* __restrict__ num_splits, int uniform_splits, const void* __restrict__ ws_o_,
-    const float2* __restrict__ ws_ml, const float* __restrict__ ws_d, const float* __restrict__ ws_corr, int corr_terms,
+// Grid (sequence, 8-row block), one warp per row, lane j owning dv columns
+// [16 j, 16 j + 16).  A sequence with exactly one split was finished by the
+// decode kernel: only its LSE correction is left.  Otherwise up to four splits
+// are merged with every load issued before any is used, more 32 at a time with
+// a rescale of what is accumulated so far between rounds:
+// M = max m_s, L = sum l_s 2^(m_s - M), out = sum acc_s 2^(m_s - M) / L,
+// lse = ln2 (M + log2 L).  Partial slots are [slot][128] rows of dv = 512
+// bf16, sequence bi owning the slots from num_splits[bi].  With qerr non-null
+// (FP8 dots) every row's LSE also gets the first-order Q-quantisation
+// correction lse -= softmax_scale (q_hat - q) . out, from the row's stored
+// error (bf16 x 512 at qerr + bi * qerr_stride) and the finished output row.
+__global__ void __launch_bounds__(256) mla_combine_kernel(
+    const int32_t* __restrict__ num_splits, const uint16_t* __restrict__ ws_o, const float2* __restrict__ ws_ml,
     const uint8_t* __restrict__ qerr, size_t qerr_stride, float softmax_scale, uint16_t* __restrict__ out,
-    float* __restrict__ lse, int rows, int slot_rows) {
+    float* __restrict__ lse, int rows) {
   const int bi = blockIdx.x;
   const int r = blockIdx.y * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // The split counts were written before the decode kernel started (it waited
-  // for them), so they are read before waiting for the decode kernel itself.
-  const int s0 = uniform_splits > 0 ? bi * uniform_splits : __ldg(num_splits + bi);
-  const int ns = uniform_splits > 0 ? uniform_splits : __ldg(num_splits + bi + 1) - s0;
-  // The row's Q quantisation error (FP8 dots: q_hat qs - q as bf16), also
-  // final before the decode kernel started; this lane's 16 columns.
+  // The split counts and the quantisation error were final before the decode
+  // kernel started (it waited for them), so they are read before waiting for it.
+  const int s0 = __ldg(num_splits + bi);
+  const int ns = __ldg(num_splits + bi + 1) - s0;
   uint4 ev0 = make_uint4(0, 0, 0, 0), ev1 = ev0;
   if (qerr != nullptr && r < rows) {
     const uint4* e = reinterpret_cast<const uint4*>(qerr + bi * qerr_stride + static_cast<size_t>(r) * kMlaDV * 2) +
@@ -227,31 +223,23 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
     ev0 = __ldg(e);
     ev1 = __ldg(e + 1);
   }
-  // (q_hat - q) . o for this lane's 16 columns of an output row o
+  // (q_hat - q) . o over the whole row, o holding this lane's 16 columns
   auto err_dot = [&](const float (&o)[16]) {
     const uint32_t w[8] = {ev0.x, ev0.y, ev0.z, ev0.w, ev1.x, ev1.y, ev1.z, ev1.w};
     float d = 0.f;
 #pragma unroll
     for (int q = 0; q < 8; ++q) d += bf16_lo(w[q]) * o[2 * q] + bf16_hi(w[q]) * o[2 * q + 1];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
     return d;
   };
   griddep_wait();  // launched as a dependent of the decode kernel
   if (r >= rows) return;
   const size_t row = static_cast<size_t>(bi) * rows + r;
-  auto corr_sum = [&](const float* p) {  // the row's correction shares (4, 2 or 0 of them)
-    if (corr_terms == 4) {
-      const float4 c = __ldg(reinterpret_cast<const float4*>(p));
-      return (c.x + c.y) + (c.z + c.w);
-    }
-    float c = 0.f;
-    for (int t = 0; t < corr_terms; ++t) c += __ldg(p + t);
-    return c;
-  };
+  uint16_t* orow = out + row * kMlaDV + lane * 16;
   if (ns == 1) {
     if (qerr != nullptr) {
-      // the LSE correction from the finished output row: lse -= scale (q_hat - q) . out
-      const uint4* orow4 = reinterpret_cast<const uint4*>(out + row * kMlaDV) + lane * 2;
-      const uint4 a = orow4[0], b2 = orow4[1];
+      const uint4 a = reinterpret_cast<const uint4*>(orow)[0], b2 = reinterpret_cast<const uint4*>(orow)[1];
       const uint32_t w[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
       float o[16];
 #pragma unroll
@@ -259,21 +247,14 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
         o[2 * q] = bf16_lo(w[q]);
         o[2 * q + 1] = bf16_hi(w[q]);
       }
-      float d = err_dot(o);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      const float d = err_dot(o);
       if (lane == 0) {
         const float l = lse[row];
         if (l != kNegInf) lse[row] = l - softmax_scale * d;
       }
-    } else if (corr_terms > 0 && lane == 0) {
-      const float c = corr_sum(ws_corr + static_cast<size_t>(corr_terms) * row);
-      const float l = lse[row];
-      if (l != kNegInf) lse[row] = l + c;
     }
     return;
   }
-  uint16_t* orow = out + row * kMlaDV + lane * 16;
   if (ns <= 0) {
     *reinterpret_cast<uint4*>(orow) = make_uint4(0, 0, 0, 0);
     *reinterpret_cast<uint4*>(orow + 8) = make_uint4(0, 0, 0, 0);
@@ -283,27 +264,34 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
   float acc[16];
 #pragma unroll
   for (int c = 0; c < 16; ++c) acc[c] = 0.f;
-  float big_l = 0.f, dq = 0.f, big_m = kNegInf;
-  if (kBf16 && ns <= 4) {
+  float big_l = 0.f, big_m = kNegInf;
+  // acc += wj * (this lane's 16 columns of split j's partial row)
+  auto load_partial = [&](int j, uint4 (&v)[2]) {
+    const size_t slot = static_cast<size_t>(s0 + j) * kMlaRows + r;
+    const uint4* src = reinterpret_cast<const uint4*>(ws_o + slot * kMlaDV + lane * 16);
+    v[0] = __ldg(src);
+    v[1] = __ldg(src + 1);
+  };
+  auto accumulate = [&](float wj, const uint4 (&v)[2]) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t w4[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[8 * c + 2 * q] += wj * bf16_lo(w4[q]);
+        acc[8 * c + 2 * q + 1] += wj * bf16_hi(w4[q]);
+      }
+    }
+  };
+  if (ns <= 4) {
     // few splits (the usual case): every load is issued before any is used
     constexpr int kMax = 4;
     uint4 v[kMax][2];
-    float2 ml = make_float2(kNegInf, 0.f);
-    float d = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMax; ++j) {
-      if (j < ns) {
-        const size_t slot = static_cast<size_t>(s0 + j) * slot_rows + r;
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(ws_o_) + slot * kMlaDV + lane * 16);
-        v[j][0] = __ldg(src);
-        v[j][1] = __ldg(src + 1);
-      }
-    }
-    if (lane < ns) {
-      const size_t slot = static_cast<size_t>(s0 + lane) * slot_rows + r;
-      ml = __ldg(ws_ml + slot);
-      if (corr_terms > 0) d = corr_sum(ws_d + static_cast<size_t>(corr_terms) * slot);
-    }
+    for (int j = 0; j < kMax; ++j)
+      if (j < ns) load_partial(j, v[j]);
+    const float2 ml =
+        lane < ns ? __ldg(ws_ml + static_cast<size_t>(s0 + lane) * kMlaRows + r) : make_float2(kNegInf, 0.f);
     float m_all = ml.x;
 #pragma unroll
     for (int o = 2; o > 0; o >>= 1) m_all = fmaxf(m_all, __shfl_xor_sync(0xffffffffu, m_all, o));
@@ -312,106 +300,55 @@ __global__ void __launch_bounds__(256) split_combine_kernel(
       big_m = m_all;
       const float w = (ml.x == kNegInf) ? 0.f : ex2_approx(ml.x - big_m);  // an empty split adds nothing
       big_l = ml.y * w;
-      dq = w * d;
 #pragma unroll
-      for (int j = 0; j < kMax; ++j) {
-        if (j < ns) {
-          const float wj = __shfl_sync(0xffffffffu, w, j);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t w4[4] = {v[j][c].x, v[j][c].y, v[j][c].z, v[j][c].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              acc[8 * c + 2 * q] += wj * bf16_lo(w4[q]);
-              acc[8 * c + 2 * q + 1] += wj * bf16_hi(w4[q]);
-            }
-          }
-        }
-      }
+      for (int j = 0; j < kMax; ++j)
+        if (j < ns) accumulate(__shfl_sync(0xffffffffu, w, j), v[j]);
     }
-  } else
-  for (int base = 0; base < ns; base += 32) {
-    // this round's splits: lane j holds split base + j's (m, l) and correction
-    const int cnt = min(32, ns - base);
-    float2 ml = make_float2(kNegInf, 0.f);
-    float d = 0.f;
-    if (lane < cnt) {
-      const size_t slot = static_cast<size_t>(s0 + base + lane) * slot_rows + r;
-      ml = __ldg(ws_ml + slot);
-      if (corr_terms > 0) d = corr_sum(ws_d + static_cast<size_t>(corr_terms) * slot);
-    }
-    float m_round = ml.x;
+  } else {
+    for (int base = 0; base < ns; base += 32) {
+      // this round's splits: lane j holds split base + j's (m, l)
+      const int cnt = min(32, ns - base);
+      const float2 ml = lane < cnt ? __ldg(ws_ml + static_cast<size_t>(s0 + base + lane) * kMlaRows + r)
+                                   : make_float2(kNegInf, 0.f);
+      float m_round = ml.x;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m_round = fmaxf(m_round, __shfl_xor_sync(0xffffffffu, m_round, o));
-    if (m_round == kNegInf) continue;  // every split of this round is empty
-    // fold this round into the running (big_m, big_l, acc, dq)
-    const float m_new = fmaxf(big_m, m_round);
-    const float a_old = (big_m == kNegInf) ? 0.f : ex2_approx(big_m - m_new);
-    big_l *= a_old;
-    dq *= a_old;
+      for (int o = 16; o > 0; o >>= 1) m_round = fmaxf(m_round, __shfl_xor_sync(0xffffffffu, m_round, o));
+      if (m_round == kNegInf) continue;  // every split of this round is empty
+      // fold this round into the running (big_m, big_l, acc)
+      const float m_new = fmaxf(big_m, m_round);
+      const float a_old = (big_m == kNegInf) ? 0.f : ex2_approx(big_m - m_new);
+      big_l *= a_old;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) acc[c] *= a_old;
-    big_m = m_new;
-    const float w = (ml.x == kNegInf) ? 0.f : ex2_approx(ml.x - big_m);  // an empty split is the neutral element
-    big_l += ml.y * w;
-    dq += w * d;
+      for (int c = 0; c < 16; ++c) acc[c] *= a_old;
+      big_m = m_new;
+      const float w = (ml.x == kNegInf) ? 0.f : ex2_approx(ml.x - big_m);  // an empty split is the neutral element
+      big_l += ml.y * w;
 #pragma unroll 4
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      const size_t slot = static_cast<size_t>(s0 + base + j) * slot_rows + r;
-      if constexpr (kBf16) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(ws_o_) + slot * kMlaDV + lane * 16);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint4 v = __ldg(src + c);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[8 * c + 2 * q] += wj * bf16_lo(w4[q]);
-            acc[8 * c + 2 * q + 1] += wj * bf16_hi(w4[q]);
-          }
-        }
-      } else {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(ws_o_) + slot * kMlaDV + lane * 16);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float4 v = __ldg(src + c);
-          acc[4 * c + 0] += wj * v.x;
-          acc[4 * c + 1] += wj * v.y;
-          acc[4 * c + 2] += wj * v.z;
-          acc[4 * c + 3] += wj * v.w;
-        }
+      for (int j = 0; j < cnt; ++j) {
+        uint4 v[2];
+        load_partial(base + j, v);
+        accumulate(__shfl_sync(0xffffffffu, w, j), v);
       }
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    big_l += __shfl_xor_sync(0xffffffffu, big_l, o);
-    dq += __shfl_xor_sync(0xffffffffu, dq, o);
-  }
+  for (int o = 16; o > 0; o >>= 1) big_l += __shfl_xor_sync(0xffffffffu, big_l, o);
   const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
-  if (qerr != nullptr) {  // the LSE correction from the merged output row
-    float o[16];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) o[c] = acc[c] * inv;
-    float d = err_dot(o);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-    dq = d * big_l;  // the lse line below divides by big_l
-  }
+  for (int c = 0; c < 16; ++c) acc[c] *= inv;
+  const float d = qerr != nullptr ? err_dot(acc) : 0.f;  // the LSE correction from the merged output row
   uint4 w0, w1;
-  w0.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  w0.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-  w0.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-  w0.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-  w1.x = pack_bf16x2(acc[8] * inv, acc[9] * inv);
-  w1.y = pack_bf16x2(acc[10] * inv, acc[11] * inv);
-  w1.z = pack_bf16x2(acc[12] * inv, acc[13] * inv);
-  w1.w = pack_bf16x2(acc[14] * inv, acc[15] * inv);
+  w0.x = pack_bf16x2(acc[0], acc[1]);
+  w0.y = pack_bf16x2(acc[2], acc[3]);
+  w0.z = pack_bf16x2(acc[4], acc[5]);
+  w0.w = pack_bf16x2(acc[6], acc[7]);
+  w1.x = pack_bf16x2(acc[8], acc[9]);
+  w1.y = pack_bf16x2(acc[10], acc[11]);
+  w1.z = pack_bf16x2(acc[12], acc[13]);
+  w1.w = pack_bf16x2(acc[14], acc[15]);
   *reinterpret_cast<uint4*>(orow) = w0;
   *reinterpret_cast<uint4*>(orow + 8) = w1;
-  if (lane == 0)
-    lse[row] = big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 - softmax_scale * dq * inv : kNegInf;
+  if (lane == 0) lse[row] = big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 - softmax_scale * d : kNegInf;
 }
 
 }  // namespace
@@ -437,28 +374,13 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const void* ws_o, bool partials_bf16,
-                                 const float2* ws_ml,
-                                 const float* ws_d, const float* ws_corr, int corr_terms, const uint8_t* qerr,
-                                 size_t qerr_stride, float softmax_scale,
-                                 uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream) {
-  if (b == 0) return cudaSuccess;
-  dim3 grid(b, (rows + 7) / 8);
-  if (partials_bf16)
-    return launch_dependent(split_combine_kernel<true>, grid, dim3(256), 0, stream, num_splits, uniform_splits, ws_o,
-                            ws_ml, ws_d, ws_corr, corr_terms, qerr, qerr_stride, softmax_scale, out, lse, rows,
-                            slot_rows);
-  return launch_dependent(split_combine_kernel<false>, grid, dim3(256), 0, stream, num_splits, uniform_splits, ws_o,
-                          ws_ml, ws_d, ws_corr, corr_terms, qerr, qerr_stride, softmax_scale, out, lse, rows,
-                          slot_rows);
-}
-
 cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,
                                const uint8_t* qbuf, float softmax_scale, uint16_t* out, float* lse, int b, int rows,
                                cudaStream_t stream) {
-  return launch_split_combine(num_splits, 0, ws_o, true, ws_ml, nullptr, nullptr, 0,
-                              qbuf != nullptr ? qbuf + kMlaQErrOff : nullptr, kMlaQBytes, softmax_scale, out, lse, b,
-                              rows, kMlaRows, stream);
+  if (b == 0) return cudaSuccess;
+  const uint8_t* qerr = qbuf != nullptr ? qbuf + kMlaQErrOff : nullptr;
+  return launch_dependent(mla_combine_kernel, dim3(b, (rows + 7) / 8), dim3(256), 0, stream, num_splits, ws_o, ws_ml,
+                          qerr, static_cast<size_t>(kMlaQBytes), softmax_scale, out, lse, rows);
 }
 
 uint32_t metadata_read_and_clear_status() {

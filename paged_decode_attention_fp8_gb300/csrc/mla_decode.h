@@ -60,16 +60,6 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
 cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,
                                const uint8_t* qbuf, float softmax_scale, uint16_t* out, float* lse, int b, int rows,
                                cudaStream_t stream);
-// The same merge for any variant whose partial slots hold slot_rows rows of dv = 512
-// (fp32, or bf16 when partials_bf16).  The LSE correction comes either from
-// corr_terms shares per row or piece (ws_corr / ws_d; 0: none) or, with qerr
-// non-null, from the quantisation error rows (bf16 x 512) of sequence i at
-// qerr + i * qerr_stride.
-cudaError_t launch_split_combine(const int32_t* num_splits, int uniform_splits, const void* ws_o, bool partials_bf16,
-                                 const float2* ws_ml,
-                                 const float* ws_d, const float* ws_corr, int corr_terms, const uint8_t* qerr,
-                                 size_t qerr_stride, float softmax_scale,
-                                 uint16_t* out, float* lse, int b, int rows, int slot_rows, cudaStream_t stream);
 uint32_t metadata_read_and_clear_status();
 
 }  // namespace fp8mla
