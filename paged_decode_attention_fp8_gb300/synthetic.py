@@ -301,3 +301,61 @@ def gqa_inputs(seed: int, bs: int, seqlens, h_q: int = 32, h_kv: int = 8, hd: in
                      seqlens=torch.from_numpy(seqlens.astype(np.int32)),
                      k_scale=scales[0], v_scale=scales[1],
                      softmax_scale=float(np.float32(1.0 / math.sqrt(hd))))
+
+
+# ------------------------------------------------------ cache write inputs --
+
+
+@dataclass
+class CacheWriteInputs:
+    base: torch.Tensor         # bf16 [base_tokens, h_kv, hd]: N(0, 1) rows
+    exponent: np.ndarray       # int64 [n_tokens]: token t is base[t % base_tokens] * 2^exponent[t]
+    slot_mapping: torch.Tensor # int32 [n_tokens]: block * page + offset, -1 = padding
+    num_blocks: int
+    page: int
+    seqlens: np.ndarray        # int64 [bs]: tokens of each sequence, in token order
+
+
+def cache_write_inputs(seed: int, seqlens, h_kv: int = 8, hd: int = 128, page: int = 16,
+                       base_tokens: int = 4096, spare_blocks: int = 0, pad_tokens: int = 0,
+                       exp_range: int = 8) -> CacheWriteInputs:
+    """New K (or V) rows of whole sequences and the slots a paged cache gives them.
+
+    Sequence i's tokens take the blocks of a seeded random permutation of the
+    pool in order (as in ``gqa_inputs``); ``pad_tokens`` slots of -1 are mixed
+    in at seeded positions.  Row values: a block of ``base_tokens`` N(0, 1)
+    rows (bf16) repeated, token t scaled by 2^e (e uniform in
+    [-exp_range, exp_range]), so rows span many magnitudes and a full-size
+    batch needs no full-size draw; ``materialise`` builds any rows of it
+    exactly, on any device."""
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    n_blocks = (seqlens + page - 1) // page
+    used = int(n_blocks.sum())
+    num_blocks = max(used + spare_blocks, 1)
+    perm = permutation(seed, 11, num_blocks)
+    slots = []
+    k = 0
+    for i in range(len(seqlens)):
+        j = np.arange(int(seqlens[i]), dtype=np.int64)
+        slots.append(perm[k + j // page].astype(np.int64) * page + j % page)
+        k += int(n_blocks[i])
+    slots = np.concatenate(slots) if slots else np.zeros(0, dtype=np.int64)
+    if pad_tokens:
+        at = np.sort(randint(seed, 12, pad_tokens, 0, len(slots)))
+        slots = np.insert(slots, at, -1)
+    n = len(slots)
+    exponent = randint(seed, 13, n, -exp_range, exp_range) if n else np.zeros(0, dtype=np.int64)
+    base = to_bf16(normal(seed, 14, (base_tokens, h_kv, hd)))
+    return CacheWriteInputs(base=base, exponent=exponent.astype(np.int64),
+                            slot_mapping=torch.from_numpy(slots.astype(np.int32)),
+                            num_blocks=num_blocks, page=page, seqlens=seqlens)
+
+
+def materialise(inp: CacheWriteInputs, tokens=None, device=None) -> torch.Tensor:
+    """bf16 rows of the given tokens (all by default): base row times 2^exponent (exact)."""
+    n = len(inp.exponent)
+    t = torch.arange(n, dtype=torch.int64) if tokens is None else torch.as_tensor(tokens, dtype=torch.int64)
+    base = inp.base.to(device) if device is not None else inp.base
+    idx = (t % base.shape[0]).to(base.device)
+    f = torch.from_numpy(np.ldexp(1.0, inp.exponent[t.numpy()]).astype(np.float32)).to(base.device)
+    return (base[idx].float() * f[:, None, None]).to(torch.bfloat16)
