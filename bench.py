@@ -358,12 +358,15 @@ def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, worl
 
 
 def run_secondary(args):
-    """µs/call and roofline of the sparse top-k MLA or the paged GQA variant (one GPU).
+    """µs/call and roofline of the sparse top-k MLA, the paged GQA variant or the
+    paged KV-cache write (one GPU).
 
     Sparse: 16 heads, d = dv = 512, 131072-token E4M3 cache, top-k 2048, s_q query
     tokens, FP8 dots, auto split; three cache copies rotate (3 x 64 MiB > L2).
     GQA: 32/8 heads, hd 128, page 16, bs 32 with contexts uniform in [1024, 16384],
     16-bit dots, auto split; two copies of the ~570 MB caches rotate.
+    KV write: K and V rows (8 heads x 128, bf16) of the same 32 sequences
+    quantised into paged E4M3 caches with per-row scales; ~1.1 GB of input.
     """
     import torch
 
@@ -393,6 +396,29 @@ def run_secondary(args):
         cfg = dict(workload="sparse_topk_mla_decode", s_q=s_q, h_q=h_q, d=512, topk=topk, num_tokens=131072,
                    dot="fp8", splits="auto", l2="3 rotating cache copies (192 MiB) > L2")
         metric = f"sparse top-k MLA decode us/call (s_q={s_q}, 16 heads, top-k 2048)"
+        launches = 2
+    elif args.workload == "kvwrite":
+        seqlens = syn.uniform_seqlens(5, 32, 1024, 16384)
+        kin, vin = syn.cache_write_inputs(5, seqlens), syn.cache_write_inputs(6, seqlens)
+        xk, xv = syn.materialise(kin, device=dev), syn.materialise(vin, device=dev)
+        slots = kin.slot_mapping.to(dev)
+        n_tok, h_kv, hd = xk.shape
+        caches = [torch.empty((kin.num_blocks, h_kv, 16, hd), dtype=torch.uint8, device=dev) for _ in range(2)]
+        scales = [torch.empty((kin.num_blocks, h_kv, 16), dtype=torch.float32, device=dev) for _ in range(2)]
+
+        def call(i):
+            fm.paged_cache_write(xk, slots, caches[0], token_scales=scales[0])
+            fm.paged_cache_write(xv, slots, caches[1], token_scales=scales[1])
+
+        # per step: K and V rows read (bf16), codes and per-row scales written, slot mapping read twice
+        nbytes = 2 * (n_tok * h_kv * hd * 3 + n_tok * h_kv * 4 + n_tok * 4)
+        flops = 0.0
+        t_tensor = 0.0
+        cfg = dict(workload="paged_kv_cache_write", tokens=n_tok, h_kv=h_kv, head_dim=hd, page=16,
+                   seqlens="uniform[1024,16384] seed 5, 32 sequences", scales="per row (amax/448)",
+                   tensors="K and V (2 launches per step)",
+                   l2="inputs 2 x %.0f MB bf16 > L2" % (n_tok * h_kv * hd * 2 / 1e6))
+        metric = "paged KV-cache write (quantise on write) us/call, a call = the K and V writes of 32 sequences"
         launches = 2
     else:
         seqlens = syn.uniform_seqlens(5, 32, 1024, 16384)
@@ -441,7 +467,7 @@ def run_secondary(args):
         "metric": metric, "value": round(avg * 1e3, 2), "unit": "us/call", "higher_is_better": False,
         "steps": args.steps, "warmup": args.warmup, "n_gpus": 1, "data": "synthetic", "config": cfg,
         "p10_us": round(ms[len(ms) // 10] * 1e3, 2), "p90_us": round(ms[(9 * len(ms)) // 10] * 1e3, 2),
-        "tflops": round(flops / (avg * 1e-3) / 1e12, 2),
+        "tflops": round(flops / (avg * 1e-3) / 1e12, 2) if flops else None,
         "roofline": dict(bound="hbm" if t_hbm >= t_tensor else "tensor",
                          achieved=round(nbytes / (avg * 1e-3) / 1e9, 1), peak=peaks["hbm"], unit="GB/s",
                          frac=round(nbytes / (avg * 1e-3) / 1e9 / peaks["hbm"], 4),
@@ -542,8 +568,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--dot", choices=["fp8", "bf16"], default="fp8")
-    ap.add_argument("--workload", choices=["mla", "sparse", "gqa"], default="mla",
-                    help="mla = the headline line; sparse / gqa = measurement legs of the other variants")
+    ap.add_argument("--workload", choices=["mla", "sparse", "gqa", "kvwrite"], default="mla",
+                    help="mla = the headline line; sparse / gqa / kvwrite = measurement legs of the other rows")
     ap.add_argument("--sq", type=int, default=2, help="query tokens of the sparse leg (2 or 16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (short runs under a profiler)")

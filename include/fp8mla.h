@@ -26,6 +26,12 @@
  *       (partial (max, sum_exp, weighted sum) triples, empty shards publish
  *       m = -inf, l = 0, acc = 0).
  *
+ * and the step that fills the cache:
+ *
+ *   fp8_paged_cache_write -- quantise new bf16 K or V rows into an E4M3
+ *       paged cache, with per-row scales amax / 448 or one given per-tensor
+ *       scale.  InfiniCore page, Summary: the paged_caching write kernel.
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every pointer argument that names a tensor is a DEVICE pointer unless
@@ -104,6 +110,7 @@ typedef enum {
 #define FP8MLA_DEV_BAD_PAGE 0x2u       /* block-table entry outside [0, num_pages) */
 #define FP8MLA_DEV_BAD_SEQLEN 0x4u     /* seqlen < 0 or more pages than the block table row */
 #define FP8MLA_DEV_BAD_INDEX 0x8u      /* top-k index outside [-1, num_tokens) */
+#define FP8MLA_DEV_BAD_SLOT 0x10u      /* cache-write slot >= num_blocks * page_size */
 
 /* ------------------------------------------------------------------ MLA ---
  * Work units.  The dense MLA kernel runs one work unit per pair of SMs (the
@@ -209,6 +216,45 @@ FP8MLA_API size_t paged_gqa_workspace_bytes(int bs, int h_q, int head_dim, int m
 /* Number of key shards paged_gqa_decode will use for these arguments
  * (num_splits as passed: 0 = auto).  Host-only, no device access. */
 FP8MLA_API int paged_gqa_num_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_splits);
+
+/* ---------------------------------------------------------- cache write ---
+ * fp8_paged_cache_write -- quantise-on-write of new K or V rows into an E4M3
+ * paged cache (InfiniCore "add FP8 blockwise dequantize/GEMM operators and
+ * FP8(E4M3) KV cache support in paged attention", Summary, paged_caching: a
+ * write kernel over (token, kv_head) rows; per-row scale amax / 448, 1 when
+ * amax is 0, kept in a float32 [num_blocks, h_kv, page] array).
+ *   x             bf16 (device): the row of token t, head h starts at element
+ *                 t * x_token_stride + h * head_dim and holds head_dim values;
+ *                 x 16-byte aligned, x_token_stride a multiple of 8 and
+ *                 >= h_kv * head_dim
+ *   slot_mapping  int32 [n_tokens] (device): token t goes to block
+ *                 slot / page_size, offset slot % page_size.  A negative slot
+ *                 skips the token; a slot >= num_blocks * page_size sets
+ *                 FP8MLA_DEV_BAD_SLOT and skips it.  Two tokens with the same
+ *                 slot race: which one lands is undefined.
+ *   cache         E4M3 bytes [num_blocks, h_kv, page_size, head_dim] (device,
+ *                 16-byte aligned).  The dense MLA cache [num_pages, 64, 576]
+ *                 is h_kv = 1, page_size = 64, head_dim = 576.
+ *   exactly one of
+ *     tensor_scale  float32 [1] (device): code = E4M3(fp32(x * inv)) with
+ *                   inv = fp32(1 / tensor_scale); the value must be a normal
+ *                   float > 0 (it is not read on the host)
+ *     token_scales  float32 [num_blocks, h_kv, page_size] (device): each
+ *                   written row gets scale = fp32(max|x| / 448) (1.0 when the
+ *                   row is all zeros), stored at its slot, and
+ *                   code = E4M3(fp32(x * inv)) with inv = fp32(448 / max|x|)
+ *                   (1.0 for a zero row); a row with max|x| < 2^-64 is first
+ *                   multiplied by 2^64 (exact), so inv stays finite
+ * Every float operation rounds to nearest even; E4M3 rounding is to nearest
+ * even with saturation to +-448.  x must be finite.  head_dim is a multiple
+ * of 8 in [8, 1024]; kv_dtype must be FP8MLA_KV_E4M3.  n_tokens = 0 is a
+ * no-op.  Bytes and scales of slots no token maps to are not touched.
+ * Asynchronous on `stream`; the caller owns every buffer. */
+FP8MLA_API fp8mla_status_t fp8_paged_cache_write(const void* x, int64_t x_token_stride, const int32_t* slot_mapping,
+                                                 int n_tokens, int h_kv, int head_dim, int page_size,
+                                                 int num_blocks, fp8mla_kv_dtype_t kv_dtype, void* cache,
+                                                 const float* tensor_scale, float* token_scales,
+                                                 fp8mla_stream_t stream);
 
 /* ------------------------------------------------------ no allocation ---
  * fp8mla_decode_no_alloc -- the dense MLA decode for callers that cannot

@@ -30,6 +30,7 @@ DEV_WAIT_TIMEOUT = 0x1
 DEV_BAD_PAGE = 0x2
 DEV_BAD_SEQLEN = 0x4
 DEV_BAD_INDEX = 0x8
+DEV_BAD_SLOT = 0x10
 
 MLA_D, MLA_DV, MLA_PAGE, MLA_ROWS = 576, 512, 64, 128
 
@@ -60,6 +61,7 @@ _SIGNATURES = {
     "paged_gqa_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "paged_gqa_num_splits": (_I, [_I, _I, _I, _I, _I]),
     "fp8mla_decode_no_alloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _F, _I, _P, _P, _I, _I, _I, _I, _P]),
+    "fp8_paged_cache_write": (_I, [_P, ctypes.c_int64, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "fp8mla_get_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "fp8mla_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -316,6 +318,48 @@ def paged_gqa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                                   bs, h_q, h_kv, hd, page, _stream(q.device)),
            "paged_gqa_decode")
     return out, lse
+
+
+# ------------------------------------------------------------ cache write --
+
+
+def paged_cache_write(x: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.Tensor, *,
+                      tensor_scale: torch.Tensor | None = None,
+                      token_scales: torch.Tensor | None = None) -> None:
+    """Quantise bf16 rows into an E4M3 paged cache, in place.
+
+    cache E4M3 (or uint8) [num_blocks, h_kv, page, head_dim] with x bf16
+    [n_tokens, h_kv, head_dim], or the dense MLA form [num_pages, page, d]
+    with x [n_tokens, d].  slot_mapping int32 [n_tokens] (block * page +
+    offset; negative = skip).  Exactly one of tensor_scale (float32 [1]) or
+    token_scales (float32 [num_blocks, h_kv, page], written per row) is given.
+    x may be strided along tokens; each token's rows must be contiguous."""
+    if cache.dim() == 3:
+        cache4 = cache.unsqueeze(1)
+        x3 = x.unsqueeze(1) if x.dim() == 2 else x
+    else:
+        cache4, x3 = cache, x
+    if not x3.is_cuda or x3.dtype != torch.bfloat16 or x3.dim() != 3:
+        raise ValueError("x must be a CUDA bf16 tensor [n_tokens, h_kv, head_dim] (or [n_tokens, d])")
+    _need(cache4, "cache", None, 4)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    num_blocks, h_kv, page, hd = cache4.shape
+    n_tokens = x3.shape[0]
+    if tuple(x3.shape[1:]) != (h_kv, hd) or slot_mapping.shape[0] != n_tokens:
+        raise ValueError("x, slot_mapping and cache shapes disagree")
+    if x3.stride(2) != 1 or (h_kv > 1 and x3.stride(1) != hd):
+        raise ValueError("each token's rows of x must be contiguous")
+    if tensor_scale is not None:
+        _need(tensor_scale, "tensor_scale", torch.float32)
+    if token_scales is not None:
+        _need(token_scales, "token_scales", torch.float32)
+        if tuple(token_scales.shape) != (num_blocks, h_kv, page):
+            raise ValueError("token_scales must be [num_blocks, h_kv, page]")
+    _check(lib().fp8_paged_cache_write(_ptr(x3), x3.stride(0) if n_tokens > 0 else h_kv * hd,
+                                       _ptr(slot_mapping), n_tokens, h_kv, hd, page, num_blocks,
+                                       kv_dtype_code(cache4), _ptr(cache4), _ptr(tensor_scale),
+                                       _ptr(token_scales), _stream(x3.device)),
+           "fp8_paged_cache_write")
 
 
 def last_device_error(device=None) -> int:

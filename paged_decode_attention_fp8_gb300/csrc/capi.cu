@@ -6,6 +6,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "cache_write.h"
 #include "fp8mla.h"
 #include "gqa_decode.h"
 #include "mla_decode.h"
@@ -248,11 +249,33 @@ fp8mla_status_t paged_gqa_decode(const void* q, const void* k_cache, const void*
                           page_size, reinterpret_cast<cudaStream_t>(stream));
 }
 
+fp8mla_status_t fp8_paged_cache_write(const void* x, int64_t x_token_stride, const int32_t* slot_mapping,
+                                      int n_tokens, int h_kv, int head_dim, int page_size, int num_blocks,
+                                      fp8mla_kv_dtype_t kv_dtype, void* cache, const float* tensor_scale,
+                                      float* token_scales, fp8mla_stream_t stream) {
+  fp8mla_status_t st = check_kv_dtype(kv_dtype);
+  if (st != FP8MLA_OK) return st;
+  CacheWriteArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.x_token_stride = x_token_stride;
+  a.slot_mapping = slot_mapping;
+  a.n_tokens = n_tokens;
+  a.h_kv = h_kv;
+  a.head_dim = head_dim;
+  a.page_size = page_size;
+  a.num_blocks = num_blocks;
+  a.cache = static_cast<uint8_t*>(cache);
+  a.tensor_scale = tensor_scale;
+  a.token_scales = token_scales;
+  return cache_write_entry(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 fp8mla_status_t fp8mla_get_last_device_error(fp8mla_stream_t stream, uint32_t* code_out) {
   if (code_out == nullptr) return FP8MLA_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8MLA_ERR_CUDA;
   *code_out = mla_read_and_clear_status() | metadata_read_and_clear_status() |
-              sparse_read_and_clear_status() | gqa_read_and_clear_status();
+              sparse_read_and_clear_status() | gqa_read_and_clear_status() |
+              cache_write_read_and_clear_status();
   return FP8MLA_OK;
 }
 

@@ -116,3 +116,27 @@ def test_python_dtype_mapping():
     assert fm.kv_dtype_code(torch.empty(1, dtype=torch.float8_e5m2)) == fm.KV_E5M2
     assert fm.kv_dtype_code(torch.empty(1, dtype=torch.int8)) == fm.KV_OTHER
     assert fm.kv_dtype_code(torch.empty(1, dtype=torch.bool)) == fm.KV_OTHER
+
+
+def _cache_write(**over):
+    a = dict(x=1 << 20, stride=1024, slots=1 << 20, n=4, h_kv=8, hd=128, page=16, blocks=64, dtype=fm.KV_E4M3,
+             cache=1 << 20, tscale=None, rscales=1 << 20)
+    a.update(over)
+    return fm.lib().fp8_paged_cache_write(a["x"], a["stride"], a["slots"], a["n"], a["h_kv"], a["hd"], a["page"],
+                                          a["blocks"], a["dtype"], a["cache"], a["tscale"], a["rscales"], None)
+
+
+@pytest.mark.parametrize("over", [dict(tscale=1 << 20), dict(rscales=None), dict(hd=12), dict(hd=0), dict(hd=1032),
+                                  dict(stride=1000), dict(stride=1020), dict(x=None), dict(slots=None),
+                                  dict(cache=None), dict(x=(1 << 20) + 8), dict(cache=(1 << 20) + 4),
+                                  dict(page=0), dict(blocks=0), dict(h_kv=0), dict(n=-1)])
+def test_cache_write_bad_arguments_refused(over):
+    assert _cache_write(**over) == 1
+
+
+def test_cache_write_refuses_foreign_encodings_and_empty_is_a_no_op():
+    assert _cache_write(dtype=fm.KV_E5M2) == 2
+    assert _cache_write(dtype=fm.KV_E4M3FNUZ) == 2
+    # nothing to write: accepted without touching the device (null pointers allowed)
+    assert _cache_write(n=0, x=None, slots=None, cache=None) == 0
+
