@@ -52,6 +52,30 @@ KERNEL_SOURCE = os.path.join(ROOT, "paged_decode_attention_fp8_gb300", "csrc", "
 # ----------------------------------------------------------- accounting ----
 
 
+def replica_seed(rank: int) -> int:
+    """Seed of rank's batch: every replica draws its own Q and KV values (the
+    sequence lengths stay those of seed 2, so every replica does the same work)."""
+    return 2 + 1000 * rank
+
+
+def slowest_rank_ms(ms: float, world: int, device=None) -> float:
+    """The timed region's length on the slowest rank: a MAX all-reduce over
+    the default process group (NCCL on GPUs, gloo in the CPU tests)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_replica: float, ms_per_step: float) -> float:
+    """TFLOPS of the whole job: the work of all `world` replicas over one step
+    of the slowest rank."""
+    return world * flops_per_replica / (ms_per_step * 1e-3) / 1e12
+
+
 def mla_flops(seqlens, s_q, h_q, d=MLA_D, dv=MLA_DV):
     """2 * s_q * h_q * s_k * (d + dv) per sequence (causal mask not discounted)."""
     return sum(2.0 * s_q * h_q * int(s) * (d + dv) for s in seqlens)
@@ -186,7 +210,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     w = WORKLOAD
     b, s_q, h_q = w["b"], w["s_q"], w["h_q"]
-    inp, seqlens, sets, bt, sl, scale = build_inputs(2 + 1000 * rank, dev)
+    inp, seqlens, sets, bt, sl, scale = build_inputs(replica_seed(rank), dev)
     units = fm.metadata_units()
     tile_sched = torch.empty((units, 8), dtype=torch.int32, device=dev)
     num_splits = torch.empty((b + 1,), dtype=torch.int32, device=dev)
@@ -235,11 +259,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = slowest_rank_ms(t0.elapsed_time(t1), world, dev)
     dec_ms = [a.elapsed_time(b_) for a, b_ in kernel_events]
     assert fm.last_device_error() == 0
 
@@ -247,7 +267,7 @@ def run_ours(args):
     flops = mla_flops(seqlens, s_q, h_q)
     nbytes = mla_bytes(seqlens, b, s_q, h_q)
     kv_bytes = sum(seqlens) * MLA_D
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms_per_step)
 
     peaks = measured_peaks()
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
@@ -339,6 +359,9 @@ def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, worl
     for i in range(3):
         step(i)
     torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -346,10 +369,10 @@ def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, worl
         step(i)
     t1.record(stream)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / steps
+    ms = slowest_rank_ms(t0.elapsed_time(t1), world, dev) / steps
     h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
-    return dict(value=round(world * flops / (ms * 1e-3) / 1e12, 2), unit="TFLOPS", ms_per_step=round(ms, 5),
+    return dict(value=round(whole_job_tflops(world, flops, ms), 2), unit="TFLOPS", ms_per_step=round(ms, 5),
                 h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h), steps=steps,
                 note="KV cache resident in HBM; per-step Q/block table/seqlens in, out/lse back")
 
