@@ -26,7 +26,9 @@ against the pages by eye:
   (aiter page, Results: 16 heads, rope-free 512, top-k 2048).
 * ``gqa_decode`` -- paged GQA decode with separate K and V caches
   [num_blocks, h_kv, page, head_dim] and per-tensor k_scale / v_scale
-  (InfiniCore page, Summary: the FP8 paged-attention decode kernel).
+  (InfiniCore page, Summary: the FP8 paged-attention decode kernel), or
+  per-row scales [num_blocks, h_kv, page] (the same page's scale layout);
+  ``mla_decode`` takes per-row scales [num_pages, 1, page] the same way.
 * ``partial_attention`` / ``merge_partials`` -- the split-KV algebra: each
   shard publishes (max, sum of exponentials, weighted sum) and the merge
   rescales by exp(m_s - M) (InfiniCore page, split-kv commit: "log2-domain
@@ -150,15 +152,33 @@ def mla_visible_keys(s_k: int, s_q: int, i: int, causal: bool) -> int:
     return max(0, s_k - s_q + i + 1) if causal else s_k
 
 
-def mla_gather_keys(kv_cache, block_table_row, s_k: int, kv_scale: float, page: int = 64):
-    """Dequantised keys [s_k, d] of one sequence, read page by page."""
+def key_scales(scale, pages, head: int, s_k: int):
+    """The dequantisation scale of each of a sequence's s_k keys.
+
+    ``scale`` is one float (per tensor) or an array [num_blocks, h_kv, page]
+    with one float per cached row (InfiniCore page, Summary: FP8 caches carry
+    scales of shape [num_blocks, num_kv_heads, block_size]); key j of the
+    sequence lives in block pages[j // page] at offset j % page.  Returns a
+    float or a column [s_k, 1]."""
+    if np.ndim(scale) == 0:
+        return float(scale)
+    sc = as_float64(scale)
+    if not pages:
+        return np.zeros((0, 1))
+    return np.concatenate([sc[p, head] for p in pages])[:s_k][:, None]
+
+
+def mla_gather_keys(kv_cache, block_table_row, s_k: int, kv_scale, page: int = 64):
+    """Dequantised keys [s_k, d] of one sequence, read page by page.  kv_scale:
+    one float, or per cached row [num_pages, 1, page]."""
     cache = as_bytes(kv_cache)
     n_pages = (s_k + page - 1) // page
-    rows = [cache[int(block_table_row[p])] for p in range(n_pages)]
+    pages = [int(block_table_row[p]) for p in range(n_pages)]
+    rows = [cache[p] for p in pages]
     if not rows:
         return np.zeros((0, cache.shape[-1]))
     keys = np.concatenate(rows, axis=0)[:s_k]
-    return e4m3_decode(keys) * float(kv_scale)
+    return e4m3_decode(keys) * key_scales(kv_scale, pages, 0, s_k)
 
 
 def mla_decode(q, kv_cache, block_table, seqlens, kv_scale, softmax_scale, causal,
@@ -218,7 +238,8 @@ def sparse_mla_decode(q, kv_cache, topk_idx, kv_scale, softmax_scale, tokens=Non
 
 def gqa_decode(q, k_cache, v_cache, block_table, seqlens, k_scale, v_scale, softmax_scale,
                batches=None):
-    """Paged GQA decode.  q [bs, h_q, hd]; caches [num_blocks, h_kv, page, hd]."""
+    """Paged GQA decode.  q [bs, h_q, hd]; caches [num_blocks, h_kv, page, hd];
+    k_scale / v_scale one float each, or per cached row [num_blocks, h_kv, page]."""
     q = as_float64(q)
     kc = as_bytes(k_cache)
     vc = as_bytes(v_cache)
@@ -235,8 +256,10 @@ def gqa_decode(q, k_cache, v_cache, block_table, seqlens, k_scale, v_scale, soft
         pages = [int(bt[bi, p]) for p in range(n_blocks)]
         for kvh in range(h_kv):
             if pages:
-                keys = e4m3_decode(np.concatenate([kc[p, kvh] for p in pages])[:s_k]) * float(k_scale)
-                vals = e4m3_decode(np.concatenate([vc[p, kvh] for p in pages])[:s_k]) * float(v_scale)
+                keys = e4m3_decode(np.concatenate([kc[p, kvh] for p in pages])[:s_k]) * \
+                    key_scales(k_scale, pages, kvh, s_k)
+                vals = e4m3_decode(np.concatenate([vc[p, kvh] for p in pages])[:s_k]) * \
+                    key_scales(v_scale, pages, kvh, s_k)
             else:
                 keys = np.zeros((0, hd))
                 vals = np.zeros((0, hd))
