@@ -29,6 +29,8 @@ against the pages by eye:
   (InfiniCore page, Summary: the FP8 paged-attention decode kernel), or
   per-row scales [num_blocks, h_kv, page] (the same page's scale layout);
   ``mla_decode`` takes per-row scales [num_pages, 1, page] the same way.
+* ``gqa_decode_ext`` -- the same with the XQA options of the FlashInfer page
+  (speculative-decoding block with a mask, sliding window, attention sinks).
 * ``partial_attention`` / ``merge_partials`` -- the split-KV algebra: each
   shard publishes (max, sum of exponentials, weighted sum) and the merge
   rescales by exp(m_s - M) (InfiniCore page, split-kv commit: "log2-domain
@@ -252,20 +254,90 @@ def gqa_decode(q, k_cache, v_cache, block_table, seqlens, k_scale, v_scale, soft
     lse = np.full((bs, h_q), np.nan)
     for bi in (range(bs) if batches is None else batches):
         s_k = int(sl[bi])
-        n_blocks = (s_k + page - 1) // page
-        pages = [int(bt[bi, p]) for p in range(n_blocks)]
         for kvh in range(h_kv):
-            if pages:
-                keys = e4m3_decode(np.concatenate([kc[p, kvh] for p in pages])[:s_k]) * \
-                    key_scales(k_scale, pages, kvh, s_k)
-                vals = e4m3_decode(np.concatenate([vc[p, kvh] for p in pages])[:s_k]) * \
-                    key_scales(v_scale, pages, kvh, s_k)
-            else:
-                keys = np.zeros((0, hd))
-                vals = np.zeros((0, hd))
+            keys, vals = gqa_gather(kc, vc, bt[bi], s_k, kvh, k_scale, v_scale)
             for h in range(kvh * group, (kvh + 1) * group):
                 scores = (keys @ q[bi, h]) * float(softmax_scale)
                 out[bi, h], lse[bi, h] = softmax_attention(scores, vals)
+    return out, lse
+
+
+def gqa_gather(kc, vc, block_table_row, s_k: int, kvh: int, k_scale, v_scale):
+    """Dequantised keys and values [s_k, hd] of one sequence and KV head."""
+    page, hd = kc.shape[2], kc.shape[3]
+    pages = [int(block_table_row[p]) for p in range((s_k + page - 1) // page)]
+    if not pages:
+        return np.zeros((0, hd)), np.zeros((0, hd))
+    keys = e4m3_decode(np.concatenate([kc[p, kvh] for p in pages])[:s_k]) * key_scales(k_scale, pages, kvh, s_k)
+    vals = e4m3_decode(np.concatenate([vc[p, kvh] for p in pages])[:s_k]) * key_scales(v_scale, pages, kvh, s_k)
+    return keys, vals
+
+
+def spec_visible(s_k: int, q_len: int, i: int, mask_row=None, window: int = 0) -> np.ndarray:
+    """Keys query token i of a speculative block sees (FlashInfer "add xqa fp8
+    mha and fp8 kv cache": the XQA mask gate).  The q_len query tokens are the
+    last q_len cache positions, token i at p = s_k - q_len + i.  Keys before
+    the block are always visible; key s_k - q_len + c of the block is visible
+    iff mask_row[c] (no mask: c <= i, the causal case).  A sliding window
+    W > 0 further keeps only keys with p - j < W.  Returns a bool [s_k]."""
+    j = np.arange(s_k)
+    start = s_k - q_len
+    vis = j < start
+    c = j - start
+    in_block = (c >= 0) & (c < q_len)
+    if mask_row is None:
+        vis |= in_block & (c <= i)
+    else:
+        m = np.asarray(mask_row, dtype=bool)
+        vis |= in_block & m[np.clip(c, 0, q_len - 1)]
+    if window > 0:
+        vis &= (start + i) - j < window
+    return vis
+
+
+def gqa_decode_ext(q, k_cache, v_cache, block_table, seqlens, k_scale, v_scale, softmax_scale,
+                   spec_mask=None, window: int = 0, sinks=None):
+    """Paged GQA decode with the XQA options of the FlashInfer page: a block of
+    q_len query tokens per sequence (q [bs, q_len, h_q, hd]) under a
+    speculative-decoding mask spec_mask [bs, q_len, q_len] (None: causal), a
+    sliding window (0: off) and attention sinks (one logit per query head,
+    None: off).
+
+    With a sink s_h, head h's softmax denominator gains e^{s_h} (a key with no
+    value): out = sum_j e^{s_j} v_j / (sum_j e^{s_j} + e^{s_h}) and
+    lse = ln(sum_j e^{s_j} + e^{s_h}).  A row that sees no key has out = 0 and
+    lse = s_h (-inf without a sink) -- zeros, not the mean of V (FlashInfer
+    page, review of masked rows).  Returns out [bs, q_len, h_q, hd] and lse
+    [bs, q_len, h_q]."""
+    q = as_float64(q)
+    kc = as_bytes(k_cache)
+    vc = as_bytes(v_cache)
+    bt = as_int64(block_table)
+    sl = as_int64(seqlens)
+    bs, q_len, h_q, hd = q.shape
+    h_kv = kc.shape[1]
+    group = h_q // h_kv
+    sk = None if sinks is None else as_float64(sinks)
+    out = np.zeros((bs, q_len, h_q, hd))
+    lse = np.full((bs, q_len, h_q), np.nan)
+    for bi in range(bs):
+        s_k = int(sl[bi])
+        for kvh in range(h_kv):
+            keys, vals = gqa_gather(kc, vc, bt[bi], s_k, kvh, k_scale, v_scale)
+            for i in range(q_len):
+                vis = spec_visible(s_k, q_len, i, None if spec_mask is None else as_int64(spec_mask)[bi, i],
+                                   window)
+                for h in range(kvh * group, (kvh + 1) * group):
+                    scores = (keys[vis] @ q[bi, i, h]) * float(softmax_scale)
+                    o, l = softmax_attention(scores, vals[vis])
+                    if sk is not None and sk[h] != -math.inf:
+                        # the sink joins the denominator (shifted by the larger exponent)
+                        m = max(l, sk[h])
+                        w_keys = math.exp(l - m) if l != -math.inf else 0.0
+                        denom = w_keys + math.exp(sk[h] - m)
+                        o = o * (w_keys / denom)
+                        l = m + math.log(denom)
+                    out[bi, i, h], lse[bi, i, h] = o, l
     return out, lse
 
 
