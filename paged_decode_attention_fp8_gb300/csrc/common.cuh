@@ -58,26 +58,6 @@ __device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Bounded wait until a shared-memory counter (published with st_release_cta)
-// reaches target; the same abort and limit rules as wait_bounded.
-__device__ __forceinline__ bool wait_counter_bounded(const uint32_t* ctr, uint32_t target,
-                                                     volatile uint32_t* abort_flag, uint32_t* status) {
-  if (ld_acquire_cta(ctr) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    __nanosleep(32);
-    if (ld_acquire_cta(ctr) >= target) return true;
-    if ((it & 31u) == 0) {
-      if (abort_flag != nullptr && *abort_flag) return false;
-      if (it > kWaitMinPolls && globaltimer_ns() - t0 > kWaitLimitNs) {
-        if (abort_flag != nullptr) *abort_flag = 1u;
-        atomicOr(status, FP8MLA_DEV_WAIT_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
 // Pages of a sequence; 0 (and a status bit) for a length the block table cannot hold.
 __device__ __forceinline__ int seq_pages(int s_k, int page, int max_pages, uint32_t* status) {
   if (s_k <= 0) {
