@@ -400,7 +400,8 @@ def run_secondary(args):
     stream = torch.cuda.current_stream(dev)
     peaks = measured_peaks()
     if args.workload == "sparse":
-        inp = syn.sparse_inputs(4, args.sq)
+        rule = "affine" if args.sq > 256 else "permutation"  # prefill-sized batches: vectorised index draw
+        inp = syn.sparse_inputs(4, args.sq, index_rule=rule)
         sets = [(inp.q.to(dev), inp.kv_cache.to(dev)) for _ in range(3)]
         idx = inp.topk_idx.to(dev)
         scale = torch.tensor([inp.kv_scale], dtype=torch.float32, device=dev)
@@ -417,7 +418,7 @@ def run_secondary(args):
         flops = 2.0 * s_q * h_q * topk * 1024
         t_tensor = flops / (2.0 * peaks["bf16"] * 1e12)
         cfg = dict(workload="sparse_topk_mla_decode", s_q=s_q, h_q=h_q, d=512, topk=topk, num_tokens=131072,
-                   dot="fp8", splits="auto", l2="3 rotating cache copies (192 MiB) > L2")
+                   dot="fp8", splits="auto", indices=rule, l2="3 rotating cache copies (192 MiB) > L2")
         metric = f"sparse top-k MLA decode us/call (s_q={s_q}, 16 heads, top-k 2048)"
         launches = 2
     elif args.workload == "kvwrite":
@@ -593,7 +594,8 @@ def main():
     ap.add_argument("--dot", choices=["fp8", "bf16"], default="fp8")
     ap.add_argument("--workload", choices=["mla", "sparse", "gqa", "kvwrite"], default="mla",
                     help="mla = the headline line; sparse / gqa / kvwrite = measurement legs of the other rows")
-    ap.add_argument("--sq", type=int, default=2, help="query tokens of the sparse leg (2 or 16)")
+    ap.add_argument("--sq", type=int, default=2,
+                    help="query tokens of the sparse leg (2 or 16 for decode, 16384 for the prefill-sized batch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (short runs under a profiler)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

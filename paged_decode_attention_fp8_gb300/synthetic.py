@@ -193,13 +193,32 @@ class SparseInputs:
 
 
 def sparse_inputs(seed: int, s_q: int, h_q: int = 16, num_tokens: int = 131072,
-                  topk: int = 2048) -> SparseInputs:
+                  topk: int = 2048, index_rule: str = "permutation") -> SparseInputs:
+    """Top-k sparse MLA inputs: each query token's topk distinct cache rows.
+
+    index_rule "permutation": token t takes the first topk entries of its own
+    seeded permutation of the rows.  "affine" (large batches, num_tokens a
+    power of two): one seeded permutation P of the rows, and token t takes
+    P[(a_t k + b_t) mod num_tokens] for k < topk with a_t odd -- distinct,
+    since multiplying by an odd number permutes the residues -- drawn for all
+    tokens at once."""
     vals = normal(seed, 2, (num_tokens, SPARSE_D))
     scale = per_tensor_scale(vals)
     cache = to_e4m3_bytes(vals, scale)
-    idx = np.empty((s_q, topk), dtype=np.int32)
-    for t in range(s_q):
-        idx[t] = permutation(seed, 100 + t, num_tokens)[:topk]
+    if index_rule == "permutation":
+        idx = np.empty((s_q, topk), dtype=np.int32)
+        for t in range(s_q):
+            idx[t] = permutation(seed, 100 + t, num_tokens)[:topk]
+    elif index_rule == "affine":
+        if num_tokens & (num_tokens - 1) or topk > num_tokens:
+            raise ValueError("the affine index rule needs a power-of-two cache of at least topk rows")
+        perm = permutation(seed, 99, num_tokens).astype(np.int64)
+        a = randint(seed, 97, s_q, 0, num_tokens // 2 - 1) * 2 + 1
+        b = randint(seed, 98, s_q, 0, num_tokens - 1)
+        k = np.arange(topk, dtype=np.int64)
+        idx = perm[(a[:, None] * k[None, :] + b[:, None]) & (num_tokens - 1)].astype(np.int32)
+    else:
+        raise ValueError(f"index rule {index_rule!r}")
     q = to_bf16(normal(seed, 3, (s_q, h_q, SPARSE_D)))
     return SparseInputs(q=q, kv_cache=torch.from_numpy(cache), topk_idx=torch.from_numpy(idx),
                         kv_scale=scale,
