@@ -309,3 +309,36 @@ def test_poisoned_slots_are_never_read():
     # the generator did poison: the tail of each last page is 0x7F
     last = inp.block_table[1, 0].item()
     assert np.all(inp.kv_cache[last, 5:].numpy() == 0x7F)
+
+
+def test_sparse_single_index_and_all_skipped():
+    # a list that names one row (the rest -1) returns that row and its own score;
+    # a list of only -1 sees no key: zeros and -inf
+    inp = syn.sparse_inputs(61, 2, num_tokens=4096, topk=64)
+    idx = np.full((2, 64), -1, dtype=np.int32)
+    idx[0, 37] = 1234
+    out, lse = oracle.sparse_mla_decode(inp.q, inp.kv_cache, idx, inp.kv_scale, inp.softmax_scale)
+    row = oracle.e4m3_decode(inp.kv_cache.numpy()[1234]) * inp.kv_scale
+    q = inp.q.float().numpy().astype(np.float64)
+    for h in range(q.shape[1]):
+        assert np.array_equal(out[0, h], row)
+        assert abs(lse[0, h] - math.fsum(q[0, h] * row) * inp.softmax_scale) < 1e-12
+    assert np.all(out[1] == 0) and np.all(lse[1] == -np.inf)
+
+
+def test_two_shard_merge_by_hand():
+    # shard A: m = 1, l = 2, acc = [2, 4]; shard B: m = 3, l = 1, acc = [1, 0]
+    # M = 3, L = 2 e^-2 + 1, out = (e^-2 [2, 4] + [1, 0]) / L, lse = 3 + ln L
+    out, lse = oracle.merge_partials([(1.0, 2.0, np.array([2.0, 4.0])), (3.0, 1.0, np.array([1.0, 0.0])),
+                                      (-math.inf, 0.0, np.zeros(2))])
+    big_l = 2.0 * math.exp(-2.0) + 1.0
+    assert np.allclose(out, [(2.0 * math.exp(-2.0) + 1.0) / big_l, 4.0 * math.exp(-2.0) / big_l], rtol=1e-15)
+    assert abs(lse - (3.0 + math.log(big_l))) < 1e-15
+    # a split of explicit scores agrees with the softmax written out
+    s = np.array([0.5, -1.0, 2.0, 0.0])
+    v = np.array([[1.0, 0.0], [0.0, 1.0], [2.0, 2.0], [-1.0, 3.0]])
+    direct = oracle.softmax_attention(s, v)
+    merged = oracle.merge_partials([oracle.partial_attention(s[:1], v[:1]), oracle.partial_attention(s[1:], v[1:])])
+    w = np.exp(s) / np.exp(s).sum()
+    assert np.allclose(direct[0], w @ v, rtol=1e-14) and np.allclose(merged[0], w @ v, rtol=1e-14)
+    assert abs(merged[1] - math.log(np.exp(s).sum())) < 1e-14
