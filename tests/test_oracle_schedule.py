@@ -90,3 +90,21 @@ def test_all_empty_batch():
     assert np.all(splits == 0)
     for u in range(5):
         assert unit_segments(sched[u], [0, 0, 0]) == []
+
+
+def test_balanced_rule_worked_by_hand():
+    # pages [10, 3] (64-token pages), 3 units, fixed cost 4 per sequence:
+    # cost line 14 + 7 = 21 positions; units start at floor(u * 21 / 3) = 0, 7, 14.
+    # position 0 -> sequence 0 page max(0, 0 - 4) = 0; position 7 -> sequence 0 page 3;
+    # position 14 -> sequence 1 page 0.  Unit 0 = seq 0 pages [0, 3), unit 1 = seq 0
+    # pages [3, 10) (its second piece), unit 2 = seq 1 whole; pieces per sequence 2 and 1.
+    sched, ns = oracle.schedule([640, 192], 3)
+    assert sched[:, :5].tolist() == [[0, 0, 0, 3, 0], [0, 3, 1, 0, 1], [1, 0, 2, 0, 0]]
+    assert ns.tolist() == [0, 2, 3]
+    # pages [2, 0, 5], 4 units: cost line 6 + 0 + 9 = 15; units start at positions
+    # 0, 3, 7, 11 -> (0, 0); (0, 0) [offset 3 < 4]; (2, 0) [offset 1 of sequence 2];
+    # (2, 1) [offset 5, page 5 - 4].  Unit 0 is empty, unit 1 = sequence 0 (sequence 1
+    # is empty), unit 2 = sequence 2 page 0, unit 3 = its pages [1, 5) as its second piece.
+    sched, ns = oracle.schedule([128, 0, 300], 4)
+    assert sched[:, :4].tolist() == [[0, 0, 0, 0], [0, 0, 2, 0], [2, 0, 2, 1], [2, 1, 3, 0]]
+    assert ns.tolist() == [0, 1, 1, 3]
