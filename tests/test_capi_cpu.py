@@ -140,3 +140,62 @@ def test_cache_write_refuses_foreign_encodings_and_empty_is_a_no_op():
     # nothing to write: accepted without touching the device (null pointers allowed)
     assert _cache_write(n=0, x=None, slots=None, cache=None) == 0
 
+
+
+def _gqa(**over):
+    a = dict(q=1 << 20, k=1 << 20, v=1 << 20, dtype=fm.KV_E4M3, nb=64, ks=1 << 20, vs=1 << 20, bt=1 << 20, mb=8,
+             sl=1 << 20, scale=0.08, splits=1, ws=1 << 20, ws_bytes=1 << 40, out=1 << 20, lse=1 << 20, bs=2,
+             h_q=32, h_kv=8, hd=128, page=16)
+    a.update(over)
+    return fm.lib().paged_gqa_decode(a["q"], a["k"], a["v"], a["dtype"], a["nb"], a["ks"], a["vs"], a["bt"], a["mb"],
+                                     a["sl"], a["scale"], a["splits"], a["ws"], a["ws_bytes"], a["out"], a["lse"],
+                                     a["bs"], a["h_q"], a["h_kv"], a["hd"], a["page"], None)
+
+
+@pytest.mark.parametrize("over", [dict(hd=64), dict(page=32), dict(h_q=30), dict(h_q=136), dict(splits=-1),
+                                  dict(scale=0.0), dict(nb=0), dict(mb=0), dict(q=None), dict(lse=None),
+                                  dict(k=(1 << 20) + 8), dict(splits=4, ws=None), dict(splits=4, ws=(1 << 20) + 64)])
+def test_gqa_shape_and_argument_refusals(over):
+    assert _gqa(**over) == 1
+
+
+def test_gqa_small_workspace_and_empty_batch():
+    assert _gqa(splits=4, ws_bytes=256) == 3
+    assert _gqa(bs=0, q=None, out=None, lse=None) == 0      # nothing to do, nothing touched
+
+
+def _sparse(**over):
+    a = dict(q=1 << 20, kv=1 << 20, dtype=fm.KV_E4M3, n=131072, idx=1 << 20, topk=2048, scale=1 << 20, sm=0.04,
+             splits=1, ws=1 << 20, ws_bytes=1 << 40, out=1 << 20, lse=1 << 20, dot=fm.DOT_FP8, s_q=2, h_q=16)
+    a.update(over)
+    return fm.lib().sparse_mla_decode(a["q"], a["kv"], a["dtype"], a["n"], a["idx"], a["topk"], a["scale"], a["sm"],
+                                      a["splits"], a["ws"], a["ws_bytes"], a["out"], a["lse"], a["dot"], a["s_q"],
+                                      a["h_q"], None)
+
+
+@pytest.mark.parametrize("over", [dict(h_q=17), dict(topk=0), dict(dot=fm.DOT_16BIT), dict(n=0), dict(sm=0.0),
+                                  dict(splits=-1), dict(q=None), dict(idx=None), dict(out=(1 << 20) + 4),
+                                  dict(n=1 << 31), dict(splits=4, ws=None)])
+def test_sparse_argument_refusals(over):
+    assert _sparse(**over) == 1
+
+
+def test_sparse_small_workspace_and_no_tokens():
+    assert _sparse(splits=4, ws_bytes=256) == 3
+    assert _sparse(s_q=0, q=None, out=None, lse=None) == 0
+
+
+def _no_alloc(**over):
+    a = dict(q=1 << 20, kv=1 << 20, dtype=fm.KV_E4M3, np_=16, bt=1 << 20, mp=8, sl=1 << 20, scale=1 << 20, sm=0.04,
+             causal=1, out=1 << 20, lse=1 << 20, dot=fm.DOT_FP8, b=2, s_q=2, h_q=64)
+    a.update(over)
+    return fm.lib().fp8mla_decode_no_alloc(a["q"], a["kv"], a["dtype"], a["np_"], a["bt"], a["mp"], a["sl"],
+                                           a["scale"], a["sm"], a["causal"], a["out"], a["lse"], a["dot"], a["b"],
+                                           a["s_q"], a["h_q"], None)
+
+
+def test_no_alloc_host_checks():
+    assert _no_alloc(b=65) == 3                 # beyond the fixed array: refused before any launch
+    assert _no_alloc(dtype=fm.KV_E5M2) == 2
+    assert _no_alloc(h_q=128) == 1              # s_q * h_q > 128
+    assert _no_alloc(b=0, q=None, out=None, lse=None) == 0
