@@ -199,3 +199,19 @@ def test_no_alloc_host_checks():
     assert _no_alloc(dtype=fm.KV_E5M2) == 2
     assert _no_alloc(h_q=128) == 1              # s_q * h_q > 128
     assert _no_alloc(b=0, q=None, out=None, lse=None) == 0
+
+
+def test_gqa_split_rule_on_the_host():
+    lib = fm.lib()
+    # forced: capped at the 128-token steps the longest context has
+    assert lib.paged_gqa_num_splits(1, 8, 16384, 152, 4) == 4
+    assert lib.paged_gqa_num_splits(1, 8, 256, 152, 8) == 2
+    # a grid that fills the GPU (32 x 8 = 256 CTAs >= 0.8 x 152): about six CTAs per SM,
+    # ceil(6 * 152 / 256) = 4 pieces, each at least 8 steps (16384 / 128 / 8 = 16 allows it)
+    assert lib.paged_gqa_num_splits(32, 8, 16384, 152, 0) == 4
+    assert lib.paged_gqa_num_splits(256, 8, 1024, 152, 0) == 1     # 8 steps: pieces would be shorter
+    # a small grid: the fewest pieces whose wave efficiency is within 85 % of the best up to 16;
+    # 8 CTAs x s pieces fit in one wave of 152 for s <= 16, efficiency 8 s / 152, best at 16,
+    # and 8 s / 152 >= 0.85 * 128 / 152 first at s = 14
+    assert lib.paged_gqa_num_splits(1, 8, 16384, 152, 0) == 14
+    assert lib.paged_gqa_num_splits(1, 8, 128, 152, 0) == 1        # one step: nothing to split
