@@ -53,9 +53,9 @@ def assert_close(metrics, mode):
 
 
 def record(name, metrics):
-    """Appends a parity result to gpurun_out/parity_metrics.jsonl when that folder exists."""
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    out = os.path.join(root, "gpurun_out")
-    if os.path.isdir(out):
+    """Appends a parity result to $PARITY_METRICS_DIR/parity_metrics.jsonl when
+    that variable names an existing folder (nothing is written otherwise)."""
+    out = os.environ.get("PARITY_METRICS_DIR", "")
+    if out and os.path.isdir(out):
         with open(os.path.join(out, "parity_metrics.jsonl"), "a") as f:
             f.write(json.dumps(dict(name=name, **metrics)) + "\n")
