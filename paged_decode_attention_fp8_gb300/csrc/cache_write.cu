@@ -239,17 +239,17 @@ FastDiv make_fast_div(int d) {
   return f;
 }
 
+// SM count of the current device, queried once per device (152 if unknown).
 int device_sms() {
-  static int sms[64] = {0};
+  static std::atomic<int> sms[64];  // zero-initialised: static storage
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 152;
-  if (sms[dev] == 0) {
-    int n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
-    sms[dev] = n;
+    sms[dev].store(n, std::memory_order_relaxed);
   }
-  return sms[dev];
+  return n;
 }
 
 template <int kL, int kC>

@@ -1,11 +1,13 @@
 // Shared constants and the bounded mbarrier wait used by every kernel.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <utility>
 
 #include "fp8mla.h"
+#include "host_util.h"
 #include "ptx.cuh"
 
 namespace fp8mla {
@@ -78,6 +80,15 @@ __device__ __forceinline__ int seq_pages(int s_k, int page, int max_pages, uint3
 __device__ __forceinline__ void warp_arrive(uint64_t* bar) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// once_per_device on the current device; a failing cudaGetDevice is returned.
+template <typename F>
+inline cudaError_t configure_once(std::atomic<uint64_t>& done, F&& set) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return once_per_device(done, dev, std::forward<F>(set));
 }
 
 // Launches `kernel` on `stream` as a programmatic dependent of the previous

@@ -676,17 +676,19 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   prm.group = h_q / h_kv;
   prm.splits = splits;
   prm.softmax_scale = softmax_scale;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(gqa::gqa_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(gqa::kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(gqa::gqa_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(gqa::kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(gqa::gqa_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(gqa::kSmemBytes)) != cudaSuccess)
-      return FP8MLA_ERR_CUDA;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
+  if (configure_once(configured, [] {
+        cudaError_t e = cudaFuncSetAttribute(gqa::gqa_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(gqa::kSmemBytes));
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(gqa::gqa_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(gqa::kSmemBytes));
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(gqa::gqa_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(gqa::kSmemBytes));
+        return e;
+      }) != cudaSuccess)
+    return FP8MLA_ERR_CUDA;
   const long long grid = static_cast<long long>(bs) * h_kv * splits;
   if (grid > 0x7FFFFFFFll) return FP8MLA_ERR_INVALID_ARG;
   auto kernel = prm.group <= 4 ? gqa::gqa_decode_kernel<4>

@@ -362,13 +362,12 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
                                 int32_t* num_splits, cudaStream_t stream) {
   const size_t smem = metadata_smem_bytes(b, num_units);
   if (smem > kMetadataMaxSmem) return cudaErrorInvalidValue;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kMetadataMaxSmem));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
+  const cudaError_t e = configure_once(configured, [] {
+    return cudaFuncSetAttribute(mla_metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kMetadataMaxSmem));
+  });
+  if (e != cudaSuccess) return e;
   mla_metadata_kernel<<<1, kMetaThreads, smem, stream>>>(seqlens, b, num_units, force_splits, tile_sched,
                                                          num_splits);
   return cudaGetLastError();

@@ -1288,26 +1288,24 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
 
 cudaError_t launch_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
                        cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(f8::smem_bytes()));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
+  const cudaError_t e = configure_once(configured, [] {
+    return cudaFuncSetAttribute(mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(f8::smem_bytes()));
+  });
+  if (e != cudaSuccess) return e;
   return launch_dependent(mla_fp8_kernel, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream, tm_lat,
                           tm_rope, prm);
 }
 
 cudaError_t launch_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
                          cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_16bit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes16()));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
+  const cudaError_t e = configure_once(configured, [] {
+    return cudaFuncSetAttribute(mla_decode_16bit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem_bytes16()));
+  });
+  if (e != cudaSuccess) return e;
   return launch_dependent(mla_decode_16bit_kernel, dim3(num_units * Cfg16::kParts), dim3(Cfg16::kThreads),
                           smem_bytes16(), stream, tm_lat, tm_rope, prm);
 }

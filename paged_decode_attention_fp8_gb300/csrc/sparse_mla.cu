@@ -622,13 +622,12 @@ fp8mla_status_t sparse_decode_entry(const void* q, const void* kv_cache, int64_t
   prm.h_q = h_q;
   prm.splits = splits;
   prm.chunks = (topk + sparse::kKeys - 1) / sparse::kKeys;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(sparse::sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sparse::kSmemBytes)) != cudaSuccess)
-      return FP8MLA_ERR_CUDA;
-    configured = true;
-  }
+  static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
+  if (configure_once(configured, [] {
+        return cudaFuncSetAttribute(sparse::sparse_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(sparse::kSmemBytes));
+      }) != cudaSuccess)
+    return FP8MLA_ERR_CUDA;
   if (launch_dependent(sparse::sparse_mla_kernel, dim3(s_q * splits), dim3(sparse::kThreads), sparse::kSmemBytes,
                        stream, tm, prm) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
