@@ -312,6 +312,10 @@ def run_ours(args):
         # per step: schedule, (FP8 dots: Q quantisation,) decode, combine
         "gpu_launches": (4 if dot == "fp8" else 3) * args.steps,
     }
+    if rank == 0 and world == 1 and not args.no_legs:
+        # the other rows of the path, each on its own workload (not part of the headline value)
+        del sets
+        res["legs"] = run_legs(dev, max(20, min(args.steps, 200)), 5)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(inp, seqlens, budget_s=args.cpu_budget)
     if rank == 0:
@@ -377,129 +381,227 @@ def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, worl
                 note="KV cache resident in HBM; per-step Q/block table/seqlens in, out/lse back")
 
 
-# ------------------------------------------- sparse / GQA measurement legs ----
+# ------------------------------------------------------- measurement legs ----
+#
+# Every other row of the path, timed on one GPU after the headline: each leg
+# builds its seeded inputs, times `steps` calls with CUDA events around each
+# call (after warm-up), and reports us/call with the roofline of its own
+# algorithmic bytes and flops.  L2: every leg reads more than L2 (129 MB) per
+# call or rotates input copies that together exceed it.
 
 
-def run_secondary(args):
-    """µs/call and roofline of the sparse top-k MLA, the paged GQA variant or the
-    paged KV-cache write (one GPU).
-
-    Sparse: 16 heads, d = dv = 512, 131072-token E4M3 cache, top-k 2048, s_q query
-    tokens, FP8 dots, auto split; three cache copies rotate (3 x 64 MiB > L2).
-    GQA: 32/8 heads, hd 128, page 16, bs 32 with contexts uniform in [1024, 16384],
-    16-bit dots, auto split; two copies of the ~570 MB caches rotate.
-    KV write: K and V rows (8 heads x 128, bf16) of the same 32 sequences
-    quantised into paged E4M3 caches with per-row scales; ~1.1 GB of input.
-    """
+def _time_calls(call, steps, warmup, stream):
     import torch
 
     import paged_decode_attention_fp8_gb300 as fm
-    from paged_decode_attention_fp8_gb300 import synthetic as syn
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream(dev)
-    peaks = measured_peaks()
-    if args.workload == "sparse":
-        rule = "affine" if args.sq > 256 else "permutation"  # prefill-sized batches: vectorised index draw
-        inp = syn.sparse_inputs(4, args.sq, index_rule=rule)
-        sets = [(inp.q.to(dev), inp.kv_cache.to(dev)) for _ in range(3)]
-        idx = inp.topk_idx.to(dev)
-        scale = torch.tensor([inp.kv_scale], dtype=torch.float32, device=dev)
-        s_q, h_q, topk = inp.q.shape[0], inp.q.shape[1], idx.shape[1]
-        ws = torch.empty((max(fm.sparse_workspace_bytes(s_q, h_q, topk, 0), 256),), dtype=torch.uint8, device=dev)
-        out = torch.empty((s_q, h_q, 512), dtype=torch.bfloat16, device=dev)
-        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=dev)
-
-        def call(i):
-            q, kv = sets[i % len(sets)]
-            fm.sparse_mla_decode(q, kv, idx, scale, inp.softmax_scale, out=out, lse=lse, workspace=ws)
-
-        nbytes = s_q * topk * 512 + 2 * s_q * h_q * 512 * 2 + s_q * h_q * 4 + s_q * topk * 4
-        flops = 2.0 * s_q * h_q * topk * 1024
-        t_tensor = flops / (2.0 * peaks["bf16"] * 1e12)
-        cfg = dict(workload="sparse_topk_mla_decode", s_q=s_q, h_q=h_q, d=512, topk=topk, num_tokens=131072,
-                   dot="fp8", splits="auto", indices=rule, l2="3 rotating cache copies (192 MiB) > L2")
-        metric = f"sparse top-k MLA decode us/call (s_q={s_q}, 16 heads, top-k 2048)"
-        launches = 2
-    elif args.workload == "kvwrite":
-        seqlens = syn.uniform_seqlens(5, 32, 1024, 16384)
-        kin, vin = syn.cache_write_inputs(5, seqlens), syn.cache_write_inputs(6, seqlens)
-        xk, xv = syn.materialise(kin, device=dev), syn.materialise(vin, device=dev)
-        slots = kin.slot_mapping.to(dev)
-        n_tok, h_kv, hd = xk.shape
-        caches = [torch.empty((kin.num_blocks, h_kv, 16, hd), dtype=torch.uint8, device=dev) for _ in range(2)]
-        scales = [torch.empty((kin.num_blocks, h_kv, 16), dtype=torch.float32, device=dev) for _ in range(2)]
-
-        def call(i):
-            fm.paged_cache_write(xk, slots, caches[0], token_scales=scales[0])
-            fm.paged_cache_write(xv, slots, caches[1], token_scales=scales[1])
-
-        # per step: K and V rows read (bf16), codes and per-row scales written, slot mapping read twice
-        nbytes = 2 * (n_tok * h_kv * hd * 3 + n_tok * h_kv * 4 + n_tok * 4)
-        flops = 0.0
-        t_tensor = 0.0
-        cfg = dict(workload="paged_kv_cache_write", tokens=n_tok, h_kv=h_kv, head_dim=hd, page=16,
-                   seqlens="uniform[1024,16384] seed 5, 32 sequences", scales="per row (amax/448)",
-                   tensors="K and V (2 launches per step)",
-                   l2="inputs 2 x %.0f MB bf16 > L2" % (n_tok * h_kv * hd * 2 / 1e6))
-        metric = "paged KV-cache write (quantise on write) us/call, a call = the K and V writes of 32 sequences"
-        launches = 2
-    else:
-        seqlens = syn.uniform_seqlens(5, 32, 1024, 16384)
-        inp = syn.gqa_inputs(5, 32, seqlens)
-        sets = [(inp.k_cache.to(dev), inp.v_cache.to(dev)) for _ in range(2)]
-        q, bt, sl = inp.q.to(dev), inp.block_table.to(dev), inp.seqlens.to(dev)
-        ks = torch.tensor([inp.k_scale], dtype=torch.float32, device=dev)
-        vs = torch.tensor([inp.v_scale], dtype=torch.float32, device=dev)
-        bs, h_q, hd = inp.q.shape
-        h_kv = inp.k_cache.shape[1]
-        splits = fm.gqa_num_splits(bs, h_kv, bt.shape[1] * 16)
-        ws = torch.empty((max(fm.gqa_workspace_bytes(bs, h_q, hd, splits), 256),), dtype=torch.uint8, device=dev)
-        out = torch.empty((bs, h_q, hd), dtype=torch.bfloat16, device=dev)
-        lse = torch.empty((bs, h_q), dtype=torch.float32, device=dev)
-
-        def call(i):
-            kc, vc = sets[i % len(sets)]
-            fm.paged_gqa_decode(q, kc, vc, bt, sl, ks, vs, inp.softmax_scale, num_splits=0, out=out, lse=lse,
-                                workspace=ws)
-
-        keys = sum(seqlens)
-        nbytes = keys * h_kv * hd * 2 + 2 * bs * h_q * hd * 2 + bs * h_q * 4 + sum((x + 15) // 16 for x in seqlens) * 4
-        flops = 2.0 * keys * h_q * hd * 2
-        t_tensor = flops / (peaks["bf16"] * 1e12)
-        cfg = dict(workload="paged_gqa_decode", bs=bs, h_q=h_q, h_kv=h_kv, head_dim=hd, page=16,
-                   seqlens="uniform[1024,16384] seed 5", dot="f16", splits=splits,
-                   l2="2 rotating cache copies (~1.1 GB) > L2")
-        metric = "paged GQA decode us/call (bs=32, 32/8 heads, hd 128, ctx U[1024,16384])"
-        launches = 1 if splits == 1 else 2
-    for i in range(args.warmup):
+    for i in range(warmup):
         call(i)
     torch.cuda.synchronize()
     assert fm.last_device_error() == 0
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     torch.cuda.synchronize()
-    for i in range(args.steps):
+    for i in range(steps):
         evs[i][0].record(stream)
-        call(i)
+        call(warmup + i)
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     assert fm.last_device_error() == 0
     ms = sorted(a.elapsed_time(b) for a, b in evs)
-    avg = sum(ms) / len(ms)
+    return sum(ms) / len(ms), ms
+
+
+def _leg_result(metric, avg_ms, ms, nbytes, flops_fp8, flops_16, peaks, cfg, launches):
     t_hbm = nbytes / (peaks["hbm"] * 1e9)
-    res = {
-        "metric": metric, "value": round(avg * 1e3, 2), "unit": "us/call", "higher_is_better": False,
-        "steps": args.steps, "warmup": args.warmup, "n_gpus": 1, "data": "synthetic", "config": cfg,
-        "p10_us": round(ms[len(ms) // 10] * 1e3, 2), "p90_us": round(ms[(9 * len(ms)) // 10] * 1e3, 2),
-        "tflops": round(flops / (avg * 1e-3) / 1e12, 2) if flops else None,
-        "roofline": dict(bound="hbm" if t_hbm >= t_tensor else "tensor",
-                         achieved=round(nbytes / (avg * 1e-3) / 1e9, 1), peak=peaks["hbm"], unit="GB/s",
-                         frac=round(nbytes / (avg * 1e-3) / 1e9 / peaks["hbm"], 4),
+    t_tensor = flops_fp8 / (2.0 * peaks["bf16"] * 1e12) + flops_16 / (peaks["bf16"] * 1e12)
+    flops = flops_fp8 + flops_16
+    achieved = nbytes / (avg_ms * 1e-3) / 1e9
+    return {
+        "metric": metric, "value": round(avg_ms * 1e3, 2), "unit": "us/call", "higher_is_better": False,
+        "config": cfg, "p10_us": round(ms[len(ms) // 10] * 1e3, 2),
+        "p90_us": round(ms[(9 * len(ms)) // 10] * 1e3, 2), "calls": len(ms),
+        "tflops": round(flops / (avg_ms * 1e-3) / 1e12, 2) if flops else None,
+        "roofline": dict(bound="hbm" if t_hbm >= t_tensor else "tensor", achieved=round(achieved, 1),
+                         peak=peaks["hbm"], unit="GB/s", frac=round(achieved / peaks["hbm"], 4),
                          algorithmic_bytes_per_launch=int(nbytes), t_hbm_us=round(t_hbm * 1e6, 2),
                          t_tensor_us=round(t_tensor * 1e6, 2),
-                         roofline_frac_of_time=round(max(t_hbm, t_tensor) / (avg * 1e-3), 4)),
+                         roofline_frac_of_time=round(max(t_hbm, t_tensor) / (avg_ms * 1e-3), 4)),
         "gpu_launches_per_call": launches,
     }
+
+
+def leg_mla(dev, peaks, steps, warmup, dot, seqlens, seed, label, value_pages=None):
+    """Dense MLA decode call (FP8 or 16-bit dots) on b = len(seqlens), s_q = 2, h_q = 64."""
+    import torch
+
+    import paged_decode_attention_fp8_gb300 as fm
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    b, s_q, h_q = len(seqlens), 2, 64
+    inp = syn.mla_inputs(seed, b, s_q, h_q, seqlens, causal=True, spare_pages=16, value_pages=value_pages)
+    kv_bytes = sum(seqlens) * MLA_D
+    copies = max(1, min(3, math.ceil(2 * 129e6 / kv_bytes)))
+    kvs = [inp.kv_cache.to(dev) for _ in range(copies)]
+    q, bt, sl = inp.q.to(dev), inp.block_table.to(dev), inp.seqlens.to(dev)
+    scale = torch.tensor([inp.kv_scale], dtype=torch.float32, device=dev)
+    units = fm.metadata_units()
+    ts, ns = fm.get_metadata(sl, h_q, s_q, num_units=units)
+    out = torch.empty((b, s_q, h_q, MLA_DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=dev)
+    ws = torch.empty((fm.workspace_bytes(b, s_q, h_q, units),), dtype=torch.uint8, device=dev)
+
+    def call(i):
+        fm.decode(q, kvs[i % copies], bt, sl, scale, inp.softmax_scale, True, ts, ns, dot_mode=dot, out=out,
+                  lse=lse, workspace=ws)
+
+    avg, ms = _time_calls(call, steps, warmup, torch.cuda.current_stream(dev))
+    f8, f16 = mla_split_flops(seqlens, s_q, h_q)
+    if dot != "fp8":
+        f8, f16 = 0.0, f8 + f16
+    cfg = dict(workload="mla_decode", b=b, s_q=s_q, h_q=h_q, d=576, dv=512, page=64, seqlens=label, causal=True,
+               dot=dot, l2=f"{copies} rotating cache copies ({copies * kv_bytes / 1e6:.0f} MB)",
+               values="pooled N(0,1) pages" if value_pages else "N(0,1)")
+    res = _leg_result(f"dense MLA decode us/call ({label}, {dot} dots)", avg, ms, mla_bytes(seqlens, b, s_q, h_q),
+                      f8, f16, peaks, cfg, 3 if dot == "fp8" else 2)
+    res["tflops_convention"] = round(mla_flops(seqlens, s_q, h_q) / (avg * 1e-3) / 1e12, 1)
+    return res
+
+
+def leg_sparse(dev, peaks, steps, warmup, s_q):
+    import torch
+
+    import paged_decode_attention_fp8_gb300 as fm
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    rule = "affine" if s_q > 256 else "permutation"  # prefill-sized batches: vectorised index draw
+    inp = syn.sparse_inputs(4, s_q, index_rule=rule)
+    sets = [(inp.q.to(dev), inp.kv_cache.to(dev)) for _ in range(3)]
+    idx = inp.topk_idx.to(dev)
+    scale = torch.tensor([inp.kv_scale], dtype=torch.float32, device=dev)
+    h_q, topk = inp.q.shape[1], idx.shape[1]
+    ws = torch.empty((max(fm.sparse_workspace_bytes(s_q, h_q, topk, 0), 256),), dtype=torch.uint8, device=dev)
+    out = torch.empty((s_q, h_q, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((s_q, h_q), dtype=torch.float32, device=dev)
+
+    def call(i):
+        q, kv = sets[i % len(sets)]
+        fm.sparse_mla_decode(q, kv, idx, scale, inp.softmax_scale, out=out, lse=lse, workspace=ws)
+
+    avg, ms = _time_calls(call, steps, warmup, torch.cuda.current_stream(dev))
+    nbytes = s_q * topk * 512 + 2 * s_q * h_q * 512 * 2 + s_q * h_q * 4 + s_q * topk * 4
+    flops = 2.0 * s_q * h_q * topk * 1024
+    cfg = dict(workload="sparse_topk_mla_decode", s_q=s_q, h_q=h_q, d=512, topk=topk, num_tokens=131072,
+               dot="fp8", splits="auto", indices=rule, l2="3 rotating cache copies (192 MiB) > L2")
+    launches = 1 if fm.sparse_workspace_bytes(s_q, h_q, topk, 0) == 0 else 2
+    return _leg_result(f"sparse top-k MLA decode us/call (s_q={s_q}, 16 heads, top-k 2048)", avg, ms, nbytes,
+                       flops, 0.0, peaks, cfg, launches)
+
+
+def leg_gqa(dev, peaks, steps, warmup):
+    import torch
+
+    import paged_decode_attention_fp8_gb300 as fm
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    seqlens = syn.uniform_seqlens(5, 32, 1024, 16384)
+    inp = syn.gqa_inputs(5, 32, seqlens, value_blocks=4096)
+    sets = [(inp.k_cache.to(dev), inp.v_cache.to(dev)) for _ in range(2)]
+    q, bt, sl = inp.q.to(dev), inp.block_table.to(dev), inp.seqlens.to(dev)
+    ks = torch.tensor([inp.k_scale], dtype=torch.float32, device=dev)
+    vs = torch.tensor([inp.v_scale], dtype=torch.float32, device=dev)
+    bs, h_q, hd = inp.q.shape
+    h_kv = inp.k_cache.shape[1]
+    splits = fm.gqa_num_splits(bs, h_kv, bt.shape[1] * 16)
+    ws = torch.empty((max(fm.gqa_workspace_bytes(bs, h_q, hd, splits), 256),), dtype=torch.uint8, device=dev)
+    out = torch.empty((bs, h_q, hd), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((bs, h_q), dtype=torch.float32, device=dev)
+
+    def call(i):
+        kc, vc = sets[i % len(sets)]
+        fm.paged_gqa_decode(q, kc, vc, bt, sl, ks, vs, inp.softmax_scale, num_splits=0, out=out, lse=lse,
+                            workspace=ws)
+
+    avg, ms = _time_calls(call, steps, warmup, torch.cuda.current_stream(dev))
+    keys = sum(seqlens)
+    nbytes = keys * h_kv * hd * 2 + 2 * bs * h_q * hd * 2 + bs * h_q * 4 + sum((x + 15) // 16 for x in seqlens) * 4
+    flops = 2.0 * keys * h_q * hd * 2
+    cfg = dict(workload="paged_gqa_decode", bs=bs, h_q=h_q, h_kv=h_kv, head_dim=hd, page=16,
+               seqlens="uniform[1024,16384] seed 5", dot="f16", splits=splits,
+               values="pooled N(0,1) blocks", l2="2 rotating cache copies (~1.1 GB) > L2")
+    return _leg_result("paged GQA decode us/call (bs=32, 32/8 heads, hd 128, ctx U[1024,16384])", avg, ms, nbytes,
+                       0.0, flops, peaks, cfg, 1 if splits == 1 else 2)
+
+
+def leg_kvwrite(dev, peaks, steps, warmup):
+    import torch
+
+    import paged_decode_attention_fp8_gb300 as fm
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    seqlens = syn.uniform_seqlens(5, 32, 1024, 16384)
+    kin, vin = syn.cache_write_inputs(5, seqlens), syn.cache_write_inputs(6, seqlens)
+    xk, xv = syn.materialise(kin, device=dev), syn.materialise(vin, device=dev)
+    slots = kin.slot_mapping.to(dev)
+    n_tok, h_kv, hd = xk.shape
+    caches = [torch.empty((kin.num_blocks, h_kv, 16, hd), dtype=torch.uint8, device=dev) for _ in range(2)]
+    scales = [torch.empty((kin.num_blocks, h_kv, 16), dtype=torch.float32, device=dev) for _ in range(2)]
+
+    def call(i):
+        fm.paged_cache_write(xk, slots, caches[0], token_scales=scales[0])
+        fm.paged_cache_write(xv, slots, caches[1], token_scales=scales[1])
+
+    avg, ms = _time_calls(call, steps, warmup, torch.cuda.current_stream(dev))
+    # per call: K and V rows read (bf16), codes and per-row scales written, slot mapping read twice
+    nbytes = 2 * (n_tok * h_kv * hd * 3 + n_tok * h_kv * 4 + n_tok * 4)
+    cfg = dict(workload="paged_kv_cache_write", tokens=n_tok, h_kv=h_kv, head_dim=hd, page=16,
+               seqlens="uniform[1024,16384] seed 5, 32 sequences", scales="per row (amax/448)",
+               tensors="K and V (2 launches per call)",
+               l2="inputs 2 x %.0f MB bf16 > L2" % (n_tok * h_kv * hd * 2 / 1e6))
+    return _leg_result("paged KV-cache write (quantise on write) us/call, a call = the K and V writes of "
+                       "32 sequences", avg, ms, nbytes, 0.0, 0.0, peaks, cfg, 2)
+
+
+def run_leg(name, dev, peaks, steps, warmup):
+    from paged_decode_attention_fp8_gb300 import synthetic as syn
+    if name == "mla_bf16":
+        return leg_mla(dev, peaks, steps, warmup, "bf16", syn.uniform_seqlens(2, 64, 2048, 6144), 2,
+                       "uniform[2048,6144] seed 2")
+    if name == "mla_fixed4096":
+        return leg_mla(dev, peaks, steps, warmup, "fp8", [4096] * 64, 12, "fixed 4096")
+    if name.startswith("mla_long_b"):
+        b = int(name[len("mla_long_b"):])
+        return leg_mla(dev, peaks, steps, warmup, "fp8", [8196] * b, 3, "fixed 8196", value_pages=512)
+    if name.startswith("sparse_sq"):
+        return leg_sparse(dev, peaks, steps, warmup, int(name[len("sparse_sq"):]))
+    if name == "gqa_bs32":
+        return leg_gqa(dev, peaks, steps, warmup)
+    if name == "kvwrite":
+        return leg_kvwrite(dev, peaks, steps, warmup)
+    raise ValueError(name)
+
+
+LEGS = ("mla_bf16", "mla_fixed4096", "mla_long_b32", "mla_long_b48", "mla_long_b64", "mla_long_b128",
+        "sparse_sq2", "sparse_sq16", "sparse_sq16384", "gqa_bs32", "kvwrite")
+
+
+def run_legs(dev, steps, warmup, names=LEGS):
+    import gc
+
+    import torch
+    peaks = measured_peaks()
+    legs = {}
+    for name in names:
+        leg_steps = min(steps, 30) if name == "sparse_sq16384" else steps
+        legs[name] = run_leg(name, dev, peaks, leg_steps, warmup)
+        gc.collect()
+        torch.cuda.empty_cache()
+    return legs
+
+
+def run_secondary(args):
+    """One leg as its own JSON line (``--workload``)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    names = {"sparse": f"sparse_sq{args.sq}", "gqa": "gqa_bs32", "kvwrite": "kvwrite",
+             "mla_bf16": "mla_bf16", "mla_fixed4096": "mla_fixed4096", "mla_long": f"mla_long_b{args.b}"}
+    res = run_leg(names[args.workload], dev, measured_peaks(), args.steps, args.warmup)
+    res.update(steps=args.steps, warmup=args.warmup, n_gpus=1, data="synthetic")
     print(json.dumps(res), flush=True)
 
 
@@ -592,10 +694,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--dot", choices=["fp8", "bf16"], default="fp8")
-    ap.add_argument("--workload", choices=["mla", "sparse", "gqa", "kvwrite"], default="mla",
-                    help="mla = the headline line; sparse / gqa / kvwrite = measurement legs of the other rows")
+    ap.add_argument("--workload", choices=["mla", "sparse", "gqa", "kvwrite", "mla_bf16", "mla_fixed4096", "mla_long"],
+                    default="mla", help="mla = the headline line (which also carries every leg under 'legs'); "
+                    "the others print one measurement leg alone")
     ap.add_argument("--sq", type=int, default=2,
                     help="query tokens of the sparse leg (2 or 16 for decode, 16384 for the prefill-sized batch)")
+    ap.add_argument("--b", type=int, default=64, help="batch of the mla_long leg (32, 48, 64 or 128)")
+    ap.add_argument("--no-legs", action="store_true", help="headline only (skip the other rows' legs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (short runs under a profiler)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

@@ -173,22 +173,32 @@ FP8MLA_API fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp
 /* ----------------------------------------------------------- sparse MLA ---
  * sparse_mla_decode -- query token t attends to the cache rows
  * topk_idx[t][0..topk) (an index of -1 is skipped), d = dv = 512 rope-free.
- *   q            bf16 [s_q, h_q, 512], h_q <= 16... multiple of 1, h_q <= 64
- *   kv_cache     E4M3 bytes [num_tokens, 512]
- *   topk_idx     int32 [s_q, topk]
+ *   q            bf16 [s_q, h_q, 512], 1 <= h_q <= 16 (the heads are the N
+ *                dimension of one MMA tile); h_q > 16 -> FP8MLA_ERR_INVALID_ARG
+ *   kv_cache     E4M3 bytes [num_tokens, 512], num_tokens < 2^31
+ *   topk_idx     int32 [s_q, topk]; an index outside [-1, num_tokens) sets
+ *                FP8MLA_DEV_BAD_INDEX and the key is skipped
  *   kv_scale     float32 [1] (device), NULL refused
- *   num_splits   0 = auto, 1 = no split-K (one pass over all keys), k > 1 =
- *                keys cut into k contiguous shards merged by the combine step
+ *   num_splits   0 = auto (about one CTA per SM over s_q tokens, at most one
+ *                split per 128-key chunk), 1 = no split-K (one pass over all
+ *                keys), k > 1 = keys cut into k contiguous shards merged by
+ *                the combine step
  *   workspace    >= sparse_mla_workspace_bytes(s_q, h_q, topk, num_splits)
+ *                bytes, 256-byte aligned; may be NULL when that is 0
  *   out          bf16 [s_q, h_q, 512]; lse float32 [s_q, h_q]
- *   dot_mode     FP8MLA_DOT_FP8 (Q quantised per row, P as E4M3(128 p)) or
- *                FP8MLA_DOT_16BIT */
+ *   dot_mode     must be FP8MLA_DOT_FP8 (Q quantised per row with a
+ *                power-of-two scale, P as E4M3(128 p)); FP8MLA_DOT_16BIT is
+ *                refused with FP8MLA_ERR_INVALID_ARG (this variant runs the
+ *                aiter page's FP8-dot path only) */
 FP8MLA_API fp8mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype,
                                   int64_t num_tokens, const int32_t* topk_idx, int topk, const float* kv_scale,
                                   float softmax_scale, int num_splits, void* workspace, size_t workspace_bytes,
                                   void* out, float* lse, fp8mla_dot_mode_t dot_mode, int s_q, int h_q,
                                   fp8mla_stream_t stream);
 
+/* Workspace bytes of sparse_mla_decode with these arguments: the split
+ * partials of the split count the call will choose (auto uses the SM count
+ * of the current device); 0 when that is a single split. */
 FP8MLA_API size_t sparse_mla_workspace_bytes(int s_q, int h_q, int topk, int num_splits);
 
 /* ------------------------------------------------------------------ GQA ---

@@ -720,17 +720,19 @@ __device__ __forceinline__ void fill_q_row(const MlaParams& prm, int b, int r, i
 }
 // Quantised Q for FP8 dots in the ring's Q-slot layout, one grid ahead of the
 // decode kernel: grid (b, 4), 256 threads, eight threads per row, 32 rows per
-// CTA.  It lets the decode kernel start its prologue at once, and completes
-// only after the grid it was launched behind (so that the decode kernel's
-// wait on this grid also covers the tile schedule written before it).
+// CTA.  It is the first kernel of a decode call and is launched as a
+// programmatic dependent of whatever the caller enqueued before (which may
+// have written Q), so it waits for that work before reading Q; it lets the
+// decode kernel start its prologue at once, and the decode kernel's wait on
+// this grid then also covers the tile schedule written before it.
 __global__ void __launch_bounds__(256) mla_qprep_kernel(const MlaParams prm) {
   griddep_launch_dependents();
+  griddep_wait();
   const int b = blockIdx.x;
   const int r = blockIdx.y * 32 + threadIdx.x / 8;
   uint8_t* q = prm.qbuf + static_cast<size_t>(b) * kMlaQBytes;
   fill_q_row<8>(prm, b, r, threadIdx.x % 8, q, q + kQLatSlotBytes, q + 2 * kQLatSlotBytes, q + kQErrOff,
                 prm.qscale + static_cast<size_t>(b) * kRows);
-  griddep_wait();
 }
 
 // Lanes in groups of N (N = 4 or 8) each hold N 16-byte pieces; afterwards

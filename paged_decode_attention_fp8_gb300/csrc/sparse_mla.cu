@@ -575,11 +575,11 @@ int sparse_choose_splits(int s_q, int topk, int num_splits) {
 
 size_t sparse_workspace_bytes(int s_q, int h_q, int topk, int num_splits) {
   (void)h_q;
-  if (s_q < 1 || topk < 1) return 0;
-  const int chunks = (topk + sparse::kKeys - 1) / sparse::kKeys;
-  // a forced split count is capped at the chunk count; auto takes at most one split per chunk
-  const int splits = num_splits > 0 ? std::min(num_splits, chunks) : chunks;
-  return sparse::layout(s_q, splits).total;
+  if (s_q < 1 || topk < 1 || num_splits < 0) return 0;
+  // the split count the decode call will choose (auto: from the current
+  // device's SM count); one split writes no partials and needs no workspace
+  const int splits = sparse_choose_splits(s_q, topk, num_splits);
+  return splits > 1 ? sparse::layout(s_q, splits).total : 0;
 }
 
 fp8mla_status_t sparse_decode_entry(const void* q, const void* kv_cache, int64_t num_tokens, const int32_t* topk_idx,

@@ -129,12 +129,11 @@ class MLAInputs:
         return self.q.shape[2]
 
 
-def mla_inputs(seed: int, b: int, s_q: int, h_q: int, seqlens, causal: bool = True,
-               spare_pages: int = 0, softmax_scale: float | None = None,
-               page_order: np.ndarray | None = None) -> MLAInputs:
-    """Paged MLA decode inputs.  ``seqlens`` is a list of cache lengths."""
-    seqlens = np.asarray(seqlens, dtype=np.int64)
-    assert seqlens.shape == (b,)
+def _mla_layout(seed: int, seqlens: np.ndarray, spare_pages: int, page_order=None):
+    """Page placement shared by the MLA generators: (num_pages, used pages,
+    pages per sequence, block table) with the used pages at a seeded random
+    permutation of the pool and every unused table entry naming a spare page."""
+    b = seqlens.shape[0]
     n_pages = (seqlens + MLA_PAGE - 1) // MLA_PAGE
     used = int(n_pages.sum())
     num_pages = max(used + spare_pages, 1)
@@ -142,27 +141,81 @@ def mla_inputs(seed: int, b: int, s_q: int, h_q: int, seqlens, causal: bool = Tr
     max_pages = max(int(n_pages.max()) if b else 1, 1)
     fill = int(perm[used]) if num_pages > used else 0
     block_table = np.full((b, max_pages), fill, dtype=np.int32)
-    cache = np.full((num_pages, MLA_PAGE, MLA_D), POISON_BYTE, dtype=np.uint8)
-
-    vals = normal(seed, 2, (max(used, 1) * MLA_PAGE, MLA_D))[: used * MLA_PAGE]
-    valid = np.zeros(used * MLA_PAGE, dtype=bool)
     k = 0
     for i in range(b):
         for p in range(int(n_pages[i])):
             block_table[i, p] = perm[k + p]
+        k += int(n_pages[i])
+    return num_pages, used, n_pages, block_table
+
+
+def _mla_valid(seqlens: np.ndarray, used: int, n_pages: np.ndarray) -> np.ndarray:
+    """[used * 64] mask of the rows that hold a key (the used pages in sequence order)."""
+    valid = np.zeros(used * MLA_PAGE, dtype=bool)
+    k = 0
+    for i in range(seqlens.shape[0]):
         lo = k * MLA_PAGE
         valid[lo: lo + int(seqlens[i])] = True
         k += int(n_pages[i])
-    scale = per_tensor_scale(vals[valid])
-    enc = to_e4m3_bytes(vals, scale)
+    return valid
+
+
+def _mla_place(enc: np.ndarray, valid: np.ndarray, num_pages: int, used: int, n_pages: np.ndarray,
+               block_table: np.ndarray) -> np.ndarray:
+    """The cache [num_pages, 64, 576]: the used pages' encoded rows (sequence
+    order) at their block-table entries, 0x7F everywhere else."""
+    enc = enc.reshape(used * MLA_PAGE, MLA_D)
     enc[~valid] = POISON_BYTE
     enc = enc.reshape(used, MLA_PAGE, MLA_D)
+    cache = np.full((num_pages, MLA_PAGE, MLA_D), POISON_BYTE, dtype=np.uint8)
     k = 0
-    for i in range(b):
+    for i in range(n_pages.shape[0]):
         for p in range(int(n_pages[i])):
             cache[block_table[i, p]] = enc[k + p]
         k += int(n_pages[i])
+    return cache
 
+
+def _mla_cache(vals: np.ndarray, seqlens: np.ndarray, num_pages: int, used: int, n_pages: np.ndarray,
+               block_table: np.ndarray, scale: float | None = None):
+    """E4M3 cache [num_pages, 64, 576] holding ``vals`` (the used pages'
+    rows in sequence order), every slot past a sequence end and every spare
+    page poisoned with 0x7F; the scale is amax / 448 over the valid rows
+    unless given."""
+    valid = _mla_valid(seqlens, used, n_pages)
+    if scale is None:
+        scale = per_tensor_scale(vals[valid])
+    cache = _mla_place(to_e4m3_bytes(vals, scale), valid, num_pages, used, n_pages, block_table)
+    return cache, scale
+
+
+def mla_inputs(seed: int, b: int, s_q: int, h_q: int, seqlens, causal: bool = True,
+               spare_pages: int = 0, softmax_scale: float | None = None,
+               page_order: np.ndarray | None = None, value_pages: int | None = None) -> MLAInputs:
+    """Paged MLA decode inputs.  ``seqlens`` is a list of cache lengths.
+
+    Every cached value is an N(0, 1) draw.  By default each used page gets
+    its own draws; with ``value_pages`` = n (large batches, e.g. 128 x 8196
+    tokens) n distinct pages of draws are made and every used page copies
+    one of them, chosen by a seeded index, so the generator's time and host
+    memory stay bounded (the kernels see ordinary pages; which pages share
+    values does not matter to them, and the oracle reads the same bytes)."""
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    assert seqlens.shape == (b,)
+    num_pages, used, n_pages, block_table = _mla_layout(seed, seqlens, spare_pages, page_order)
+    if value_pages is None:
+        vals = normal(seed, 2, (max(used, 1) * MLA_PAGE, MLA_D))[: used * MLA_PAGE]
+        cache, scale = _mla_cache(vals, seqlens, num_pages, used, n_pages, block_table)
+    else:
+        # amax / 448 over the valid rows from the pool's per-row maxima; the
+        # pool is encoded once and its pages copied
+        pool = normal(seed, 2, (value_pages, MLA_PAGE, MLA_D))
+        pick = randint(seed, 4, max(used, 1), 0, value_pages - 1)[:used]
+        valid = _mla_valid(seqlens, used, n_pages)
+        row_amax = np.abs(pool).max(axis=2)[pick].reshape(-1)
+        amax = float(row_amax[valid].max()) if valid.any() else 0.0
+        scale = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+        cache = _mla_place(to_e4m3_bytes(pool, scale)[pick], valid, num_pages, used, n_pages, block_table)
     q = to_bf16(normal(seed, 3, (b, s_q, h_q, MLA_D)))
     if softmax_scale is None:
         softmax_scale = float(np.float32(1.0 / math.sqrt(MLA_D)))
@@ -170,6 +223,51 @@ def mla_inputs(seed: int, b: int, s_q: int, h_q: int, seqlens, causal: bool = Tr
                      block_table=torch.from_numpy(block_table),
                      seqlens=torch.from_numpy(seqlens.astype(np.int32)),
                      kv_scale=scale, softmax_scale=softmax_scale, causal=causal)
+
+
+def mla_peaky_inputs(seed: int, b: int = 2, h_q: int = 64, s_k: int = 2048,
+                     spare_pages: int = 4) -> MLAInputs:
+    """Dense MLA inputs in which one key per sequence scores +9 above the
+    others (s_q = 1, no causal mask): the sparse peaky construction carried
+    over to the 576-wide rows.
+
+    Latent dims [0, 256) carry the score and [256, 512) the values; Q is 0 on
+    dims [256, 576) (so the RoPE keys, N(0, 1), add nothing).  Tail keys are 0
+    on [0, 256) and w + 0.1 N(0, 1) on [256, 512); the peak key (at a seeded
+    position) holds kappa on dim 0, 0 on [1, 256) and z on [256, 512).
+    kappa is the cache's largest magnitude, so it encodes to exactly 448 and
+    the peak scores softmax_scale * 7 * 448 * kv_scale = 9 up to float32
+    rounding of the scales, every tail key exactly 0.  With s_k = 2048 the
+    2047 tail keys carry e^-9 * 2047 / (1 + e^-9 * 2047) = 0.2017 of the
+    weight, so the output on [256, 512) is about 0.8 z + 0.2 w."""
+    seqlens = np.full(b, s_k, dtype=np.int64)
+    num_pages, used, n_pages, block_table = _mla_layout(seed, seqlens, spare_pages)
+    softmax_scale = float(np.float32(1.0 / math.sqrt(MLA_D)))
+    kappa = PEAKY_MARGIN / (softmax_scale * PEAKY_Q0)
+    kv_scale = float(np.float32(kappa / E4M3_MAX))
+    half = SPARSE_D // 2
+    w = normal(seed, 11, (half,))
+    z = normal(seed, 12, (half,))
+    vals = np.zeros((used * MLA_PAGE, MLA_D))
+    vals[:, 512:] = normal(seed, 15, (used * MLA_PAGE, MLA_D - 512))
+    peaks = randint(seed, 14, b, 0, s_k - 1)
+    k = 0
+    for i in range(b):
+        lo = k * MLA_PAGE
+        vals[lo:lo + s_k, half:512] = w[None, :] + 0.1 * normal(seed, 20 + i, (s_k, half))
+        j = lo + int(peaks[i])
+        vals[j, :512] = 0.0
+        vals[j, 0] = E4M3_MAX * kv_scale
+        vals[j, half:512] = z
+        k += int(n_pages[i])
+    cache, _ = _mla_cache(vals, seqlens, num_pages, used, n_pages, block_table, scale=kv_scale)
+    q = np.zeros((b, 1, h_q, MLA_D))
+    q[..., 0] = PEAKY_Q0
+    q[..., 1:half] = normal(seed, 30, (b, 1, h_q, half - 1))
+    return MLAInputs(q=to_bf16(q), kv_cache=torch.from_numpy(cache),
+                     block_table=torch.from_numpy(block_table),
+                     seqlens=torch.from_numpy(seqlens.astype(np.int32)),
+                     kv_scale=kv_scale, softmax_scale=softmax_scale, causal=False)
 
 
 def uniform_seqlens(seed: int, b: int, lo: int, hi: int) -> list[int]:
@@ -283,7 +381,14 @@ class GQAInputs:
 
 
 def gqa_inputs(seed: int, bs: int, seqlens, h_q: int = 32, h_kv: int = 8, hd: int = 128,
-               page: int = 16, spare_blocks: int = 0) -> GQAInputs:
+               page: int = 16, spare_blocks: int = 0, value_blocks: int | None = None) -> GQAInputs:
+    """Paged GQA decode inputs: separate E4M3 K and V caches [num_blocks,
+    h_kv, page, hd], each with its per-tensor scale amax / 448 over the
+    valid rows; the used blocks sit at a seeded random permutation of the
+    pool, spare blocks and slots past a sequence end hold 0x7F.  With
+    ``value_blocks`` = n, n distinct blocks of N(0, 1) draws are made per
+    cache and every used block copies one of them (seeded choice), which
+    bounds the generator's time and memory for large batches."""
     seqlens = np.asarray(seqlens, dtype=np.int64)
     n_blocks = (seqlens + page - 1) // page
     used = int(n_blocks.sum())
@@ -292,26 +397,33 @@ def gqa_inputs(seed: int, bs: int, seqlens, h_q: int = 32, h_kv: int = 8, hd: in
     max_blocks = max(int(n_blocks.max()) if bs else 1, 1)
     fill = int(perm[used]) if num_blocks > used else 0
     block_table = np.full((bs, max_blocks), fill, dtype=np.int32)
-    valid = np.zeros((used, page), dtype=bool)
-    k = 0
-    for i in range(bs):
-        for p in range(int(n_blocks[i])):
-            block_table[i, p] = perm[k + p]
-            valid[k + p, : min(page, int(seqlens[i]) - p * page)] = True
-        k += int(n_blocks[i])
+    # used block u belongs to sequence seq[u] as its logical block lp[u]
+    seq = np.repeat(np.arange(bs), n_blocks)
+    first = np.concatenate([[0], np.cumsum(n_blocks)[:-1]]).astype(np.int64) if bs else np.zeros(0, np.int64)
+    lp = np.arange(used) - np.repeat(first, n_blocks)
+    block_table[seq, lp] = perm[:used]
+    rows_valid = np.minimum(page, seqlens[seq] - lp * page) if used else np.zeros(0, np.int64)
+    valid = np.arange(page)[None, :] < rows_valid[:, None]
     caches, scales = [], []
     for purpose in (2, 4):
-        vals = normal(seed, purpose, (max(used, 1), h_kv, page, hd))[:used]
-        vmask = np.broadcast_to(valid[:, None, :, None], vals.shape)
-        scale = per_tensor_scale(vals[vmask])
-        enc = to_e4m3_bytes(vals, scale)
+        if value_blocks is None:
+            vals = normal(seed, purpose, (max(used, 1), h_kv, page, hd))[:used]
+            vmask = np.broadcast_to(valid[:, None, :, None], vals.shape)
+            scale = per_tensor_scale(vals[vmask])
+            enc = to_e4m3_bytes(vals, scale)
+        else:
+            # the same amax / 448 over the valid rows, taken from per-row maxima
+            # of the pool; the pool is encoded once and its blocks copied
+            pool = normal(seed, purpose, (value_blocks, h_kv, page, hd))
+            pick = randint(seed, purpose + 10, max(used, 1), 0, value_blocks - 1)[:used]
+            row_amax = np.abs(pool).max(axis=3)[pick]  # [used, h_kv, page]
+            amax = float(row_amax[np.broadcast_to(valid[:, None, :], row_amax.shape)].max()) if used else 0.0
+            scale = float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+            enc = to_e4m3_bytes(pool, scale)[pick]
+            vmask = np.broadcast_to(valid[:, None, :, None], enc.shape)
         enc[~vmask] = POISON_BYTE
         cache = np.full((num_blocks, h_kv, page, hd), POISON_BYTE, dtype=np.uint8)
-        k = 0
-        for i in range(bs):
-            for p in range(int(n_blocks[i])):
-                cache[block_table[i, p]] = enc[k + p]
-            k += int(n_blocks[i])
+        cache[perm[:used]] = enc
         caches.append(torch.from_numpy(cache))
         scales.append(scale)
     q = to_bf16(normal(seed, 3, (bs, h_q, hd)))

@@ -4,6 +4,17 @@ Tolerances (from the target stated for this path): relative L2 <= 1e-2 with
 16-bit dots, <= 5e-2 with FP8 Q/P dots and cosine >= 0.999; |delta lse| <=
 2e-3 over rows with a finite reference LSE; rows whose reference LSE is
 -inf must come back exactly 0 with LSE -inf.
+
+The whole-tensor rel-L2 can hide one wrong output row: at the 8 192-row
+headline shape a row that is entirely wrong moves the tensor's rel-L2 by
+only ~1.5e-2.  So every row (one query token of one head) is also held to
+its own bound, ``row_rel_l2`` = 3x the tensor bound.  The aiter sparse_mla
+page (Accuracy) reports the FP8-dot error as 3.4 % (N(0, 1) data) to 4.5 %
+(the peaky case) of the output, an average over rows; a single row of 512
+values can sit a few times above that average, and 3x leaves room for it
+while a wrong row (rel-L2 near 1 or above: a wrong value slice, a dropped
+or doubled split) fails by an order of magnitude.  The observed maxima are
+recorded with every parity result.
 """
 
 import json
@@ -13,8 +24,8 @@ import os
 import numpy as np
 
 TOL = {
-    "fp8": dict(rel_l2=5e-2, cos=0.999, lse=2e-3),
-    "bf16": dict(rel_l2=1e-2, cos=0.9999, lse=2e-3),
+    "fp8": dict(rel_l2=5e-2, cos=0.999, lse=2e-3, row_rel_l2=0.15),
+    "bf16": dict(rel_l2=1e-2, cos=0.9999, lse=2e-3, row_rel_l2=3e-2),
 }
 
 
@@ -39,6 +50,17 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, mode, mask=None):
     nrm = np.linalg.norm(ol.ravel()) * den
     res["cos"] = float(np.dot(ol.ravel(), rl.ravel()) / nrm) if nrm > 0 else 1.0
     res["lse_max_abs"] = float(np.max(np.abs(l[live] - lse_ref[live]))) if live.any() else 0.0
+    # per-row rel-L2 over the last (value) dimension; rows whose reference is
+    # all zeros are held to an absolute bound of the same size
+    if live.any():
+        rows_o = ol.reshape(-1, ol.shape[-1])
+        rows_r = rl.reshape(-1, rl.shape[-1])
+        rn = np.linalg.norm(rows_r, axis=1)
+        dn = np.linalg.norm(rows_o - rows_r, axis=1)
+        per_row = np.where(rn > 0, dn / np.where(rn > 0, rn, 1.0), dn)
+        res["row_rel_l2_max"] = float(np.max(per_row))
+    else:
+        res["row_rel_l2_max"] = 0.0
     res["finite"] = bool(np.all(np.isfinite(o)) and np.all(np.isfinite(l[live])))
     return res
 
@@ -50,6 +72,7 @@ def assert_close(metrics, mode):
     assert metrics["rel_l2"] <= tol["rel_l2"], metrics
     assert metrics["cos"] >= tol["cos"], metrics
     assert metrics["lse_max_abs"] <= tol["lse"], metrics
+    assert metrics["row_rel_l2_max"] <= tol["row_rel_l2"], metrics
 
 
 def record(name, metrics):

@@ -117,14 +117,42 @@ def test_headline_mtp_decode(mode):
     check(inp, mode, name=f"headline_b64_sq2_{mode}")
 
 
-def test_fixed_long_cache_b32_sampled():
-    inp = syn.mla_inputs(3, 32, 2, 64, [8196] * 32, causal=True)
+@pytest.mark.parametrize("b", [32, 48, 64, 128])
+def test_fixed_long_cache_sampled(b):
+    # the FlashMLA page's H20 table: cache 8196, MTP = 2, 64 heads, FP8 dots;
+    # the whole batch runs, four sequences spread over it are checked
+    inp = syn.mla_inputs(3, b, 2, 64, [8196] * b, causal=True, value_pages=512)
     out, lse = run_mla(inp, "fp8")
-    picks = [0, 7, 19, 31]
+    picks = [0, b // 3, (2 * b) // 3, b - 1]
     ro, rl = ref(inp, batches=picks)
     m = compare(out[picks], lse[picks], ro[picks], rl[picks], "fp8")
-    record("long_b32_sk8196_fp8_sampled", m)
+    record(f"long_b{b}_sk8196_fp8_sampled", m)
     assert_close(m, "fp8")
+    assert fm.last_device_error() == 0
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_fixed_4096_mtp_decode(mode):
+    # the FlashMLA page's H800 run: b = 64, s_q = 2, every s_k = 4096, causal
+    inp = syn.mla_inputs(12, 64, 2, 64, [4096] * 64, causal=True, spare_pages=16)
+    check(inp, mode, name=f"fixed_b64_sq2_sk4096_{mode}")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_peaky_tail_kept_with_split_off(mode):
+    # one key +9 above 2047 that carry a fifth of the output (aiter page,
+    # Accuracy), on the dense kernel: its P scale (E4M3(64 p) with FP8 dots)
+    # must keep the tail, which an unscaled E4M3 P would flush
+    inp = syn.mla_peaky_inputs(13, b=2, h_q=64, s_k=2048)
+    out, lse = run_mla(inp, mode, force_splits=1)
+    ro, rl = ref(inp)
+    m = compare(out, lse, ro, rl, mode)
+    record(f"dense_peaky_splits1_{mode}", m)
+    assert_close(m, mode)
+    mv = compare(out[..., 256:], lse, ro[..., 256:], rl, mode)
+    record(f"dense_peaky_value_dims_{mode}", mv)
+    assert mv["rel_l2"] < (5e-2 if mode == "fp8" else 1e-2)
+    assert fm.last_device_error() == 0
 
 
 # --------------------------------------------------------- invariances ----
@@ -188,3 +216,22 @@ def test_bad_page_index_is_reported_not_faulted():
     run_mla(inp, "fp8")
     assert fm.last_device_error() & fm.DEV_BAD_PAGE
     assert fm.last_device_error() == 0   # read-and-clear
+
+
+def test_q_written_just_before_the_call_is_seen():
+    # Q is produced by a torch kernel on the same stream right before the
+    # FP8-dot call (as a projection GEMM would leave it): the call's first
+    # kernel must wait for that write before it reads Q
+    inp = syn.mla_inputs(14, 8, 2, 64, syn.uniform_seqlens(14, 8, 100, 3000), causal=True)
+    d = to_dev(inp)
+    src = d["q"].clone()
+    ts, ns = fm.get_metadata(d["sl"], inp.h_q, inp.s_q)
+    ro, rl = ref(inp)
+    for _ in range(3):
+        q = torch.zeros_like(src)
+        torch.cuda.synchronize()
+        q.add_(src * 1.0)  # two torch kernels, enqueued just ahead of the decode
+        out, lse = fm.decode(q, d["kv"], d["bt"], d["sl"], d["scale"], inp.softmax_scale, True, ts, ns,
+                             dot_mode="fp8")
+        torch.cuda.synchronize()
+        assert_close(compare(out, lse, ro, rl, "fp8"), "fp8")

@@ -43,3 +43,36 @@ def test_unscaled_p_loses_the_tail_scaled_keeps_it():
     err_unscaled = rel(_quantised_p_attention(inp, 1.0))
     assert err_scaled < 0.03
     assert err_unscaled > 0.15
+
+
+def _dense_quantised_p_attention(inp, p_scale):
+    """The dense MLA analogue: one softmax over a sequence's whole cache,
+    p quantised as E4M3(p_scale * p), V = the first 512 dims of each key."""
+    q = inp.q.double().numpy()[:, 0]  # s_q = 1
+    cache = inp.kv_cache.numpy()
+    bt = inp.block_table.numpy()
+    outs = []
+    for i, s_k in enumerate(inp.seqlens.numpy()):
+        pages = bt[i, : (s_k + 63) // 64]
+        keys = (e4m3_decode(cache[pages]) * inp.kv_scale).reshape(-1, 576)[:s_k]
+        s = q[i] @ keys.T * inp.softmax_scale
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        pq = torch.from_numpy((p * p_scale).astype(np.float32)).to(torch.float8_e4m3fn).double().numpy()
+        outs.append((pq @ keys[:, :512]) / (p.sum(axis=1, keepdims=True) * p_scale))
+    return np.stack(outs)[:, None]
+
+
+def test_dense_peaky_case_closed_form_and_p_scale():
+    # the dense construction reproduces the page's numbers: the peak key's
+    # weight 1 / (1 + 2047 e^-9) and lse = 9 + ln(1 + 2047 e^-9)
+    inp = syn.mla_peaky_inputs(5, b=2, h_q=8)
+    ref, lse = oracle.mla_decode(inp.q, inp.kv_cache, inp.block_table, inp.seqlens, inp.kv_scale,
+                                 inp.softmax_scale, False)
+    assert np.allclose(lse, 9.0 + np.log1p(2047 * np.exp(-9.0)), atol=1e-5)
+
+    def rel(x):
+        return np.linalg.norm((x - ref)[..., 256:]) / np.linalg.norm(ref[..., 256:])
+
+    # E4M3(64 p) keeps the tail (the dense kernel's P scale), E4M3(p) flushes it
+    assert rel(_dense_quantised_p_attention(inp, 64.0)) < 0.03
+    assert rel(_dense_quantised_p_attention(inp, 1.0)) > 0.15

@@ -92,3 +92,20 @@ def test_out_of_range_index_reported():
     idx[0, 5] = 5000
     run(inp, 1, idx)
     assert fm.last_device_error() & fm.DEV_BAD_INDEX
+
+
+def test_prefill_scale_sampled():
+    # the aiter page's prefill leg: 16 384 query tokens, 16 heads, top-k 2048
+    # over a 131 072-token E4M3 cache (indices by the affine rule); the whole
+    # batch runs with the automatic split choice, 24 tokens spread over it
+    # are checked against the oracle one by one
+    inp = syn.sparse_inputs(4, 16384, index_rule="affine")
+    assert fm.sparse_workspace_bytes(16384, 16, 2048, 0) < (1 << 30)
+    out, lse = run(inp, num_splits=0)
+    picks = sorted({int(x) for x in np.linspace(0, 16383, 24)})
+    ro, rl = oracle.sparse_mla_decode(inp.q, inp.kv_cache, inp.topk_idx, inp.kv_scale, inp.softmax_scale,
+                                      tokens=picks)
+    m = compare(out[picks], lse[picks], ro[picks], rl[picks], "fp8")
+    record("sparse_prefill_sq16384_sampled", m)
+    assert_close(m, "fp8")
+    assert fm.last_device_error() == 0

@@ -33,3 +33,43 @@ def test_cache_write_slots_are_distinct_and_follow_pages():
     # consecutive tokens of a sequence share a block until the page fills
     first = real[:17]
     assert np.all(first[:16] // 16 == first[0] // 16) and np.all(first % 16 == np.arange(17) % 16)
+
+
+def _decoded(codes):
+    from oracle.attention import e4m3_decode  # the oracle's table, used here only to read bytes back
+    return e4m3_decode(codes)
+
+
+def test_pooled_mla_values_keep_the_scale_rule_and_the_poison():
+    sl = [8196, 100, 5, 700, 0]
+    inp = syn.mla_inputs(3, len(sl), 2, 64, sl, causal=True, spare_pages=2, value_pages=8)
+    cache, bt = inp.kv_cache.numpy(), inp.block_table.numpy()
+    valid = []
+    for i, s_k in enumerate(sl):
+        for p in range((s_k + 63) // 64):
+            rows = cache[bt[i, p]]
+            n = min(64, s_k - 64 * p)
+            valid.append(rows[:n])
+            assert np.all(rows[n:] == syn.POISON_BYTE)
+    v = _decoded(np.concatenate(valid))
+    assert np.all(np.isfinite(v))
+    assert np.max(np.abs(v)) == 448.0       # amax / 448 over the valid rows: the largest encodes to 448
+    # seeded, and the pool is shared between pages (bounded distinct values)
+    again = syn.mla_inputs(3, len(sl), 2, 64, sl, causal=True, spare_pages=2, value_pages=8)
+    assert np.array_equal(cache, again.kv_cache.numpy())
+
+
+def test_pooled_gqa_values_keep_the_scale_rule_and_the_poison():
+    sl = [1024, 17, 300]
+    inp = syn.gqa_inputs(5, 3, sl, spare_blocks=2, value_blocks=4)
+    for cache in (inp.k_cache.numpy(), inp.v_cache.numpy()):
+        bt = inp.block_table.numpy()
+        valid = []
+        for i, s_k in enumerate(sl):
+            for p in range((s_k + 15) // 16):
+                blk = cache[bt[i, p]]
+                n = min(16, s_k - 16 * p)
+                valid.append(blk[:, :n].reshape(-1, 128))
+                assert np.all(blk[:, n:] == syn.POISON_BYTE)
+        v = _decoded(np.concatenate(valid))
+        assert np.all(np.isfinite(v)) and np.max(np.abs(v)) == 448.0
