@@ -302,6 +302,13 @@ FP8MLA_API fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
  * recorded since the last call on the current device, and clears them. */
 FP8MLA_API fp8mla_status_t fp8mla_get_last_device_error(fp8mla_stream_t stream, uint32_t* code_out);
 
+/* Diagnostics of FP8MLA_DEV_WAIT_TIMEOUT in the dense MLA decode: synchronises
+ * `stream` and writes where[0..2] = {source line of the wait, block index,
+ * thread index} of the first bounded wait that ran out since the last call
+ * on the current device (all 0 if none ran out), then clears the record.
+ * where: host pointer to 3 uint32_t. */
+FP8MLA_API fp8mla_status_t fp8mla_get_wait_timeout_site(fp8mla_stream_t stream, uint32_t* where);
+
 /* Static string naming a status code. */
 FP8MLA_API const char* fp8mla_status_string(fp8mla_status_t status);
 

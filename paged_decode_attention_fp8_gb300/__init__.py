@@ -63,6 +63,7 @@ _SIGNATURES = {
     "fp8mla_decode_no_alloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _F, _I, _P, _P, _I, _I, _I, _I, _P]),
     "fp8_paged_cache_write": (_I, [_P, ctypes.c_int64, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "fp8mla_get_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "fp8mla_get_wait_timeout_site": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "fp8mla_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -360,6 +361,14 @@ def paged_cache_write(x: torch.Tensor, slot_mapping: torch.Tensor, cache: torch.
                                        kv_dtype_code(cache4), _ptr(cache4), _ptr(tensor_scale),
                                        _ptr(token_scales), _stream(x3.device)),
            "fp8_paged_cache_write")
+
+
+def wait_timeout_site(device=None):
+    """(source line, block, thread) of the first dense-MLA bounded wait that ran out
+    since the last call, or None (synchronises the current stream; clears the record)."""
+    where = (ctypes.c_uint32 * 3)()
+    _check(lib().fp8mla_get_wait_timeout_site(_stream(device), where), "fp8mla_get_wait_timeout_site")
+    return None if where[0] == 0 else (where[0], where[1], where[2])
 
 
 def last_device_error(device=None) -> int:

@@ -115,6 +115,13 @@ using namespace fp8mla;
 
 extern "C" {
 
+fp8mla_status_t fp8mla_get_wait_timeout_site(fp8mla_stream_t stream, uint32_t* where) {
+  if (where == nullptr) return FP8MLA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8MLA_ERR_CUDA;
+  mla_read_and_clear_timeout_site(where);
+  return FP8MLA_OK;
+}
+
 const char* fp8mla_status_string(fp8mla_status_t s) {
   switch (s) {
     case FP8MLA_OK: return "ok";

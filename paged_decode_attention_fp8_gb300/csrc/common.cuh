@@ -14,27 +14,62 @@ namespace fp8mla {
 
 // A wait that has not completed after this long is treated as a hang: the
 // kernel records FP8MLA_DEV_WAIT_TIMEOUT and stops instead of spinning on.
+// The limit lives in device memory (one copy per translation unit) so that a
+// test can shorten it for the kernels of one file (fp8mla_test_fault_injection).
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint32_t kWaitMinPolls = 1u << 16;
+static __device__ uint64_t g_wait_limit_ns = kWaitLimitNs;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
+// The first bounded wait of this translation unit's kernels that ran out:
+// {site (a source line), block, thread, recorded}; read and cleared by the host.
+static __device__ uint32_t g_timeout_where[4];
+
+__device__ __forceinline__ void record_timeout_site(uint32_t site) {
+  if (atomicCAS(&g_timeout_where[3], 0u, 1u) == 0u) {
+    g_timeout_where[0] = site;
+    g_timeout_where[1] = blockIdx.x;
+    g_timeout_where[2] = threadIdx.x;
+  }
+}
+
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_probe_try(uint64_t* bar, uint32_t parity) {
+  if constexpr (kCluster)
+    return mbar_try_wait_cl(bar, parity);
+  else
+    return mbar_try_wait(bar, parity);
+}
+
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_probe_test(uint64_t* bar, uint32_t parity) {
+  if constexpr (kCluster)
+    return mbar_test_wait_cl(bar, parity);
+  else
+    return mbar_test_wait(bar, parity);
+}
+
 // Bounded wait on an mbarrier phase.  Returns false (without waiting further)
 // once *abort_flag is set by any thread of the CTA, or after the limit, in
-// which case it sets the flag and the status bit itself.
+// which case it sets the flag and the status bit itself.  kCluster: the
+// barrier receives arrivals from other CTAs of the cluster, and completing
+// the wait acquires their released writes at cluster scope.
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                             uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                             uint32_t* status, uint32_t site = 0) {
+  if (mbar_probe_try<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_probe_try<kCluster>(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (it > kWaitMinPolls && globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (it > kWaitMinPolls && globaltimer_ns() - t0 > *(volatile uint64_t*)&g_wait_limit_ns) {
         if (abort_flag != nullptr) *abort_flag = 1u;
         atomicOr(status, FP8MLA_DEV_WAIT_TIMEOUT);
+        record_timeout_site(site);
         return false;
       }
     }
@@ -43,17 +78,19 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
 
 // The same contract as wait_bounded, but polling with the non-blocking probe:
 // for waits on the critical path, where a suspended thread wakes up late.
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                          uint32_t* status) {
-  if (mbar_test_wait(bar, parity)) return true;
+                                          uint32_t* status, uint32_t site = 0) {
+  if (mbar_probe_test<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_test_wait(bar, parity)) return true;
+    if (mbar_probe_test<kCluster>(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
-      if (it > kWaitMinPolls && globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (it > kWaitMinPolls && globaltimer_ns() - t0 > *(volatile uint64_t*)&g_wait_limit_ns) {
         if (abort_flag != nullptr) *abort_flag = 1u;
         atomicOr(status, FP8MLA_DEV_WAIT_TIMEOUT);
+        record_timeout_site(site);
         return false;
       }
     }

@@ -48,6 +48,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "common.cuh"
@@ -130,14 +131,20 @@ struct SegmentWalker {
   }
 };
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  const bool ok = wait_bounded(bar, parity, abort_flag, &g_status_mla);
+// kCluster: the barrier also receives arrivals from the other CTA of a cluster
+// site: a source line recorded if the wait runs out
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint32_t site = 0) {
+  const bool ok = wait_bounded<kCluster>(bar, parity, abort_flag, &g_status_mla, site);
   return __all_sync(0xffffffffu, ok);
 }
 
 // warp_wait polling without suspension, for the waits on the per-page critical path
-__device__ __forceinline__ bool warp_spin(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  const bool ok = wait_spin(bar, parity, abort_flag, &g_status_mla);
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_spin(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          uint32_t site = 0) {
+  const bool ok = wait_spin<kCluster>(bar, parity, abort_flag, &g_status_mla, site);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -595,65 +602,22 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
 }
 
 // ===========================================================================
-// FP8-dots kernel.
-//
-// Work unit = 2 CTAs, each owning one 256-wide dv slice.  The shared-memory
-// ring of 5 stages carries, in one order that every role walks, three Q slots
-// at the start of each segment (the segment's quantised Q: two latent halves
-// and the RoPE part) followed by the segment's KV pages, so no separate Q
-// buffer competes with the KV pages for shared memory.  TMEM: O 256 + two S
-// buffers of 64 + Q latent 128 columns.
+// Q preparation for FP8 dots (one grid ahead of the decode kernel).
 // ===========================================================================
 namespace f8 {
-constexpr int kStages = 5;
-constexpr int kThreads = 384;
-constexpr int kOffRope8 = 4 * kLatBox;             // 64 tokens x 64 E4M3 RoPE bytes, no swizzle
-constexpr int kStageBytes = kOffRope8 + kPage * 64;
-// Shared memory after the ring: two buffers for a page's RoPE part as f16
-// (64 keys x 128 B, 128-byte swizzle), Q's RoPE part (128 rows x 128 B f16,
-// 128-byte swizzle), and P (128 rows x 64 E4M3 keys) as 8-row x 16-byte core
-// matrices: row group g and 16-byte key chunk c at g * kPSbo + c * kPLbo.
-constexpr int kCvtBytes = kLatBox;
-constexpr int kOffCvt = kStages * kStageBytes;
-constexpr int kOffQRope = kOffCvt + 2 * kCvtBytes;
-constexpr int kOffP = kOffQRope + kRows * 128;
-constexpr int kPLbo = 128, kPSbo = 512;
-constexpr int kSmemData = kOffP + kRows * kPage;
-constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
-constexpr float kTau = 2.75f;                     // 64 * 2^2.75 = 430.5 < 448
-// TMEM columns: O slice, two S buffers (pages alternate), Q latent (E4M3).
-constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
-// Quantised Q of a sequence, as three ring slots: slot h (h = 0, 1) holds per
-// row latent bytes [256 h, 256 h + 256) at a 272-byte pitch, slot 2 the RoPE
-// values as f16 at a 144-byte pitch (pitches chosen so a quarter-warp's
-// 16-byte row accesses hit distinct banks).
+// Quantised Q of a sequence (FP8 dots), as written by mla_qprep_kernel: two
+// latent slots, slot h (h = 0, 1) holding per row latent bytes [256 h,
+// 256 h + 256) at a 272-byte pitch, then the RoPE values as f16 at a 144-byte
+// pitch (pitches chosen so a quarter-warp's 16-byte row accesses hit distinct
+// banks), then the latent quantisation error q_hat qs - q, 128 rows x 512
+// bf16, read by the combine kernel for the LSE correction.
 constexpr int kQLatPitch = 272;
 constexpr int kQRopePitch = 144;
 constexpr int kQLatSlotBytes = kRows * kQLatPitch;
 constexpr int kQRopeSlotBytes = kRows * kQRopePitch;
-static_assert(kQLatSlotBytes <= kStageBytes && kQRopeSlotBytes <= kStageBytes, "a Q slot fits one stage");
-// After the slots: the latent quantisation error q_hat qs - q, 128 rows x 512
-// bf16, read by the combine kernel for the LSE correction.
 constexpr int kQErrOff = 2 * kQLatSlotBytes + kQRopeSlotBytes;
 static_assert(kQErrOff == kMlaQErrOff && kQErrOff + kRows * kDLat * 2 == kMlaQBytes, "quantised-Q layout");
-static_assert(kStageBytes % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
-              "1 KB aligned tiles");
-static_assert(kStageBytes == static_cast<int>(kPageTxBytes), "a page fills one stage");
-
-struct Bars {
-  uint64_t kv_full[kStages];    // stage holds its page (TMA bytes) or its Q slot (Q warps' arrival)
-  uint64_t kv_empty[kStages];   // stage may be refilled
-  uint64_t cvt_ready[kStages];  // the page's RoPE part is converted and its dead rows zeroed
-  uint64_t s_full[2];           // S buffer b holds a page's scores
-  uint64_t p_full;              // P written (one arrival per softmax warp)
-  uint64_t pv_done;             // the P.V that read P completed
-  uint64_t q_full, final_mma, xchg;
-  uint32_t tmem_base, abort_flag, cvt_ok;
-  float xsum[2][kRows];         // row-sum halves
-};
-
-constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
-static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
+static_assert(kQLatPitch % 16 == 0 && kQRopePitch % 16 == 0 && kQLatSlotBytes % 16 == 0, "16-byte rows");
 
 // Quantises the Q rows of sequence b into the three Q slots: latent -> E4M3(q / qs),
 // RoPE -> f16(q / qs), qs = smallest power of two with amax <= 448 qs.  kTpr
@@ -762,10 +726,118 @@ __device__ __forceinline__ void lane_group_transpose(uint4 (&pc)[N], int lane) {
 }
 }  // namespace f8
 
-__global__ void __launch_bounds__(f8::kThreads, 1)
-    mla_fp8_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
-                   const MlaParams prm) {
-  using namespace f8;
+// ===========================================================================
+// FP8-dots kernel: one work unit = a cluster of two CTAs.
+//
+// CTA `rank` (0 or 1) owns dv columns [256 rank, 256 rank + 256) of O, and
+// the unit's pages alternate between the two CTAs: page g of the unit's page
+// stream (counted across its segments) belongs to CTA g % 2.  The owner of a
+// page computes its scores S = Q K^T and its probabilities P; the other CTA
+// only multiplies P by its own dv half of the page's V.  P (128 rows x 64
+// keys, E4M3) and the running row maximum that P was computed against travel
+// to the other CTA through distributed shared memory, so each page's Q.K^T
+// and softmax run once per unit (the pair no longer repeats them).
+//
+// The running maximum follows the page order exactly: the owner of page g
+// takes the maximum after page g - 1 (computed by the other CTA), raises it
+// if page g's maximum exceeds it by more than kTau, and sends the result on
+// with P; so both CTAs rescale their O halves at the same pages by the same
+// factors, and the result is the one a single sequential pass would give.
+//
+// Per CTA: TMEM holds its O half (256 columns), two S buffers (64 each; its
+// own pages alternate) and the latent Q (128, E4M3).  Shared memory holds a
+// ring of whole pages for its own pages (3 x 36 KB), a ring of V halves for
+// the other CTA's pages (3 x 16 KB), two f16 RoPE conversion buffers, the Q
+// RoPE tile and two P tiles (P of even pages in tile 0, written by CTA 0 in
+// both CTAs; odd pages in tile 1, written by CTA 1).
+// ===========================================================================
+namespace pr {
+constexpr int kOwnStages = 3;
+constexpr int kPeerStages = 3;
+constexpr int kThreads = 384;
+constexpr int kOwnBytes = 4 * kLatBox + kPage * 64;  // a whole page: 4 latent boxes + the RoPE box
+constexpr int kPeerBytes = 2 * kLatBox;               // this CTA's dv half of a page's latent bytes
+constexpr int kOffOwn = 0;
+constexpr int kOffPeer = kOffOwn + kOwnStages * kOwnBytes;
+constexpr int kOffCvt = kOffPeer + kPeerStages * kPeerBytes;  // two f16 RoPE buffers (64 keys x 128 B)
+constexpr int kOffQRope = kOffCvt + 2 * kLatBox;               // Q RoPE, 128 rows x 64 f16, 128-byte swizzle
+constexpr int kOffP = kOffQRope + kRows * 128;                 // two P tiles
+constexpr int kPTile = kRows * kPage;
+constexpr int kSmemData = kOffP + 2 * kPTile;
+// P: 8-row x 16-byte core matrices, key chunk c of row group G at c * kPLbo + G * kPSbo, so the 32
+// rows x 16 bytes that one warp writes per key chunk are one contiguous 512-byte piece
+constexpr int kPLbo = 2048, kPSbo = 128;
+constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
+constexpr float kTau = 2.75f;                    // 64 * 2^2.75 = 430.5 < 448
+constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
+static_assert(kOwnBytes == static_cast<int>(kPageTxBytes), "a page fills one own stage");
+static_assert(kOffPeer % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
+              "1 KB aligned tiles");
+
+struct Bars {
+  uint64_t own_full[kOwnStages];    // own page loaded
+  uint64_t own_empty[kOwnStages];   // own stage may be refilled
+  uint64_t own_cvt[kOwnStages];     // own page's RoPE part converted, dead V rows zeroed
+  uint64_t peer_full[kPeerStages];  // V half of the other CTA's page loaded
+  uint64_t peer_empty[kPeerStages];
+  uint64_t peer_cvt[kPeerStages];   // its dead rows zeroed
+  uint64_t s_full[2];               // S buffer holds an own page's scores
+  uint64_t p_full[2];               // by page parity: P written here (own page) / O ready here (other's page)
+  uint64_t p_rx;                    // the other CTA's P tile copied in (transaction bytes; armed by the MMA warp)
+  uint64_t pv_done[2];              // by page parity: this CTA's P.V of the page completed
+  uint64_t pv_peer;                 // the other CTA's P.V of one of this CTA's pages completed
+  uint64_t mx_full;                 // the other CTA's row maxima for one of its pages arrived (4 warps)
+  uint64_t lx_full[2];              // by segment parity: the other CTA's row sums arrived (4 warps)
+  uint64_t q_full;                  // a segment's Q copied in (8 softmax warps)
+  uint64_t final_mma, xchg;
+  uint32_t tmem_base, abort_flag, cvt_ok;
+  // written by 16-byte stores (the other CTA's lane 0 sends 32 rows at a time)
+  alignas(16) float mx[2][kRows];   // the other CTA's running maxima, by its page count parity
+  alignas(16) float lx[2][kRows];   // the other CTA's row sums, by segment parity
+  float xsum[2][2][kRows];          // by segment parity: row-sum halves of the two softmax threads of a row
+};
+static_assert(offsetof(Bars, mx) % 16 == 0 && offsetof(Bars, lx) % 16 == 0, "16-byte rows of maxima and sums");
+static_assert(kSmemData % 16 == 0, "the barrier block starts 16-byte aligned");
+
+constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
+static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
+
+// Pages of a unit one at a time: g counts the unit's pages across segments,
+// seg its non-empty segments.
+struct PageCursor {
+  SegmentWalker walk;
+  Segment sg;
+  int pg = 0, g = -1, seg = -1;
+  bool valid = false;
+  __device__ PageCursor(const MlaParams& p, int unit) : walk(p, unit) {}
+  __device__ bool next() {
+    if (valid && pg + 1 < sg.hi) {
+      ++pg;
+      ++g;
+      return true;
+    }
+    valid = walk.next(sg);
+    if (!valid) return false;
+    pg = sg.lo;
+    ++g;
+    ++seg;
+    return true;
+  }
+  __device__ bool first() const { return pg == sg.lo; }
+  __device__ bool last() const { return pg == sg.hi - 1; }
+};
+
+// Unit-level fault injection for the bounded-wait test: when g_fault_page is
+// p + 1, CTA 0 of unit 0 never issues the loads of its page p, so every wait
+// on them runs out (see fp8mla_test_fault_injection).
+__device__ int g_fault_page = 0;
+
+}  // namespace pr
+
+__global__ void __launch_bounds__(pr::kThreads, 1)
+    mla_fp8_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                        const MlaParams prm) {
+  using namespace pr;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -775,22 +847,41 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int unit = blockIdx.x / 2;
-  const int part = blockIdx.x % 2;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t other = rank ^ 1u;
+  auto remote = [&](const void* p) { return mapa_shared(smem_u32(p), other); };
+  // stop this CTA and tell the other one, whose waits then end too
+  auto fail = [&]() {
+    *abort_flag = 1u;
+    st_cluster_u32(remote(&bars->abort_flag), 1u);
+  };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
-      mbar_init(&bars->cvt_ready[s], 1);
+    for (int s = 0; s < kOwnStages; ++s) {
+      mbar_init(&bars->own_full[s], 1);
+      mbar_init(&bars->own_empty[s], 1);
+      mbar_init(&bars->own_cvt[s], 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&bars->s_full[b], 1);
-    mbar_init(&bars->p_full, kSoftmaxThreads / 32);
-    mbar_init(&bars->pv_done, 1);
+    for (int s = 0; s < kPeerStages; ++s) {
+      mbar_init(&bars->peer_full[s], 1);
+      mbar_init(&bars->peer_empty[s], 1);
+      mbar_init(&bars->peer_cvt[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], kSoftmaxThreads / 32);
+      mbar_init(&bars->pv_done[b], 1);
+    }
+    mbar_init(&bars->pv_peer, 1);
+    mbar_init(&bars->p_rx, 1);
+    mbar_init(&bars->mx_full, kSoftmaxThreads / 64);
+    for (int b = 0; b < 2; ++b) mbar_init(&bars->lx_full[b], kSoftmaxThreads / 64);
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->xchg, kSoftmaxThreads / 32);
     bars->abort_flag = 0;
     fence_barrier_init();
+    mbar_arrive_expect_tx(&bars->p_rx, kPTile);  // the first P tile from the other CTA
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -802,51 +893,27 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // both CTAs' barriers are initialised before either arrives on the other's
+  cluster_arrive();
+  cluster_wait();
   griddep_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
 
-  // Ring protocol.  Every role walks the same slot sequence: three Q slots at
-  // the start of each segment (its quantised Q, prepared by mla_qprep_kernel)
-  // and then its pages.  Each stage barrier completes one
-  // phase per occupancy of its stage, and every role that waits on one
-  // observes each of its phases in turn, so a parity wait can never pass on a
-  // phase two behind or two ahead: kv_empty is waited by the producer only;
-  // kv_full by the converter for every occupancy, by the MMA warp for pages
-  // and by the softmax warps for Q slots; each stage is released only after
-  // the converter's cvt_ready for that occupancy.
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
-    // The warp loads 32 block-table entries at a time (one per lane); lane 0
-    // issues the loads.
+    // Own pages: the whole page (four 128-byte latent boxes + the RoPE box).
+    // The other CTA's pages: this CTA's dv half (latent boxes 2 rank, 2 rank + 1).
     if (lane == 0) {
       tma_prefetch_desc(&tm_lat);
       tma_prefetch_desc(&tm_rope);
     }
+    const int fault = (unit == 0 && rank == 0) ? *(volatile int*)&g_fault_page : 0;
     SegmentWalker walk(prm, unit);
     Segment sg;
-    int k = 0;
-    uint32_t issued = 0, par = 0;  // per stage: last occupant was loaded here, and its use parity
+    int g = 0;
+    uint32_t own_issued = 0, own_par = 0, peer_issued = 0, peer_par = 0;
     bool ok = true;
     while (ok && walk.next(sg)) {
-      // the segment's quantised Q: two latent halves and the RoPE part
-      for (int q = 0; q < 3 && ok; ++q, ++k) {
-        const int st = k % kStages, use = k / kStages;
-        const uint32_t bytes = (q < 2) ? kQLatSlotBytes : kQRopeSlotBytes;
-        bool waited = true;
-        if (lane == 0) {
-          waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla);
-          if (waited) {
-            mbar_arrive_expect_tx(&bars->kv_full[st], bytes);
-            bulk_load(smem + st * kStageBytes,
-                      prm.qbuf + static_cast<size_t>(sg.b) * kMlaQBytes + static_cast<size_t>(q) * kQLatSlotBytes,
-                      bytes, &bars->kv_full[st]);
-            issued |= 1u << st;
-            par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0;
-      }
-      if (!ok) break;
       const int32_t* bt = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
       for (int chunk = sg.lo; ok && chunk < sg.hi; chunk += 32) {
         int mine = 0;
@@ -858,21 +925,37 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           }
         }
         const int cnt = min(32, sg.hi - chunk);
-        for (int j = 0; j < cnt; ++j, ++k) {
-          const int phys = __shfl_sync(0xffffffffu, mine, j);
-          const int st = k % kStages;
-          const int use = k / kStages;
+        for (int jj = 0; jj < cnt; ++jj, ++g) {
+          const int phys = __shfl_sync(0xffffffffu, mine, jj);
+          const int idx = g >> 1;
           bool waited = true;
           if (lane == 0) {
-            waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla);
-            if (waited) {
-              uint8_t* sb = smem + st * kStageBytes;
-              mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
+            const bool skip = fault == g + 1;
+            if ((g & 1) == static_cast<int>(rank)) {
+              const int st = idx % kOwnStages, use = idx / kOwnStages;
+              waited = use == 0 || wait_bounded(&bars->own_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
+              if (waited && !skip) {
+                uint8_t* sb = smem + kOffOwn + st * kOwnBytes;
+                mbar_arrive_expect_tx(&bars->own_full[st], kOwnBytes);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kLatBox, &tm_lat, &bars->kv_full[st], q * 128, 0, phys);
-              tma_load_3d(sb + kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
-              issued |= 1u << st;
-              par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+                for (int q = 0; q < 4; ++q)
+                  tma_load_3d(sb + q * kLatBox, &tm_lat, &bars->own_full[st], q * 128, 0, phys);
+                tma_load_3d(sb + 4 * kLatBox, &tm_rope, &bars->own_full[st], kDLat, 0, phys);
+                own_issued |= 1u << st;
+                own_par = (own_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+              }
+            } else {
+              const int st = idx % kPeerStages, use = idx / kPeerStages;
+              waited = use == 0 || wait_bounded(&bars->peer_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
+              if (waited && !skip) {
+                uint8_t* sb = smem + kOffPeer + st * kPeerBytes;
+                mbar_arrive_expect_tx(&bars->peer_full[st], kPeerBytes);
+                tma_load_3d(sb, &tm_lat, &bars->peer_full[st], static_cast<int>(rank) * 256, 0, phys);
+                tma_load_3d(sb + kLatBox, &tm_lat, &bars->peer_full[st], static_cast<int>(rank) * 256 + 128, 0,
+                            phys);
+                peer_issued |= 1u << st;
+                peer_par = (peer_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+              }
             }
           }
           if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
@@ -882,156 +965,157 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         }
       }
     }
+    if (!ok && lane == 0) fail();
     // Never leave with copies in flight: wait for the last load of each stage.
-    if (lane == 0)
-      for (int s = 0; s < kStages; ++s)
-        if ((issued >> s) & 1u) wait_bounded(&bars->kv_full[s], (par >> s) & 1u, nullptr, &g_status_mla);
+    if (lane == 0) {
+      for (int s = 0; s < kOwnStages; ++s)
+        if ((own_issued >> s) & 1u) wait_bounded(&bars->own_full[s], (own_par >> s) & 1u, nullptr, &g_status_mla, __LINE__);
+      for (int s = 0; s < kPeerStages; ++s)
+        if ((peer_issued >> s) & 1u)
+          wait_bounded(&bars->peer_full[s], (peer_par >> s) & 1u, nullptr, &g_status_mla, __LINE__);
+    }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    // The whole warp runs the loop (so descriptors stay warp-uniform) and one
-    // elected lane issues -- from a lone thread each MMA costs about twice as
-    // long to issue.  Pages alternate between two S buffers, so the Q.K^T of
-    // page i runs while the softmax warps work on page i - 1.  Per page i: wait
-    // until S buffer i % 2 was read out (page i - 2), Q.K^T as 16 E4M3 MMAs
-    // (latent, Q from TMEM, K = 32) and 4 f16 MMAs (RoPE, Q from shared
-    // memory, K = 16), then the P.V of page i - 1 (2 E4M3 MMAs, K = 32 keys,
-    // N = 256) once its P is written.
-    {
-      constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
-      constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
-      constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
-      const uint32_t t_o = tmem + kTO;
-      const bool leader = elect_one();
-      const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
-      const uint64_t pd = make_sdesc(smem_u32(smem + kOffP), kPLbo, kPSbo, SWIZZLE_NONE);
-      SegmentWalker walk(prm, unit);
-      Segment sg;
-      int i = 0, k = 0, seg = 0;
-      int j = 0;           // next page whose P.V is due (pages j .. i - 1 have their Q.K^T issued)
-      uint32_t pend = 0;   // per pending page p, byte p % 4: its stage | first-of-segment << 3
-      bool ok = true;
-      // the P.V of page j, once its P is written; it releases the page's stage
-      auto issue_pv = [&]() -> bool {
-        if (!warp_spin(&bars->p_full, j & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t e = (pend >> (8 * (j & 3))) & 0xFFu;
-        const int st = static_cast<int>(e & 7u);
-        const bool first = ((e >> 3) & 1u) != 0;
-        const uint32_t v_base = smem_u32(smem + st * kStageBytes) + part * 2 * kLatBox;
-        const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-          mma_f8_ss_if(leader, t_o, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
-                       (first && kk == 0) ? 0u : 1u);
-        tc_commit_if(leader, &bars->pv_done);
-        tc_commit_if(leader, &bars->kv_empty[st]);
-        ++j;
-        return true;
-      };
-      while (ok && walk.next(sg)) {
-        // The previous segment's last P.V comes first: the softmax warps write
-        // its P before they copy this segment's Q.
-        while (ok && j < i) ok = issue_pv();
-        // the softmax warps have copied the Q slots (and the converter has seen them)
-        bool qok = ok && warp_wait(&bars->q_full, seg & 1, abort_flag);
-        for (int q = 0; q < 3 && qok; ++q)
-          qok = warp_wait(&bars->cvt_ready[(k + q) % kStages], ((k + q) / kStages) & 1, abort_flag);
-        if (!qok) {
-          ok = false;
-          break;
-        }
-        if (leader)
-          for (int q = 0; q < 3; ++q) mbar_arrive(&bars->kv_empty[(k + q) % kStages]);
-        __syncwarp();
-        k += 3;
-        // Page i's conversion is waited for while the P.V of page i - 2 runs (so
-        // that Q.K^T(i) follows that P.V in the tensor pipe without a gap).  S
-        // buffer i % 2 last held page i - 2, whose P (written after its S was
-        // read) that P.V waited for -- or the previous segment's flush did.
-        if (!warp_spin(&bars->cvt_ready[k % kStages], (k / kStages) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        for (int pg = sg.lo; pg < sg.hi; ++pg, ++i, ++k) {
-          const int st = k % kStages;
-          const int sbuf = i & 1;
-          tc_fence_after();
-          const uint32_t t_s = tmem + kTS + sbuf * kPage;
-          const uint64_t kd = make_sdesc(smem_u32(smem + st * kStageBytes), 16, 1024, SWIZZLE_128B);
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk)
-            mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4),
-                         idesc8, kk > 0 ? 1u : 0u);
-          const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + sbuf * kCvtBytes), 16, 1024, SWIZZLE_128B);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ss_if(leader, t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
-          tc_commit_if(leader, &bars->s_full[sbuf]);
-          const uint32_t e = static_cast<uint32_t>(st) | ((pg == sg.lo) ? 8u : 0u);
-          pend = (pend & ~(0xFFu << (8 * (i & 3)))) | (e << (8 * (i & 3)));
-          // the P.V of the previous page (queued right behind this Q.K^T), then
-          // the next page's conversion while that P.V runs
-          if (pg > sg.lo && !issue_pv()) {  // j == i - 1 here
-            ok = false;
-            break;
-          }
-          if (pg + 1 < sg.hi &&
-              !warp_spin(&bars->cvt_ready[(k + 1) % kStages], ((k + 1) / kStages) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-        }
-        ++seg;
-      }
-      while (ok && j < i) ok = issue_pv();  // the last P.V
-      if (leader) tc_commit(&bars->final_mma);
-      __syncwarp();
-      warp_wait(&bars->final_mma, 0, nullptr);
-    }
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------- RoPE conversion, tail zeroing (64 threads) ----
-    const int t = threadIdx.x - 64;  // token row of the page
-    SegmentWalker walk(prm, unit);
-    Segment sg;
-    int k = 0, i = 0;  // ring slots, pages
+    // The whole warp runs the loop and one elected lane issues.  Order: the
+    // Q.K^T of the first own page (and of the second if it shares the first's
+    // segment), then for every page g of the unit its P.V (once its P is
+    // written and O is ready), followed by the Q.K^T of the own page g + 4 if
+    // there is one (its S buffer last held own page g - 4's scores, read
+    // before that page's P was written).  A Q.K^T that opens a segment waits
+    // for that segment's Q, which the softmax warps copy in after writing P
+    // of this CTA's previous own page L, and only once the segments before
+    // L's are finished; so it is issued only after the P.V of L (every P.V
+    // those warps wait for comes before it).
+    constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
+    constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
+    constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
+    const bool leader = elect_one();
+    const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
+    const uint16_t other_mask = static_cast<uint16_t>(1u << other);
+    PageCursor qk(prm, unit);  // next own page whose Q.K^T is due
+    PageCursor pv(prm, unit);  // every page, in order, for P.V
+    int qn = 0, qk_seg = -1;
+    auto qk_advance = [&]() -> bool {
+      while (qk.next())
+        if ((qk.g & 1) == static_cast<int>(rank)) return true;
+      return false;
+    };
+    bool qk_more = qk_advance();
     bool ok = true;
-    while (ok && walk.next(sg)) {
-      // the Q slots need no conversion, but their fills are waited for and
-      // acknowledged like the pages' so that each stage phase is seen in turn
+    auto issue_qk = [&]() -> bool {
+      const int j = qk.g >> 1;
+      if (qk.seg != qk_seg) {  // the segment's first own page: its Q must be in place
+        qk_seg = qk.seg;
+        if (!warp_wait(&bars->q_full, qn & 1, abort_flag, __LINE__)) return false;
+        ++qn;
+      }
+      const int st = j % kOwnStages;
+      if (!warp_spin(&bars->own_cvt[st], (j / kOwnStages) & 1, abort_flag, __LINE__)) return false;
+      tc_fence_after();
+      const uint32_t t_s = tmem + kTS + (j & 1) * kPage;
+      const uint64_t kd = make_sdesc(smem_u32(smem + kOffOwn + st * kOwnBytes), 16, 1024, SWIZZLE_128B);
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk)
+        mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4), idesc8,
+                     kk > 0 ? 1u : 0u);
+      const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + (j & 1) * kLatBox), 16, 1024, SWIZZLE_128B);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16_ss_if(leader, t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
+      tc_commit_if(leader, &bars->s_full[j & 1]);
+      return true;
+    };
+    int last_qk = -1;  // page of the last Q.K^T issued
+    // a Q.K^T may be issued after the P.V of page g (g = -1: before any)
+    auto qk_due = [&](int g) {
+      return qk_more && qk.g <= g + 4 && (qk.seg == qk_seg || qk_seg < 0 || g >= last_qk);
+    };
+    while (ok && qk_due(-1) && (last_qk < 0 || qk.seg == qk_seg)) {
+      last_qk = qk.g;
+      ok = issue_qk();
+      qk_more = qk_advance();
+    }
+    while (ok && pv.next()) {
+      const int g = pv.g;
+      const bool mine = (g & 1) == static_cast<int>(rank);
+      const int idx = g >> 1;
+      // P(g) written here (own page) or O ready for it here (the other CTA's page)
+      if (!warp_spin(&bars->p_full[g & 1], idx & 1, abort_flag, __LINE__)) {
+        ok = false;
+        break;
+      }
+      uint32_t v_base;
+      uint64_t* empty;
+      if (mine) {
+        const int st = idx % kOwnStages;  // converted before its Q.K^T
+        v_base = smem_u32(smem + kOffOwn + st * kOwnBytes) + rank * 2 * kLatBox;
+        empty = &bars->own_empty[st];
+      } else {
+        const int st = idx % kPeerStages;
+        // the other CTA's P tile copied in; then the next one's bytes are expected
+        if (!warp_spin(&bars->p_rx, idx & 1, abort_flag, __LINE__) ||
+            !warp_spin(&bars->peer_cvt[st], (idx / kPeerStages) & 1, abort_flag, __LINE__)) {
+          ok = false;
+          break;
+        }
+        if (leader) mbar_arrive_expect_tx(&bars->p_rx, kPTile);
+        __syncwarp();
+        v_base = smem_u32(smem + kOffPeer + st * kPeerBytes);
+        empty = &bars->peer_empty[st];
+      }
+      tc_fence_after();
+      const uint64_t pd = make_sdesc(smem_u32(smem + kOffP + (g & 1) * kPTile), kPLbo, kPSbo, SWIZZLE_NONE);
+      const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
+      const bool first = pv.first();
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        mma_f8_ss_if(leader, tmem + kTO, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
+                     (first && kk == 0) ? 0u : 1u);
+      tc_commit_if(leader, &bars->pv_done[g & 1]);
+      tc_commit_if(leader, empty);
+      if (!mine) tc_commit_mc_if(leader, &bars->pv_peer, other_mask);  // the owner may reuse its P tile
+      while (ok && qk_due(g)) {
+        last_qk = qk.g;
+        ok = issue_qk();
+        qk_more = qk_advance();
+      }
+    }
+    if (!ok) fail();
+    if (leader) tc_commit(&bars->final_mma);
+    __syncwarp();
+    warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
+  } else if (warp == 2 || warp == 3) {
+    // ------------------- RoPE conversion, tail zeroing (64 threads) ----
+    // Own pages: the RoPE part to f16 (exact) in buffer j % 2, free once the
+    // Q.K^T of own page j - 2 completed; dead rows (past the sequence end) of
+    // this CTA's V half zeroed.  The other CTA's pages: dead rows zeroed.
+    const int t = threadIdx.x - 64;  // token row of the page
+    PageCursor pc(prm, unit);
+    bool ok = true;
+    while (ok && pc.next()) {
+      const int g = pc.g, idx = g >> 1;
+      const bool mine = (g & 1) == static_cast<int>(rank);
+      const int st = mine ? idx % kOwnStages : idx % kPeerStages;
+      const int use = mine ? idx / kOwnStages : idx / kPeerStages;
       if (t == 0) {
-        bool filled = true;
-        for (int q = 0; q < 3 && filled; ++q)
-          filled = wait_bounded(&bars->kv_full[(k + q) % kStages], ((k + q) / kStages) & 1, abort_flag,
-                                &g_status_mla);
-        if (filled)
-          for (int q = 0; q < 3; ++q) mbar_arrive(&bars->cvt_ready[(k + q) % kStages]);
-        bars->cvt_ok = filled ? 1u : 0u;
+        bool w = wait_bounded(mine ? &bars->own_full[st] : &bars->peer_full[st], use & 1, abort_flag, &g_status_mla, __LINE__);
+        if (w && mine && idx >= 2)
+          w = wait_bounded(&bars->s_full[idx & 1], ((idx - 2) >> 1) & 1, abort_flag, &g_status_mla, __LINE__);
+        bars->cvt_ok = w ? 1u : 0u;
       }
       named_bar_sync(1, 64);
-      if (!bars->cvt_ok) break;
-      named_bar_sync(1, 64);  // cvt_ok is rewritten below
-      k += 3;
-      for (int pg = sg.lo; pg < sg.hi; ++pg, ++k, ++i) {
-        const int st = k % kStages;
-        const int use = k / kStages;
-        // conversion buffer i % 2 is free once the Q.K^T of page i - 2 completed
-        if (t == 0)
-          bars->cvt_ok = (wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla) &&
-                          (i < 2 || wait_bounded(&bars->s_full[i & 1], ((i - 2) >> 1) & 1, abort_flag, &g_status_mla)))
-                             ? 1u
-                             : 0u;
-        named_bar_sync(1, 64);
-        if (!bars->cvt_ok) {
-          ok = false;
-          break;
-        }
-        uint8_t* sb = smem + st * kStageBytes;
-        const bool dead = (pg == sg.n - 1) && (t >= sg.s_k - pg * kPage);  // slot past the sequence end
-        const uint4 z = make_uint4(0, 0, 0, 0);
+      if (!bars->cvt_ok) {
+        ok = false;
+        break;
+      }
+      const bool dead = (pc.pg == pc.sg.n - 1) && (t >= pc.sg.s_k - pc.pg * kPage);  // slot past the end
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      uint8_t* vhalf = mine ? smem + kOffOwn + st * kOwnBytes + rank * 2 * kLatBox : smem + kOffPeer + st * kPeerBytes;
+      if (mine) {
         const int sw = t & 7;
-        const uint4* src = reinterpret_cast<const uint4*>(sb + kOffRope8 + t * 64);
-        uint8_t* dst = smem + kOffCvt + (i & 1) * kCvtBytes + t * 128;
+        const uint4* src = reinterpret_cast<const uint4*>(smem + kOffOwn + st * kOwnBytes + 4 * kLatBox + t * 64);
+        uint8_t* dst = smem + kOffCvt + (idx & 1) * kLatBox + t * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint4 lo = z, hi = z;
@@ -1049,19 +1133,20 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
           *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
         }
-        if (dead) {  // zero the slot's V row (all four 128-byte slices)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint4* row = reinterpret_cast<uint4*>(sb + j * kLatBox + t * 128);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) row[c] = z;
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 64);
-        if (t == 0) mbar_arrive(&bars->cvt_ready[st]);
       }
+      if (dead) {  // zero the slot's row in this CTA's two V boxes
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint4* row = reinterpret_cast<uint4*>(vhalf + j * kLatBox + t * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) row[c] = z;
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 64);
+      if (t == 0) mbar_arrive(mine ? &bars->own_cvt[st] : &bars->peer_cvt[st]);
     }
+    if (!ok && t == 0) fail();
   } else {
     // ------------------ softmax / Q copy / epilogue (8 warps, 2 per row) ----
     const int hf = (warp - 4) / 4;         // which half of the row
@@ -1073,89 +1158,189 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     uint32_t xphase = 0;
     auto xsync = [&]() -> bool {  // bounded, abort-aware exchange point of the 256 softmax threads
       warp_arrive(&bars->xchg);
-      const bool ok = warp_wait(&bars->xchg, xphase & 1, abort_flag);
+      const bool ok = warp_wait(&bars->xchg, xphase & 1, abort_flag, __LINE__);
       ++xphase;
       return ok;
     };
-    // Copies this half of the Q row of the segment whose Q slots start at ring
-    // slot kq: latent bytes [256 hf, +256) into TMEM columns kTQ + 64 hf..,
-    // RoPE values [32 hf, +32) into the shared Q RoPE tile (128-byte swizzle).
-    auto copy_q = [&](int kq, int b_seq, float& qs_out) -> bool {
-      const int st = (kq + hf) % kStages, use = (kq + hf) / kStages;
-      const int st_r = (kq + 2) % kStages, use_r = (kq + 2) / kStages;
-      if (!warp_wait(&bars->kv_full[st], use & 1, abort_flag) ||
-          !warp_wait(&bars->kv_full[st_r], use_r & 1, abort_flag))
-        return false;
-      const uint4* lat = reinterpret_cast<const uint4*>(smem + st * kStageBytes + r * kQLatPitch);
+    const uint32_t r_mx = remote(&bars->mx[0][r]);
+    const uint32_t r_lx = remote(&bars->lx[0][r]);
+    const uint32_t r_prx = remote(&bars->p_rx);
+    const uint32_t r_mxfull = remote(&bars->mx_full);
+    const uint32_t r_lxfull0 = remote(&bars->lx_full[0]);
+    const uint32_t r_p0 = remote(smem + kOffP);
+    const uint32_t prow = static_cast<uint32_t>((r >> 3) * kPSbo + (r & 7) * 16);
+    // Sends the 32 values v of this warp's rows (rows 32 (warp % 4) .. + 31) to
+    // the other CTA at cluster address dst and arrives on its barrier rbar:
+    // lane 0 gathers them and stores them itself, so that its release covers
+    // every value (other lanes' remote stores would not be ordered by it).
+    auto send_rows = [&](uint32_t dst, float v, uint32_t rbar) {
+      uint4 w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        w[i].x = __float_as_uint(__shfl_sync(0xffffffffu, v, 4 * i));
+        w[i].y = __float_as_uint(__shfl_sync(0xffffffffu, v, 4 * i + 1));
+        w[i].z = __float_as_uint(__shfl_sync(0xffffffffu, v, 4 * i + 2));
+        w[i].w = __float_as_uint(__shfl_sync(0xffffffffu, v, 4 * i + 3));
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) st_cluster_v4(dst + 16 * i, w[i]);
+        mbar_arrive_cluster(rbar, 1);
+      }
+    };
+
+    // Copies this half of sequence b_seq's quantised Q row (prepared by
+    // mla_qprep_kernel) in: latent bytes [256 hf, +256) into TMEM columns
+    // kTQ + 64 hf.., RoPE values [32 hf, +32) into the Q RoPE tile.
+    int qn = 0;
+    float qs_cur = 1.f;
+    auto copy_q = [&](int b_seq) -> bool {
+      const uint8_t* qb = prm.qbuf + static_cast<size_t>(b_seq) * kMlaQBytes;
+      const uint4* lat = reinterpret_cast<const uint4*>(qb + hf * f8::kQLatSlotBytes + r * f8::kQLatPitch);
+      const uint4* rope = reinterpret_cast<const uint4*>(qb + 2 * f8::kQLatSlotBytes + r * f8::kQRopePitch + hf * 64);
+      uint4 v[16], w[4];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] = __ldg(lat + c);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) w[c] = __ldg(rope + c);
+      qs_cur = __ldg(prm.qscale + static_cast<size_t>(b_seq) * kRows + r);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint4 v = lat[4 * ch + c];
-          pk[4 * c + 0] = v.x;
-          pk[4 * c + 1] = v.y;
-          pk[4 * c + 2] = v.z;
-          pk[4 * c + 3] = v.w;
+          pk[4 * c + 0] = v[4 * ch + c].x;
+          pk[4 * c + 1] = v[4 * ch + c].y;
+          pk[4 * c + 2] = v[4 * ch + c].z;
+          pk[4 * c + 3] = v[4 * ch + c].w;
         }
         tmem_st16(lane_base + kTQ + (4 * hf + ch) * 16, pk);
       }
-      {
-        const uint4* rope = reinterpret_cast<const uint4*>(smem + st_r * kStageBytes + r * kQRopePitch);
-        uint8_t* dst = smem + kOffQRope + r * 128;
+      uint8_t* dst = smem + kOffQRope + r * 128;
 #pragma unroll
-        for (int c = 4 * hf; c < 4 * hf + 4; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = rope[c];
-      }
-      qs_out = prm.qscale[static_cast<size_t>(b_seq) * kRows + r];
-      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs, the slots refilled by TMA
+      for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(dst + (((4 * hf + c) ^ (r & 7)) << 4)) = w[c];
+      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bars->q_full);
+      ++qn;
+      return true;
+    };
+    // true if some segment after the cursor's holds a page of this CTA; its sequence in *b_out
+    auto next_q_segment = [&](const PageCursor& at, int* b_out) -> bool {
+      SegmentWalker peek = at.walk;
+      Segment nx;
+      int g0 = at.g + (at.sg.hi - at.pg);  // unit index of the next segment's first page
+      while (peek.next(nx)) {
+        const int n = nx.hi - nx.lo;
+        if (n >= 2 || (g0 & 1) == static_cast<int>(rank)) {
+          *b_out = nx.b;
+          return true;
+        }
+        g0 += n;
+      }
+      return false;
+    };
+
+    PageCursor pc(prm, unit);
+    bool ok = true;
+    int cur_seg = -1;
+    float m_run = kNegInf, l_run = 0.f;
+    int pend = -1;  // the other CTA's page whose rescale / O-ready is still due
+    bool pend_first = false;
+    int qtok = 0, visible = 0, min_visible = 0;
+    float c_row = 0.f;
+
+    // The other CTA's page g (after this CTA's page g - 1): take its running
+    // maximum, rescale l and (if it rose) O, and declare O ready for its P.V.
+    auto finish_other = [&](int g, bool first) -> bool {
+      const int k = g >> 1;
+      if (!warp_spin<true>(&bars->mx_full, k & 1, abort_flag, __LINE__)) return false;
+      const float m_new = bars->mx[k & 1][r];
+      const bool rescale = !first && m_new != m_run;
+      const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.f;
+      l_run = first ? 0.f : l_run * alpha;
+      m_run = m_new;
+      // this CTA's arrivals for page g come after page g - 2's phase completed
+      if (g >= 2 && !warp_spin(&bars->pv_done[g & 1], ((g - 2) >> 1) & 1, abort_flag, __LINE__)) return false;
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!warp_spin(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag, __LINE__)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < kOHalf / 32; ++ch) {
+          const uint32_t col = kTO + hf * kOHalf + ch * 32;
+          uint32_t o[32];
+          tmem_ld32(lane_base + col, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st32(lane_base + col, o);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[g & 1]);
       return true;
     };
 
-    SegmentWalker walk(prm, unit);
-    Segment sg;
-    int i = 0, k = 0, seg = 0;
-    float qs_next = 1.f;
-    bool ok = walk.next(sg) && copy_q(0, sg.b, qs_next);
-    while (ok) {
-      const float qs = qs_next;
-      const float c_row = prm.softmax_scale * kLog2e * qs * kv_scale;
-      SegmentWalker peek = walk;
-      Segment nx;
-      const bool has_next = peek.next(nx);
-      const int k_next = k + 3 + (sg.hi - sg.lo);
-      const int col0 = part * 256 + hf * kOHalf;  // this thread's O columns
-      // keys visible to this row (bottom-right causal alignment); pages wholly
-      // below every row's limit need no mask
-      const int qtok = (r < R) ? r / prm.h_q : 0;
-      const int visible = prm.causal ? (sg.s_k - prm.s_q + qtok + 1) : sg.s_k;
-      const int min_visible = prm.causal ? (sg.s_k - prm.s_q + 1) : sg.s_k;
-      float m_run = kNegInf, l_run = 0.f;  // l_run sums the stored-scale p (kPScale p)
-      for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
-        const int sbuf = i & 1;
-        if (!warp_spin(&bars->s_full[sbuf], (i >> 1) & 1, abort_flag)) {
+    // Q of the first segment holding a page of this CTA
+    {
+      PageCursor probe(prm, unit);
+      if (probe.next()) {
+        int bq = probe.sg.b;
+        const int n = probe.sg.hi - probe.sg.lo;
+        bool have = n >= 2 || (probe.g & 1) == static_cast<int>(rank);
+        if (!have) have = next_q_segment(probe, &bq);
+        if (have) {
+          ok = copy_q(bq);
+        }
+      }
+    }
+
+    while (ok && pc.next()) {
+      const int g = pc.g;
+      if (pc.seg != cur_seg) {  // a new segment
+        cur_seg = pc.seg;
+        m_run = kNegInf;
+        l_run = 0.f;
+        qtok = (r < R) ? r / prm.h_q : 0;
+        visible = prm.causal ? (pc.sg.s_k - prm.s_q + qtok + 1) : pc.sg.s_k;
+        min_visible = prm.causal ? (pc.sg.s_k - prm.s_q + 1) : pc.sg.s_k;
+        if (r < R && pc.first()) {  // warm L2 with the Q of the segment after this one
+          int bn;
+          if (next_q_segment(pc, &bn)) {
+            const char* nq = reinterpret_cast<const char*>(prm.qbuf + static_cast<size_t>(bn) * kMlaQBytes);
+            prefetch_l2(nq + hf * f8::kQLatSlotBytes + r * f8::kQLatPitch);
+            prefetch_l2(nq + hf * f8::kQLatSlotBytes + r * f8::kQLatPitch + 128);
+          }
+        }
+      }
+      const bool mine = (g & 1) == static_cast<int>(rank);
+      if (!mine) {
+        pend = g;
+        pend_first = pc.first();
+      } else {
+        const int j = g >> 1;
+        c_row = prm.softmax_scale * kLog2e * qs_cur * kv_scale;
+        if (!warp_spin(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag, __LINE__)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // Both halves of the row are read: the other half only for the row max,
-        // so each warp takes the max of all 64 keys without waiting on its partner.
+        // both halves of the row: the other half only for the row max
         uint32_t s[32], so[32];
-        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * hf, s);
-        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * (1 - hf), so);
+        tmem_ld32(lane_base + kTS + (j & 1) * kPage + 32 * hf, s);
+        tmem_ld32(lane_base + kTS + (j & 1) * kPage + 32 * (1 - hf), so);
         tmem_ld_wait();
-
-        if (pg * kPage + kPage > min_visible) {
-          const int base = pg * kPage + 32 * hf, base_o = pg * kPage + 32 * (1 - hf);
+        if (pc.pg * kPage + kPage > min_visible) {
+          const int base = pc.pg * kPage + 32 * hf, base_o = pc.pg * kPage + 32 * (1 - hf);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             if (base + c >= visible) s[c] = __float_as_uint(kNegInf);
             if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
           }
         }
-        // row max of the 64 scores as a tree of three-way maxima
         float m22[22];
 #pragma unroll
         for (int c = 0; c < 10; ++c) {
@@ -1169,16 +1354,30 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
         m8[7] = m22[21];
-        const float m3a = fmax3(m8[0], m8[1], m8[2]), m3b = fmax3(m8[3], m8[4], m8[5]);
-        const float mx = fmax3(m3a, m3b, fmaxf(m8[6], m8[7])) * c_row;  // c_row > 0; both warps agree
-        float alpha = 1.f;
-        bool rescale = false;
-        if (mx > m_run + kTau) {
-          alpha = ex2_approx(m_run - mx);
-          rescale = (pg != sg.lo);
-          m_run = mx;
+        const float mx =
+            fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
+        // the other CTA's previous page first: its maximum precedes this page's
+        if (pend >= 0) {
+          if (!finish_other(pend, pend_first)) {
+            ok = false;
+            break;
+          }
+          pend = -1;
         }
-        const float bias = (m_run == kNegInf) ? 0.f : (kPLog2 - m_run);
+        // P tile g % 2 is free once both CTAs' P.V of page g - 2 completed
+        if (g >= 2 && (!warp_spin(&bars->pv_done[g & 1], ((g - 2) >> 1) & 1, abort_flag, __LINE__) ||
+                       !warp_spin<true>(&bars->pv_peer, (j - 1) & 1, abort_flag, __LINE__))) {
+          ok = false;
+          break;
+        }
+        const bool first = pc.first();
+        const float m_prev = first ? kNegInf : m_run;
+        const float m_new = (mx > m_prev + kTau) ? mx : m_prev;
+        if (hf == 0) send_rows(r_mx - lane * 4 + (j & 1) * kRows * 4, m_new, r_mxfull);
+        const bool rescale = !first && m_new != m_prev;
+        const float alpha = rescale ? ex2_approx(m_prev - m_new) : 1.f;
+        m_run = m_new;
+        const float bias = (m_new == kNegInf) ? 0.f : (kPLog2 - m_new);
         float sum = 0.f;
         uint32_t pk[8];
 #pragma unroll
@@ -1190,17 +1389,13 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           sum += (p0 + p1) + (p2 + p3);
           pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
         }
-        l_run = l_run * alpha + sum;
-
-        // P has one tile and O one accumulator: the previous page's P.V must
-        // have completed before either is touched
-        if (i >= 1 && !warp_spin(&bars->pv_done, (i - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        l_run = first ? sum : l_run * alpha + sum;
         if (__any_sync(0xffffffffu, rescale)) {
-          const float f = rescale ? alpha : 1.f;
+          if (!warp_spin(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag, __LINE__)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < kOHalf / 32; ++ch) {
             const uint32_t col = kTO + hf * kOHalf + ch * 32;
@@ -1208,75 +1403,119 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
             tmem_ld32(lane_base + col, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
             tmem_st32(lane_base + col, o);
           }
           tmem_st_wait();
         }
-        {  // this warp's 32 keys of row r: 16-byte chunks 2 hf and 2 hf + 1
-          uint8_t* prow = smem + kOffP + (r >> 3) * kPSbo + (r & 7) * 16;
-          *reinterpret_cast<uint4*>(prow + (2 * hf) * kPLbo) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(prow + (2 * hf + 1) * kPLbo) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        {  // this thread's 32 keys of row r: 16-byte chunks 2 hf and 2 hf + 1
+          uint8_t* lp = smem + kOffP + (g & 1) * kPTile + prow;
+          *reinterpret_cast<uint4*>(lp + (2 * hf) * kPLbo) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(lp + (2 * hf + 1) * kPLbo) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        warp_arrive(&bars->p_full);
-        // the segment's last Q.K^T is done: the next segment's Q may replace it now
-        if (pg == sg.hi - 1 && has_next && !copy_q(k_next, nx.b, qs_next)) {
-          ok = false;
-          break;
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->p_full[g & 1]);  // P written (and O rescaled) here
+          // the warp's two 512-byte pieces of P to the other CTA's tile, by the
+          // async proxy, counted on its p_rx barrier
+          const uint32_t piece = static_cast<uint32_t>((g & 1) * kPTile + (warp % 4) * 4 * kPSbo);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t off = piece + (2 * hf + c) * kPLbo;
+            bulk_copy_to_cluster(r_p0 + off, smem + kOffP + off, 32 * 16, r_prx);
+          }
+        }
+        // this CTA's last page of the segment: the next segment's Q may replace this one's
+        bool last_own = pc.last() || (pc.pg + 1 == pc.sg.hi - 1);
+        if (last_own) {
+          int bn;
+          if (next_q_segment(pc, &bn)) {
+            ok = copy_q(bn);
+          }
         }
       }
       if (!ok) break;
+      if (!pc.last()) continue;
 
-      // ---- epilogue: O is final once the segment's last P.V completes ----
-      bars->xsum[hf][r] = l_run;
-      if (!xsync()) break;
-      const float l_tot = (bars->xsum[0][r] + bars->xsum[1][r]) * (1.0f / kPScale);  // sum of p
-      const bool whole = (sg.lo == 0 && sg.hi == sg.n);
+      // ---- segment end ----
+      if (pend >= 0) {
+        if (!finish_other(pend, pend_first)) {
+          ok = false;
+          break;
+        }
+        pend = -1;
+      }
+      // row sum: this CTA's two halves, then the other CTA's
+      const int sp = cur_seg & 1;
+      bars->xsum[sp][hf][r] = l_run;
+      if (!xsync()) {
+        ok = false;
+        break;
+      }
+      const float l_here = bars->xsum[sp][0][r] + bars->xsum[sp][1][r];
+      // one barrier per slot: the other CTA may finish the next segment before this one reads this slot
+      if (hf == 0) send_rows(r_lx - lane * 4 + sp * kRows * 4, l_here, r_lxfull0 + sp * 8);
+      if (!warp_spin<true>(&bars->lx_full[sp], (cur_seg >> 1) & 1, abort_flag, __LINE__)) {
+        ok = false;
+        break;
+      }
+      const float l_tot = (l_here + bars->lx[sp][r]) * (1.0f / kPScale);  // sum of p
+      const bool whole = (pc.sg.lo == 0 && pc.sg.hi == pc.sg.n);
       const float o_scale = kv_scale / kPScale;  // tensor-core units -> true units
       const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
-      const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
-      if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag)) break;
+      const int slot = whole ? 0 : prm.num_splits[pc.sg.b] + pc.sg.split;
+      // O is final once this CTA's P.V of the segment's last page completed
+      if (!warp_wait(&bars->pv_done[g & 1], (g >> 1) & 1, abort_flag, __LINE__)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      // O out as bf16, 32 columns at a time.  A thread holds one row; groups of
-      // four lanes transpose their 16-byte pieces so that each store writes
-      // 64-byte runs of rows.  A whole sequence goes straight to out, a piece
-      // to its bf16 partial slot; the combine kernel adds the LSE correction.
-      const int grow = (warp % 4) * 32 + (lane & ~3);  // the lane group's first row
-      uint16_t* obase = whole ? prm.out + static_cast<size_t>(sg.b) * R * kDV
+      const int col0 = static_cast<int>(rank) * 256 + hf * kOHalf;  // this thread's O columns
+      const int grow = (warp % 4) * 32 + (lane & ~3);                // the lane group's first row
+      uint16_t* obase = whole ? prm.out + static_cast<size_t>(pc.sg.b) * R * kDV
                               : prm.ws_o + static_cast<size_t>(slot) * kRows * kDV;
 #pragma unroll 1
       for (int ch = 0; ch < kOHalf / 32; ++ch) {
         uint32_t o[32];
         tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
         tmem_ld_wait();
-        uint4 pc[4];
+        uint4 pcs[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          pc[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
-          pc[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
-          pc[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
-          pc[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
+          pcs[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
+          pcs[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
+          pcs[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
+          pcs[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
         }
-        lane_group_transpose<4>(pc, lane);
+        f8::lane_group_transpose<4>(pcs, lane);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           if (grow + kk < R)
-            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(grow + kk) * kDV + col0 + ch * 32 + 8 * (lane & 3)) =
-                pc[kk];
+            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(grow + kk) * kDV + col0 + ch * 32 +
+                                      8 * (lane & 3)) = pcs[kk];
       }
-      if (r < R && part == 0 && hf == 0) {  // the row's (uncorrected) LSE, or the piece's (m, l)
+      tc_fence_before();  // O is overwritten by the next segment's first P.V after the next p_full
+      if (r < R && rank == 0 && hf == 0) {  // the row's (uncorrected) LSE, or the piece's (m, l)
         if (whole) {
-          prm.lse[static_cast<size_t>(sg.b) * R + r] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
+          prm.lse[static_cast<size_t>(pc.sg.b) * R + r] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
         } else {
           prm.ws_ml[static_cast<size_t>(slot) * kRows + r] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
         }
       }
-      if (!has_next) break;
-      walk.next(sg);
-      k = k_next;
-      ++seg;
+    }
+    if (!ok) fail();
+    // The other CTA's last P.V of this CTA's pages: its arrival must land
+    // before this CTA may exit.
+    // (Each pv_peer phase j is waited for before own page j + 1's P; the last
+    // own page's phase is waited for here.)
+    if (ok) {
+      int nown = 0;
+      PageCursor cnt(prm, unit);
+      while (cnt.next())
+        if ((cnt.g & 1) == static_cast<int>(rank)) ++nown;
+      if (nown > 0) warp_spin<true>(&bars->pv_peer, (nown - 1) & 1, abort_flag, __LINE__);
     }
   }
 
@@ -1286,18 +1525,34 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // no CTA leaves while the other may still write to its shared memory
+  cluster_arrive();
+  cluster_wait();
 }
 
 cudaError_t launch_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
                        cudaStream_t stream) {
   static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
   const cudaError_t e = configure_once(configured, [] {
-    return cudaFuncSetAttribute(mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(f8::smem_bytes()));
+    return cudaFuncSetAttribute(mla_fp8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(pr::smem_bytes()));
   });
   if (e != cudaSuccess) return e;
-  return launch_dependent(mla_fp8_kernel, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream, tm_lat,
-                          tm_rope, prm);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_units * 2);
+  cfg.blockDim = dim3(pr::kThreads);
+  cfg.dynamicSmemBytes = pr::smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, mla_fp8_pair_kernel, tm_lat, tm_rope, prm);
 }
 
 cudaError_t launch_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
@@ -1327,6 +1582,13 @@ cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap
 cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream) {
   if (prm.b == 0) return cudaSuccess;
   return launch_dependent(mla::f8::mla_qprep_kernel, dim3(prm.b, mla::kRows / 32), dim3(256), 0, stream, prm);
+}
+
+void mla_read_and_clear_timeout_site(uint32_t where[3]) {
+  uint32_t v[4] = {0, 0, 0, 0}, z[4] = {0, 0, 0, 0};
+  cudaMemcpyFromSymbol(v, g_timeout_where, sizeof(v));
+  cudaMemcpyToSymbol(g_timeout_where, z, sizeof(z));
+  for (int i = 0; i < 3; ++i) where[i] = v[3] ? v[i] : 0u;
 }
 
 uint32_t mla_read_and_clear_status() {

@@ -47,6 +47,9 @@ cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& 
 cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                     int num_units, cudaStream_t stream);
 uint32_t mla_read_and_clear_status();
+// {source line, block, thread} of the first bounded wait of the dense MLA kernels that ran
+// out since the last call (all 0 if none), and clears it.
+void mla_read_and_clear_timeout_site(uint32_t where[3]);
 // Quantises every sequence's Q rows for FP8 dots into prm.qbuf / prm.qscale
 // (launched right before launch_mla_decode_fp8, as a programmatic dependent).
 cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream);
