@@ -36,20 +36,23 @@ __device__ __forceinline__ void record_timeout_site(uint32_t site) {
   }
 }
 
+// Probes poll with the CTA-scope form (cheap); a wait on a barrier that
+// other CTAs arrive on (kCluster) takes one cluster-scope acquire fence after
+// the phase is seen complete, instead of an acquire at cluster scope on every poll.
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_probe_try(uint64_t* bar, uint32_t parity) {
+  const bool ok = mbar_try_wait(bar, parity);
   if constexpr (kCluster)
-    return mbar_try_wait_cl(bar, parity);
-  else
-    return mbar_try_wait(bar, parity);
+    if (ok) fence_acq_rel_cluster();
+  return ok;
 }
 
 template <bool kCluster>
 __device__ __forceinline__ bool mbar_probe_test(uint64_t* bar, uint32_t parity) {
+  const bool ok = mbar_test_wait(bar, parity);
   if constexpr (kCluster)
-    return mbar_test_wait_cl(bar, parity);
-  else
-    return mbar_test_wait(bar, parity);
+    if (ok) fence_acq_rel_cluster();
+  return ok;
 }
 
 // Bounded wait on an mbarrier phase.  Returns false (without waiting further)

@@ -738,18 +738,24 @@ __device__ __forceinline__ void lane_group_transpose(uint4 (&pc)[N], int lane) {
 // to the other CTA through distributed shared memory, so each page's Q.K^T
 // and softmax run once per unit (the pair no longer repeats them).
 //
-// The running maximum follows the page order exactly: the owner of page g
-// takes the maximum after page g - 1 (computed by the other CTA), raises it
-// if page g's maximum exceeds it by more than kTau, and sends the result on
-// with P; so both CTAs rescale their O halves at the same pages by the same
-// factors, and the result is the one a single sequential pass would give.
+// Page g's P is taken against a reference m_g (log2 units) that the owner
+// decides from what it already has: m_g = max(m_{g-2}, m_{g-3}) (its own
+// previous page's reference and the other CTA's reference of page g - 3,
+// within the segment), raised to page g's row maximum when that exceeds it by
+// more than kTau.  m_g travels with P; both CTAs rescale their O halves and
+// row sums to m_g before page g's P.V, so both apply the same factors in the
+// same order (a factor may be above 1 for a page after the other CTA raised
+// its reference), every stored P is at most 64 * 2^kTau < 448, and no page
+// waits for the other CTA's decision on the page just before it.
 //
-// Per CTA: TMEM holds its O half (256 columns), two S buffers (64 each; its
-// own pages alternate) and the latent Q (128, E4M3).  Shared memory holds a
+// Per CTA: TMEM holds its O half (256 columns), one S buffer (64), the
+// latent Q (128, E4M3) and Q's RoPE part (32, f16).  Shared memory holds a
 // ring of whole pages for its own pages (3 x 36 KB), a ring of V halves for
-// the other CTA's pages (3 x 16 KB), two f16 RoPE conversion buffers, the Q
-// RoPE tile and two P tiles (P of even pages in tile 0, written by CTA 0 in
-// both CTAs; odd pages in tile 1, written by CTA 1).
+// the other CTA's pages (3 x 16 KB), two f16 RoPE conversion buffers and four
+// P messages: page g's P and its 128 row references go to message g % 4 in
+// both CTAs (to the other CTA by an async bulk copy, which the sender does not
+// wait for), and a message is rewritten four pages later, after both CTAs'
+// P.V of the page before read it.
 // ===========================================================================
 namespace pr {
 constexpr int kOwnStages = 3;
@@ -760,19 +766,22 @@ constexpr int kPeerBytes = 2 * kLatBox;               // this CTA's dv half of a
 constexpr int kOffOwn = 0;
 constexpr int kOffPeer = kOffOwn + kOwnStages * kOwnBytes;
 constexpr int kOffCvt = kOffPeer + kPeerStages * kPeerBytes;  // two f16 RoPE buffers (64 keys x 128 B)
-constexpr int kOffQRope = kOffCvt + 2 * kLatBox;               // Q RoPE, 128 rows x 64 f16, 128-byte swizzle
-constexpr int kOffP = kOffQRope + kRows * 128;                 // two P tiles
-constexpr int kPTile = kRows * kPage;
-constexpr int kSmemData = kOffP + 2 * kPTile;
+constexpr int kOffP = kOffCvt + 2 * kLatBox;                   // four P messages
+constexpr int kPBytes = kRows * kPage;                         // P: 128 rows x 64 E4M3 keys
+constexpr int kPTile = kPBytes + kRows * 4;                    // then the 128 row references (float)
+constexpr int kPTiles = 4;
+static_assert(kPTile % 128 == 0, "16-byte aligned P tiles and reference pieces");
+constexpr int kSmemData = kOffP + kPTiles * kPTile;
 // P: 8-row x 16-byte core matrices, key chunk c of row group G at c * kPLbo + G * kPSbo, so the 32
 // rows x 16 bytes that one warp writes per key chunk are one contiguous 512-byte piece
 constexpr int kPLbo = 2048, kPSbo = 128;
 constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
 constexpr float kTau = 2.75f;                    // 64 * 2^2.75 = 430.5 < 448
-constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
+// TMEM columns: O half, S, Q latent (E4M3, the A operand of the latent Q.K^T),
+// Q RoPE (f16, the A operand of the RoPE Q.K^T)
+constexpr uint32_t kTO = 0, kTS = 256, kTQ = 320, kTQR = 448;
 static_assert(kOwnBytes == static_cast<int>(kPageTxBytes), "a page fills one own stage");
-static_assert(kOffPeer % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
-              "1 KB aligned tiles");
+static_assert(kOffPeer % 1024 == 0 && kOffCvt % 1024 == 0 && kOffP % 1024 == 0, "1 KB aligned tiles");
 
 struct Bars {
   uint64_t own_full[kOwnStages];    // own page loaded
@@ -780,23 +789,25 @@ struct Bars {
   uint64_t own_cvt[kOwnStages];     // own page's RoPE part converted, dead V rows zeroed
   uint64_t peer_full[kPeerStages];  // V half of the other CTA's page loaded
   uint64_t peer_empty[kPeerStages];
-  uint64_t peer_cvt[kPeerStages];   // its dead rows zeroed
-  uint64_t s_full[2];               // S buffer holds an own page's scores
-  uint64_t p_full[2];               // by page parity: P written here (own page) / O ready here (other's page)
-  uint64_t p_rx;                    // the other CTA's P tile copied in (transaction bytes; armed by the MMA warp)
-  uint64_t pv_done[2];              // by page parity: this CTA's P.V of the page completed
-  uint64_t pv_peer;                 // the other CTA's P.V of one of this CTA's pages completed
-  uint64_t mx_full;                 // the other CTA's row maxima for one of its pages arrived (4 warps)
+  uint64_t peer_tail[4];            // the n-th of them that ends a sequence, in [n % 4]: its dead rows zeroed
+                                    // (the load of the one four later lands only after this one's P.V)
+  uint64_t s_full;                  // S holds an own page's scores
+  uint64_t s_free;                  // S read out (8 softmax warps)
+  uint64_t cvt_free[2];             // by own-page parity: the Q.K^T that read a RoPE buffer completed
+  uint64_t p_full[kPTiles];         // by tile: P written here (own page) / O ready here (other's page)
+  uint64_t p_rx[2];                 // by tile (g / 2 % 2): the other CTA's P message copied in
+                                    // (transaction bytes; re-armed by a softmax thread)
+  uint64_t pv_done[kPTiles];        // by tile: this CTA's P.V of the page completed
+  uint64_t pv_peer[2];              // by own-page parity: the other CTA's P.V of this CTA's page completed
   uint64_t lx_full[2];              // by segment parity: the other CTA's row sums arrived (4 warps)
   uint64_t q_full;                  // a segment's Q copied in (8 softmax warps)
   uint64_t final_mma, xchg;
   uint32_t tmem_base, abort_flag, cvt_ok;
   // written by 16-byte stores (the other CTA's lane 0 sends 32 rows at a time)
-  alignas(16) float mx[2][kRows];   // the other CTA's running maxima, by its page count parity
   alignas(16) float lx[2][kRows];   // the other CTA's row sums, by segment parity
   float xsum[2][2][kRows];          // by segment parity: row-sum halves of the two softmax threads of a row
 };
-static_assert(offsetof(Bars, mx) % 16 == 0 && offsetof(Bars, lx) % 16 == 0, "16-byte rows of maxima and sums");
+static_assert(offsetof(Bars, lx) % 16 == 0, "16-byte rows of sums");
 static_assert(kSmemData % 16 == 0, "the barrier block starts 16-byte aligned");
 
 constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
@@ -865,23 +876,26 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     for (int s = 0; s < kPeerStages; ++s) {
       mbar_init(&bars->peer_full[s], 1);
       mbar_init(&bars->peer_empty[s], 1);
-      mbar_init(&bars->peer_cvt[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, kSoftmaxThreads / 32);
+    for (int b = 0; b < kPTiles; ++b) {
       mbar_init(&bars->p_full[b], kSoftmaxThreads / 32);
       mbar_init(&bars->pv_done[b], 1);
     }
-    mbar_init(&bars->pv_peer, 1);
-    mbar_init(&bars->p_rx, 1);
-    mbar_init(&bars->mx_full, kSoftmaxThreads / 64);
+    for (int b = 0; b < 4; ++b) mbar_init(&bars->peer_tail[b], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->cvt_free[b], 1);
+      mbar_init(&bars->pv_peer[b], 1);
+      mbar_init(&bars->p_rx[b], 1);
+    }
     for (int b = 0; b < 2; ++b) mbar_init(&bars->lx_full[b], kSoftmaxThreads / 64);
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->xchg, kSoftmaxThreads / 32);
     bars->abort_flag = 0;
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bars->p_rx, kPTile);  // the first P tile from the other CTA
+    for (int b = 0; b < 2; ++b) mbar_arrive_expect_tx(&bars->p_rx[b], kPTile);  // the first two messages
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -977,108 +991,110 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    // The whole warp runs the loop and one elected lane issues.  Order: the
-    // Q.K^T of the first own page (and of the second if it shares the first's
-    // segment), then for every page g of the unit its P.V (once its P is
-    // written and O is ready), followed by the Q.K^T of the own page g + 4 if
-    // there is one (its S buffer last held own page g - 4's scores, read
-    // before that page's P was written).  A Q.K^T that opens a segment waits
-    // for that segment's Q, which the softmax warps copy in after writing P
-    // of this CTA's previous own page L, and only once the segments before
-    // L's are finished; so it is issued only after the P.V of L (every P.V
-    // those warps wait for comes before it).
+    // The whole warp runs the loop and one elected lane issues.  The warp
+    // polls the conditions of the next own page's Q.K^T and of the next
+    // page's P.V and issues whichever is ready (the Q.K^T first), so neither
+    // waits behind the other.  Q.K^T(j) needs S read out (the previous own
+    // page's scores), its page converted and, when it opens a segment, that
+    // segment's Q; P.V(g) needs P(g) written and O ready, and the page's V
+    // half (loaded; and for a sequence's last page, its dead rows zeroed).
     constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
     constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
     constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
     const bool leader = elect_one();
-    const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
     const uint16_t other_mask = static_cast<uint16_t>(1u << other);
     PageCursor qk(prm, unit);  // next own page whose Q.K^T is due
-    PageCursor pv(prm, unit);  // every page, in order, for P.V
-    int qn = 0, qk_seg = -1;
+    PageCursor pv(prm, unit);  // next page whose P.V is due
+    int qn = 0, qk_seg = -1, qk_n = 0;  // Q copies consumed, segment of the last Q.K^T, Q.K^Ts issued
+    int tail_n = 0;                     // the other CTA's sequence-tail pages consumed
     auto qk_advance = [&]() -> bool {
       while (qk.next())
         if ((qk.g & 1) == static_cast<int>(rank)) return true;
       return false;
     };
     bool qk_more = qk_advance();
+    bool pv_more = pv.next();
     bool ok = true;
-    auto issue_qk = [&]() -> bool {
-      const int j = qk.g >> 1;
-      if (qk.seg != qk_seg) {  // the segment's first own page: its Q must be in place
-        qk_seg = qk.seg;
-        if (!warp_wait(&bars->q_full, qn & 1, abort_flag, __LINE__)) return false;
-        ++qn;
-      }
-      const int st = j % kOwnStages;
-      if (!warp_spin(&bars->own_cvt[st], (j / kOwnStages) & 1, abort_flag, __LINE__)) return false;
-      tc_fence_after();
-      const uint32_t t_s = tmem + kTS + (j & 1) * kPage;
-      const uint64_t kd = make_sdesc(smem_u32(smem + kOffOwn + st * kOwnBytes), 16, 1024, SWIZZLE_128B);
+    uint64_t t_idle = globaltimer_ns();
+    uint32_t polls = 0;
+    while (ok && (qk_more || pv_more)) {
+      bool did = false;
+      if (qk_more) {
+        const int j = qk.g >> 1;
+        const int st = j % kOwnStages;
+        const bool opens = qk.seg != qk_seg;
+        const bool ready = (!opens || mbar_test_wait(&bars->q_full, qn & 1)) &&
+                           (qk_n == 0 || mbar_test_wait(&bars->s_free, (qk_n - 1) & 1)) &&
+                           mbar_test_wait(&bars->own_cvt[st], (j / kOwnStages) & 1);
+        if (__all_sync(0xffffffffu, ready)) {
+          if (opens) {
+            qk_seg = qk.seg;
+            ++qn;
+          }
+          ++qk_n;
+          tc_fence_after();
+          const uint32_t t_s = tmem + kTS;
+          const uint64_t kd = make_sdesc(smem_u32(smem + kOffOwn + st * kOwnBytes), 16, 1024, SWIZZLE_128B);
 #pragma unroll
-      for (int kk = 0; kk < 16; ++kk)
-        mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4), idesc8,
-                     kk > 0 ? 1u : 0u);
-      const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + (j & 1) * kLatBox), 16, 1024, SWIZZLE_128B);
+          for (int kk = 0; kk < 16; ++kk)
+            mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4),
+                         idesc8, kk > 0 ? 1u : 0u);
+          const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + (j & 1) * kLatBox), 16, 1024, SWIZZLE_128B);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_f16_ss_if(leader, t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
-      tc_commit_if(leader, &bars->s_full[j & 1]);
-      return true;
-    };
-    int last_qk = -1;  // page of the last Q.K^T issued
-    // a Q.K^T may be issued after the P.V of page g (g = -1: before any)
-    auto qk_due = [&](int g) {
-      return qk_more && qk.g <= g + 4 && (qk.seg == qk_seg || qk_seg < 0 || g >= last_qk);
-    };
-    while (ok && qk_due(-1) && (last_qk < 0 || qk.seg == qk_seg)) {
-      last_qk = qk.g;
-      ok = issue_qk();
-      qk_more = qk_advance();
-    }
-    while (ok && pv.next()) {
-      const int g = pv.g;
-      const bool mine = (g & 1) == static_cast<int>(rank);
-      const int idx = g >> 1;
-      // P(g) written here (own page) or O ready for it here (the other CTA's page)
-      if (!warp_spin(&bars->p_full[g & 1], idx & 1, abort_flag, __LINE__)) {
-        ok = false;
-        break;
-      }
-      uint32_t v_base;
-      uint64_t* empty;
-      if (mine) {
-        const int st = idx % kOwnStages;  // converted before its Q.K^T
-        v_base = smem_u32(smem + kOffOwn + st * kOwnBytes) + rank * 2 * kLatBox;
-        empty = &bars->own_empty[st];
-      } else {
-        const int st = idx % kPeerStages;
-        // the other CTA's P tile copied in; then the next one's bytes are expected
-        if (!warp_spin(&bars->p_rx, idx & 1, abort_flag, __LINE__) ||
-            !warp_spin(&bars->peer_cvt[st], (idx / kPeerStages) & 1, abort_flag, __LINE__)) {
-          ok = false;
-          break;
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ts_if(leader, t_s, tmem + kTQR + kk * 8, rd + ((kk * 32) >> 4), idesc16, 1u);
+          tc_commit_if(leader, &bars->s_full);
+          tc_commit_if(leader, &bars->cvt_free[j & 1]);
+          qk_more = qk_advance();
+          did = true;
         }
-        if (leader) mbar_arrive_expect_tx(&bars->p_rx, kPTile);
-        __syncwarp();
-        v_base = smem_u32(smem + kOffPeer + st * kPeerBytes);
-        empty = &bars->peer_empty[st];
       }
-      tc_fence_after();
-      const uint64_t pd = make_sdesc(smem_u32(smem + kOffP + (g & 1) * kPTile), kPLbo, kPSbo, SWIZZLE_NONE);
-      const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
-      const bool first = pv.first();
+      if (!did && pv_more) {
+        const int g = pv.g;
+        const bool mine = (g & 1) == static_cast<int>(rank);
+        const int idx = g >> 1;
+        const bool tail = !mine && pv.pg == pv.sg.n - 1 && (pv.sg.s_k % kPage) != 0;
+        const int st = mine ? idx % kOwnStages : idx % kPeerStages;
+        // P(g) written here (own page) or O ready for it here (the other CTA's page;
+        // its P message arrived before that); the other CTA's page: its V half
+        bool ready = mbar_test_wait(&bars->p_full[g & 3], (g >> 2) & 1);
+        if (ready && !mine)
+          ready = tail ? mbar_test_wait(&bars->peer_tail[tail_n & 3], (tail_n >> 2) & 1)
+                       : mbar_test_wait(&bars->peer_full[st], (idx / kPeerStages) & 1);
+        if (__all_sync(0xffffffffu, ready)) {
+          if (tail) ++tail_n;
+          const uint32_t v_base = mine ? smem_u32(smem + kOffOwn + st * kOwnBytes) + rank * 2 * kLatBox
+                                       : smem_u32(smem + kOffPeer + st * kPeerBytes);
+          uint64_t* empty = mine ? &bars->own_empty[st] : &bars->peer_empty[st];
+          tc_fence_after();
+          const uint64_t pd = make_sdesc(smem_u32(smem + kOffP + (g & 3) * kPTile), kPLbo, kPSbo, SWIZZLE_NONE);
+          const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
+          const bool first = pv.first();
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
-        mma_f8_ss_if(leader, tmem + kTO, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
-                     (first && kk == 0) ? 0u : 1u);
-      tc_commit_if(leader, &bars->pv_done[g & 1]);
-      tc_commit_if(leader, empty);
-      if (!mine) tc_commit_mc_if(leader, &bars->pv_peer, other_mask);  // the owner may reuse its P tile
-      while (ok && qk_due(g)) {
-        last_qk = qk.g;
-        ok = issue_qk();
-        qk_more = qk_advance();
+          for (int kk = 0; kk < 2; ++kk)
+            mma_f8_ss_if(leader, tmem + kTO, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
+                         (first && kk == 0) ? 0u : 1u);
+          tc_commit_if(leader, &bars->pv_done[g & 3]);
+          tc_commit_if(leader, empty);
+          if (!mine) tc_commit_mc_if(leader, &bars->pv_peer[idx & 1], other_mask);  // the owner may reuse its P tile
+          pv_more = pv.next();
+          did = true;
+        }
+      }
+      // bounded: no progress for the wait limit (or another role stopped) ends the loop
+      if (did) {
+        polls = 0;
+      } else if ((++polls & 255u) == 0) {
+        if (*abort_flag) ok = false;
+        if (polls == 256) t_idle = globaltimer_ns();
+        if (ok && polls > kWaitMinPolls && globaltimer_ns() - t_idle > *(volatile uint64_t*)&g_wait_limit_ns) {
+          if (lane == 0) {
+            atomicOr(&g_status_mla, FP8MLA_DEV_WAIT_TIMEOUT);
+            record_timeout_site(__LINE__);
+          }
+          ok = false;
+        }
+        ok = __all_sync(0xffffffffu, ok);
       }
     }
     if (!ok) fail();
@@ -1088,20 +1104,26 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
   } else if (warp == 2 || warp == 3) {
     // ------------------- RoPE conversion, tail zeroing (64 threads) ----
     // Own pages: the RoPE part to f16 (exact) in buffer j % 2, free once the
-    // Q.K^T of own page j - 2 completed; dead rows (past the sequence end) of
-    // this CTA's V half zeroed.  The other CTA's pages: dead rows zeroed.
+    // Q.K^T of own page j - 2 completed (cvt_free); dead rows (past the sequence end) of
+    // this CTA's V half zeroed.  The other CTA's pages: only a sequence's last
+    // page with dead rows, which are zeroed (peer_tail); the MMA warp waits for
+    // the load of the others itself.
     const int t = threadIdx.x - 64;  // token row of the page
     PageCursor pc(prm, unit);
     bool ok = true;
+    int tails = 0;  // the other CTA's sequence-tail pages done
     while (ok && pc.next()) {
       const int g = pc.g, idx = g >> 1;
       const bool mine = (g & 1) == static_cast<int>(rank);
       const int st = mine ? idx % kOwnStages : idx % kPeerStages;
       const int use = mine ? idx / kOwnStages : idx / kPeerStages;
+      // every load is waited for in turn (so no wait here can pass on a phase
+      // two ahead), but the other CTA's pages need work only at a sequence tail
+      const bool work = mine || (pc.pg == pc.sg.n - 1 && (pc.sg.s_k % kPage) != 0);
       if (t == 0) {
         bool w = wait_bounded(mine ? &bars->own_full[st] : &bars->peer_full[st], use & 1, abort_flag, &g_status_mla, __LINE__);
         if (w && mine && idx >= 2)
-          w = wait_bounded(&bars->s_full[idx & 1], ((idx - 2) >> 1) & 1, abort_flag, &g_status_mla, __LINE__);
+          w = wait_bounded(&bars->cvt_free[idx & 1], ((idx - 2) >> 1) & 1, abort_flag, &g_status_mla, __LINE__);
         bars->cvt_ok = w ? 1u : 0u;
       }
       named_bar_sync(1, 64);
@@ -1109,6 +1131,7 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         ok = false;
         break;
       }
+      if (!work) continue;
       const bool dead = (pc.pg == pc.sg.n - 1) && (t >= pc.sg.s_k - pc.pg * kPage);  // slot past the end
       const uint4 z = make_uint4(0, 0, 0, 0);
       uint8_t* vhalf = mine ? smem + kOffOwn + st * kOwnBytes + rank * 2 * kLatBox : smem + kOffPeer + st * kPeerBytes;
@@ -1144,7 +1167,8 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 64);
-      if (t == 0) mbar_arrive(mine ? &bars->own_cvt[st] : &bars->peer_cvt[st]);
+      if (t == 0) mbar_arrive(mine ? &bars->own_cvt[st] : &bars->peer_tail[tails & 3]);
+      if (!mine) ++tails;
     }
     if (!ok && t == 0) fail();
   } else {
@@ -1162,10 +1186,8 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       ++xphase;
       return ok;
     };
-    const uint32_t r_mx = remote(&bars->mx[0][r]);
     const uint32_t r_lx = remote(&bars->lx[0][r]);
-    const uint32_t r_prx = remote(&bars->p_rx);
-    const uint32_t r_mxfull = remote(&bars->mx_full);
+    const uint32_t r_prx0 = remote(&bars->p_rx[0]);
     const uint32_t r_lxfull0 = remote(&bars->lx_full[0]);
     const uint32_t r_p0 = remote(smem + kOffP);
     const uint32_t prow = static_cast<uint32_t>((r >> 3) * kPSbo + (r & 7) * 16);
@@ -1191,7 +1213,7 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
 
     // Copies this half of sequence b_seq's quantised Q row (prepared by
     // mla_qprep_kernel) in: latent bytes [256 hf, +256) into TMEM columns
-    // kTQ + 64 hf.., RoPE values [32 hf, +32) into the Q RoPE tile.
+    // kTQ + 64 hf.., RoPE values [32 hf, +32) into columns kTQR + 16 hf..
     int qn = 0;
     float qs_cur = 1.f;
     auto copy_q = [&](int b_seq) -> bool {
@@ -1216,10 +1238,17 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         }
         tmem_st16(lane_base + kTQ + (4 * hf + ch) * 16, pk);
       }
-      uint8_t* dst = smem + kOffQRope + r * 128;
+      {
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(dst + (((4 * hf + c) ^ (r & 7)) << 4)) = w[c];
-      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs
+        for (int c = 0; c < 4; ++c) {
+          pk[4 * c + 0] = w[c].x;
+          pk[4 * c + 1] = w[c].y;
+          pk[4 * c + 2] = w[c].z;
+          pk[4 * c + 3] = w[c].w;
+        }
+        tmem_st16(lane_base + kTQR + 16 * hf, pk);
+      }
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bars->q_full);
@@ -1245,26 +1274,24 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     PageCursor pc(prm, unit);
     bool ok = true;
     int cur_seg = -1;
-    float m_run = kNegInf, l_run = 0.f;
+    float m_run = kNegInf, l_run = 0.f;  // reference of O and l; this CTA's share of l
+    float m_own = kNegInf;                // this CTA's latest reference in the segment
     int pend = -1;  // the other CTA's page whose rescale / O-ready is still due
     bool pend_first = false;
     int qtok = 0, visible = 0, min_visible = 0;
     float c_row = 0.f;
 
-    // The other CTA's page g (after this CTA's page g - 1): take its running
-    // maximum, rescale l and (if it rose) O, and declare O ready for its P.V.
-    auto finish_other = [&](int g, bool first) -> bool {
-      const int k = g >> 1;
-      if (!warp_spin<true>(&bars->mx_full, k & 1, abort_flag, __LINE__)) return false;
-      const float m_new = bars->mx[k & 1][r];
-      const bool rescale = !first && m_new != m_run;
+    // Moves O and l to a new reference before a page's P.V: both are
+    // multiplied by 2^(m_run - m_new) once the P.V of page g - 1 completed.
+    // A reference of -inf (the row sees no key of the page, so its P is 0)
+    // leaves them where they are, in both CTAs alike.
+    auto rescale_to = [&](int g, float m_new, bool first) -> bool {
+      const bool rescale = !first && m_new != m_run && m_new != kNegInf;
       const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.f;
       l_run = first ? 0.f : l_run * alpha;
-      m_run = m_new;
-      // this CTA's arrivals for page g come after page g - 2's phase completed
-      if (g >= 2 && !warp_spin(&bars->pv_done[g & 1], ((g - 2) >> 1) & 1, abort_flag, __LINE__)) return false;
+      if (first || rescale) m_run = m_new;
       if (__any_sync(0xffffffffu, rescale)) {
-        if (!warp_spin(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag, __LINE__)) return false;
+        if (!warp_spin(&bars->pv_done[(g - 1) & 3], ((g - 1) >> 2) & 1, abort_flag, __LINE__)) return false;
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < kOHalf / 32; ++ch) {
@@ -1278,9 +1305,26 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         }
         tmem_st_wait();
       }
+      return true;
+    };
+    // The other CTA's page g: wait for its P message, take the reference it
+    // carries (kept for this CTA's page g + 3), rescale O and l to it, and
+    // declare O ready for the page's P.V.
+    float m_other = kNegInf;  // the other CTA's latest reference in this segment
+    auto finish_other = [&](int g, bool first) -> bool {
+      const int k = g >> 1;
+      if (!warp_spin(&bars->p_rx[k & 1], (k >> 1) & 1, abort_flag, __LINE__)) return false;
+      // (every softmax thread has passed this phase before the message's next
+      // bytes can come: they follow this page's P.V here)
+      if (warp == 4 && lane == 0) mbar_arrive_expect_tx(&bars->p_rx[k & 1], kPTile);
+      const float m_new = reinterpret_cast<const float*>(smem + kOffP + (g & 3) * kPTile + kPBytes)[r];
+      m_other = m_new;
+      // this CTA's arrivals for page g come after page g - 4's phase of the tile completed
+      if (g >= 4 && !warp_spin(&bars->pv_done[g & 3], ((g - 4) >> 2) & 1, abort_flag, __LINE__)) return false;
+      if (!rescale_to(g, m_new, first)) return false;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[g & 1]);
+      if (lane == 0) mbar_arrive(&bars->p_full[g & 3]);
       return true;
     };
 
@@ -1304,6 +1348,8 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         cur_seg = pc.seg;
         m_run = kNegInf;
         l_run = 0.f;
+        m_own = kNegInf;
+        m_other = kNegInf;
         qtok = (r < R) ? r / prm.h_q : 0;
         visible = prm.causal ? (pc.sg.s_k - prm.s_q + qtok + 1) : pc.sg.s_k;
         min_visible = prm.causal ? (pc.sg.s_k - prm.s_q + 1) : pc.sg.s_k;
@@ -1323,16 +1369,18 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       } else {
         const int j = g >> 1;
         c_row = prm.softmax_scale * kLog2e * qs_cur * kv_scale;
-        if (!warp_spin(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag, __LINE__)) {
+        if (!warp_spin(&bars->s_full, j & 1, abort_flag, __LINE__)) {
           ok = false;
           break;
         }
         tc_fence_after();
         // both halves of the row: the other half only for the row max
         uint32_t s[32], so[32];
-        tmem_ld32(lane_base + kTS + (j & 1) * kPage + 32 * hf, s);
-        tmem_ld32(lane_base + kTS + (j & 1) * kPage + 32 * (1 - hf), so);
+        tmem_ld32(lane_base + kTS + 32 * hf, s);
+        tmem_ld32(lane_base + kTS + 32 * (1 - hf), so);
         tmem_ld_wait();
+        tc_fence_before();
+        warp_arrive(&bars->s_free);  // the next own page's Q.K^T may overwrite S
         if (pc.pg * kPage + kPage > min_visible) {
           const int base = pc.pg * kPage + 32 * hf, base_o = pc.pg * kPage + 32 * (1 - hf);
 #pragma unroll
@@ -1356,27 +1404,18 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         m8[7] = m22[21];
         const float mx =
             fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
-        // the other CTA's previous page first: its maximum precedes this page's
-        if (pend >= 0) {
-          if (!finish_other(pend, pend_first)) {
-            ok = false;
-            break;
-          }
-          pend = -1;
-        }
-        // P tile g % 2 is free once both CTAs' P.V of page g - 2 completed
-        if (g >= 2 && (!warp_spin(&bars->pv_done[g & 1], ((g - 2) >> 1) & 1, abort_flag, __LINE__) ||
-                       !warp_spin<true>(&bars->pv_peer, (j - 1) & 1, abort_flag, __LINE__))) {
+        // P tile g % 4 is free once both CTAs' P.V of page g - 4 completed
+        if (g >= 4 && (!warp_spin(&bars->pv_done[g & 3], ((g - 4) >> 2) & 1, abort_flag, __LINE__) ||
+                       !warp_spin(&bars->pv_peer[j & 1], ((j - 2) >> 1) & 1, abort_flag, __LINE__))) {
           ok = false;
           break;
         }
+        // the reference: this CTA's and the other's latest ones (pages g - 2 and g - 3),
+        // raised to this page's maximum when that exceeds them by more than kTau
         const bool first = pc.first();
-        const float m_prev = first ? kNegInf : m_run;
-        const float m_new = (mx > m_prev + kTau) ? mx : m_prev;
-        if (hf == 0) send_rows(r_mx - lane * 4 + (j & 1) * kRows * 4, m_new, r_mxfull);
-        const bool rescale = !first && m_new != m_prev;
-        const float alpha = rescale ? ex2_approx(m_prev - m_new) : 1.f;
-        m_run = m_new;
+        const float m_known = fmaxf(m_own, m_other);
+        const float m_new = (mx > m_known + kTau) ? mx : m_known;
+        m_own = m_new;
         const float bias = (m_new == kNegInf) ? 0.f : (kPLog2 - m_new);
         float sum = 0.f;
         uint32_t pk[8];
@@ -1389,44 +1428,48 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
           sum += (p0 + p1) + (p2 + p3);
           pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
         }
-        l_run = first ? sum : l_run * alpha + sum;
-        if (__any_sync(0xffffffffu, rescale)) {
-          if (!warp_spin(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag, __LINE__)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (int ch = 0; ch < kOHalf / 32; ++ch) {
-            const uint32_t col = kTO + hf * kOHalf + ch * 32;
-            uint32_t o[32];
-            tmem_ld32(lane_base + col, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st32(lane_base + col, o);
-          }
-          tmem_st_wait();
-        }
-        {  // this thread's 32 keys of row r: 16-byte chunks 2 hf and 2 hf + 1
-          uint8_t* lp = smem + kOffP + (g & 1) * kPTile + prow;
+        {  // this thread's 32 keys of row r (16-byte chunks 2 hf, 2 hf + 1), and the row's reference
+          uint8_t* tile = smem + kOffP + (g & 3) * kPTile;
+          uint8_t* lp = tile + prow;
           *reinterpret_cast<uint4*>(lp + (2 * hf) * kPLbo) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           *reinterpret_cast<uint4*>(lp + (2 * hf + 1) * kPLbo) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          if (hf == 0) reinterpret_cast<float*>(tile + kPBytes)[r] = m_new;
         }
         fence_proxy_async_smem();
-        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bars->p_full[g & 1]);  // P written (and O rescaled) here
-          // the warp's two 512-byte pieces of P to the other CTA's tile, by the
-          // async proxy, counted on its p_rx barrier
-          const uint32_t piece = static_cast<uint32_t>((g & 1) * kPTile + (warp % 4) * 4 * kPSbo);
+          // the warp's two 512-byte pieces of P (and the hf 0 warps' 32 row
+          // references) to the other CTA's message, by the async proxy,
+          // counted on its p_rx barrier of that message
+          const uint32_t tile = static_cast<uint32_t>((g & 3) * kPTile);
+          const uint32_t piece = tile + (warp % 4) * 4 * kPSbo;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const uint32_t off = piece + (2 * hf + c) * kPLbo;
-            bulk_copy_to_cluster(r_p0 + off, smem + kOffP + off, 32 * 16, r_prx);
+            bulk_copy_to_cluster(r_p0 + off, smem + kOffP + off, 32 * 16, r_prx0 + (j & 1) * 8);
+          }
+          if (hf == 0) {
+            const uint32_t off = tile + kPBytes + (warp % 4) * 128;
+            bulk_copy_to_cluster(r_p0 + off, smem + kOffP + off, 128, r_prx0 + (j & 1) * 8);
           }
         }
+        // the other CTA's previous page: O moves to its reference and is declared
+        // ready for its P.V before this page's rescale
+        if (pend >= 0) {
+          if (!finish_other(pend, pend_first)) {
+            ok = false;
+            break;
+          }
+          pend = -1;
+        }
+        if (!rescale_to(g, m_new, first)) {
+          ok = false;
+          break;
+        }
+        l_run += sum;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[g & 3]);  // P written and O rescaled here
         // this CTA's last page of the segment: the next segment's Q may replace this one's
         bool last_own = pc.last() || (pc.pg + 1 == pc.sg.hi - 1);
         if (last_own) {
@@ -1457,7 +1500,7 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       const float l_here = bars->xsum[sp][0][r] + bars->xsum[sp][1][r];
       // one barrier per slot: the other CTA may finish the next segment before this one reads this slot
       if (hf == 0) send_rows(r_lx - lane * 4 + sp * kRows * 4, l_here, r_lxfull0 + sp * 8);
-      if (!warp_spin<true>(&bars->lx_full[sp], (cur_seg >> 1) & 1, abort_flag, __LINE__)) {
+      if (!warp_wait<true>(&bars->lx_full[sp], (cur_seg >> 1) & 1, abort_flag, __LINE__)) {
         ok = false;
         break;
       }
@@ -1467,7 +1510,7 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
       const int slot = whole ? 0 : prm.num_splits[pc.sg.b] + pc.sg.split;
       // O is final once this CTA's P.V of the segment's last page completed
-      if (!warp_wait(&bars->pv_done[g & 1], (g >> 1) & 1, abort_flag, __LINE__)) {
+      if (!warp_wait(&bars->pv_done[g & 3], (g >> 2) & 1, abort_flag, __LINE__)) {
         ok = false;
         break;
       }
@@ -1515,7 +1558,8 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       PageCursor cnt(prm, unit);
       while (cnt.next())
         if ((cnt.g & 1) == static_cast<int>(rank)) ++nown;
-      if (nown > 0) warp_spin<true>(&bars->pv_peer, (nown - 1) & 1, abort_flag, __LINE__);
+      if (nown > 0) warp_spin(&bars->pv_peer[(nown - 1) & 1], ((nown - 1) >> 1) & 1, abort_flag, __LINE__);
+      if (nown > 1) warp_spin(&bars->pv_peer[nown & 1], ((nown - 2) >> 1) & 1, abort_flag, __LINE__);
     }
   }
 

@@ -144,6 +144,11 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity)
   return ok != 0;
 }
 
+// Acquire-release fence at cluster scope: after a wait observed an mbarrier
+// phase that threads of another CTA completed with release arrivals, their
+// earlier writes are visible to this thread.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 // Generic-proxy writes to shared memory anywhere in the cluster -> visible to the async proxy.
 __device__ __forceinline__ void fence_proxy_async_cluster() {
   asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
