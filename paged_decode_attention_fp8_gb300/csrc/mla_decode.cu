@@ -748,27 +748,38 @@ __device__ __forceinline__ void lane_group_transpose(uint4 (&pc)[N], int lane) {
 // its reference), every stored P is at most 64 * 2^kTau < 448, and no page
 // waits for the other CTA's decision on the page just before it.
 //
-// Per CTA: TMEM holds its O half (256 columns), one S buffer (64), the
-// latent Q (128, E4M3) and Q's RoPE part (32, f16).  Shared memory holds a
-// ring of whole pages for its own pages (3 x 36 KB), a ring of V halves for
-// the other CTA's pages (3 x 16 KB), two f16 RoPE conversion buffers and four
-// P messages: page g's P and its 128 row references go to message g % 4 in
-// both CTAs (to the other CTA by an async bulk copy, which the sender does not
-// wait for), and a message is rewritten four pages later, after both CTAs'
-// P.V of the page before read it.
+// Per CTA: TMEM holds its O half (256 columns), two S buffers (64 each; its
+// own pages alternate, so one page's Q.K^T runs while the softmax works on
+// the previous one) and the latent Q (128, E4M3).  Shared memory holds a V
+// ring with this CTA's dv half of the latent bytes of every page (6 x 16 KB,
+// released by the page's P.V), a K ring with the rest of this CTA's own pages
+// (3 x 24 KB: the other latent half and the RoPE part, converted to f16 in
+// place; released when the page's Q.K^T completes -- Q.K^T reads the page's
+// latent bytes from both rings), Q's RoPE part (f16, 16 KB) and four P
+// messages: page g's P and its 128 row references go to message g % 4 in
+// both CTAs (to the other CTA by asynchronous remote stores that count their
+// bytes on its p_rx barrier; the sender does not wait for them), and a
+// message is rewritten four pages later, after both CTAs' P.V of the page
+// before read it.
 // ===========================================================================
 namespace pr {
-constexpr int kOwnStages = 3;
-constexpr int kPeerStages = 3;
+constexpr int kKStages = 3;   // own pages: the other latent half and the RoPE part, for Q.K^T
+constexpr int kVStages = 6;   // this CTA's latent half of every page, for P.V (and own pages' Q.K^T)
 constexpr int kThreads = 384;
-constexpr int kOwnBytes = 4 * kLatBox + kPage * 64;  // a whole page: 4 latent boxes + the RoPE box
-constexpr int kPeerBytes = 2 * kLatBox;               // this CTA's dv half of a page's latent bytes
-constexpr int kOffOwn = 0;
-constexpr int kOffPeer = kOffOwn + kOwnStages * kOwnBytes;
-constexpr int kOffCvt = kOffPeer + kPeerStages * kPeerBytes;  // two f16 RoPE buffers (64 keys x 128 B)
-constexpr int kOffP = kOffCvt + 2 * kLatBox;                   // four P messages
-constexpr int kPBytes = kRows * kPage;                         // P: 128 rows x 64 E4M3 keys
-constexpr int kPTile = kPBytes + kRows * 4;                    // then the 128 row references (float)
+// a K stage: the other CTA's two 128-byte latent boxes, then the RoPE part as
+// f16 (64 keys x 128 B, 128-byte swizzle), converted in place from the E4M3
+// RoPE box that the load puts in the second half of that region
+constexpr int kKRope = 2 * kLatBox;
+constexpr int kKRopeRaw = kKRope + kPage * 64;
+constexpr int kKBytes = kKRope + kLatBox;
+constexpr uint32_t kKTx = 2 * kLatBox + kPage * 64;   // bytes the K part of an own page's load delivers
+constexpr int kVBytes = 2 * kLatBox;                  // latent bytes [256 rank, 256 rank + 256) of a page
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kKStages * kKBytes;
+constexpr int kOffQRope = kOffV + kVStages * kVBytes;  // Q RoPE, 128 rows x 64 f16, 128-byte swizzle
+constexpr int kOffP = kOffQRope + kRows * 128;         // four P messages
+constexpr int kPBytes = kRows * kPage;                 // P: 128 rows x 64 E4M3 keys
+constexpr int kPTile = kPBytes + kRows * 4;            // then the 128 row references (float)
 constexpr int kPTiles = 4;
 static_assert(kPTile % 128 == 0, "16-byte aligned P tiles and reference pieces");
 constexpr int kSmemData = kOffP + kPTiles * kPTile;
@@ -777,28 +788,25 @@ constexpr int kSmemData = kOffP + kPTiles * kPTile;
 constexpr int kPLbo = 2048, kPSbo = 128;
 constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
 constexpr float kTau = 2.75f;                    // 64 * 2^2.75 = 430.5 < 448
-// TMEM columns: O half, S, Q latent (E4M3, the A operand of the latent Q.K^T),
-// Q RoPE (f16, the A operand of the RoPE Q.K^T)
-constexpr uint32_t kTO = 0, kTS = 256, kTQ = 320, kTQR = 448;
-static_assert(kOwnBytes == static_cast<int>(kPageTxBytes), "a page fills one own stage");
-static_assert(kOffPeer % 1024 == 0 && kOffCvt % 1024 == 0 && kOffP % 1024 == 0, "1 KB aligned tiles");
+// TMEM columns: O half, two S buffers, Q latent (E4M3, the A operand of the latent Q.K^T)
+constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
+static_assert(kKBytes % 1024 == 0 && kOffV % 1024 == 0 && kVBytes % 1024 == 0 && kOffP % 1024 == 0 &&
+                  kKRope % 1024 == 0 && kOffQRope % 1024 == 0,
+              "1 KB aligned tiles");
 
 struct Bars {
-  uint64_t own_full[kOwnStages];    // own page loaded
-  uint64_t own_empty[kOwnStages];   // own stage may be refilled
-  uint64_t own_cvt[kOwnStages];     // own page's RoPE part converted, dead V rows zeroed
-  uint64_t peer_full[kPeerStages];  // V half of the other CTA's page loaded
-  uint64_t peer_empty[kPeerStages];
-  uint64_t peer_tail[4];            // the n-th of them that ends a sequence, in [n % 4]: its dead rows zeroed
-                                    // (the load of the one four later lands only after this one's P.V)
-  uint64_t s_full;                  // S holds an own page's scores
-  uint64_t s_free;                  // S read out (8 softmax warps)
-  uint64_t cvt_free[2];             // by own-page parity: the Q.K^T that read a RoPE buffer completed
+  uint64_t k_full[kKStages];        // own page's other latent half and RoPE part loaded
+  uint64_t k_cvt[kKStages];         // its RoPE part converted to f16
+  uint64_t k_empty[kKStages];       // its Q.K^T completed: the stage may be refilled
+  uint64_t v_full[kVStages];        // by page g % kVStages: this CTA's latent half of page g loaded
+  uint64_t v_empty[kVStages];       // its P.V (and for an own page its Q.K^T) completed
+  uint64_t s_full[2];               // by own-page parity: S buffer holds the page's scores
+  uint64_t s_free[2];               // S buffer read out (8 softmax warps)
   uint64_t p_full[kPTiles];         // by tile: P written here (own page) / O ready here (other's page)
   uint64_t p_rx[2];                 // by tile (g / 2 % 2): the other CTA's P message copied in
                                     // (transaction bytes; re-armed by a softmax thread)
-  uint64_t pv_done[kPTiles];        // by tile: this CTA's P.V of the page completed
-  uint64_t pv_peer[2];              // by own-page parity: the other CTA's P.V of this CTA's page completed
+  uint64_t pv_done[kPTiles];        // by tile: the P.V of the page completed here -- and, for the tiles of
+                                    // this CTA's pages (g % 2 = rank), in the other CTA too (2 arrivals)
   uint64_t lx_full[2];              // by segment parity: the other CTA's row sums arrived (4 warps)
   uint64_t q_full;                  // a segment's Q copied in (8 softmax warps)
   uint64_t final_mma, xchg;
@@ -868,27 +876,24 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kOwnStages; ++s) {
-      mbar_init(&bars->own_full[s], 1);
-      mbar_init(&bars->own_empty[s], 1);
-      mbar_init(&bars->own_cvt[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_cvt[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
     }
-    for (int s = 0; s < kPeerStages; ++s) {
-      mbar_init(&bars->peer_full[s], 1);
-      mbar_init(&bars->peer_empty[s], 1);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, kSoftmaxThreads / 32);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], kSoftmaxThreads / 32);
+    }
     for (int b = 0; b < kPTiles; ++b) {
       mbar_init(&bars->p_full[b], kSoftmaxThreads / 32);
-      mbar_init(&bars->pv_done[b], 1);
+      mbar_init(&bars->pv_done[b], (b & 1) == static_cast<int>(rank) ? 2 : 1);
     }
-    for (int b = 0; b < 4; ++b) mbar_init(&bars->peer_tail[b], 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->cvt_free[b], 1);
-      mbar_init(&bars->pv_peer[b], 1);
-      mbar_init(&bars->p_rx[b], 1);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(&bars->p_rx[b], 1);
     for (int b = 0; b < 2; ++b) mbar_init(&bars->lx_full[b], kSoftmaxThreads / 64);
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
     mbar_init(&bars->final_mma, 1);
@@ -915,78 +920,92 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
-    // Own pages: the whole page (four 128-byte latent boxes + the RoPE box).
-    // The other CTA's pages: this CTA's dv half (latent boxes 2 rank, 2 rank + 1).
+    // Two streams of loads, issued by lane 0 as their stages free up (own pages
+    // first).  Own page g: its latent half [256 rank, +256) into V stage
+    // g % kVStages, the other half and the RoPE box into the next K stage.  The
+    // other CTA's page g: this CTA's latent half into V stage g % kVStages.
+    // Each stream fetches the block-table entry of its next page right after
+    // issuing a load, so the entry is at hand when the stages free up.
     if (lane == 0) {
       tma_prefetch_desc(&tm_lat);
       tma_prefetch_desc(&tm_rope);
-    }
-    const int fault = (unit == 0 && rank == 0) ? *(volatile int*)&g_fault_page : 0;
-    SegmentWalker walk(prm, unit);
-    Segment sg;
-    int g = 0;
-    uint32_t own_issued = 0, own_par = 0, peer_issued = 0, peer_par = 0;
-    bool ok = true;
-    while (ok && walk.next(sg)) {
-      const int32_t* bt = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
-      for (int chunk = sg.lo; ok && chunk < sg.hi; chunk += 32) {
-        int mine = 0;
-        if (chunk + lane < sg.hi) {
-          mine = __ldg(bt + chunk + lane);
-          if (mine < 0 || mine >= prm.num_pages) {
-            atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
-            mine = 0;
+      const int fault = (unit == 0 && rank == 0) ? *(volatile int*)&g_fault_page : 0;
+      auto phys_of = [&](const PageCursor& c) -> int {
+        int ph = __ldg(prm.block_table + static_cast<size_t>(c.sg.b) * prm.max_pages + c.pg);
+        if (ph < 0 || ph >= prm.num_pages) {
+          atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
+          ph = 0;
+        }
+        return ph;
+      };
+      PageCursor oc(prm, unit), xc(prm, unit);  // own pages; the other CTA's pages
+      auto advance = [&](PageCursor& c, int want) -> bool {
+        while (c.next())
+          if ((c.g & 1) == want) return true;
+        return false;
+      };
+      bool o_more = advance(oc, static_cast<int>(rank)), x_more = advance(xc, static_cast<int>(other));
+      int o_phys = o_more ? phys_of(oc) : 0, x_phys = x_more ? phys_of(xc) : 0;
+      int kn = 0;  // own-page loads issued
+      uint32_t v_last = 0, v_par = 0, k_last = 0, k_par = 0;  // per stage: loaded here, and its phase parity
+      auto v_free = [&](int g) { return g < kVStages || mbar_test_wait(&bars->v_empty[g % kVStages], ((g / kVStages) - 1) & 1); };
+      auto load_v = [&](int g, int phys) {
+        const int st = g % kVStages;
+        uint8_t* sb = smem + kOffV + st * kVBytes;
+        mbar_arrive_expect_tx(&bars->v_full[st], kVBytes);
+        tma_load_3d(sb, &tm_lat, &bars->v_full[st], static_cast<int>(rank) * 256, 0, phys);
+        tma_load_3d(sb + kLatBox, &tm_lat, &bars->v_full[st], static_cast<int>(rank) * 256 + 128, 0, phys);
+        v_last |= 1u << st;
+        v_par = (v_par & ~(1u << st)) | (static_cast<uint32_t>((g / kVStages) & 1) << st);
+      };
+      uint32_t polls = 0;
+      uint64_t t_idle = 0;
+      bool ok = true;
+      while (ok && (o_more || x_more)) {
+        bool did = false;
+        if (o_more) {
+          const int st = kn % kKStages, use = kn / kKStages;
+          if ((use == 0 || mbar_test_wait(&bars->k_empty[st], (use - 1) & 1)) && v_free(oc.g)) {
+            if (fault != oc.g + 1) {
+              load_v(oc.g, o_phys);
+              uint8_t* sb = smem + kOffK + st * kKBytes;
+              mbar_arrive_expect_tx(&bars->k_full[st], kKTx);
+              tma_load_3d(sb, &tm_lat, &bars->k_full[st], static_cast<int>(other) * 256, 0, o_phys);
+              tma_load_3d(sb + kLatBox, &tm_lat, &bars->k_full[st], static_cast<int>(other) * 256 + 128, 0, o_phys);
+              tma_load_3d(sb + kKRopeRaw, &tm_rope, &bars->k_full[st], kDLat, 0, o_phys);
+              k_last |= 1u << st;
+              k_par = (k_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+            }
+            ++kn;
+            o_more = advance(oc, static_cast<int>(rank));
+            if (o_more) o_phys = phys_of(oc);
+            did = true;
           }
         }
-        const int cnt = min(32, sg.hi - chunk);
-        for (int jj = 0; jj < cnt; ++jj, ++g) {
-          const int phys = __shfl_sync(0xffffffffu, mine, jj);
-          const int idx = g >> 1;
-          bool waited = true;
-          if (lane == 0) {
-            const bool skip = fault == g + 1;
-            if ((g & 1) == static_cast<int>(rank)) {
-              const int st = idx % kOwnStages, use = idx / kOwnStages;
-              waited = use == 0 || wait_bounded(&bars->own_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
-              if (waited && !skip) {
-                uint8_t* sb = smem + kOffOwn + st * kOwnBytes;
-                mbar_arrive_expect_tx(&bars->own_full[st], kOwnBytes);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  tma_load_3d(sb + q * kLatBox, &tm_lat, &bars->own_full[st], q * 128, 0, phys);
-                tma_load_3d(sb + 4 * kLatBox, &tm_rope, &bars->own_full[st], kDLat, 0, phys);
-                own_issued |= 1u << st;
-                own_par = (own_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
-              }
-            } else {
-              const int st = idx % kPeerStages, use = idx / kPeerStages;
-              waited = use == 0 || wait_bounded(&bars->peer_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
-              if (waited && !skip) {
-                uint8_t* sb = smem + kOffPeer + st * kPeerBytes;
-                mbar_arrive_expect_tx(&bars->peer_full[st], kPeerBytes);
-                tma_load_3d(sb, &tm_lat, &bars->peer_full[st], static_cast<int>(rank) * 256, 0, phys);
-                tma_load_3d(sb + kLatBox, &tm_lat, &bars->peer_full[st], static_cast<int>(rank) * 256 + 128, 0,
-                            phys);
-                peer_issued |= 1u << st;
-                peer_par = (peer_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
-              }
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
+        if (!did && x_more && v_free(xc.g)) {
+          if (fault != xc.g + 1) load_v(xc.g, x_phys);
+          x_more = advance(xc, static_cast<int>(other));
+          if (x_more) x_phys = phys_of(xc);
+          did = true;
+        }
+        if (did) {
+          polls = 0;
+        } else if ((++polls & 255u) == 0) {
+          if (*abort_flag) ok = false;
+          if (polls == 256) t_idle = globaltimer_ns();
+          if (ok && polls > kWaitMinPolls && globaltimer_ns() - t_idle > *(volatile uint64_t*)&g_wait_limit_ns) {
+            atomicOr(&g_status_mla, FP8MLA_DEV_WAIT_TIMEOUT);
+            record_timeout_site(__LINE__);
             ok = false;
-            break;
           }
         }
       }
-    }
-    if (!ok && lane == 0) fail();
-    // Never leave with copies in flight: wait for the last load of each stage.
-    if (lane == 0) {
-      for (int s = 0; s < kOwnStages; ++s)
-        if ((own_issued >> s) & 1u) wait_bounded(&bars->own_full[s], (own_par >> s) & 1u, nullptr, &g_status_mla, __LINE__);
-      for (int s = 0; s < kPeerStages; ++s)
-        if ((peer_issued >> s) & 1u)
-          wait_bounded(&bars->peer_full[s], (peer_par >> s) & 1u, nullptr, &g_status_mla, __LINE__);
+      if (!ok) fail();
+      // Never leave with copies in flight: wait for the last load of each stage.
+      for (int st = 0; st < kKStages; ++st)
+        if ((k_last >> st) & 1u) wait_bounded(&bars->k_full[st], (k_par >> st) & 1u, nullptr, &g_status_mla, __LINE__);
+      for (int st = 0; st < kVStages; ++st)
+        if ((v_last >> st) & 1u) wait_bounded(&bars->v_full[st], (v_par >> st) & 1u, nullptr, &g_status_mla, __LINE__);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -994,19 +1013,21 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     // The whole warp runs the loop and one elected lane issues.  The warp
     // polls the conditions of the next own page's Q.K^T and of the next
     // page's P.V and issues whichever is ready (the Q.K^T first), so neither
-    // waits behind the other.  Q.K^T(j) needs S read out (the previous own
-    // page's scores), its page converted and, when it opens a segment, that
-    // segment's Q; P.V(g) needs P(g) written and O ready, and the page's V
-    // half (loaded; and for a sequence's last page, its dead rows zeroed).
+    // waits behind the other.  Q.K^T(j) needs S buffer j % 2 read out (own
+    // page j - 2's scores), its page loaded and converted and, when it opens a
+    // segment, that segment's Q; P.V(g) needs P(g) written and O ready, and
+    // the page's V half loaded.  Before the P.V of a sequence's last page the
+    // warp zeroes the V rows past the sequence end (they may hold anything,
+    // and P is 0 there).
     constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
     constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
     constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
     const bool leader = elect_one();
     const uint16_t other_mask = static_cast<uint16_t>(1u << other);
+    const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
     PageCursor qk(prm, unit);  // next own page whose Q.K^T is due
     PageCursor pv(prm, unit);  // next page whose P.V is due
     int qn = 0, qk_seg = -1, qk_n = 0;  // Q copies consumed, segment of the last Q.K^T, Q.K^Ts issued
-    int tail_n = 0;                     // the other CTA's sequence-tail pages consumed
     auto qk_advance = [&]() -> bool {
       while (qk.next())
         if ((qk.g & 1) == static_cast<int>(rank)) return true;
@@ -1015,17 +1036,21 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     bool qk_more = qk_advance();
     bool pv_more = pv.next();
     bool ok = true;
-    uint64_t t_idle = globaltimer_ns();
+    uint64_t t_idle = 0;
     uint32_t polls = 0;
     while (ok && (qk_more || pv_more)) {
       bool did = false;
       if (qk_more) {
-        const int j = qk.g >> 1;
-        const int st = j % kOwnStages;
+        const int j = qk_n;  // own pages in order
+        const int st = j % kKStages;
         const bool opens = qk.seg != qk_seg;
+        // (its V-stage probe comes after the K-stage one: a converted K part means the
+        // page's load was issued, so the V stage's previous phase has completed)
+        const int vst = qk.g % kVStages;
         const bool ready = (!opens || mbar_test_wait(&bars->q_full, qn & 1)) &&
-                           (qk_n == 0 || mbar_test_wait(&bars->s_free, (qk_n - 1) & 1)) &&
-                           mbar_test_wait(&bars->own_cvt[st], (j / kOwnStages) & 1);
+                           (j < 2 || mbar_test_wait(&bars->s_free[j & 1], ((j - 2) >> 1) & 1)) &&
+                           mbar_test_wait(&bars->k_cvt[st], (j / kKStages) & 1) &&
+                           mbar_test_wait(&bars->v_full[vst], (qk.g / kVStages) & 1);
         if (__all_sync(0xffffffffu, ready)) {
           if (opens) {
             qk_seg = qk.seg;
@@ -1033,18 +1058,23 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
           }
           ++qk_n;
           tc_fence_after();
-          const uint32_t t_s = tmem + kTS;
-          const uint64_t kd = make_sdesc(smem_u32(smem + kOffOwn + st * kOwnBytes), 16, 1024, SWIZZLE_128B);
+          const uint32_t t_s = tmem + kTS + (j & 1) * kPage;
+          const uint32_t kb = smem_u32(smem + kOffK + st * kKBytes);
+          // latent box q (128 bytes of each key row) is in the V stage for this CTA's half, else in the K stage
+          const uint64_t kd = make_sdesc(kb, 16, 1024, SWIZZLE_128B);
+          const uint64_t vd = make_sdesc(smem_u32(smem + kOffV + vst * kVBytes), 16, 1024, SWIZZLE_128B);
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk)
-            mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4),
-                         idesc8, kk > 0 ? 1u : 0u);
-          const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + (j & 1) * kLatBox), 16, 1024, SWIZZLE_128B);
+          for (int kk = 0; kk < 16; ++kk) {
+            const int q = kk >> 2;
+            const uint64_t bd = ((q >> 1) == static_cast<int>(rank)) ? vd + (((q & 1) * kLatBox + (kk & 3) * 32) >> 4)
+                                                                     : kd + (((q & 1) * kLatBox + (kk & 3) * 32) >> 4);
+            mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, bd, idesc8, kk > 0 ? 1u : 0u);
+          }
+          const uint64_t rd = make_sdesc(kb + kKRope, 16, 1024, SWIZZLE_128B);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f16_ts_if(leader, t_s, tmem + kTQR + kk * 8, rd + ((kk * 32) >> 4), idesc16, 1u);
-          tc_commit_if(leader, &bars->s_full);
-          tc_commit_if(leader, &bars->cvt_free[j & 1]);
+          for (int kk = 0; kk < 4; ++kk) mma_f16_ss_if(leader, t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
+          tc_commit_if(leader, &bars->s_full[j & 1]);
+          tc_commit_if(leader, &bars->k_empty[st]);
           qk_more = qk_advance();
           did = true;
         }
@@ -1053,30 +1083,35 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         const int g = pv.g;
         const bool mine = (g & 1) == static_cast<int>(rank);
         const int idx = g >> 1;
-        const bool tail = !mine && pv.pg == pv.sg.n - 1 && (pv.sg.s_k % kPage) != 0;
-        const int st = mine ? idx % kOwnStages : idx % kPeerStages;
-        // P(g) written here (own page) or O ready for it here (the other CTA's page;
-        // its P message arrived before that); the other CTA's page: its V half
-        bool ready = mbar_test_wait(&bars->p_full[g & 3], (g >> 2) & 1);
-        if (ready && !mine)
-          ready = tail ? mbar_test_wait(&bars->peer_tail[tail_n & 3], (tail_n >> 2) & 1)
-                       : mbar_test_wait(&bars->peer_full[st], (idx / kPeerStages) & 1);
+        const int st = g % kVStages;
+        // P(g) written here (own page) or O ready for it here (the other CTA's
+        // page; its P message arrived before that), and the V half loaded
+        const bool ready = mbar_test_wait(&bars->p_full[g & 3], (g >> 2) & 1) &&
+                           mbar_test_wait(&bars->v_full[st], (g / kVStages) & 1);
         if (__all_sync(0xffffffffu, ready)) {
-          if (tail) ++tail_n;
-          const uint32_t v_base = mine ? smem_u32(smem + kOffOwn + st * kOwnBytes) + rank * 2 * kLatBox
-                                       : smem_u32(smem + kOffPeer + st * kPeerBytes);
-          uint64_t* empty = mine ? &bars->own_empty[st] : &bars->peer_empty[st];
+          uint8_t* vs = smem + kOffV + st * kVBytes;
+          const int live = pv.sg.s_k - pv.pg * kPage;  // rows of the page that hold keys
+          if (pv.pg == pv.sg.n - 1 && live < kPage) {  // zero the rows past the sequence end
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int i = lane; i < (kPage - live) * 16; i += 32) {
+              const int row = live + i / 16, c = i % 16;
+              *reinterpret_cast<uint4*>(vs + (c >> 3) * kLatBox + row * 128 + ((c & 7) << 4)) = z;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
           tc_fence_after();
           const uint64_t pd = make_sdesc(smem_u32(smem + kOffP + (g & 3) * kPTile), kPLbo, kPSbo, SWIZZLE_NONE);
-          const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
+          const uint64_t vd = make_sdesc(smem_u32(vs), kLatBox, 1024, SWIZZLE_128B);
           const bool first = pv.first();
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk)
             mma_f8_ss_if(leader, tmem + kTO, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
                          (first && kk == 0) ? 0u : 1u);
           tc_commit_if(leader, &bars->pv_done[g & 3]);
-          tc_commit_if(leader, empty);
-          if (!mine) tc_commit_mc_if(leader, &bars->pv_peer[idx & 1], other_mask);  // the owner may reuse its P tile
+          tc_commit_if(leader, &bars->v_empty[st]);
+          // the other CTA's page: its owner may reuse the tile once both P.Vs completed
+          if (!mine) tc_commit_mc_if(leader, &bars->pv_done[g & 3], other_mask);
           pv_more = pv.next();
           did = true;
         }
@@ -1102,73 +1137,53 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     __syncwarp();
     warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
   } else if (warp == 2 || warp == 3) {
-    // ------------------- RoPE conversion, tail zeroing (64 threads) ----
-    // Own pages: the RoPE part to f16 (exact) in buffer j % 2, free once the
-    // Q.K^T of own page j - 2 completed (cvt_free); dead rows (past the sequence end) of
-    // this CTA's V half zeroed.  The other CTA's pages: only a sequence's last
-    // page with dead rows, which are zeroed (peer_tail); the MMA warp waits for
-    // the load of the others itself.
+    // ---------------------- RoPE conversion of own pages (64 threads) ----
+    // Thread t reads the E4M3 RoPE bytes of token row t from the second half
+    // of the stage's RoPE region, and after all have read, writes them as f16
+    // (exact) over the whole region, 128-byte swizzled; rows past the sequence
+    // end become 0 (their scores are masked anyway).
     const int t = threadIdx.x - 64;  // token row of the page
     PageCursor pc(prm, unit);
     bool ok = true;
-    int tails = 0;  // the other CTA's sequence-tail pages done
+    int j = 0;
     while (ok && pc.next()) {
-      const int g = pc.g, idx = g >> 1;
-      const bool mine = (g & 1) == static_cast<int>(rank);
-      const int st = mine ? idx % kOwnStages : idx % kPeerStages;
-      const int use = mine ? idx / kOwnStages : idx / kPeerStages;
-      // every load is waited for in turn (so no wait here can pass on a phase
-      // two ahead), but the other CTA's pages need work only at a sequence tail
-      const bool work = mine || (pc.pg == pc.sg.n - 1 && (pc.sg.s_k % kPage) != 0);
-      if (t == 0) {
-        bool w = wait_bounded(mine ? &bars->own_full[st] : &bars->peer_full[st], use & 1, abort_flag, &g_status_mla, __LINE__);
-        if (w && mine && idx >= 2)
-          w = wait_bounded(&bars->cvt_free[idx & 1], ((idx - 2) >> 1) & 1, abort_flag, &g_status_mla, __LINE__);
-        bars->cvt_ok = w ? 1u : 0u;
-      }
+      if ((pc.g & 1) != static_cast<int>(rank)) continue;
+      const int st = j % kKStages, use = j / kKStages;
+      ++j;
+      if (t == 0)
+        bars->cvt_ok = wait_bounded(&bars->k_full[st], use & 1, abort_flag, &g_status_mla, __LINE__) ? 1u : 0u;
       named_bar_sync(1, 64);
       if (!bars->cvt_ok) {
         ok = false;
         break;
       }
-      if (!work) continue;
+      uint8_t* kb = smem + kOffK + st * kKBytes;
       const bool dead = (pc.pg == pc.sg.n - 1) && (t >= pc.sg.s_k - pc.pg * kPage);  // slot past the end
       const uint4 z = make_uint4(0, 0, 0, 0);
-      uint8_t* vhalf = mine ? smem + kOffOwn + st * kOwnBytes + rank * 2 * kLatBox : smem + kOffPeer + st * kPeerBytes;
-      if (mine) {
-        const int sw = t & 7;
-        const uint4* src = reinterpret_cast<const uint4*>(smem + kOffOwn + st * kOwnBytes + 4 * kLatBox + t * 64);
-        uint8_t* dst = smem + kOffCvt + (idx & 1) * kLatBox + t * 128;
+      uint4 raw[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint4 lo = z, hi = z;
-          if (!dead) {
-            const uint4 v = src[c];
-            lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
-            lo.y = e4m3x2_to_f16x2(v.x >> 16);
-            lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
-            lo.w = e4m3x2_to_f16x2(v.y >> 16);
-            hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
-            hi.y = e4m3x2_to_f16x2(v.z >> 16);
-            hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
-            hi.w = e4m3x2_to_f16x2(v.w >> 16);
-          }
-          *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
-          *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
-        }
-      }
-      if (dead) {  // zero the slot's row in this CTA's two V boxes
+      for (int c = 0; c < 4; ++c) raw[c] = dead ? z : reinterpret_cast<const uint4*>(kb + kKRopeRaw + t * 64)[c];
+      named_bar_sync(1, 64);  // every raw row is read before the f16 rows overwrite them
+      const int sw = t & 7;
+      uint8_t* dst = kb + kKRope + t * 128;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint4* row = reinterpret_cast<uint4*>(vhalf + j * kLatBox + t * 128);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) row[c] = z;
-        }
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = raw[c];
+        uint4 lo, hi;
+        lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
+        lo.y = e4m3x2_to_f16x2(v.x >> 16);
+        lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
+        lo.w = e4m3x2_to_f16x2(v.y >> 16);
+        hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
+        hi.y = e4m3x2_to_f16x2(v.z >> 16);
+        hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
+        hi.w = e4m3x2_to_f16x2(v.w >> 16);
+        *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
+        *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 64);
-      if (t == 0) mbar_arrive(mine ? &bars->own_cvt[st] : &bars->peer_tail[tails & 3]);
-      if (!mine) ++tails;
+      if (t == 0) mbar_arrive(&bars->k_cvt[st]);
     }
     if (!ok && t == 0) fail();
   } else {
@@ -1213,7 +1228,7 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
 
     // Copies this half of sequence b_seq's quantised Q row (prepared by
     // mla_qprep_kernel) in: latent bytes [256 hf, +256) into TMEM columns
-    // kTQ + 64 hf.., RoPE values [32 hf, +32) into columns kTQR + 16 hf..
+    // kTQ + 64 hf.., RoPE values [32 hf, +32) into the Q RoPE tile.
     int qn = 0;
     float qs_cur = 1.f;
     auto copy_q = [&](int b_seq) -> bool {
@@ -1238,17 +1253,10 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         }
         tmem_st16(lane_base + kTQ + (4 * hf + ch) * 16, pk);
       }
-      {
-        uint32_t pk[16];
+      uint8_t* dst = smem + kOffQRope + r * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          pk[4 * c + 0] = w[c].x;
-          pk[4 * c + 1] = w[c].y;
-          pk[4 * c + 2] = w[c].z;
-          pk[4 * c + 3] = w[c].w;
-        }
-        tmem_st16(lane_base + kTQR + 16 * hf, pk);
-      }
+      for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(dst + (((4 * hf + c) ^ (r & 7)) << 4)) = w[c];
+      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bars->q_full);
@@ -1314,13 +1322,14 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     auto finish_other = [&](int g, bool first) -> bool {
       const int k = g >> 1;
       if (!warp_spin(&bars->p_rx[k & 1], (k >> 1) & 1, abort_flag, __LINE__)) return false;
+      fence_proxy_async_smem();  // the remotely stored P is read by this CTA's P.V
       // (every softmax thread has passed this phase before the message's next
       // bytes can come: they follow this page's P.V here)
       if (warp == 4 && lane == 0) mbar_arrive_expect_tx(&bars->p_rx[k & 1], kPTile);
       const float m_new = reinterpret_cast<const float*>(smem + kOffP + (g & 3) * kPTile + kPBytes)[r];
       m_other = m_new;
-      // this CTA's arrivals for page g come after page g - 4's phase of the tile completed
-      if (g >= 4 && !warp_spin(&bars->pv_done[g & 3], ((g - 4) >> 2) & 1, abort_flag, __LINE__)) return false;
+      // (this CTA's arrival for page g comes after page g - 4's phase of the tile
+      // completed: the message's sender waited for this CTA's P.V of page g - 4)
       if (!rescale_to(g, m_new, first)) return false;
       tc_fence_before();
       __syncwarp();
@@ -1369,18 +1378,18 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       } else {
         const int j = g >> 1;
         c_row = prm.softmax_scale * kLog2e * qs_cur * kv_scale;
-        if (!warp_spin(&bars->s_full, j & 1, abort_flag, __LINE__)) {
+        if (!warp_spin(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag, __LINE__)) {
           ok = false;
           break;
         }
         tc_fence_after();
         // both halves of the row: the other half only for the row max
         uint32_t s[32], so[32];
-        tmem_ld32(lane_base + kTS + 32 * hf, s);
-        tmem_ld32(lane_base + kTS + 32 * (1 - hf), so);
+        tmem_ld32(lane_base + kTS + (j & 1) * kPage + 32 * hf, s);
+        tmem_ld32(lane_base + kTS + (j & 1) * kPage + 32 * (1 - hf), so);
         tmem_ld_wait();
         tc_fence_before();
-        warp_arrive(&bars->s_free);  // the next own page's Q.K^T may overwrite S
+        warp_arrive(&bars->s_free[j & 1]);  // own page j + 2's Q.K^T may overwrite this S buffer
         if (pc.pg * kPage + kPage > min_visible) {
           const int base = pc.pg * kPage + 32 * hf, base_o = pc.pg * kPage + 32 * (1 - hf);
 #pragma unroll
@@ -1405,8 +1414,7 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         const float mx =
             fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
         // P tile g % 4 is free once both CTAs' P.V of page g - 4 completed
-        if (g >= 4 && (!warp_spin(&bars->pv_done[g & 3], ((g - 4) >> 2) & 1, abort_flag, __LINE__) ||
-                       !warp_spin(&bars->pv_peer[j & 1], ((j - 2) >> 1) & 1, abort_flag, __LINE__))) {
+        if (g >= 4 && !warp_spin(&bars->pv_done[g & 3], ((g - 4) >> 2) & 1, abort_flag, __LINE__)) {
           ok = false;
           break;
         }
@@ -1428,31 +1436,23 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
           sum += (p0 + p1) + (p2 + p3);
           pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
         }
-        {  // this thread's 32 keys of row r (16-byte chunks 2 hf, 2 hf + 1), and the row's reference
-          uint8_t* tile = smem + kOffP + (g & 3) * kPTile;
-          uint8_t* lp = tile + prow;
-          *reinterpret_cast<uint4*>(lp + (2 * hf) * kPLbo) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(lp + (2 * hf + 1) * kPLbo) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          if (hf == 0) reinterpret_cast<float*>(tile + kPBytes)[r] = m_new;
+        {  // this thread's 32 keys of row r (16-byte chunks 2 hf, 2 hf + 1), and the row's reference,
+           // here and (asynchronously, counted on its p_rx barrier) in the other CTA
+          const uint32_t tile = static_cast<uint32_t>((g & 3) * kPTile);
+          const uint4 a = make_uint4(pk[0], pk[1], pk[2], pk[3]), b2 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          uint8_t* lp = smem + kOffP + tile + prow;
+          *reinterpret_cast<uint4*>(lp + (2 * hf) * kPLbo) = a;
+          *reinterpret_cast<uint4*>(lp + (2 * hf + 1) * kPLbo) = b2;
+          const uint32_t rbar = r_prx0 + (j & 1) * 8;
+          st_async_v4(r_p0 + tile + prow + (2 * hf) * kPLbo, a, rbar);
+          st_async_v4(r_p0 + tile + prow + (2 * hf + 1) * kPLbo, b2, rbar);
+          if (hf == 0) {
+            reinterpret_cast<float*>(smem + kOffP + tile + kPBytes)[r] = m_new;
+            st_async_f32(r_p0 + tile + kPBytes + r * 4, m_new, rbar);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          // the warp's two 512-byte pieces of P (and the hf 0 warps' 32 row
-          // references) to the other CTA's message, by the async proxy,
-          // counted on its p_rx barrier of that message
-          const uint32_t tile = static_cast<uint32_t>((g & 3) * kPTile);
-          const uint32_t piece = tile + (warp % 4) * 4 * kPSbo;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint32_t off = piece + (2 * hf + c) * kPLbo;
-            bulk_copy_to_cluster(r_p0 + off, smem + kOffP + off, 32 * 16, r_prx0 + (j & 1) * 8);
-          }
-          if (hf == 0) {
-            const uint32_t off = tile + kPBytes + (warp % 4) * 128;
-            bulk_copy_to_cluster(r_p0 + off, smem + kOffP + off, 128, r_prx0 + (j & 1) * 8);
-          }
-        }
         // the other CTA's previous page: O moves to its reference and is declared
         // ready for its P.V before this page's rescale
         if (pend >= 0) {
@@ -1549,17 +1549,15 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       }
     }
     if (!ok) fail();
-    // The other CTA's last P.V of this CTA's pages: its arrival must land
-    // before this CTA may exit.
-    // (Each pv_peer phase j is waited for before own page j + 1's P; the last
-    // own page's phase is waited for here.)
+    // The other CTA's P.V commits of this CTA's last pages arrive in this
+    // CTA's shared memory: they must land before this CTA may exit.
     if (ok) {
-      int nown = 0;
+      int last0 = -1, last1 = -1;  // last own page on each of this CTA's two tiles
       PageCursor cnt(prm, unit);
       while (cnt.next())
-        if ((cnt.g & 1) == static_cast<int>(rank)) ++nown;
-      if (nown > 0) warp_spin(&bars->pv_peer[(nown - 1) & 1], ((nown - 1) >> 1) & 1, abort_flag, __LINE__);
-      if (nown > 1) warp_spin(&bars->pv_peer[nown & 1], ((nown - 2) >> 1) & 1, abort_flag, __LINE__);
+        if ((cnt.g & 1) == static_cast<int>(rank)) ((cnt.g >> 1) & 1 ? last1 : last0) = cnt.g;
+      if (last0 >= 0) warp_spin(&bars->pv_done[last0 & 3], (last0 >> 2) & 1, abort_flag, __LINE__);
+      if (last1 >= 0) warp_spin(&bars->pv_done[last1 & 3], (last1 >> 2) & 1, abort_flag, __LINE__);
     }
   }
 

@@ -202,6 +202,22 @@ __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, const void* s
                : "memory");
 }
 
+// Asynchronous remote stores into shared memory of a CTA of the cluster
+// (cluster addresses): each completes its byte count on the mbarrier at
+// cluster address `bar` (in the destination CTA) when it lands; the storing
+// thread does not wait for them.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, uint4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t dst, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
+               "r"(__float_as_uint(v)), "r"(bar)
+               : "memory");
+}
+
 // -------------------------------------------------- dependent launches ----
 
 // Block until every grid this one depends on (programmatic dependent launch)
