@@ -729,91 +729,93 @@ __device__ __forceinline__ void lane_group_transpose(uint4 (&pc)[N], int lane) {
 // ===========================================================================
 // FP8-dots kernel: one work unit = a cluster of two CTAs.
 //
-// CTA `rank` (0 or 1) owns dv columns [256 rank, 256 rank + 256) of O, and
-// the unit's pages alternate between the two CTAs: page g of the unit's page
-// stream (counted across its segments) belongs to CTA g % 2.  The owner of a
-// page computes its scores S = Q K^T and its probabilities P; the other CTA
-// only multiplies P by its own dv half of the page's V.  P (128 rows x 64
-// keys, E4M3) and the running row maximum that P was computed against travel
-// to the other CTA through distributed shared memory, so each page's Q.K^T
-// and softmax run once per unit (the pair no longer repeats them).
+// CTA `rank` (0 or 1) owns dv columns [256 rank, 256 rank + 256) of O.  The
+// unit's pages are taken two at a time: block h of the unit's block stream
+// (pages 2i and 2i + 1 of a segment, or its last page alone; counted across
+// the unit's segments) belongs to CTA h % 2.  The owner computes the block's
+// scores S = Q K^T as one 128-row x 128-key tile and its probabilities P; the
+// other CTA only multiplies P by its dv half of the block's V.  (A tcgen05
+// MMA with M = 128 costs nearly the same for any N up to 256, so 128-key
+// score tiles take half the tensor time per key of 64-key ones.)  P (128 rows
+// x 128 keys, E4M3) and the reference it was taken against travel to the
+// other CTA through distributed shared memory.
 //
-// Page g's P is taken against a reference m_g (log2 units) that the owner
-// decides from what it already has: m_g = max(m_{g-2}, m_{g-3}) (its own
-// previous page's reference and the other CTA's reference of page g - 3,
-// within the segment), raised to page g's row maximum when that exceeds it by
-// more than kTau.  m_g travels with P; both CTAs rescale their O halves and
-// row sums to m_g before page g's P.V, so both apply the same factors in the
-// same order (a factor may be above 1 for a page after the other CTA raised
-// its reference), every stored P is at most 64 * 2^kTau < 448, and no page
-// waits for the other CTA's decision on the page just before it.
+// Block h's P is taken against a reference m_h (log2 units) that the owner
+// decides from what it already has: m_h = max(m_{h-2}, m_{h-3}) (its own
+// previous block's reference and the other CTA's reference of block h - 3,
+// within the segment), raised to block h's row maximum when that exceeds it by
+// more than kTau.  m_h travels with P; both CTAs rescale their O halves and
+// row sums to m_h before block h's P.V, so both apply the same factors in the
+// same order (a factor may be above 1 for a block after the other CTA raised
+// its reference), every stored P is at most 64 * 2^kTau < 448, and no block
+// waits for the other CTA's decision on the block just before it.
 //
-// Per CTA: TMEM holds its O half (256 columns), two S buffers (64 each; its
-// own pages alternate, so one page's Q.K^T runs while the softmax works on
-// the previous one) and the latent Q (128, E4M3).  Shared memory holds a V
-// ring with this CTA's dv half of the latent bytes of every page (6 x 16 KB,
-// released by the page's P.V), a K ring with the rest of this CTA's own pages
-// (3 x 24 KB: the other latent half and the RoPE part, converted to f16 in
-// place; released when the page's Q.K^T completes -- Q.K^T reads the page's
-// latent bytes from both rings), Q's RoPE part (f16, 16 KB) and four P
-// messages: page g's P and its 128 row references go to message g % 4 in
+// Per CTA: TMEM holds its O half (256 columns), S (128) and the latent Q
+// (128, E4M3).  Shared memory holds a V ring with this CTA's dv half of the
+// latent bytes of every block (3 x 32 KB, released by the block's P.V), a
+// ring of 16 KB K slices for its own blocks (per block: the other latent
+// half's two 128-byte boxes, then the RoPE part, converted to f16 in place;
+// each released when its Q.K^T step completes -- Q.K^T reads this CTA's
+// latent half from the V ring), Q's RoPE part (f16, 16 KB) and two P
+// messages: block h's P and its 128 row references go to message h % 2 in
 // both CTAs (to the other CTA by asynchronous remote stores that count their
 // bytes on its p_rx barrier; the sender does not wait for them), and a
-// message is rewritten four pages later, after both CTAs' P.V of the page
+// message is rewritten two blocks later, after both CTAs' P.V of the block
 // before read it.
 // ===========================================================================
 namespace pr {
-constexpr int kKStages = 3;   // own pages: the other latent half and the RoPE part, for Q.K^T
-constexpr int kVStages = 6;   // this CTA's latent half of every page, for P.V (and own pages' Q.K^T)
 constexpr int kThreads = 384;
-// a K stage: the other CTA's two 128-byte latent boxes, then the RoPE part as
-// f16 (64 keys x 128 B, 128-byte swizzle), converted in place from the E4M3
-// RoPE box that the load puts in the second half of that region
-constexpr int kKRope = 2 * kLatBox;
-constexpr int kKRopeRaw = kKRope + kPage * 64;
-constexpr int kKBytes = kKRope + kLatBox;
-constexpr uint32_t kKTx = 2 * kLatBox + kPage * 64;   // bytes the K part of an own page's load delivers
-constexpr int kVBytes = 2 * kLatBox;                  // latent bytes [256 rank, 256 rank + 256) of a page
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKStages * kKBytes;
-constexpr int kOffQRope = kOffV + kVStages * kVBytes;  // Q RoPE, 128 rows x 64 f16, 128-byte swizzle
-constexpr int kOffP = kOffQRope + kRows * 128;         // four P messages
-constexpr int kPBytes = kRows * kPage;                 // P: 128 rows x 64 E4M3 keys
-constexpr int kPTile = kPBytes + kRows * 4;            // then the 128 row references (float)
-constexpr int kPTiles = 4;
+constexpr int kBlkPages = 2;
+constexpr int kBlkKeys = kBlkPages * kPage;   // keys of a full block (N of its Q.K^T)
+constexpr int kVStages = 3;                   // this CTA's latent half of every block, for P.V (and own Q.K^T)
+constexpr int kKSlices = 4;                   // own blocks' other latent half and RoPE part, three slices a block
+constexpr int kBoxBlk = kBlkPages * kLatBox;  // one 128-byte column box of a block: page 0 rows, then page 1 rows
+constexpr int kVBytes = 2 * kBoxBlk;          // latent bytes [256 rank, 256 rank + 256) of a block
+constexpr int kSliceBytes = kBoxBlk;
+constexpr int kRopeRaw = kPage * 64;          // in a page's 8 KB of a RoPE slice: where its E4M3 bytes land
+constexpr int kOffV = 0;
+constexpr int kOffK = kOffV + kVStages * kVBytes;
+constexpr int kOffQRope = kOffK + kKSlices * kSliceBytes;  // Q RoPE, 128 rows x 64 f16, 128-byte swizzle
+constexpr int kOffP = kOffQRope + kRows * 128;             // two P messages
+constexpr int kPBytes = kRows * kBlkKeys;                  // P: 128 rows x 128 E4M3 keys
+constexpr int kPTile = kPBytes + kRows * 4;                // then the 128 row references (float)
 static_assert(kPTile % 128 == 0, "16-byte aligned P tiles and reference pieces");
-constexpr int kSmemData = kOffP + kPTiles * kPTile;
+constexpr int kOffPtab = kOffP + 2 * kPTile;  // the unit's first kPtabMax block-table entries
+constexpr int kPtabMax = 2048;
+constexpr int kSmemData = kOffPtab + kPtabMax * 4;
 // P: 8-row x 16-byte core matrices, key chunk c of row group G at c * kPLbo + G * kPSbo, so the 32
 // rows x 16 bytes that one warp writes per key chunk are one contiguous 512-byte piece
 constexpr int kPLbo = 2048, kPSbo = 128;
 constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
 constexpr float kTau = 2.75f;                    // 64 * 2^2.75 = 430.5 < 448
-// TMEM columns: O half, two S buffers, Q latent (E4M3, the A operand of the latent Q.K^T)
+// TMEM columns: O half, S, Q latent (E4M3, the A operand of the latent Q.K^T)
 constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
-static_assert(kKBytes % 1024 == 0 && kOffV % 1024 == 0 && kVBytes % 1024 == 0 && kOffP % 1024 == 0 &&
-                  kKRope % 1024 == 0 && kOffQRope % 1024 == 0,
+static_assert(kVBytes % 1024 == 0 && kOffK % 1024 == 0 && kSliceBytes % 1024 == 0 && kOffQRope % 1024 == 0 &&
+                  kOffP % 1024 == 0,
               "1 KB aligned tiles");
 
 struct Bars {
-  uint64_t k_full[kKStages];        // own page's other latent half and RoPE part loaded
-  uint64_t k_cvt[kKStages];         // its RoPE part converted to f16
-  uint64_t k_empty[kKStages];       // its Q.K^T completed: the stage may be refilled
-  uint64_t v_full[kVStages];        // by page g % kVStages: this CTA's latent half of page g loaded
-  uint64_t v_empty[kVStages];       // its P.V (and for an own page its Q.K^T) completed
-  uint64_t s_full[2];               // by own-page parity: S buffer holds the page's scores
-  uint64_t s_free[2];               // S buffer read out (8 softmax warps)
-  uint64_t p_full[kPTiles];         // by tile: P written here (own page) / O ready here (other's page)
-  uint64_t p_rx[2];                 // by tile (g / 2 % 2): the other CTA's P message copied in
-                                    // (transaction bytes; re-armed by a softmax thread)
-  uint64_t pv_done[kPTiles];        // by tile: the P.V of the page completed here -- and, for the tiles of
-                                    // this CTA's pages (g % 2 = rank), in the other CTA too (2 arrivals)
-  uint64_t lx_full[2];              // by segment parity: the other CTA's row sums arrived (4 warps)
-  uint64_t q_full;                  // a segment's Q copied in (8 softmax warps)
+  uint64_t v_full[kVStages];   // by block h % kVStages: this CTA's latent half of block h loaded
+  uint64_t v_empty[kVStages];  // its P.V (and for an own block its Q.K^T) completed
+  uint64_t k_full[kKSlices];   // by slice n % kKSlices (slices 3j, 3j + 1, 3j + 2 of own block j) loaded
+  uint64_t k_empty[kKSlices];  // the slice's Q.K^T step completed
+  uint64_t k_cvt[2];           // by own block j % 2: its RoPE slice converted to f16
+  uint64_t s_full;             // S holds own block j's scores
+  uint64_t s_free;             // S read out (8 softmax warps)
+  uint64_t p_full[2];          // by tile h % 2: P written here (own block) / O ready here (other's block)
+  uint64_t p_rx;               // the other CTA's P message copied in (transaction bytes; re-armed by a softmax thread)
+  uint64_t pv_done[2];         // by tile: the block's P.V completed here
+  uint64_t px_done;            // this CTA's block's P.V completed in the other CTA (its commit, multicast here)
+  uint64_t rmax_full[4];       // by row group: both halves' row maxima written (2 warps)
+  uint64_t lx_full[2];         // by segment parity: the other CTA's row sums arrived (4 warps)
+  uint64_t q_full;             // a segment's Q copied in (8 softmax warps)
+  uint64_t ptab_ready;         // the block-table entries are in shared memory
   uint64_t final_mma, xchg;
   uint32_t tmem_base, abort_flag, cvt_ok;
   // written by 16-byte stores (the other CTA's lane 0 sends 32 rows at a time)
-  alignas(16) float lx[2][kRows];   // the other CTA's row sums, by segment parity
-  float xsum[2][2][kRows];          // by segment parity: row-sum halves of the two softmax threads of a row
+  alignas(16) float lx[2][kRows];  // the other CTA's row sums, by segment parity
+  float xsum[2][2][kRows];         // by segment parity: row-sum halves of the two softmax threads of a row
+  float rmax[2][2][kRows];         // by own block parity: the row maxima of the two halves of a row
 };
 static_assert(offsetof(Bars, lx) % 16 == 0, "16-byte rows of sums");
 static_assert(kSmemData % 16 == 0, "the barrier block starts 16-byte aligned");
@@ -821,35 +823,37 @@ static_assert(kSmemData % 16 == 0, "the barrier block starts 16-byte aligned");
 constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
 static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
 
-// Pages of a unit one at a time: g counts the unit's pages across segments,
-// seg its non-empty segments.
-struct PageCursor {
+// Blocks of a unit one at a time: h counts the unit's blocks across
+// segments, seg its non-empty segments; the block is pages [pg, pg + npg),
+// and u0 + (pg - sg.lo) is the unit's page count before it.
+struct BlockCursor {
   SegmentWalker walk;
   Segment sg;
-  int pg = 0, g = -1, seg = -1;
+  int pg = 0, npg = 0, h = -1, seg = -1, u0 = 0;
   bool valid = false;
-  __device__ PageCursor(const MlaParams& p, int unit) : walk(p, unit) {}
+  __device__ BlockCursor(const MlaParams& p, int unit) : walk(p, unit) {}
   __device__ bool next() {
-    if (valid && pg + 1 < sg.hi) {
-      ++pg;
-      ++g;
-      return true;
+    if (valid && pg + npg < sg.hi) {
+      pg += npg;
+    } else {
+      if (valid) u0 += sg.hi - sg.lo;
+      valid = walk.next(sg);
+      if (!valid) return false;
+      pg = sg.lo;
+      ++seg;
     }
-    valid = walk.next(sg);
-    if (!valid) return false;
-    pg = sg.lo;
-    ++g;
-    ++seg;
+    npg = min(kBlkPages, sg.hi - pg);
+    ++h;
     return true;
   }
   __device__ bool first() const { return pg == sg.lo; }
-  __device__ bool last() const { return pg == sg.hi - 1; }
+  __device__ bool last() const { return pg + npg == sg.hi; }
 };
 
-// Unit-level fault injection for the bounded-wait test: when g_fault_page is
-// p + 1, CTA 0 of unit 0 never issues the loads of its page p, so every wait
-// on them runs out (see fp8mla_test_fault_injection).
-__device__ int g_fault_page = 0;
+// Unit-level fault injection for the bounded-wait test: when g_fault_block is
+// h + 1, CTA 0 of unit 0 never issues the loads of its block h, so every wait
+// on them runs out.
+__device__ int g_fault_block = 0;
 
 }  // namespace pr
 
@@ -868,6 +872,7 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
   const int unit = blockIdx.x / 2;
   const uint32_t rank = cluster_ctarank();
   const uint32_t other = rank ^ 1u;
+  const int irank = static_cast<int>(rank);
   auto remote = [&](const void* p) { return mapa_shared(smem_u32(p), other); };
   // stop this CTA and tell the other one, whose waits then end too
   auto fail = [&]() {
@@ -876,31 +881,32 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
   };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_cvt[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
+    for (int s = 0; s < kKSlices; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], kSoftmaxThreads / 32);
-    }
-    for (int b = 0; b < kPTiles; ++b) {
+      mbar_init(&bars->k_cvt[b], 1);
       mbar_init(&bars->p_full[b], kSoftmaxThreads / 32);
-      mbar_init(&bars->pv_done[b], (b & 1) == static_cast<int>(rank) ? 2 : 1);
+      mbar_init(&bars->pv_done[b], 1);
+      mbar_init(&bars->lx_full[b], kSoftmaxThreads / 64);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&bars->p_rx[b], 1);
-    for (int b = 0; b < 2; ++b) mbar_init(&bars->lx_full[b], kSoftmaxThreads / 64);
+    for (int b = 0; b < 4; ++b) mbar_init(&bars->rmax_full[b], 2);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, kSoftmaxThreads / 32);
+    mbar_init(&bars->p_rx, 1);
+    mbar_init(&bars->px_done, 1);
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
+    mbar_init(&bars->ptab_ready, 1);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->xchg, kSoftmaxThreads / 32);
     bars->abort_flag = 0;
     fence_barrier_init();
-    for (int b = 0; b < 2; ++b) mbar_arrive_expect_tx(&bars->p_rx[b], kPTile);  // the first two messages
+    mbar_arrive_expect_tx(&bars->p_rx, kPTile);  // the first message
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -920,72 +926,95 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
-    // Two streams of loads, issued by lane 0 as their stages free up (own pages
-    // first).  Own page g: its latent half [256 rank, +256) into V stage
-    // g % kVStages, the other half and the RoPE box into the next K stage.  The
-    // other CTA's page g: this CTA's latent half into V stage g % kVStages.
-    // Each stream fetches the block-table entry of its next page right after
-    // issuing a load, so the entry is at hand when the stages free up.
+    // Two streams of loads, issued by lane 0 as their stages free up: the V
+    // half of every block in block order (this CTA's latent bytes
+    // [256 rank, +256) of each page), and the three K slices of each own
+    // block (the other latent half's two boxes, then the RoPE bytes).
     if (lane == 0) {
       tma_prefetch_desc(&tm_lat);
       tma_prefetch_desc(&tm_rope);
-      const int fault = (unit == 0 && rank == 0) ? *(volatile int*)&g_fault_page : 0;
-      auto phys_of = [&](const PageCursor& c) -> int {
-        int ph = __ldg(prm.block_table + static_cast<size_t>(c.sg.b) * prm.max_pages + c.pg);
+      const int fault = (unit == 0 && rank == 0) ? *(volatile int*)&g_fault_block : 0;
+      const int32_t* ptab = reinterpret_cast<const int32_t*>(smem + kOffPtab);
+      bool ptab_ok = false;
+      // a block-table entry: from the shared-memory copy once it is in, else from global memory
+      auto phys_of = [&](const BlockCursor& c, int i) -> int {
+        const int u = c.u0 + (c.pg - c.sg.lo) + i;
+        if (!ptab_ok && u < kPtabMax) ptab_ok = mbar_test_wait(&bars->ptab_ready, 0);
+        int ph = (ptab_ok && u < kPtabMax)
+                     ? ptab[u]
+                     : __ldg(prm.block_table + static_cast<size_t>(c.sg.b) * prm.max_pages + c.pg + i);
         if (ph < 0 || ph >= prm.num_pages) {
           atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
           ph = 0;
         }
         return ph;
       };
-      PageCursor oc(prm, unit), xc(prm, unit);  // own pages; the other CTA's pages
-      auto advance = [&](PageCursor& c, int want) -> bool {
+      auto fetch = [&](const BlockCursor& c, int (&ph)[2]) {
+        ph[0] = phys_of(c, 0);
+        ph[1] = c.npg > 1 ? phys_of(c, 1) : 0;
+      };
+      BlockCursor vc(prm, unit), kc(prm, unit);  // next block to load V for; next own block for K slices
+      auto adv_own = [&](BlockCursor& c) -> bool {
         while (c.next())
-          if ((c.g & 1) == want) return true;
+          if ((c.h & 1) == irank) return true;
         return false;
       };
-      bool o_more = advance(oc, static_cast<int>(rank)), x_more = advance(xc, static_cast<int>(other));
-      int o_phys = o_more ? phys_of(oc) : 0, x_phys = x_more ? phys_of(xc) : 0;
-      int kn = 0;  // own-page loads issued
+      bool v_more = vc.next(), k_more = adv_own(kc);
+      int vp[2] = {0, 0}, kp[2] = {0, 0};
+      if (v_more) fetch(vc, vp);
+      if (k_more) fetch(kc, kp);
+      int kn = 0, ks = 0;  // K slices issued; slice of the current own block (0, 1 latent, 2 RoPE)
       uint32_t v_last = 0, v_par = 0, k_last = 0, k_par = 0;  // per stage: loaded here, and its phase parity
-      auto v_free = [&](int g) { return g < kVStages || mbar_test_wait(&bars->v_empty[g % kVStages], ((g / kVStages) - 1) & 1); };
-      auto load_v = [&](int g, int phys) {
-        const int st = g % kVStages;
-        uint8_t* sb = smem + kOffV + st * kVBytes;
-        mbar_arrive_expect_tx(&bars->v_full[st], kVBytes);
-        tma_load_3d(sb, &tm_lat, &bars->v_full[st], static_cast<int>(rank) * 256, 0, phys);
-        tma_load_3d(sb + kLatBox, &tm_lat, &bars->v_full[st], static_cast<int>(rank) * 256 + 128, 0, phys);
-        v_last |= 1u << st;
-        v_par = (v_par & ~(1u << st)) | (static_cast<uint32_t>((g / kVStages) & 1) << st);
-      };
       uint32_t polls = 0;
       uint64_t t_idle = 0;
       bool ok = true;
-      while (ok && (o_more || x_more)) {
+      while (ok && (v_more || k_more)) {
         bool did = false;
-        if (o_more) {
-          const int st = kn % kKStages, use = kn / kKStages;
-          if ((use == 0 || mbar_test_wait(&bars->k_empty[st], (use - 1) & 1)) && v_free(oc.g)) {
-            if (fault != oc.g + 1) {
-              load_v(oc.g, o_phys);
-              uint8_t* sb = smem + kOffK + st * kKBytes;
-              mbar_arrive_expect_tx(&bars->k_full[st], kKTx);
-              tma_load_3d(sb, &tm_lat, &bars->k_full[st], static_cast<int>(other) * 256, 0, o_phys);
-              tma_load_3d(sb + kLatBox, &tm_lat, &bars->k_full[st], static_cast<int>(other) * 256 + 128, 0, o_phys);
-              tma_load_3d(sb + kKRopeRaw, &tm_rope, &bars->k_full[st], kDLat, 0, o_phys);
+        if (k_more) {
+          const int st = kn % kKSlices, use = kn / kKSlices;
+          if (use == 0 || mbar_test_wait(&bars->k_empty[st], (use - 1) & 1)) {
+            if (fault != kc.h + 1) {
+              uint8_t* sb = smem + kOffK + st * kSliceBytes;
+              mbar_arrive_expect_tx(&bars->k_full[st], static_cast<uint32_t>((ks < 2 ? kLatBox : kRopeRaw) * kc.npg));
+#pragma unroll
+              for (int i = 0; i < kBlkPages; ++i) {  // (compile-time indices keep kp in registers)
+                if (i >= kc.npg) break;
+                if (ks < 2)
+                  tma_load_3d(sb + i * kLatBox, &tm_lat, &bars->k_full[st], static_cast<int>(other) * 256 + ks * 128,
+                              0, kp[i]);
+                else
+                  tma_load_3d(sb + i * kLatBox + kRopeRaw, &tm_rope, &bars->k_full[st], kDLat, 0, kp[i]);
+              }
               k_last |= 1u << st;
               k_par = (k_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
             }
             ++kn;
-            o_more = advance(oc, static_cast<int>(rank));
-            if (o_more) o_phys = phys_of(oc);
+            if (++ks == 3) {
+              ks = 0;
+              k_more = adv_own(kc);
+              if (k_more) fetch(kc, kp);
+            }
             did = true;
           }
         }
-        if (!did && x_more && v_free(xc.g)) {
-          if (fault != xc.g + 1) load_v(xc.g, x_phys);
-          x_more = advance(xc, static_cast<int>(other));
-          if (x_more) x_phys = phys_of(xc);
+        if (v_more && (vc.h < kVStages ||
+                       mbar_test_wait(&bars->v_empty[vc.h % kVStages], ((vc.h / kVStages) - 1) & 1))) {
+          const int st = vc.h % kVStages;
+          if (fault != vc.h + 1) {
+            uint8_t* sb = smem + kOffV + st * kVBytes;
+            mbar_arrive_expect_tx(&bars->v_full[st], static_cast<uint32_t>(2 * kLatBox * vc.npg));
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+              for (int i = 0; i < kBlkPages; ++i)
+                if (i < vc.npg)
+                  tma_load_3d(sb + q * kBoxBlk + i * kLatBox, &tm_lat, &bars->v_full[st], irank * 256 + q * 128, 0,
+                              vp[i]);
+            v_last |= 1u << st;
+            v_par = (v_par & ~(1u << st)) | (static_cast<uint32_t>((vc.h / kVStages) & 1) << st);
+          }
+          v_more = vc.next();
+          if (v_more) fetch(vc, vp);
           did = true;
         }
         if (did) {
@@ -1002,7 +1031,7 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       }
       if (!ok) fail();
       // Never leave with copies in flight: wait for the last load of each stage.
-      for (int st = 0; st < kKStages; ++st)
+      for (int st = 0; st < kKSlices; ++st)
         if ((k_last >> st) & 1u) wait_bounded(&bars->k_full[st], (k_par >> st) & 1u, nullptr, &g_status_mla, __LINE__);
       for (int st = 0; st < kVStages; ++st)
         if ((v_last >> st) & 1u) wait_bounded(&bars->v_full[st], (v_par >> st) & 1u, nullptr, &g_status_mla, __LINE__);
@@ -1011,26 +1040,29 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
     // The whole warp runs the loop and one elected lane issues.  The warp
-    // polls the conditions of the next own page's Q.K^T and of the next
-    // page's P.V and issues whichever is ready (the Q.K^T first), so neither
-    // waits behind the other.  Q.K^T(j) needs S buffer j % 2 read out (own
-    // page j - 2's scores), its page loaded and converted and, when it opens a
-    // segment, that segment's Q; P.V(g) needs P(g) written and O ready, and
-    // the page's V half loaded.  Before the P.V of a sequence's last page the
-    // warp zeroes the V rows past the sequence end (they may hold anything,
-    // and P is 0 there).
-    constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
-    constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
-    constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
+    // polls the next block's P.V and the next step of the next own block's
+    // Q.K^T and issues whichever is ready (P.V first: it frees a V stage and
+    // the other CTA's message), so neither waits behind the other.  Q.K^T(j)
+    // runs in four steps: the other latent half's first box (its K slice)
+    // once S is read out and, when it opens a segment, that segment's Q is
+    // in; its second box; the converted RoPE slice; and last this CTA's
+    // latent half from the V stage (probed only after the P.V of the stage's
+    // previous block was issued, so the probe cannot see that block's phase),
+    // which the block's V load gates.
+    // P.V(h) needs P(h) written and O ready, and the block's V half loaded.
+    // Before the P.V of a block holding a sequence's last page the warp zeroes
+    // that page's V rows past the sequence end (they may hold anything, and P
+    // is 0 there).
+    constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128);  // e4m3, B MN-major, N = 256
     const bool leader = elect_one();
     const uint16_t other_mask = static_cast<uint16_t>(1u << other);
     const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
-    PageCursor qk(prm, unit);  // next own page whose Q.K^T is due
-    PageCursor pv(prm, unit);  // next page whose P.V is due
-    int qn = 0, qk_seg = -1, qk_n = 0;  // Q copies consumed, segment of the last Q.K^T, Q.K^Ts issued
+    BlockCursor qk(prm, unit);  // next own block whose Q.K^T is due
+    BlockCursor pv(prm, unit);  // next block whose P.V is due
+    int qn = 0, qk_seg = -1, qj = 0, step = 0;  // Q copies consumed, segment of the last Q.K^T, own blocks done, step
     auto qk_advance = [&]() -> bool {
       while (qk.next())
-        if ((qk.g & 1) == static_cast<int>(rank)) return true;
+        if ((qk.h & 1) == irank) return true;
       return false;
     };
     bool qk_more = qk_advance();
@@ -1040,80 +1072,104 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     uint32_t polls = 0;
     while (ok && (qk_more || pv_more)) {
       bool did = false;
-      if (qk_more) {
-        const int j = qk_n;  // own pages in order
-        const int st = j % kKStages;
-        const bool opens = qk.seg != qk_seg;
-        // (its V-stage probe comes after the K-stage one: a converted K part means the
-        // page's load was issued, so the V stage's previous phase has completed)
-        const int vst = qk.g % kVStages;
-        const bool ready = (!opens || mbar_test_wait(&bars->q_full, qn & 1)) &&
-                           (j < 2 || mbar_test_wait(&bars->s_free[j & 1], ((j - 2) >> 1) & 1)) &&
-                           mbar_test_wait(&bars->k_cvt[st], (j / kKStages) & 1) &&
-                           mbar_test_wait(&bars->v_full[vst], (qk.g / kVStages) & 1);
+      if (pv_more) {
+        const int h = pv.h;
+        const bool mine = (h & 1) == irank;
+        const int st = h % kVStages;
+        // P(h) written here (own block) or O ready for it here (the other CTA's
+        // block; its P message arrived before that), and the V half loaded
+        const bool ready = mbar_test_wait(&bars->p_full[h & 1], (h >> 1) & 1) &&
+                           mbar_test_wait(&bars->v_full[st], (h / kVStages) & 1);
         if (__all_sync(0xffffffffu, ready)) {
-          if (opens) {
-            qk_seg = qk.seg;
-            ++qn;
+          uint8_t* vs = smem + kOffV + st * kVBytes;
+          if (pv.pg + pv.npg == pv.sg.n) {  // the sequence's last page: zero its rows past the end
+            const int lp = pv.npg - 1;
+            const int live = pv.sg.s_k - (pv.pg + lp) * kPage;  // rows of the page that hold keys
+            if (live < kPage) {
+              const uint4 z = make_uint4(0, 0, 0, 0);
+              for (int i = lane; i < (kPage - live) * 16; i += 32) {
+                const int row = live + i / 16, c = i % 16;
+                *reinterpret_cast<uint4*>(vs + (c >> 3) * kBoxBlk + lp * kLatBox + row * 128 + ((c & 7) << 4)) = z;
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
           }
-          ++qk_n;
           tc_fence_after();
-          const uint32_t t_s = tmem + kTS + (j & 1) * kPage;
-          const uint32_t kb = smem_u32(smem + kOffK + st * kKBytes);
-          // latent box q (128 bytes of each key row) is in the V stage for this CTA's half, else in the K stage
-          const uint64_t kd = make_sdesc(kb, 16, 1024, SWIZZLE_128B);
-          const uint64_t vd = make_sdesc(smem_u32(smem + kOffV + vst * kVBytes), 16, 1024, SWIZZLE_128B);
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const int q = kk >> 2;
-            const uint64_t bd = ((q >> 1) == static_cast<int>(rank)) ? vd + (((q & 1) * kLatBox + (kk & 3) * 32) >> 4)
-                                                                     : kd + (((q & 1) * kLatBox + (kk & 3) * 32) >> 4);
-            mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, bd, idesc8, kk > 0 ? 1u : 0u);
-          }
-          const uint64_t rd = make_sdesc(kb + kKRope, 16, 1024, SWIZZLE_128B);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) mma_f16_ss_if(leader, t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
-          tc_commit_if(leader, &bars->s_full[j & 1]);
-          tc_commit_if(leader, &bars->k_empty[st]);
-          qk_more = qk_advance();
+          const uint64_t pd = make_sdesc(smem_u32(smem + kOffP + (h & 1) * kPTile), kPLbo, kPSbo, SWIZZLE_NONE);
+          const uint64_t vd = make_sdesc(smem_u32(vs), kBoxBlk, 1024, SWIZZLE_128B);
+          const bool first = pv.first();
+          for (int kk = 0; kk < 2 * pv.npg; ++kk)
+            mma_f8_ss_if(leader, tmem + kTO, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
+                         (first && kk == 0) ? 0u : 1u);
+          tc_commit_if(leader, &bars->pv_done[h & 1]);
+          tc_commit_if(leader, &bars->v_empty[st]);
+          // the other CTA's block: its owner may reuse the message once this P.V completed
+          if (!mine) tc_commit_mc_if(leader, &bars->px_done, other_mask);
+          pv_more = pv.next();
           did = true;
         }
       }
-      if (!did && pv_more) {
-        const int g = pv.g;
-        const bool mine = (g & 1) == static_cast<int>(rank);
-        const int idx = g >> 1;
-        const int st = g % kVStages;
-        // P(g) written here (own page) or O ready for it here (the other CTA's
-        // page; its P message arrived before that), and the V half loaded
-        const bool ready = mbar_test_wait(&bars->p_full[g & 3], (g >> 2) & 1) &&
-                           mbar_test_wait(&bars->v_full[st], (g / kVStages) & 1);
-        if (__all_sync(0xffffffffu, ready)) {
-          uint8_t* vs = smem + kOffV + st * kVBytes;
-          const int live = pv.sg.s_k - pv.pg * kPage;  // rows of the page that hold keys
-          if (pv.pg == pv.sg.n - 1 && live < kPage) {  // zero the rows past the sequence end
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int i = lane; i < (kPage - live) * 16; i += 32) {
-              const int row = live + i / 16, c = i % 16;
-              *reinterpret_cast<uint4*>(vs + (c >> 3) * kLatBox + row * 128 + ((c & 7) << 4)) = z;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-          tc_fence_after();
-          const uint64_t pd = make_sdesc(smem_u32(smem + kOffP + (g & 3) * kPTile), kPLbo, kPSbo, SWIZZLE_NONE);
-          const uint64_t vd = make_sdesc(smem_u32(vs), kLatBox, 1024, SWIZZLE_128B);
-          const bool first = pv.first();
+      if (!did && qk_more) {
+        const int j = qj;
+        const uint32_t n_keys = static_cast<uint32_t>(kPage * qk.npg);
+        const uint32_t idesc8 = make_idesc(0, 0, 0, 0, n_keys, 128);   // e4m3 x e4m3, both K-major
+        const uint32_t idesc16 = make_idesc(0, 0, 0, 0, n_keys, 128);  // f16 x f16 (E4M3 keys are exact in f16)
+        if (step == 3) {
+          const int vst = qk.h % kVStages;
+          const bool ready = (!pv_more || pv.h > qk.h - kVStages) &&
+                             mbar_test_wait(&bars->v_full[vst], (qk.h / kVStages) & 1);
+          if (__all_sync(0xffffffffu, ready)) {
+            tc_fence_after();
+            const uint64_t vd = make_sdesc(smem_u32(smem + kOffV + vst * kVBytes), 16, 1024, SWIZZLE_128B);
+            // boxes q = 2 rank + i hold Q.K^T bytes [128 q, 128 q + 128) of the keys
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma_f8_ss_if(leader, tmem + kTO, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
-                         (first && kk == 0) ? 0u : 1u);
-          tc_commit_if(leader, &bars->pv_done[g & 3]);
-          tc_commit_if(leader, &bars->v_empty[st]);
-          // the other CTA's page: its owner may reuse the tile once both P.Vs completed
-          if (!mine) tc_commit_mc_if(leader, &bars->pv_done[g & 3], other_mask);
-          pv_more = pv.next();
-          did = true;
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8_ts_if(leader, tmem + kTS, tmem + kTQ + (4 * (2 * irank + i) + kk) * 8,
+                             vd + ((i * kBoxBlk + kk * 32) >> 4), idesc8, 1u);
+            tc_commit_if(leader, &bars->s_full);
+            ++qj;
+            step = 0;
+            qk_more = qk_advance();
+            did = true;
+          }
+        } else {
+          const int n = 3 * j + step;  // steps 0, 1: the other latent boxes; step 2: RoPE
+          const int st = n % kKSlices;
+          const bool opens = step == 0 && qk.seg != qk_seg;
+          bool ready;
+          if (step == 0)
+            ready = (!opens || mbar_test_wait(&bars->q_full, qn & 1)) &&
+                    (j < 1 || mbar_test_wait(&bars->s_free, (j - 1) & 1)) &&
+                    mbar_test_wait(&bars->k_full[st], (n / kKSlices) & 1);
+          else if (step == 1)
+            ready = mbar_test_wait(&bars->k_full[st], (n / kKSlices) & 1);
+          else
+            ready = mbar_test_wait(&bars->k_cvt[j & 1], (j >> 1) & 1);
+          if (__all_sync(0xffffffffu, ready)) {
+            if (opens) {
+              qk_seg = qk.seg;
+              ++qn;
+            }
+            tc_fence_after();
+            const uint64_t kd = make_sdesc(smem_u32(smem + kOffK + st * kSliceBytes), 16, 1024, SWIZZLE_128B);
+            if (step < 2) {
+              const int q = 2 * static_cast<int>(other) + step;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8_ts_if(leader, tmem + kTS, tmem + kTQ + (4 * q + kk) * 8, kd + ((kk * 32) >> 4), idesc8,
+                             (step | kk) ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ss_if(leader, tmem + kTS, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), idesc16, 1u);
+            }
+            tc_commit_if(leader, &bars->k_empty[st]);
+            ++step;
+            did = true;
+          }
         }
       }
       // bounded: no progress for the wait limit (or another role stopped) ends the loop
@@ -1137,58 +1193,89 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     __syncwarp();
     warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
   } else if (warp == 2 || warp == 3) {
-    // ---------------------- RoPE conversion of own pages (64 threads) ----
-    // Thread t reads the E4M3 RoPE bytes of token row t from the second half
-    // of the stage's RoPE region, and after all have read, writes them as f16
-    // (exact) over the whole region, 128-byte swizzled; rows past the sequence
-    // end become 0 (their scores are masked anyway).
-    const int t = threadIdx.x - 64;  // token row of the page
-    PageCursor pc(prm, unit);
+    // ---------------------- RoPE conversion of own blocks (64 threads) ----
+    // Thread 0 waits for every K slice in order (so no wait can see a stage's
+    // phase two ahead).  For a block's RoPE slice, thread t reads the E4M3
+    // RoPE bytes of token row t of each page from the second half of the
+    // page's 8 KB and, after all have read, writes them as f16 (exact) over
+    // the whole 8 KB, 128-byte swizzled; rows past the sequence end become 0
+    // (their scores are masked anyway).
+    const int t = threadIdx.x - 64;  // token row of a page
+    {  // first the unit's block-table entries (as many as fit) into shared memory, for the producer
+      int32_t* ptab = reinterpret_cast<int32_t*>(smem + kOffPtab);
+      SegmentWalker w(prm, unit);
+      Segment sg;
+      int u0 = 0;
+      while (u0 < kPtabMax && w.next(sg)) {
+        const int32_t* row = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
+        const int n = min(sg.hi - sg.lo, kPtabMax - u0);
+        for (int i = t; i < n; i += 64) cp_async4(ptab + u0 + i, row + sg.lo + i);
+        u0 += n;
+      }
+      cp_async_wait_all();
+      named_bar_sync(1, 64);
+      if (t == 0) mbar_arrive(&bars->ptab_ready);
+    }
+    BlockCursor bc(prm, unit);
     bool ok = true;
-    int j = 0;
-    while (ok && pc.next()) {
-      if ((pc.g & 1) != static_cast<int>(rank)) continue;
-      const int st = j % kKStages, use = j / kKStages;
-      ++j;
-      if (t == 0)
-        bars->cvt_ok = wait_bounded(&bars->k_full[st], use & 1, abort_flag, &g_status_mla, __LINE__) ? 1u : 0u;
+    int n = 0;  // K slices waited for
+    while (ok && bc.next()) {
+      if ((bc.h & 1) != irank) continue;
+      const int j = n / 3;
+      const int st = (n + 2) % kKSlices;
+      if (t == 0) {
+        bool good = true;
+        for (int s3 = 0; s3 < 3 && good; ++s3)
+          good = wait_bounded(&bars->k_full[(n + s3) % kKSlices], ((n + s3) / kKSlices) & 1, abort_flag,
+                              &g_status_mla, __LINE__);
+        bars->cvt_ok = good ? 1u : 0u;
+      }
+      n += 3;
       named_bar_sync(1, 64);
       if (!bars->cvt_ok) {
         ok = false;
         break;
       }
-      uint8_t* kb = smem + kOffK + st * kKBytes;
-      const bool dead = (pc.pg == pc.sg.n - 1) && (t >= pc.sg.s_k - pc.pg * kPage);  // slot past the end
+      uint8_t* kb = smem + kOffK + st * kSliceBytes;
       const uint4 z = make_uint4(0, 0, 0, 0);
-      uint4 raw[4];
+      uint4 raw[kBlkPages][4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) raw[c] = dead ? z : reinterpret_cast<const uint4*>(kb + kKRopeRaw + t * 64)[c];
+      for (int i = 0; i < kBlkPages; ++i) {
+        const bool dead = i >= bc.npg || (bc.pg + i == bc.sg.n - 1 && t >= bc.sg.s_k - (bc.pg + i) * kPage);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          raw[i][c] = dead ? z : reinterpret_cast<const uint4*>(kb + i * kLatBox + kRopeRaw + t * 64)[c];
+      }
       named_bar_sync(1, 64);  // every raw row is read before the f16 rows overwrite them
       const int sw = t & 7;
-      uint8_t* dst = kb + kKRope + t * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 v = raw[c];
-        uint4 lo, hi;
-        lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
-        lo.y = e4m3x2_to_f16x2(v.x >> 16);
-        lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
-        lo.w = e4m3x2_to_f16x2(v.y >> 16);
-        hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
-        hi.y = e4m3x2_to_f16x2(v.z >> 16);
-        hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
-        hi.w = e4m3x2_to_f16x2(v.w >> 16);
-        *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
-        *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
+      for (int i = 0; i < kBlkPages; ++i) {
+        if (i >= bc.npg) break;
+        uint8_t* dst = kb + i * kLatBox + t * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = raw[i][c];
+          uint4 lo, hi;
+          lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
+          lo.y = e4m3x2_to_f16x2(v.x >> 16);
+          lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
+          lo.w = e4m3x2_to_f16x2(v.y >> 16);
+          hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
+          hi.y = e4m3x2_to_f16x2(v.z >> 16);
+          hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
+          hi.w = e4m3x2_to_f16x2(v.w >> 16);
+          *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
+        }
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 64);
-      if (t == 0) mbar_arrive(&bars->k_cvt[st]);
+      if (t == 0) mbar_arrive(&bars->k_cvt[j & 1]);
     }
     if (!ok && t == 0) fail();
   } else {
     // ------------------ softmax / Q copy / epilogue (8 warps, 2 per row) ----
-    const int hf = (warp - 4) / 4;         // which half of the row
+    const int hf = (warp - 4) / 4;         // which half of the row (keys [64 hf, 64 hf + 64) of a block)
     const int r = (warp % 4) * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const float kv_scale = *prm.kv_scale;
@@ -1202,9 +1289,9 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       return ok;
     };
     const uint32_t r_lx = remote(&bars->lx[0][r]);
-    const uint32_t r_prx0 = remote(&bars->p_rx[0]);
+    const uint32_t r_prx = remote(&bars->p_rx);
     const uint32_t r_lxfull0 = remote(&bars->lx_full[0]);
-    const uint32_t r_p0 = remote(smem + kOffP);
+    const uint32_t r_pt = remote(smem + kOffP + rank * kPTile);  // this CTA's message in the other CTA
     const uint32_t prow = static_cast<uint32_t>((r >> 3) * kPSbo + (r & 7) * 16);
     // Sends the 32 values v of this warp's rows (rows 32 (warp % 4) .. + 31) to
     // the other CTA at cluster address dst and arrives on its barrier rbar:
@@ -1263,43 +1350,43 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       ++qn;
       return true;
     };
-    // true if some segment after the cursor's holds a page of this CTA; its sequence in *b_out
-    auto next_q_segment = [&](const PageCursor& at, int* b_out) -> bool {
+    // true if some segment after the cursor's holds a block of this CTA; its sequence in *b_out
+    auto next_q_segment = [&](const BlockCursor& at, int* b_out) -> bool {
       SegmentWalker peek = at.walk;
       Segment nx;
-      int g0 = at.g + (at.sg.hi - at.pg);  // unit index of the next segment's first page
+      int h0 = at.h + (at.sg.hi - at.pg + 1) / 2;  // unit index of the next segment's first block
       while (peek.next(nx)) {
-        const int n = nx.hi - nx.lo;
-        if (n >= 2 || (g0 & 1) == static_cast<int>(rank)) {
+        const int nb = (nx.hi - nx.lo + 1) / 2;
+        if (nb >= 2 || (h0 & 1) == irank) {
           *b_out = nx.b;
           return true;
         }
-        g0 += n;
+        h0 += nb;
       }
       return false;
     };
 
-    PageCursor pc(prm, unit);
+    BlockCursor pc(prm, unit);
     bool ok = true;
     int cur_seg = -1;
     float m_run = kNegInf, l_run = 0.f;  // reference of O and l; this CTA's share of l
     float m_own = kNegInf;                // this CTA's latest reference in the segment
-    int pend = -1;  // the other CTA's page whose rescale / O-ready is still due
+    int pend = -1;  // the other CTA's block whose rescale / O-ready is still due
     bool pend_first = false;
-    int qtok = 0, visible = 0, min_visible = 0;
+    int qtok = 0, visible = 0;
     float c_row = 0.f;
 
-    // Moves O and l to a new reference before a page's P.V: both are
-    // multiplied by 2^(m_run - m_new) once the P.V of page g - 1 completed.
-    // A reference of -inf (the row sees no key of the page, so its P is 0)
+    // Moves O and l to a new reference before a block's P.V: both are
+    // multiplied by 2^(m_run - m_new) once the P.V of block h - 1 completed.
+    // A reference of -inf (the row sees no key of the block, so its P is 0)
     // leaves them where they are, in both CTAs alike.
-    auto rescale_to = [&](int g, float m_new, bool first) -> bool {
+    auto rescale_to = [&](int h, float m_new, bool first) -> bool {
       const bool rescale = !first && m_new != m_run && m_new != kNegInf;
       const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.f;
       l_run = first ? 0.f : l_run * alpha;
       if (first || rescale) m_run = m_new;
       if (__any_sync(0xffffffffu, rescale)) {
-        if (!warp_spin(&bars->pv_done[(g - 1) & 3], ((g - 1) >> 2) & 1, abort_flag, __LINE__)) return false;
+        if (!warp_spin(&bars->pv_done[(h - 1) & 1], ((h - 1) >> 1) & 1, abort_flag, __LINE__)) return false;
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < kOHalf / 32; ++ch) {
@@ -1315,53 +1402,52 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       }
       return true;
     };
-    // The other CTA's page g: wait for its P message, take the reference it
-    // carries (kept for this CTA's page g + 3), rescale O and l to it, and
-    // declare O ready for the page's P.V.
-    float m_other = kNegInf;  // the other CTA's latest reference in this segment
-    auto finish_other = [&](int g, bool first) -> bool {
-      const int k = g >> 1;
-      if (!warp_spin(&bars->p_rx[k & 1], (k >> 1) & 1, abort_flag, __LINE__)) return false;
+    // The other CTA's block h: wait for its P message, take the reference it
+    // carries (kept for this CTA's block h + 3), rescale O and l to it, and
+    // declare O ready for the block's P.V.
+    float m_o_last = kNegInf, m_o_prev = kNegInf;  // the other CTA's last two references in this segment
+    int h_o_last = -4;                             // the block of m_o_last
+    auto finish_other = [&](int h, bool first) -> bool {
+      const int k = h >> 1;  // the other CTA's k-th block: message k
+      if (!warp_spin(&bars->p_rx, k & 1, abort_flag, __LINE__)) return false;
       fence_proxy_async_smem();  // the remotely stored P is read by this CTA's P.V
-      // (every softmax thread has passed this phase before the message's next
-      // bytes can come: they follow this page's P.V here)
-      if (warp == 4 && lane == 0) mbar_arrive_expect_tx(&bars->p_rx[k & 1], kPTile);
-      const float m_new = reinterpret_cast<const float*>(smem + kOffP + (g & 3) * kPTile + kPBytes)[r];
-      m_other = m_new;
-      // (this CTA's arrival for page g comes after page g - 4's phase of the tile
-      // completed: the message's sender waited for this CTA's P.V of page g - 4)
-      if (!rescale_to(g, m_new, first)) return false;
+      // (every softmax thread has passed this phase before the next message's
+      // bytes can come: they follow this block's P.V here)
+      if (warp == 4 && lane == 0) mbar_arrive_expect_tx(&bars->p_rx, kPTile);
+      const float m_new = reinterpret_cast<const float*>(smem + kOffP + (h & 1) * kPTile + kPBytes)[r];
+      m_o_prev = m_o_last;
+      m_o_last = m_new;
+      h_o_last = h;
+      if (!rescale_to(h, m_new, first)) return false;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[g & 3]);
+      if (lane == 0) mbar_arrive(&bars->p_full[h & 1]);
       return true;
     };
 
-    // Q of the first segment holding a page of this CTA
+    // Q of the first segment holding a block of this CTA
     {
-      PageCursor probe(prm, unit);
+      BlockCursor probe(prm, unit);
       if (probe.next()) {
         int bq = probe.sg.b;
-        const int n = probe.sg.hi - probe.sg.lo;
-        bool have = n >= 2 || (probe.g & 1) == static_cast<int>(rank);
+        const int nb = (probe.sg.hi - probe.sg.lo + 1) / 2;
+        bool have = nb >= 2 || (probe.h & 1) == irank;
         if (!have) have = next_q_segment(probe, &bq);
-        if (have) {
-          ok = copy_q(bq);
-        }
+        if (have) ok = copy_q(bq);
       }
     }
 
     while (ok && pc.next()) {
-      const int g = pc.g;
+      const int h = pc.h;
       if (pc.seg != cur_seg) {  // a new segment
         cur_seg = pc.seg;
         m_run = kNegInf;
         l_run = 0.f;
         m_own = kNegInf;
-        m_other = kNegInf;
+        m_o_last = m_o_prev = kNegInf;
+        h_o_last = -4;
         qtok = (r < R) ? r / prm.h_q : 0;
         visible = prm.causal ? (pc.sg.s_k - prm.s_q + qtok + 1) : pc.sg.s_k;
-        min_visible = prm.causal ? (pc.sg.s_k - prm.s_q + 1) : pc.sg.s_k;
         if (r < R && pc.first()) {  // warm L2 with the Q of the segment after this one
           int bn;
           if (next_q_segment(pc, &bn)) {
@@ -1371,31 +1457,59 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
           }
         }
       }
-      const bool mine = (g & 1) == static_cast<int>(rank);
+      const bool mine = (h & 1) == irank;
       if (!mine) {
-        pend = g;
+        pend = h;
         pend_first = pc.first();
       } else {
-        const int j = g >> 1;
+        const int j = h >> 1;
         c_row = prm.softmax_scale * kLog2e * qs_cur * kv_scale;
-        if (!warp_spin(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag, __LINE__)) {
-          ok = false;
-          break;
+        // wait for S; the other CTA's block before this one is finished meanwhile
+        // if its message lands first (its P.V need not wait for this block's P)
+        {
+          uint32_t polls = 0;
+          uint64_t t_idle = 0;
+          while (ok) {
+            if (pend >= 0 && __shfl_sync(0xffffffffu, mbar_test_wait(&bars->p_rx, (pend >> 1) & 1) ? 1 : 0, 0)) {
+              ok = finish_other(pend, pend_first);
+              pend = -1;
+              polls = 0;
+              continue;
+            }
+            if (__shfl_sync(0xffffffffu, mbar_test_wait(&bars->s_full, j & 1) ? 1 : 0, 0)) break;
+            if ((++polls & 63u) == 0) {
+              if (*abort_flag) ok = false;
+              if (polls == 64) t_idle = globaltimer_ns();
+              if (ok && polls > kWaitMinPolls && globaltimer_ns() - t_idle > *(volatile uint64_t*)&g_wait_limit_ns) {
+                if (lane == 0) {
+                  atomicOr(&g_status_mla, FP8MLA_DEV_WAIT_TIMEOUT);
+                  record_timeout_site(__LINE__);
+                }
+                ok = false;
+              }
+              ok = __all_sync(0xffffffffu, ok);
+            }
+          }
+          if (!ok || !warp_spin(&bars->s_full, j & 1, abort_flag, __LINE__)) {
+            ok = false;
+            break;
+          }
         }
         tc_fence_after();
-        // both halves of the row: the other half only for the row max
-        uint32_t s[32], so[32];
-        tmem_ld32(lane_base + kTS + (j & 1) * kPage + 32 * hf, s);
-        tmem_ld32(lane_base + kTS + (j & 1) * kPage + 32 * (1 - hf), so);
+        uint32_t s[32], s2[32];  // keys [64 hf, +32) and [64 hf + 32, +32) of the block
+        tmem_ld32(lane_base + kTS + 64 * hf, s);
+        tmem_ld32(lane_base + kTS + 64 * hf + 32, s2);
         tmem_ld_wait();
         tc_fence_before();
-        warp_arrive(&bars->s_free[j & 1]);  // own page j + 2's Q.K^T may overwrite this S buffer
-        if (pc.pg * kPage + kPage > min_visible) {
-          const int base = pc.pg * kPage + 32 * hf, base_o = pc.pg * kPage + 32 * (1 - hf);
+        warp_arrive(&bars->s_free);  // own block j + 1's Q.K^T may overwrite S
+        // keys past the row's causal limit or past the segment's pages
+        const int key0 = pc.pg * kPage + 64 * hf;
+        const int lim = min(visible, (pc.pg + pc.npg) * kPage);
+        if (key0 + 64 > lim) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            if (base + c >= visible) s[c] = __float_as_uint(kNegInf);
-            if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
+            if (key0 + c >= lim) s[c] = __float_as_uint(kNegInf);
+            if (key0 + 32 + c >= lim) s2[c] = __float_as_uint(kNegInf);
           }
         }
         float m22[22];
@@ -1403,30 +1517,41 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
         for (int c = 0; c < 10; ++c) {
           m22[c] = fmax3(__uint_as_float(s[3 * c]), __uint_as_float(s[3 * c + 1]), __uint_as_float(s[3 * c + 2]));
           m22[10 + c] =
-              fmax3(__uint_as_float(so[3 * c]), __uint_as_float(so[3 * c + 1]), __uint_as_float(so[3 * c + 2]));
+              fmax3(__uint_as_float(s2[3 * c]), __uint_as_float(s2[3 * c + 1]), __uint_as_float(s2[3 * c + 2]));
         }
         m22[20] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
-        m22[21] = fmaxf(__uint_as_float(so[30]), __uint_as_float(so[31]));
+        m22[21] = fmaxf(__uint_as_float(s2[30]), __uint_as_float(s2[31]));
         float m8[8];
 #pragma unroll
         for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
         m8[7] = m22[21];
-        const float mx =
+        const float mhalf =
             fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
-        // P tile g % 4 is free once both CTAs' P.V of page g - 4 completed
-        if (g >= 4 && !warp_spin(&bars->pv_done[g & 3], ((g - 4) >> 2) & 1, abort_flag, __LINE__)) {
+        // the row's maximum: this half's, and the other half's from its thread (warp warp +- 4)
+        bars->rmax[j & 1][hf][r] = mhalf;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->rmax_full[warp % 4]);
+        if (!warp_spin(&bars->rmax_full[warp % 4], j & 1, abort_flag, __LINE__)) {
           ok = false;
           break;
         }
-        // the reference: this CTA's and the other's latest ones (pages g - 2 and g - 3),
-        // raised to this page's maximum when that exceeds them by more than kTau
+        const float mx = fmaxf(mhalf, bars->rmax[j & 1][1 - hf][r]);
+        // this CTA's message is free once both CTAs' P.V of its block h - 2 completed
+        if (h >= 2 && !(warp_spin(&bars->pv_done[h & 1], ((h - 2) >> 1) & 1, abort_flag, __LINE__) &&
+                        warp_spin(&bars->px_done, ((h - 2) >> 1) & 1, abort_flag, __LINE__))) {
+          ok = false;
+          break;
+        }
+        // the reference: this CTA's and the other's latest ones (blocks h - 2 and h - 3),
+        // raised to this block's maximum when that exceeds them by more than kTau
         const bool first = pc.first();
+        const float m_other = (h_o_last == h - 1) ? m_o_prev : m_o_last;  // block h - 3's
         const float m_known = fmaxf(m_own, m_other);
         const float m_new = (mx > m_known + kTau) ? mx : m_known;
         m_own = m_new;
         const float bias = (m_new == kNegInf) ? 0.f : (kPLog2 - m_new);
         float sum = 0.f;
-        uint32_t pk[8];
+        uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
@@ -1436,25 +1561,33 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
           sum += (p0 + p1) + (p2 + p3);
           pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
         }
-        {  // this thread's 32 keys of row r (16-byte chunks 2 hf, 2 hf + 1), and the row's reference,
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s2[c]), c_row, bias));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s2[c + 1]), c_row, bias));
+          const float p2 = ex2_approx(fmaf(__uint_as_float(s2[c + 2]), c_row, bias));
+          const float p3 = ex2_approx(fmaf(__uint_as_float(s2[c + 3]), c_row, bias));
+          sum += (p0 + p1) + (p2 + p3);
+          pk[8 + c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+        }
+        {  // this thread's 64 keys of row r (16-byte chunks 4 hf .. 4 hf + 3), and the row's reference,
            // here and (asynchronously, counted on its p_rx barrier) in the other CTA
-          const uint32_t tile = static_cast<uint32_t>((g & 3) * kPTile);
-          const uint4 a = make_uint4(pk[0], pk[1], pk[2], pk[3]), b2 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          uint8_t* lp = smem + kOffP + tile + prow;
-          *reinterpret_cast<uint4*>(lp + (2 * hf) * kPLbo) = a;
-          *reinterpret_cast<uint4*>(lp + (2 * hf + 1) * kPLbo) = b2;
-          const uint32_t rbar = r_prx0 + (j & 1) * 8;
-          st_async_v4(r_p0 + tile + prow + (2 * hf) * kPLbo, a, rbar);
-          st_async_v4(r_p0 + tile + prow + (2 * hf + 1) * kPLbo, b2, rbar);
+          uint8_t* lp = smem + kOffP + rank * kPTile + prow;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            *reinterpret_cast<uint4*>(lp + (4 * hf + q) * kPLbo) = v;
+            st_async_v4(r_pt + prow + (4 * hf + q) * kPLbo, v, r_prx);
+          }
           if (hf == 0) {
-            reinterpret_cast<float*>(smem + kOffP + tile + kPBytes)[r] = m_new;
-            st_async_f32(r_p0 + tile + kPBytes + r * 4, m_new, rbar);
+            reinterpret_cast<float*>(smem + kOffP + rank * kPTile + kPBytes)[r] = m_new;
+            st_async_f32(r_pt + kPBytes + r * 4, m_new, r_prx);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        // the other CTA's previous page: O moves to its reference and is declared
-        // ready for its P.V before this page's rescale
+        // the other CTA's previous block: O moves to its reference and is declared
+        // ready for its P.V before this block's rescale
         if (pend >= 0) {
           if (!finish_other(pend, pend_first)) {
             ok = false;
@@ -1462,21 +1595,19 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
           }
           pend = -1;
         }
-        if (!rescale_to(g, m_new, first)) {
+        if (!rescale_to(h, m_new, first)) {
           ok = false;
           break;
         }
         l_run += sum;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full[g & 3]);  // P written and O rescaled here
-        // this CTA's last page of the segment: the next segment's Q may replace this one's
-        bool last_own = pc.last() || (pc.pg + 1 == pc.sg.hi - 1);
+        if (lane == 0) mbar_arrive(&bars->p_full[h & 1]);  // P written and O rescaled here
+        // this CTA's last block of the segment: the next segment's Q may replace this one's
+        const bool last_own = pc.last() || (pc.sg.hi - pc.pg <= 2 * kBlkPages);
         if (last_own) {
           int bn;
-          if (next_q_segment(pc, &bn)) {
-            ok = copy_q(bn);
-          }
+          if (next_q_segment(pc, &bn)) ok = copy_q(bn);
         }
       }
       if (!ok) break;
@@ -1509,14 +1640,14 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       const float o_scale = kv_scale / kPScale;  // tensor-core units -> true units
       const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
       const int slot = whole ? 0 : prm.num_splits[pc.sg.b] + pc.sg.split;
-      // O is final once this CTA's P.V of the segment's last page completed
-      if (!warp_wait(&bars->pv_done[g & 3], (g >> 2) & 1, abort_flag, __LINE__)) {
+      // O is final once this CTA's P.V of the segment's last block completed
+      if (!warp_wait(&bars->pv_done[h & 1], (h >> 1) & 1, abort_flag, __LINE__)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int col0 = static_cast<int>(rank) * 256 + hf * kOHalf;  // this thread's O columns
-      const int grow = (warp % 4) * 32 + (lane & ~3);                // the lane group's first row
+      const int col0 = irank * 256 + hf * kOHalf;      // this thread's O columns
+      const int grow = (warp % 4) * 32 + (lane & ~3);  // the lane group's first row
       uint16_t* obase = whole ? prm.out + static_cast<size_t>(pc.sg.b) * R * kDV
                               : prm.ws_o + static_cast<size_t>(slot) * kRows * kDV;
 #pragma unroll 1
@@ -1549,15 +1680,14 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       }
     }
     if (!ok) fail();
-    // The other CTA's P.V commits of this CTA's last pages arrive in this
+    // The other CTA's P.V commits of this CTA's last blocks arrive in this
     // CTA's shared memory: they must land before this CTA may exit.
     if (ok) {
-      int last0 = -1, last1 = -1;  // last own page on each of this CTA's two tiles
-      PageCursor cnt(prm, unit);
+      int last = -1;  // last own block
+      BlockCursor cnt(prm, unit);
       while (cnt.next())
-        if ((cnt.g & 1) == static_cast<int>(rank)) ((cnt.g >> 1) & 1 ? last1 : last0) = cnt.g;
-      if (last0 >= 0) warp_spin(&bars->pv_done[last0 & 3], (last0 >> 2) & 1, abort_flag, __LINE__);
-      if (last1 >= 0) warp_spin(&bars->pv_done[last1 & 3], (last1 >> 2) & 1, abort_flag, __LINE__);
+        if ((cnt.h & 1) == irank) last = cnt.h;
+      if (last >= 0) warp_spin(&bars->px_done, (last >> 1) & 1, abort_flag, __LINE__);
     }
   }
 
