@@ -309,6 +309,18 @@ FP8MLA_API fp8mla_status_t fp8mla_get_last_device_error(fp8mla_stream_t stream, 
  * where: host pointer to 3 uint32_t. */
 FP8MLA_API fp8mla_status_t fp8mla_get_wait_timeout_site(fp8mla_stream_t stream, uint32_t* where);
 
+/* Test hook of the bounded waits (FP8 dot mode of fp8mla_decode and
+ * fp8mla_decode_no_alloc), for the current device.  fault_page = p + 1 makes
+ * CTA 0 of work unit 0 of every later FP8-dots decode skip the loads of the
+ * p-th page of its unit, so the waits on that page run out: the decode then
+ * finishes with FP8MLA_DEV_WAIT_TIMEOUT recorded (fp8mla_get_last_device_error)
+ * and wrong values in that unit's outputs, and the CUDA context stays usable.
+ * fault_page = 0 turns the hook off.  wait_limit_ns sets how long a bounded
+ * wait may see no progress before it gives up (0 = the default, 4 s).
+ * Not for production use; returns FP8MLA_ERR_CUDA if the symbols cannot be
+ * written, FP8MLA_ERR_INVALID_ARG if fault_page < 0. */
+FP8MLA_API fp8mla_status_t fp8mla_set_wait_test(int32_t fault_page, uint64_t wait_limit_ns);
+
 /* Static string naming a status code. */
 FP8MLA_API const char* fp8mla_status_string(fp8mla_status_t status);
 

@@ -64,6 +64,7 @@ _SIGNATURES = {
     "fp8_paged_cache_write": (_I, [_P, ctypes.c_int64, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "fp8mla_get_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "fp8mla_get_wait_timeout_site": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "fp8mla_set_wait_test": (_I, [ctypes.c_int32, ctypes.c_uint64]),
     "fp8mla_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -369,6 +370,13 @@ def wait_timeout_site(device=None):
     where = (ctypes.c_uint32 * 3)()
     _check(lib().fp8mla_get_wait_timeout_site(_stream(device), where), "fp8mla_get_wait_timeout_site")
     return None if where[0] == 0 else (where[0], where[1], where[2])
+
+
+def set_wait_test(fault_page: int = 0, wait_limit_ns: int = 0) -> None:
+    """Test hook of the bounded waits of the FP8-dots MLA decode (current device):
+    fault_page = p + 1 makes CTA 0 of work unit 0 skip the loads of its p-th page,
+    so its waits run out (0 = off); wait_limit_ns replaces the wait limit (0 = default)."""
+    _check(lib().fp8mla_set_wait_test(int(fault_page), int(wait_limit_ns)), "fp8mla_set_wait_test")
 
 
 def last_device_error(device=None) -> int:

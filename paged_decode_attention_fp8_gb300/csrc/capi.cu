@@ -115,6 +115,11 @@ using namespace fp8mla;
 
 extern "C" {
 
+fp8mla_status_t fp8mla_set_wait_test(int32_t fault_page, uint64_t wait_limit_ns) {
+  if (fault_page < 0) return FP8MLA_ERR_INVALID_ARG;
+  return mla_set_wait_test(fault_page, wait_limit_ns) == cudaSuccess ? FP8MLA_OK : FP8MLA_ERR_CUDA;
+}
+
 fp8mla_status_t fp8mla_get_wait_timeout_site(fp8mla_stream_t stream, uint32_t* where) {
   if (where == nullptr) return FP8MLA_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8MLA_ERR_CUDA;

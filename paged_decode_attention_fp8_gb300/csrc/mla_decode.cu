@@ -131,7 +131,6 @@ struct SegmentWalker {
   }
 };
 
-// kCluster: the barrier also receives arrivals from the other CTA of a cluster
 // site: a source line recorded if the wait runs out
 template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
@@ -242,7 +241,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
           const int use = i / C::kStages;
           bool waited = true;
           if (lane == 0) {
-            waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla);
+            waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
             if (waited) {
               uint8_t* sb = smem + st * C::kStageBytes;
               mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
@@ -262,7 +261,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
     // Never leave with copies in flight: wait for the last loads issued.
     if (lane == 0)
       for (int j = max(0, i - C::kStages); j < i; ++j)
-        wait_bounded(&bars->kv_full[j % C::kStages], (j / C::kStages) & 1, nullptr, &g_status_mla);
+        wait_bounded(&bars->kv_full[j % C::kStages], (j / C::kStages) & 1, nullptr, &g_status_mla, __LINE__);
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
@@ -286,7 +285,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
       };
 
       auto issue_pv = [&](int j, bool first_in_seg) -> bool {
-        if (!wait_bounded(&bars->p_full, j & 1, abort_flag, &g_status_mla)) return false;
+        if (!wait_bounded(&bars->p_full, j & 1, abort_flag, &g_status_mla, __LINE__)) return false;
         tc_fence_after();
         const int st = j % C::kStages;
         const uint32_t sb = smem_u32(smem + st * C::kStageBytes);
@@ -305,14 +304,14 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
       };
 
       while (ok && walk.next(sg)) {
-        if (!wait_bounded(&bars->q_full, seg_i & 1, abort_flag, &g_status_mla)) break;
+        if (!wait_bounded(&bars->q_full, seg_i & 1, abort_flag, &g_status_mla, __LINE__)) break;
         const int first_i = i;
         for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
           const int st = i % C::kStages;
           const int use = i / C::kStages;
-          if (!wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla) ||
-              !wait_bounded(&bars->cvt_ready[st], use & 1, abort_flag, &g_status_mla) ||
-              (i > 0 && !wait_bounded(&bars->s_free, (i - 1) & 1, abort_flag, &g_status_mla))) {
+          if (!wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla, __LINE__) ||
+              !wait_bounded(&bars->cvt_ready[st], use & 1, abort_flag, &g_status_mla, __LINE__) ||
+              (i > 0 && !wait_bounded(&bars->s_free, (i - 1) & 1, abort_flag, &g_status_mla, __LINE__))) {
             ok = false;
             break;
           }
@@ -329,7 +328,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
         ++seg_i;
       }
       tc_commit(&bars->final_mma);
-      wait_bounded(&bars->final_mma, 0, nullptr, &g_status_mla);
+      wait_bounded(&bars->final_mma, 0, nullptr, &g_status_mla, __LINE__);
     }
     __syncwarp();
   } else if (warp == 2 || warp == 3) {
@@ -343,7 +342,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
       for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
         const int st = i % C::kStages;
         const int use = i / C::kStages;
-        if (t == 0) bars->cvt_ok = wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla) ? 1u : 0u;
+        if (t == 0) bars->cvt_ok = wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla, __LINE__) ? 1u : 0u;
         named_bar_sync(1, 64);
         if (!bars->cvt_ok) {
           ok = false;
@@ -410,7 +409,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
     uint32_t xphase = 0;
     auto xsync = [&]() -> bool {
       warp_arrive(&bars->xchg);
-      const bool ok = warp_wait(&bars->xchg, xphase & 1, abort_flag);
+      const bool ok = warp_wait(&bars->xchg, xphase & 1, abort_flag, __LINE__);
       ++xphase;
       return ok;
     };
@@ -459,7 +458,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
       float m_run = kNegInf, l_run = 0.f;  // l_run sums the scaled p (2^kPLog2 p)
       bool ok = true;
       for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
-        if (!warp_wait(&bars->s_full, i & 1, abort_flag)) {
+        if (!warp_wait(&bars->s_full, i & 1, abort_flag, __LINE__)) {
           ok = false;
           break;
         }
@@ -515,7 +514,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
         }
         l_run = l_run * alpha + sum;
 
-        if (i > 0 && !warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag)) {
+        if (i > 0 && !warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag, __LINE__)) {
           ok = false;
           break;
         }
@@ -541,7 +540,7 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
       if (!ok) break;
 
       // ---- epilogue: O is final once the segment's last P.V completes ----
-      if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag)) break;
+      if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag, __LINE__)) break;
       tc_fence_after();
       bars->xsum[hf][r] = l_run;
       if (!xsync()) break;
@@ -602,22 +601,67 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
 }
 
 // ===========================================================================
-// Q preparation for FP8 dots (one grid ahead of the decode kernel).
+// FP8-dots kernel.
+//
+// Work unit = 2 CTAs, each owning one 256-wide dv slice.  The shared-memory
+// ring of 5 stages carries, in one order that every role walks, three Q slots
+// at the start of each segment (the segment's quantised Q: two latent halves
+// and the RoPE part) followed by the segment's KV pages, so no separate Q
+// buffer competes with the KV pages for shared memory.  TMEM: O 256 + two S
+// buffers of 64 + Q latent 128 columns.
 // ===========================================================================
 namespace f8 {
-// Quantised Q of a sequence (FP8 dots), as written by mla_qprep_kernel: two
-// latent slots, slot h (h = 0, 1) holding per row latent bytes [256 h,
-// 256 h + 256) at a 272-byte pitch, then the RoPE values as f16 at a 144-byte
-// pitch (pitches chosen so a quarter-warp's 16-byte row accesses hit distinct
-// banks), then the latent quantisation error q_hat qs - q, 128 rows x 512
-// bf16, read by the combine kernel for the LSE correction.
+constexpr int kStages = 5;
+// Test hook of the bounded waits (0 = off); set by mla_set_wait_test.
+__device__ int g_fault_page = 0;
+constexpr int kThreads = 384;
+constexpr int kOffRope8 = 4 * kLatBox;             // 64 tokens x 64 E4M3 RoPE bytes, no swizzle
+constexpr int kStageBytes = kOffRope8 + kPage * 64;
+// Shared memory after the ring: two buffers for a page's RoPE part as f16
+// (64 keys x 128 B, 128-byte swizzle), Q's RoPE part (128 rows x 128 B f16,
+// 128-byte swizzle), and P (128 rows x 64 E4M3 keys) as 8-row x 16-byte core
+// matrices: row group g and 16-byte key chunk c at g * kPSbo + c * kPLbo.
+constexpr int kCvtBytes = kLatBox;
+constexpr int kOffCvt = kStages * kStageBytes;
+constexpr int kOffQRope = kOffCvt + 2 * kCvtBytes;
+constexpr int kOffP = kOffQRope + kRows * 128;
+constexpr int kPLbo = 128, kPSbo = 512;
+constexpr int kSmemData = kOffP + kRows * kPage;
+constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
+constexpr float kTau = 2.75f;                     // 64 * 2^2.75 = 430.5 < 448
+// TMEM columns: O slice, two S buffers (pages alternate), Q latent (E4M3).
+constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
+// Quantised Q of a sequence, as three ring slots: slot h (h = 0, 1) holds per
+// row latent bytes [256 h, 256 h + 256) at a 272-byte pitch, slot 2 the RoPE
+// values as f16 at a 144-byte pitch (pitches chosen so a quarter-warp's
+// 16-byte row accesses hit distinct banks).
 constexpr int kQLatPitch = 272;
 constexpr int kQRopePitch = 144;
 constexpr int kQLatSlotBytes = kRows * kQLatPitch;
 constexpr int kQRopeSlotBytes = kRows * kQRopePitch;
+static_assert(kQLatSlotBytes <= kStageBytes && kQRopeSlotBytes <= kStageBytes, "a Q slot fits one stage");
+// After the slots: the latent quantisation error q_hat qs - q, 128 rows x 512
+// bf16, read by the combine kernel for the LSE correction.
 constexpr int kQErrOff = 2 * kQLatSlotBytes + kQRopeSlotBytes;
 static_assert(kQErrOff == kMlaQErrOff && kQErrOff + kRows * kDLat * 2 == kMlaQBytes, "quantised-Q layout");
-static_assert(kQLatPitch % 16 == 0 && kQRopePitch % 16 == 0 && kQLatSlotBytes % 16 == 0, "16-byte rows");
+static_assert(kStageBytes % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
+              "1 KB aligned tiles");
+static_assert(kStageBytes == static_cast<int>(kPageTxBytes), "a page fills one stage");
+
+struct Bars {
+  uint64_t kv_full[kStages];    // stage holds its page (TMA bytes) or its Q slot (Q warps' arrival)
+  uint64_t kv_empty[kStages];   // stage may be refilled
+  uint64_t cvt_ready[kStages];  // the page's RoPE part is converted and its dead rows zeroed
+  uint64_t s_full[2];           // S buffer b holds a page's scores
+  uint64_t p_full;              // P written (one arrival per softmax warp)
+  uint64_t pv_done;             // the P.V that read P completed
+  uint64_t q_full, final_mma, xchg;
+  uint32_t tmem_base, abort_flag, cvt_ok;
+  float xsum[2][kRows];         // row-sum halves
+};
+
+constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
+static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
 
 // Quantises the Q rows of sequence b into the three Q slots: latent -> E4M3(q / qs),
 // RoPE -> f16(q / qs), qs = smallest power of two with amax <= 448 qs.  kTpr
@@ -726,141 +770,10 @@ __device__ __forceinline__ void lane_group_transpose(uint4 (&pc)[N], int lane) {
 }
 }  // namespace f8
 
-// ===========================================================================
-// FP8-dots kernel: one work unit = a cluster of two CTAs.
-//
-// CTA `rank` (0 or 1) owns dv columns [256 rank, 256 rank + 256) of O.  The
-// unit's pages are taken two at a time: block h of the unit's block stream
-// (pages 2i and 2i + 1 of a segment, or its last page alone; counted across
-// the unit's segments) belongs to CTA h % 2.  The owner computes the block's
-// scores S = Q K^T as one 128-row x 128-key tile and its probabilities P; the
-// other CTA only multiplies P by its dv half of the block's V.  (A tcgen05
-// MMA with M = 128 costs nearly the same for any N up to 256, so 128-key
-// score tiles take half the tensor time per key of 64-key ones.)  P (128 rows
-// x 128 keys, E4M3) and the reference it was taken against travel to the
-// other CTA through distributed shared memory.
-//
-// Block h's P is taken against a reference m_h (log2 units) that the owner
-// decides from what it already has: m_h = max(m_{h-2}, m_{h-3}) (its own
-// previous block's reference and the other CTA's reference of block h - 3,
-// within the segment), raised to block h's row maximum when that exceeds it by
-// more than kTau.  m_h travels with P; both CTAs rescale their O halves and
-// row sums to m_h before block h's P.V, so both apply the same factors in the
-// same order (a factor may be above 1 for a block after the other CTA raised
-// its reference), every stored P is at most 64 * 2^kTau < 448, and no block
-// waits for the other CTA's decision on the block just before it.
-//
-// Per CTA: TMEM holds its O half (256 columns), S (128) and the latent Q
-// (128, E4M3).  Shared memory holds a V ring with this CTA's dv half of the
-// latent bytes of every block (3 x 32 KB, released by the block's P.V), a
-// ring of 16 KB K slices for its own blocks (per block: the other latent
-// half's two 128-byte boxes, then the RoPE part, converted to f16 in place;
-// each released when its Q.K^T step completes -- Q.K^T reads this CTA's
-// latent half from the V ring), Q's RoPE part (f16, 16 KB) and two P
-// messages: block h's P and its 128 row references go to message h % 2 in
-// both CTAs (to the other CTA by asynchronous remote stores that count their
-// bytes on its p_rx barrier; the sender does not wait for them), and a
-// message is rewritten two blocks later, after both CTAs' P.V of the block
-// before read it.
-// ===========================================================================
-namespace pr {
-constexpr int kThreads = 384;
-constexpr int kBlkPages = 2;
-constexpr int kBlkKeys = kBlkPages * kPage;   // keys of a full block (N of its Q.K^T)
-constexpr int kVStages = 3;                   // this CTA's latent half of every block, for P.V (and own Q.K^T)
-constexpr int kKSlices = 4;                   // own blocks' other latent half and RoPE part, three slices a block
-constexpr int kBoxBlk = kBlkPages * kLatBox;  // one 128-byte column box of a block: page 0 rows, then page 1 rows
-constexpr int kVBytes = 2 * kBoxBlk;          // latent bytes [256 rank, 256 rank + 256) of a block
-constexpr int kSliceBytes = kBoxBlk;
-constexpr int kRopeRaw = kPage * 64;          // in a page's 8 KB of a RoPE slice: where its E4M3 bytes land
-constexpr int kOffV = 0;
-constexpr int kOffK = kOffV + kVStages * kVBytes;
-constexpr int kOffQRope = kOffK + kKSlices * kSliceBytes;  // Q RoPE, 128 rows x 64 f16, 128-byte swizzle
-constexpr int kOffP = kOffQRope + kRows * 128;             // two P messages
-constexpr int kPBytes = kRows * kBlkKeys;                  // P: 128 rows x 128 E4M3 keys
-constexpr int kPTile = kPBytes + kRows * 4;                // then the 128 row references (float)
-static_assert(kPTile % 128 == 0, "16-byte aligned P tiles and reference pieces");
-constexpr int kOffPtab = kOffP + 2 * kPTile;  // the unit's first kPtabMax block-table entries
-constexpr int kPtabMax = 2048;
-constexpr int kSmemData = kOffPtab + kPtabMax * 4;
-// P: 8-row x 16-byte core matrices, key chunk c of row group G at c * kPLbo + G * kPSbo, so the 32
-// rows x 16 bytes that one warp writes per key chunk are one contiguous 512-byte piece
-constexpr int kPLbo = 2048, kPSbo = 128;
-constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
-constexpr float kTau = 2.75f;                    // 64 * 2^2.75 = 430.5 < 448
-// TMEM columns: O half, S, Q latent (E4M3, the A operand of the latent Q.K^T)
-constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
-static_assert(kVBytes % 1024 == 0 && kOffK % 1024 == 0 && kSliceBytes % 1024 == 0 && kOffQRope % 1024 == 0 &&
-                  kOffP % 1024 == 0,
-              "1 KB aligned tiles");
-
-struct Bars {
-  uint64_t v_full[kVStages];   // by block h % kVStages: this CTA's latent half of block h loaded
-  uint64_t v_empty[kVStages];  // its P.V (and for an own block its Q.K^T) completed
-  uint64_t k_full[kKSlices];   // by slice n % kKSlices (slices 3j, 3j + 1, 3j + 2 of own block j) loaded
-  uint64_t k_empty[kKSlices];  // the slice's Q.K^T step completed
-  uint64_t k_cvt[2];           // by own block j % 2: its RoPE slice converted to f16
-  uint64_t s_full;             // S holds own block j's scores
-  uint64_t s_free;             // S read out (8 softmax warps)
-  uint64_t p_full[2];          // by tile h % 2: P written here (own block) / O ready here (other's block)
-  uint64_t p_rx;               // the other CTA's P message copied in (transaction bytes; re-armed by a softmax thread)
-  uint64_t pv_done[2];         // by tile: the block's P.V completed here
-  uint64_t px_done;            // this CTA's block's P.V completed in the other CTA (its commit, multicast here)
-  uint64_t rmax_full[4];       // by row group: both halves' row maxima written (2 warps)
-  uint64_t lx_full[2];         // by segment parity: the other CTA's row sums arrived (4 warps)
-  uint64_t q_full;             // a segment's Q copied in (8 softmax warps)
-  uint64_t ptab_ready;         // the block-table entries are in shared memory
-  uint64_t final_mma, xchg;
-  uint32_t tmem_base, abort_flag, cvt_ok;
-  // written by 16-byte stores (the other CTA's lane 0 sends 32 rows at a time)
-  alignas(16) float lx[2][kRows];  // the other CTA's row sums, by segment parity
-  float xsum[2][2][kRows];         // by segment parity: row-sum halves of the two softmax threads of a row
-  float rmax[2][2][kRows];         // by own block parity: the row maxima of the two halves of a row
-};
-static_assert(offsetof(Bars, lx) % 16 == 0, "16-byte rows of sums");
-static_assert(kSmemData % 16 == 0, "the barrier block starts 16-byte aligned");
-
-constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
-static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
-
-// Blocks of a unit one at a time: h counts the unit's blocks across
-// segments, seg its non-empty segments; the block is pages [pg, pg + npg),
-// and u0 + (pg - sg.lo) is the unit's page count before it.
-struct BlockCursor {
-  SegmentWalker walk;
-  Segment sg;
-  int pg = 0, npg = 0, h = -1, seg = -1, u0 = 0;
-  bool valid = false;
-  __device__ BlockCursor(const MlaParams& p, int unit) : walk(p, unit) {}
-  __device__ bool next() {
-    if (valid && pg + npg < sg.hi) {
-      pg += npg;
-    } else {
-      if (valid) u0 += sg.hi - sg.lo;
-      valid = walk.next(sg);
-      if (!valid) return false;
-      pg = sg.lo;
-      ++seg;
-    }
-    npg = min(kBlkPages, sg.hi - pg);
-    ++h;
-    return true;
-  }
-  __device__ bool first() const { return pg == sg.lo; }
-  __device__ bool last() const { return pg + npg == sg.hi; }
-};
-
-// Unit-level fault injection for the bounded-wait test: when g_fault_block is
-// h + 1, CTA 0 of unit 0 never issues the loads of its block h, so every wait
-// on them runs out.
-__device__ int g_fault_block = 0;
-
-}  // namespace pr
-
-__global__ void __launch_bounds__(pr::kThreads, 1)
-    mla_fp8_pair_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
-                        const MlaParams prm) {
-  using namespace pr;
+__global__ void __launch_bounds__(f8::kThreads, 1)
+    mla_fp8_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
+                   const MlaParams prm) {
+  using namespace f8;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -870,43 +783,22 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int unit = blockIdx.x / 2;
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t other = rank ^ 1u;
-  const int irank = static_cast<int>(rank);
-  auto remote = [&](const void* p) { return mapa_shared(smem_u32(p), other); };
-  // stop this CTA and tell the other one, whose waits then end too
-  auto fail = [&]() {
-    *abort_flag = 1u;
-    st_cluster_u32(remote(&bars->abort_flag), 1u);
-  };
+  const int part = blockIdx.x % 2;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->cvt_ready[s], 1);
     }
-    for (int s = 0; s < kKSlices; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->k_cvt[b], 1);
-      mbar_init(&bars->p_full[b], kSoftmaxThreads / 32);
-      mbar_init(&bars->pv_done[b], 1);
-      mbar_init(&bars->lx_full[b], kSoftmaxThreads / 64);
-    }
-    for (int b = 0; b < 4; ++b) mbar_init(&bars->rmax_full[b], 2);
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, kSoftmaxThreads / 32);
-    mbar_init(&bars->p_rx, 1);
-    mbar_init(&bars->px_done, 1);
+    for (int b = 0; b < 2; ++b) mbar_init(&bars->s_full[b], 1);
+    mbar_init(&bars->p_full, kSoftmaxThreads / 32);
+    mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
-    mbar_init(&bars->ptab_ready, 1);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->xchg, kSoftmaxThreads / 32);
     bars->abort_flag = 0;
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bars->p_rx, kPTile);  // the first message
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -918,364 +810,272 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // both CTAs' barriers are initialised before either arrives on the other's
-  cluster_arrive();
-  cluster_wait();
   griddep_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
 
+  // Ring protocol.  Every role walks the same slot sequence: three Q slots at
+  // the start of each segment (its quantised Q, prepared by mla_qprep_kernel)
+  // and then its pages.  Each stage barrier completes one
+  // phase per occupancy of its stage, and every role that waits on one
+  // observes each of its phases in turn, so a parity wait can never pass on a
+  // phase two behind or two ahead: kv_empty is waited by the producer only;
+  // kv_full by the converter for every occupancy, by the MMA warp for pages
+  // and by the softmax warps for Q slots; each stage is released only after
+  // the converter's cvt_ready for that occupancy.
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
-    // Two streams of loads, issued by lane 0 as their stages free up: the V
-    // half of every block in block order (this CTA's latent bytes
-    // [256 rank, +256) of each page), and the three K slices of each own
-    // block (the other latent half's two boxes, then the RoPE bytes).
+    // The warp loads 32 block-table entries at a time (one per lane); lane 0
+    // issues the loads.
     if (lane == 0) {
       tma_prefetch_desc(&tm_lat);
       tma_prefetch_desc(&tm_rope);
-      const int fault = (unit == 0 && rank == 0) ? *(volatile int*)&g_fault_block : 0;
-      const int32_t* ptab = reinterpret_cast<const int32_t*>(smem + kOffPtab);
-      bool ptab_ok = false;
-      // a block-table entry: from the shared-memory copy once it is in, else from global memory
-      auto phys_of = [&](const BlockCursor& c, int i) -> int {
-        const int u = c.u0 + (c.pg - c.sg.lo) + i;
-        if (!ptab_ok && u < kPtabMax) ptab_ok = mbar_test_wait(&bars->ptab_ready, 0);
-        int ph = (ptab_ok && u < kPtabMax)
-                     ? ptab[u]
-                     : __ldg(prm.block_table + static_cast<size_t>(c.sg.b) * prm.max_pages + c.pg + i);
-        if (ph < 0 || ph >= prm.num_pages) {
-          atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
-          ph = 0;
-        }
-        return ph;
-      };
-      auto fetch = [&](const BlockCursor& c, int (&ph)[2]) {
-        ph[0] = phys_of(c, 0);
-        ph[1] = c.npg > 1 ? phys_of(c, 1) : 0;
-      };
-      BlockCursor vc(prm, unit), kc(prm, unit);  // next block to load V for; next own block for K slices
-      auto adv_own = [&](BlockCursor& c) -> bool {
-        while (c.next())
-          if ((c.h & 1) == irank) return true;
-        return false;
-      };
-      bool v_more = vc.next(), k_more = adv_own(kc);
-      int vp[2] = {0, 0}, kp[2] = {0, 0};
-      if (v_more) fetch(vc, vp);
-      if (k_more) fetch(kc, kp);
-      int kn = 0, ks = 0;  // K slices issued; slice of the current own block (0, 1 latent, 2 RoPE)
-      uint32_t v_last = 0, v_par = 0, k_last = 0, k_par = 0;  // per stage: loaded here, and its phase parity
-      uint32_t polls = 0;
-      uint64_t t_idle = 0;
-      bool ok = true;
-      while (ok && (v_more || k_more)) {
-        bool did = false;
-        if (k_more) {
-          const int st = kn % kKSlices, use = kn / kKSlices;
-          if (use == 0 || mbar_test_wait(&bars->k_empty[st], (use - 1) & 1)) {
-            if (fault != kc.h + 1) {
-              uint8_t* sb = smem + kOffK + st * kSliceBytes;
-              mbar_arrive_expect_tx(&bars->k_full[st], static_cast<uint32_t>((ks < 2 ? kLatBox : kRopeRaw) * kc.npg));
-#pragma unroll
-              for (int i = 0; i < kBlkPages; ++i) {  // (compile-time indices keep kp in registers)
-                if (i >= kc.npg) break;
-                if (ks < 2)
-                  tma_load_3d(sb + i * kLatBox, &tm_lat, &bars->k_full[st], static_cast<int>(other) * 256 + ks * 128,
-                              0, kp[i]);
-                else
-                  tma_load_3d(sb + i * kLatBox + kRopeRaw, &tm_rope, &bars->k_full[st], kDLat, 0, kp[i]);
-              }
-              k_last |= 1u << st;
-              k_par = (k_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
-            }
-            ++kn;
-            if (++ks == 3) {
-              ks = 0;
-              k_more = adv_own(kc);
-              if (k_more) fetch(kc, kp);
-            }
-            did = true;
+    }
+    // bounded-wait test hook: CTA 0 of unit 0 never loads its page (g_fault_page - 1) of the unit
+    const int fault = (unit == 0 && part == 0) ? *reinterpret_cast<volatile int*>(&g_fault_page) : 0;
+    int upg = 0;  // the unit's pages so far
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int k = 0;
+    uint32_t issued = 0, par = 0;  // per stage: last occupant was loaded here, and its use parity
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      // the segment's quantised Q: two latent halves and the RoPE part
+      for (int q = 0; q < 3 && ok; ++q, ++k) {
+        const int st = k % kStages, use = k / kStages;
+        const uint32_t bytes = (q < 2) ? kQLatSlotBytes : kQRopeSlotBytes;
+        bool waited = true;
+        if (lane == 0) {
+          waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
+          if (waited) {
+            mbar_arrive_expect_tx(&bars->kv_full[st], bytes);
+            bulk_load(smem + st * kStageBytes,
+                      prm.qbuf + static_cast<size_t>(sg.b) * kMlaQBytes + static_cast<size_t>(q) * kQLatSlotBytes,
+                      bytes, &bars->kv_full[st]);
+            issued |= 1u << st;
+            par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
           }
         }
-        if (v_more && (vc.h < kVStages ||
-                       mbar_test_wait(&bars->v_empty[vc.h % kVStages], ((vc.h / kVStages) - 1) & 1))) {
-          const int st = vc.h % kVStages;
-          if (fault != vc.h + 1) {
-            uint8_t* sb = smem + kOffV + st * kVBytes;
-            mbar_arrive_expect_tx(&bars->v_full[st], static_cast<uint32_t>(2 * kLatBox * vc.npg));
-#pragma unroll
-            for (int q = 0; q < 2; ++q)
-#pragma unroll
-              for (int i = 0; i < kBlkPages; ++i)
-                if (i < vc.npg)
-                  tma_load_3d(sb + q * kBoxBlk + i * kLatBox, &tm_lat, &bars->v_full[st], irank * 256 + q * 128, 0,
-                              vp[i]);
-            v_last |= 1u << st;
-            v_par = (v_par & ~(1u << st)) | (static_cast<uint32_t>((vc.h / kVStages) & 1) << st);
+        ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0;
+      }
+      if (!ok) break;
+      const int32_t* bt = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
+      for (int chunk = sg.lo; ok && chunk < sg.hi; chunk += 32) {
+        int mine = 0;
+        if (chunk + lane < sg.hi) {
+          mine = __ldg(bt + chunk + lane);
+          if (mine < 0 || mine >= prm.num_pages) {
+            atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
+            mine = 0;
           }
-          v_more = vc.next();
-          if (v_more) fetch(vc, vp);
-          did = true;
         }
-        if (did) {
-          polls = 0;
-        } else if ((++polls & 255u) == 0) {
-          if (*abort_flag) ok = false;
-          if (polls == 256) t_idle = globaltimer_ns();
-          if (ok && polls > kWaitMinPolls && globaltimer_ns() - t_idle > *(volatile uint64_t*)&g_wait_limit_ns) {
-            atomicOr(&g_status_mla, FP8MLA_DEV_WAIT_TIMEOUT);
-            record_timeout_site(__LINE__);
+        const int cnt = min(32, sg.hi - chunk);
+        for (int j = 0; j < cnt; ++j, ++k, ++upg) {
+          const int phys = __shfl_sync(0xffffffffu, mine, j);
+          const int st = k % kStages;
+          const int use = k / kStages;
+          bool waited = true;
+          if (lane == 0) {
+            waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
+            if (waited && fault != upg + 1) {
+              uint8_t* sb = smem + st * kStageBytes;
+              mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kLatBox, &tm_lat, &bars->kv_full[st], q * 128, 0, phys);
+              tma_load_3d(sb + kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
+              issued |= 1u << st;
+              par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
             ok = false;
+            break;
           }
         }
       }
-      if (!ok) fail();
-      // Never leave with copies in flight: wait for the last load of each stage.
-      for (int st = 0; st < kKSlices; ++st)
-        if ((k_last >> st) & 1u) wait_bounded(&bars->k_full[st], (k_par >> st) & 1u, nullptr, &g_status_mla, __LINE__);
-      for (int st = 0; st < kVStages; ++st)
-        if ((v_last >> st) & 1u) wait_bounded(&bars->v_full[st], (v_par >> st) & 1u, nullptr, &g_status_mla, __LINE__);
     }
+    // Never leave with copies in flight: wait for the last load of each stage.
+    if (lane == 0)
+      for (int s = 0; s < kStages; ++s)
+        if ((issued >> s) & 1u) wait_bounded(&bars->kv_full[s], (par >> s) & 1u, nullptr, &g_status_mla, __LINE__);
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    // The whole warp runs the loop and one elected lane issues.  The warp
-    // polls the next block's P.V and the next step of the next own block's
-    // Q.K^T and issues whichever is ready (P.V first: it frees a V stage and
-    // the other CTA's message), so neither waits behind the other.  Q.K^T(j)
-    // runs in four steps: the other latent half's first box (its K slice)
-    // once S is read out and, when it opens a segment, that segment's Q is
-    // in; its second box; the converted RoPE slice; and last this CTA's
-    // latent half from the V stage (probed only after the P.V of the stage's
-    // previous block was issued, so the probe cannot see that block's phase),
-    // which the block's V load gates.
-    // P.V(h) needs P(h) written and O ready, and the block's V half loaded.
-    // Before the P.V of a block holding a sequence's last page the warp zeroes
-    // that page's V rows past the sequence end (they may hold anything, and P
-    // is 0 there).
-    constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128);  // e4m3, B MN-major, N = 256
-    const bool leader = elect_one();
-    const uint16_t other_mask = static_cast<uint16_t>(1u << other);
-    const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
-    BlockCursor qk(prm, unit);  // next own block whose Q.K^T is due
-    BlockCursor pv(prm, unit);  // next block whose P.V is due
-    int qn = 0, qk_seg = -1, qj = 0, step = 0;  // Q copies consumed, segment of the last Q.K^T, own blocks done, step
-    auto qk_advance = [&]() -> bool {
-      while (qk.next())
-        if ((qk.h & 1) == irank) return true;
-      return false;
-    };
-    bool qk_more = qk_advance();
-    bool pv_more = pv.next();
-    bool ok = true;
-    uint64_t t_idle = 0;
-    uint32_t polls = 0;
-    while (ok && (qk_more || pv_more)) {
-      bool did = false;
-      if (pv_more) {
-        const int h = pv.h;
-        const bool mine = (h & 1) == irank;
-        const int st = h % kVStages;
-        // P(h) written here (own block) or O ready for it here (the other CTA's
-        // block; its P message arrived before that), and the V half loaded
-        const bool ready = mbar_test_wait(&bars->p_full[h & 1], (h >> 1) & 1) &&
-                           mbar_test_wait(&bars->v_full[st], (h / kVStages) & 1);
-        if (__all_sync(0xffffffffu, ready)) {
-          uint8_t* vs = smem + kOffV + st * kVBytes;
-          if (pv.pg + pv.npg == pv.sg.n) {  // the sequence's last page: zero its rows past the end
-            const int lp = pv.npg - 1;
-            const int live = pv.sg.s_k - (pv.pg + lp) * kPage;  // rows of the page that hold keys
-            if (live < kPage) {
-              const uint4 z = make_uint4(0, 0, 0, 0);
-              for (int i = lane; i < (kPage - live) * 16; i += 32) {
-                const int row = live + i / 16, c = i % 16;
-                *reinterpret_cast<uint4*>(vs + (c >> 3) * kBoxBlk + lp * kLatBox + row * 128 + ((c & 7) << 4)) = z;
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-            }
-          }
-          tc_fence_after();
-          const uint64_t pd = make_sdesc(smem_u32(smem + kOffP + (h & 1) * kPTile), kPLbo, kPSbo, SWIZZLE_NONE);
-          const uint64_t vd = make_sdesc(smem_u32(vs), kBoxBlk, 1024, SWIZZLE_128B);
-          const bool first = pv.first();
-          for (int kk = 0; kk < 2 * pv.npg; ++kk)
-            mma_f8_ss_if(leader, tmem + kTO, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
-                         (first && kk == 0) ? 0u : 1u);
-          tc_commit_if(leader, &bars->pv_done[h & 1]);
-          tc_commit_if(leader, &bars->v_empty[st]);
-          // the other CTA's block: its owner may reuse the message once this P.V completed
-          if (!mine) tc_commit_mc_if(leader, &bars->px_done, other_mask);
-          pv_more = pv.next();
-          did = true;
-        }
-      }
-      if (!did && qk_more) {
-        const int j = qj;
-        const uint32_t n_keys = static_cast<uint32_t>(kPage * qk.npg);
-        const uint32_t idesc8 = make_idesc(0, 0, 0, 0, n_keys, 128);   // e4m3 x e4m3, both K-major
-        const uint32_t idesc16 = make_idesc(0, 0, 0, 0, n_keys, 128);  // f16 x f16 (E4M3 keys are exact in f16)
-        if (step == 3) {
-          const int vst = qk.h % kVStages;
-          const bool ready = (!pv_more || pv.h > qk.h - kVStages) &&
-                             mbar_test_wait(&bars->v_full[vst], (qk.h / kVStages) & 1);
-          if (__all_sync(0xffffffffu, ready)) {
-            tc_fence_after();
-            const uint64_t vd = make_sdesc(smem_u32(smem + kOffV + vst * kVBytes), 16, 1024, SWIZZLE_128B);
-            // boxes q = 2 rank + i hold Q.K^T bytes [128 q, 128 q + 128) of the keys
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ts_if(leader, tmem + kTS, tmem + kTQ + (4 * (2 * irank + i) + kk) * 8,
-                             vd + ((i * kBoxBlk + kk * 32) >> 4), idesc8, 1u);
-            tc_commit_if(leader, &bars->s_full);
-            ++qj;
-            step = 0;
-            qk_more = qk_advance();
-            did = true;
-          }
-        } else {
-          const int n = 3 * j + step;  // steps 0, 1: the other latent boxes; step 2: RoPE
-          const int st = n % kKSlices;
-          const bool opens = step == 0 && qk.seg != qk_seg;
-          bool ready;
-          if (step == 0)
-            ready = (!opens || mbar_test_wait(&bars->q_full, qn & 1)) &&
-                    (j < 1 || mbar_test_wait(&bars->s_free, (j - 1) & 1)) &&
-                    mbar_test_wait(&bars->k_full[st], (n / kKSlices) & 1);
-          else if (step == 1)
-            ready = mbar_test_wait(&bars->k_full[st], (n / kKSlices) & 1);
-          else
-            ready = mbar_test_wait(&bars->k_cvt[j & 1], (j >> 1) & 1);
-          if (__all_sync(0xffffffffu, ready)) {
-            if (opens) {
-              qk_seg = qk.seg;
-              ++qn;
-            }
-            tc_fence_after();
-            const uint64_t kd = make_sdesc(smem_u32(smem + kOffK + st * kSliceBytes), 16, 1024, SWIZZLE_128B);
-            if (step < 2) {
-              const int q = 2 * static_cast<int>(other) + step;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ts_if(leader, tmem + kTS, tmem + kTQ + (4 * q + kk) * 8, kd + ((kk * 32) >> 4), idesc8,
-                             (step | kk) ? 1u : 0u);
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ss_if(leader, tmem + kTS, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), idesc16, 1u);
-            }
-            tc_commit_if(leader, &bars->k_empty[st]);
-            ++step;
-            did = true;
-          }
-        }
-      }
-      // bounded: no progress for the wait limit (or another role stopped) ends the loop
-      if (did) {
-        polls = 0;
-      } else if ((++polls & 255u) == 0) {
-        if (*abort_flag) ok = false;
-        if (polls == 256) t_idle = globaltimer_ns();
-        if (ok && polls > kWaitMinPolls && globaltimer_ns() - t_idle > *(volatile uint64_t*)&g_wait_limit_ns) {
-          if (lane == 0) {
-            atomicOr(&g_status_mla, FP8MLA_DEV_WAIT_TIMEOUT);
-            record_timeout_site(__LINE__);
-          }
-          ok = false;
-        }
-        ok = __all_sync(0xffffffffu, ok);
-      }
-    }
-    if (!ok) fail();
-    if (leader) tc_commit(&bars->final_mma);
-    __syncwarp();
-    warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
-  } else if (warp == 2 || warp == 3) {
-    // ---------------------- RoPE conversion of own blocks (64 threads) ----
-    // Thread 0 waits for every K slice in order (so no wait can see a stage's
-    // phase two ahead).  For a block's RoPE slice, thread t reads the E4M3
-    // RoPE bytes of token row t of each page from the second half of the
-    // page's 8 KB and, after all have read, writes them as f16 (exact) over
-    // the whole 8 KB, 128-byte swizzled; rows past the sequence end become 0
-    // (their scores are masked anyway).
-    const int t = threadIdx.x - 64;  // token row of a page
-    {  // first the unit's block-table entries (as many as fit) into shared memory, for the producer
-      int32_t* ptab = reinterpret_cast<int32_t*>(smem + kOffPtab);
-      SegmentWalker w(prm, unit);
+    // The whole warp runs the loop (so descriptors stay warp-uniform) and one
+    // elected lane issues -- from a lone thread each MMA costs about twice as
+    // long to issue.  Pages alternate between two S buffers, so the Q.K^T of
+    // page i runs while the softmax warps work on page i - 1.  Per page i: wait
+    // until S buffer i % 2 was read out (page i - 2), Q.K^T as 16 E4M3 MMAs
+    // (latent, Q from TMEM, K = 32) and 4 f16 MMAs (RoPE, Q from shared
+    // memory, K = 16), then the P.V of page i - 1 (2 E4M3 MMAs, K = 32 keys,
+    // N = 256) once its P is written.
+    {
+      constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
+      constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
+      constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
+      const uint32_t t_o = tmem + kTO;
+      const bool leader = elect_one();
+      const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
+      const uint64_t pd = make_sdesc(smem_u32(smem + kOffP), kPLbo, kPSbo, SWIZZLE_NONE);
+      SegmentWalker walk(prm, unit);
       Segment sg;
-      int u0 = 0;
-      while (u0 < kPtabMax && w.next(sg)) {
-        const int32_t* row = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
-        const int n = min(sg.hi - sg.lo, kPtabMax - u0);
-        for (int i = t; i < n; i += 64) cp_async4(ptab + u0 + i, row + sg.lo + i);
-        u0 += n;
+      int i = 0, k = 0, seg = 0;
+      int j = 0;           // next page whose P.V is due (pages j .. i - 1 have their Q.K^T issued)
+      uint32_t pend = 0;   // per pending page p, byte p % 4: its stage | first-of-segment << 3
+      bool ok = true;
+      // the P.V of page j, once its P is written; it releases the page's stage
+      auto issue_pv = [&]() -> bool {
+        if (!warp_spin(&bars->p_full, j & 1, abort_flag, __LINE__)) return false;
+        tc_fence_after();
+        const uint32_t e = (pend >> (8 * (j & 3))) & 0xFFu;
+        const int st = static_cast<int>(e & 7u);
+        const bool first = ((e >> 3) & 1u) != 0;
+        const uint32_t v_base = smem_u32(smem + st * kStageBytes) + part * 2 * kLatBox;
+        const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          mma_f8_ss_if(leader, t_o, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
+                       (first && kk == 0) ? 0u : 1u);
+        tc_commit_if(leader, &bars->pv_done);
+        tc_commit_if(leader, &bars->kv_empty[st]);
+        ++j;
+        return true;
+      };
+      while (ok && walk.next(sg)) {
+        // The previous segment's last P.V comes first: the softmax warps write
+        // its P before they copy this segment's Q.
+        while (ok && j < i) ok = issue_pv();
+        // the softmax warps have copied the Q slots (and the converter has seen them)
+        bool qok = ok && warp_wait(&bars->q_full, seg & 1, abort_flag, __LINE__);
+        for (int q = 0; q < 3 && qok; ++q)
+          qok = warp_wait(&bars->cvt_ready[(k + q) % kStages], ((k + q) / kStages) & 1, abort_flag, __LINE__);
+        if (!qok) {
+          ok = false;
+          break;
+        }
+        if (leader)
+          for (int q = 0; q < 3; ++q) mbar_arrive(&bars->kv_empty[(k + q) % kStages]);
+        __syncwarp();
+        k += 3;
+        // Page i's conversion is waited for while the P.V of page i - 2 runs (so
+        // that Q.K^T(i) follows that P.V in the tensor pipe without a gap).  S
+        // buffer i % 2 last held page i - 2, whose P (written after its S was
+        // read) that P.V waited for -- or the previous segment's flush did.
+        if (!warp_spin(&bars->cvt_ready[k % kStages], (k / kStages) & 1, abort_flag, __LINE__)) {
+          ok = false;
+          break;
+        }
+        for (int pg = sg.lo; pg < sg.hi; ++pg, ++i, ++k) {
+          const int st = k % kStages;
+          const int sbuf = i & 1;
+          tc_fence_after();
+          const uint32_t t_s = tmem + kTS + sbuf * kPage;
+          const uint64_t kd = make_sdesc(smem_u32(smem + st * kStageBytes), 16, 1024, SWIZZLE_128B);
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)
+            mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4),
+                         idesc8, kk > 0 ? 1u : 0u);
+          const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + sbuf * kCvtBytes), 16, 1024, SWIZZLE_128B);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ss_if(leader, t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
+          tc_commit_if(leader, &bars->s_full[sbuf]);
+          const uint32_t e = static_cast<uint32_t>(st) | ((pg == sg.lo) ? 8u : 0u);
+          pend = (pend & ~(0xFFu << (8 * (i & 3)))) | (e << (8 * (i & 3)));
+          // the P.V of the previous page (queued right behind this Q.K^T), then
+          // the next page's conversion while that P.V runs
+          if (pg > sg.lo && !issue_pv()) {  // j == i - 1 here
+            ok = false;
+            break;
+          }
+          if (pg + 1 < sg.hi &&
+              !warp_spin(&bars->cvt_ready[(k + 1) % kStages], ((k + 1) / kStages) & 1, abort_flag, __LINE__)) {
+            ok = false;
+            break;
+          }
+        }
+        ++seg;
       }
-      cp_async_wait_all();
-      named_bar_sync(1, 64);
-      if (t == 0) mbar_arrive(&bars->ptab_ready);
+      while (ok && j < i) ok = issue_pv();  // the last P.V
+      if (leader) tc_commit(&bars->final_mma);
+      __syncwarp();
+      warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
     }
-    BlockCursor bc(prm, unit);
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------- RoPE conversion, tail zeroing (64 threads) ----
+    const int t = threadIdx.x - 64;  // token row of the page
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int k = 0, i = 0;  // ring slots, pages
     bool ok = true;
-    int n = 0;  // K slices waited for
-    while (ok && bc.next()) {
-      if ((bc.h & 1) != irank) continue;
-      const int j = n / 3;
-      const int st = (n + 2) % kKSlices;
+    while (ok && walk.next(sg)) {
+      // the Q slots need no conversion, but their fills are waited for and
+      // acknowledged like the pages' so that each stage phase is seen in turn
       if (t == 0) {
-        bool good = true;
-        for (int s3 = 0; s3 < 3 && good; ++s3)
-          good = wait_bounded(&bars->k_full[(n + s3) % kKSlices], ((n + s3) / kKSlices) & 1, abort_flag,
-                              &g_status_mla, __LINE__);
-        bars->cvt_ok = good ? 1u : 0u;
+        bool filled = true;
+        for (int q = 0; q < 3 && filled; ++q)
+          filled = wait_bounded(&bars->kv_full[(k + q) % kStages], ((k + q) / kStages) & 1, abort_flag,
+                                &g_status_mla, __LINE__);
+        if (filled)
+          for (int q = 0; q < 3; ++q) mbar_arrive(&bars->cvt_ready[(k + q) % kStages]);
+        bars->cvt_ok = filled ? 1u : 0u;
       }
-      n += 3;
       named_bar_sync(1, 64);
-      if (!bars->cvt_ok) {
-        ok = false;
-        break;
-      }
-      uint8_t* kb = smem + kOffK + st * kSliceBytes;
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      uint4 raw[kBlkPages][4];
-#pragma unroll
-      for (int i = 0; i < kBlkPages; ++i) {
-        const bool dead = i >= bc.npg || (bc.pg + i == bc.sg.n - 1 && t >= bc.sg.s_k - (bc.pg + i) * kPage);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          raw[i][c] = dead ? z : reinterpret_cast<const uint4*>(kb + i * kLatBox + kRopeRaw + t * 64)[c];
-      }
-      named_bar_sync(1, 64);  // every raw row is read before the f16 rows overwrite them
-      const int sw = t & 7;
-#pragma unroll
-      for (int i = 0; i < kBlkPages; ++i) {
-        if (i >= bc.npg) break;
-        uint8_t* dst = kb + i * kLatBox + t * 128;
+      if (!bars->cvt_ok) break;
+      named_bar_sync(1, 64);  // cvt_ok is rewritten below
+      k += 3;
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++k, ++i) {
+        const int st = k % kStages;
+        const int use = k / kStages;
+        // conversion buffer i % 2 is free once the Q.K^T of page i - 2 completed
+        if (t == 0)
+          bars->cvt_ok = (wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla, __LINE__) &&
+                          (i < 2 || wait_bounded(&bars->s_full[i & 1], ((i - 2) >> 1) & 1, abort_flag, &g_status_mla, __LINE__)))
+                             ? 1u
+                             : 0u;
+        named_bar_sync(1, 64);
+        if (!bars->cvt_ok) {
+          ok = false;
+          break;
+        }
+        uint8_t* sb = smem + st * kStageBytes;
+        const bool dead = (pg == sg.n - 1) && (t >= sg.s_k - pg * kPage);  // slot past the sequence end
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        const int sw = t & 7;
+        const uint4* src = reinterpret_cast<const uint4*>(sb + kOffRope8 + t * 64);
+        uint8_t* dst = smem + kOffCvt + (i & 1) * kCvtBytes + t * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint4 v = raw[i][c];
-          uint4 lo, hi;
-          lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
-          lo.y = e4m3x2_to_f16x2(v.x >> 16);
-          lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
-          lo.w = e4m3x2_to_f16x2(v.y >> 16);
-          hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
-          hi.y = e4m3x2_to_f16x2(v.z >> 16);
-          hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
-          hi.w = e4m3x2_to_f16x2(v.w >> 16);
+          uint4 lo = z, hi = z;
+          if (!dead) {
+            const uint4 v = src[c];
+            lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
+            lo.y = e4m3x2_to_f16x2(v.x >> 16);
+            lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
+            lo.w = e4m3x2_to_f16x2(v.y >> 16);
+            hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
+            hi.y = e4m3x2_to_f16x2(v.z >> 16);
+            hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
+            hi.w = e4m3x2_to_f16x2(v.w >> 16);
+          }
           *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
           *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
         }
+        if (dead) {  // zero the slot's V row (all four 128-byte slices)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4* row = reinterpret_cast<uint4*>(sb + j * kLatBox + t * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) row[c] = z;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 64);
+        if (t == 0) mbar_arrive(&bars->cvt_ready[st]);
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 64);
-      if (t == 0) mbar_arrive(&bars->k_cvt[j & 1]);
     }
-    if (!ok && t == 0) fail();
   } else {
     // ------------------ softmax / Q copy / epilogue (8 warps, 2 per row) ----
-    const int hf = (warp - 4) / 4;         // which half of the row (keys [64 hf, 64 hf + 64) of a block)
+    const int hf = (warp - 4) / 4;         // which half of the row
     const int r = (warp % 4) * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const float kv_scale = *prm.kv_scale;
@@ -1288,270 +1088,110 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
       ++xphase;
       return ok;
     };
-    const uint32_t r_lx = remote(&bars->lx[0][r]);
-    const uint32_t r_prx = remote(&bars->p_rx);
-    const uint32_t r_lxfull0 = remote(&bars->lx_full[0]);
-    const uint32_t r_pt = remote(smem + kOffP + rank * kPTile);  // this CTA's message in the other CTA
-    const uint32_t prow = static_cast<uint32_t>((r >> 3) * kPSbo + (r & 7) * 16);
-    // Sends the 32 values v of this warp's rows (rows 32 (warp % 4) .. + 31) to
-    // the other CTA at cluster address dst and arrives on its barrier rbar:
-    // lane 0 gathers them and stores them itself, so that its release covers
-    // every value (other lanes' remote stores would not be ordered by it).
-    auto send_rows = [&](uint32_t dst, float v, uint32_t rbar) {
-      uint4 w[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        w[i].x = __float_as_uint(__shfl_sync(0xffffffffu, v, 4 * i));
-        w[i].y = __float_as_uint(__shfl_sync(0xffffffffu, v, 4 * i + 1));
-        w[i].z = __float_as_uint(__shfl_sync(0xffffffffu, v, 4 * i + 2));
-        w[i].w = __float_as_uint(__shfl_sync(0xffffffffu, v, 4 * i + 3));
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) st_cluster_v4(dst + 16 * i, w[i]);
-        mbar_arrive_cluster(rbar, 1);
-      }
-    };
-
-    // Copies this half of sequence b_seq's quantised Q row (prepared by
-    // mla_qprep_kernel) in: latent bytes [256 hf, +256) into TMEM columns
-    // kTQ + 64 hf.., RoPE values [32 hf, +32) into the Q RoPE tile.
-    int qn = 0;
-    float qs_cur = 1.f;
-    auto copy_q = [&](int b_seq) -> bool {
-      const uint8_t* qb = prm.qbuf + static_cast<size_t>(b_seq) * kMlaQBytes;
-      const uint4* lat = reinterpret_cast<const uint4*>(qb + hf * f8::kQLatSlotBytes + r * f8::kQLatPitch);
-      const uint4* rope = reinterpret_cast<const uint4*>(qb + 2 * f8::kQLatSlotBytes + r * f8::kQRopePitch + hf * 64);
-      uint4 v[16], w[4];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) v[c] = __ldg(lat + c);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) w[c] = __ldg(rope + c);
-      qs_cur = __ldg(prm.qscale + static_cast<size_t>(b_seq) * kRows + r);
+    // Copies this half of the Q row of the segment whose Q slots start at ring
+    // slot kq: latent bytes [256 hf, +256) into TMEM columns kTQ + 64 hf..,
+    // RoPE values [32 hf, +32) into the shared Q RoPE tile (128-byte swizzle).
+    auto copy_q = [&](int kq, int b_seq, float& qs_out) -> bool {
+      const int st = (kq + hf) % kStages, use = (kq + hf) / kStages;
+      const int st_r = (kq + 2) % kStages, use_r = (kq + 2) / kStages;
+      if (!warp_wait(&bars->kv_full[st], use & 1, abort_flag, __LINE__) ||
+          !warp_wait(&bars->kv_full[st_r], use_r & 1, abort_flag, __LINE__))
+        return false;
+      const uint4* lat = reinterpret_cast<const uint4*>(smem + st * kStageBytes + r * kQLatPitch);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          pk[4 * c + 0] = v[4 * ch + c].x;
-          pk[4 * c + 1] = v[4 * ch + c].y;
-          pk[4 * c + 2] = v[4 * ch + c].z;
-          pk[4 * c + 3] = v[4 * ch + c].w;
+          const uint4 v = lat[4 * ch + c];
+          pk[4 * c + 0] = v.x;
+          pk[4 * c + 1] = v.y;
+          pk[4 * c + 2] = v.z;
+          pk[4 * c + 3] = v.w;
         }
         tmem_st16(lane_base + kTQ + (4 * hf + ch) * 16, pk);
       }
-      uint8_t* dst = smem + kOffQRope + r * 128;
+      {
+        const uint4* rope = reinterpret_cast<const uint4*>(smem + st_r * kStageBytes + r * kQRopePitch);
+        uint8_t* dst = smem + kOffQRope + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(dst + (((4 * hf + c) ^ (r & 7)) << 4)) = w[c];
-      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs
+        for (int c = 4 * hf; c < 4 * hf + 4; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = rope[c];
+      }
+      qs_out = prm.qscale[static_cast<size_t>(b_seq) * kRows + r];
+      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs, the slots refilled by TMA
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bars->q_full);
-      ++qn;
       return true;
     };
-    // true if some segment after the cursor's holds a block of this CTA; its sequence in *b_out
-    auto next_q_segment = [&](const BlockCursor& at, int* b_out) -> bool {
-      SegmentWalker peek = at.walk;
+
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int i = 0, k = 0, seg = 0;
+    float qs_next = 1.f;
+    bool ok = walk.next(sg) && copy_q(0, sg.b, qs_next);
+    while (ok) {
+      const float qs = qs_next;
+      const float c_row = prm.softmax_scale * kLog2e * qs * kv_scale;
+      SegmentWalker peek = walk;
       Segment nx;
-      int h0 = at.h + (at.sg.hi - at.pg + 1) / 2;  // unit index of the next segment's first block
-      while (peek.next(nx)) {
-        const int nb = (nx.hi - nx.lo + 1) / 2;
-        if (nb >= 2 || (h0 & 1) == irank) {
-          *b_out = nx.b;
-          return true;
-        }
-        h0 += nb;
-      }
-      return false;
-    };
-
-    BlockCursor pc(prm, unit);
-    bool ok = true;
-    int cur_seg = -1;
-    float m_run = kNegInf, l_run = 0.f;  // reference of O and l; this CTA's share of l
-    float m_own = kNegInf;                // this CTA's latest reference in the segment
-    int pend = -1;  // the other CTA's block whose rescale / O-ready is still due
-    bool pend_first = false;
-    int qtok = 0, visible = 0;
-    float c_row = 0.f;
-
-    // Moves O and l to a new reference before a block's P.V: both are
-    // multiplied by 2^(m_run - m_new) once the P.V of block h - 1 completed.
-    // A reference of -inf (the row sees no key of the block, so its P is 0)
-    // leaves them where they are, in both CTAs alike.
-    auto rescale_to = [&](int h, float m_new, bool first) -> bool {
-      const bool rescale = !first && m_new != m_run && m_new != kNegInf;
-      const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.f;
-      l_run = first ? 0.f : l_run * alpha;
-      if (first || rescale) m_run = m_new;
-      if (__any_sync(0xffffffffu, rescale)) {
-        if (!warp_spin(&bars->pv_done[(h - 1) & 1], ((h - 1) >> 1) & 1, abort_flag, __LINE__)) return false;
-        tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < kOHalf / 32; ++ch) {
-          const uint32_t col = kTO + hf * kOHalf + ch * 32;
-          uint32_t o[32];
-          tmem_ld32(lane_base + col, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st32(lane_base + col, o);
-        }
-        tmem_st_wait();
-      }
-      return true;
-    };
-    // The other CTA's block h: wait for its P message, take the reference it
-    // carries (kept for this CTA's block h + 3), rescale O and l to it, and
-    // declare O ready for the block's P.V.
-    float m_o_last = kNegInf, m_o_prev = kNegInf;  // the other CTA's last two references in this segment
-    int h_o_last = -4;                             // the block of m_o_last
-    auto finish_other = [&](int h, bool first) -> bool {
-      const int k = h >> 1;  // the other CTA's k-th block: message k
-      if (!warp_spin(&bars->p_rx, k & 1, abort_flag, __LINE__)) return false;
-      fence_proxy_async_smem();  // the remotely stored P is read by this CTA's P.V
-      // (every softmax thread has passed this phase before the next message's
-      // bytes can come: they follow this block's P.V here)
-      if (warp == 4 && lane == 0) mbar_arrive_expect_tx(&bars->p_rx, kPTile);
-      const float m_new = reinterpret_cast<const float*>(smem + kOffP + (h & 1) * kPTile + kPBytes)[r];
-      m_o_prev = m_o_last;
-      m_o_last = m_new;
-      h_o_last = h;
-      if (!rescale_to(h, m_new, first)) return false;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[h & 1]);
-      return true;
-    };
-
-    // Q of the first segment holding a block of this CTA
-    {
-      BlockCursor probe(prm, unit);
-      if (probe.next()) {
-        int bq = probe.sg.b;
-        const int nb = (probe.sg.hi - probe.sg.lo + 1) / 2;
-        bool have = nb >= 2 || (probe.h & 1) == irank;
-        if (!have) have = next_q_segment(probe, &bq);
-        if (have) ok = copy_q(bq);
-      }
-    }
-
-    while (ok && pc.next()) {
-      const int h = pc.h;
-      if (pc.seg != cur_seg) {  // a new segment
-        cur_seg = pc.seg;
-        m_run = kNegInf;
-        l_run = 0.f;
-        m_own = kNegInf;
-        m_o_last = m_o_prev = kNegInf;
-        h_o_last = -4;
-        qtok = (r < R) ? r / prm.h_q : 0;
-        visible = prm.causal ? (pc.sg.s_k - prm.s_q + qtok + 1) : pc.sg.s_k;
-        if (r < R && pc.first()) {  // warm L2 with the Q of the segment after this one
-          int bn;
-          if (next_q_segment(pc, &bn)) {
-            const char* nq = reinterpret_cast<const char*>(prm.qbuf + static_cast<size_t>(bn) * kMlaQBytes);
-            prefetch_l2(nq + hf * f8::kQLatSlotBytes + r * f8::kQLatPitch);
-            prefetch_l2(nq + hf * f8::kQLatSlotBytes + r * f8::kQLatPitch + 128);
-          }
-        }
-      }
-      const bool mine = (h & 1) == irank;
-      if (!mine) {
-        pend = h;
-        pend_first = pc.first();
-      } else {
-        const int j = h >> 1;
-        c_row = prm.softmax_scale * kLog2e * qs_cur * kv_scale;
-        // wait for S; the other CTA's block before this one is finished meanwhile
-        // if its message lands first (its P.V need not wait for this block's P)
-        {
-          uint32_t polls = 0;
-          uint64_t t_idle = 0;
-          while (ok) {
-            if (pend >= 0 && __shfl_sync(0xffffffffu, mbar_test_wait(&bars->p_rx, (pend >> 1) & 1) ? 1 : 0, 0)) {
-              ok = finish_other(pend, pend_first);
-              pend = -1;
-              polls = 0;
-              continue;
-            }
-            if (__shfl_sync(0xffffffffu, mbar_test_wait(&bars->s_full, j & 1) ? 1 : 0, 0)) break;
-            if ((++polls & 63u) == 0) {
-              if (*abort_flag) ok = false;
-              if (polls == 64) t_idle = globaltimer_ns();
-              if (ok && polls > kWaitMinPolls && globaltimer_ns() - t_idle > *(volatile uint64_t*)&g_wait_limit_ns) {
-                if (lane == 0) {
-                  atomicOr(&g_status_mla, FP8MLA_DEV_WAIT_TIMEOUT);
-                  record_timeout_site(__LINE__);
-                }
-                ok = false;
-              }
-              ok = __all_sync(0xffffffffu, ok);
-            }
-          }
-          if (!ok || !warp_spin(&bars->s_full, j & 1, abort_flag, __LINE__)) {
-            ok = false;
-            break;
-          }
+      const bool has_next = peek.next(nx);
+      const int k_next = k + 3 + (sg.hi - sg.lo);
+      const int col0 = part * 256 + hf * kOHalf;  // this thread's O columns
+      // keys visible to this row (bottom-right causal alignment); pages wholly
+      // below every row's limit need no mask
+      const int qtok = (r < R) ? r / prm.h_q : 0;
+      const int visible = prm.causal ? (sg.s_k - prm.s_q + qtok + 1) : sg.s_k;
+      const int min_visible = prm.causal ? (sg.s_k - prm.s_q + 1) : sg.s_k;
+      float m_run = kNegInf, l_run = 0.f;  // l_run sums the stored-scale p (kPScale p)
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+        const int sbuf = i & 1;
+        if (!warp_spin(&bars->s_full[sbuf], (i >> 1) & 1, abort_flag, __LINE__)) {
+          ok = false;
+          break;
         }
         tc_fence_after();
-        uint32_t s[32], s2[32];  // keys [64 hf, +32) and [64 hf + 32, +32) of the block
-        tmem_ld32(lane_base + kTS + 64 * hf, s);
-        tmem_ld32(lane_base + kTS + 64 * hf + 32, s2);
+        // Both halves of the row are read: the other half only for the row max,
+        // so each warp takes the max of all 64 keys without waiting on its partner.
+        uint32_t s[32], so[32];
+        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * hf, s);
+        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * (1 - hf), so);
         tmem_ld_wait();
-        tc_fence_before();
-        warp_arrive(&bars->s_free);  // own block j + 1's Q.K^T may overwrite S
-        // keys past the row's causal limit or past the segment's pages
-        const int key0 = pc.pg * kPage + 64 * hf;
-        const int lim = min(visible, (pc.pg + pc.npg) * kPage);
-        if (key0 + 64 > lim) {
+
+        if (pg * kPage + kPage > min_visible) {
+          const int base = pg * kPage + 32 * hf, base_o = pg * kPage + 32 * (1 - hf);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            if (key0 + c >= lim) s[c] = __float_as_uint(kNegInf);
-            if (key0 + 32 + c >= lim) s2[c] = __float_as_uint(kNegInf);
+            if (base + c >= visible) s[c] = __float_as_uint(kNegInf);
+            if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
           }
         }
+        // row max of the 64 scores as a tree of three-way maxima
         float m22[22];
 #pragma unroll
         for (int c = 0; c < 10; ++c) {
           m22[c] = fmax3(__uint_as_float(s[3 * c]), __uint_as_float(s[3 * c + 1]), __uint_as_float(s[3 * c + 2]));
           m22[10 + c] =
-              fmax3(__uint_as_float(s2[3 * c]), __uint_as_float(s2[3 * c + 1]), __uint_as_float(s2[3 * c + 2]));
+              fmax3(__uint_as_float(so[3 * c]), __uint_as_float(so[3 * c + 1]), __uint_as_float(so[3 * c + 2]));
         }
         m22[20] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
-        m22[21] = fmaxf(__uint_as_float(s2[30]), __uint_as_float(s2[31]));
+        m22[21] = fmaxf(__uint_as_float(so[30]), __uint_as_float(so[31]));
         float m8[8];
 #pragma unroll
         for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
         m8[7] = m22[21];
-        const float mhalf =
-            fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
-        // the row's maximum: this half's, and the other half's from its thread (warp warp +- 4)
-        bars->rmax[j & 1][hf][r] = mhalf;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->rmax_full[warp % 4]);
-        if (!warp_spin(&bars->rmax_full[warp % 4], j & 1, abort_flag, __LINE__)) {
-          ok = false;
-          break;
+        const float m3a = fmax3(m8[0], m8[1], m8[2]), m3b = fmax3(m8[3], m8[4], m8[5]);
+        const float mx = fmax3(m3a, m3b, fmaxf(m8[6], m8[7])) * c_row;  // c_row > 0; both warps agree
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_run + kTau) {
+          alpha = ex2_approx(m_run - mx);
+          rescale = (pg != sg.lo);
+          m_run = mx;
         }
-        const float mx = fmaxf(mhalf, bars->rmax[j & 1][1 - hf][r]);
-        // this CTA's message is free once both CTAs' P.V of its block h - 2 completed
-        if (h >= 2 && !(warp_spin(&bars->pv_done[h & 1], ((h - 2) >> 1) & 1, abort_flag, __LINE__) &&
-                        warp_spin(&bars->px_done, ((h - 2) >> 1) & 1, abort_flag, __LINE__))) {
-          ok = false;
-          break;
-        }
-        // the reference: this CTA's and the other's latest ones (blocks h - 2 and h - 3),
-        // raised to this block's maximum when that exceeds them by more than kTau
-        const bool first = pc.first();
-        const float m_other = (h_o_last == h - 1) ? m_o_prev : m_o_last;  // block h - 3's
-        const float m_known = fmaxf(m_own, m_other);
-        const float m_new = (mx > m_known + kTau) ? mx : m_known;
-        m_own = m_new;
-        const float bias = (m_new == kNegInf) ? 0.f : (kPLog2 - m_new);
+        const float bias = (m_run == kNegInf) ? 0.f : (kPLog2 - m_run);
         float sum = 0.f;
-        uint32_t pk[16];
+        uint32_t pk[8];
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
@@ -1561,133 +1201,93 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
           sum += (p0 + p1) + (p2 + p3);
           pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
         }
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s2[c]), c_row, bias));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s2[c + 1]), c_row, bias));
-          const float p2 = ex2_approx(fmaf(__uint_as_float(s2[c + 2]), c_row, bias));
-          const float p3 = ex2_approx(fmaf(__uint_as_float(s2[c + 3]), c_row, bias));
-          sum += (p0 + p1) + (p2 + p3);
-          pk[8 + c / 4] = pack_e4m3x4(p0, p1, p2, p3);
-        }
-        {  // this thread's 64 keys of row r (16-byte chunks 4 hf .. 4 hf + 3), and the row's reference,
-           // here and (asynchronously, counted on its p_rx barrier) in the other CTA
-          uint8_t* lp = smem + kOffP + rank * kPTile + prow;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 v = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            *reinterpret_cast<uint4*>(lp + (4 * hf + q) * kPLbo) = v;
-            st_async_v4(r_pt + prow + (4 * hf + q) * kPLbo, v, r_prx);
-          }
-          if (hf == 0) {
-            reinterpret_cast<float*>(smem + kOffP + rank * kPTile + kPBytes)[r] = m_new;
-            st_async_f32(r_pt + kPBytes + r * 4, m_new, r_prx);
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        // the other CTA's previous block: O moves to its reference and is declared
-        // ready for its P.V before this block's rescale
-        if (pend >= 0) {
-          if (!finish_other(pend, pend_first)) {
-            ok = false;
-            break;
-          }
-          pend = -1;
-        }
-        if (!rescale_to(h, m_new, first)) {
+        l_run = l_run * alpha + sum;
+
+        // P has one tile and O one accumulator: the previous page's P.V must
+        // have completed before either is touched
+        if (i >= 1 && !warp_spin(&bars->pv_done, (i - 1) & 1, abort_flag, __LINE__)) {
           ok = false;
           break;
         }
-        l_run += sum;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+          for (int ch = 0; ch < kOHalf / 32; ++ch) {
+            const uint32_t col = kTO + hf * kOHalf + ch * 32;
+            uint32_t o[32];
+            tmem_ld32(lane_base + col, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+            tmem_st32(lane_base + col, o);
+          }
+          tmem_st_wait();
+        }
+        {  // this warp's 32 keys of row r: 16-byte chunks 2 hf and 2 hf + 1
+          uint8_t* prow = smem + kOffP + (r >> 3) * kPSbo + (r & 7) * 16;
+          *reinterpret_cast<uint4*>(prow + (2 * hf) * kPLbo) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(prow + (2 * hf + 1) * kPLbo) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        fence_proxy_async_smem();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full[h & 1]);  // P written and O rescaled here
-        // this CTA's last block of the segment: the next segment's Q may replace this one's
-        const bool last_own = pc.last() || (pc.sg.hi - pc.pg <= 2 * kBlkPages);
-        if (last_own) {
-          int bn;
-          if (next_q_segment(pc, &bn)) ok = copy_q(bn);
+        warp_arrive(&bars->p_full);
+        // the segment's last Q.K^T is done: the next segment's Q may replace it now
+        if (pg == sg.hi - 1 && has_next && !copy_q(k_next, nx.b, qs_next)) {
+          ok = false;
+          break;
         }
       }
       if (!ok) break;
-      if (!pc.last()) continue;
 
-      // ---- segment end ----
-      if (pend >= 0) {
-        if (!finish_other(pend, pend_first)) {
-          ok = false;
-          break;
-        }
-        pend = -1;
-      }
-      // row sum: this CTA's two halves, then the other CTA's
-      const int sp = cur_seg & 1;
-      bars->xsum[sp][hf][r] = l_run;
-      if (!xsync()) {
-        ok = false;
-        break;
-      }
-      const float l_here = bars->xsum[sp][0][r] + bars->xsum[sp][1][r];
-      // one barrier per slot: the other CTA may finish the next segment before this one reads this slot
-      if (hf == 0) send_rows(r_lx - lane * 4 + sp * kRows * 4, l_here, r_lxfull0 + sp * 8);
-      if (!warp_wait<true>(&bars->lx_full[sp], (cur_seg >> 1) & 1, abort_flag, __LINE__)) {
-        ok = false;
-        break;
-      }
-      const float l_tot = (l_here + bars->lx[sp][r]) * (1.0f / kPScale);  // sum of p
-      const bool whole = (pc.sg.lo == 0 && pc.sg.hi == pc.sg.n);
+      // ---- epilogue: O is final once the segment's last P.V completes ----
+      bars->xsum[hf][r] = l_run;
+      if (!xsync()) break;
+      const float l_tot = (bars->xsum[0][r] + bars->xsum[1][r]) * (1.0f / kPScale);  // sum of p
+      const bool whole = (sg.lo == 0 && sg.hi == sg.n);
       const float o_scale = kv_scale / kPScale;  // tensor-core units -> true units
       const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
-      const int slot = whole ? 0 : prm.num_splits[pc.sg.b] + pc.sg.split;
-      // O is final once this CTA's P.V of the segment's last block completed
-      if (!warp_wait(&bars->pv_done[h & 1], (h >> 1) & 1, abort_flag, __LINE__)) {
-        ok = false;
-        break;
-      }
+      const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
+      if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag, __LINE__)) break;
       tc_fence_after();
-      const int col0 = irank * 256 + hf * kOHalf;      // this thread's O columns
+      // O out as bf16, 32 columns at a time.  A thread holds one row; groups of
+      // four lanes transpose their 16-byte pieces so that each store writes
+      // 64-byte runs of rows.  A whole sequence goes straight to out, a piece
+      // to its bf16 partial slot; the combine kernel adds the LSE correction.
       const int grow = (warp % 4) * 32 + (lane & ~3);  // the lane group's first row
-      uint16_t* obase = whole ? prm.out + static_cast<size_t>(pc.sg.b) * R * kDV
+      uint16_t* obase = whole ? prm.out + static_cast<size_t>(sg.b) * R * kDV
                               : prm.ws_o + static_cast<size_t>(slot) * kRows * kDV;
 #pragma unroll 1
       for (int ch = 0; ch < kOHalf / 32; ++ch) {
         uint32_t o[32];
         tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
         tmem_ld_wait();
-        uint4 pcs[4];
+        uint4 pc[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          pcs[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
-          pcs[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
-          pcs[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
-          pcs[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
+          pc[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
+          pc[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
+          pc[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
+          pc[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
         }
-        f8::lane_group_transpose<4>(pcs, lane);
+        lane_group_transpose<4>(pc, lane);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           if (grow + kk < R)
-            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(grow + kk) * kDV + col0 + ch * 32 +
-                                      8 * (lane & 3)) = pcs[kk];
+            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(grow + kk) * kDV + col0 + ch * 32 + 8 * (lane & 3)) =
+                pc[kk];
       }
-      tc_fence_before();  // O is overwritten by the next segment's first P.V after the next p_full
-      if (r < R && rank == 0 && hf == 0) {  // the row's (uncorrected) LSE, or the piece's (m, l)
+      if (r < R && part == 0 && hf == 0) {  // the row's (uncorrected) LSE, or the piece's (m, l)
         if (whole) {
-          prm.lse[static_cast<size_t>(pc.sg.b) * R + r] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
+          prm.lse[static_cast<size_t>(sg.b) * R + r] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
         } else {
           prm.ws_ml[static_cast<size_t>(slot) * kRows + r] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
         }
       }
-    }
-    if (!ok) fail();
-    // The other CTA's P.V commits of this CTA's last blocks arrive in this
-    // CTA's shared memory: they must land before this CTA may exit.
-    if (ok) {
-      int last = -1;  // last own block
-      BlockCursor cnt(prm, unit);
-      while (cnt.next())
-        if ((cnt.h & 1) == irank) last = cnt.h;
-      if (last >= 0) warp_spin(&bars->px_done, (last >> 1) & 1, abort_flag, __LINE__);
+      if (!has_next) break;
+      walk.next(sg);
+      k = k_next;
+      ++seg;
     }
   }
 
@@ -1697,34 +1297,18 @@ __global__ void __launch_bounds__(pr::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  // no CTA leaves while the other may still write to its shared memory
-  cluster_arrive();
-  cluster_wait();
 }
 
 cudaError_t launch_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
                        cudaStream_t stream) {
   static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
   const cudaError_t e = configure_once(configured, [] {
-    return cudaFuncSetAttribute(mla_fp8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(pr::smem_bytes()));
+    return cudaFuncSetAttribute(mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(f8::smem_bytes()));
   });
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_units * 2);
-  cfg.blockDim = dim3(pr::kThreads);
-  cfg.dynamicSmemBytes = pr::smem_bytes();
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = 2;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, mla_fp8_pair_kernel, tm_lat, tm_rope, prm);
+  return launch_dependent(mla_fp8_kernel, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream, tm_lat,
+                          tm_rope, prm);
 }
 
 cudaError_t launch_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
@@ -1754,6 +1338,13 @@ cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap
 cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream) {
   if (prm.b == 0) return cudaSuccess;
   return launch_dependent(mla::f8::mla_qprep_kernel, dim3(prm.b, mla::kRows / 32), dim3(256), 0, stream, prm);
+}
+
+cudaError_t mla_set_wait_test(int fault_page, uint64_t wait_limit_ns) {
+  const uint64_t limit = wait_limit_ns ? wait_limit_ns : kWaitLimitNs;
+  cudaError_t e = cudaMemcpyToSymbol(mla::f8::g_fault_page, &fault_page, sizeof(fault_page));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_wait_limit_ns, &limit, sizeof(limit));
+  return e;
 }
 
 void mla_read_and_clear_timeout_site(uint32_t where[3]) {

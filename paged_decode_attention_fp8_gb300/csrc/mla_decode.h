@@ -50,6 +50,10 @@ uint32_t mla_read_and_clear_status();
 // {source line, block, thread} of the first bounded wait of the dense MLA kernels that ran
 // out since the last call (all 0 if none), and clears it.
 void mla_read_and_clear_timeout_site(uint32_t where[3]);
+// Test hook of the bounded waits of the FP8-dots MLA kernel on the current device:
+// fault_page = p + 1 makes CTA 0 of work unit 0 skip the loads of its p-th page
+// (0 = off); wait_limit_ns replaces the wait limit (0 = the default).
+cudaError_t mla_set_wait_test(int fault_page, uint64_t wait_limit_ns);
 // Quantises every sequence's Q rows for FP8 dots into prm.qbuf / prm.qscale
 // (launched right before launch_mla_decode_fp8, as a programmatic dependent).
 cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream);
