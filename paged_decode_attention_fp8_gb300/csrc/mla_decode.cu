@@ -603,119 +603,65 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
 // ===========================================================================
 // FP8-dots kernel.
 //
-// Work unit = 2 CTAs, each owning one 256-wide dv slice [256 part, +256).
-// Both walk the unit's pages two at a time: block h is pages 2i and 2i + 1 of
-// a segment, or its last page alone.  Each CTA computes the block's scores
-// S = Q K^T as one 128-row x 128-key tile and its probabilities P itself (the
-// two CTAs of a unit compute the same S and P; a tcgen05 MMA with M = 128
-// costs nearly the same for any N up to 256, so the 128-key tiles take half
-// the tensor time per key of 64-key ones), then multiplies P by its dv slice
-// of the block's V.
-//
-// TMEM: O slice (256 columns), S (128), Q latent (128, E4M3).  Shared memory:
-// a V ring with this CTA's latent half of each block (3 x 32 KB, released by
-// the block's P.V; Q.K^T reads it too), a ring of five 16 KB K slices (per
-// block three: the other latent half's two 128-byte boxes, then the RoPE
-// part, converted to f16 in place; each released when its Q.K^T step
-// completes; five keep the next block's slices and part of the one after in
-// flight, since a slice takes over a microsecond to land),
-// Q's RoPE part (f16), P (128 rows x 128 E4M3 keys) and the unit's first
-// block-table entries.
+// Work unit = 2 CTAs, each owning one 256-wide dv slice.  The shared-memory
+// ring of 5 stages carries, in one order that every role walks, three Q slots
+// at the start of each segment (the segment's quantised Q: two latent halves
+// and the RoPE part) followed by the segment's KV pages, so no separate Q
+// buffer competes with the KV pages for shared memory.  TMEM: O 256 + two S
+// buffers of 64 + Q latent 128 columns.
 // ===========================================================================
 namespace f8 {
+constexpr int kStages = 5;
+// Test hook of the bounded waits (0 = off); set by mla_set_wait_test.
+__device__ int g_fault_page = 0;
 constexpr int kThreads = 384;
-constexpr int kBlkPages = 2;
-constexpr int kBlkKeys = kBlkPages * kPage;   // keys of a full block (N of its Q.K^T)
-constexpr int kVStages = 3;
-constexpr int kKSlices = 5;
-constexpr int kBoxBlk = kBlkPages * kLatBox;  // one 128-byte column box of a block: page 0 rows, then page 1 rows
-constexpr int kVBytes = 2 * kBoxBlk;          // latent bytes [256 part, 256 part + 256) of a block
-constexpr int kSliceBytes = kBoxBlk;
-constexpr int kRopeRaw = kPage * 64;          // in a page's 8 KB of a RoPE slice: where its E4M3 bytes land
-constexpr int kOffV = 0;
-constexpr int kOffK = kOffV + kVStages * kVBytes;
-constexpr int kOffQRope = kOffK + kKSlices * kSliceBytes;  // Q RoPE, 128 rows x 64 f16, 128-byte swizzle
+constexpr int kOffRope8 = 4 * kLatBox;             // 64 tokens x 64 E4M3 RoPE bytes, no swizzle
+constexpr int kStageBytes = kOffRope8 + kPage * 64;
+// Shared memory after the ring: two buffers for a page's RoPE part as f16
+// (64 keys x 128 B, 128-byte swizzle), Q's RoPE part (128 rows x 128 B f16,
+// 128-byte swizzle), and P (128 rows x 64 E4M3 keys) as 8-row x 16-byte core
+// matrices: row group g and 16-byte key chunk c at g * kPSbo + c * kPLbo.
+constexpr int kCvtBytes = kLatBox;
+constexpr int kOffCvt = kStages * kStageBytes;
+constexpr int kOffQRope = kOffCvt + 2 * kCvtBytes;
 constexpr int kOffP = kOffQRope + kRows * 128;
-constexpr int kPBytes = kRows * kBlkKeys;  // P: 128 rows x 128 E4M3 keys
-constexpr int kOffPtab = kOffP + kPBytes;  // the unit's first kPtabMax block-table entries
-constexpr int kPtabMax = 2048;
-constexpr int kSmemData = kOffPtab + kPtabMax * 4;
-// P: 8-row x 16-byte core matrices, key chunk c of row group G at c * kPLbo + G * kPSbo, so the 32
-// rows x 16 bytes that one warp writes per key chunk are one contiguous 512-byte piece
-constexpr int kPLbo = 2048, kPSbo = 128;
+constexpr int kPLbo = 128, kPSbo = 512;
+constexpr int kSmemData = kOffP + kRows * kPage;
 constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
-constexpr float kTau = 2.75f;                    // 64 * 2^2.75 = 430.5 < 448
-// TMEM columns: O slice, S, Q latent (E4M3, the A operand of the latent Q.K^T)
+constexpr float kTau = 2.75f;                     // 64 * 2^2.75 = 430.5 < 448
+// TMEM columns: O slice, two S buffers (pages alternate), Q latent (E4M3).
 constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
-static_assert(kVBytes % 1024 == 0 && kOffK % 1024 == 0 && kSliceBytes % 1024 == 0 && kOffQRope % 1024 == 0 &&
-                  kOffP % 1024 == 0,
-              "1 KB aligned tiles");
-// Quantised Q of a sequence (written by mla_qprep_kernel): per row latent bytes
-// [256 h, 256 h + 256) at a 272-byte pitch for h = 0, 1, then the RoPE values as
-// f16 at a 144-byte pitch (pitches chosen so a quarter-warp's 16-byte row
-// accesses hit distinct banks).
+// Quantised Q of a sequence, as three ring slots: slot h (h = 0, 1) holds per
+// row latent bytes [256 h, 256 h + 256) at a 272-byte pitch, slot 2 the RoPE
+// values as f16 at a 144-byte pitch (pitches chosen so a quarter-warp's
+// 16-byte row accesses hit distinct banks).
 constexpr int kQLatPitch = 272;
 constexpr int kQRopePitch = 144;
 constexpr int kQLatSlotBytes = kRows * kQLatPitch;
 constexpr int kQRopeSlotBytes = kRows * kQRopePitch;
+static_assert(kQLatSlotBytes <= kStageBytes && kQRopeSlotBytes <= kStageBytes, "a Q slot fits one stage");
 // After the slots: the latent quantisation error q_hat qs - q, 128 rows x 512
 // bf16, read by the combine kernel for the LSE correction.
 constexpr int kQErrOff = 2 * kQLatSlotBytes + kQRopeSlotBytes;
 static_assert(kQErrOff == kMlaQErrOff && kQErrOff + kRows * kDLat * 2 == kMlaQBytes, "quantised-Q layout");
+static_assert(kStageBytes % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
+              "1 KB aligned tiles");
+static_assert(kStageBytes == static_cast<int>(kPageTxBytes), "a page fills one stage");
 
 struct Bars {
-  uint64_t v_full[kVStages];   // by block h % kVStages: this CTA's latent half of block h loaded
-  uint64_t v_empty[kVStages];  // its P.V (after its Q.K^T) completed
-  uint64_t k_full[kKSlices];   // by slice n % kKSlices (slices 3h, 3h + 1, 3h + 2 of block h) loaded
-  uint64_t k_empty[kKSlices];  // the slice's Q.K^T step completed
-  uint64_t k_cvt[2];           // by block h % 2: its RoPE slice converted to f16
-  uint64_t s_full;             // S holds block h's scores
-  uint64_t s_free;             // S read out (8 softmax warps)
-  uint64_t p_full;             // P written and O rescaled (8 softmax warps)
-  uint64_t pv_done;            // the block's P.V completed
-  uint64_t rmax_full[4];       // by row group: both halves' row maxima written (2 warps)
-  uint64_t q_full;             // a segment's Q copied in (8 softmax warps)
-  uint64_t ptab_ready;         // the block-table entries are in shared memory
-  uint64_t final_mma, xchg;
+  uint64_t kv_full[kStages];    // stage holds its page (TMA bytes) or its Q slot (Q warps' arrival)
+  uint64_t kv_empty[kStages];   // stage may be refilled
+  uint64_t cvt_ready[kStages];  // the page's RoPE part is converted and its dead rows zeroed
+  uint64_t s_full[2];           // S buffer b holds a page's scores
+  uint64_t p_full;              // P written (one arrival per softmax warp)
+  uint64_t pv_done;             // the P.V that read P completed
+  uint64_t q_full, final_mma, xchg;
   uint32_t tmem_base, abort_flag, cvt_ok;
-  float xsum[2][2][kRows];  // by segment parity: row-sum halves of the two softmax threads of a row
-  float rmax[2][2][kRows];  // by block parity: the row maxima of the two halves of a row
+  float xsum[2][kRows];         // row-sum halves
 };
-static_assert(kSmemData % 16 == 0, "the barrier block starts 16-byte aligned");
 
 constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
 static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
-
-// Test hook of the bounded waits (0 = off); set by mla_set_wait_test.
-__device__ int g_fault_page = 0;
-
-// Blocks of a unit one at a time: h counts the unit's blocks across
-// segments, seg its non-empty segments; the block is pages [pg, pg + npg),
-// and u0 + (pg - sg.lo) is the unit's page count before it.
-struct BlockCursor {
-  SegmentWalker walk;
-  Segment sg;
-  int pg = 0, npg = 0, h = -1, seg = -1, u0 = 0;
-  bool valid = false;
-  __device__ BlockCursor(const MlaParams& p, int unit) : walk(p, unit) {}
-  __device__ bool next() {
-    if (valid && pg + npg < sg.hi) {
-      pg += npg;
-    } else {
-      if (valid) u0 += sg.hi - sg.lo;
-      valid = walk.next(sg);
-      if (!valid) return false;
-      pg = sg.lo;
-      ++seg;
-    }
-    npg = min(kBlkPages, sg.hi - pg);
-    ++h;
-    return true;
-  }
-  __device__ bool first() const { return pg == sg.lo; }
-  __device__ bool last() const { return pg + npg == sg.hi; }
-  __device__ int upage() const { return u0 + (pg - sg.lo); }
-};
 
 // Quantises the Q rows of sequence b into the three Q slots: latent -> E4M3(q / qs),
 // RoPE -> f16(q / qs), qs = smallest power of two with amax <= 448 qs.  kTpr
@@ -837,26 +783,18 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int unit = blockIdx.x / 2;
-  const int part = blockIdx.x % 2;  // dv slice [256 part, 256 part + 256); this CTA's latent half
-  const int other = part ^ 1;       // the other latent half (Q.K^T only)
+  const int part = blockIdx.x % 2;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->cvt_ready[s], 1);
     }
-    for (int s = 0; s < kKSlices; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) mbar_init(&bars->k_cvt[b], 1);
-    for (int b = 0; b < 4; ++b) mbar_init(&bars->rmax_full[b], 2);
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, kSoftmaxThreads / 32);
+    for (int b = 0; b < 2; ++b) mbar_init(&bars->s_full[b], 1);
     mbar_init(&bars->p_full, kSoftmaxThreads / 32);
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
-    mbar_init(&bars->ptab_ready, 1);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->xchg, kSoftmaxThreads / 32);
     bars->abort_flag = 0;
@@ -867,7 +805,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     tmem_relinquish();
   }
   // Everything above overlaps the previous kernel (launched as its dependent);
-  // from here on this grid reads the schedule and the quantised Q.
+  // from here on this grid reads the schedule and writes outputs.
   griddep_wait();
   tc_fence_before();
   __syncthreads();
@@ -875,342 +813,269 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
   griddep_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
 
+  // Ring protocol.  Every role walks the same slot sequence: three Q slots at
+  // the start of each segment (its quantised Q, prepared by mla_qprep_kernel)
+  // and then its pages.  Each stage barrier completes one
+  // phase per occupancy of its stage, and every role that waits on one
+  // observes each of its phases in turn, so a parity wait can never pass on a
+  // phase two behind or two ahead: kv_empty is waited by the producer only;
+  // kv_full by the converter for every occupancy, by the MMA warp for pages
+  // and by the softmax warps for Q slots; each stage is released only after
+  // the converter's cvt_ready for that occupancy.
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
-    // Two streams of loads, issued by lane 0 as their stages free up: the V
-    // half of every block (this CTA's latent bytes [256 part, +256) of each
-    // page) and the three K slices of every block (the other latent half's
-    // two boxes, then the RoPE bytes).
+    // The warp loads 32 block-table entries at a time (one per lane); lane 0
+    // issues the loads.
     if (lane == 0) {
       tma_prefetch_desc(&tm_lat);
       tma_prefetch_desc(&tm_rope);
-      // bounded-wait test hook: CTA 0 of unit 0 never loads the block holding its page g_fault_page - 1
-      const int fault = (unit == 0 && part == 0) ? *reinterpret_cast<volatile int*>(&g_fault_page) : 0;
-      auto skipped = [&](const BlockCursor& c) { return fault > c.upage() && fault <= c.upage() + c.npg; };
-      const int32_t* ptab = reinterpret_cast<const int32_t*>(smem + kOffPtab);
-      bool ptab_ok = false;
-      // a block-table entry: from the shared-memory copy once it is in, else from global memory
-      auto phys_of = [&](const BlockCursor& c, int i) -> int {
-        const int u = c.upage() + i;
-        if (!ptab_ok && u < kPtabMax) ptab_ok = mbar_test_wait(&bars->ptab_ready, 0);
-        int ph = (ptab_ok && u < kPtabMax)
-                     ? ptab[u]
-                     : __ldg(prm.block_table + static_cast<size_t>(c.sg.b) * prm.max_pages + c.pg + i);
-        if (ph < 0 || ph >= prm.num_pages) {
-          atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
-          ph = 0;
-        }
-        return ph;
-      };
-      BlockCursor vc(prm, unit), kc(prm, unit);  // next block to load V for; next block for K slices
-      bool v_more = vc.next(), k_more = kc.next();
-      int vp0 = 0, vp1 = 0, kp0 = 0, kp1 = 0;  // physical pages of those blocks
-      if (v_more) {
-        vp0 = phys_of(vc, 0);
-        vp1 = vc.npg > 1 ? phys_of(vc, 1) : 0;
-      }
-      if (k_more) {
-        kp0 = phys_of(kc, 0);
-        kp1 = kc.npg > 1 ? phys_of(kc, 1) : 0;
-      }
-      int kn = 0, ks = 0;  // K slices issued; slice of the current block (0, 1 latent, 2 RoPE)
-      uint32_t v_last = 0, v_par = 0, k_last = 0, k_par = 0;  // per stage: loaded here, and its phase parity
-      uint32_t polls = 0;
-      uint64_t t_idle = 0;
-      bool ok = true;
-      while (ok && (v_more || k_more)) {
-        bool did = false;
-        if (k_more) {
-          const int st = kn % kKSlices, use = kn / kKSlices;
-          if (use == 0 || mbar_test_wait(&bars->k_empty[st], (use - 1) & 1)) {
-            if (!skipped(kc)) {
-              uint8_t* sb = smem + kOffK + st * kSliceBytes;
-              mbar_arrive_expect_tx(&bars->k_full[st], static_cast<uint32_t>((ks < 2 ? kLatBox : kRopeRaw) * kc.npg));
-              if (ks < 2) {
-                tma_load_3d(sb, &tm_lat, &bars->k_full[st], other * 256 + ks * 128, 0, kp0);
-                if (kc.npg > 1) tma_load_3d(sb + kLatBox, &tm_lat, &bars->k_full[st], other * 256 + ks * 128, 0, kp1);
-              } else {
-                tma_load_3d(sb + kRopeRaw, &tm_rope, &bars->k_full[st], kDLat, 0, kp0);
-                if (kc.npg > 1) tma_load_3d(sb + kLatBox + kRopeRaw, &tm_rope, &bars->k_full[st], kDLat, 0, kp1);
-              }
-              k_last |= 1u << st;
-              k_par = (k_par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
-            }
-            ++kn;
-            if (++ks == 3) {
-              ks = 0;
-              k_more = kc.next();
-              if (k_more) {
-                kp0 = phys_of(kc, 0);
-                kp1 = kc.npg > 1 ? phys_of(kc, 1) : 0;
-              }
-            }
-            did = true;
-          }
-        }
-        if (v_more && (vc.h < kVStages ||
-                       mbar_test_wait(&bars->v_empty[vc.h % kVStages], ((vc.h / kVStages) - 1) & 1))) {
-          const int st = vc.h % kVStages;
-          if (!skipped(vc)) {
-            uint8_t* sb = smem + kOffV + st * kVBytes;
-            mbar_arrive_expect_tx(&bars->v_full[st], static_cast<uint32_t>(2 * kLatBox * vc.npg));
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              tma_load_3d(sb + q * kBoxBlk, &tm_lat, &bars->v_full[st], part * 256 + q * 128, 0, vp0);
-              if (vc.npg > 1)
-                tma_load_3d(sb + q * kBoxBlk + kLatBox, &tm_lat, &bars->v_full[st], part * 256 + q * 128, 0, vp1);
-            }
-            v_last |= 1u << st;
-            v_par = (v_par & ~(1u << st)) | (static_cast<uint32_t>((vc.h / kVStages) & 1) << st);
-          }
-          v_more = vc.next();
-          if (v_more) {
-            vp0 = phys_of(vc, 0);
-            vp1 = vc.npg > 1 ? phys_of(vc, 1) : 0;
-          }
-          did = true;
-        }
-        if (did) {
-          polls = 0;
-        } else if ((++polls & 255u) == 0) {
-          if (*abort_flag) ok = false;
-          if (polls == 256) t_idle = globaltimer_ns();
-          if (ok && polls > kWaitMinPolls && globaltimer_ns() - t_idle > *(volatile uint64_t*)&g_wait_limit_ns) {
-            atomicOr(&g_status_mla, FP8MLA_DEV_WAIT_TIMEOUT);
-            record_timeout_site(__LINE__);
-            ok = false;
-          }
-        }
-      }
-      if (!ok) *abort_flag = 1u;
-      // Never leave with copies in flight: wait for the last load of each stage.
-      for (int st = 0; st < kKSlices; ++st)
-        if ((k_last >> st) & 1u) wait_bounded(&bars->k_full[st], (k_par >> st) & 1u, nullptr, &g_status_mla, __LINE__);
-      for (int st = 0; st < kVStages; ++st)
-        if ((v_last >> st) & 1u) wait_bounded(&bars->v_full[st], (v_par >> st) & 1u, nullptr, &g_status_mla, __LINE__);
     }
+    // bounded-wait test hook: CTA 0 of unit 0 never loads its page (g_fault_page - 1) of the unit
+    const int fault = (unit == 0 && part == 0) ? *reinterpret_cast<volatile int*>(&g_fault_page) : 0;
+    int upg = 0;  // the unit's pages so far
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int k = 0;
+    uint32_t issued = 0, par = 0;  // per stage: last occupant was loaded here, and its use parity
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      // the segment's quantised Q: two latent halves and the RoPE part
+      for (int q = 0; q < 3 && ok; ++q, ++k) {
+        const int st = k % kStages, use = k / kStages;
+        const uint32_t bytes = (q < 2) ? kQLatSlotBytes : kQRopeSlotBytes;
+        bool waited = true;
+        if (lane == 0) {
+          waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
+          if (waited) {
+            mbar_arrive_expect_tx(&bars->kv_full[st], bytes);
+            bulk_load(smem + st * kStageBytes,
+                      prm.qbuf + static_cast<size_t>(sg.b) * kMlaQBytes + static_cast<size_t>(q) * kQLatSlotBytes,
+                      bytes, &bars->kv_full[st]);
+            issued |= 1u << st;
+            par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, waited ? 1 : 0, 0) != 0;
+      }
+      if (!ok) break;
+      const int32_t* bt = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
+      for (int chunk = sg.lo; ok && chunk < sg.hi; chunk += 32) {
+        int mine = 0;
+        if (chunk + lane < sg.hi) {
+          mine = __ldg(bt + chunk + lane);
+          if (mine < 0 || mine >= prm.num_pages) {
+            atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
+            mine = 0;
+          }
+        }
+        const int cnt = min(32, sg.hi - chunk);
+        for (int j = 0; j < cnt; ++j, ++k, ++upg) {
+          const int phys = __shfl_sync(0xffffffffu, mine, j);
+          const int st = k % kStages;
+          const int use = k / kStages;
+          bool waited = true;
+          if (lane == 0) {
+            waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
+            if (waited && fault != upg + 1) {
+              uint8_t* sb = smem + st * kStageBytes;
+              mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kLatBox, &tm_lat, &bars->kv_full[st], q * 128, 0, phys);
+              tma_load_3d(sb + kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
+              issued |= 1u << st;
+              par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
+            ok = false;
+            break;
+          }
+        }
+      }
+    }
+    // Never leave with copies in flight: wait for the last load of each stage.
+    if (lane == 0)
+      for (int s = 0; s < kStages; ++s)
+        if ((issued >> s) & 1u) wait_bounded(&bars->kv_full[s], (par >> s) & 1u, nullptr, &g_status_mla, __LINE__);
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    // The whole warp runs the loop and one elected lane issues.  The warp
-    // polls the next block's P.V and the next step of the next block's Q.K^T
-    // and issues whichever is ready (P.V first: it frees a V stage and P), so
-    // neither waits behind the other.  Q.K^T(h) runs in four steps: this
-    // CTA's latent half from the V stage once S is read out and, when the
-    // block opens a segment, that segment's Q is in (the stage is probed only
-    // after the P.V of its previous block was issued, so the probe cannot see
-    // that block's phase); the other latent half's two boxes (K slices); and
-    // the converted RoPE slice.  P.V(h) needs P(h) written and O rescaled.
-    // Before the P.V of a block holding a sequence's last page the warp zeroes
-    // that page's V rows past the sequence end (they may hold anything, and P
-    // is 0 there).
-    constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128);  // e4m3, B MN-major, N = 256
-    const bool leader = elect_one();
-    const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
-    const uint64_t pd = make_sdesc(smem_u32(smem + kOffP), kPLbo, kPSbo, SWIZZLE_NONE);
-    BlockCursor qk(prm, unit);  // next block whose Q.K^T is due
-    BlockCursor pv(prm, unit);  // next block whose P.V is due
-    int qn = 0, qk_seg = -1, step = 0;  // Q copies consumed, segment of the last Q.K^T, next step
-    bool qk_more = qk.next();
-    bool pv_more = pv.next();
-    bool ok = true;
-    uint64_t t_idle = 0;
-    uint32_t polls = 0;
-    while (ok && (qk_more || pv_more)) {
-      bool did = false;
-      if (pv_more) {
-        const int h = pv.h;
-        const int st = h % kVStages;
-        const bool ready = mbar_test_wait(&bars->p_full, h & 1) && mbar_test_wait(&bars->v_full[st], (h / kVStages) & 1);
-        if (__all_sync(0xffffffffu, ready)) {
-          uint8_t* vs = smem + kOffV + st * kVBytes;
-          if (pv.pg + pv.npg == pv.sg.n) {  // the sequence's last page: zero its rows past the end
-            const int lp = pv.npg - 1;
-            const int live = pv.sg.s_k - (pv.pg + lp) * kPage;  // rows of the page that hold keys
-            if (live < kPage) {
-              const uint4 z = make_uint4(0, 0, 0, 0);
-              for (int i = lane; i < (kPage - live) * 16; i += 32) {
-                const int row = live + i / 16, c = i % 16;
-                *reinterpret_cast<uint4*>(vs + (c >> 3) * kBoxBlk + lp * kLatBox + row * 128 + ((c & 7) << 4)) = z;
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-            }
-          }
-          tc_fence_after();
-          const uint64_t vd = make_sdesc(smem_u32(vs), kBoxBlk, 1024, SWIZZLE_128B);
-          const bool first = pv.first();
-          for (int kk = 0; kk < 2 * pv.npg; ++kk)
-            mma_f8_ss_if(leader, tmem + kTO, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
-                         (first && kk == 0) ? 0u : 1u);
-          tc_commit_if(leader, &bars->pv_done);
-          tc_commit_if(leader, &bars->v_empty[st]);
-          pv_more = pv.next();
-          did = true;
-        }
-      }
-      if (!did && qk_more) {
-        const int h = qk.h;
-        const uint32_t n_keys = static_cast<uint32_t>(kPage * qk.npg);
-        const uint32_t idesc8 = make_idesc(0, 0, 0, 0, n_keys, 128);   // e4m3 x e4m3, both K-major
-        const uint32_t idesc16 = make_idesc(0, 0, 0, 0, n_keys, 128);  // f16 x f16 (E4M3 keys are exact in f16)
-        if (step == 0) {
-          const bool opens = qk.seg != qk_seg;
-          const int vst = h % kVStages;
-          const bool ready = (!opens || mbar_test_wait(&bars->q_full, qn & 1)) &&
-                             (h < 1 || mbar_test_wait(&bars->s_free, (h - 1) & 1)) &&
-                             (!pv_more || pv.h > h - kVStages) &&
-                             mbar_test_wait(&bars->v_full[vst], (h / kVStages) & 1);
-          if (__all_sync(0xffffffffu, ready)) {
-            if (opens) {
-              qk_seg = qk.seg;
-              ++qn;
-            }
-            tc_fence_after();
-            const uint64_t vd = make_sdesc(smem_u32(smem + kOffV + vst * kVBytes), 16, 1024, SWIZZLE_128B);
-            // boxes q = 2 part + i hold Q.K^T bytes [128 q, 128 q + 128) of the keys
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ts_if(leader, tmem + kTS, tmem + kTQ + (4 * (2 * part + i) + kk) * 8,
-                             vd + ((i * kBoxBlk + kk * 32) >> 4), idesc8, (i | kk) ? 1u : 0u);
-            step = 1;
-            did = true;
-          }
-        } else {
-          const int n = 3 * h + step - 1;  // steps 1, 2: the other latent boxes; step 3: RoPE
-          const int st = n % kKSlices;
-          const bool ready = step < 3 ? mbar_test_wait(&bars->k_full[st], (n / kKSlices) & 1)
-                                      : mbar_test_wait(&bars->k_cvt[h & 1], (h >> 1) & 1);
-          if (__all_sync(0xffffffffu, ready)) {
-            tc_fence_after();
-            const uint64_t kd = make_sdesc(smem_u32(smem + kOffK + st * kSliceBytes), 16, 1024, SWIZZLE_128B);
-            if (step < 3) {
-              const int q = 2 * other + step - 1;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ts_if(leader, tmem + kTS, tmem + kTQ + (4 * q + kk) * 8, kd + ((kk * 32) >> 4), idesc8, 1u);
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ss_if(leader, tmem + kTS, qd + ((kk * 32) >> 4), kd + ((kk * 32) >> 4), idesc16, 1u);
-            }
-            tc_commit_if(leader, &bars->k_empty[st]);
-            if (step == 3) {
-              tc_commit_if(leader, &bars->s_full);
-              step = 0;
-              qk_more = qk.next();
-            } else {
-              ++step;
-            }
-            did = true;
-          }
-        }
-      }
-      // bounded: no progress for the wait limit (or another role stopped) ends the loop
-      if (did) {
-        polls = 0;
-      } else if ((++polls & 255u) == 0) {
-        if (*abort_flag) ok = false;
-        if (polls == 256) t_idle = globaltimer_ns();
-        if (ok && polls > kWaitMinPolls && globaltimer_ns() - t_idle > *(volatile uint64_t*)&g_wait_limit_ns) {
-          if (lane == 0) {
-            atomicOr(&g_status_mla, FP8MLA_DEV_WAIT_TIMEOUT);
-            record_timeout_site(__LINE__);
-          }
-          ok = false;
-        }
-        ok = __all_sync(0xffffffffu, ok);
-      }
-    }
-    if (!ok && lane == 0) *abort_flag = 1u;
-    if (leader) tc_commit(&bars->final_mma);
-    __syncwarp();
-    warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
-  } else if (warp == 2 || warp == 3) {
-    // ---------------------- RoPE conversion (64 threads) ----
-    // First the unit's block-table entries (as many as fit) go into shared
-    // memory for the producer.  Then thread 0 waits for every K slice in order
-    // (so no wait can see a stage's phase two ahead), and for a block's RoPE
-    // slice thread t reads the E4M3 RoPE bytes of token row t of each page
-    // from the second half of the page's 8 KB and, after all have read, writes
-    // them as f16 (exact) over the whole 8 KB, 128-byte swizzled; rows past
-    // the sequence end become 0 (their scores are masked anyway).
-    const int t = threadIdx.x - 64;  // token row of a page
+    // The whole warp runs the loop (so descriptors stay warp-uniform) and one
+    // elected lane issues -- from a lone thread each MMA costs about twice as
+    // long to issue.  Pages alternate between two S buffers, so the Q.K^T of
+    // page i runs while the softmax warps work on page i - 1.  Per page i: wait
+    // until S buffer i % 2 was read out (page i - 2), Q.K^T as 16 E4M3 MMAs
+    // (latent, Q from TMEM, K = 32) and 4 f16 MMAs (RoPE, Q from shared
+    // memory, K = 16), then the P.V of page i - 1 (2 E4M3 MMAs, K = 32 keys,
+    // N = 256) once its P is written.
     {
-      int32_t* ptab = reinterpret_cast<int32_t*>(smem + kOffPtab);
-      SegmentWalker w(prm, unit);
+      constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
+      constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
+      constexpr uint32_t idesc_pv = make_idesc(0, 0, 0, 1, 256, 128); // e4m3, B MN-major, N = 256
+      const uint32_t t_o = tmem + kTO;
+      const bool leader = elect_one();
+      const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
+      const uint64_t pd = make_sdesc(smem_u32(smem + kOffP), kPLbo, kPSbo, SWIZZLE_NONE);
+      SegmentWalker walk(prm, unit);
       Segment sg;
-      int u0 = 0;
-      while (u0 < kPtabMax && w.next(sg)) {
-        const int32_t* row = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
-        const int n = min(sg.hi - sg.lo, kPtabMax - u0);
-        for (int i = t; i < n; i += 64) cp_async4(ptab + u0 + i, row + sg.lo + i);
-        u0 += n;
+      int i = 0, k = 0, seg = 0;
+      int j = 0;           // next page whose P.V is due (pages j .. i - 1 have their Q.K^T issued)
+      uint32_t pend = 0;   // per pending page p, byte p % 4: its stage | first-of-segment << 3
+      bool ok = true;
+      // the P.V of page j, once its P is written; it releases the page's stage
+      auto issue_pv = [&]() -> bool {
+        if (!warp_spin(&bars->p_full, j & 1, abort_flag, __LINE__)) return false;
+        tc_fence_after();
+        const uint32_t e = (pend >> (8 * (j & 3))) & 0xFFu;
+        const int st = static_cast<int>(e & 7u);
+        const bool first = ((e >> 3) & 1u) != 0;
+        const uint32_t v_base = smem_u32(smem + st * kStageBytes) + part * 2 * kLatBox;
+        const uint64_t vd = make_sdesc(v_base, kLatBox, 1024, SWIZZLE_128B);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          mma_f8_ss_if(leader, t_o, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
+                       (first && kk == 0) ? 0u : 1u);
+        tc_commit_if(leader, &bars->pv_done);
+        tc_commit_if(leader, &bars->kv_empty[st]);
+        ++j;
+        return true;
+      };
+      while (ok && walk.next(sg)) {
+        // The previous segment's last P.V comes first: the softmax warps write
+        // its P before they copy this segment's Q.
+        while (ok && j < i) ok = issue_pv();
+        // the softmax warps have copied the Q slots (and the converter has seen them)
+        bool qok = ok && warp_wait(&bars->q_full, seg & 1, abort_flag, __LINE__);
+        for (int q = 0; q < 3 && qok; ++q)
+          qok = warp_wait(&bars->cvt_ready[(k + q) % kStages], ((k + q) / kStages) & 1, abort_flag, __LINE__);
+        if (!qok) {
+          ok = false;
+          break;
+        }
+        if (leader)
+          for (int q = 0; q < 3; ++q) mbar_arrive(&bars->kv_empty[(k + q) % kStages]);
+        __syncwarp();
+        k += 3;
+        // Page i's conversion is waited for while the P.V of page i - 2 runs (so
+        // that Q.K^T(i) follows that P.V in the tensor pipe without a gap).  S
+        // buffer i % 2 last held page i - 2, whose P (written after its S was
+        // read) that P.V waited for -- or the previous segment's flush did.
+        if (!warp_spin(&bars->cvt_ready[k % kStages], (k / kStages) & 1, abort_flag, __LINE__)) {
+          ok = false;
+          break;
+        }
+        for (int pg = sg.lo; pg < sg.hi; ++pg, ++i, ++k) {
+          const int st = k % kStages;
+          const int sbuf = i & 1;
+          tc_fence_after();
+          const uint32_t t_s = tmem + kTS + sbuf * kPage;
+          const uint64_t kd = make_sdesc(smem_u32(smem + st * kStageBytes), 16, 1024, SWIZZLE_128B);
+#pragma unroll
+          for (int kk = 0; kk < 16; ++kk)
+            mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4),
+                         idesc8, kk > 0 ? 1u : 0u);
+          const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + sbuf * kCvtBytes), 16, 1024, SWIZZLE_128B);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16_ss_if(leader, t_s, qd + ((kk * 32) >> 4), rd + ((kk * 32) >> 4), idesc16, 1u);
+          tc_commit_if(leader, &bars->s_full[sbuf]);
+          const uint32_t e = static_cast<uint32_t>(st) | ((pg == sg.lo) ? 8u : 0u);
+          pend = (pend & ~(0xFFu << (8 * (i & 3)))) | (e << (8 * (i & 3)));
+          // the P.V of the previous page (queued right behind this Q.K^T), then
+          // the next page's conversion while that P.V runs
+          if (pg > sg.lo && !issue_pv()) {  // j == i - 1 here
+            ok = false;
+            break;
+          }
+          if (pg + 1 < sg.hi &&
+              !warp_spin(&bars->cvt_ready[(k + 1) % kStages], ((k + 1) / kStages) & 1, abort_flag, __LINE__)) {
+            ok = false;
+            break;
+          }
+        }
+        ++seg;
       }
-      cp_async_wait_all();
-      named_bar_sync(1, 64);
-      if (t == 0) mbar_arrive(&bars->ptab_ready);
+      while (ok && j < i) ok = issue_pv();  // the last P.V
+      if (leader) tc_commit(&bars->final_mma);
+      __syncwarp();
+      warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
     }
-    BlockCursor bc(prm, unit);
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------- RoPE conversion, tail zeroing (64 threads) ----
+    const int t = threadIdx.x - 64;  // token row of the page
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int k = 0, i = 0;  // ring slots, pages
     bool ok = true;
-    int n = 0;  // K slices waited for
-    while (ok && bc.next()) {
-      const int st = (n + 2) % kKSlices;
+    while (ok && walk.next(sg)) {
+      // the Q slots need no conversion, but their fills are waited for and
+      // acknowledged like the pages' so that each stage phase is seen in turn
       if (t == 0) {
-        bool good = true;
-        for (int s3 = 0; s3 < 3 && good; ++s3)
-          good = wait_bounded(&bars->k_full[(n + s3) % kKSlices], ((n + s3) / kKSlices) & 1, abort_flag,
-                              &g_status_mla, __LINE__);
-        bars->cvt_ok = good ? 1u : 0u;
+        bool filled = true;
+        for (int q = 0; q < 3 && filled; ++q)
+          filled = wait_bounded(&bars->kv_full[(k + q) % kStages], ((k + q) / kStages) & 1, abort_flag,
+                                &g_status_mla, __LINE__);
+        if (filled)
+          for (int q = 0; q < 3; ++q) mbar_arrive(&bars->cvt_ready[(k + q) % kStages]);
+        bars->cvt_ok = filled ? 1u : 0u;
       }
-      n += 3;
       named_bar_sync(1, 64);
-      if (!bars->cvt_ok) {
-        ok = false;
-        break;
-      }
-      uint8_t* kb = smem + kOffK + st * kSliceBytes;
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      uint4 raw[kBlkPages][4];
-#pragma unroll
-      for (int i = 0; i < kBlkPages; ++i) {
-        const bool dead = i >= bc.npg || (bc.pg + i == bc.sg.n - 1 && t >= bc.sg.s_k - (bc.pg + i) * kPage);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          raw[i][c] = dead ? z : reinterpret_cast<const uint4*>(kb + i * kLatBox + kRopeRaw + t * 64)[c];
-      }
-      named_bar_sync(1, 64);  // every raw row is read before the f16 rows overwrite them
-      const int sw = t & 7;
-#pragma unroll
-      for (int i = 0; i < kBlkPages; ++i) {
-        if (i >= bc.npg) break;
-        uint8_t* dst = kb + i * kLatBox + t * 128;
+      if (!bars->cvt_ok) break;
+      named_bar_sync(1, 64);  // cvt_ok is rewritten below
+      k += 3;
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++k, ++i) {
+        const int st = k % kStages;
+        const int use = k / kStages;
+        // conversion buffer i % 2 is free once the Q.K^T of page i - 2 completed
+        if (t == 0)
+          bars->cvt_ok = (wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla, __LINE__) &&
+                          (i < 2 || wait_bounded(&bars->s_full[i & 1], ((i - 2) >> 1) & 1, abort_flag, &g_status_mla, __LINE__)))
+                             ? 1u
+                             : 0u;
+        named_bar_sync(1, 64);
+        if (!bars->cvt_ok) {
+          ok = false;
+          break;
+        }
+        uint8_t* sb = smem + st * kStageBytes;
+        const bool dead = (pg == sg.n - 1) && (t >= sg.s_k - pg * kPage);  // slot past the sequence end
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        const int sw = t & 7;
+        const uint4* src = reinterpret_cast<const uint4*>(sb + kOffRope8 + t * 64);
+        uint8_t* dst = smem + kOffCvt + (i & 1) * kCvtBytes + t * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint4 v = raw[i][c];
-          uint4 lo, hi;
-          lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
-          lo.y = e4m3x2_to_f16x2(v.x >> 16);
-          lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
-          lo.w = e4m3x2_to_f16x2(v.y >> 16);
-          hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
-          hi.y = e4m3x2_to_f16x2(v.z >> 16);
-          hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
-          hi.w = e4m3x2_to_f16x2(v.w >> 16);
+          uint4 lo = z, hi = z;
+          if (!dead) {
+            const uint4 v = src[c];
+            lo.x = e4m3x2_to_f16x2(v.x & 0xFFFFu);
+            lo.y = e4m3x2_to_f16x2(v.x >> 16);
+            lo.z = e4m3x2_to_f16x2(v.y & 0xFFFFu);
+            lo.w = e4m3x2_to_f16x2(v.y >> 16);
+            hi.x = e4m3x2_to_f16x2(v.z & 0xFFFFu);
+            hi.y = e4m3x2_to_f16x2(v.z >> 16);
+            hi.z = e4m3x2_to_f16x2(v.w & 0xFFFFu);
+            hi.w = e4m3x2_to_f16x2(v.w >> 16);
+          }
           *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
           *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
         }
+        if (dead) {  // zero the slot's V row (all four 128-byte slices)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4* row = reinterpret_cast<uint4*>(sb + j * kLatBox + t * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) row[c] = z;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 64);
+        if (t == 0) mbar_arrive(&bars->cvt_ready[st]);
       }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 64);
-      if (t == 0) mbar_arrive(&bars->k_cvt[bc.h & 1]);
     }
-    if (!ok && t == 0) *abort_flag = 1u;
   } else {
     // ------------------ softmax / Q copy / epilogue (8 warps, 2 per row) ----
-    const int hf = (warp - 4) / 4;         // which half of the row (keys [64 hf, 64 hf + 64) of a block)
+    const int hf = (warp - 4) / 4;         // which half of the row
     const int r = (warp % 4) * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
     const float kv_scale = *prm.kv_scale;
@@ -1223,241 +1088,207 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       ++xphase;
       return ok;
     };
-    const uint32_t prow = static_cast<uint32_t>((r >> 3) * kPSbo + (r & 7) * 16);
-
-    // Copies this half of sequence b_seq's quantised Q row (prepared by
-    // mla_qprep_kernel) in: latent bytes [256 hf, +256) into TMEM columns
-    // kTQ + 64 hf.., RoPE values [32 hf, +32) into the Q RoPE tile.
-    float qs_cur = 1.f;
-    auto copy_q = [&](int b_seq) {
-      const uint8_t* qb = prm.qbuf + static_cast<size_t>(b_seq) * kMlaQBytes;
-      const uint4* lat = reinterpret_cast<const uint4*>(qb + hf * kQLatSlotBytes + r * kQLatPitch);
-      const uint4* rope = reinterpret_cast<const uint4*>(qb + 2 * kQLatSlotBytes + r * kQRopePitch + hf * 64);
-      uint4 v[16], w[4];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) v[c] = __ldg(lat + c);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) w[c] = __ldg(rope + c);
-      qs_cur = __ldg(prm.qscale + static_cast<size_t>(b_seq) * kRows + r);
+    // Copies this half of the Q row of the segment whose Q slots start at ring
+    // slot kq: latent bytes [256 hf, +256) into TMEM columns kTQ + 64 hf..,
+    // RoPE values [32 hf, +32) into the shared Q RoPE tile (128-byte swizzle).
+    auto copy_q = [&](int kq, int b_seq, float& qs_out) -> bool {
+      const int st = (kq + hf) % kStages, use = (kq + hf) / kStages;
+      const int st_r = (kq + 2) % kStages, use_r = (kq + 2) / kStages;
+      if (!warp_wait(&bars->kv_full[st], use & 1, abort_flag, __LINE__) ||
+          !warp_wait(&bars->kv_full[st_r], use_r & 1, abort_flag, __LINE__))
+        return false;
+      const uint4* lat = reinterpret_cast<const uint4*>(smem + st * kStageBytes + r * kQLatPitch);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          pk[4 * c + 0] = v[4 * ch + c].x;
-          pk[4 * c + 1] = v[4 * ch + c].y;
-          pk[4 * c + 2] = v[4 * ch + c].z;
-          pk[4 * c + 3] = v[4 * ch + c].w;
+          const uint4 v = lat[4 * ch + c];
+          pk[4 * c + 0] = v.x;
+          pk[4 * c + 1] = v.y;
+          pk[4 * c + 2] = v.z;
+          pk[4 * c + 3] = v.w;
         }
         tmem_st16(lane_base + kTQ + (4 * hf + ch) * 16, pk);
       }
-      uint8_t* dst = smem + kOffQRope + r * 128;
+      {
+        const uint4* rope = reinterpret_cast<const uint4*>(smem + st_r * kStageBytes + r * kQRopePitch);
+        uint8_t* dst = smem + kOffQRope + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(dst + (((4 * hf + c) ^ (r & 7)) << 4)) = w[c];
-      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs
+        for (int c = 4 * hf; c < 4 * hf + 4; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = rope[c];
+      }
+      qs_out = prm.qscale[static_cast<size_t>(b_seq) * kRows + r];
+      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs, the slots refilled by TMA
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bars->q_full);
+      return true;
     };
 
-    BlockCursor pc(prm, unit);
-    bool ok = true;
-    int cur_seg = -1;
-    float m_run = kNegInf, l_run = 0.f;  // reference of O and l; this thread's share of l
-    int qtok = 0, visible = 0;
-    float c_row = 0.f;
-
-    // Moves O and l to a new reference before a block's P.V (whose P was
-    // taken against it), once the P.V of the block before completed (the
-    // caller has waited for it).
-    auto rescale_to = [&](float m_new, bool first) {
-      const bool rescale = !first && m_new != m_run;
-      const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.f;
-      l_run = first ? 0.f : l_run * alpha;
-      if (first || rescale) m_run = m_new;
-      if (__any_sync(0xffffffffu, rescale)) {
-        tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < kOHalf / 32; ++ch) {
-          const uint32_t col = kTO + hf * kOHalf + ch * 32;
-          uint32_t o[32];
-          tmem_ld32(lane_base + col, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st32(lane_base + col, o);
+    SegmentWalker walk(prm, unit);
+    Segment sg;
+    int i = 0, k = 0, seg = 0;
+    float qs_next = 1.f;
+    bool ok = walk.next(sg) && copy_q(0, sg.b, qs_next);
+    while (ok) {
+      const float qs = qs_next;
+      const float c_row = prm.softmax_scale * kLog2e * qs * kv_scale;
+      SegmentWalker peek = walk;
+      Segment nx;
+      const bool has_next = peek.next(nx);
+      const int k_next = k + 3 + (sg.hi - sg.lo);
+      const int col0 = part * 256 + hf * kOHalf;  // this thread's O columns
+      // keys visible to this row (bottom-right causal alignment); pages wholly
+      // below every row's limit need no mask
+      const int qtok = (r < R) ? r / prm.h_q : 0;
+      const int visible = prm.causal ? (sg.s_k - prm.s_q + qtok + 1) : sg.s_k;
+      const int min_visible = prm.causal ? (sg.s_k - prm.s_q + 1) : sg.s_k;
+      float m_run = kNegInf, l_run = 0.f;  // l_run sums the stored-scale p (kPScale p)
+      for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
+        const int sbuf = i & 1;
+        if (!warp_spin(&bars->s_full[sbuf], (i >> 1) & 1, abort_flag, __LINE__)) {
+          ok = false;
+          break;
         }
-        tmem_st_wait();
-      }
-    };
+        tc_fence_after();
+        // Both halves of the row are read: the other half only for the row max,
+        // so each warp takes the max of all 64 keys without waiting on its partner.
+        uint32_t s[32], so[32];
+        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * hf, s);
+        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * (1 - hf), so);
+        tmem_ld_wait();
 
-    if (pc.next()) copy_q(pc.sg.b);
-    pc = BlockCursor(prm, unit);
-
-    while (ok && pc.next()) {
-      const int h = pc.h;
-      if (pc.seg != cur_seg) {  // a new segment
-        cur_seg = pc.seg;
-        m_run = kNegInf;
-        l_run = 0.f;
-        qtok = (r < R) ? r / prm.h_q : 0;
-        visible = prm.causal ? (pc.sg.s_k - prm.s_q + qtok + 1) : pc.sg.s_k;
-        c_row = prm.softmax_scale * kLog2e * qs_cur * kv_scale;
-        if (r < R) {  // warm L2 with the Q of the segment after this one
-          SegmentWalker peek = pc.walk;
-          Segment nx;
-          if (peek.next(nx)) {
-            const char* nq = reinterpret_cast<const char*>(prm.qbuf + static_cast<size_t>(nx.b) * kMlaQBytes);
-            prefetch_l2(nq + hf * kQLatSlotBytes + r * kQLatPitch);
-            prefetch_l2(nq + hf * kQLatSlotBytes + r * kQLatPitch + 128);
+        if (pg * kPage + kPage > min_visible) {
+          const int base = pg * kPage + 32 * hf, base_o = pg * kPage + 32 * (1 - hf);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (base + c >= visible) s[c] = __float_as_uint(kNegInf);
+            if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
           }
         }
-      }
-      if (!warp_spin(&bars->s_full, h & 1, abort_flag, __LINE__)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t s[32], s2[32];  // keys [64 hf, +32) and [64 hf + 32, +32) of the block
-      tmem_ld32(lane_base + kTS + 64 * hf, s);
-      tmem_ld32(lane_base + kTS + 64 * hf + 32, s2);
-      tmem_ld_wait();
-      tc_fence_before();
-      warp_arrive(&bars->s_free);  // block h + 1's Q.K^T may overwrite S
-      // the segment's last block: its Q.K^T is done, so the next segment's Q may replace this one's
-      if (pc.last()) {
-        SegmentWalker peek = pc.walk;
-        Segment nx;
-        if (peek.next(nx)) copy_q(nx.b);
-      }
-      // keys past the row's causal limit or past the segment's pages
-      const int key0 = pc.pg * kPage + 64 * hf;
-      const int lim = min(visible, (pc.pg + pc.npg) * kPage);
-      if (key0 + 64 > lim) {
+        // row max of the 64 scores as a tree of three-way maxima
+        float m22[22];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (key0 + c >= lim) s[c] = __float_as_uint(kNegInf);
-          if (key0 + 32 + c >= lim) s2[c] = __float_as_uint(kNegInf);
+        for (int c = 0; c < 10; ++c) {
+          m22[c] = fmax3(__uint_as_float(s[3 * c]), __uint_as_float(s[3 * c + 1]), __uint_as_float(s[3 * c + 2]));
+          m22[10 + c] =
+              fmax3(__uint_as_float(so[3 * c]), __uint_as_float(so[3 * c + 1]), __uint_as_float(so[3 * c + 2]));
+        }
+        m22[20] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
+        m22[21] = fmaxf(__uint_as_float(so[30]), __uint_as_float(so[31]));
+        float m8[8];
+#pragma unroll
+        for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
+        m8[7] = m22[21];
+        const float m3a = fmax3(m8[0], m8[1], m8[2]), m3b = fmax3(m8[3], m8[4], m8[5]);
+        const float mx = fmax3(m3a, m3b, fmaxf(m8[6], m8[7])) * c_row;  // c_row > 0; both warps agree
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_run + kTau) {
+          alpha = ex2_approx(m_run - mx);
+          rescale = (pg != sg.lo);
+          m_run = mx;
+        }
+        const float bias = (m_run == kNegInf) ? 0.f : (kPLog2 - m_run);
+        float sum = 0.f;
+        uint32_t pk[8];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c_row, bias));
+          const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
+          const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
+          sum += (p0 + p1) + (p2 + p3);
+          pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+        }
+        l_run = l_run * alpha + sum;
+
+        // P has one tile and O one accumulator: the previous page's P.V must
+        // have completed before either is touched
+        if (i >= 1 && !warp_spin(&bars->pv_done, (i - 1) & 1, abort_flag, __LINE__)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+          for (int ch = 0; ch < kOHalf / 32; ++ch) {
+            const uint32_t col = kTO + hf * kOHalf + ch * 32;
+            uint32_t o[32];
+            tmem_ld32(lane_base + col, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+            tmem_st32(lane_base + col, o);
+          }
+          tmem_st_wait();
+        }
+        {  // this warp's 32 keys of row r: 16-byte chunks 2 hf and 2 hf + 1
+          uint8_t* prow = smem + kOffP + (r >> 3) * kPSbo + (r & 7) * 16;
+          *reinterpret_cast<uint4*>(prow + (2 * hf) * kPLbo) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(prow + (2 * hf + 1) * kPLbo) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(&bars->p_full);
+        // the segment's last Q.K^T is done: the next segment's Q may replace it now
+        if (pg == sg.hi - 1 && has_next && !copy_q(k_next, nx.b, qs_next)) {
+          ok = false;
+          break;
         }
       }
-      float m22[22];
-#pragma unroll
-      for (int c = 0; c < 10; ++c) {
-        m22[c] = fmax3(__uint_as_float(s[3 * c]), __uint_as_float(s[3 * c + 1]), __uint_as_float(s[3 * c + 2]));
-        m22[10 + c] = fmax3(__uint_as_float(s2[3 * c]), __uint_as_float(s2[3 * c + 1]), __uint_as_float(s2[3 * c + 2]));
-      }
-      m22[20] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
-      m22[21] = fmaxf(__uint_as_float(s2[30]), __uint_as_float(s2[31]));
-      float m8[8];
-#pragma unroll
-      for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
-      m8[7] = m22[21];
-      const float mhalf = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
-      // the row's maximum: this half's, and the other half's from its thread (warp warp +- 4)
-      bars->rmax[h & 1][hf][r] = mhalf;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->rmax_full[warp % 4]);
-      if (!warp_spin(&bars->rmax_full[warp % 4], h & 1, abort_flag, __LINE__)) {
-        ok = false;
-        break;
-      }
-      const float mx = fmaxf(mhalf, bars->rmax[h & 1][1 - hf][r]);
-      // the reference: kept unless this block's maximum exceeds it by more than kTau
-      const bool first = pc.first();
-      const float m_new = (first || mx > m_run + kTau) ? mx : m_run;
-      const float bias = (m_new == kNegInf) ? 0.f : (kPLog2 - m_new);
-      float sum = 0.f;
-      uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c_row, bias));
-        const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
-        const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
-        sum += (p0 + p1) + (p2 + p3);
-        pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
-      }
-#pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(s2[c]), c_row, bias));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(s2[c + 1]), c_row, bias));
-        const float p2 = ex2_approx(fmaf(__uint_as_float(s2[c + 2]), c_row, bias));
-        const float p3 = ex2_approx(fmaf(__uint_as_float(s2[c + 3]), c_row, bias));
-        sum += (p0 + p1) + (p2 + p3);
-        pk[8 + c / 4] = pack_e4m3x4(p0, p1, p2, p3);
-      }
-      // P and O are free once the block before's P.V completed
-      if (h >= 1 && !warp_spin(&bars->pv_done, (h - 1) & 1, abort_flag, __LINE__)) {
-        ok = false;
-        break;
-      }
-      {  // this thread's 64 keys of row r: 16-byte chunks 4 hf .. 4 hf + 3
-        uint8_t* lp = smem + kOffP + prow;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(lp + (4 * hf + q) * kPLbo) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-      }
-      fence_proxy_async_smem();
-      rescale_to(m_new, first);
-      l_run += sum;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);  // P written and O rescaled
-      if (!pc.last()) continue;
+      if (!ok) break;
 
-      // ---- segment end ----
-      const int sp = cur_seg & 1;
-      bars->xsum[sp][hf][r] = l_run;
-      if (!xsync()) {
-        ok = false;
-        break;
-      }
-      const float l_tot = (bars->xsum[sp][0][r] + bars->xsum[sp][1][r]) * (1.0f / kPScale);  // sum of p
-      const bool whole = (pc.sg.lo == 0 && pc.sg.hi == pc.sg.n);
+      // ---- epilogue: O is final once the segment's last P.V completes ----
+      bars->xsum[hf][r] = l_run;
+      if (!xsync()) break;
+      const float l_tot = (bars->xsum[0][r] + bars->xsum[1][r]) * (1.0f / kPScale);  // sum of p
+      const bool whole = (sg.lo == 0 && sg.hi == sg.n);
       const float o_scale = kv_scale / kPScale;  // tensor-core units -> true units
       const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
-      const int slot = whole ? 0 : prm.num_splits[pc.sg.b] + pc.sg.split;
-      // O is final once the P.V of the segment's last block completed
-      if (!warp_wait(&bars->pv_done, h & 1, abort_flag, __LINE__)) {
-        ok = false;
-        break;
-      }
+      const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
+      if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag, __LINE__)) break;
       tc_fence_after();
-      const int col0 = part * 256 + hf * kOHalf;       // this thread's O columns
+      // O out as bf16, 32 columns at a time.  A thread holds one row; groups of
+      // four lanes transpose their 16-byte pieces so that each store writes
+      // 64-byte runs of rows.  A whole sequence goes straight to out, a piece
+      // to its bf16 partial slot; the combine kernel adds the LSE correction.
       const int grow = (warp % 4) * 32 + (lane & ~3);  // the lane group's first row
-      uint16_t* obase = whole ? prm.out + static_cast<size_t>(pc.sg.b) * R * kDV
+      uint16_t* obase = whole ? prm.out + static_cast<size_t>(sg.b) * R * kDV
                               : prm.ws_o + static_cast<size_t>(slot) * kRows * kDV;
 #pragma unroll 1
       for (int ch = 0; ch < kOHalf / 32; ++ch) {
         uint32_t o[32];
         tmem_ld32(lane_base + kTO + hf * kOHalf + ch * 32, o);
         tmem_ld_wait();
-        uint4 pcs[4];
+        uint4 pc[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          pcs[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
-          pcs[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
-          pcs[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
-          pcs[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
+          pc[c].x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
+          pc[c].y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
+          pc[c].z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
+          pc[c].w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
         }
-        lane_group_transpose<4>(pcs, lane);
+        lane_group_transpose<4>(pc, lane);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           if (grow + kk < R)
-            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(grow + kk) * kDV + col0 + ch * 32 +
-                                      8 * (lane & 3)) = pcs[kk];
+            *reinterpret_cast<uint4*>(obase + static_cast<size_t>(grow + kk) * kDV + col0 + ch * 32 + 8 * (lane & 3)) =
+                pc[kk];
       }
-      tc_fence_before();  // O is overwritten by the next segment's first P.V after the next p_full
       if (r < R && part == 0 && hf == 0) {  // the row's (uncorrected) LSE, or the piece's (m, l)
         if (whole) {
-          prm.lse[static_cast<size_t>(pc.sg.b) * R + r] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
+          prm.lse[static_cast<size_t>(sg.b) * R + r] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
         } else {
           prm.ws_ml[static_cast<size_t>(slot) * kRows + r] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
         }
       }
+      if (!has_next) break;
+      walk.next(sg);
+      k = k_next;
+      ++seg;
     }
-    if (!ok && lane == 0) *abort_flag = 1u;
   }
 
   tc_fence_before();
