@@ -296,6 +296,24 @@ FP8MLA_API fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
                                                   fp8mla_dot_mode_t dot_mode, int b, int s_q, int h_q,
                                                   fp8mla_stream_t stream);
 
+/* ------------------------------------------------------- measurement ---- */
+
+/* Stage timing of fp8mla_decode, a measurement aid (off by default).  While
+ * enabled, fp8mla_decode records CUDA events before and after each of its
+ * kernels (Q quantisation for FP8 dots, the decode kernel, the combine);
+ * those events keep the kernels from overlapping one another, so time the
+ * call itself with timing off.  One timer per process, used by one thread at
+ * a time: a decode call that times holds it for the call.  Enabling or
+ * disabling discards the last record.  Returns FP8MLA_OK. */
+FP8MLA_API fp8mla_status_t fp8mla_set_stage_timing(int enable);
+
+/* Synchronises `stream` and writes ms[0..2] = milliseconds of the last timed
+ * fp8mla_decode call's Q quantisation (0 for 16-bit dots), decode kernel and
+ * combine.  ms: host pointer to 3 floats.  FP8MLA_ERR_INVALID_ARG if no call
+ * was timed since timing was enabled; FP8MLA_ERR_CUDA if the events cannot be
+ * read (for instance when the last timed call ran on another device). */
+FP8MLA_API fp8mla_status_t fp8mla_get_stage_times(fp8mla_stream_t stream, float* ms);
+
 /* ------------------------------------------------------------- status ---- */
 
 /* Synchronises `stream`, returns in *code_out the OR of the FP8MLA_DEV_* bits

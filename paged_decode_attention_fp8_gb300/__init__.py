@@ -65,6 +65,8 @@ _SIGNATURES = {
     "fp8mla_get_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "fp8mla_get_wait_timeout_site": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "fp8mla_set_wait_test": (_I, [ctypes.c_int32, ctypes.c_uint64]),
+    "fp8mla_set_stage_timing": (_I, [ctypes.c_int]),
+    "fp8mla_get_stage_times": (_I, [_P, ctypes.POINTER(ctypes.c_float)]),
     "fp8mla_status_string": (ctypes.c_char_p, [_I]),
 }
 
@@ -377,6 +379,20 @@ def set_wait_test(fault_page: int = 0, wait_limit_ns: int = 0) -> None:
     fault_page = p + 1 makes CTA 0 of work unit 0 skip the loads of its p-th page,
     so its waits run out (0 = off); wait_limit_ns replaces the wait limit (0 = default)."""
     _check(lib().fp8mla_set_wait_test(int(fault_page), int(wait_limit_ns)), "fp8mla_set_wait_test")
+
+
+def set_stage_timing(enable: bool) -> None:
+    """Measurement aid: while enabled, ``decode`` records events between its kernels
+    (which stops them overlapping); ``stage_times`` then reads the last call's stages."""
+    _check(lib().fp8mla_set_stage_timing(1 if enable else 0), "fp8mla_set_stage_timing")
+
+
+def stage_times(device=None):
+    """(Q quantisation, decode kernel, combine) milliseconds of the last timed ``decode``
+    call (synchronises the current stream)."""
+    ms = (ctypes.c_float * 3)()
+    _check(lib().fp8mla_get_stage_times(_stream(device), ms), "fp8mla_get_stage_times")
+    return ms[0], ms[1], ms[2]
 
 
 def last_device_error(device=None) -> int:

@@ -15,6 +15,34 @@
 namespace fp8mla {
 namespace {
 
+// Stage timing of fp8mla_decode (a measurement aid, off by default): events
+// recorded between the call's kernels, on the device of the last timed call.
+struct StageTimer {
+  std::mutex mu;
+  bool enabled = false;
+  bool timed = false;  // a call was timed since the last enable
+  int device = -1;
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+};
+StageTimer& stage_timer() {
+  static StageTimer t;
+  return t;
+}
+// Events of the current device (created on first use, re-created when the device changes).
+bool stage_events(StageTimer& t) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (t.device == dev && t.ev[0] != nullptr) return true;
+  for (cudaEvent_t& e : t.ev) {
+    if (e != nullptr) cudaEventDestroy(e);
+    e = nullptr;
+  }
+  t.device = dev;
+  for (cudaEvent_t& e : t.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return false;
+  return true;
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -211,14 +239,50 @@ fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dty
   prm.h_q = h_q;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_qprep(prm, s) : cudaSuccess;
+  StageTimer& timer = stage_timer();
+  std::unique_lock<std::mutex> timing(timer.mu, std::defer_lock);
+  bool timed = false;
+  {
+    std::lock_guard<std::mutex> g(timer.mu);
+    timed = timer.enabled;
+  }
+  if (timed) {
+    timing.lock();
+    if (!stage_events(timer)) return FP8MLA_ERR_CUDA;
+  }
+  auto mark = [&](int i) { return timed ? cudaEventRecord(timer.ev[i], s) : cudaSuccess; };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess && dot_mode == FP8MLA_DOT_FP8) e = launch_mla_qprep(prm, s);
+  if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess)
     e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_decode_fp8(tm_lat, tm_rope, prm, num_units, s)
                                      : launch_mla_decode_16bit(tm_lat, tm_rope, prm, num_units, s);
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess)
+    e = launch_mla_combine(num_splits, prm.ws_o, prm.ws_ml, dot_mode == FP8MLA_DOT_FP8 ? prm.qbuf : nullptr,
+                           softmax_scale, prm.out, lse, b, s_q * h_q, s);
+  if (e == cudaSuccess) e = mark(3);
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
-  if (launch_mla_combine(num_splits, prm.ws_o, prm.ws_ml, dot_mode == FP8MLA_DOT_FP8 ? prm.qbuf : nullptr,
-                         softmax_scale, prm.out, lse, b, s_q * h_q, s) != cudaSuccess)
-    return FP8MLA_ERR_CUDA;
+  if (timed) timer.timed = true;
+  return FP8MLA_OK;
+}
+
+fp8mla_status_t fp8mla_set_stage_timing(int enable) {
+  StageTimer& t = stage_timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  t.enabled = enable != 0;
+  t.timed = false;
+  return FP8MLA_OK;
+}
+
+fp8mla_status_t fp8mla_get_stage_times(fp8mla_stream_t stream, float* ms) {
+  if (ms == nullptr) return FP8MLA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8MLA_ERR_CUDA;
+  StageTimer& t = stage_timer();
+  std::lock_guard<std::mutex> g(t.mu);
+  if (!t.timed) return FP8MLA_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i)
+    if (cudaEventElapsedTime(&ms[i], t.ev[i], t.ev[i + 1]) != cudaSuccess) return FP8MLA_ERR_CUDA;
   return FP8MLA_OK;
 }
 
