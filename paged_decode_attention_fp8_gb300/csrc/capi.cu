@@ -137,6 +137,12 @@ fp8mla_status_t check_kv_dtype(fp8mla_kv_dtype_t t) {
 }
 
 }  // namespace
+
+// The two TMA descriptors of a dense MLA cache (both entry points use this one cached encoder).
+bool mla_kv_maps(const void* kv, int num_pages, CUtensorMap* lat, CUtensorMap* rope) {
+  return mla_maps(kv, num_pages, lat, rope);
+}
+
 }  // namespace fp8mla
 
 using namespace fp8mla;

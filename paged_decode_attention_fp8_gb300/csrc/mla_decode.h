@@ -47,6 +47,9 @@ cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& 
 cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                     int num_units, cudaStream_t stream);
 uint32_t mla_read_and_clear_status();
+// The TMA descriptors of a dense MLA cache [num_pages, 64, 576] E4M3: 128-byte latent boxes
+// (128-byte swizzle) and the 64-byte RoPE box, cached per (pointer, pages, device).
+bool mla_kv_maps(const void* kv, int num_pages, CUtensorMap* lat, CUtensorMap* rope);
 // {source line, block, thread} of the first bounded wait of the dense MLA kernels that ran
 // out since the last call (all 0 if none), and clears it.
 void mla_read_and_clear_timeout_site(uint32_t where[3]);

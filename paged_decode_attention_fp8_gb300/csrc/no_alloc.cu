@@ -44,32 +44,6 @@ void* scratch_for_current_device() {
   return g_scratch_ptr[dev];
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-bool encode_page_view(CUtensorMap* map, const void* kv, int num_pages, uint32_t box_inner, CUtensorMapSwizzle sw) {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kMlaD), static_cast<cuuint64_t>(kMlaPage),
-                              static_cast<cuuint64_t>(num_pages)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kMlaD), static_cast<cuuint64_t>(kMlaD) * kMlaPage};
-  const cuuint32_t box[3] = {box_inner, static_cast<cuuint32_t>(kMlaPage), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 }  // namespace fp8mla
 
@@ -102,9 +76,7 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
   float* qscale = reinterpret_cast<float*>(qbuf + kQBufBytes);
 
   CUtensorMap tm_lat, tm_rope;
-  if (!encode_page_view(&tm_lat, kv_cache, num_pages, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_page_view(&tm_rope, kv_cache, num_pages, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return FP8MLA_ERR_CUDA;
+  if (!mla_kv_maps(kv_cache, num_pages, &tm_lat, &tm_rope)) return FP8MLA_ERR_CUDA;
 
   // One unit per sequence: every sequence is one whole piece, so the split
   // partials (ws_o, ws_ml) are never written or read.  The schedule and the
