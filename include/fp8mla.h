@@ -221,6 +221,35 @@ FP8MLA_API fp8mla_status_t paged_gqa_decode(const void* q, const void* k_cache, 
                                  size_t workspace_bytes, void* out, float* lse, int bs, int h_q, int h_kv,
                                  int head_dim, int page_size, fp8mla_stream_t stream);
 
+/* paged_gqa_decode_ext -- paged_gqa_decode with per-row KV scales and the XQA
+ * options (FlashInfer "add xqa fp8 mha and fp8 kv cache": launcher arguments
+ * for speculative decoding, sliding window and attention sinks; InfiniCore
+ * page, Summary: scales of shape [num_blocks, num_kv_heads, block_size]).
+ *   q            bf16 [bs, q_len, h_q, head_dim]: q_len query tokens per
+ *                sequence, taken to be its last q_len cache positions (token i
+ *                at position s_k - q_len + i)
+ *   k_scale, v_scale  float32 [1] each, or with scale_per_row != 0 one float
+ *                per cached row, [num_blocks, h_kv, page_size], 16-byte aligned
+ *   spec_mask    uint8 [bs, q_len, q_len] (device) or NULL: token i sees key
+ *                s_k - q_len + c of its own block iff spec_mask[b][i][c] != 0;
+ *                NULL = causal inside the block (c <= i).  Keys before the
+ *                block are always visible.
+ *   window       0 = off; W > 0 keeps only keys j with (s_k - q_len + i) - j < W
+ *   sinks        float32 [h_q] (device) or NULL: head h's softmax denominator
+ *                gains e^{sinks[h]} (a key without value; -inf = no sink)
+ *   out          bf16 [bs, q_len, h_q, head_dim]; lse float32 [bs, q_len, h_q]
+ * A row that sees no key gets out = 0 and lse = its sink (-inf without one).
+ * Requires q_len >= 1 and q_len * (h_q / h_kv) <= 16, window >= 0, and the
+ * other requirements of paged_gqa_decode; workspace as paged_gqa_decode's. */
+FP8MLA_API fp8mla_status_t paged_gqa_decode_ext(const void* q, const void* k_cache, const void* v_cache,
+                                                fp8mla_kv_dtype_t kv_dtype, int num_blocks, const float* k_scale,
+                                                const float* v_scale, int scale_per_row, const int32_t* block_table,
+                                                int max_blocks, const int32_t* seqlens, float softmax_scale, int q_len,
+                                                const uint8_t* spec_mask, int window, const float* sinks,
+                                                int num_splits, void* workspace, size_t workspace_bytes, void* out,
+                                                float* lse, int bs, int h_q, int h_kv, int head_dim, int page_size,
+                                                fp8mla_stream_t stream);
+
 FP8MLA_API size_t paged_gqa_workspace_bytes(int bs, int h_q, int head_dim, int max_splits);
 
 /* Number of key shards paged_gqa_decode will use for these arguments

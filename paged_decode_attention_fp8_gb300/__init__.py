@@ -58,6 +58,8 @@ _SIGNATURES = {
     "sparse_mla_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "paged_gqa_decode": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _F, _I, _P, _SZ, _P, _P, _I, _I, _I, _I, _I,
                               _P]),
+    "paged_gqa_decode_ext": (_I, [_P, _P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _F, _I, _P, _I, _P, _I, _P, _SZ,
+                                  _P, _P, _I, _I, _I, _I, _I, _P]),
     "paged_gqa_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "paged_gqa_num_splits": (_I, [_I, _I, _I, _I, _I]),
     "fp8mla_decode_no_alloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _F, _I, _P, _P, _I, _I, _I, _I, _P]),
@@ -321,6 +323,62 @@ def paged_gqa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                                   workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
                                   bs, h_q, h_kv, hd, page, _stream(q.device)),
            "paged_gqa_decode")
+    return out, lse
+
+
+def paged_gqa_decode_ext(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         block_table: torch.Tensor, seqlens: torch.Tensor, k_scale: torch.Tensor,
+                         v_scale: torch.Tensor, softmax_scale: float | None = None, spec_mask=None,
+                         window: int = 0, sinks=None, num_splits: int = 0, max_seqlen: int | None = None,
+                         out=None, lse=None, workspace=None):
+    """Paged GQA decode with per-row scales and the XQA options.  q bf16 [bs, q_len, h_q, hd]
+    (the sequence's last q_len cache positions); k_scale / v_scale float32 [1] or per cached row
+    [num_blocks, h_kv, page]; spec_mask uint8 [bs, q_len, q_len] or None (causal inside the
+    block); window 0 = off; sinks float32 [h_q] or None.  Returns (out bf16 [bs, q_len, h_q, hd],
+    lse [bs, q_len, h_q])."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_cache, "k_cache", None, 4)
+    _need(v_cache, "v_cache", None, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seqlens, "seqlens", torch.int32, 1)
+    _need(k_scale, "k_scale", torch.float32)
+    _need(v_scale, "v_scale", torch.float32)
+    if k_cache.dtype != v_cache.dtype or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must match")
+    bs, q_len, h_q, hd = q.shape
+    num_blocks, h_kv, page, hd2 = k_cache.shape
+    if hd2 != hd:
+        raise ValueError("head_dim mismatch")
+    per_row = k_scale.numel() != 1 or v_scale.numel() != 1
+    if per_row and (tuple(k_scale.shape) != (num_blocks, h_kv, page) or tuple(v_scale.shape) != (num_blocks, h_kv, page)):
+        raise ValueError("per-row scales must both be [num_blocks, h_kv, page]")
+    if spec_mask is not None:
+        _need(spec_mask, "spec_mask", torch.uint8, 3)
+        if tuple(spec_mask.shape) != (bs, q_len, q_len):
+            raise ValueError("spec_mask must be [bs, q_len, q_len]")
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, 1)
+        if sinks.numel() != h_q:
+            raise ValueError("sinks must be [h_q]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(hd)
+    if max_seqlen is None:
+        max_seqlen = block_table.shape[1] * page
+    splits = gqa_num_splits(bs, h_kv, max_seqlen, num_splits)
+    if out is None:
+        out = torch.empty((bs, q_len, h_q, hd), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((bs, q_len, h_q), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = gqa_workspace_bytes(bs, h_q, hd, splits)
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+    _check(lib().paged_gqa_decode_ext(_ptr(q), _ptr(k_cache), _ptr(v_cache), kv_dtype_code(k_cache), num_blocks,
+                                      _ptr(k_scale), _ptr(v_scale), 1 if per_row else 0, _ptr(block_table),
+                                      block_table.shape[1], _ptr(seqlens), float(softmax_scale), q_len,
+                                      _ptr(spec_mask), int(window), _ptr(sinks), splits, _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+                                      bs, h_q, h_kv, hd, page, _stream(q.device)),
+           "paged_gqa_decode_ext")
     return out, lse
 
 

@@ -326,9 +326,25 @@ fp8mla_status_t paged_gqa_decode(const void* q, const void* k_cache, const void*
   fp8mla_status_t st = check_kv_dtype(kv_dtype);
   if (st != FP8MLA_OK) return st;
   if (k_scale == nullptr || v_scale == nullptr) return FP8MLA_ERR_INVALID_ARG;
-  return gqa_decode_entry(q, k_cache, v_cache, num_blocks, k_scale, v_scale, block_table, max_blocks, seqlens,
-                          softmax_scale, num_splits, workspace, workspace_bytes, out, lse, bs, h_q, h_kv, head_dim,
-                          page_size, reinterpret_cast<cudaStream_t>(stream));
+  return gqa_decode_entry(q, k_cache, v_cache, num_blocks, k_scale, v_scale, 0, block_table, max_blocks, seqlens,
+                          softmax_scale, 1, nullptr, 0, nullptr, num_splits, workspace, workspace_bytes, out, lse, bs,
+                          h_q, h_kv, head_dim, page_size, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fp8mla_status_t paged_gqa_decode_ext(const void* q, const void* k_cache, const void* v_cache,
+                                     fp8mla_kv_dtype_t kv_dtype, int num_blocks, const float* k_scale,
+                                     const float* v_scale, int scale_per_row, const int32_t* block_table,
+                                     int max_blocks, const int32_t* seqlens, float softmax_scale, int q_len,
+                                     const uint8_t* spec_mask, int window, const float* sinks, int num_splits,
+                                     void* workspace, size_t workspace_bytes, void* out, float* lse, int bs, int h_q,
+                                     int h_kv, int head_dim, int page_size, fp8mla_stream_t stream) {
+  fp8mla_status_t st = check_kv_dtype(kv_dtype);
+  if (st != FP8MLA_OK) return st;
+  if (k_scale == nullptr || v_scale == nullptr) return FP8MLA_ERR_INVALID_ARG;
+  return gqa_decode_entry(q, k_cache, v_cache, num_blocks, k_scale, v_scale, scale_per_row, block_table, max_blocks,
+                          seqlens, softmax_scale, q_len, spec_mask, window, sinks, num_splits, workspace,
+                          workspace_bytes, out, lse, bs, h_q, h_kv, head_dim, page_size,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 fp8mla_status_t fp8_paged_cache_write(const void* x, int64_t x_token_stride, const int32_t* slot_mapping,

@@ -25,6 +25,17 @@
 //     count within 85% of the best wave efficiency (InfiniCore page,
 //     Summary: the "auto" heuristic); a grid that already fills the GPU is
 //     still cut into about six CTAs per SM so unequal contexts balance.
+//   * Per-row scales [num_blocks, h_kv, 16] (InfiniCore page, Summary): each
+//     page's 16 K and 16 V scales arrive by bulk copy with its tiles; V rows
+//     are dequantised to f16 by the converter warps, K rows stay exact and
+//     their scale multiplies the token's scores in fp32 in the softmax.
+//   * XQA options (FlashInfer "add xqa fp8 mha and fp8 kv cache", launcher
+//     arguments): the N = 16 MMA columns hold (query token, head) pairs of a
+//     speculative block of q_len tokens (the last q_len cache positions),
+//     masked per column by the block mask (or causally) and a sliding window
+//     (steps wholly before every token's window are not loaded); sink logits
+//     join the denominator once, in the epilogue or the combine.  Each option
+//     set is its own kernel instance, so plain decode carries none of it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -61,26 +72,38 @@ constexpr float kTau = 8.0f;
 constexpr uint32_t kTmemCols = 256, kTS = 0, kTO = 32, kTK = 64;
 
 struct Params {
-  const uint16_t* q;           // bf16 [bs, h_q, 128]
+  const uint16_t* q;           // bf16 [bs, q_len, h_q, 128]
   const int32_t* block_table;  // [bs, max_blocks]
   const int32_t* seqlens;      // [bs]
-  const float* k_scale;
+  const float* k_scale;        // [1], or per cached row [num_blocks, h_kv, 16] when scale_rows
   const float* v_scale;
-  uint16_t* out;               // bf16 [bs, h_q, 128]
-  float* lse;                  // [bs, h_q]
+  const uint8_t* spec_mask;    // [bs, q_len, q_len] (nonzero = visible) or null: causal inside the block
+  const float* sinks;          // [h_q] sink logits or null
+  uint16_t* out;               // bf16 [bs, q_len, h_q, 128]
+  float* lse;                  // [bs, q_len, h_q]
   float* ws_o;                 // [bs * h_kv * splits, 16, 128]  -- indexed per (b, kv head) sequence
   float2* ws_ml;
   int num_blocks, max_blocks, bs, h_q, h_kv, group, splits;
+  int q_len;                   // query tokens per sequence; MMA column n = token (n / group), head (n % group)
+  int window;                  // sliding window W (0 = off): token at position p sees keys j with p - j < W
+  int scale_rows;              // 1: k_scale / v_scale are per-row arrays
   float softmax_scale;
 };
 
 struct Smem {
+  float row_scale[kRawStages][2][kTok];  // per-row scales of a raw stage's K and V rows (scale_rows)
   uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   uint64_t cvt_ready[kV16Slots], k16_empty[kV16Slots], v16_empty[kV16Slots];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];  // by step parity
   uint64_t q_full, final_mma, xchg;
   uint32_t tmem_base, abort_flag;
   float qs[kN];
+  uint16_t vis_block[kN];  // per query token: bit c = key c of the speculative block visible
+  // per-row K scales of a step's token rows, from the converter to the softmax (by step % 4; a slot
+  // is rewritten four steps later, after the softmax read it: the converter's step i + 4 follows
+  // Q.K^T of step i + 2, which follows the softmax's read of step i)
+  float kscale_s[4][kTok];
+  uint64_t ks_ready[4];
   float red[2][4][kN];   // per-warp partial maxima, double-buffered by step parity
   float red2[4][kN];
 };
@@ -106,11 +129,43 @@ __device__ __forceinline__ int pow2_exp_f16(float amax) {
 
 __device__ __forceinline__ uint32_t f16x2_of_e4m3x2(uint32_t two_bytes) { return e4m3x2_to_f16x2(two_bytes); }
 
-// kG: the softmax handles heads [0, kG) of the N = 16 MMA columns (kG >= the head group).
-template <int kG>
+// Two E4M3 codes times a row's dequantisation scale, as f16 (the dequantised values, rounded once).
+__device__ __forceinline__ uint32_t f16x2_scaled(uint32_t two_bytes, float sc) {
+  const uint32_t h = e4m3x2_to_f16x2(two_bytes);
+  return pack_f16x2(f16_lo(h) * sc, f16_hi(h) * sc);
+}
+
+// The end of one output row: key weights summed to l against reference m (log2
+// units of the scaled scores), an optional sink logit `sink` (natural units,
+// -inf = none) joining the denominator once.  Returns the output factor f
+// (times the accumulated P.V) and the row's LSE (natural log).  No key and no
+// sink: f = 0, LSE -inf; no key with a sink: f = 0, LSE = sink.
+__device__ __forceinline__ void finish_row(float m, float l, float sink, float v_scale, float* f, float* lse) {
+  if (sink == kNegInf) {
+    *f = l > 0.f ? v_scale / l : 0.f;
+    *lse = l > 0.f ? (m + lg2_approx(l)) * kLn2 : kNegInf;
+    return;
+  }
+  const float sk2 = sink * kLog2e;
+  if (!(l > 0.f)) {
+    *f = 0.f;
+    *lse = sink;
+    return;
+  }
+  const float mm = fmaxf(m, sk2);
+  const float wk = ex2_approx(m - mm);
+  const float den = l * wk + ex2_approx(sk2 - mm);
+  *f = v_scale * wk / den;
+  *lse = (mm + lg2_approx(den)) * kLn2;
+}
+
+// kG: the softmax handles MMA columns [0, kG) of the N = 16 (kG >= q_len * group).
+// kMode bit 0: per-row scales; bit 1: the XQA options (q_len > 1, a mask, a window or sinks).
+template <int kG, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const Params prm) {
+  constexpr bool kRows = (kMode & 1) != 0, kExt = (kMode & 2) != 0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -134,10 +189,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_k = 0;
     n_pages = 0;
   }
-  const int n_steps_all = (n_pages + kPagesPerStep - 1) / kPagesPerStep;
-  const int st0 = static_cast<int>((static_cast<long long>(split) * n_steps_all) / prm.splits);
-  const int st1 = static_cast<int>((static_cast<long long>(split + 1) * n_steps_all) / prm.splits);
+  // The query block's tokens are the last q_len cache positions; with a
+  // sliding window no token sees a key before k_lo, so steps wholly before it
+  // are left out of the split partition.
+  const int start = s_k - prm.q_len;  // position of the block's first token
+  const int k_lo = (kExt && prm.window > 0) ? max(0, start - prm.window + 1) : 0;
+  const int n_steps_total = (n_pages + kPagesPerStep - 1) / kPagesPerStep;
+  const int step_lo = min(k_lo / kTok, n_steps_total);
+  const int n_steps_all = n_steps_total - step_lo;
+  const int st0 = step_lo + static_cast<int>((static_cast<long long>(split) * n_steps_all) / prm.splits);
+  const int st1 = step_lo + static_cast<int>((static_cast<long long>(split + 1) * n_steps_all) / prm.splits);
   const int nsteps = st1 - st0;
+  const int ncols = prm.q_len * prm.group;  // MMA columns that hold (token, head) pairs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRawStages; ++s) {
@@ -156,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->pv_done[bf], 1);
     }
     mbar_init(&sm->q_full, 4);
+    for (int k = 0; k < 4; ++k) mbar_init(&sm->ks_ready[k], 4);  // one arrival per converter warp
     mbar_init(&sm->final_mma, 1);
     mbar_init(&sm->xchg, 4);
     sm->abort_flag = 0;
@@ -199,13 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         ok = use == 0 || wait_bounded(&sm->raw_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa);
         if (ok) {
-          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd);
+          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd + (kRows ? 2u * np * kPage * 4u : 0u));
           uint8_t* sb = smem + st * kRawStageBytes;
 #pragma unroll
           for (int p = 0; p < kPagesPerStep; ++p) {
             if (p >= np) break;
             tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->raw_full[st], 0, rows[p], 0);
             tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->raw_full[st], 0, rows[p], 0);
+            if constexpr (kRows) {  // the page's 16 row scales of K and of V (rows are the scales' index too)
+              bulk_load(&sm->row_scale[st][0][p * kPage], prm.k_scale + rows[p], kPage * 4u, &sm->raw_full[st]);
+              bulk_load(&sm->row_scale[st][1][p * kPage], prm.v_scale + rows[p], kPage * 4u, &sm->raw_full[st]);
+            }
           }
         }
       }
@@ -285,11 +353,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         vraw[c] = live ? *reinterpret_cast<const uint4*>(sb + kOffRawV + r * 128 + ((c ^ sw) << 4))
                        : make_uint4(0, 0, 0, 0);
       }
+      // per-row scales: V rows are dequantised here; K rows stay exact and their scale goes to the
+      // softmax, which applies it to the token's scores in fp32 (per-tensor scales come later)
+      float vsc = 1.f, ksc = 1.f;
+      if constexpr (kRows) {
+        vsc = live ? sm->row_scale[st][1][r] : 1.f;
+        ksc = live ? sm->row_scale[st][0][r] : 1.f;
+      }
+      auto cvt = [&](uint32_t two, float sc) {
+        if constexpr (kRows) return f16x2_scaled(two, sc);
+        return f16x2_of_e4m3x2(two);
+      };
       warp_arrive(&sm->raw_empty[st]);  // the raw stage may be refilled
       // the K slot and the V slot of this step were last read two steps ago
       if (i >= kV16Slots && (!warp_wait(&sm->k16_empty[vs], ((i - kV16Slots) / kV16Slots) & 1, abort_flag) ||
                              !warp_wait(&sm->v16_empty[vs], ((i - kV16Slots) / kV16Slots) & 1, abort_flag)))
         break;
+      if constexpr (kRows) {  // (the slot's step i - 4 was read: Q.K^T of step i - 2 has completed)
+        sm->kscale_s[i & 3][r] = ksc;
+        warp_arrive(&sm->ks_ready[i & 3]);
+      }
       tc_fence_after();
 #pragma unroll
       for (int half = 0; half < 2; ++half) {  // K: dims [64 half, 64 half + 64) -> 32 columns of f16 pairs
@@ -312,10 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 8; ++c) {   // V: 16 E4M3 -> 16 f16 (two 16-byte chunks)
         const uint4 x = vraw[c];
-        const uint4 vo = make_uint4(f16x2_of_e4m3x2(x.x & 0xFFFFu), f16x2_of_e4m3x2(x.x >> 16),
-                                    f16x2_of_e4m3x2(x.y & 0xFFFFu), f16x2_of_e4m3x2(x.y >> 16));
-        const uint4 vo2 = make_uint4(f16x2_of_e4m3x2(x.z & 0xFFFFu), f16x2_of_e4m3x2(x.z >> 16),
-                                     f16x2_of_e4m3x2(x.w & 0xFFFFu), f16x2_of_e4m3x2(x.w >> 16));
+        const uint4 vo = make_uint4(cvt(x.x & 0xFFFFu, vsc), cvt(x.x >> 16, vsc), cvt(x.y & 0xFFFFu, vsc),
+                                    cvt(x.y >> 16, vsc));
+        const uint4 vo2 = make_uint4(cvt(x.z & 0xFFFFu, vsc), cvt(x.z >> 16, vsc), cvt(x.w & 0xFFFFu, vsc),
+                                     cvt(x.w >> 16, vsc));
         // dims [16 c, 16 c + 16): f16 atom c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1
         uint8_t* dv = vslot + (c / 4) * kCvtAtom + r * 128;
         *reinterpret_cast<uint4*>(dv + (((2 * (c % 4)) ^ sw) << 4)) = vo;
@@ -339,15 +422,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++xphase;
       return ok;
     };
-    const float k_scale = *prm.k_scale, v_scale = *prm.v_scale;
-    const uint16_t* qgrp = prm.q + (static_cast<size_t>(b) * prm.h_q + kvh * prm.group) * kHd;
+    // per-row scales were applied by the converter warps
+    const float k_scale = kRows ? 1.f : *prm.k_scale, v_scale = kRows ? 1.f : *prm.v_scale;
+    // column n of the MMA: query token n / group, head kvh * group + n % group
+    auto q_row = [&](int n) -> const uint16_t* {
+      return prm.q + ((static_cast<size_t>(b) * prm.q_len + n / prm.group) * prm.h_q + kvh * prm.group +
+                      n % prm.group) * kHd;
+    };
+    if (kExt && r < prm.q_len) {  // which keys of the speculative block token r sees: the mask row, or c <= r
+      uint32_t bits = 0;
+      if (prm.spec_mask != nullptr) {
+        const uint8_t* row = prm.spec_mask + (static_cast<size_t>(b) * prm.q_len + r) * prm.q_len;
+        for (int c = 0; c < prm.q_len; ++c)
+          if (__ldg(row + c)) bits |= 1u << c;
+      } else {
+        bits = (2u << r) - 1u;
+      }
+      sm->vis_block[r] = static_cast<uint16_t>(bits);
+    }
     {
-      // Q tile: thread (head qh, eighth qj) converts dims [16 qj, 16 qj + 16) to f16 / qs
+      // Q tile: thread (column qh, eighth qj) converts dims [16 qj, 16 qj + 16) to f16 / qs
       const int qh = r / 8, qj = r % 8;
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (qh < prm.group) {
-        v0 = __ldg(reinterpret_cast<const uint4*>(qgrp + qh * kHd + qj * 16));
-        v1 = __ldg(reinterpret_cast<const uint4*>(qgrp + qh * kHd + qj * 16 + 8));
+      if (qh < ncols) {
+        v0 = __ldg(reinterpret_cast<const uint4*>(q_row(qh) + qj * 16));
+        v1 = __ldg(reinterpret_cast<const uint4*>(q_row(qh) + qj * 16 + 8));
       }
       float amax = 0.f;
       const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -372,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = r; i < 2 * kPBytes / 16; i += 128) reinterpret_cast<uint4*>(p_tile)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
-    bool ok = xsync();  // qs[] and the zeroed P tile complete
+    bool ok = xsync();  // qs[], the block's visibility bits and the zeroed P tile complete
     float c_h[kG], m_h[kG], l_h[kG];
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
@@ -380,6 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_h[h] = kNegInf;
       l_h[h] = 0.f;
     }
+    const uint32_t grp_bits = (1u << prm.group) - 1u;
+    const uint32_t pad_cols = ncols >= 32 ? 0u : (0xFFFFFFFFu << ncols);  // padding columns: no output
+    const bool plain = !kExt || (prm.q_len == 1 && prm.window == 0);
     for (int i = 0; ok && i < nsteps; ++i) {
       const int bf = i & 1;
       const int tok = (st0 + i) * kTok + r;
@@ -392,12 +494,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t s[kN];
       tmem_ld16(lane_base + kTS + bf * kN, s);
+      float kro = 1.f;  // this token's K row scale
+      if constexpr (kRows) {
+        if (!warp_wait(&sm->ks_ready[i & 3], (i >> 2) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        kro = sm->kscale_s[i & 3][r];
+      }
       tmem_ld_wait();
       tc_fence_before();
       warp_arrive(&sm->s_free[bf]);
+      // columns that see this thread's key: per query token ti, keys before the block always,
+      // keys inside it by the token's bits, and (window W) only if ti - c_blk < W (the token's
+      // position less than W past the key)
+      uint32_t colvis = pad_cols;
+      if (!kExt || plain) {  // one query token, no window: every column sees every live key
+        colvis = live ? 0xFFFFFFFFu : pad_cols;
+      } else if (live) {
+        const int c_blk = tok - start;
+        for (int ti = 0; ti < prm.q_len; ++ti) {
+          const bool vis = (c_blk < 0 || ((sm->vis_block[ti] >> c_blk) & 1u)) &&
+                           (prm.window == 0 || ti - c_blk < prm.window);
+          if (vis) colvis |= grp_bits << (ti * prm.group);
+        }
+      }
       float v[kG];
 #pragma unroll
-      for (int h = 0; h < kG; ++h) v[h] = live ? __uint_as_float(s[h]) * c_h[h] : kNegInf;
+      for (int h = 0; h < kG; ++h) v[h] = ((colvis >> h) & 1u) ? __uint_as_float(s[h]) * kro * c_h[h] : kNegInf;
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
         float x = v[h];
@@ -484,27 +608,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
-        if (h >= prm.group) break;
+        if (h >= ncols) break;
         const float lsum = (sm->red2[0][h] + sm->red2[1][h]) + (sm->red2[2][h] + sm->red2[3][h]);
-        const int hq = kvh * prm.group + h;
+        const int hq = kvh * prm.group + h % prm.group;
+        const size_t orow = (static_cast<size_t>(b) * prm.q_len + h / prm.group) * prm.h_q + hq;
         if (whole) {
-          const float f = lsum > 0.f ? v_scale / lsum : 0.f;
-          prm.out[(static_cast<size_t>(b) * prm.h_q + hq) * kHd + r] =
-              static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[h]) * f, 0.f));
-          if (r == 0)
-            prm.lse[static_cast<size_t>(b) * prm.h_q + hq] =
-                lsum > 0.f ? (m_h[h] + lg2_approx(lsum)) * kLn2 : kNegInf;
+          float f, lse_v;
+          finish_row(m_h[h], lsum, (kExt && prm.sinks) ? prm.sinks[hq] : kNegInf, v_scale, &f, &lse_v);
+          prm.out[orow * kHd + r] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[h]) * f, 0.f));
+          if (r == 0) prm.lse[orow] = lse_v;
         } else {
           prm.ws_o[(slot * kN + h) * kHd + r] = __uint_as_float(o[h]) * v_scale;
           if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(lsum > 0.f ? m_h[h] : kNegInf, lsum);
         }
       }
     } else if (ok && nsteps == 0) {
-      for (int h = 0; h < prm.group; ++h) {
-        const int hq = kvh * prm.group + h;
-        if (whole) {
-          prm.out[(static_cast<size_t>(b) * prm.h_q + hq) * kHd + r] = 0;
-          if (r == 0) prm.lse[static_cast<size_t>(b) * prm.h_q + hq] = kNegInf;
+      for (int h = 0; h < ncols; ++h) {
+        const int hq = kvh * prm.group + h % prm.group;
+        const size_t orow = (static_cast<size_t>(b) * prm.q_len + h / prm.group) * prm.h_q + hq;
+        if (whole) {  // no key: out 0, lse the sink's logit (-inf without one)
+          prm.out[orow * kHd + r] = 0;
+          if (r == 0) prm.lse[orow] = (kExt && prm.sinks) ? prm.sinks[hq] : kNegInf;
         } else {
           prm.ws_o[(slot * kN + h) * kHd + r] = 0.f;
           if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(kNegInf, 0.f);
@@ -521,22 +645,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge of split partials: one warp per (sequence = (b, kv head), head), lane l owns 4 dims.
+// Merge of split partials: one warp per (sequence = (b, kv head), column = (token, head)), lane l owns
+// 4 dims; a sink logit joins the merged denominator once.
 __global__ void gqa_combine_kernel(const float* __restrict__ ws_o, const float2* __restrict__ ws_ml, int splits,
-                                   int group, int h_q, int h_kv, uint16_t* __restrict__ out, float* __restrict__ lse) {
+                                   int group, int q_len, int h_q, int h_kv, const float* __restrict__ sinks,
+                                   uint16_t* __restrict__ out, float* __restrict__ lse) {
   griddep_wait();  // launched as a dependent of the decode kernel
   const int seq = blockIdx.x;
   const int h = blockIdx.y * 4 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  if (h >= group) return;
+  if (h >= q_len * group) return;
   const int b = seq / h_kv, kvh = seq % h_kv;
-  const size_t row = static_cast<size_t>(b) * h_q + kvh * group + h;
+  const int hq = kvh * group + h % group;
+  const size_t row = (static_cast<size_t>(b) * q_len + h / group) * h_q + hq;
+  const float sink = sinks ? sinks[hq] : kNegInf;
   float big_m = kNegInf;
   for (int s = 0; s < splits; ++s) big_m = fmaxf(big_m, ws_ml[(static_cast<size_t>(seq) * splits + s) * kN + h].x);
   uint16_t* orow = out + row * kHd + lane * 4;
-  if (big_m == kNegInf) {
+  if (big_m == kNegInf) {  // no key: out 0, lse the sink's logit (-inf without one)
     *reinterpret_cast<uint2*>(orow) = make_uint2(0, 0);
-    if (lane == 0) lse[row] = kNegInf;
+    if (lane == 0) lse[row] = sink;
     return;
   }
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, big_l = 0.f;
@@ -552,10 +680,11 @@ __global__ void gqa_combine_kernel(const float* __restrict__ ws_o, const float2*
     acc[2] += wgt * v.z;
     acc[3] += wgt * v.w;
   }
-  const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
+  float inv, lse_v;
+  finish_row(big_m, big_l, sink, 1.f, &inv, &lse_v);
   *reinterpret_cast<uint2*>(orow) =
       make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
-  if (lane == 0) lse[row] = big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 : kNegInf;
+  if (lane == 0) lse[row] = lse_v;
 }
 
 // ---------------------------------------------------------------- host ----
@@ -625,12 +754,15 @@ size_t gqa_workspace_bytes(int bs, int h_q, int head_dim, int max_splits) {
 }
 
 fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void* v_cache, int num_blocks,
-                                 const float* k_scale, const float* v_scale, const int32_t* block_table,
-                                 int max_blocks, const int32_t* seqlens, float softmax_scale, int num_splits,
-                                 void* workspace, size_t workspace_bytes, void* out, float* lse, int bs, int h_q,
-                                 int h_kv, int head_dim, int page_size, cudaStream_t stream) {
+                                 const float* k_scale, const float* v_scale, int scale_rows,
+                                 const int32_t* block_table, int max_blocks, const int32_t* seqlens,
+                                 float softmax_scale, int q_len, const uint8_t* spec_mask, int window,
+                                 const float* sinks, int num_splits, void* workspace, size_t workspace_bytes,
+                                 void* out, float* lse, int bs, int h_q, int h_kv, int head_dim, int page_size,
+                                 cudaStream_t stream) {
   if (head_dim != gqa::kHd || page_size != gqa::kPage || bs < 0 || h_q < 1 || h_kv < 1 || h_q % h_kv != 0 ||
-      h_q / h_kv > gqa::kN || num_blocks < 1 || max_blocks < 1 || num_splits < 0 || !(softmax_scale > 0.f))
+      q_len < 1 || static_cast<long long>(q_len) * (h_q / h_kv) > gqa::kN || window < 0 || num_blocks < 1 ||
+      max_blocks < 1 || num_splits < 0 || !(softmax_scale > 0.f))
     return FP8MLA_ERR_INVALID_ARG;
   if (bs == 0) return FP8MLA_OK;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr || seqlens == nullptr ||
@@ -638,6 +770,9 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
     return FP8MLA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
        reinterpret_cast<uintptr_t>(v_cache)) & 15u)
+    return FP8MLA_ERR_INVALID_ARG;
+  // per-row scales arrive by 64-byte bulk copies
+  if (scale_rows && ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 15u))
     return FP8MLA_ERR_INVALID_ARG;
   int splits = std::min(num_splits, 1 << 16);
   if (splits == 0) {  // auto: the waves rule for this GPU, with the block table's capacity as the longest context
@@ -661,6 +796,11 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   prm.seqlens = seqlens;
   prm.k_scale = k_scale;
   prm.v_scale = v_scale;
+  prm.scale_rows = scale_rows ? 1 : 0;
+  prm.spec_mask = spec_mask;
+  prm.sinks = sinks;
+  prm.q_len = q_len;
+  prm.window = window;
   prm.out = static_cast<uint16_t*>(out);
   prm.lse = lse;
   const size_t slots = static_cast<size_t>(bs) * h_kv * splits;
@@ -678,28 +818,38 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   prm.softmax_scale = softmax_scale;
   static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
   if (configure_once(configured, [] {
-        cudaError_t e = cudaFuncSetAttribute(gqa::gqa_decode_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(gqa::kSmemBytes));
-        if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(gqa::gqa_decode_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(gqa::kSmemBytes));
-        if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(gqa::gqa_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(gqa::kSmemBytes));
+        const void* fns[12] = {
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 0>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 0>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 0>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 1>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 1>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 1>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 2>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 2>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 2>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 3>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 3>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 3>)};
+        cudaError_t e = cudaSuccess;
+        for (const void* f : fns)
+          if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(gqa::kSmemBytes));
         return e;
       }) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   const long long grid = static_cast<long long>(bs) * h_kv * splits;
   if (grid > 0x7FFFFFFFll) return FP8MLA_ERR_INVALID_ARG;
-  auto kernel = prm.group <= 4 ? gqa::gqa_decode_kernel<4>
-                                : (prm.group <= 8 ? gqa::gqa_decode_kernel<8> : gqa::gqa_decode_kernel<16>);
+  const int ncols = q_len * prm.group;
+  using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const gqa::Params);
+  static const KernelFn table[4][3] = {
+      {gqa::gqa_decode_kernel<4, 0>, gqa::gqa_decode_kernel<8, 0>, gqa::gqa_decode_kernel<16, 0>},
+      {gqa::gqa_decode_kernel<4, 1>, gqa::gqa_decode_kernel<8, 1>, gqa::gqa_decode_kernel<16, 1>},
+      {gqa::gqa_decode_kernel<4, 2>, gqa::gqa_decode_kernel<8, 2>, gqa::gqa_decode_kernel<16, 2>},
+      {gqa::gqa_decode_kernel<4, 3>, gqa::gqa_decode_kernel<8, 3>, gqa::gqa_decode_kernel<16, 3>}};
+  const bool ext = q_len > 1 || window > 0 || spec_mask != nullptr || sinks != nullptr;
+  const KernelFn kernel = table[(scale_rows ? 1 : 0) | (ext ? 2 : 0)][ncols <= 4 ? 0 : (ncols <= 8 ? 1 : 2)];
   if (launch_dependent(kernel, dim3(static_cast<unsigned>(grid)), dim3(gqa::kThreads), gqa::kSmemBytes, stream, tk,
                        tv, prm) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   if (splits > 1) {
-    dim3 cg(static_cast<unsigned>(bs * h_kv), (prm.group + 3) / 4);
+    dim3 cg(static_cast<unsigned>(bs * h_kv), (ncols + 3) / 4);
     if (launch_dependent(gqa::gqa_combine_kernel, cg, dim3(128), 0, stream, prm.ws_o, prm.ws_ml, splits, prm.group,
-                         h_q, h_kv, prm.out, lse) != cudaSuccess)
+                         q_len, h_q, h_kv, sinks, prm.out, lse) != cudaSuccess)
       return FP8MLA_ERR_CUDA;
   }
   return FP8MLA_OK;

@@ -490,3 +490,30 @@ def materialise(inp: CacheWriteInputs, tokens=None, device=None) -> torch.Tensor
     idx = (t % base.shape[0]).to(base.device)
     f = torch.from_numpy(np.ldexp(1.0, inp.exponent[t.numpy()]).astype(np.float32)).to(base.device)
     return (base[idx].float() * f[:, None, None]).to(torch.bfloat16)
+
+
+def per_row_scales(seed: int, purpose: int, shape, base: float) -> torch.Tensor:
+    """Positive float32 scales, one per cached row: base * 2^u with u uniform in [-2, 2]
+    (a seeded stand-in for the amax / 448 of each row)."""
+    n = int(np.prod(shape))
+    u = uniform(seed, purpose, n).reshape(shape) * 4.0 - 2.0
+    return torch.from_numpy((base * np.exp2(u)).astype(np.float32))
+
+
+def gqa_block_q(seed: int, bs: int, q_len: int, h_q: int, hd: int = 128) -> torch.Tensor:
+    """bf16 [bs, q_len, h_q, hd] N(0, 1) queries of a speculative block of q_len tokens."""
+    return to_bf16(normal(seed, 31, (bs, q_len, h_q, hd)))
+
+
+def spec_mask(seed: int, bs: int, q_len: int) -> torch.Tensor:
+    """uint8 [bs, q_len, q_len] speculative-decoding mask: each token sees itself and a seeded
+    half of the block's other keys (a tree of draft tokens need not be causal)."""
+    m = (uniform(seed, 32, bs * q_len * q_len).reshape(bs, q_len, q_len) < 0.5).astype(np.uint8)
+    idx = np.arange(q_len)
+    m[:, idx, idx] = 1
+    return torch.from_numpy(m)
+
+
+def sink_logits(seed: int, h_q: int) -> torch.Tensor:
+    """float32 [h_q] attention-sink logits, uniform in [-2, 6] (the scale of the scaled scores)."""
+    return torch.from_numpy((uniform(seed, 33, h_q) * 8.0 - 2.0).astype(np.float32))

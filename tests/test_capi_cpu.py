@@ -164,6 +164,30 @@ def test_gqa_small_workspace_and_empty_batch():
     assert _gqa(bs=0, q=None, out=None, lse=None) == 0      # nothing to do, nothing touched
 
 
+def _gqa_ext(**over):
+    a = dict(q=1 << 20, k=1 << 20, v=1 << 20, dtype=fm.KV_E4M3, nb=64, ks=1 << 20, vs=1 << 20, rows=0,
+             bt=1 << 20, mb=8, sl=1 << 20, scale=0.08, q_len=1, mask=None, window=0, sinks=None, splits=1,
+             ws=1 << 20, ws_bytes=1 << 40, out=1 << 20, lse=1 << 20, bs=2, h_q=32, h_kv=8, hd=128, page=16)
+    a.update(over)
+    return fm.lib().paged_gqa_decode_ext(a["q"], a["k"], a["v"], a["dtype"], a["nb"], a["ks"], a["vs"], a["rows"],
+                                         a["bt"], a["mb"], a["sl"], a["scale"], a["q_len"], a["mask"], a["window"],
+                                         a["sinks"], a["splits"], a["ws"], a["ws_bytes"], a["out"], a["lse"],
+                                         a["bs"], a["h_q"], a["h_kv"], a["hd"], a["page"], None)
+
+
+@pytest.mark.parametrize("over", [dict(q_len=0), dict(q_len=5), dict(q_len=2, h_q=72, h_kv=8), dict(window=-1),
+                                  dict(rows=1, ks=(1 << 20) + 4), dict(rows=1, vs=(1 << 20) + 8), dict(ks=None),
+                                  dict(hd=64), dict(h_q=30)])
+def test_gqa_ext_argument_refusals(over):
+    # group 4: q_len * group must stay <= 16; per-row scale arrays must be 16-byte aligned
+    assert _gqa_ext(**over) == 1
+
+
+def test_gqa_ext_foreign_encoding_and_empty_batch():
+    assert _gqa_ext(dtype=fm.KV_E4M3FNUZ) == 2
+    assert _gqa_ext(bs=0, q=None, out=None, lse=None, q_len=4) == 0
+
+
 def _sparse(**over):
     a = dict(q=1 << 20, kv=1 << 20, dtype=fm.KV_E4M3, n=131072, idx=1 << 20, topk=2048, scale=1 << 20, sm=0.04,
              splits=1, ws=1 << 20, ws_bytes=1 << 40, out=1 << 20, lse=1 << 20, dot=fm.DOT_FP8, s_q=2, h_q=16)
