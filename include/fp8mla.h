@@ -170,6 +170,27 @@ FP8MLA_API fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp
                               void* out, float* lse, fp8mla_dot_mode_t dot_mode, int b, int s_q, int h_q,
                               fp8mla_stream_t stream);
 
+/* fp8mla_decode_ext -- fp8mla_decode with one dequantisation scale per cached
+ * row (InfiniCore page, Summary: FP8 caches carry scales of shape
+ * [num_blocks, num_kv_heads, block_size]; here one KV head, so [num_pages, 64]).
+ *   kv_scale_rows  float32 [num_pages, 64] (device, 16-byte aligned) or NULL;
+ *                  when set, row t of physical page p (its 512 latent and 64
+ *                  RoPE values, K and V alike) is E4M3 code times
+ *                  kv_scale_rows[p * 64 + t], every scale of a row a key uses
+ *                  must be positive and finite, kv_scale is ignored (may be
+ *                  NULL), and only FP8MLA_DOT_FP8 is accepted
+ *                  (FP8MLA_ERR_INVALID_ARG otherwise)
+ *   kv_scale_rows NULL: exactly fp8mla_decode.
+ * Other arguments, results and errors as fp8mla_decode. */
+FP8MLA_API fp8mla_status_t fp8mla_decode_ext(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype,
+                                             int num_pages, const int32_t* block_table, int max_pages,
+                                             const int32_t* cache_seqlens, const float* kv_scale,
+                                             const float* kv_scale_rows, float softmax_scale, int causal,
+                                             const int32_t* tile_sched, const int32_t* num_splits, int num_units,
+                                             void* workspace, size_t workspace_bytes, void* out, float* lse,
+                                             fp8mla_dot_mode_t dot_mode, int b, int s_q, int h_q,
+                                             fp8mla_stream_t stream);
+
 /* ----------------------------------------------------------- sparse MLA ---
  * sparse_mla_decode -- query token t attends to the cache rows
  * topk_idx[t][0..topk) (an index of -1 is skipped), d = dv = 512 rope-free.

@@ -54,6 +54,8 @@ _SIGNATURES = {
     "fp8mla_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "fp8mla_decode": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _F, _I, _P, _P, _I, _P, _SZ, _P, _P, _I, _I, _I, _I,
                            _P]),
+    "fp8mla_decode_ext": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _F, _I, _P, _P, _I, _P, _SZ, _P, _P, _I, _I, _I,
+                               _I, _P]),
     "sparse_mla_decode": (_I, [_P, _P, _I, ctypes.c_int64, _P, _I, _P, _F, _I, _P, _SZ, _P, _P, _I, _I, _I, _P]),
     "sparse_mla_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "paged_gqa_decode": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _F, _I, _P, _SZ, _P, _P, _I, _I, _I, _I, _I,
@@ -172,7 +174,9 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
            causal: bool = True, tile_sched: torch.Tensor | None = None,
            num_splits: torch.Tensor | None = None, dot_mode="fp8", out: torch.Tensor | None = None,
            lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
-    """Dense MLA decode.  q bf16 [b, s_q, h_q, 576]; kv_cache E4M3 [num_pages, 64, 576].
+    """Dense MLA decode.  q bf16 [b, s_q, h_q, 576]; kv_cache E4M3 [num_pages, 64, 576];
+    kv_scale float32 [1] (per tensor) or [num_pages, 64] / [num_pages, 1, 64] (one scale per
+    cached row, FP8 dots only).
 
     Returns (out bf16 [b, s_q, h_q, 512], lse float32 [b, s_q, h_q]).
     """
@@ -196,6 +200,17 @@ def decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
     need = workspace_bytes(b, s_q, h_q, units)
     if workspace is None:
         workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=q.device)
+    if kv_scale.numel() != 1:  # one scale per cached row
+        if kv_scale.numel() != kv_cache.shape[0] * MLA_PAGE:
+            raise ValueError("per-row kv_scale must hold num_pages * 64 floats")
+        _check(lib().fp8mla_decode_ext(_ptr(q), _ptr(kv_cache), kv_dtype_code(kv_cache), kv_cache.shape[0],
+                                       _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens), None,
+                                       _ptr(kv_scale), float(softmax_scale), 1 if causal else 0, _ptr(tile_sched),
+                                       _ptr(num_splits), units, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+                                       _dot(dot_mode), b, s_q, h_q, _stream(q.device)),
+               "fp8mla_decode_ext")
+        return out, lse
     _check(lib().fp8mla_decode(_ptr(q), _ptr(kv_cache), kv_dtype_code(kv_cache), kv_cache.shape[0],
                                _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens), _ptr(kv_scale),
                                float(softmax_scale), 1 if causal else 0, _ptr(tile_sched), _ptr(num_splits),

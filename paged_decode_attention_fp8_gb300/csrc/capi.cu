@@ -197,18 +197,25 @@ fp8mla_status_t fp8mla_get_metadata(const int32_t* cache_seqlens, int b, int h_q
   return FP8MLA_OK;
 }
 
-fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype, int num_pages,
-                              const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
-                              const float* kv_scale, float softmax_scale, int causal, const int32_t* tile_sched,
-                              const int32_t* num_splits, int num_units, void* workspace, size_t workspace_bytes,
-                              void* out, float* lse, fp8mla_dot_mode_t dot_mode, int b, int s_q, int h_q,
-                              fp8mla_stream_t stream) {
+}  // extern "C"
+
+namespace fp8mla {
+namespace {
+// fp8mla_decode and fp8mla_decode_ext: kv_rows non-null = per-row scales [num_pages, 64].
+fp8mla_status_t mla_decode_call(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype, int num_pages,
+                                const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                                const float* kv_scale, const float* kv_rows, float softmax_scale, int causal,
+                                const int32_t* tile_sched, const int32_t* num_splits, int num_units, void* workspace,
+                                size_t workspace_bytes, void* out, float* lse, fp8mla_dot_mode_t dot_mode, int b,
+                                int s_q, int h_q, fp8mla_stream_t stream) {
   fp8mla_status_t st = check_kv_dtype(kv_dtype);
   if (st != FP8MLA_OK) return st;
   if (b < 0 || s_q < 1 || h_q < 1 || s_q * h_q > kMlaRows || num_units < 1 || num_pages < 1 || max_pages < 1)
     return FP8MLA_ERR_INVALID_ARG;
   if (dot_mode != FP8MLA_DOT_FP8 && dot_mode != FP8MLA_DOT_16BIT) return FP8MLA_ERR_INVALID_ARG;
-  if (kv_scale == nullptr) return FP8MLA_ERR_INVALID_ARG;  // an FP8 cache without its scale
+  if (kv_scale == nullptr && kv_rows == nullptr) return FP8MLA_ERR_INVALID_ARG;  // an FP8 cache without its scale
+  // per-row scales: FP8 dots only, arriving by 256-byte bulk copies
+  if (kv_rows != nullptr && (dot_mode != FP8MLA_DOT_FP8 || !aligned(kv_rows, 16))) return FP8MLA_ERR_INVALID_ARG;
   if (b == 0) return FP8MLA_OK;
   if (q == nullptr || kv_cache == nullptr || block_table == nullptr || cache_seqlens == nullptr ||
       tile_sched == nullptr || num_splits == nullptr || out == nullptr || lse == nullptr || workspace == nullptr)
@@ -223,11 +230,12 @@ fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dty
 
   const MlaWorkspace wl = mla_workspace_layout(b, num_units);
   char* ws = static_cast<char*>(workspace);
-  MlaParams prm;
+  MlaParams prm{};
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_table = block_table;
   prm.seqlens = cache_seqlens;
   prm.kv_scale = kv_scale;
+  prm.kv_rows = kv_rows;
   prm.tile_sched = tile_sched;
   prm.num_splits = num_splits;
   prm.ws_o = reinterpret_cast<uint16_t*>(ws + wl.o);
@@ -271,6 +279,33 @@ fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dty
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
   if (timed) timer.timed = true;
   return FP8MLA_OK;
+}
+}  // namespace
+}  // namespace fp8mla
+
+extern "C" {
+
+fp8mla_status_t fp8mla_decode(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype, int num_pages,
+                              const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                              const float* kv_scale, float softmax_scale, int causal, const int32_t* tile_sched,
+                              const int32_t* num_splits, int num_units, void* workspace, size_t workspace_bytes,
+                              void* out, float* lse, fp8mla_dot_mode_t dot_mode, int b, int s_q, int h_q,
+                              fp8mla_stream_t stream) {
+  if (kv_scale == nullptr && check_kv_dtype(kv_dtype) == FP8MLA_OK) return FP8MLA_ERR_INVALID_ARG;
+  return mla_decode_call(q, kv_cache, kv_dtype, num_pages, block_table, max_pages, cache_seqlens, kv_scale, nullptr,
+                         softmax_scale, causal, tile_sched, num_splits, num_units, workspace, workspace_bytes, out,
+                         lse, dot_mode, b, s_q, h_q, stream);
+}
+
+fp8mla_status_t fp8mla_decode_ext(const void* q, const void* kv_cache, fp8mla_kv_dtype_t kv_dtype, int num_pages,
+                                  const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                                  const float* kv_scale, const float* kv_scale_rows, float softmax_scale, int causal,
+                                  const int32_t* tile_sched, const int32_t* num_splits, int num_units, void* workspace,
+                                  size_t workspace_bytes, void* out, float* lse, fp8mla_dot_mode_t dot_mode, int b,
+                                  int s_q, int h_q, fp8mla_stream_t stream) {
+  return mla_decode_call(q, kv_cache, kv_dtype, num_pages, block_table, max_pages, cache_seqlens, kv_scale,
+                         kv_scale_rows, softmax_scale, causal, tile_sched, num_splits, num_units, workspace,
+                         workspace_bytes, out, lse, dot_mode, b, s_q, h_q, stream);
 }
 
 fp8mla_status_t fp8mla_set_stage_timing(int enable) {

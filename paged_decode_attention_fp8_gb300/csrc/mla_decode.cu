@@ -658,6 +658,9 @@ struct Bars {
   uint64_t q_full, final_mma, xchg;
   uint32_t tmem_base, abort_flag, cvt_ok;
   float xsum[2][kRows];         // row-sum halves
+  // per-row scales (kv_rows): by stage, the page's 64 scales sigma as bulk-copied, then (written by
+  // the converter warps, one key each) sigma, log2 sigma and 1 / sigma
+  alignas(16) float scl[kStages][3][kPage];
 };
 
 constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
@@ -770,6 +773,8 @@ __device__ __forceinline__ void lane_group_transpose(uint4 (&pc)[N], int lane) {
 }
 }  // namespace f8
 
+// kRowScales: per-row KV scales (prm.kv_rows) instead of the per-tensor kv_scale.
+template <bool kRowScales>
 __global__ void __launch_bounds__(f8::kThreads, 1)
     mla_fp8_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                    const MlaParams prm) {
@@ -878,10 +883,13 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
             waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
             if (waited && fault != upg + 1) {
               uint8_t* sb = smem + st * kStageBytes;
-              mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
+              mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes + (kRowScales ? kPage * 4u : 0u));
 #pragma unroll
               for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kLatBox, &tm_lat, &bars->kv_full[st], q * 128, 0, phys);
               tma_load_3d(sb + kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
+              if constexpr (kRowScales)  // the page's 64 row scales (256 bytes)
+                bulk_load(&bars->scl[st][0][0], prm.kv_rows + static_cast<size_t>(phys) * kPage, kPage * 4u,
+                          &bars->kv_full[st]);
               issued |= 1u << st;
               par = (par & ~(1u << st)) | (static_cast<uint32_t>(use & 1) << st);
             }
@@ -1039,6 +1047,12 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         }
         uint8_t* sb = smem + st * kStageBytes;
         const bool dead = (pg == sg.n - 1) && (t >= sg.s_k - pg * kPage);  // slot past the sequence end
+        if constexpr (kRowScales) {  // key t's scale (1 past the end), its log2 and its inverse, for the softmax
+          const float sgm = dead ? 1.f : bars->scl[st][0][t];
+          bars->scl[st][0][t] = sgm;
+          bars->scl[st][1][t] = lg2_approx(sgm);
+          bars->scl[st][2][t] = 1.f / sgm;
+        }
         const uint4 z = make_uint4(0, 0, 0, 0);
         const int sw = t & 7;
         const uint4* src = reinterpret_cast<const uint4*>(sb + kOffRope8 + t * 64);
@@ -1078,7 +1092,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     const int hf = (warp - 4) / 4;         // which half of the row
     const int r = (warp % 4) * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-    const float kv_scale = *prm.kv_scale;
+    const float kv_scale = kRowScales ? 1.f : *prm.kv_scale;  // per-row scales enter through P and S
     const int R = prm.s_q * prm.h_q;
     constexpr int kOHalf = 128;  // O columns of this thread
     uint32_t xphase = 0;
@@ -1156,6 +1170,17 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         uint32_t s[32], so[32];
         tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * hf, s);
         tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * (1 - hf), so);
+        // per-row scales: the page's stage (its slot follows the segment's three Q slots); its
+        // conversion barrier covers the scale arrays, and its phase is this page's (the stage is
+        // refilled only after this page's P.V)
+        const int pslot = k + 3 + (pg - sg.lo);
+        const int pst = pslot % kStages;
+        if constexpr (kRowScales) {
+          if (!warp_spin(&bars->cvt_ready[pst], (pslot / kStages) & 1, abort_flag, __LINE__)) {
+            ok = false;
+            break;
+          }
+        }
         tmem_ld_wait();
 
         if (pg * kPage + kPage > min_visible) {
@@ -1164,6 +1189,18 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           for (int c = 0; c < 32; ++c) {
             if (base + c >= visible) s[c] = __float_as_uint(kNegInf);
             if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
+          }
+        }
+        if constexpr (kRowScales) {
+          // u_j = s_j c sigma_j + log2 sigma_j: the key's score with its K scale, plus its V scale's
+          // log, so that P' = 2^(u_j - m) carries sigma_j (masked keys stay -inf)
+          const float* sgv = bars->scl[pst][0];
+          const float* lgv = bars->scl[pst][1];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int kk = 32 * hf + c, ko = 32 * (1 - hf) + c;
+            s[c] = __float_as_uint(fmaf(__uint_as_float(s[c]), c_row * sgv[kk], lgv[kk]));
+            so[c] = __float_as_uint(fmaf(__uint_as_float(so[c]), c_row * sgv[ko], lgv[ko]));
           }
         }
         // row max of the 64 scores as a tree of three-way maxima
@@ -1181,7 +1218,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
         m8[7] = m22[21];
         const float m3a = fmax3(m8[0], m8[1], m8[2]), m3b = fmax3(m8[3], m8[4], m8[5]);
-        const float mx = fmax3(m3a, m3b, fmaxf(m8[6], m8[7])) * c_row;  // c_row > 0; both warps agree
+        const float mx = fmax3(m3a, m3b, fmaxf(m8[6], m8[7])) * (kRowScales ? 1.f : c_row);  // c_row > 0; both warps agree
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_run + kTau) {
@@ -1192,14 +1229,28 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         const float bias = (m_run == kNegInf) ? 0.f : (kPLog2 - m_run);
         float sum = 0.f;
         uint32_t pk[8];
+        if constexpr (kRowScales) {
+          // P' = 2^(u_j - m) (stored, times kPScale); the row sum takes P' / sigma_j = 2^(s_j c sigma_j - m)
+          const float* ivv = bars->scl[pst][2] + 32 * hf;
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c_row, bias));
-          const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
-          const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
-          sum += (p0 + p1) + (p2 + p3);
-          pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+          for (int c = 0; c < 32; c += 4) {
+            const float p0 = ex2_approx(__uint_as_float(s[c]) + bias);
+            const float p1 = ex2_approx(__uint_as_float(s[c + 1]) + bias);
+            const float p2 = ex2_approx(__uint_as_float(s[c + 2]) + bias);
+            const float p3 = ex2_approx(__uint_as_float(s[c + 3]) + bias);
+            sum += (p0 * ivv[c] + p1 * ivv[c + 1]) + (p2 * ivv[c + 2] + p3 * ivv[c + 3]);
+            pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c_row, bias));
+            const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
+            const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
+            sum += (p0 + p1) + (p2 + p3);
+            pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+          }
         }
         l_run = l_run * alpha + sum;
 
@@ -1303,11 +1354,14 @@ cudaError_t launch_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, co
                        cudaStream_t stream) {
   static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
   const cudaError_t e = configure_once(configured, [] {
-    return cudaFuncSetAttribute(mla_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e2 = cudaFuncSetAttribute(mla_fp8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(f8::smem_bytes()));
+    if (e2 != cudaSuccess) return e2;
+    return cudaFuncSetAttribute(mla_fp8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(f8::smem_bytes()));
   });
   if (e != cudaSuccess) return e;
-  return launch_dependent(mla_fp8_kernel, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream, tm_lat,
+  return launch_dependent(prm.kv_rows ? mla_fp8_kernel<true> : mla_fp8_kernel<false>, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream, tm_lat,
                           tm_rope, prm);
 }
 

@@ -13,6 +13,7 @@ struct MlaParams {
   const int32_t* block_table;  // [b, max_pages]
   const int32_t* seqlens;      // [b]
   const float* kv_scale;       // [1]
+  const float* kv_rows;        // per-row scales [num_pages, 64] or null (FP8 dots only)
   const int32_t* tile_sched;   // [num_units, 8]
   const int32_t* num_splits;   // [b + 1]
   uint16_t* ws_o;              // [slots, 128, 512] partial accumulators as bf16 (true units)

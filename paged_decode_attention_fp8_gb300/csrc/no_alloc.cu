@@ -86,11 +86,12 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
   const int units = b;
   if (launch_mla_metadata(cache_seqlens, b, units, 1, tile_sched, num_splits, s) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
-  MlaParams prm;
+  MlaParams prm{};
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_table = block_table;
   prm.seqlens = cache_seqlens;
   prm.kv_scale = kv_scale;
+  prm.kv_rows = nullptr;  // per-tensor scale only
   prm.tile_sched = tile_sched;
   prm.num_splits = num_splits;
   prm.ws_o = nullptr;

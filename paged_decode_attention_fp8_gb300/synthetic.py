@@ -90,8 +90,9 @@ def per_tensor_scale(values: np.ndarray) -> float:
     return float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
 
 
-def to_e4m3_bytes(x: np.ndarray, scale: float) -> np.ndarray:
-    """E4M3 bytes of x / scale (torch's float8_e4m3fn cast after clamping)."""
+def to_e4m3_bytes(x: np.ndarray, scale) -> np.ndarray:
+    """E4M3 bytes of x / scale (torch's float8_e4m3fn cast after clamping); scale is a float or an
+    array that broadcasts against x."""
     y = np.clip(np.asarray(x, dtype=np.float64) / scale, -E4M3_MAX, E4M3_MAX)
     t = torch.from_numpy(np.ascontiguousarray(y, dtype=np.float32)).to(torch.float8_e4m3fn)
     return t.view(torch.uint8).numpy().copy()
@@ -223,6 +224,41 @@ def mla_inputs(seed: int, b: int, s_q: int, h_q: int, seqlens, causal: bool = Tr
                      block_table=torch.from_numpy(block_table),
                      seqlens=torch.from_numpy(seqlens.astype(np.int32)),
                      kv_scale=scale, softmax_scale=softmax_scale, causal=causal)
+
+
+def mla_row_scaled_inputs(seed: int, b: int, s_q: int, h_q: int, seqlens, causal: bool = True,
+                          spare_pages: int = 0, value_pages: int | None = None, spread: float = 3.0):
+    """Dense MLA inputs with one scale per cached row: (inputs, scales float32 [num_pages, 1, 64]).
+
+    Row j holds N(0, 1) draws x_j stored as E4M3(x_j / sigma_j) with sigma_j = (amax_j / 448) 2^v_j,
+    v_j uniform in [0, spread]: the keys keep the statistics of ``mla_inputs`` while the scales span
+    a factor 2^spread and the codes use less of the E4M3 range as v_j grows.  ``inputs.kv_scale`` is
+    1.0 and unused.  With ``value_pages`` = n, n pages of draws and their row scales are made and each
+    used page copies one of them (codes and scales), as in ``mla_inputs``.  Spare pages and rows past
+    a sequence end hold 0x7F with scale 1."""
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    assert seqlens.shape == (b,)
+    num_pages, used, n_pages, block_table = _mla_layout(seed, seqlens, spare_pages)
+    n_pool = max(used, 1) if value_pages is None else value_pages
+    pool = normal(seed, 2, (n_pool, MLA_PAGE, MLA_D))
+    amax = np.abs(pool).max(axis=2)
+    v = uniform(seed, 5, n_pool * MLA_PAGE).reshape(n_pool, MLA_PAGE) * spread
+    sigma = (amax / E4M3_MAX * np.exp2(v)).astype(np.float32)
+    codes = to_e4m3_bytes(pool, sigma.astype(np.float64)[:, :, None])
+    pick = np.arange(used) if value_pages is None else randint(seed, 4, max(used, 1), 0, value_pages - 1)[:used]
+    valid = _mla_valid(seqlens, used, n_pages)
+    cache = _mla_place(codes[pick], valid, num_pages, used, n_pages, block_table)
+    rows = np.ones((num_pages, MLA_PAGE), dtype=np.float32)
+    k = 0
+    for i in range(b):
+        for p in range(int(n_pages[i])):
+            rows[block_table[i, p]] = sigma[pick[k + p]]
+        k += int(n_pages[i])
+    q = to_bf16(normal(seed, 3, (b, s_q, h_q, MLA_D)))
+    inp = MLAInputs(q=q, kv_cache=torch.from_numpy(cache), block_table=torch.from_numpy(block_table),
+                    seqlens=torch.from_numpy(seqlens.astype(np.int32)), kv_scale=1.0,
+                    softmax_scale=float(np.float32(1.0 / math.sqrt(MLA_D))), causal=causal)
+    return inp, torch.from_numpy(rows.reshape(num_pages, 1, MLA_PAGE))
 
 
 def mla_peaky_inputs(seed: int, b: int = 2, h_q: int = 64, s_k: int = 2048,

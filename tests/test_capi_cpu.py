@@ -85,6 +85,30 @@ def test_bad_arguments_refused(over):
     assert _decode(**over) == 1
 
 
+def _decode_ext(**over):
+    a = dict(q=1 << 20, kv=1 << 20, kv_dtype=fm.KV_E4M3, num_pages=16, bt=1 << 20, max_pages=8, sl=1 << 20,
+             scale=None, rows=1 << 20, softmax_scale=0.04, causal=1, ts=1 << 20, ns=1 << 20, units=76, ws=1 << 20,
+             ws_bytes=1 << 40, out=1 << 20, lse=1 << 20, dot=fm.DOT_FP8, b=2, s_q=2, h_q=64)
+    a.update(over)
+    return fm.lib().fp8mla_decode_ext(a["q"], a["kv"], a["kv_dtype"], a["num_pages"], a["bt"], a["max_pages"],
+                                      a["sl"], a["scale"], a["rows"], a["softmax_scale"], a["causal"], a["ts"],
+                                      a["ns"], a["units"], a["ws"], a["ws_bytes"], a["out"], a["lse"], a["dot"],
+                                      a["b"], a["s_q"], a["h_q"], None)
+
+
+@pytest.mark.parametrize("over", [dict(rows=None), dict(dot=fm.DOT_16BIT), dict(rows=(1 << 20) + 4),
+                                  dict(h_q=128), dict(q=None)])
+def test_decode_ext_refusals(over):
+    # neither scale given; per-row scales with 16-bit dots; rows not 16-byte aligned; bad shapes
+    assert _decode_ext(**over) == 1
+
+
+def test_decode_ext_foreign_encoding_workspace_and_empty_batch():
+    assert _decode_ext(kv_dtype=fm.KV_E5M2) == 2
+    assert _decode_ext(ws_bytes=1024) == 3
+    assert _decode_ext(b=0, q=None, out=None, lse=None) == 0
+
+
 def test_small_workspace_refused():
     assert _decode(ws_bytes=1024) == 3
 
