@@ -118,6 +118,9 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
   int32_t* iscratch = ustart + 2 * (U + 1);                            // [kMetaThreads + 1]
   if (blockIdx.x != 0) return;
   griddep_launch_dependents();  // the decode kernel's prologue may overlap this one
+  // Launched as a programmatic dependent of whatever the caller enqueued
+  // before (which may have written seqlens): wait for it before reading.
+  griddep_wait();
   const int tid = threadIdx.x, nt = blockDim.x;
   for (int i = tid; i < B; i += nt) {
     n[i] = pages_of(seqlens[i]);
@@ -368,9 +371,9 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
                                 static_cast<int>(kMetadataMaxSmem));
   });
   if (e != cudaSuccess) return e;
-  mla_metadata_kernel<<<1, kMetaThreads, smem, stream>>>(seqlens, b, num_units, force_splits, tile_sched,
-                                                         num_splits);
-  return cudaGetLastError();
+  // a programmatic dependent: its launch overlaps the tail of the previous kernel
+  return launch_dependent(mla_metadata_kernel, dim3(1), dim3(kMetaThreads), smem, stream, seqlens, b, num_units,
+                          force_splits, tile_sched, num_splits);
 }
 
 cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,

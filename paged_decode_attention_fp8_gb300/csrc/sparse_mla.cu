@@ -7,14 +7,21 @@
 // with V = K (the same 512 cached values) and index -1 meaning "no key".
 //
 // GB300 design (swap-AB, one CTA per (token, split of the key list)):
-//   * 128 keys per step.  The rows are gathered by TMA tile::gather4 (four
-//     rows of one 128-byte column box per instruction, 128 instructions per
-//     step issued by the 32 lanes of the producer warp) into four
-//     128-byte-swizzled atoms; index -1 and out-of-range rows land as zeros
-//     (the copy's out-of-bounds fill) and are masked by select.
+//   * 128 keys per step, gathered into four 128-byte-swizzled atoms (one per
+//     128-byte column box) by two engines at once: the first 32 rows by TMA
+//     tile::gather4 (four rows of one column box per instruction, 32
+//     instructions from 8 lanes), the other 96 by 16-byte cp.async from three
+//     warps, one warp instruction per row.  The TMA unit takes ~29 ns per
+//     gather4 request (~17.6 GB/s per SM), so gathering all 128 rows through
+//     it took 3.7 us per step; the load/store path moves a row per warp
+//     instruction.  Index -1 and out-of-range rows land as zeros (the TMA
+//     copy's out-of-bounds fill; cp.async with no source bytes) and are
+//     masked by select.
 //   * S^T = K Q^T on tcgen05 kind::f8f6f4: M = 128 keys, N = 16 heads,
 //     K = 512 (16 MMAs); Q is quantised in-kernel per head with a power-of-
-//     two scale (aiter page, Technical details: in-kernel Q quantisation).
+//     two scale (aiter page, Technical details: in-kernel Q quantisation),
+//     and its rounding error q_hat - q (exact in bf16) is kept in shared
+//     memory for the epilogue's LSE correction.
 //     S^T lives in TMEM: thread j of the softmax warpgroup owns key j.
 //   * Softmax across TMEM lanes: per-head max by warp shuffles + a 4-warp
 //     exchange, lazily raised (threshold 1 in log2 units so 128 p <= 256);
@@ -53,6 +60,9 @@ constexpr int kAtom = kKeys * 128;  // one 128-byte column slice of a step (16 K
 constexpr int kStageBytes = 4 * kAtom;
 constexpr int kQBytes = 4 * kN * 128;   // Q tile: 4 atoms x [16 rows x 128 B]
 constexpr int kPBytes = kN * 128;       // P^T tile: [16 rows x 128 keys]
+constexpr int kEBytes = kN * kD * 2;    // Q's rounding error q_hat - q, bf16 [16 heads][512]
+constexpr int kTmaKeys = 32;            // rows of a step gathered by TMA; the rest by cp.async
+constexpr int kCopyWarps = 3;           // warps 0, 2 and 3 issue the cp.async rows
 constexpr float kPScale = 128.0f;
 constexpr float kTau = 1.0f;
 constexpr uint32_t kTmemCols = 128;     // S^T 16 + O^T 64
@@ -60,6 +70,7 @@ constexpr uint32_t kTS = 0, kTO = 16;
 
 struct Params {
   const uint16_t* q;       // bf16 [s_q, h_q, 512]
+  const uint8_t* kv;       // E4M3 [num_tokens, 512]
   const int32_t* idx;      // [s_q, topk]
   const float* kv_scale;
   uint16_t* out;           // bf16 [s_q, h_q, 512]
@@ -75,13 +86,14 @@ struct Params {
 struct Smem {
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma, xchg;
-  uint32_t tmem_base, abort_flag, prod_ok;
+  uint32_t tmem_base, abort_flag;
   float qs[kN];
   float red[2][4][kN];   // per-warp partial maxima, double-buffered by step parity
   float red2[4][kN];
 };
 
-constexpr size_t kSmemBytes = kStages * kStageBytes + kQBytes + kPBytes + sizeof(Smem) + 1024;
+constexpr size_t kSmemBytes = kStages * kStageBytes + kQBytes + kPBytes + kEBytes + sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
   const bool ok = wait_bounded(bar, parity, abort_flag, &g_status_sparse);
@@ -116,7 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* q_tile = smem + kStages * kStageBytes;
   uint8_t* p_tile = q_tile + kQBytes;
-  Smem* sm = reinterpret_cast<Smem*>(p_tile + kPBytes);
+  uint8_t* e_tile = p_tile + kPBytes;
+  Smem* sm = reinterpret_cast<Smem*>(e_tile + kEBytes);
   volatile uint32_t* abort_flag = &sm->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -129,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm->kv_full[s], 1);
+      mbar_init(&sm->kv_full[s], 1 + 32 * kCopyWarps);  // the TMA part's arrival + one per copying lane
       mbar_init(&sm->kv_empty[s], 1);
     }
     mbar_init(&sm->s_full, 1);
@@ -153,27 +166,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
   const uint32_t tmem = sm->tmem_base;
 
-  if (warp == 0) {
-    // ---------------------------------------- gather producer (warp) ----
-    if (lane == 0) tma_prefetch_desc(&tm_rows);
+  if (warp == 0 || warp == 2 || warp == 3) {
+    // ------------------------------- gather producers (warps 0, 2, 3) ----
+    // Key k of a step (k = 4 j + q) comes from lane j's q-th index.  Rows
+    // 0..31 (index lanes 0..7): TMA gather4 from warp 0.  Rows 32..127: index
+    // lanes 8..31 in turn to the three warps; a row is one warp instruction,
+    // lane l copying its bytes [16 l, 16 l + 16) into column box l / 8 as
+    // 16-byte chunk l % 8, XOR-swizzled by the row (128-byte swizzle).  Each
+    // copying lane arrives on the stage's full barrier once its copies land.
+    const int pw = warp == 0 ? 0 : warp - 1;
+    const int cb = lane / 8, cc = lane % 8;
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_rows);
     int i = 0;
     for (; i < nchunks; ++i) {
       const int st = i % kStages, use = i / kStages;
-      if (lane == 0) {
-        bool ok = use == 0 || wait_bounded(&sm->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_sparse);
-        if (ok) mbar_arrive_expect_tx(&sm->kv_full[st], kStageBytes);
-        sm->prod_ok = ok ? 1u : 0u;
-      }
-      __syncwarp();
-      if (!sm->prod_ok) break;
+      bool ok = true;
+      if (lane == 0) ok = use == 0 || wait_bounded(&sm->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_sparse);
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
       const int kbase = (c0 + i) * kKeys + 4 * lane;
       const int r0 = key_row(prm, t, kbase), r1 = key_row(prm, t, kbase + 1);
       const int r2 = key_row(prm, t, kbase + 2), r3 = key_row(prm, t, kbase + 3);
-      uint8_t* sb = smem + st * kStageBytes + (4 * lane) * 128;
+      uint8_t* sb = smem + st * kStageBytes;
+      if (warp == 0) {
+        if (lane == 0) mbar_arrive_expect_tx(&sm->kv_full[st], kTmaKeys * kD);
+        __syncwarp();
+        if (lane < kTmaKeys / 4) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tma_gather4(sb + j * kAtom, &tm_rows, &sm->kv_full[st], j * 128, r0, r1, r2, r3);
+          for (int j = 0; j < 4; ++j)
+            tma_gather4(sb + j * kAtom + (4 * lane) * 128, &tm_rows, &sm->kv_full[st], j * 128, r0, r1, r2, r3);
+        }
+      }
+#pragma unroll 1
+      for (int src = kTmaKeys / 4 + pw; src < 32; src += kCopyWarps) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int kk = 4 * src + q;
+          const int row = __shfl_sync(0xffffffffu, q == 0 ? r0 : (q == 1 ? r1 : (q == 2 ? r2 : r3)), src);
+          cp_async16(smem_u32(sb + cb * kAtom + kk * 128 + ((cc ^ (kk & 7)) << 4)),
+                     prm.kv + static_cast<size_t>(row >= 0 ? row : 0) * kD + 16 * lane, row >= 0 ? 16u : 0u);
+        }
+      }
+      cp_async_mbar_arrive(&sm->kv_full[st]);
     }
-    if (lane == 0)
+    cp_async_wait_all();  // this lane's copies have landed before the CTA can exit
+    if (warp == 0 && lane == 0)
       for (int j = max(0, i - kStages); j < i; ++j)
         wait_bounded(&sm->kv_full[j % kStages], (j / kStages) & 1, nullptr, &g_status_sparse);
     __syncwarp();
@@ -211,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        fence_proxy_async_smem();  // the cp.async rows were written through the generic proxy
         tc_fence_after();
         const uint32_t sb = smem_u32(smem + st * kStageBytes);
 #pragma unroll
@@ -261,9 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
       const int e = pow2_exp_448(amax);
-      const float inv = exp2i(-e);
-      if (qj == 0) sm->qs[qh] = exp2i(e);
+      const float inv = exp2i(-e), qsv = exp2i(e);
+      if (qj == 0) sm->qs[qh] = qsv;
       uint8_t* row = q_tile + (qj / 2) * (kN * 128) + (qh / 8) * 1024 + (qh % 8) * 128;
+      uint4* erow = reinterpret_cast<uint4*>(e_tile + qh * (kD * 2) + qj * 128);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {  // 16 values -> one 16-byte chunk
         const uint4 a = v[2 * c], b = v[2 * c + 1];
@@ -274,6 +312,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         o.w = pack_e4m3x4(bf16_lo(b.z) * inv, bf16_hi(b.z) * inv, bf16_lo(b.w) * inv, bf16_hi(b.w) * inv);
         const int chunk = 4 * (qj % 2) + c;
         *reinterpret_cast<uint4*>(row + ((chunk ^ (qh % 8)) << 4)) = o;
+        // q_hat - q of these 16 values: both have few significant bits at the
+        // same scale, so the difference is exact in fp32 and in bf16
+        const uint32_t code[4] = {o.x, o.y, o.z, o.w};
+        const uint32_t src[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t ew[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t lo = e4m3x2_to_f16x2(code[k] & 0xFFFFu), hi = e4m3x2_to_f16x2(code[k] >> 16);
+          ew[2 * k] = pack_bf16x2(f16_lo(lo) * qsv - bf16_lo(src[2 * k]), f16_hi(lo) * qsv - bf16_hi(src[2 * k]));
+          ew[2 * k + 1] =
+              pack_bf16x2(f16_lo(hi) * qsv - bf16_lo(src[2 * k + 1]), f16_hi(hi) * qsv - bf16_hi(src[2 * k + 1]));
+        }
+        erow[2 * c] = make_uint4(ew[0], ew[1], ew[2], ew[3]);
+        erow[2 * c + 1] = make_uint4(ew[4], ew[5], ew[6], ew[7]);
       }
       fence_proxy_async_smem();
       warp_arrive(&sm->q_full);
@@ -381,6 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool whole = prm.splits == 1;
       const size_t slot = static_cast<size_t>(t) * prm.splits + split;
       const float o_scale = kv_scale / kPScale;
+      float f_h[kN];
+#pragma unroll
+      for (int h = 0; h < kN; ++h) f_h[h] = whole ? (lsum[h] > 0.f ? o_scale / lsum[h] : 0.f) : o_scale;
+      const uint16_t* e16 = reinterpret_cast<const uint16_t*>(e_tile);
+      // thread r writes dim mt * 128 + r of every head (consecutive threads, consecutive dims);
+      // no branch on h_q inside the loop, so its loads and stores issue back to back
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
         uint32_t o[kN];
@@ -389,18 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int d = mt * 128 + r;
 #pragma unroll
         for (int h = 0; h < kN; ++h) {
-          if (h >= prm.h_q) break;
-          const float f = whole ? (lsum[h] > 0.f ? o_scale / lsum[h] : 0.f) : o_scale;
-          const float val = __uint_as_float(o[h]) * f;
+          const float val = __uint_as_float(o[h]) * f_h[h];
           // first-order LSE correction term: (q_hat - q) * value along this dim
-          const float x = bf16_lo(static_cast<uint32_t>(qtok[h * kD + d]));
-          const float qs = sm->qs[h];
-          const uint32_t hq = e4m3x2_to_f16x2(pack_e4m3x2(x / qs, 0.f));
-          dq[h] += (f16_lo(hq) * qs - x) * val;
-          if (whole)
-            prm.out[(static_cast<size_t>(t) * prm.h_q + h) * kD + d] = static_cast<uint16_t>(pack_bf16x2(val, 0.f));
-          else
-            prm.ws_o[(slot * kN + h) * kD + d] = val;
+          dq[h] += bf16_lo(static_cast<uint32_t>(e16[h * kD + d])) * val;
+          if (h < prm.h_q) {
+            if (whole)
+              prm.out[(static_cast<size_t>(t) * prm.h_q + h) * kD + d] = static_cast<uint16_t>(pack_bf16x2(val, 0.f));
+            else
+              prm.ws_o[(slot * kN + h) * kD + d] = val;
+          }
         }
       }
 #pragma unroll
@@ -608,6 +663,7 @@ fp8mla_status_t sparse_decode_entry(const void* q, const void* kv_cache, int64_t
   sparse::Params prm;
   char* ws = static_cast<char*>(workspace);
   prm.q = static_cast<const uint16_t*>(q);
+  prm.kv = static_cast<const uint8_t*>(kv_cache);
   prm.idx = topk_idx;
   prm.kv_scale = kv_scale;
   prm.out = static_cast<uint16_t*>(out);
