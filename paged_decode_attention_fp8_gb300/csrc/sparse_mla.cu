@@ -8,15 +8,17 @@
 //
 // GB300 design (swap-AB, one CTA per (token, split of the key list)):
 //   * 128 keys per step, gathered into four 128-byte-swizzled atoms (one per
-//     128-byte column box) by two engines at once: the first 32 rows by TMA
-//     tile::gather4 (four rows of one column box per instruction, 32
-//     instructions from 8 lanes), the other 96 by 16-byte cp.async from three
-//     warps, one warp instruction per row.  The TMA unit takes ~29 ns per
-//     gather4 request (~17.6 GB/s per SM), so gathering all 128 rows through
-//     it took 3.7 us per step; the load/store path moves a row per warp
-//     instruction.  Index -1 and out-of-range rows land as zeros (the TMA
-//     copy's out-of-bounds fill; cp.async with no source bytes) and are
-//     masked by select.
+//     128-byte column box) by two engines at once: 32 rows by TMA
+//     tile::gather4 from warp 0 (four rows of one column box per
+//     instruction), 96 by 16-byte cp.async from warps 2 and 3 (one warp
+//     instruction per row); the next step's indices load while a step
+//     issues.  The TMA unit takes ~29 ns per gather4 request (all 128 rows
+//     through it: 3.7 us per step), and the cp.async rows are limited by the
+//     misses an SM keeps in flight; at s_q = 16384 a 32-row TMA share ran
+//     3.56 ms per call against 4.07 ms with no TMA rows and 5.43 ms with 64.
+//     Index -1 and out-of-range rows land as zeros (the TMA copy's
+//     out-of-bounds fill; cp.async with no source bytes) and are masked by
+//     select.
 //   * S^T = K Q^T on tcgen05 kind::f8f6f4: M = 128 keys, N = 16 heads,
 //     K = 512 (16 MMAs); Q is quantised in-kernel per head with a power-of-
 //     two scale (aiter page, Technical details: in-kernel Q quantisation),
@@ -62,7 +64,7 @@ constexpr int kQBytes = 4 * kN * 128;   // Q tile: 4 atoms x [16 rows x 128 B]
 constexpr int kPBytes = kN * 128;       // P^T tile: [16 rows x 128 keys]
 constexpr int kEBytes = kN * kD * 2;    // Q's rounding error q_hat - q, bf16 [16 heads][512]
 constexpr int kTmaKeys = 32;            // rows of a step gathered by TMA; the rest by cp.async
-constexpr int kCopyWarps = 3;           // warps 0, 2 and 3 issue the cp.async rows
+constexpr int kCopyWarps = 2;           // warps 2 and 3 issue the cp.async rows
 constexpr float kPScale = 128.0f;
 constexpr float kTau = 1.0f;
 constexpr uint32_t kTmemCols = 128;     // S^T 16 + O^T 64
@@ -121,6 +123,15 @@ __device__ __forceinline__ int key_row(const Params& p, int t, int k) {
   return v;
 }
 
+// A loaded index as a cache row: -1 (no key) stays -1; out of range is flagged and skipped.
+__device__ __forceinline__ int checked_row(const Params& p, int v) {
+  if (v < -1 || v >= p.num_tokens) {
+    atomicOr(&g_status_sparse, FP8MLA_DEV_BAD_INDEX);
+    return -1;
+  }
+  return v;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_rows, const Params prm) {
   extern __shared__ uint8_t smem_raw[];
@@ -142,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm->kv_full[s], 1 + 32 * kCopyWarps);  // the TMA part's arrival + one per copying lane
+      mbar_init(&sm->kv_full[s], 1 + 32 * kCopyWarps);  // the TMA warp's arrival + one per copying lane
       mbar_init(&sm->kv_empty[s], 1);
     }
     mbar_init(&sm->s_full, 1);
@@ -169,23 +180,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 || warp == 2 || warp == 3) {
     // ------------------------------- gather producers (warps 0, 2, 3) ----
     // Key k of a step (k = 4 j + q) comes from lane j's q-th index.  Rows
-    // 0..31 (index lanes 0..7): TMA gather4 from warp 0.  Rows 32..127: index
-    // lanes 8..31 in turn to the three warps; a row is one warp instruction,
-    // lane l copying its bytes [16 l, 16 l + 16) into column box l / 8 as
-    // 16-byte chunk l % 8, XOR-swizzled by the row (128-byte swizzle).  Each
-    // copying lane arrives on the stage's full barrier once its copies land.
-    const int pw = warp == 0 ? 0 : warp - 1;
+    // [0, kTmaKeys): TMA gather4 from warp 0 (four rows of one column box per
+    // instruction).  The other rows: cp.async from warps 2 and 3, index lanes
+    // in turn; a row is one warp instruction, lane l copying its bytes
+    // [16 l, 16 l + 16) into column box l / 8 as 16-byte chunk l % 8,
+    // XOR-swizzled by the row (128-byte swizzle).  Each copying lane arrives on
+    // the stage's full barrier once its copies land.  The next step's indices
+    // are loaded while this step's copies issue.
+    const int cw = warp - 2;  // copy warp 0 or 1 (warp 0: the TMA warp)
     const int cb = lane / 8, cc = lane % 8;
     if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_rows);
+    const int32_t* idx_t = prm.idx + static_cast<size_t>(t) * prm.topk;
+    auto load_idx = [&](int ch, int (&v)[4]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int k = (c0 + ch) * kKeys + 4 * lane + q;
+        v[q] = k < prm.topk ? __ldg(idx_t + k) : -1;
+      }
+    };
+    int raw[4] = {-1, -1, -1, -1};
+    if (nchunks > 0) load_idx(0, raw);
     int i = 0;
     for (; i < nchunks; ++i) {
       const int st = i % kStages, use = i / kStages;
+      int nxt[4] = {-1, -1, -1, -1};
+      if (i + 1 < nchunks) load_idx(i + 1, nxt);
       bool ok = true;
       if (lane == 0) ok = use == 0 || wait_bounded(&sm->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_sparse);
       if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
-      const int kbase = (c0 + i) * kKeys + 4 * lane;
-      const int r0 = key_row(prm, t, kbase), r1 = key_row(prm, t, kbase + 1);
-      const int r2 = key_row(prm, t, kbase + 2), r3 = key_row(prm, t, kbase + 3);
+      const int r0 = checked_row(prm, raw[0]), r1 = checked_row(prm, raw[1]);
+      const int r2 = checked_row(prm, raw[2]), r3 = checked_row(prm, raw[3]);
       uint8_t* sb = smem + st * kStageBytes;
       if (warp == 0) {
         if (lane == 0) mbar_arrive_expect_tx(&sm->kv_full[st], kTmaKeys * kD);
@@ -195,18 +219,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j)
             tma_gather4(sb + j * kAtom + (4 * lane) * 128, &tm_rows, &sm->kv_full[st], j * 128, r0, r1, r2, r3);
         }
-      }
+      } else {
 #pragma unroll 1
-      for (int src = kTmaKeys / 4 + pw; src < 32; src += kCopyWarps) {
+        for (int src = kTmaKeys / 4 + cw; src < 32; src += kCopyWarps) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int kk = 4 * src + q;
-          const int row = __shfl_sync(0xffffffffu, q == 0 ? r0 : (q == 1 ? r1 : (q == 2 ? r2 : r3)), src);
-          cp_async16(smem_u32(sb + cb * kAtom + kk * 128 + ((cc ^ (kk & 7)) << 4)),
-                     prm.kv + static_cast<size_t>(row >= 0 ? row : 0) * kD + 16 * lane, row >= 0 ? 16u : 0u);
+          for (int q = 0; q < 4; ++q) {
+            const int kk = 4 * src + q;
+            const int row = __shfl_sync(0xffffffffu, q == 0 ? r0 : (q == 1 ? r1 : (q == 2 ? r2 : r3)), src);
+            cp_async16(smem_u32(sb + cb * kAtom + kk * 128 + ((cc ^ (kk & 7)) << 4)),
+                       prm.kv + static_cast<size_t>(row >= 0 ? row : 0) * kD + 16 * lane, row >= 0 ? 16u : 0u);
+          }
         }
+        cp_async_mbar_arrive(&sm->kv_full[st]);
       }
-      cp_async_mbar_arrive(&sm->kv_full[st]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) raw[q] = nxt[q];
     }
     cp_async_wait_all();  // this lane's copies have landed before the CTA can exit
     if (warp == 0 && lane == 0)
