@@ -33,10 +33,15 @@
 //     and written to shared memory as the K-major B operand.
 //   * O^T = V^T P^T in four M = 128 tiles (dv = 512), A = the same gathered
 //     atoms read MN-major (no transpose), B = P^T.  O^T sits in TMEM.
-//   * Split-KV: shards publish (m, l, acc, (q_hat - q) . acc) and the shared
-//     combine kernel merges them (InfiniCore split-kv commit).  Because V = K,
-//     the first-order LSE error of Q's quantisation is scale * (q_hat - q) .
-//     out, which the epilogue (or the combine) subtracts.
+//   * Split-KV: shards publish (m, l, acc, (q_hat - q) . acc) and the
+//     combine kernel merges them (InfiniCore split-kv commit); with up to 16
+//     splits each of its threads loads every split's (m, l, d) with its own
+//     partial columns, so the merge is one round trip and has no barrier.
+//     (Merging inside a cooperatively launched decode grid was tried: the
+//     cooperative launch alone cost ~4.6 us per call at s_q = 2, more than
+//     the combine kernel.)  Because V = K, the first-order LSE error of Q's
+//     quantisation is scale * (q_hat - q) . out, which the epilogue (or the
+//     combine) subtracts.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -508,17 +513,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           prm.ws_d[(slot * kN + h) * 2 + 1] = 0.f;
         }
       }
-    } else if (nchunks == 0 && r < prm.h_q) {
-      // no key at all in this shard
-      const size_t slot = static_cast<size_t>(t) * prm.splits + split;
-      if (prm.splits == 1) {
-        for (int d = 0; d < kD; ++d) prm.out[(static_cast<size_t>(t) * prm.h_q + r) * kD + d] = 0;
-        prm.lse[static_cast<size_t>(t) * prm.h_q + r] = kNegInf;
-      } else {
-        prm.ws_ml[slot * kN + r] = make_float2(kNegInf, 0.f);
-        prm.ws_d[(slot * kN + r) * 2] = 0.f;
-        prm.ws_d[(slot * kN + r) * 2 + 1] = 0.f;
-        for (int d = 0; d < kD; ++d) prm.ws_o[(slot * kN + r) * kD + d] = 0.f;
+    } else if (nchunks == 0) {
+      if (r < prm.h_q) {  // no key at all in this shard
+        const size_t slot = static_cast<size_t>(t) * prm.splits + split;
+        if (prm.splits == 1) {
+          for (int d = 0; d < kD; ++d) prm.out[(static_cast<size_t>(t) * prm.h_q + r) * kD + d] = 0;
+          prm.lse[static_cast<size_t>(t) * prm.h_q + r] = kNegInf;
+        } else {
+          prm.ws_ml[slot * kN + r] = make_float2(kNegInf, 0.f);
+          prm.ws_d[(slot * kN + r) * 2] = 0.f;
+          prm.ws_d[(slot * kN + r) * 2 + 1] = 0.f;
+          for (int d = 0; d < kD; ++d) prm.ws_o[(slot * kN + r) * kD + d] = 0.f;
+        }
       }
     }
   }
@@ -575,13 +581,18 @@ Layout layout(int s_q, int splits) {
 }
 
 // Merge of the splits of one (token, head) row: grid (s_q, h_q), 128 threads,
-// thread t owns output columns 4t .. 4t + 3.  Split j of token bi holds the
+// thread t owning output columns 4t .. 4t + 3.  Split j of token bi holds the
 // row's fp32 partial O (true units, unnormalised) and (m, l) with m in log2
 // units, plus the two LSE-correction shares d_j; the result is
 // out = sum_j w_j O_j / L and lse = ln2 (M + log2 L) - scale sum_j w_j d_j / L,
-// w_j = 2^(m_j - M), M = max_j m_j, L = sum_j w_j l_j.  Every thread recomputes
-// the weights it needs from (m, l) (a broadcast read), and issues the partial
-// loads of 16 splits before using any of them.
+// w_j = 2^(m_j - M), M = max_j m_j, L = sum_j w_j l_j, every sum in split
+// order.  Up to kFewSplits splits: every thread loads every split's (m, l, d)
+// (broadcast reads) together with its own partial columns and computes M, L
+// and the correction itself -- one round trip, no barrier.  More splits: the
+// maximum is reduced across the CTA first, then 16 splits' loads are issued
+// at a time.
+constexpr int kFewSplits = 16;
+
 __global__ void __launch_bounds__(128) combine_kernel(int splits, const float* __restrict__ ws_o,
                                                       const float2* __restrict__ ws_ml,
                                                       const float* __restrict__ ws_d, float softmax_scale,
@@ -589,69 +600,104 @@ __global__ void __launch_bounds__(128) combine_kernel(int splits, const float* _
   griddep_wait();  // launched as a dependent of the decode kernel
   const int bi = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
   const size_t slot0 = static_cast<size_t>(bi) * splits;
-  __shared__ float red[4], l_sh;
-  float mx = kNegInf;
-  for (int j = t; j < splits; j += 128) mx = fmaxf(mx, __ldg(ws_ml + (slot0 + j) * kN + h).x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((t & 31) == 0) red[t >> 5] = mx;
-  __syncthreads();
-  const float big_m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   uint16_t* orow = out + (static_cast<size_t>(bi) * h_q + h) * kMlaDV + 4 * t;
-  if (big_m == kNegInf) {  // every split of the row is empty
-    *reinterpret_cast<uint2*>(orow) = make_uint2(0, 0);
-    if (t == 0) lse[static_cast<size_t>(bi) * h_q + h] = kNegInf;
-    return;
-  }
+  float* lrow = lse + static_cast<size_t>(bi) * h_q + h;
+  const float2* ws_d2 = reinterpret_cast<const float2*>(ws_d);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float big_l = 0.f, dq = 0.f;
-  for (int j0 = 0; j0 < splits; j0 += 16) {
-    float4 v[16];
-    float2 ml[16];
+  float big_m = kNegInf, big_l = 0.f, dq = 0.f;
+  auto add = [&](float w, const float4& v) {
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  };
+  if (splits <= kFewSplits) {
+    float4 v[kFewSplits];
+    float2 ml[kFewSplits], dd[kFewSplits];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      if (j0 + q < splits) {
-        const size_t slot = (slot0 + j0 + q) * kN + h;
+    for (int q = 0; q < kFewSplits; ++q) {
+      if (q < splits) {
+        const size_t slot = (slot0 + q) * kN + h;
         v[q] = __ldg(reinterpret_cast<const float4*>(ws_o + slot * kMlaDV) + t);
         ml[q] = __ldg(ws_ml + slot);
+        dd[q] = __ldg(ws_d2 + slot);
       }
     }
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      if (j0 + q < splits) {
-        const float w = (ml[q].x == kNegInf) ? 0.f : ex2_approx(ml[q].x - big_m);  // an empty split adds nothing
-        acc.x += w * v[q].x;
-        acc.y += w * v[q].y;
-        acc.z += w * v[q].z;
-        acc.w += w * v[q].w;
-        if (t == 0) {
-          const size_t slot = (slot0 + j0 + q) * kN + h;
+    for (int q = 0; q < kFewSplits; ++q)
+      if (q < splits) big_m = fmaxf(big_m, ml[q].x);
+    if (big_m != kNegInf) {
+#pragma unroll
+      for (int q = 0; q < kFewSplits; ++q) {
+        if (q < splits) {
+          const float w = (ml[q].x == kNegInf) ? 0.f : ex2_approx(ml[q].x - big_m);  // an empty split adds nothing
+          add(w, v[q]);
           big_l += w * ml[q].y;
-          dq += w * (__ldg(ws_d + 2 * slot) + __ldg(ws_d + 2 * slot + 1));
+          dq += w * (dd[q].x + dd[q].y);
+        }
+      }
+    }
+  } else {
+    __shared__ float red[4];
+    for (int j = t; j < splits; j += 128) big_m = fmaxf(big_m, __ldg(ws_ml + (slot0 + j) * kN + h).x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, o));
+    if ((t & 31) == 0) red[t >> 5] = big_m;
+    __syncthreads();
+    big_m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    if (big_m != kNegInf) {
+      for (int j0 = 0; j0 < splits; j0 += 16) {
+        float4 v[16];
+        float2 ml[16], dd[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          if (j0 + q < splits) {
+            const size_t slot = (slot0 + j0 + q) * kN + h;
+            v[q] = __ldg(reinterpret_cast<const float4*>(ws_o + slot * kMlaDV) + t);
+            ml[q] = __ldg(ws_ml + slot);
+            dd[q] = __ldg(ws_d2 + slot);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          if (j0 + q < splits) {
+            const float w = (ml[q].x == kNegInf) ? 0.f : ex2_approx(ml[q].x - big_m);
+            add(w, v[q]);
+            big_l += w * ml[q].y;
+            dq += w * (dd[q].x + dd[q].y);
+          }
         }
       }
     }
   }
-  if (t == 0) l_sh = big_l;
-  __syncthreads();
-  big_l = l_sh;
+  if (big_m == kNegInf) {  // every split of the row is empty
+    *reinterpret_cast<uint2*>(orow) = make_uint2(0, 0);
+    if (t == 0) *lrow = kNegInf;
+    return;
+  }
   const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
   *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  if (t == 0)
-    lse[static_cast<size_t>(bi) * h_q + h] =
-        big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 - softmax_scale * dq * inv : kNegInf;
+  if (t == 0) *lrow = big_l > 0.f ? (big_m + lg2_approx(big_l)) * kLn2 - softmax_scale * dq * inv : kNegInf;
 }
 
 }  // namespace sparse
 
-int sparse_choose_splits(int s_q, int topk, int num_splits) {
-  const int chunks = (topk + sparse::kKeys - 1) / sparse::kKeys;
-  if (num_splits > 0) return std::min(num_splits, std::max(chunks, 1));
+namespace {
+// SMs of the current device (148 if it cannot be read).
+int current_sms() {
   int sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                 cudaSuccess)
     sms = 148;
-  const int want = std::max(1, sms / std::max(s_q, 1));
+  return sms;
+}
+
+}  // namespace
+
+int sparse_choose_splits(int s_q, int topk, int num_splits) {
+  const int chunks = (topk + sparse::kKeys - 1) / sparse::kKeys;
+  if (num_splits > 0) return std::min(num_splits, std::max(chunks, 1));
+  const int want = std::max(1, current_sms() / std::max(s_q, 1));
   return std::max(1, std::min(want, chunks));
 }
 

@@ -72,6 +72,17 @@ def test_skipped_and_ragged_indices():
     assert fm.last_device_error() == 0
 
 
+@pytest.mark.parametrize("s_q,splits", [(38, 4), (48, 4), (3, 24)])
+def test_split_merge_more_tokens_and_many_splits(s_q, splits):
+    # more CTAs than SMs (48 x 4), and more than 16 splits per token (the
+    # combine kernel's general path: a CTA-wide maximum, then 16 splits at a time)
+    inp = syn.sparse_inputs(13, s_q, num_tokens=8192, topk=3072)
+    out, lse = run(inp, num_splits=splits)
+    ro, rl = ref(inp)
+    assert_close(compare(out, lse, ro, rl, "fp8"), "fp8")
+    assert fm.last_device_error() == 0
+
+
 def test_fewer_heads():
     inp = syn.sparse_inputs(10, 2, h_q=5, num_tokens=4096, topk=512)
     out, lse = run(inp)
