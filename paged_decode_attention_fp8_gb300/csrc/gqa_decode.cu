@@ -238,23 +238,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer ----
-    // lanes 0..7 fetch the step's block-table entries at once; lane 0 issues the loads
+    // lanes 0..7 fetch a step's block-table entries at once, one step ahead
+    // (the load is in flight while the previous step's loads issue); lane 0
+    // issues the loads
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
+    const int32_t* bt_row = prm.block_table + static_cast<size_t>(b) * prm.max_blocks;
+    auto fetch = [&](int step) {
+      const int p0 = (st0 + step) * kPagesPerStep;
+      return (step < nsteps && lane < min(kPagesPerStep, n_pages - p0)) ? __ldg(bt_row + p0 + lane) : 0;
+    };
+    int next = fetch(0);
     int i = 0;
     for (; i < nsteps; ++i) {
       const int st = i % kRawStages, use = i / kRawStages;
       const int p0 = (st0 + i) * kPagesPerStep;
       const int np = min(kPagesPerStep, n_pages - p0);
-      int mine = 0;
-      if (lane < np) {
-        mine = __ldg(prm.block_table + static_cast<size_t>(b) * prm.max_blocks + p0 + lane);
-        if (mine < 0 || mine >= prm.num_blocks) {
-          atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_PAGE);
-          mine = 0;
-        }
+      int mine = next;
+      next = fetch(i + 1);
+      if (lane < np && (mine < 0 || mine >= prm.num_blocks)) {
+        atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_PAGE);
+        mine = 0;
       }
       int rows[kPagesPerStep];
 #pragma unroll
