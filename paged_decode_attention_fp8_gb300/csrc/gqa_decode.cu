@@ -651,6 +651,420 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------------
+// Plain decode (one query token, per-tensor scales) with E4M3 operands read
+// straight from the TMA tiles.  Q and P each enter the tensor core as two
+// E4M3 terms, hi = E4M3(x) and lo = E4M3(x - hi) (together ~8 significant
+// bits, as many as bf16), side by side in one N = 32 operand: rows 0..15 hi,
+// rows 16..31 lo.  A step is then 4 MMAs for S^T = K [Q_hi | Q_lo]^T (K-major
+// K tile as A) and 4 for O^T = V^T [P_hi | P_lo]^T (the V tile read MN-major),
+// with no conversion warps; the softmax adds the two S columns of a head and
+// the epilogue the two O columns.  With no f16 buffers the CTA needs ~110 KB
+// of shared memory and 128 TMEM columns, so two CTAs share an SM and one's
+// pipeline fill and drain overlap the other's steady state.  The dead rows
+// (past the sequence end) of a step's V tile are zeroed by the softmax thread
+// that owns the token before P.V reads them, so stale bytes never meet a zero
+// weight in the MMA.
+namespace x2 {
+constexpr int kThreads = 192;          // warp 0 producer, warp 1 MMA, warps 2-5 softmax and epilogue
+constexpr int kStages = 3;             // raw K and V steps in flight (two CTAs per SM: six)
+constexpr int kQBytes = 2 * kN * 128;  // [Q_hi ; Q_lo]: 32 rows x 128 dims E4M3, 128-byte swizzle
+constexpr int kPBytes = 2 * kN * 128;  // [P_hi ; P_lo]^T: 32 rows x 128 tokens E4M3, one buffer of two
+constexpr float kPScale = 64.f;
+constexpr float kTau = 2.75f;          // a raised reference keeps 64 p <= 64 * 2^2.75 < 448
+// TMEM: S^T (two buffers of 32 columns: hi heads 0..15, lo heads 16..31), O^T (32 columns, same split)
+constexpr uint32_t kTmemCols = 128, kTS = 0, kTO = 64;
+
+struct Smem {
+  uint64_t raw_full[kStages], raw_empty[kStages];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];  // by step parity
+  uint64_t q_full, final_mma, xchg;
+  uint32_t tmem_base, abort_flag;
+  float qs[kN];
+  float red[2][4][kN];  // per-warp partial maxima, double-buffered by step parity
+  float red2[4][kN];
+};
+
+constexpr size_t kSmemBytes = kStages * kRawStageBytes + kQBytes + 2 * kPBytes + sizeof(Smem) + 1024;
+static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs fit in an SM's shared memory");
+
+// Smallest e with amax <= 448 * 2^e (the per-head power-of-two scale of Q's hi term).
+__device__ __forceinline__ int pow2_exp_448(float amax) {
+  const uint32_t bits = __float_as_uint(amax);
+  const int expo = static_cast<int>((bits >> 23) & 0xFFu);
+  if (expo == 0) return -126;
+  const uint32_t mant = bits & 0x7FFFFFu;
+  return max((expo - 127) - (mant <= 0x600000u ? 8 : 7), -126);
+}
+
+// x -> (hi, lo) E4M3 codes of four values, hi = E4M3(x), lo = E4M3(x - hi).
+__device__ __forceinline__ void split_e4m3x4(float a, float b, float c, float d, uint32_t& hi, uint32_t& lo) {
+  hi = pack_e4m3x4(a, b, c, d);
+  const uint32_t h01 = e4m3x2_to_f16x2(hi & 0xFFFFu), h23 = e4m3x2_to_f16x2(hi >> 16);
+  lo = pack_e4m3x4(a - f16_lo(h01), b - f16_hi(h01), c - f16_lo(h23), d - f16_hi(h23));
+}
+}  // namespace x2
+
+template <int kG>
+__global__ void __launch_bounds__(x2::kThreads, 2)
+    gqa_x2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const Params prm) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* q_tile = smem + x2::kStages * kRawStageBytes;
+  uint8_t* p_tile = q_tile + x2::kQBytes;
+  x2::Smem* sm = reinterpret_cast<x2::Smem*>(p_tile + 2 * x2::kPBytes);
+  volatile uint32_t* abort_flag = &sm->abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int split = blockIdx.x % prm.splits;
+  const int seq = blockIdx.x / prm.splits;  // (b, kv head)
+  const int b = seq / prm.h_kv;
+  const int kvh = seq % prm.h_kv;
+
+  int s_k = prm.seqlens[b];
+  int n_pages = s_k > 0 ? (s_k + kPage - 1) / kPage : 0;
+  if (s_k < 0 || n_pages > prm.max_blocks) {
+    if (threadIdx.x == 0) atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_SEQLEN);
+    s_k = 0;
+    n_pages = 0;
+  }
+  const int n_steps_all = (n_pages + kPagesPerStep - 1) / kPagesPerStep;
+  const int st0 = static_cast<int>((static_cast<long long>(split) * n_steps_all) / prm.splits);
+  const int st1 = static_cast<int>((static_cast<long long>(split + 1) * n_steps_all) / prm.splits);
+  const int nsteps = st1 - st0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < x2::kStages; ++s) {
+      mbar_init(&sm->raw_full[s], 1);
+      mbar_init(&sm->raw_empty[s], 1);  // the P.V that read the step's V
+    }
+    for (int bf = 0; bf < 2; ++bf) {
+      mbar_init(&sm->s_full[bf], 1);
+      mbar_init(&sm->s_free[bf], 4);
+      mbar_init(&sm->p_full[bf], 4);
+      mbar_init(&sm->pv_done[bf], 1);
+    }
+    mbar_init(&sm->q_full, 4);
+    mbar_init(&sm->final_mma, 1);
+    mbar_init(&sm->xchg, 4);
+    sm->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm->tmem_base, x2::kTmemCols);
+    tmem_relinquish();
+  }
+  griddep_wait();  // inputs may come from the previous kernel in the stream
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_launch_dependents();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ----
+    // lanes 0..7 fetch a step's block-table entries one step ahead; lane 0 issues the loads
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    const int32_t* bt_row = prm.block_table + static_cast<size_t>(b) * prm.max_blocks;
+    auto fetch = [&](int step) {
+      const int p0 = (st0 + step) * kPagesPerStep;
+      return (step < nsteps && lane < min(kPagesPerStep, n_pages - p0)) ? __ldg(bt_row + p0 + lane) : 0;
+    };
+    int next = fetch(0);
+    int i = 0;
+    for (; i < nsteps; ++i) {
+      const int st = i % x2::kStages, use = i / x2::kStages;
+      const int p0 = (st0 + i) * kPagesPerStep;
+      const int np = min(kPagesPerStep, n_pages - p0);
+      int mine = next;
+      next = fetch(i + 1);
+      if (lane < np && (mine < 0 || mine >= prm.num_blocks)) {
+        atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_PAGE);
+        mine = 0;
+      }
+      int rows[kPagesPerStep];
+#pragma unroll
+      for (int p = 0; p < kPagesPerStep; ++p) rows[p] = (__shfl_sync(0xffffffffu, mine, p) * prm.h_kv + kvh) * kPage;
+      bool ok = true;
+      if (lane == 0) {
+        ok = use == 0 || wait_bounded(&sm->raw_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa);
+        if (ok) {
+          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd);
+          uint8_t* sb = smem + st * kRawStageBytes;
+#pragma unroll
+          for (int p = 0; p < kPagesPerStep; ++p) {
+            if (p >= np) break;
+            tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->raw_full[st], 0, rows[p], 0);
+            tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->raw_full[st], 0, rows[p], 0);
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    }
+    if (lane == 0)
+      for (int j = max(0, i - x2::kStages); j < i; ++j)
+        wait_bounded(&sm->raw_full[j % x2::kStages], (j / x2::kStages) & 1, nullptr, &g_status_gqa);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------- MMA issuer ----
+    // Q.K^T of step i, then P.V of step i - 1 once its P is written; the raw
+    // stage of a step is released by the commit after its P.V.
+    constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, 2 * kN, 128);  // E4M3: K (K-major) x [Q_hi|Q_lo]
+    constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, 0, 2 * kN, 128);  // E4M3: V^T (MN-major) x [P_hi|P_lo]^T
+    const bool leader = elect_one();
+    const uint32_t qb = smem_u32(q_tile);
+    bool ok = warp_wait(&sm->q_full, 0, abort_flag);
+    auto issue_pv = [&](int j) -> bool {
+      const int bf = j & 1, st = j % x2::kStages;
+      if (!warp_wait(&sm->p_full[bf], (j >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t vb = smem_u32(smem + st * kRawStageBytes + kOffRawV);
+      const uint32_t pb = smem_u32(p_tile + bf * x2::kPBytes);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // 32 tokens per MMA
+        mma_f8_ss_if(leader, tmem + x2::kTO, make_sdesc(vb + kk * 4096, kRawTile, 1024, SWIZZLE_128B),
+                     make_sdesc(pb + kk * 32, 16, 1024, SWIZZLE_128B), idesc_pv, (j == 0 && kk == 0) ? 0u : 1u);
+      tc_commit_if(leader, &sm->pv_done[bf]);
+      tc_commit_if(leader, &sm->raw_empty[st]);
+      return true;
+    };
+    for (int i = 0; ok && i < nsteps; ++i) {
+      const int st = i % x2::kStages, bf = i & 1;
+      if (!warp_wait(&sm->raw_full[st], (i / x2::kStages) & 1, abort_flag) ||
+          (i >= 2 && !warp_wait(&sm->s_free[bf], ((i - 2) >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t kb = smem_u32(smem + st * kRawStageBytes + kOffRawK);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // 32 dims per MMA
+        mma_f8_ss_if(leader, tmem + x2::kTS + bf * 2 * kN, make_sdesc(kb + kk * 32, 16, 1024, SWIZZLE_128B),
+                     make_sdesc(qb + kk * 32, 16, 1024, SWIZZLE_128B), idesc_qk, kk > 0 ? 1u : 0u);
+      tc_commit_if(leader, &sm->s_full[bf]);
+      if (i > 0 && !issue_pv(i - 1)) ok = false;
+    }
+    if (ok && nsteps > 0) issue_pv(nsteps - 1);
+    if (leader) tc_commit(&sm->final_mma);
+    __syncwarp();
+    warp_wait(&sm->final_mma, 0, nullptr);
+  } else {
+    // ------------------------- Q prep, softmax, epilogue (warps 2-5) ----
+    const int w = warp % 4;               // TMEM lane quarter of this warp
+    const int r = w * 32 + lane;          // token row of a step / TMEM lane / output dim
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(w * 32) << 16);
+    uint32_t xphase = 0;
+    auto xsync = [&]() -> bool {  // bounded, abort-aware exchange point of the 128 threads
+      warp_arrive(&sm->xchg);
+      const bool ok = warp_wait(&sm->xchg, xphase & 1, abort_flag);
+      ++xphase;
+      return ok;
+    };
+    const float k_scale = *prm.k_scale, v_scale = *prm.v_scale;
+    {
+      // [Q_hi ; Q_lo]: thread (head qh, eighth qj) splits dims [16 qj, 16 qj + 16) of q / qs
+      const int qh = r / 8, qj = r % 8;
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (qh < prm.group) {
+        const uint16_t* qrow = prm.q + (static_cast<size_t>(b) * prm.h_q + kvh * prm.group + qh) * kHd + qj * 16;
+        v0 = __ldg(reinterpret_cast<const uint4*>(qrow));
+        v1 = __ldg(reinterpret_cast<const uint4*>(qrow + 8));
+      }
+      const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      float amax = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(wd[k])), fabsf(bf16_hi(wd[k]))));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+      const int e = x2::pow2_exp_448(amax);
+      const float inv = exp2i(-e);
+      if (qj == 0) sm->qs[qh] = exp2i(e);
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        x2::split_e4m3x4(bf16_lo(wd[2 * k]) * inv, bf16_hi(wd[2 * k]) * inv, bf16_lo(wd[2 * k + 1]) * inv,
+                         bf16_hi(wd[2 * k + 1]) * inv, hi[k], lo[k]);
+      // row n, dims [16 qj, 16 qj + 16) = 16-byte chunk qj of the 128-byte row, XOR-swizzled by n % 8
+      const int nh = qh, nl = kN + qh;
+      *reinterpret_cast<uint4*>(q_tile + (nh / 8) * 1024 + (nh % 8) * 128 + ((qj ^ (nh % 8)) << 4)) =
+          make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(q_tile + (nl / 8) * 1024 + (nl % 8) * 128 + ((qj ^ (nl % 8)) << 4)) =
+          make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      for (int k = r; k < 2 * x2::kPBytes / 16; k += 128) reinterpret_cast<uint4*>(p_tile)[k] = make_uint4(0, 0, 0, 0);
+      fence_proxy_async_smem();
+      warp_arrive(&sm->q_full);
+    }
+    bool ok = xsync();  // qs[] and the zeroed P tiles complete
+    float c_h[kG], m_h[kG], l_h[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      c_h[h] = prm.softmax_scale * kLog2e * sm->qs[h] * k_scale;
+      m_h[h] = kNegInf;
+      l_h[h] = 0.f;
+    }
+    for (int i = 0; ok && i < nsteps; ++i) {
+      const int bf = i & 1, st = i % x2::kStages;
+      const bool live = (st0 + i) * kTok + r < s_k;
+      if (!warp_wait(&sm->s_full[bf], (i >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t s[2 * kN];
+      tmem_ld32(lane_base + x2::kTS + bf * 2 * kN, s);
+      tmem_ld_wait();
+      tc_fence_before();
+      warp_arrive(&sm->s_free[bf]);
+      if (!live) {  // a token past the end: zero its V row, so that P.V multiplies zeros by its zero weight
+        uint4* vrow = reinterpret_cast<uint4*>(smem + st * kRawStageBytes + kOffRawV + r * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) vrow[c] = make_uint4(0, 0, 0, 0);
+      }
+      float v[kG];
+#pragma unroll
+      for (int h = 0; h < kG; ++h)
+        v[h] = live ? (__uint_as_float(s[h]) + __uint_as_float(s[kN + h])) * c_h[h] : kNegInf;
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        float x = v[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        if (lane == 0) sm->red[i & 1][w][h] = x;
+      }
+      if (!xsync()) {
+        ok = false;
+        break;
+      }
+      float alpha[kG];
+      bool any_rescale = false;
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        const float* rm = &sm->red[i & 1][0][0];
+        const float mx = fmaxf(fmaxf(rm[h], rm[kN + h]), fmaxf(rm[2 * kN + h], rm[3 * kN + h]));
+        alpha[h] = 1.f;
+        if (mx > m_h[h] + x2::kTau) {
+          alpha[h] = ex2_approx(m_h[h] - mx);
+          any_rescale |= (i > 0);
+          m_h[h] = mx;
+        }
+      }
+      uint8_t phi[kG], plo[kG];
+#pragma unroll
+      for (int h = 0; h < kG; h += 4) {
+        float p[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          p[k] = ex2_approx(v[h + k] - (m_h[h + k] == kNegInf ? 0.f : m_h[h + k]));
+          l_h[h + k] = l_h[h + k] * alpha[h + k] + p[k];
+        }
+        uint32_t hi, lo;
+        x2::split_e4m3x4(p[0] * x2::kPScale, p[1] * x2::kPScale, p[2] * x2::kPScale, p[3] * x2::kPScale, hi, lo);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          phi[h + k] = static_cast<uint8_t>(hi >> (8 * k));
+          plo[h + k] = static_cast<uint8_t>(lo >> (8 * k));
+        }
+      }
+      // O is rescaled only after the previous step's P.V; the P buffer is
+      // rewritten only after the P.V that read it two steps ago
+      if (any_rescale) {
+        if (!warp_wait(&sm->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+      } else if (i >= 2 && !warp_wait(&sm->pv_done[bf], ((i - 2) >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (any_rescale) {
+        uint32_t o[2 * kN];
+        tmem_ld32(lane_base + x2::kTO, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+          o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+          o[kN + h] = __float_as_uint(__uint_as_float(o[kN + h]) * alpha[h]);
+        }
+        tmem_st32(lane_base + x2::kTO, o);
+        tmem_st_wait();
+      }
+      // [P_hi ; P_lo]^T (K-major over tokens): row n, token r -> 16-byte chunk r / 16 (XOR n % 8), byte r % 16
+      {
+        uint8_t* pt = p_tile + bf * x2::kPBytes;
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+          const int nl = kN + h;
+          pt[(h / 8) * 1024 + (h % 8) * 128 + (((r >> 4) ^ (h % 8)) << 4) + (r & 15)] = phi[h];
+          pt[(nl / 8) * 1024 + (nl % 8) * 128 + (((r >> 4) ^ (nl % 8)) << 4) + (r & 15)] = plo[h];
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      warp_arrive(&sm->p_full[bf]);
+    }
+
+    const bool whole = prm.splits == 1;
+    const size_t slot = static_cast<size_t>(seq) * prm.splits + split;
+    const float o_scale = v_scale / x2::kPScale;
+    if (ok && nsteps > 0 && warp_wait(&sm->pv_done[(nsteps - 1) & 1], ((nsteps - 1) >> 1) & 1, abort_flag)) {
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        float x = l_h[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) sm->red2[w][h] = x;
+      }
+      ok = xsync();
+      uint32_t o[2 * kN];
+      tmem_ld32(lane_base + x2::kTO, o);
+      tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        if (h >= prm.group) break;
+        const float lsum = (sm->red2[0][h] + sm->red2[1][h]) + (sm->red2[2][h] + sm->red2[3][h]);
+        const float oh = __uint_as_float(o[h]) + __uint_as_float(o[kN + h]);
+        const size_t orow = static_cast<size_t>(b) * prm.h_q + kvh * prm.group + h;
+        if (whole) {
+          float f, lse_v;
+          finish_row(m_h[h], lsum, kNegInf, o_scale, &f, &lse_v);
+          prm.out[orow * kHd + r] = static_cast<uint16_t>(pack_bf16x2(oh * f, 0.f));
+          if (r == 0) prm.lse[orow] = lse_v;
+        } else {
+          prm.ws_o[(slot * kN + h) * kHd + r] = oh * o_scale;
+          if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(lsum > 0.f ? m_h[h] : kNegInf, lsum);
+        }
+      }
+    } else if (ok && nsteps == 0) {
+      for (int h = 0; h < prm.group; ++h) {
+        const size_t orow = static_cast<size_t>(b) * prm.h_q + kvh * prm.group + h;
+        if (whole) {  // no key: out 0, lse -inf
+          prm.out[orow * kHd + r] = 0;
+          if (r == 0) prm.lse[orow] = kNegInf;
+        } else {
+          prm.ws_o[(slot * kN + h) * kHd + r] = 0.f;
+          if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(kNegInf, 0.f);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, x2::kTmemCols);
+  }
+}
+
 // Merge of split partials: one warp per (sequence = (b, kv head), column = (token, head)), lane l owns
 // 4 dims; a sink logit joins the merged denominator once.
 __global__ void gqa_combine_kernel(const float* __restrict__ ws_o, const float2* __restrict__ ws_ml, int splits,
@@ -824,17 +1238,23 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   prm.softmax_scale = softmax_scale;
   static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
   if (configure_once(configured, [] {
-        const void* fns[12] = {
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 0>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 0>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 0>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 1>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 1>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 1>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 2>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 2>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 2>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 3>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 3>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 3>)};
+        const void* f16[9] = {
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 1>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 1>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 1>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 2>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 2>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 2>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 3>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 3>),
+            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 3>)};
+        const void* two_term[3] = {reinterpret_cast<const void*>(gqa::gqa_x2_kernel<4>),
+                                   reinterpret_cast<const void*>(gqa::gqa_x2_kernel<8>),
+                                   reinterpret_cast<const void*>(gqa::gqa_x2_kernel<16>)};
         cudaError_t e = cudaSuccess;
-        for (const void* f : fns)
+        for (const void* f : f16)
           if (e == cudaSuccess)
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(gqa::kSmemBytes));
+        for (const void* f : two_term)
+          if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(gqa::x2::kSmemBytes));
         return e;
       }) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
@@ -842,16 +1262,21 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   if (grid > 0x7FFFFFFFll) return FP8MLA_ERR_INVALID_ARG;
   const int ncols = q_len * prm.group;
   using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const gqa::Params);
-  static const KernelFn table[4][3] = {
-      {gqa::gqa_decode_kernel<4, 0>, gqa::gqa_decode_kernel<8, 0>, gqa::gqa_decode_kernel<16, 0>},
+  // plain decode: the two-term E4M3 kernel; per-row scales or the XQA options: the f16 kernel's instances
+  static const KernelFn two_term[3] = {gqa::gqa_x2_kernel<4>, gqa::gqa_x2_kernel<8>, gqa::gqa_x2_kernel<16>};
+  static const KernelFn table[3][3] = {
       {gqa::gqa_decode_kernel<4, 1>, gqa::gqa_decode_kernel<8, 1>, gqa::gqa_decode_kernel<16, 1>},
       {gqa::gqa_decode_kernel<4, 2>, gqa::gqa_decode_kernel<8, 2>, gqa::gqa_decode_kernel<16, 2>},
       {gqa::gqa_decode_kernel<4, 3>, gqa::gqa_decode_kernel<8, 3>, gqa::gqa_decode_kernel<16, 3>}};
   const bool ext = q_len > 1 || window > 0 || spec_mask != nullptr || sinks != nullptr;
-  const KernelFn kernel = table[(scale_rows ? 1 : 0) | (ext ? 2 : 0)][ncols <= 4 ? 0 : (ncols <= 8 ? 1 : 2)];
-  if (launch_dependent(kernel, dim3(static_cast<unsigned>(grid)), dim3(gqa::kThreads), gqa::kSmemBytes, stream, tk,
-                       tv, prm) != cudaSuccess)
-    return FP8MLA_ERR_CUDA;
+  const int mode = (scale_rows ? 1 : 0) | (ext ? 2 : 0);
+  const int gi = ncols <= 4 ? 0 : (ncols <= 8 ? 1 : 2);
+  const cudaError_t le =
+      mode == 0 ? launch_dependent(two_term[gi], dim3(static_cast<unsigned>(grid)), dim3(gqa::x2::kThreads),
+                                   gqa::x2::kSmemBytes, stream, tk, tv, prm)
+                : launch_dependent(table[mode - 1][gi], dim3(static_cast<unsigned>(grid)), dim3(gqa::kThreads),
+                                   gqa::kSmemBytes, stream, tk, tv, prm);
+  if (le != cudaSuccess) return FP8MLA_ERR_CUDA;
   if (splits > 1) {
     dim3 cg(static_cast<unsigned>(bs * h_kv), (ncols + 3) / 4);
     if (launch_dependent(gqa::gqa_combine_kernel, cg, dim3(128), 0, stream, prm.ws_o, prm.ws_ml, splits, prm.group,
