@@ -139,8 +139,8 @@ FP8MLA_API fp8mla_status_t fp8mla_get_metadata(const int32_t* cache_seqlens, int
 
 /* Workspace of fp8mla_decode: (b + num_units) split-KV partial slots of
  * 128 x 512 bf16 accumulators plus 128 (m, l) pairs each, then (FP8 dots) per
- * sequence its quantised Q (219 136 bytes: the decode kernel's Q slots and the
- * bf16 quantisation error used for the LSE correction) and 128 Q scales. */
+ * sequence its quantised Q (88 064 bytes: the decode kernel's Q slots) and
+ * 128 Q scales. */
 FP8MLA_API size_t fp8mla_workspace_bytes(int b, int s_q, int h_q, int num_units);
 
 /* fp8mla_decode -- dense MLA decode over the paged E4M3 cache.
@@ -326,8 +326,8 @@ FP8MLA_API fp8mla_status_t fp8_paged_cache_write(const void* x, int64_t x_token_
  *
  * Same arguments and results as fp8mla_decode without the schedule and the
  * workspace: the call schedules one work unit per sequence (no split-KV) and
- * keeps its schedule, split counts and quantised Q (with its quantisation error) in a fixed
- * device array compiled into this library (14.1 MB, held by every GPU that
+ * keeps its schedule, split counts and quantised Q in a fixed
+ * device array compiled into this library (5.7 MB, held by every GPU that
  * loads the library until the process exits).  It calls no allocator.
  *   b <= FP8MLA_NO_ALLOC_MAX_BATCH; a larger batch returns
  *   FP8MLA_ERR_WORKSPACE_TOO_SMALL and launches nothing.

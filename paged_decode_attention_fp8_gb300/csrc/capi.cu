@@ -115,8 +115,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [partial O | partial (m, l) | quantised Q and its quantisation
-//             error (FP8 dots) | per-row Q scale]
+// Workspace: [partial O | partial (m, l) | quantised Q (FP8 dots) | per-row Q scale]
 struct MlaWorkspace {
   size_t o, ml, qbuf, qscale, total;
 };
@@ -273,8 +272,9 @@ fp8mla_status_t mla_decode_call(const void* q, const void* kv_cache, fp8mla_kv_d
                                      : launch_mla_decode_16bit(tm_lat, tm_rope, prm, num_units, s);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess)
-    e = launch_mla_combine(num_splits, prm.ws_o, prm.ws_ml, dot_mode == FP8MLA_DOT_FP8 ? prm.qbuf : nullptr,
-                           softmax_scale, prm.out, lse, b, s_q * h_q, s);
+    e = launch_mla_combine(num_splits, prm.ws_o, prm.ws_ml, dot_mode == FP8MLA_DOT_FP8 ? prm.q : nullptr,
+                           dot_mode == FP8MLA_DOT_FP8 ? prm.qscale : nullptr, softmax_scale, prm.out, lse, b,
+                           s_q * h_q, s);
   if (e == cudaSuccess) e = mark(3);
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
   if (timed) timer.timed = true;

@@ -204,34 +204,50 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
 // a rescale of what is accumulated so far between rounds:
 // M = max m_s, L = sum l_s 2^(m_s - M), out = sum acc_s 2^(m_s - M) / L,
 // lse = ln2 (M + log2 L).  Partial slots are [slot][128] rows of dv = 512
-// bf16, sequence bi owning the slots from num_splits[bi].  With qerr non-null
+// bf16, sequence bi owning the slots from num_splits[bi].  With q non-null
 // (FP8 dots) every row's LSE also gets the first-order Q-quantisation
-// correction lse -= softmax_scale (q_hat - q) . out, from the row's stored
-// error (bf16 x 512 at qerr + bi * qerr_stride) and the finished output row.
+// correction lse -= softmax_scale (q_hat - q) . out, from the finished output
+// row and q_hat - q of the row's latent part: q_hat = E4M3(q / qs) qs with the
+// row's power-of-two scale qs, the prep kernel's rounding (exact in fp32).
 __global__ void __launch_bounds__(256) mla_combine_kernel(
     const int32_t* __restrict__ num_splits, const uint16_t* __restrict__ ws_o, const float2* __restrict__ ws_ml,
-    const uint8_t* __restrict__ qerr, size_t qerr_stride, float softmax_scale, uint16_t* __restrict__ out,
-    float* __restrict__ lse, int rows) {
+    const uint16_t* __restrict__ q, const float* __restrict__ qscale, float softmax_scale,
+    uint16_t* __restrict__ out, float* __restrict__ lse, int rows) {
   const int bi = blockIdx.x;
   const int r = blockIdx.y * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // The split counts and the quantisation error were final before the decode
-  // kernel started (it waited for them), so they are read before waiting for it.
+  // The split counts and the row scales were final before the decode kernel
+  // started (it waited for them), so they are read before waiting for it.
   const int s0 = __ldg(num_splits + bi);
   const int ns = __ldg(num_splits + bi + 1) - s0;
-  uint4 ev0 = make_uint4(0, 0, 0, 0), ev1 = ev0;
-  if (qerr != nullptr && r < rows) {
-    const uint4* e = reinterpret_cast<const uint4*>(qerr + bi * qerr_stride + static_cast<size_t>(r) * kMlaDV * 2) +
-                     lane * 2;
-    ev0 = __ldg(e);
-    ev1 = __ldg(e + 1);
+  float ev[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) ev[k] = 0.f;
+  if (q != nullptr && r < rows) {
+    const size_t row_q = static_cast<size_t>(bi) * rows + r;
+    const uint4* qv = reinterpret_cast<const uint4*>(q + row_q * kMlaD) + lane * 2;  // latent dims [16 lane, +16)
+    const uint4 a = __ldg(qv), c = __ldg(qv + 1);
+    const float qs = __ldg(qscale + static_cast<size_t>(bi) * kMlaRows + r);
+    // 1 / qs as the prep kernel forms it: the power of two with the opposite exponent
+    const int qe = static_cast<int>((__float_as_uint(qs) >> 23) & 0xFFu) - 127;
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - qe) << 23);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+      const uint32_t codes = pack_e4m3x4(bf16_lo(w[k]) * inv, bf16_hi(w[k]) * inv, bf16_lo(w[k + 1]) * inv,
+                                         bf16_hi(w[k + 1]) * inv);
+      const uint32_t h01 = e4m3x2_to_f16x2(codes & 0xFFFFu), h23 = e4m3x2_to_f16x2(codes >> 16);
+      ev[2 * k] = f16_lo(h01) * qs - bf16_lo(w[k]);
+      ev[2 * k + 1] = f16_hi(h01) * qs - bf16_hi(w[k]);
+      ev[2 * k + 2] = f16_lo(h23) * qs - bf16_lo(w[k + 1]);
+      ev[2 * k + 3] = f16_hi(h23) * qs - bf16_hi(w[k + 1]);
+    }
   }
   // (q_hat - q) . o over the whole row, o holding this lane's 16 columns
   auto err_dot = [&](const float (&o)[16]) {
-    const uint32_t w[8] = {ev0.x, ev0.y, ev0.z, ev0.w, ev1.x, ev1.y, ev1.z, ev1.w};
     float d = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) d += bf16_lo(w[q]) * o[2 * q] + bf16_hi(w[q]) * o[2 * q + 1];
+    for (int k = 0; k < 8; ++k) d += ev[2 * k] * o[2 * k] + ev[2 * k + 1] * o[2 * k + 1];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
     return d;
@@ -241,7 +257,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(
   const size_t row = static_cast<size_t>(bi) * rows + r;
   uint16_t* orow = out + row * kMlaDV + lane * 16;
   if (ns == 1) {
-    if (qerr != nullptr) {
+    if (q != nullptr) {
       const uint4 a = reinterpret_cast<const uint4*>(orow)[0], b2 = reinterpret_cast<const uint4*>(orow)[1];
       const uint32_t w[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
       float o[16];
@@ -339,7 +355,7 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(
   const float inv = big_l > 0.f ? 1.f / big_l : 0.f;
 #pragma unroll
   for (int c = 0; c < 16; ++c) acc[c] *= inv;
-  const float d = qerr != nullptr ? err_dot(acc) : 0.f;  // the LSE correction from the merged output row
+  const float d = q != nullptr ? err_dot(acc) : 0.f;  // the LSE correction from the merged output row
   uint4 w0, w1;
   w0.x = pack_bf16x2(acc[0], acc[1]);
   w0.y = pack_bf16x2(acc[2], acc[3]);
@@ -377,12 +393,11 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
 }
 
 cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,
-                               const uint8_t* qbuf, float softmax_scale, uint16_t* out, float* lse, int b, int rows,
-                               cudaStream_t stream) {
+                               const uint16_t* q, const float* qscale, float softmax_scale, uint16_t* out,
+                               float* lse, int b, int rows, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
-  const uint8_t* qerr = qbuf != nullptr ? qbuf + kMlaQErrOff : nullptr;
   return launch_dependent(mla_combine_kernel, dim3(b, (rows + 7) / 8), dim3(256), 0, stream, num_splits, ws_o, ws_ml,
-                          qerr, static_cast<size_t>(kMlaQBytes), softmax_scale, out, lse, rows);
+                          q, qscale, softmax_scale, out, lse, rows);
 }
 
 uint32_t metadata_read_and_clear_status() {

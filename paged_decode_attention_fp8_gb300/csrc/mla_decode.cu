@@ -38,7 +38,8 @@
 //   * FP8 dots perturb the LSE by softmax_scale * (q_hat - q) . k_mean, where
 //     k_mean = sum_j p_j k_j; its latent part is exactly the output row, so
 //     the combine kernel subtracts softmax_scale * (q_hat - q) . out, from the
-//     quantisation error the prep kernel stored and the finished output row.
+//     finished output row and q_hat - q recomputed from q and the row's scale
+//     with the prep kernel's rounding.
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
 // owner, warps 2-3 page conversion (the RoPE part to f16, or the whole page
@@ -640,10 +641,7 @@ constexpr int kQRopePitch = 144;
 constexpr int kQLatSlotBytes = kRows * kQLatPitch;
 constexpr int kQRopeSlotBytes = kRows * kQRopePitch;
 static_assert(kQLatSlotBytes <= kStageBytes && kQRopeSlotBytes <= kStageBytes, "a Q slot fits one stage");
-// After the slots: the latent quantisation error q_hat qs - q, 128 rows x 512
-// bf16, read by the combine kernel for the LSE correction.
-constexpr int kQErrOff = 2 * kQLatSlotBytes + kQRopeSlotBytes;
-static_assert(kQErrOff == kMlaQErrOff && kQErrOff + kRows * kDLat * 2 == kMlaQBytes, "quantised-Q layout");
+static_assert(2 * kQLatSlotBytes + kQRopeSlotBytes == kMlaQBytes, "quantised-Q layout");
 static_assert(kStageBytes % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
               "1 KB aligned tiles");
 static_assert(kStageBytes == static_cast<int>(kPageTxBytes), "a page fills one stage");
@@ -672,7 +670,7 @@ static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a
 // of the row's 72 (64 latent, 8 RoPE).
 template <int kTpr>
 __device__ __forceinline__ void fill_q_row(const MlaParams& prm, int b, int r, int part, uint8_t* slot0,
-                                           uint8_t* slot1, uint8_t* slot2, uint8_t* err, float* qs_out) {
+                                           uint8_t* slot1, uint8_t* slot2, float* qs_out) {
   constexpr int kChunks = 72 / kTpr;
   constexpr bool kHold = kChunks <= 18;  // few enough chunks to keep in registers between the two passes
   const int R = prm.s_q * prm.h_q;
@@ -698,16 +696,6 @@ __device__ __forceinline__ void fill_q_row(const MlaParams& prm, int b, int r, i
       o.y = pack_e4m3x4(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs, bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs);
       uint8_t* slot = (c < 32) ? slot0 : slot1;
       *reinterpret_cast<uint2*>(slot + r * kQLatPitch + (c & 31) * 8) = o;
-      const float qs = exp2i(qe);
-      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t hq[4] = {e4m3x2_to_f16x2(o.x & 0xFFFFu), e4m3x2_to_f16x2(o.x >> 16), e4m3x2_to_f16x2(o.y & 0xFFFFu),
-                              e4m3x2_to_f16x2(o.y >> 16)};
-      uint4 ev;
-      uint32_t* e4 = &ev.x;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        e4[k] = pack_bf16x2(f16_lo(hq[k]) * qs - bf16_lo(w[k]), f16_hi(hq[k]) * qs - bf16_hi(w[k]));
-      *reinterpret_cast<uint4*>(err + r * kDLat * 2 + c * 16) = ev;
     } else {
       uint4 o;
       o.x = pack_f16x2(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs);
@@ -742,7 +730,7 @@ __global__ void __launch_bounds__(256) mla_qprep_kernel(const MlaParams prm) {
   const int b = blockIdx.x;
   const int r = blockIdx.y * 32 + threadIdx.x / 8;
   uint8_t* q = prm.qbuf + static_cast<size_t>(b) * kMlaQBytes;
-  fill_q_row<8>(prm, b, r, threadIdx.x % 8, q, q + kQLatSlotBytes, q + 2 * kQLatSlotBytes, q + kQErrOff,
+  fill_q_row<8>(prm, b, r, threadIdx.x % 8, q, q + kQLatSlotBytes, q + 2 * kQLatSlotBytes,
                 prm.qscale + static_cast<size_t>(b) * kRows);
 }
 

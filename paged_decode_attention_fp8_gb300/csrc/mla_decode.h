@@ -35,10 +35,8 @@ constexpr int kMlaPage = 64;
 constexpr int kMlaD = 576;
 constexpr int kSchedFixedCost = 4;
 // One sequence's quantised Q, in the decode kernel's ring-slot layout (two
-// latent slots of 128 x 272 bytes, one RoPE slot of 128 x 144 bytes), then
-// the latent quantisation error (q_hat qs - q) as 128 x 512 bf16.
-constexpr int kMlaQBytes = 219136;
-constexpr int kMlaQErrOff = 88064;  // offset of the quantisation error inside one sequence's block
+// latent slots of 128 x 272 bytes, one RoPE slot of 128 x 144 bytes).
+constexpr int kMlaQBytes = 88064;
 constexpr size_t kMetadataMaxSmem = 200 * 1024;  // the scheduler stages ~16 bytes per sequence and unit
 size_t metadata_smem_bytes(int b, int num_units);
 
@@ -65,12 +63,13 @@ cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream);
 // metadata + combine (metadata.cu)
 cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, int force_splits, int32_t* tile_sched,
                                 int32_t* num_splits, cudaStream_t stream);
-// Merges split partials into out / lse, and (FP8 dots: qbuf, the quantised Q
-// blocks, non-null) applies the first-order Q-quantisation correction to every
-// row's LSE from the finished output row and the stored quantisation error.
+// Merges split partials into out / lse, and (FP8 dots: q, the bf16 queries,
+// and qscale, their per-row power-of-two scales, non-null) applies the
+// first-order Q-quantisation correction to every row's LSE from the finished
+// output row and q_hat - q, recomputed with the prep kernel's rounding.
 cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,
-                               const uint8_t* qbuf, float softmax_scale, uint16_t* out, float* lse, int b, int rows,
-                               cudaStream_t stream);
+                               const uint16_t* q, const float* qscale, float softmax_scale, uint16_t* out,
+                               float* lse, int b, int rows, cudaStream_t stream);
 uint32_t metadata_read_and_clear_status();
 
 }  // namespace fp8mla

@@ -22,7 +22,7 @@ constexpr size_t kSchedBytes = 256 * 8 * sizeof(int32_t);                       
 constexpr size_t kSplitsBytes = 256 * sizeof(int32_t);                            // split prefix, <= 255 sequences
 constexpr size_t kQBufBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaQBytes;    // quantised Q
 constexpr size_t kQScaleBytes = static_cast<size_t>(kNoAllocMaxBatch) * kMlaRows * sizeof(float);
-constexpr size_t kScratchBytes = kSchedBytes + kSplitsBytes + kQBufBytes + kQScaleBytes;  // 14.1 MB
+constexpr size_t kScratchBytes = kSchedBytes + kSplitsBytes + kQBufBytes + kQScaleBytes;  // 5.7 MB
 static_assert(kNoAllocMaxBatch <= 255, "the split prefix holds b + 1 entries");
 
 // Held by every GPU that loads the library, for the life of the process.
@@ -112,8 +112,9 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
     e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_decode_fp8(tm_lat, tm_rope, prm, units, s)
                                      : launch_mla_decode_16bit(tm_lat, tm_rope, prm, units, s);
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
-  if (launch_mla_combine(num_splits, nullptr, nullptr, dot_mode == FP8MLA_DOT_FP8 ? qbuf : nullptr, softmax_scale,
-                         prm.out, lse, b, s_q * h_q, s) != cudaSuccess)
+  if (launch_mla_combine(num_splits, nullptr, nullptr, dot_mode == FP8MLA_DOT_FP8 ? prm.q : nullptr,
+                         dot_mode == FP8MLA_DOT_FP8 ? qscale : nullptr, softmax_scale, prm.out, lse, b, s_q * h_q,
+                         s) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   return FP8MLA_OK;
 }
