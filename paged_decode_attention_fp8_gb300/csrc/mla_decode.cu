@@ -266,7 +266,11 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer ----
-    if (lane == 0) {
+    // The whole warp runs the loop (warp-uniform descriptors and bounded
+    // waits) and one elected lane issues: from a lone thread each MMA costs
+    // about twice as long.
+    {
+      const bool leader = elect_one();
       const uint32_t t_s = tmem + C::kTS, t_o = tmem + C::kTO;
       SegmentWalker walk(prm, unit);
       Segment sg;
@@ -274,51 +278,47 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
       bool ok = true;
 
       auto issue_qk = [&](uint32_t sb) {
-        {
-          constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);
+        constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);
 #pragma unroll
-          for (int kk = 0; kk < 36; ++kk) {
-            const uint64_t bd =
-                make_sdesc(sb + C::kOffCvt + (kk >> 2) * kLatBox + (kk & 3) * 32, 16, 1024, SWIZZLE_128B);
-            mma_f16_ts(t_s, tmem + C::kTQ + kk * 8, bd, idesc16, kk > 0 ? 1u : 0u);
-          }
+        for (int kk = 0; kk < 36; ++kk) {
+          const uint64_t bd =
+              make_sdesc(sb + C::kOffCvt + (kk >> 2) * kLatBox + (kk & 3) * 32, 16, 1024, SWIZZLE_128B);
+          mma_f16_ts_if(leader, t_s, tmem + C::kTQ + kk * 8, bd, idesc16, kk > 0 ? 1u : 0u);
         }
       };
 
       auto issue_pv = [&](int j, bool first_in_seg) -> bool {
-        if (!wait_bounded(&bars->p_full, j & 1, abort_flag, &g_status_mla, __LINE__)) return false;
+        if (!warp_wait(&bars->p_full, j & 1, abort_flag, __LINE__)) return false;
         tc_fence_after();
         const int st = j % C::kStages;
         const uint32_t sb = smem_u32(smem + st * C::kStageBytes);
-        {
-          constexpr uint32_t idesc = make_idesc(1, 1, 0, 1, 128, 128);   // bf16, B MN-major, N = 128
-          const uint32_t v_base = sb + C::kOffCvt + part * 2 * kLatBox;
+        constexpr uint32_t idesc = make_idesc(1, 1, 0, 1, 128, 128);  // bf16, B MN-major, N = 128
+        const uint32_t v_base = sb + C::kOffCvt + part * 2 * kLatBox;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = make_sdesc(v_base + kk * 2048, kLatBox, 1024, SWIZZLE_128B);
-            mma_f16_ts(t_o, tmem + C::kTP + kk * 8, bd, idesc, (first_in_seg && kk == 0) ? 0u : 1u);
-          }
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bd = make_sdesc(v_base + kk * 2048, kLatBox, 1024, SWIZZLE_128B);
+          mma_f16_ts_if(leader, t_o, tmem + C::kTP + kk * 8, bd, idesc, (first_in_seg && kk == 0) ? 0u : 1u);
         }
-        tc_commit(&bars->pv_done);
-        tc_commit(&bars->kv_empty[st]);
+        tc_commit_if(leader, &bars->pv_done);
+        tc_commit_if(leader, &bars->kv_empty[st]);
         return true;
       };
 
       while (ok && walk.next(sg)) {
-        if (!wait_bounded(&bars->q_full, seg_i & 1, abort_flag, &g_status_mla, __LINE__)) break;
+        if (!warp_wait(&bars->q_full, seg_i & 1, abort_flag, __LINE__)) break;
         const int first_i = i;
         for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
           const int st = i % C::kStages;
           const int use = i / C::kStages;
-          if (!wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla, __LINE__) ||
-              !wait_bounded(&bars->cvt_ready[st], use & 1, abort_flag, &g_status_mla, __LINE__) ||
-              (i > 0 && !wait_bounded(&bars->s_free, (i - 1) & 1, abort_flag, &g_status_mla, __LINE__))) {
+          if (!warp_wait(&bars->kv_full[st], use & 1, abort_flag, __LINE__) ||
+              !warp_wait(&bars->cvt_ready[st], use & 1, abort_flag, __LINE__) ||
+              (i > 0 && !warp_wait(&bars->s_free, (i - 1) & 1, abort_flag, __LINE__))) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_qk(smem_u32(smem + st * C::kStageBytes));
-          tc_commit(&bars->s_full);
+          tc_commit_if(leader, &bars->s_full);
           if (i > first_i && !issue_pv(i - 1, i - 1 == first_i)) {
             ok = false;
             break;
@@ -328,10 +328,10 @@ __global__ void __launch_bounds__(Cfg16::kThreads, 1)
         if (!issue_pv(i - 1, i - 1 == first_i)) break;
         ++seg_i;
       }
-      tc_commit(&bars->final_mma);
-      wait_bounded(&bars->final_mma, 0, nullptr, &g_status_mla, __LINE__);
+      if (leader) tc_commit(&bars->final_mma);
+      __syncwarp();
+      warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
     }
-    __syncwarp();
   } else if (warp == 2 || warp == 3) {
     // ------------------------------- page conversion, tail zeroing ----
     const int t = threadIdx.x - 64;  // token row of the page
