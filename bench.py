@@ -474,19 +474,24 @@ def _leg_result(metric, avg_ms, ms, nbytes, flops_fp8, flops_16, peaks, cfg, lau
     }
 
 
-def leg_mla(dev, peaks, steps, warmup, dot, seqlens, seed, label, value_pages=None):
-    """Dense MLA decode call (FP8 or 16-bit dots) on b = len(seqlens), s_q = 2, h_q = 64."""
+def leg_mla(dev, peaks, steps, warmup, dot, seqlens, seed, label, value_pages=None, rows=False):
+    """Dense MLA decode call (FP8 or 16-bit dots) on b = len(seqlens), s_q = 2, h_q = 64; with
+    rows, one KV scale per cached row ([num_pages, 1, 64], FP8 dots)."""
     import torch
 
     import paged_decode_attention_fp8_gb300 as fm
     from paged_decode_attention_fp8_gb300 import synthetic as syn
     b, s_q, h_q = len(seqlens), 2, 64
-    inp = syn.mla_inputs(seed, b, s_q, h_q, seqlens, causal=True, spare_pages=16, value_pages=value_pages)
+    if rows:
+        inp, row_scales = syn.mla_row_scaled_inputs(seed, b, s_q, h_q, seqlens, causal=True, spare_pages=16,
+                                                    value_pages=value_pages)
+    else:
+        inp = syn.mla_inputs(seed, b, s_q, h_q, seqlens, causal=True, spare_pages=16, value_pages=value_pages)
     kv_bytes = sum(seqlens) * MLA_D
     copies = max(1, min(3, math.ceil(2 * 129e6 / kv_bytes)))
     kvs = [inp.kv_cache.to(dev) for _ in range(copies)]
     q, bt, sl = inp.q.to(dev), inp.block_table.to(dev), inp.seqlens.to(dev)
-    scale = torch.tensor([inp.kv_scale], dtype=torch.float32, device=dev)
+    scale = row_scales.to(dev) if rows else torch.tensor([inp.kv_scale], dtype=torch.float32, device=dev)
     units = fm.metadata_units()
     ts, ns = fm.get_metadata(sl, h_q, s_q, num_units=units)
     out = torch.empty((b, s_q, h_q, MLA_DV), dtype=torch.bfloat16, device=dev)
@@ -503,9 +508,12 @@ def leg_mla(dev, peaks, steps, warmup, dot, seqlens, seed, label, value_pages=No
         f8, f16 = 0.0, f8 + f16
     cfg = dict(workload="mla_decode", b=b, s_q=s_q, h_q=h_q, d=576, dv=512, page=64, seqlens=label, causal=True,
                dot=dot, l2=f"{copies} rotating cache copies ({copies * kv_bytes / 1e6:.0f} MB)",
-               values="pooled N(0,1) pages" if value_pages else "N(0,1)")
-    res = _leg_result(f"dense MLA decode us/call ({label}, {dot} dots)", avg, ms, mla_bytes(seqlens, b, s_q, h_q),
-                      f8, f16, peaks, cfg, 3 if dot == "fp8" else 2)
+               values="pooled N(0,1) pages" if value_pages else "N(0,1)",
+               scales="per row [num_pages, 1, 64], (amax/448) 2^U[0,3]" if rows else "per tensor")
+    nbytes = mla_bytes(seqlens, b, s_q, h_q) + (sum((x + 63) // 64 for x in seqlens) * 64 * 4 if rows else 0)
+    what = f"{label}, {dot} dots" + (", per-row KV scales" if rows else "")
+    res = _leg_result(f"dense MLA decode us/call ({what})", avg, ms, nbytes, f8, f16, peaks, cfg,
+                      3 if dot == "fp8" else 2)
     res["tflops_convention"] = round(mla_flops(seqlens, s_q, h_q) / (avg * 1e-3) / 1e12, 1)
     return res
 
@@ -539,7 +547,11 @@ def leg_sparse(dev, peaks, steps, warmup, s_q):
                        flops, 0.0, peaks, cfg, launches)
 
 
-def leg_gqa(dev, peaks, steps, warmup):
+def leg_gqa(dev, peaks, steps, warmup, variant="plain"):
+    """Paged GQA decode, bs = 32, 32/8 heads, hd 128, ctx U[1024, 16384].  variant "plain": one
+    query token, per-tensor scales (paged_gqa_decode); "rows": one KV scale per cached row;
+    "xqa": a speculative block of 4 query tokens with a seeded block mask, a 4096-key sliding
+    window and attention sinks (paged_gqa_decode_ext)."""
     import torch
 
     import paged_decode_attention_fp8_gb300 as fm
@@ -547,30 +559,57 @@ def leg_gqa(dev, peaks, steps, warmup):
     seqlens = syn.uniform_seqlens(5, 32, 1024, 16384)
     inp = syn.gqa_inputs(5, 32, seqlens, value_blocks=4096)
     sets = [(inp.k_cache.to(dev), inp.v_cache.to(dev)) for _ in range(2)]
-    q, bt, sl = inp.q.to(dev), inp.block_table.to(dev), inp.seqlens.to(dev)
-    ks = torch.tensor([inp.k_scale], dtype=torch.float32, device=dev)
-    vs = torch.tensor([inp.v_scale], dtype=torch.float32, device=dev)
+    bt, sl = inp.block_table.to(dev), inp.seqlens.to(dev)
     bs, h_q, hd = inp.q.shape
     h_kv = inp.k_cache.shape[1]
+    q_len, window = (4, 4096) if variant == "xqa" else (1, 0)
+    if variant == "rows":
+        shape = tuple(inp.k_cache.shape[:3])
+        ks = syn.per_row_scales(5, 50, shape, inp.k_scale).to(dev)
+        vs = syn.per_row_scales(5, 51, shape, inp.v_scale).to(dev)
+    else:
+        ks = torch.tensor([inp.k_scale], dtype=torch.float32, device=dev)
+        vs = torch.tensor([inp.v_scale], dtype=torch.float32, device=dev)
+    q = (syn.gqa_block_q(5, bs, q_len, h_q) if variant == "xqa" else inp.q.unsqueeze(1)).to(dev)
+    mask = syn.spec_mask(5, bs, q_len).to(dev) if variant == "xqa" else None
+    sinks = syn.sink_logits(5, h_q).to(dev) if variant == "xqa" else None
     splits = fm.gqa_num_splits(bs, h_kv, bt.shape[1] * 16)
     ws = torch.empty((max(fm.gqa_workspace_bytes(bs, h_q, hd, splits), 256),), dtype=torch.uint8, device=dev)
-    out = torch.empty((bs, h_q, hd), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((bs, h_q), dtype=torch.float32, device=dev)
+    out = torch.empty((bs, q_len, h_q, hd), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((bs, q_len, h_q), dtype=torch.float32, device=dev)
 
     def call(i):
         kc, vc = sets[i % len(sets)]
-        fm.paged_gqa_decode(q, kc, vc, bt, sl, ks, vs, inp.softmax_scale, num_splits=0, out=out, lse=lse,
-                            workspace=ws)
+        if variant == "plain":
+            fm.paged_gqa_decode(q[:, 0], kc, vc, bt, sl, ks, vs, inp.softmax_scale, num_splits=0, out=out[:, 0],
+                                lse=lse[:, 0], workspace=ws)
+        else:
+            fm.paged_gqa_decode_ext(q, kc, vc, bt, sl, ks, vs, inp.softmax_scale, spec_mask=mask, window=window,
+                                    sinks=sinks, num_splits=0, out=out, lse=lse, workspace=ws)
 
     avg, ms = _time_calls(call, steps, warmup, torch.cuda.current_stream(dev))
-    keys = sum(seqlens)
-    nbytes = keys * h_kv * hd * 2 + 2 * bs * h_q * hd * 2 + bs * h_q * 4 + sum((x + 15) // 16 for x in seqlens) * 4
-    flops = 2.0 * keys * h_q * hd * 2
+    # keys a call must read: all of them, or with the window the last W + q_len - 1 of each sequence
+    keys = sum(min(x, window + q_len - 1) if window else x for x in seqlens)
+    nbytes = (keys * h_kv * hd * 2 + 2 * bs * q_len * h_q * hd * 2 + bs * q_len * h_q * 4 +
+              sum((x + 15) // 16 for x in seqlens) * 4)
+    if variant == "rows":
+        nbytes += keys * h_kv * 2 * 4
+    flops = 2.0 * keys * q_len * h_q * hd * 2
     cfg = dict(workload="paged_gqa_decode", bs=bs, h_q=h_q, h_kv=h_kv, head_dim=hd, page=16,
-               seqlens="uniform[1024,16384] seed 5", dot="f16", splits=splits,
-               values="pooled N(0,1) blocks", l2="2 rotating cache copies (~1.1 GB) > L2")
-    return _leg_result("paged GQA decode us/call (bs=32, 32/8 heads, hd 128, ctx U[1024,16384])", avg, ms, nbytes,
-                       0.0, flops, peaks, cfg, 1 if splits == 1 else 2)
+               seqlens="uniform[1024,16384] seed 5", splits=splits, values="pooled N(0,1) blocks",
+               l2="2 rotating cache copies (~1.1 GB) > L2")
+    if variant == "plain":
+        cfg.update(dot="e4m3 operands, Q and P as two E4M3 terms", scales="per tensor")
+        what = "bs=32, 32/8 heads, hd 128, ctx U[1024,16384]"
+    elif variant == "rows":
+        cfg.update(dot="f16", scales="per row [num_blocks, h_kv, 16], base 2^U[-2,2]")
+        what = "bs=32, 32/8 heads, hd 128, ctx U[1024,16384], per-row KV scales"
+    else:
+        cfg.update(dot="f16", scales="per tensor", q_len=q_len, mask="seeded block mask", window=window,
+                   sinks="seeded logits U[-2,6]")
+        what = "bs=32, 32/8 heads, hd 128, ctx U[1024,16384], 4-token speculative block, window 4096, sinks"
+    return _leg_result(f"paged GQA decode us/call ({what})", avg, ms, nbytes, 0.0, flops, peaks, cfg,
+                       1 if splits == 1 else 2)
 
 
 def leg_kvwrite(dev, peaks, steps, warmup):
@@ -615,13 +654,20 @@ def run_leg(name, dev, peaks, steps, warmup):
         return leg_sparse(dev, peaks, steps, warmup, int(name[len("sparse_sq"):]))
     if name == "gqa_bs32":
         return leg_gqa(dev, peaks, steps, warmup)
+    if name == "gqa_bs32_rows":
+        return leg_gqa(dev, peaks, steps, warmup, "rows")
+    if name == "gqa_bs32_xqa":
+        return leg_gqa(dev, peaks, steps, warmup, "xqa")
+    if name == "mla_rows":
+        return leg_mla(dev, peaks, steps, warmup, "fp8", syn.uniform_seqlens(2, 64, 2048, 6144), 2,
+                       "uniform[2048,6144] seed 2", value_pages=96, rows=True)
     if name == "kvwrite":
         return leg_kvwrite(dev, peaks, steps, warmup)
     raise ValueError(name)
 
 
-LEGS = ("mla_bf16", "mla_fixed4096", "mla_long_b32", "mla_long_b48", "mla_long_b64", "mla_long_b128",
-        "sparse_sq2", "sparse_sq16", "sparse_sq16384", "gqa_bs32", "kvwrite")
+LEGS = ("mla_bf16", "mla_fixed4096", "mla_long_b32", "mla_long_b48", "mla_long_b64", "mla_long_b128", "mla_rows",
+        "sparse_sq2", "sparse_sq16", "sparse_sq16384", "gqa_bs32", "gqa_bs32_rows", "gqa_bs32_xqa", "kvwrite")
 
 
 def run_legs(dev, steps, warmup, names=LEGS):
@@ -643,8 +689,9 @@ def run_secondary(args):
     import torch
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    names = {"sparse": f"sparse_sq{args.sq}", "gqa": "gqa_bs32", "kvwrite": "kvwrite",
-             "mla_bf16": "mla_bf16", "mla_fixed4096": "mla_fixed4096", "mla_long": f"mla_long_b{args.b}"}
+    names = {"sparse": f"sparse_sq{args.sq}", "gqa": "gqa_bs32", "gqa_rows": "gqa_bs32_rows",
+             "gqa_xqa": "gqa_bs32_xqa", "kvwrite": "kvwrite", "mla_bf16": "mla_bf16",
+             "mla_fixed4096": "mla_fixed4096", "mla_long": f"mla_long_b{args.b}", "mla_rows": "mla_rows"}
     res = run_leg(names[args.workload], dev, measured_peaks(), args.steps, args.warmup)
     res.update(steps=args.steps, warmup=args.warmup, n_gpus=1, data="synthetic")
     print(json.dumps(res), flush=True)
@@ -739,7 +786,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--dot", choices=["fp8", "bf16"], default="fp8")
-    ap.add_argument("--workload", choices=["mla", "sparse", "gqa", "kvwrite", "mla_bf16", "mla_fixed4096", "mla_long"],
+    ap.add_argument("--workload", choices=["mla", "sparse", "gqa", "gqa_rows", "gqa_xqa", "kvwrite", "mla_bf16",
+                                           "mla_fixed4096", "mla_long", "mla_rows"],
                     default="mla", help="mla = the headline line (which also carries every leg under 'legs'); "
                     "the others print one measurement leg alone")
     ap.add_argument("--sq", type=int, default=2,
