@@ -379,6 +379,8 @@ def paged_gqa_decode_ext(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
         softmax_scale = 1.0 / math.sqrt(hd)
     if max_seqlen is None:
         max_seqlen = block_table.shape[1] * page
+    if window > 0:  # a window bounds the keys any sequence reads (plus one step of alignment)
+        max_seqlen = min(max_seqlen, window + q_len - 1 + 128)
     splits = gqa_num_splits(bs, h_kv, max_seqlen, num_splits)
     if out is None:
         out = torch.empty((bs, q_len, h_q, hd), dtype=torch.bfloat16, device=q.device)

@@ -10,27 +10,33 @@
 // GB300 design (swap-AB, one CTA per (sequence, KV head, split)):
 //   * 128 tokens (8 pages of 16) per step; each page's K and V tile
 //     [16 tokens x 128 B] arrives by one TMA each (128-byte swizzle) into a
-//     ring of four raw stages, so that several steps are in flight from HBM.
-//   * 16-bit dots: four converter warps turn each step into f16 (exact):
-//     token r's K row goes straight into TMEM lane r, the A operand of
-//     Q.K^T, and its V row into one of two f16 V slots in shared memory;
-//     Q (the head group, <= 16 heads) is f16 with a per-head power-of-two scale.
-//   * S^T = K Q^T: M = 128 tokens, N = 16, K = 128 (8 f16 MMAs, A from
-//     TMEM); softmax across TMEM lanes (per-head max by shuffles + a 4-warp
-//     exchange; each thread keeps partial sums), P^T (f16) to shared memory,
-//     then O^T = V^T P^T with V^T read MN-major from the f16 V slot.  S and P
-//     are double-buffered; a converged warp issues the MMAs (one elected lane).
+//     ring of three raw stages.
+//   * The tensor core reads the raw E4M3 tiles: S^T = K [Q_hi | Q_lo]^T
+//     (M = 128 tokens, N = 32, the K-major K tile as A: 4 MMAs) and
+//     O^T = V^T [P_hi | P_lo]^T (the V tile read MN-major: 4 MMAs).  Q and P
+//     enter as two E4M3 terms, hi = E4M3(x) and lo = E4M3(x - hi), about 8
+//     significant bits together, side by side in one N = 32 operand: the
+//     softmax adds a column's two S values, the epilogue its two O values.
+//     Q carries a per-column power-of-two scale; P is stored x64 with the
+//     lazy reference raised only past 2.75 (64 * 2^2.75 < 448).
+//   * Softmax across TMEM lanes (one thread per token: per-column max by
+//     shuffles + a 4-warp exchange; each thread keeps partial sums).  Tokens
+//     past the end are masked by select, and their V rows zeroed in shared
+//     memory before P.V reads the tile.
+//   * ~113 KB of shared memory and 128 TMEM columns per CTA: two CTAs share
+//     an SM, so one's fill and drain overlap the other's steady state.
 //   * Split-KV over the token dimension with a combine kernel; for small
 //     grids the split count follows the FA2-style "waves" rule, the smallest
 //     count within 85% of the best wave efficiency (InfiniCore page,
 //     Summary: the "auto" heuristic); a grid that already fills the GPU is
 //     still cut into about six CTAs per SM so unequal contexts balance.
 //   * Per-row scales [num_blocks, h_kv, 16] (InfiniCore page, Summary): each
-//     page's 16 K and 16 V scales arrive by bulk copy with its tiles; V rows
-//     are dequantised to f16 by the converter warps, K rows stay exact and
-//     their scale multiplies the token's scores in fp32 in the softmax.
+//     page's 16 K and 16 V scales arrive by bulk copy with its tiles; a
+//     token's K scale multiplies its scores in fp32, and its V scale enters
+//     the weights: u = score + log2 sigma_v, P' = 2^(u - m) carries sigma_v
+//     into P.V on the raw codes, and the row sums take P' / sigma_v.
 //   * XQA options (FlashInfer "add xqa fp8 mha and fp8 kv cache", launcher
-//     arguments): the N = 16 MMA columns hold (query token, head) pairs of a
+//     arguments): the 16 MMA columns hold (query token, head) pairs of a
 //     speculative block of q_len tokens (the last q_len cache positions),
 //     masked per column by the block mask (or causally) and a sliding window
 //     (steps wholly before every token's window are not loaded); sink logits
@@ -58,18 +64,8 @@ constexpr int kPage = 16;
 constexpr int kTok = 128;               // tokens per step (MMA M)
 constexpr int kPagesPerStep = kTok / kPage;
 constexpr int kN = 16;                  // head group, padded (MMA N)
-constexpr int kThreads = 384;           // producer, MMA, 2 idle, 4 softmax, 4 converter warps
-constexpr int kRawStages = 4;           // E4M3 K and V of a step, in flight from HBM
-constexpr int kV16Slots = 2;            // f16 V of a step, from conversion until its P.V
 constexpr int kRawTile = kTok * kHd;    // 16 KB of E4M3 per operand per step
-constexpr int kCvtAtom = kTok * 128;    // one 64-dim f16 atom (16 KB)
 constexpr int kOffRawK = 0, kOffRawV = kRawTile, kRawStageBytes = 2 * kRawTile;   // 32 KB
-constexpr int kV16Bytes = 2 * kCvtAtom;                                            // 32 KB
-constexpr int kQBytes = 2 * kN * 128;
-constexpr int kPBytes = 2 * kN * 128;   // one P^T buffer (two are kept)
-constexpr float kTau = 8.0f;
-// TMEM: S (two buffers of 16 columns), O (16), K of a step as f16 (two slots of 64)
-constexpr uint32_t kTmemCols = 256, kTS = 0, kTO = 32, kTK = 64;
 
 struct Params {
   const uint16_t* q;           // bf16 [bs, q_len, h_q, 128]
@@ -90,50 +86,12 @@ struct Params {
   float softmax_scale;
 };
 
-struct Smem {
-  float row_scale[kRawStages][2][kTok];  // per-row scales of a raw stage's K and V rows (scale_rows)
-  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
-  uint64_t cvt_ready[kV16Slots], k16_empty[kV16Slots], v16_empty[kV16Slots];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];  // by step parity
-  uint64_t q_full, final_mma, xchg;
-  uint32_t tmem_base, abort_flag;
-  float qs[kN];
-  uint16_t vis_block[kN];  // per query token: bit c = key c of the speculative block visible
-  // per-row K scales of a step's token rows, from the converter to the softmax (by step % 4; a slot
-  // is rewritten four steps later, after the softmax read it: the converter's step i + 4 follows
-  // Q.K^T of step i + 2, which follows the softmax's read of step i)
-  float kscale_s[4][kTok];
-  uint64_t ks_ready[4];
-  float red[2][4][kN];   // per-warp partial maxima, double-buffered by step parity
-  float red2[4][kN];
-};
-
-constexpr size_t kSmemBytes =
-    kRawStages * kRawStageBytes + kV16Slots * kV16Bytes + kQBytes + 2 * kPBytes + sizeof(Smem) + 1024;
-
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
   const bool ok = wait_bounded(bar, parity, abort_flag, &g_status_gqa);
   return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
-
-// Smallest e with amax <= 2^14 * 2^e: keeps f16 products of Q and E4M3 values far from overflow.
-__device__ __forceinline__ int pow2_exp_f16(float amax) {
-  const uint32_t bits = __float_as_uint(amax);
-  const int expo = static_cast<int>((bits >> 23) & 0xFFu);
-  if (expo == 0) return 0;
-  const int e = (expo - 127) + ((bits & 0x7FFFFFu) ? 1 : 0) - 14;
-  return max(min(e, 100), -100);
-}
-
-__device__ __forceinline__ uint32_t f16x2_of_e4m3x2(uint32_t two_bytes) { return e4m3x2_to_f16x2(two_bytes); }
-
-// Two E4M3 codes times a row's dequantisation scale, as f16 (the dequantised values, rounded once).
-__device__ __forceinline__ uint32_t f16x2_scaled(uint32_t two_bytes, float sc) {
-  const uint32_t h = e4m3x2_to_f16x2(two_bytes);
-  return pack_f16x2(f16_lo(h) * sc, f16_hi(h) * sc);
-}
 
 // The end of one output row: key weights summed to l against reference m (log2
 // units of the scaled scores), an optional sink logit `sink` (natural units,
@@ -159,512 +117,9 @@ __device__ __forceinline__ void finish_row(float m, float l, float sink, float v
   *lse = (mm + lg2_approx(den)) * kLn2;
 }
 
-// kG: the softmax handles MMA columns [0, kG) of the N = 16 (kG >= q_len * group).
-// kMode bit 0: per-row scales; bit 1: the XQA options (q_len > 1, a mask, a window or sinks).
-template <int kG, int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
-    gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const Params prm) {
-  constexpr bool kRows = (kMode & 1) != 0, kExt = (kMode & 2) != 0;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  uint8_t* v16 = smem + kRawStages * kRawStageBytes;    // f16 V slots
-  uint8_t* q_tile = v16 + kV16Slots * kV16Bytes;
-  uint8_t* p_tile = q_tile + kQBytes;
-  Smem* sm = reinterpret_cast<Smem*>(p_tile + 2 * kPBytes);
-  volatile uint32_t* abort_flag = &sm->abort_flag;
-
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  const int split = blockIdx.x % prm.splits;
-  const int seq = blockIdx.x / prm.splits;      // (b, kv head)
-  const int b = seq / prm.h_kv;
-  const int kvh = seq % prm.h_kv;
-
-  int s_k = prm.seqlens[b];
-  int n_pages = s_k > 0 ? (s_k + kPage - 1) / kPage : 0;
-  if (s_k < 0 || n_pages > prm.max_blocks) {
-    if (threadIdx.x == 0) atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_SEQLEN);
-    s_k = 0;
-    n_pages = 0;
-  }
-  // The query block's tokens are the last q_len cache positions; with a
-  // sliding window no token sees a key before k_lo, so steps wholly before it
-  // are left out of the split partition.
-  const int start = s_k - prm.q_len;  // position of the block's first token
-  const int k_lo = (kExt && prm.window > 0) ? max(0, start - prm.window + 1) : 0;
-  const int n_steps_total = (n_pages + kPagesPerStep - 1) / kPagesPerStep;
-  const int step_lo = min(k_lo / kTok, n_steps_total);
-  const int n_steps_all = n_steps_total - step_lo;
-  const int st0 = step_lo + static_cast<int>((static_cast<long long>(split) * n_steps_all) / prm.splits);
-  const int st1 = step_lo + static_cast<int>((static_cast<long long>(split + 1) * n_steps_all) / prm.splits);
-  const int nsteps = st1 - st0;
-  const int ncols = prm.q_len * prm.group;  // MMA columns that hold (token, head) pairs
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&sm->raw_full[s], 1);
-      mbar_init(&sm->raw_empty[s], 4);  // one arrival per converter warp
-    }
-    for (int s = 0; s < kV16Slots; ++s) {
-      mbar_init(&sm->cvt_ready[s], 4);
-      mbar_init(&sm->k16_empty[s], 1);
-      mbar_init(&sm->v16_empty[s], 1);
-    }
-    for (int bf = 0; bf < 2; ++bf) {
-      mbar_init(&sm->s_full[bf], 1);
-      mbar_init(&sm->s_free[bf], 4);
-      mbar_init(&sm->p_full[bf], 4);
-      mbar_init(&sm->pv_done[bf], 1);
-    }
-    mbar_init(&sm->q_full, 4);
-    for (int k = 0; k < 4; ++k) mbar_init(&sm->ks_ready[k], 4);  // one arrival per converter warp
-    mbar_init(&sm->final_mma, 1);
-    mbar_init(&sm->xchg, 4);
-    sm->abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&sm->tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  griddep_wait();  // inputs may come from the previous kernel in the stream
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  griddep_launch_dependents();
-  const uint32_t tmem = sm->tmem_base;
-
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer ----
-    // lanes 0..7 fetch a step's block-table entries at once, one step ahead
-    // (the load is in flight while the previous step's loads issue); lane 0
-    // issues the loads
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-    }
-    const int32_t* bt_row = prm.block_table + static_cast<size_t>(b) * prm.max_blocks;
-    auto fetch = [&](int step) {
-      const int p0 = (st0 + step) * kPagesPerStep;
-      return (step < nsteps && lane < min(kPagesPerStep, n_pages - p0)) ? __ldg(bt_row + p0 + lane) : 0;
-    };
-    int next = fetch(0);
-    int i = 0;
-    for (; i < nsteps; ++i) {
-      const int st = i % kRawStages, use = i / kRawStages;
-      const int p0 = (st0 + i) * kPagesPerStep;
-      const int np = min(kPagesPerStep, n_pages - p0);
-      int mine = next;
-      next = fetch(i + 1);
-      if (lane < np && (mine < 0 || mine >= prm.num_blocks)) {
-        atomicOr(&g_status_gqa, FP8MLA_DEV_BAD_PAGE);
-        mine = 0;
-      }
-      int rows[kPagesPerStep];
-#pragma unroll
-      for (int p = 0; p < kPagesPerStep; ++p) rows[p] = (__shfl_sync(0xffffffffu, mine, p) * prm.h_kv + kvh) * kPage;
-      bool ok = true;
-      if (lane == 0) {
-        ok = use == 0 || wait_bounded(&sm->raw_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa);
-        if (ok) {
-          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd + (kRows ? 2u * np * kPage * 4u : 0u));
-          uint8_t* sb = smem + st * kRawStageBytes;
-#pragma unroll
-          for (int p = 0; p < kPagesPerStep; ++p) {
-            if (p >= np) break;
-            tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->raw_full[st], 0, rows[p], 0);
-            tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->raw_full[st], 0, rows[p], 0);
-            if constexpr (kRows) {  // the page's 16 row scales of K and of V (rows are the scales' index too)
-              bulk_load(&sm->row_scale[st][0][p * kPage], prm.k_scale + rows[p], kPage * 4u, &sm->raw_full[st]);
-              bulk_load(&sm->row_scale[st][1][p * kPage], prm.v_scale + rows[p], kPage * 4u, &sm->raw_full[st]);
-            }
-          }
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-    }
-    if (lane == 0)
-      for (int j = max(0, i - kRawStages); j < i; ++j)
-        wait_bounded(&sm->raw_full[j % kRawStages], (j / kRawStages) & 1, nullptr, &g_status_gqa);
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------- MMA issuer ----
-    // The whole warp runs the loop and one elected lane issues.  Q.K^T reads
-    // the step's K from TMEM (f16, written there by the converter warps);
-    // P.V reads V^T from the step's f16 slot in shared memory.  S and P are
-    // double-buffered, so Q.K^T of step i runs while the softmax warps work
-    // on step i - 1.
-    {
-      constexpr uint32_t idesc_qk = make_idesc(0, 0, 0, 0, kN, 128);  // f16: K (TMEM) x Q (K-major)
-      constexpr uint32_t idesc_pv = make_idesc(0, 0, 1, 0, kN, 128);  // f16: V^T (MN-major) x P^T (K-major)
-      const bool leader = elect_one();
-      const uint32_t qb = smem_u32(q_tile);
-      bool ok = warp_wait(&sm->q_full, 0, abort_flag);
-      auto issue_pv = [&](int j) -> bool {
-        const int bf = j & 1, vs = j % kV16Slots;
-        if (!warp_wait(&sm->p_full[bf], (j >> 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(v16 + vs * kV16Bytes);
-        const uint32_t pb = smem_u32(p_tile + bf * kPBytes);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ss_if(leader, tmem + kTO, make_sdesc(vb + kk * 2048, kCvtAtom, 1024, SWIZZLE_128B),
-                        make_sdesc(pb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_pv,
-                        (j == 0 && kk == 0) ? 0u : 1u);
-        tc_commit_if(leader, &sm->pv_done[bf]);
-        tc_commit_if(leader, &sm->v16_empty[vs]);
-        return true;
-      };
-      for (int i = 0; ok && i < nsteps; ++i) {
-        const int ks = i % kV16Slots, bf = i & 1;
-        if (!warp_wait(&sm->cvt_ready[ks], (i / kV16Slots) & 1, abort_flag) ||
-            (i >= 2 && !warp_wait(&sm->s_free[bf], ((i - 2) >> 1) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16_ts_if(leader, tmem + kTS + bf * kN, tmem + kTK + ks * 64 + kk * 8,
-                        make_sdesc(qb + (kk >> 2) * (kN * 128) + (kk & 3) * 32, 16, 1024, SWIZZLE_128B), idesc_qk,
-                        kk > 0 ? 1u : 0u);
-        tc_commit_if(leader, &sm->s_full[bf]);
-        tc_commit_if(leader, &sm->k16_empty[ks]);
-        if (i > 0 && !issue_pv(i - 1)) ok = false;
-      }
-      if (ok && nsteps > 0) issue_pv(nsteps - 1);
-      if (leader) tc_commit(&sm->final_mma);
-      __syncwarp();
-      warp_wait(&sm->final_mma, 0, nullptr);
-    }
-  } else if (warp >= 8) {
-    // ------------------------- K / V conversion to f16 (one token row each) ----
-    // Token r's K row goes to TMEM lane r (the A operand of Q.K^T), its V row
-    // to the step's f16 V slot (128-byte swizzle, read MN-major by P.V).
-    const int r = threadIdx.x - 256;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-    for (int i = 0; i < nsteps; ++i) {
-      const int st = i % kRawStages, use = i / kRawStages, vs = i % kV16Slots;
-      const bool live = (st0 + i) * kTok + r < s_k;
-      if (!warp_wait(&sm->raw_full[st], use & 1, abort_flag)) break;
-      const uint8_t* sb = smem + st * kRawStageBytes;
-      const int sw = r & 7;
-      uint4 kraw[8], vraw[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        kraw[c] = live ? *reinterpret_cast<const uint4*>(sb + kOffRawK + r * 128 + ((c ^ sw) << 4))
-                       : make_uint4(0, 0, 0, 0);
-        vraw[c] = live ? *reinterpret_cast<const uint4*>(sb + kOffRawV + r * 128 + ((c ^ sw) << 4))
-                       : make_uint4(0, 0, 0, 0);
-      }
-      // per-row scales: V rows are dequantised here; K rows stay exact and their scale goes to the
-      // softmax, which applies it to the token's scores in fp32 (per-tensor scales come later)
-      float vsc = 1.f, ksc = 1.f;
-      if constexpr (kRows) {
-        vsc = live ? sm->row_scale[st][1][r] : 1.f;
-        ksc = live ? sm->row_scale[st][0][r] : 1.f;
-      }
-      auto cvt = [&](uint32_t two, float sc) {
-        if constexpr (kRows) return f16x2_scaled(two, sc);
-        return f16x2_of_e4m3x2(two);
-      };
-      warp_arrive(&sm->raw_empty[st]);  // the raw stage may be refilled
-      // the K slot and the V slot of this step were last read two steps ago
-      if (i >= kV16Slots && (!warp_wait(&sm->k16_empty[vs], ((i - kV16Slots) / kV16Slots) & 1, abort_flag) ||
-                             !warp_wait(&sm->v16_empty[vs], ((i - kV16Slots) / kV16Slots) & 1, abort_flag)))
-        break;
-      if constexpr (kRows) {  // (the slot's step i - 4 was read: Q.K^T of step i - 2 has completed)
-        sm->kscale_s[i & 3][r] = ksc;
-        warp_arrive(&sm->ks_ready[i & 3]);
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // K: dims [64 half, 64 half + 64) -> 32 columns of f16 pairs
-        uint32_t kc[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 x = kraw[4 * half + c];
-          kc[8 * c + 0] = f16x2_of_e4m3x2(x.x & 0xFFFFu);
-          kc[8 * c + 1] = f16x2_of_e4m3x2(x.x >> 16);
-          kc[8 * c + 2] = f16x2_of_e4m3x2(x.y & 0xFFFFu);
-          kc[8 * c + 3] = f16x2_of_e4m3x2(x.y >> 16);
-          kc[8 * c + 4] = f16x2_of_e4m3x2(x.z & 0xFFFFu);
-          kc[8 * c + 5] = f16x2_of_e4m3x2(x.z >> 16);
-          kc[8 * c + 6] = f16x2_of_e4m3x2(x.w & 0xFFFFu);
-          kc[8 * c + 7] = f16x2_of_e4m3x2(x.w >> 16);
-        }
-        tmem_st32(lane_base + kTK + vs * 64 + half * 32, kc);
-      }
-      uint8_t* vslot = v16 + vs * kV16Bytes;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {   // V: 16 E4M3 -> 16 f16 (two 16-byte chunks)
-        const uint4 x = vraw[c];
-        const uint4 vo = make_uint4(cvt(x.x & 0xFFFFu, vsc), cvt(x.x >> 16, vsc), cvt(x.y & 0xFFFFu, vsc),
-                                    cvt(x.y >> 16, vsc));
-        const uint4 vo2 = make_uint4(cvt(x.z & 0xFFFFu, vsc), cvt(x.z >> 16, vsc), cvt(x.w & 0xFFFFu, vsc),
-                                     cvt(x.w >> 16, vsc));
-        // dims [16 c, 16 c + 16): f16 atom c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1
-        uint8_t* dv = vslot + (c / 4) * kCvtAtom + r * 128;
-        *reinterpret_cast<uint4*>(dv + (((2 * (c % 4)) ^ sw) << 4)) = vo;
-        *reinterpret_cast<uint4*>(dv + (((2 * (c % 4) + 1) ^ sw) << 4)) = vo2;
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      warp_arrive(&sm->cvt_ready[vs]);  // one arrival per converting warp
-    }
-  } else if (warp >= 4) {
-    // ------------------------------- Q prep, softmax, epilogue ----
-    const int r = threadIdx.x - 128;   // token row of a step / TMEM lane / output dim
-    const int w = warp - 4;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(w * 32) << 16);
-    // exchange point of the 128 softmax threads: bounded, abort-aware mbarrier waits
-    uint32_t xphase = 0;
-    auto xsync = [&]() -> bool {
-      warp_arrive(&sm->xchg);
-      const bool ok = warp_wait(&sm->xchg, xphase & 1, abort_flag);
-      ++xphase;
-      return ok;
-    };
-    // per-row scales were applied by the converter warps
-    const float k_scale = kRows ? 1.f : *prm.k_scale, v_scale = kRows ? 1.f : *prm.v_scale;
-    // column n of the MMA: query token n / group, head kvh * group + n % group
-    auto q_row = [&](int n) -> const uint16_t* {
-      return prm.q + ((static_cast<size_t>(b) * prm.q_len + n / prm.group) * prm.h_q + kvh * prm.group +
-                      n % prm.group) * kHd;
-    };
-    if (kExt && r < prm.q_len) {  // which keys of the speculative block token r sees: the mask row, or c <= r
-      uint32_t bits = 0;
-      if (prm.spec_mask != nullptr) {
-        const uint8_t* row = prm.spec_mask + (static_cast<size_t>(b) * prm.q_len + r) * prm.q_len;
-        for (int c = 0; c < prm.q_len; ++c)
-          if (__ldg(row + c)) bits |= 1u << c;
-      } else {
-        bits = (2u << r) - 1u;
-      }
-      sm->vis_block[r] = static_cast<uint16_t>(bits);
-    }
-    {
-      // Q tile: thread (column qh, eighth qj) converts dims [16 qj, 16 qj + 16) to f16 / qs
-      const int qh = r / 8, qj = r % 8;
-      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (qh < ncols) {
-        v0 = __ldg(reinterpret_cast<const uint4*>(q_row(qh) + qj * 16));
-        v1 = __ldg(reinterpret_cast<const uint4*>(q_row(qh) + qj * 16 + 8));
-      }
-      float amax = 0.f;
-      const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(wd[k])), fabsf(bf16_hi(wd[k]))));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-      const int e = pow2_exp_f16(amax);
-      const float inv = exp2i(-e);
-      if (qj == 0) sm->qs[qh] = exp2i(e);
-      uint32_t h16[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) h16[k] = pack_f16x2(bf16_lo(wd[k]) * inv, bf16_hi(wd[k]) * inv);
-      // dims [16 qj, 16 qj + 16) = atom qj / 4, chunks 2 (qj % 4), 2 (qj % 4) + 1
-      uint8_t* row = q_tile + (qj / 4) * (kN * 128) + (qh / 8) * 1024 + (qh % 8) * 128;
-      *reinterpret_cast<uint4*>(row + (((2 * (qj % 4)) ^ (qh % 8)) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-      *reinterpret_cast<uint4*>(row + (((2 * (qj % 4) + 1) ^ (qh % 8)) << 4)) =
-          make_uint4(h16[4], h16[5], h16[6], h16[7]);
-      fence_proxy_async_smem();
-      warp_arrive(&sm->q_full);
-    }
-    for (int i = r; i < 2 * kPBytes / 16; i += 128) reinterpret_cast<uint4*>(p_tile)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-    bool ok = xsync();  // qs[], the block's visibility bits and the zeroed P tile complete
-    float c_h[kG], m_h[kG], l_h[kG];
-#pragma unroll
-    for (int h = 0; h < kG; ++h) {
-      c_h[h] = prm.softmax_scale * kLog2e * sm->qs[h] * k_scale;
-      m_h[h] = kNegInf;
-      l_h[h] = 0.f;
-    }
-    const uint32_t grp_bits = (1u << prm.group) - 1u;
-    const uint32_t pad_cols = ncols >= 32 ? 0u : (0xFFFFFFFFu << ncols);  // padding columns: no output
-    const bool plain = !kExt || (prm.q_len == 1 && prm.window == 0);
-    for (int i = 0; ok && i < nsteps; ++i) {
-      const int bf = i & 1;
-      const int tok = (st0 + i) * kTok + r;
-      const bool live = tok < s_k;
-      // ---- softmax over this step's tokens ----
-      if (!warp_wait(&sm->s_full[bf], (i >> 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t s[kN];
-      tmem_ld16(lane_base + kTS + bf * kN, s);
-      float kro = 1.f;  // this token's K row scale
-      if constexpr (kRows) {
-        if (!warp_wait(&sm->ks_ready[i & 3], (i >> 2) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        kro = sm->kscale_s[i & 3][r];
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      warp_arrive(&sm->s_free[bf]);
-      // columns that see this thread's key: per query token ti, keys before the block always,
-      // keys inside it by the token's bits, and (window W) only if ti - c_blk < W (the token's
-      // position less than W past the key)
-      uint32_t colvis = pad_cols;
-      if (!kExt || plain) {  // one query token, no window: every column sees every live key
-        colvis = live ? 0xFFFFFFFFu : pad_cols;
-      } else if (live) {
-        const int c_blk = tok - start;
-        for (int ti = 0; ti < prm.q_len; ++ti) {
-          const bool vis = (c_blk < 0 || ((sm->vis_block[ti] >> c_blk) & 1u)) &&
-                           (prm.window == 0 || ti - c_blk < prm.window);
-          if (vis) colvis |= grp_bits << (ti * prm.group);
-        }
-      }
-      float v[kG];
-#pragma unroll
-      for (int h = 0; h < kG; ++h) v[h] = ((colvis >> h) & 1u) ? __uint_as_float(s[h]) * kro * c_h[h] : kNegInf;
-#pragma unroll
-      for (int h = 0; h < kG; ++h) {
-        float x = v[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (lane == 0) sm->red[i & 1][w][h] = x;
-      }
-      if (!xsync()) {
-        ok = false;
-        break;
-      }
-      float alpha[kG];
-      bool any_rescale = false;
-#pragma unroll
-      for (int h = 0; h < kG; ++h) {
-        const float* rm = &sm->red[i & 1][0][0];
-        const float mx = fmaxf(fmaxf(rm[h], rm[kN + h]), fmaxf(rm[2 * kN + h], rm[3 * kN + h]));
-        alpha[h] = 1.f;
-        if (mx > m_h[h] + kTau) {
-          alpha[h] = ex2_approx(m_h[h] - mx);
-          any_rescale |= (i > 0);
-          m_h[h] = mx;
-        }
-      }
-      uint32_t ph[kG / 2];
-#pragma unroll
-      for (int h = 0; h < kG; h += 2) {
-        const float p0 = ex2_approx(v[h] - (m_h[h] == kNegInf ? 0.f : m_h[h]));
-        const float p1 = ex2_approx(v[h + 1] - (m_h[h + 1] == kNegInf ? 0.f : m_h[h + 1]));
-        l_h[h] = l_h[h] * alpha[h] + p0;
-        l_h[h + 1] = l_h[h + 1] * alpha[h + 1] + p1;
-        ph[h / 2] = pack_f16x2(p0, p1);
-      }
-      // O is rescaled only after the previous step's P.V; the P buffer is
-      // rewritten only after the P.V that read it two steps ago
-      if (any_rescale) {
-        if (!warp_wait(&sm->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-      } else if (i >= 2 && !warp_wait(&sm->pv_done[bf], ((i - 2) >> 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (any_rescale) {
-        uint32_t o[kN];
-        tmem_ld16(lane_base + kTO, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int h = 0; h < kG; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-        tmem_st16(lane_base + kTO, o);
-        tmem_st_wait();
-      }
-      // P^T (K-major, f16): row h, token r -> atom r / 64, chunk (r % 64) / 8, element r % 8
-      {
-        const int a = r / 64, ch = (r % 64) / 8, el = r % 8;
-#pragma unroll
-        for (int h = 0; h < kG; ++h) {
-          const uint16_t val = static_cast<uint16_t>((h & 1) ? (ph[h / 2] >> 16) : (ph[h / 2] & 0xFFFFu));
-          *reinterpret_cast<uint16_t*>(p_tile + bf * kPBytes + a * (kN * 128) + (h / 8) * 1024 + (h % 8) * 128 +
-                                       ((ch ^ (h % 8)) << 4) + el * 2) = val;
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      warp_arrive(&sm->p_full[bf]);
-    }
-
-    const bool whole = prm.splits == 1;
-    const size_t slot = static_cast<size_t>(seq) * prm.splits + split;
-    if (ok && nsteps > 0 && warp_wait(&sm->pv_done[(nsteps - 1) & 1], ((nsteps - 1) >> 1) & 1, abort_flag)) {
-      tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < kG; ++h) {
-        float x = l_h[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) sm->red2[w][h] = x;
-      }
-      ok = xsync();
-      uint32_t o[kN];
-      tmem_ld16(lane_base + kTO, o);
-      tmem_ld_wait();
-#pragma unroll
-      for (int h = 0; h < kG; ++h) {
-        if (h >= ncols) break;
-        const float lsum = (sm->red2[0][h] + sm->red2[1][h]) + (sm->red2[2][h] + sm->red2[3][h]);
-        const int hq = kvh * prm.group + h % prm.group;
-        const size_t orow = (static_cast<size_t>(b) * prm.q_len + h / prm.group) * prm.h_q + hq;
-        if (whole) {
-          float f, lse_v;
-          finish_row(m_h[h], lsum, (kExt && prm.sinks) ? prm.sinks[hq] : kNegInf, v_scale, &f, &lse_v);
-          prm.out[orow * kHd + r] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[h]) * f, 0.f));
-          if (r == 0) prm.lse[orow] = lse_v;
-        } else {
-          prm.ws_o[(slot * kN + h) * kHd + r] = __uint_as_float(o[h]) * v_scale;
-          if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(lsum > 0.f ? m_h[h] : kNegInf, lsum);
-        }
-      }
-    } else if (ok && nsteps == 0) {
-      for (int h = 0; h < ncols; ++h) {
-        const int hq = kvh * prm.group + h % prm.group;
-        const size_t orow = (static_cast<size_t>(b) * prm.q_len + h / prm.group) * prm.h_q + hq;
-        if (whole) {  // no key: out 0, lse the sink's logit (-inf without one)
-          prm.out[orow * kHd + r] = 0;
-          if (r == 0) prm.lse[orow] = (kExt && prm.sinks) ? prm.sinks[hq] : kNegInf;
-        } else {
-          prm.ws_o[(slot * kN + h) * kHd + r] = 0.f;
-          if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(kNegInf, 0.f);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
 // ------------------------------------------------------------------------
-// Plain decode (one query token, per-tensor scales) with E4M3 operands read
-// straight from the TMA tiles.  Q and P each enter the tensor core as two
-// E4M3 terms, hi = E4M3(x) and lo = E4M3(x - hi) (together ~8 significant
-// bits, as many as bf16), side by side in one N = 32 operand: rows 0..15 hi,
-// rows 16..31 lo.  A step is then 4 MMAs for S^T = K [Q_hi | Q_lo]^T (K-major
-// K tile as A) and 4 for O^T = V^T [P_hi | P_lo]^T (the V tile read MN-major),
-// with no conversion warps; the softmax adds the two S columns of a head and
-// the epilogue the two O columns.  With no f16 buffers the CTA needs ~110 KB
-// of shared memory and 128 TMEM columns, so two CTAs share an SM and one's
-// pipeline fill and drain overlap the other's steady state.  The dead rows
-// (past the sequence end) of a step's V tile are zeroed by the softmax thread
-// that owns the token before P.V reads them, so stale bytes never meet a zero
-// weight in the MMA.
+// The decode kernel: E4M3 operands straight from the TMA tiles, Q and P as two
+// E4M3 terms (see the file comment).
 namespace x2 {
 constexpr int kThreads = 192;          // warp 0 producer, warp 1 MMA, warps 2-5 softmax and epilogue
 constexpr int kStages = 3;             // raw K and V steps in flight (two CTAs per SM: six)
@@ -676,12 +131,14 @@ constexpr float kTau = 2.75f;          // a raised reference keeps 64 p <= 64 * 
 constexpr uint32_t kTmemCols = 128, kTS = 0, kTO = 64;
 
 struct Smem {
+  float row_scale[kStages][2][kTok];  // per-row scales of a stage's K and V rows (scale_rows)
   uint64_t raw_full[kStages], raw_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];  // by step parity
   uint64_t q_full, final_mma, xchg;
   uint32_t tmem_base, abort_flag;
   float qs[kN];
-  float red[2][4][kN];  // per-warp partial maxima, double-buffered by step parity
+  uint16_t vis_block[kN];  // per query token: bit c = key c of the speculative block visible
+  float red[2][4][kN];     // per-warp partial maxima, double-buffered by step parity
   float red2[4][kN];
 };
 
@@ -705,10 +162,13 @@ __device__ __forceinline__ void split_e4m3x4(float a, float b, float c, float d,
 }
 }  // namespace x2
 
-template <int kG>
+// kG: the softmax handles MMA columns [0, kG) of the N = 16 (kG >= q_len * group).
+// kMode bit 0: per-row scales; bit 1: the XQA options (q_len > 1, a mask, a window or sinks).
+template <int kG, int kMode>
 __global__ void __launch_bounds__(x2::kThreads, 2)
     gqa_x2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const Params prm) {
+  constexpr bool kRows = (kMode & 1) != 0, kExt = (kMode & 2) != 0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -731,10 +191,18 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
     s_k = 0;
     n_pages = 0;
   }
-  const int n_steps_all = (n_pages + kPagesPerStep - 1) / kPagesPerStep;
-  const int st0 = static_cast<int>((static_cast<long long>(split) * n_steps_all) / prm.splits);
-  const int st1 = static_cast<int>((static_cast<long long>(split + 1) * n_steps_all) / prm.splits);
+  // The query block's tokens are the last q_len cache positions; with a
+  // sliding window no token sees a key before k_lo, so steps wholly before it
+  // are left out of the split partition.
+  const int start = s_k - prm.q_len;  // position of the block's first token
+  const int k_lo = (kExt && prm.window > 0) ? max(0, start - prm.window + 1) : 0;
+  const int n_steps_total = (n_pages + kPagesPerStep - 1) / kPagesPerStep;
+  const int step_lo = min(k_lo / kTok, n_steps_total);
+  const int n_steps_all = n_steps_total - step_lo;
+  const int st0 = step_lo + static_cast<int>((static_cast<long long>(split) * n_steps_all) / prm.splits);
+  const int st1 = step_lo + static_cast<int>((static_cast<long long>(split + 1) * n_steps_all) / prm.splits);
   const int nsteps = st1 - st0;
+  const int ncols = prm.q_len * prm.group;  // MMA columns that hold (token, head) pairs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < x2::kStages; ++s) {
@@ -795,13 +263,17 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       if (lane == 0) {
         ok = use == 0 || wait_bounded(&sm->raw_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa);
         if (ok) {
-          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd);
+          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd + (kRows ? 2u * np * kPage * 4u : 0u));
           uint8_t* sb = smem + st * kRawStageBytes;
 #pragma unroll
           for (int p = 0; p < kPagesPerStep; ++p) {
             if (p >= np) break;
             tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->raw_full[st], 0, rows[p], 0);
             tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->raw_full[st], 0, rows[p], 0);
+            if constexpr (kRows) {  // the page's 16 row scales of K and of V (rows are the scales' index too)
+              bulk_load(&sm->row_scale[st][0][p * kPage], prm.k_scale + rows[p], kPage * 4u, &sm->raw_full[st]);
+              bulk_load(&sm->row_scale[st][1][p * kPage], prm.v_scale + rows[p], kPage * 4u, &sm->raw_full[st]);
+            }
           }
         }
       }
@@ -866,13 +338,30 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       ++xphase;
       return ok;
     };
-    const float k_scale = *prm.k_scale, v_scale = *prm.v_scale;
+    // per-row scales enter per token (K on its scores, V through its weights)
+    const float k_scale = kRows ? 1.f : *prm.k_scale, v_scale = kRows ? 1.f : *prm.v_scale;
+    // column n of the MMA: query token n / group, head kvh * group + n % group
+    auto q_row = [&](int n) -> const uint16_t* {
+      return prm.q + ((static_cast<size_t>(b) * prm.q_len + n / prm.group) * prm.h_q + kvh * prm.group +
+                      n % prm.group) * kHd;
+    };
+    if (kExt && r < prm.q_len) {  // which keys of the speculative block token r sees: the mask row, or c <= r
+      uint32_t bits = 0;
+      if (prm.spec_mask != nullptr) {
+        const uint8_t* row = prm.spec_mask + (static_cast<size_t>(b) * prm.q_len + r) * prm.q_len;
+        for (int c = 0; c < prm.q_len; ++c)
+          if (__ldg(row + c)) bits |= 1u << c;
+      } else {
+        bits = (2u << r) - 1u;
+      }
+      sm->vis_block[r] = static_cast<uint16_t>(bits);
+    }
     {
-      // [Q_hi ; Q_lo]: thread (head qh, eighth qj) splits dims [16 qj, 16 qj + 16) of q / qs
+      // [Q_hi ; Q_lo]: thread (column qh, eighth qj) splits dims [16 qj, 16 qj + 16) of q / qs
       const int qh = r / 8, qj = r % 8;
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (qh < prm.group) {
-        const uint16_t* qrow = prm.q + (static_cast<size_t>(b) * prm.h_q + kvh * prm.group + qh) * kHd + qj * 16;
+      if (qh < ncols) {
+        const uint16_t* qrow = q_row(qh) + qj * 16;
         v0 = __ldg(reinterpret_cast<const uint4*>(qrow));
         v1 = __ldg(reinterpret_cast<const uint4*>(qrow + 8));
       }
@@ -901,7 +390,7 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       fence_proxy_async_smem();
       warp_arrive(&sm->q_full);
     }
-    bool ok = xsync();  // qs[] and the zeroed P tiles complete
+    bool ok = xsync();  // qs[], the block's visibility bits and the zeroed P tiles complete
     float c_h[kG], m_h[kG], l_h[kG];
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
@@ -909,12 +398,31 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       m_h[h] = kNegInf;
       l_h[h] = 0.f;
     }
+    const uint32_t grp_bits = (1u << prm.group) - 1u;
+    const bool plain = !kExt || (prm.q_len == 1 && prm.window == 0);
     for (int i = 0; ok && i < nsteps; ++i) {
       const int bf = i & 1, st = i % x2::kStages;
-      const bool live = (st0 + i) * kTok + r < s_k;
+      const int tok = (st0 + i) * kTok + r;
+      const bool live = tok < s_k;
       if (!warp_wait(&sm->s_full[bf], (i >> 1) & 1, abort_flag)) {
         ok = false;
         break;
+      }
+      // this token's K and V row scales (1 past the end: those keys are masked, and a stale
+      // scale must not turn a zero weight into a NaN); the stage cannot be refilled before
+      // this step's P is published, so its phase is this step's
+      float sk = 1.f, lsv = 0.f, isv = 1.f;
+      if constexpr (kRows) {
+        if (!warp_wait(&sm->raw_full[st], (i / x2::kStages) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (live) {
+          const float sv = sm->row_scale[st][1][r];
+          sk = sm->row_scale[st][0][r];
+          lsv = lg2_approx(sv);
+          isv = 1.f / sv;
+        }
       }
       tc_fence_after();
       uint32_t s[2 * kN];
@@ -922,15 +430,31 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       tmem_ld_wait();
       tc_fence_before();
       warp_arrive(&sm->s_free[bf]);
+      // columns that see this thread's key: per query token ti, keys before the block always,
+      // keys inside it by the token's bits, and (window W) only if ti - c_blk < W
+      uint32_t colvis = 0;
+      if (plain) {
+        colvis = live ? 0xFFFFFFFFu : 0u;
+      } else if (live) {
+        const int c_blk = tok - start;
+        for (int ti = 0; ti < prm.q_len; ++ti) {
+          const bool vis = (c_blk < 0 || ((sm->vis_block[ti] >> c_blk) & 1u)) &&
+                           (prm.window == 0 || ti - c_blk < prm.window);
+          if (vis) colvis |= grp_bits << (ti * prm.group);
+        }
+      }
       if (!live) {  // a token past the end: zero its V row, so that P.V multiplies zeros by its zero weight
         uint4* vrow = reinterpret_cast<uint4*>(smem + st * kRawStageBytes + kOffRawV + r * 128);
 #pragma unroll
         for (int c = 0; c < 8; ++c) vrow[c] = make_uint4(0, 0, 0, 0);
       }
+      // (per-row scales) u = the scaled score plus log2 of the token's V scale, so that P' = 2^(u - m)
+      // carries the V scale into P.V on the raw codes; the row sums take P' / sigma_v
       float v[kG];
 #pragma unroll
       for (int h = 0; h < kG; ++h)
-        v[h] = live ? (__uint_as_float(s[h]) + __uint_as_float(s[kN + h])) * c_h[h] : kNegInf;
+        v[h] = ((colvis >> h) & 1u) ? (__uint_as_float(s[h]) + __uint_as_float(s[kN + h])) * c_h[h] * sk + lsv
+                                    : kNegInf;
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
         float x = v[h];
@@ -962,7 +486,7 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           p[k] = ex2_approx(v[h + k] - (m_h[h + k] == kNegInf ? 0.f : m_h[h + k]));
-          l_h[h + k] = l_h[h + k] * alpha[h + k] + p[k];
+          l_h[h + k] = l_h[h + k] * alpha[h + k] + (kRows ? p[k] * isv : p[k]);
         }
         uint32_t hi, lo;
         x2::split_e4m3x4(p[0] * x2::kPScale, p[1] * x2::kPScale, p[2] * x2::kPScale, p[3] * x2::kPScale, hi, lo);
@@ -1029,13 +553,14 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       tmem_ld_wait();
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
-        if (h >= prm.group) break;
+        if (h >= ncols) break;
         const float lsum = (sm->red2[0][h] + sm->red2[1][h]) + (sm->red2[2][h] + sm->red2[3][h]);
         const float oh = __uint_as_float(o[h]) + __uint_as_float(o[kN + h]);
-        const size_t orow = static_cast<size_t>(b) * prm.h_q + kvh * prm.group + h;
+        const int hq = kvh * prm.group + h % prm.group;
+        const size_t orow = (static_cast<size_t>(b) * prm.q_len + h / prm.group) * prm.h_q + hq;
         if (whole) {
           float f, lse_v;
-          finish_row(m_h[h], lsum, kNegInf, o_scale, &f, &lse_v);
+          finish_row(m_h[h], lsum, (kExt && prm.sinks) ? prm.sinks[hq] : kNegInf, o_scale, &f, &lse_v);
           prm.out[orow * kHd + r] = static_cast<uint16_t>(pack_bf16x2(oh * f, 0.f));
           if (r == 0) prm.lse[orow] = lse_v;
         } else {
@@ -1044,11 +569,12 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
         }
       }
     } else if (ok && nsteps == 0) {
-      for (int h = 0; h < prm.group; ++h) {
-        const size_t orow = static_cast<size_t>(b) * prm.h_q + kvh * prm.group + h;
-        if (whole) {  // no key: out 0, lse -inf
+      for (int h = 0; h < ncols; ++h) {
+        const int hq = kvh * prm.group + h % prm.group;
+        const size_t orow = (static_cast<size_t>(b) * prm.q_len + h / prm.group) * prm.h_q + hq;
+        if (whole) {  // no key: out 0, lse the sink's logit (-inf without one)
           prm.out[orow * kHd + r] = 0;
-          if (r == 0) prm.lse[orow] = kNegInf;
+          if (r == 0) prm.lse[orow] = (kExt && prm.sinks) ? prm.sinks[hq] : kNegInf;
         } else {
           prm.ws_o[(slot * kN + h) * kHd + r] = 0.f;
           if (r == 0) prm.ws_ml[slot * kN + h] = make_float2(kNegInf, 0.f);
@@ -1195,12 +721,15 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   if (scale_rows && ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) & 15u))
     return FP8MLA_ERR_INVALID_ARG;
   int splits = std::min(num_splits, 1 << 16);
-  if (splits == 0) {  // auto: the waves rule for this GPU, with the block table's capacity as the longest context
+  if (splits == 0) {  // auto: the waves rule for this GPU, with the block table's capacity as the longest
+                      // context (or, with a window, the keys a window spans plus one step of alignment)
     int sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess)
       return FP8MLA_ERR_CUDA;
-    splits = gqa_choose_splits(bs, h_kv, max_blocks * gqa::kPage, sms, 0);
+    long long longest = static_cast<long long>(max_blocks) * gqa::kPage;
+    if (window > 0) longest = std::min(longest, static_cast<long long>(window) + q_len - 1 + gqa::kTok);
+    splits = gqa_choose_splits(bs, h_kv, static_cast<int>(longest), sms, 0);
   }
   if (splits > 1) {
     const size_t need = gqa_workspace_bytes(bs, h_q, head_dim, splits);
@@ -1236,46 +765,32 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   prm.group = h_q / h_kv;
   prm.splits = splits;
   prm.softmax_scale = softmax_scale;
+  // one kernel instance per (option set, column count): kMode bit 0 per-row scales, bit 1 the XQA options
+  using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const gqa::Params);
+  static const KernelFn table[4][3] = {
+      {gqa::gqa_x2_kernel<4, 0>, gqa::gqa_x2_kernel<8, 0>, gqa::gqa_x2_kernel<16, 0>},
+      {gqa::gqa_x2_kernel<4, 1>, gqa::gqa_x2_kernel<8, 1>, gqa::gqa_x2_kernel<16, 1>},
+      {gqa::gqa_x2_kernel<4, 2>, gqa::gqa_x2_kernel<8, 2>, gqa::gqa_x2_kernel<16, 2>},
+      {gqa::gqa_x2_kernel<4, 3>, gqa::gqa_x2_kernel<8, 3>, gqa::gqa_x2_kernel<16, 3>}};
   static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
   if (configure_once(configured, [] {
-        const void* f16[9] = {
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 1>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 1>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 1>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 2>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 2>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 2>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<4, 3>), reinterpret_cast<const void*>(gqa::gqa_decode_kernel<8, 3>),
-            reinterpret_cast<const void*>(gqa::gqa_decode_kernel<16, 3>)};
-        const void* two_term[3] = {reinterpret_cast<const void*>(gqa::gqa_x2_kernel<4>),
-                                   reinterpret_cast<const void*>(gqa::gqa_x2_kernel<8>),
-                                   reinterpret_cast<const void*>(gqa::gqa_x2_kernel<16>)};
         cudaError_t e = cudaSuccess;
-        for (const void* f : f16)
-          if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(gqa::kSmemBytes));
-        for (const void* f : two_term)
-          if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(gqa::x2::kSmemBytes));
+        for (const auto& row : table)
+          for (KernelFn f : row)
+            if (e == cudaSuccess)
+              e = cudaFuncSetAttribute(reinterpret_cast<const void*>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(gqa::x2::kSmemBytes));
         return e;
       }) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   const long long grid = static_cast<long long>(bs) * h_kv * splits;
   if (grid > 0x7FFFFFFFll) return FP8MLA_ERR_INVALID_ARG;
   const int ncols = q_len * prm.group;
-  using KernelFn = void (*)(const CUtensorMap, const CUtensorMap, const gqa::Params);
-  // plain decode: the two-term E4M3 kernel; per-row scales or the XQA options: the f16 kernel's instances
-  static const KernelFn two_term[3] = {gqa::gqa_x2_kernel<4>, gqa::gqa_x2_kernel<8>, gqa::gqa_x2_kernel<16>};
-  static const KernelFn table[3][3] = {
-      {gqa::gqa_decode_kernel<4, 1>, gqa::gqa_decode_kernel<8, 1>, gqa::gqa_decode_kernel<16, 1>},
-      {gqa::gqa_decode_kernel<4, 2>, gqa::gqa_decode_kernel<8, 2>, gqa::gqa_decode_kernel<16, 2>},
-      {gqa::gqa_decode_kernel<4, 3>, gqa::gqa_decode_kernel<8, 3>, gqa::gqa_decode_kernel<16, 3>}};
   const bool ext = q_len > 1 || window > 0 || spec_mask != nullptr || sinks != nullptr;
   const int mode = (scale_rows ? 1 : 0) | (ext ? 2 : 0);
   const int gi = ncols <= 4 ? 0 : (ncols <= 8 ? 1 : 2);
-  const cudaError_t le =
-      mode == 0 ? launch_dependent(two_term[gi], dim3(static_cast<unsigned>(grid)), dim3(gqa::x2::kThreads),
-                                   gqa::x2::kSmemBytes, stream, tk, tv, prm)
-                : launch_dependent(table[mode - 1][gi], dim3(static_cast<unsigned>(grid)), dim3(gqa::kThreads),
-                                   gqa::kSmemBytes, stream, tk, tv, prm);
+  const cudaError_t le = launch_dependent(table[mode][gi], dim3(static_cast<unsigned>(grid)),
+                                          dim3(gqa::x2::kThreads), gqa::x2::kSmemBytes, stream, tk, tv, prm);
   if (le != cudaSuccess) return FP8MLA_ERR_CUDA;
   if (splits > 1) {
     dim3 cg(static_cast<unsigned>(bs * h_kv), (ncols + 3) / 4);
