@@ -1182,13 +1182,19 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         if constexpr (kRowScales) {
           // u_j = s_j c sigma_j + log2 sigma_j: the key's score with its K scale, plus its V scale's
           // log, so that P' = 2^(u_j - m) carries sigma_j (masked keys stay -inf)
-          const float* sgv = bars->scl[pst][0];
-          const float* lgv = bars->scl[pst][1];
+          // (16-byte loads: the same four keys' scales for every row of the warp)
+          const float4* sg4 = reinterpret_cast<const float4*>(bars->scl[pst][0]);
+          const float4* lg4 = reinterpret_cast<const float4*>(bars->scl[pst][1]);
+          auto scale4 = [&](uint32_t* v, float4 g, float4 l) {
+            v[0] = __float_as_uint(fmaf(__uint_as_float(v[0]), c_row * g.x, l.x));
+            v[1] = __float_as_uint(fmaf(__uint_as_float(v[1]), c_row * g.y, l.y));
+            v[2] = __float_as_uint(fmaf(__uint_as_float(v[2]), c_row * g.z, l.z));
+            v[3] = __float_as_uint(fmaf(__uint_as_float(v[3]), c_row * g.w, l.w));
+          };
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int kk = 32 * hf + c, ko = 32 * (1 - hf) + c;
-            s[c] = __float_as_uint(fmaf(__uint_as_float(s[c]), c_row * sgv[kk], lgv[kk]));
-            so[c] = __float_as_uint(fmaf(__uint_as_float(so[c]), c_row * sgv[ko], lgv[ko]));
+          for (int c4 = 0; c4 < 8; ++c4) {
+            scale4(s + 4 * c4, sg4[8 * hf + c4], lg4[8 * hf + c4]);
+            scale4(so + 4 * c4, sg4[8 * (1 - hf) + c4], lg4[8 * (1 - hf) + c4]);
           }
         }
         // row max of the 64 scores as a tree of three-way maxima
@@ -1219,14 +1225,15 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         uint32_t pk[8];
         if constexpr (kRowScales) {
           // P' = 2^(u_j - m) (stored, times kPScale); the row sum takes P' / sigma_j = 2^(s_j c sigma_j - m)
-          const float* ivv = bars->scl[pst][2] + 32 * hf;
+          const float4* iv4 = reinterpret_cast<const float4*>(bars->scl[pst][2] + 32 * hf);
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const float p0 = ex2_approx(__uint_as_float(s[c]) + bias);
             const float p1 = ex2_approx(__uint_as_float(s[c + 1]) + bias);
             const float p2 = ex2_approx(__uint_as_float(s[c + 2]) + bias);
             const float p3 = ex2_approx(__uint_as_float(s[c + 3]) + bias);
-            sum += (p0 * ivv[c] + p1 * ivv[c + 1]) + (p2 * ivv[c + 2] + p3 * ivv[c + 3]);
+            const float4 iv = iv4[c / 4];
+            sum += (p0 * iv.x + p1 * iv.y) + (p2 * iv.z + p3 * iv.w);
             pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
           }
         } else {
