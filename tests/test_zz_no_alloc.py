@@ -3,7 +3,7 @@ allocate device memory.
 
 Such callers pass only inputs and outputs; the library keeps the tile
 schedule, the split counts and (FP8 dots) the quantised Q with its per-row
-scales and quantisation error in a fixed device array of its own.  It
+scales in a fixed device array of its own.  It
 schedules one unit per sequence, so fp8mla_decode with one unit per sequence
 (force_splits=1) runs the same kernels on the same schedule: the results must
 be bit-identical.  Two different batches are decoded in a row, so the second
