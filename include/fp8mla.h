@@ -83,14 +83,18 @@ typedef enum {
 } fp8mla_status_t;
 
 /* Precision of the two dot products (Q.K and P.V).
- *  FP8MLA_DOT_16BIT: Q, K, P and V enter the tensor cores as 16-bit values
- *    (the E4M3 cache converts exactly); "bf16 dots" on the aiter page.
+ *  FP8MLA_DOT_16BIT: "bf16 dots" on the aiter page: Q and P keep bf16's 8
+ *    significant bits, K and V are the cache's exact E4M3 values.  Dense MLA
+ *    computes them as two-term E4M3 dots: the latent part of Q (with a
+ *    per-row power-of-two scale) and P (as 64 * p) each enter as hi + lo,
+ *    hi = E4M3(x), lo = E4M3(x - hi); the RoPE part of Q.K is f16.
  *  FP8MLA_DOT_FP8:   the latent part of Q is quantised to E4M3 with a
  *    per-row power-of-two scale, the RoPE part of Q.K stays 16-bit (f16 in
  *    dense MLA; FlashMLA page, Improvements), and P is quantised as E4M3
  *    (64 * p in dense MLA, 128 * p in sparse MLA; aiter page, Technical
- *    details).  The first-order effect of quantising Q on the LSE is
- *    corrected (dense and sparse MLA). */
+ *    details).
+ *  The first-order effect of rounding Q on the LSE is corrected (dense MLA,
+ *  both modes; sparse MLA). */
 typedef enum { FP8MLA_DOT_16BIT = 0, FP8MLA_DOT_FP8 = 1 } fp8mla_dot_mode_t;
 
 /* Encoding of the cache bytes.  Only FP8MLA_KV_E4M3 (OCP e4m3 "fn", or a
@@ -358,7 +362,7 @@ FP8MLA_API fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
 FP8MLA_API fp8mla_status_t fp8mla_set_stage_timing(int enable);
 
 /* Synchronises `stream` and writes ms[0..2] = milliseconds of the last timed
- * fp8mla_decode call's Q quantisation (0 for 16-bit dots), decode kernel and
+ * fp8mla_decode call's Q quantisation, decode kernel and
  * combine.  ms: host pointer to 3 floats.  FP8MLA_ERR_INVALID_ARG if no call
  * was timed since timing was enabled; FP8MLA_ERR_CUDA if the events cannot be
  * read (for instance when the last timed call ran on another device). */

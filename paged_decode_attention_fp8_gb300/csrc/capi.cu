@@ -265,16 +265,15 @@ fp8mla_status_t mla_decode_call(const void* q, const void* kv_cache, fp8mla_kv_d
   }
   auto mark = [&](int i) { return timed ? cudaEventRecord(timer.ev[i], s) : cudaSuccess; };
   cudaError_t e = mark(0);
-  if (e == cudaSuccess && dot_mode == FP8MLA_DOT_FP8) e = launch_mla_qprep(prm, s);
+  if (e == cudaSuccess) e = launch_mla_qprep(prm, s);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess)
     e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_decode_fp8(tm_lat, tm_rope, prm, num_units, s)
                                      : launch_mla_decode_16bit(tm_lat, tm_rope, prm, num_units, s);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess)
-    e = launch_mla_combine(num_splits, prm.ws_o, prm.ws_ml, dot_mode == FP8MLA_DOT_FP8 ? prm.q : nullptr,
-                           dot_mode == FP8MLA_DOT_FP8 ? prm.qscale : nullptr, softmax_scale, prm.out, lse, b,
-                           s_q * h_q, s);
+    e = launch_mla_combine(num_splits, prm.ws_o, prm.ws_ml, prm.q, prm.qscale, dot_mode == FP8MLA_DOT_16BIT,
+                           softmax_scale, prm.out, lse, b, s_q * h_q, s);
   if (e == cudaSuccess) e = mark(3);
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
   if (timed) timer.timed = true;

@@ -153,13 +153,6 @@ __device__ __forceinline__ int pow2_exp_448(float amax) {
   const uint32_t mant = bits & 0x7FFFFFu;
   return max((expo - 127) - (mant <= 0x600000u ? 8 : 7), -126);
 }
-
-// x -> (hi, lo) E4M3 codes of four values, hi = E4M3(x), lo = E4M3(x - hi).
-__device__ __forceinline__ void split_e4m3x4(float a, float b, float c, float d, uint32_t& hi, uint32_t& lo) {
-  hi = pack_e4m3x4(a, b, c, d);
-  const uint32_t h01 = e4m3x2_to_f16x2(hi & 0xFFFFu), h23 = e4m3x2_to_f16x2(hi >> 16);
-  lo = pack_e4m3x4(a - f16_lo(h01), b - f16_hi(h01), c - f16_lo(h23), d - f16_hi(h23));
-}
 }  // namespace x2
 
 // kG: the softmax handles MMA columns [0, kG) of the N = 16 (kG >= q_len * group).
@@ -378,7 +371,7 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        x2::split_e4m3x4(bf16_lo(wd[2 * k]) * inv, bf16_hi(wd[2 * k]) * inv, bf16_lo(wd[2 * k + 1]) * inv,
+        split_e4m3x4(bf16_lo(wd[2 * k]) * inv, bf16_hi(wd[2 * k]) * inv, bf16_lo(wd[2 * k + 1]) * inv,
                          bf16_hi(wd[2 * k + 1]) * inv, hi[k], lo[k]);
       // row n, dims [16 qj, 16 qj + 16) = 16-byte chunk qj of the 128-byte row, XOR-swizzled by n % 8
       const int nh = qh, nl = kN + qh;
@@ -489,7 +482,7 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
           l_h[h + k] = l_h[h + k] * alpha[h + k] + (kRows ? p[k] * isv : p[k]);
         }
         uint32_t hi, lo;
-        x2::split_e4m3x4(p[0] * x2::kPScale, p[1] * x2::kPScale, p[2] * x2::kPScale, p[3] * x2::kPScale, hi, lo);
+        split_e4m3x4(p[0] * x2::kPScale, p[1] * x2::kPScale, p[2] * x2::kPScale, p[3] * x2::kPScale, hi, lo);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           phi[h + k] = static_cast<uint8_t>(hi >> (8 * k));

@@ -205,13 +205,15 @@ __global__ void __launch_bounds__(kMetaThreads) mla_metadata_kernel(const int32_
 // M = max m_s, L = sum l_s 2^(m_s - M), out = sum acc_s 2^(m_s - M) / L,
 // lse = ln2 (M + log2 L).  Partial slots are [slot][128] rows of dv = 512
 // bf16, sequence bi owning the slots from num_splits[bi].  With q non-null
-// (FP8 dots) every row's LSE also gets the first-order Q-quantisation
-// correction lse -= softmax_scale (q_hat - q) . out, from the finished output
-// row and q_hat - q of the row's latent part: q_hat = E4M3(q / qs) qs with the
-// row's power-of-two scale qs, the prep kernel's rounding (exact in fp32).
+// every row's LSE also gets the first-order Q-quantisation correction
+// lse -= softmax_scale (q_hat - q) . out, from the finished output row and
+// q_hat - q of the row's latent part, with the row's power-of-two scale qs
+// and the decode kernel's rounding (exact in fp32): q_hat = E4M3(q / qs) qs
+// for FP8 dots, q_hat = (hi + E4M3(q / qs - hi)) qs with hi = E4M3(q / qs)
+// for two-term dots (two_term != 0).
 __global__ void __launch_bounds__(256) mla_combine_kernel(
     const int32_t* __restrict__ num_splits, const uint16_t* __restrict__ ws_o, const float2* __restrict__ ws_ml,
-    const uint16_t* __restrict__ q, const float* __restrict__ qscale, float softmax_scale,
+    const uint16_t* __restrict__ q, const float* __restrict__ qscale, int two_term, float softmax_scale,
     uint16_t* __restrict__ out, float* __restrict__ lse, int rows) {
   const int bi = blockIdx.x;
   const int r = blockIdx.y * 8 + threadIdx.x / 32;
@@ -234,13 +236,16 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
-      const uint32_t codes = pack_e4m3x4(bf16_lo(w[k]) * inv, bf16_hi(w[k]) * inv, bf16_lo(w[k + 1]) * inv,
-                                         bf16_hi(w[k + 1]) * inv);
-      const uint32_t h01 = e4m3x2_to_f16x2(codes & 0xFFFFu), h23 = e4m3x2_to_f16x2(codes >> 16);
-      ev[2 * k] = f16_lo(h01) * qs - bf16_lo(w[k]);
-      ev[2 * k + 1] = f16_hi(h01) * qs - bf16_hi(w[k]);
-      ev[2 * k + 2] = f16_lo(h23) * qs - bf16_lo(w[k + 1]);
-      ev[2 * k + 3] = f16_hi(h23) * qs - bf16_hi(w[k + 1]);
+      uint32_t hi, lo;
+      split_e4m3x4(bf16_lo(w[k]) * inv, bf16_hi(w[k]) * inv, bf16_lo(w[k + 1]) * inv, bf16_hi(w[k + 1]) * inv, hi,
+                   lo);
+      if (!two_term) lo = 0u;  // E4M3 zero codes
+      const uint32_t h01 = e4m3x2_to_f16x2(hi & 0xFFFFu), h23 = e4m3x2_to_f16x2(hi >> 16);
+      const uint32_t l01 = e4m3x2_to_f16x2(lo & 0xFFFFu), l23 = e4m3x2_to_f16x2(lo >> 16);
+      ev[2 * k] = (f16_lo(h01) + f16_lo(l01)) * qs - bf16_lo(w[k]);
+      ev[2 * k + 1] = (f16_hi(h01) + f16_hi(l01)) * qs - bf16_hi(w[k]);
+      ev[2 * k + 2] = (f16_lo(h23) + f16_lo(l23)) * qs - bf16_lo(w[k + 1]);
+      ev[2 * k + 3] = (f16_hi(h23) + f16_hi(l23)) * qs - bf16_hi(w[k + 1]);
     }
   }
   // (q_hat - q) . o over the whole row, o holding this lane's 16 columns
@@ -393,11 +398,11 @@ cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, in
 }
 
 cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,
-                               const uint16_t* q, const float* qscale, float softmax_scale, uint16_t* out,
-                               float* lse, int b, int rows, cudaStream_t stream) {
+                               const uint16_t* q, const float* qscale, bool two_term, float softmax_scale,
+                               uint16_t* out, float* lse, int b, int rows, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
   return launch_dependent(mla_combine_kernel, dim3(b, (rows + 7) / 8), dim3(256), 0, stream, num_splits, ws_o, ws_ml,
-                          q, qscale, softmax_scale, out, lse, rows);
+                          q, qscale, two_term ? 1 : 0, softmax_scale, out, lse, rows);
 }
 
 uint32_t metadata_read_and_clear_status() {

@@ -6,8 +6,8 @@
 //   P = softmax(softmax_scale * S) under the causal mask, O = P V with V the
 //   first 512 dims of the same rows; lse = log sum exp.
 //
-// GB300 design: one work unit = 2 CTAs (FP8 dots, mla_fp8_kernel) or 4 CTAs
-// (16-bit dots, mla_decode_16bit_kernel), each owning one slice of dv.
+// GB300 design: one work unit = 2 CTAs of mla_fp8_kernel, each owning one
+// 256-wide slice of dv.
 //   * TMA loads a whole 64-token page through the block table: four
 //     128-byte-swizzled boxes of the 512 latent bytes (usable as K-major B
 //     for Q.K^T and as MN-major B for P.V without any transpose) and one
@@ -22,8 +22,10 @@
 //     Q.K^T = 16 E4M3 MMAs (K = 32) + 4 f16 MMAs (K = 16) into one f32
 //     accumulator -- the RoPE chunk stays 16-bit (FlashMLA page,
 //     Improvements) -- and P.V = 2 E4M3 MMAs with N = 256.
-//   * 16-bit dots: converter warps turn each page into bf16 (exact); Q, S, P
-//     and O live in TMEM and both products run as bf16 MMAs.
+//   * 16-bit dots run as two-term E4M3 dots: Q's latent part and P enter as
+//     hi + lo (hi = E4M3(x), lo = E4M3(x - hi): bf16's 8 significant bits)
+//     against the cache's exact E4M3 K and V, adding 16 Q_lo MMAs to each
+//     Q.K^T and 2 P_lo MMAs to each P.V; the RoPE chunk is f16 as above.
 //   * Online softmax in the log2 domain (InfiniCore page, Summary) with the
 //     per-tensor kv_scale and qs folded into one per-row constant; with FP8
 //     dots P is stored as E4M3(64 p) so long tails do not flush to zero, and
@@ -35,15 +37,15 @@
 //     tile was the stated limiter); scores there are masked by a select.
 //   * A unit may cover a piece of a sequence; pieces publish (m, l, O) to a
 //     workspace and a combine kernel merges them (InfiniCore split-kv commit).
-//   * FP8 dots perturb the LSE by softmax_scale * (q_hat - q) . k_mean, where
-//     k_mean = sum_j p_j k_j; its latent part is exactly the output row, so
-//     the combine kernel subtracts softmax_scale * (q_hat - q) . out, from the
-//     finished output row and q_hat - q recomputed from q and the row's scale
-//     with the prep kernel's rounding.
+//   * Rounding Q perturbs the LSE by softmax_scale * (q_hat - q) . k_mean,
+//     where k_mean = sum_j p_j k_j; its latent part is exactly the output row,
+//     so the combine kernel subtracts softmax_scale * (q_hat - q) . out, from
+//     the finished output row and q_hat - q recomputed from q and the row's
+//     scale with the decode kernel's rounding (one term or two).
 //
 // Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM
-// owner, warps 2-3 page conversion (the RoPE part to f16, or the whole page
-// to bf16) and tail zeroing, warps 4-11 softmax, Q copy and epilogue: query
+// owner, warps 2-3 page conversion (the RoPE part to f16) and tail zeroing,
+// warps 4-11 softmax, Q copy and epilogue: query
 // row r (= TMEM lane r) is shared by two threads, each owning half of the
 // page's score columns and half of the O slice.
 #include <cuda.h>
@@ -69,33 +71,6 @@ constexpr int kRows = 128;
 constexpr int kSoftmaxThreads = 256;                // two threads per query row
 constexpr int kLatBox = kPage * 128;                 // one 128-byte column slice of a page (8 KB)
 constexpr uint32_t kPageTxBytes = kPage * kD;        // bytes one page's TMA loads deliver
-
-// 16-bit dots (exact): 4 CTAs per unit, each owning a 128-column slice of dv.
-struct Cfg16 {
-  static constexpr int kParts = 4, kDvPart = 128, kStages = 2;
-  static constexpr int kThreads = 384;
-  static constexpr float kPScale = 1.0f, kPLog2 = 0.0f, kTau = 8.0f;
-  static constexpr int kOffRope8 = 4 * kLatBox;
-  static constexpr int kOffCvt = kOffRope8 + kPage * 64;  // 9 bf16 boxes: 8 latent + RoPE
-  static constexpr int kStageBytes = kOffCvt + 9 * kLatBox;
-  static constexpr uint32_t kTO = 0, kTS = 128, kTP = 192, kTQ = 224, kTQR = 224 + 256;
-};
-static_assert(Cfg16::kOffCvt % 1024 == 0 && Cfg16::kStageBytes % 1024 == 0, "1 KB aligned tiles");
-
-struct Barriers16 {
-  uint64_t kv_full[Cfg16::kStages];
-  uint64_t kv_empty[Cfg16::kStages];
-  uint64_t cvt_ready[Cfg16::kStages];
-  uint64_t s_full, s_free, p_full, pv_done, q_full, final_mma;
-  uint64_t xchg;            // softmax-group exchange barrier (all 256 softmax threads arrive)
-  uint32_t tmem_base;
-  uint32_t abort_flag;
-  uint32_t cvt_ok;
-  float xmax[2][2][kRows];  // per-page tile max of each row half, double-buffered by page parity
-  float xsum[2][kRows];     // row-sum halves
-};
-
-constexpr size_t smem_bytes16() { return Cfg16::kStages * Cfg16::kStageBytes + sizeof(Barriers16) + 1024; }
 
 // One (sequence, page range) piece of a unit's work.
 struct Segment {
@@ -165,472 +140,54 @@ __device__ __forceinline__ float absmax_bf16x8(uint4 v) {
                fmaxf(fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))), fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w)))));
 }
 
-// Dense MLA decode with 16-bit dots: Q and every page converted to bf16
-// (exact), bf16 MMAs; the reference for the FP8-dot kernel's rounding.
-__global__ void __launch_bounds__(Cfg16::kThreads, 1)
-    mla_decode_16bit_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
-                            const MlaParams prm) {
-  using C = Cfg16;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  Barriers16* bars = reinterpret_cast<Barriers16*>(smem + C::kStages * C::kStageBytes);
-  volatile uint32_t* abort_flag = &bars->abort_flag;
-
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  const int unit = blockIdx.x / C::kParts;
-  const int part = blockIdx.x % C::kParts;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
-      mbar_init(&bars->cvt_ready[s], 1);
-    }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, kSoftmaxThreads / 32);   // one arrival per softmax warp
-    mbar_init(&bars->p_full, kSoftmaxThreads / 32);
-    mbar_init(&bars->pv_done, 1);
-    mbar_init(&bars->q_full, kSoftmaxThreads / 32);
-    mbar_init(&bars->final_mma, 1);
-    mbar_init(&bars->xchg, kSoftmaxThreads / 32);
-    bars->abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
-  }
-  // Everything above overlaps the previous kernel (launched as its dependent);
-  // from here on this grid reads the schedule and writes outputs.
-  griddep_wait();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  griddep_launch_dependents();
-  const uint32_t tmem = bars->tmem_base;
-
-
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer ----
-    // The warp loads 32 block-table entries at a time (one per lane) and lane 0
-    // issues the page loads, so no page waits on its own table lookup.
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_lat);
-      tma_prefetch_desc(&tm_rope);
-    }
-    SegmentWalker walk(prm, unit);
-    Segment sg;
-    int i = 0;
-    bool ok = true;
-    while (ok && walk.next(sg)) {
-      const int32_t* bt = prm.block_table + static_cast<size_t>(sg.b) * prm.max_pages;
-      for (int chunk = sg.lo; ok && chunk < sg.hi; chunk += 32) {
-        int mine = 0;
-        if (chunk + lane < sg.hi) {
-          mine = __ldg(bt + chunk + lane);
-          if (mine < 0 || mine >= prm.num_pages) {
-            atomicOr(&g_status_mla, FP8MLA_DEV_BAD_PAGE);
-            mine = 0;
-          }
-        }
-        const int cnt = min(32, sg.hi - chunk);
-        for (int j = 0; j < cnt; ++j, ++i) {
-          const int phys = __shfl_sync(0xffffffffu, mine, j);
-          const int st = i % C::kStages;
-          const int use = i / C::kStages;
-          bool waited = true;
-          if (lane == 0) {
-            waited = use == 0 || wait_bounded(&bars->kv_empty[st], (use - 1) & 1, abort_flag, &g_status_mla, __LINE__);
-            if (waited) {
-              uint8_t* sb = smem + st * C::kStageBytes;
-              mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes);
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                tma_load_3d(sb + k * kLatBox, &tm_lat, &bars->kv_full[st], k * 128, 0, phys);
-              tma_load_3d(sb + C::kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, waited ? 1 : 0, 0)) {
-            ok = false;
-            break;
-          }
-        }
-      }
-    }
-    // Never leave with copies in flight: wait for the last loads issued.
-    if (lane == 0)
-      for (int j = max(0, i - C::kStages); j < i; ++j)
-        wait_bounded(&bars->kv_full[j % C::kStages], (j / C::kStages) & 1, nullptr, &g_status_mla, __LINE__);
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------- MMA issuer ----
-    // The whole warp runs the loop (warp-uniform descriptors and bounded
-    // waits) and one elected lane issues: from a lone thread each MMA costs
-    // about twice as long.
-    {
-      const bool leader = elect_one();
-      const uint32_t t_s = tmem + C::kTS, t_o = tmem + C::kTO;
-      SegmentWalker walk(prm, unit);
-      Segment sg;
-      int i = 0, seg_i = 0;
-      bool ok = true;
-
-      auto issue_qk = [&](uint32_t sb) {
-        constexpr uint32_t idesc16 = make_idesc(1, 1, 0, 0, 64, 128);
-#pragma unroll
-        for (int kk = 0; kk < 36; ++kk) {
-          const uint64_t bd =
-              make_sdesc(sb + C::kOffCvt + (kk >> 2) * kLatBox + (kk & 3) * 32, 16, 1024, SWIZZLE_128B);
-          mma_f16_ts_if(leader, t_s, tmem + C::kTQ + kk * 8, bd, idesc16, kk > 0 ? 1u : 0u);
-        }
-      };
-
-      auto issue_pv = [&](int j, bool first_in_seg) -> bool {
-        if (!warp_wait(&bars->p_full, j & 1, abort_flag, __LINE__)) return false;
-        tc_fence_after();
-        const int st = j % C::kStages;
-        const uint32_t sb = smem_u32(smem + st * C::kStageBytes);
-        constexpr uint32_t idesc = make_idesc(1, 1, 0, 1, 128, 128);  // bf16, B MN-major, N = 128
-        const uint32_t v_base = sb + C::kOffCvt + part * 2 * kLatBox;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = make_sdesc(v_base + kk * 2048, kLatBox, 1024, SWIZZLE_128B);
-          mma_f16_ts_if(leader, t_o, tmem + C::kTP + kk * 8, bd, idesc, (first_in_seg && kk == 0) ? 0u : 1u);
-        }
-        tc_commit_if(leader, &bars->pv_done);
-        tc_commit_if(leader, &bars->kv_empty[st]);
-        return true;
-      };
-
-      while (ok && walk.next(sg)) {
-        if (!warp_wait(&bars->q_full, seg_i & 1, abort_flag, __LINE__)) break;
-        const int first_i = i;
-        for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
-          const int st = i % C::kStages;
-          const int use = i / C::kStages;
-          if (!warp_wait(&bars->kv_full[st], use & 1, abort_flag, __LINE__) ||
-              !warp_wait(&bars->cvt_ready[st], use & 1, abort_flag, __LINE__) ||
-              (i > 0 && !warp_wait(&bars->s_free, (i - 1) & 1, abort_flag, __LINE__))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_qk(smem_u32(smem + st * C::kStageBytes));
-          tc_commit_if(leader, &bars->s_full);
-          if (i > first_i && !issue_pv(i - 1, i - 1 == first_i)) {
-            ok = false;
-            break;
-          }
-        }
-        if (!ok) break;
-        if (!issue_pv(i - 1, i - 1 == first_i)) break;
-        ++seg_i;
-      }
-      if (leader) tc_commit(&bars->final_mma);
-      __syncwarp();
-      warp_wait(&bars->final_mma, 0, nullptr, __LINE__);
-    }
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------------- page conversion, tail zeroing ----
-    const int t = threadIdx.x - 64;  // token row of the page
-    SegmentWalker walk(prm, unit);
-    Segment sg;
-    int i = 0;
-    bool ok = true;
-    while (ok && walk.next(sg)) {
-      for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
-        const int st = i % C::kStages;
-        const int use = i / C::kStages;
-        if (t == 0) bars->cvt_ok = wait_bounded(&bars->kv_full[st], use & 1, abort_flag, &g_status_mla, __LINE__) ? 1u : 0u;
-        named_bar_sync(1, 64);
-        if (!bars->cvt_ok) {
-          ok = false;
-          break;
-        }
-        uint8_t* sb = smem + st * C::kStageBytes;
-        const bool dead = (pg == sg.n - 1) && (t >= sg.s_k - pg * kPage);  // slot past the sequence end
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        const int sw = t & 7;
-        // RoPE bytes -> bf16 (box C::kOffCvt + (8 boxes))
-        {
-          const uint4* src = reinterpret_cast<const uint4*>(sb + C::kOffRope8 + t * 64);
-          uint8_t* dst = sb + C::kOffCvt + 8 * kLatBox + t * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4 lo = z, hi = z;
-            if (!dead) {
-              const uint4 v = src[c];
-              e4m3x4_to_bf16x4(v.x, lo.x, lo.y);
-              e4m3x4_to_bf16x4(v.y, lo.z, lo.w);
-              e4m3x4_to_bf16x4(v.z, hi.x, hi.y);
-              e4m3x4_to_bf16x4(v.w, hi.z, hi.w);
-            }
-            *reinterpret_cast<uint4*>(dst + (((2 * c) ^ sw) << 4)) = lo;
-            *reinterpret_cast<uint4*>(dst + (((2 * c + 1) ^ sw) << 4)) = hi;
-          }
-        }
-        {
-          // latent: raw box j chunk c (16 E4M3) -> bf16 box 2j + c/4, chunks 2(c%4), 2(c%4)+1
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            const uint8_t* src = sb + j * kLatBox + t * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint4 lo = z, hi = z;
-              if (!dead) {
-                const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
-                e4m3x4_to_bf16x4(v.x, lo.x, lo.y);
-                e4m3x4_to_bf16x4(v.y, lo.z, lo.w);
-                e4m3x4_to_bf16x4(v.z, hi.x, hi.y);
-                e4m3x4_to_bf16x4(v.w, hi.z, hi.w);
-              }
-              uint8_t* dst = sb + C::kOffCvt + (2 * j + c / 4) * kLatBox + t * 128;
-              *reinterpret_cast<uint4*>(dst + (((2 * (c % 4)) ^ sw) << 4)) = lo;
-              *reinterpret_cast<uint4*>(dst + (((2 * (c % 4) + 1) ^ sw) << 4)) = hi;
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 64);
-        if (t == 0) mbar_arrive(&bars->cvt_ready[st]);
-      }
-    }
-  } else {
-    // ------------------ softmax / Q prep / epilogue (8 warps, 2 per row) ----
-    const int hf = (warp - 4) / 4;                          // which half of the row
-    const int r = (warp % 4) * 32 + lane;                   // query row = TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp % 4) * 32) << 16);
-    const float kv_scale = *prm.kv_scale;
-    const int R = prm.s_q * prm.h_q;
-    constexpr int kOHalf = C::kDvPart / 2;                  // O columns of this thread
-    // Exchange point of the 256 softmax threads: an mbarrier with bounded,
-    // abort-aware waits, so no thread can block forever on a peer that stopped.
-    uint32_t xphase = 0;
-    auto xsync = [&]() -> bool {
-      warp_arrive(&bars->xchg);
-      const bool ok = warp_wait(&bars->xchg, xphase & 1, abort_flag, __LINE__);
-      ++xphase;
-      return ok;
-    };
-    SegmentWalker walk(prm, unit);
-    Segment sg;
-    int i = 0;
-    while (walk.next(sg)) {
-      const uint16_t* qrow = prm.q + (static_cast<size_t>(sg.b) * R + r) * kD;
-      float c_row;
-      {
-        // ---- Q preparation: bf16 as is; 64-value chunks 0-4 (hf 0) or 5-8 (hf 1) ----
-        c_row = prm.softmax_scale * kLog2e * kv_scale;
-#pragma unroll 1
-        for (int ch = hf ? 5 : 0; ch < (hf ? 9 : 5); ++ch) {
-          uint32_t pk[32];
-          const uint4* q4 = reinterpret_cast<const uint4*>(qrow + ch * 64);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < R) v = __ldg(q4 + c);
-            pk[4 * c + 0] = v.x;
-            pk[4 * c + 1] = v.y;
-            pk[4 * c + 2] = v.z;
-            pk[4 * c + 3] = v.w;
-          }
-          tmem_st32(lane_base + C::kTQ + ch * 32, pk);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(&bars->q_full);
-      {  // warm L2 with the next segment's Q rows while this one runs
-        SegmentWalker peek = walk;
-        Segment nx;
-        if (peek.next(nx) && r < R) {
-          const char* nq = reinterpret_cast<const char*>(prm.q + (static_cast<size_t>(nx.b) * R + r) * kD);
-          for (int o = hf * (kD * 2 / 2); o < (hf + 1) * (kD * 2 / 2); o += 128) prefetch_l2(nq + o);
-        }
-      }
-
-      // keys visible to this row (bottom-right causal alignment); pages wholly
-      // below every row's limit need no mask
-      const int qtok = (r < R) ? r / prm.h_q : 0;
-      const int visible = prm.causal ? (sg.s_k - prm.s_q + qtok + 1) : sg.s_k;
-      const int min_visible = prm.causal ? (sg.s_k - prm.s_q + 1) : sg.s_k;
-      float m_run = kNegInf, l_run = 0.f;  // l_run sums the scaled p (2^kPLog2 p)
-      bool ok = true;
-      for (int pg = sg.lo; pg < sg.hi; ++pg, ++i) {
-        if (!warp_wait(&bars->s_full, i & 1, abort_flag, __LINE__)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t s[32];
-        tmem_ld32(lane_base + C::kTS + 32 * hf, s);
-        tmem_ld_wait();
-        tc_fence_before();
-        warp_arrive(&bars->s_free);
-
-        float mx = kNegInf;
-        if (pg * kPage + kPage > min_visible) {
-          const int base = pg * kPage + 32 * hf;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float v = (base + c < visible) ? __uint_as_float(s[c]) : kNegInf;
-            s[c] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-        }
-        mx *= c_row;  // c_row > 0
-        float* xm = &bars->xmax[i & 1][0][0];
-        xm[hf * kRows + r] = mx;
-        if (!xsync()) {
-          ok = false;
-          break;
-        }
-        mx = fmaxf(xm[r], xm[kRows + r]);
-        float alpha = 1.f;
-        bool rescale = false;
-        if (mx > m_run + C::kTau) {
-          alpha = ex2_approx(m_run - mx);
-          rescale = (pg != sg.lo);
-          m_run = mx;
-        }
-        const float bias = (m_run == kNegInf) ? 0.f : (C::kPLog2 - m_run);
-        float sum = 0.f;
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), c_row, bias));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), c_row, bias));
-          const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
-          const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
-          sum += (p0 + p1) + (p2 + p3);
-          {
-            pk[c / 2] = pack_bf16x2(p0, p1);
-            pk[c / 2 + 1] = pack_bf16x2(p2, p3);
-          }
-        }
-        l_run = l_run * alpha + sum;
-
-        if (i > 0 && !warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag, __LINE__)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float f = rescale ? alpha : 1.f;
-#pragma unroll 1
-          for (int ch = 0; ch < kOHalf / 32; ++ch) {
-            const uint32_t col = C::kTO + hf * kOHalf + ch * 32;
-            uint32_t o[32];
-            tmem_ld32(lane_base + col, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
-            tmem_st32(lane_base + col, o);
-          }
-        }
-        tmem_st16(lane_base + C::kTP + 16 * hf, pk);
-        tmem_st_wait();
-        tc_fence_before();
-        warp_arrive(&bars->p_full);
-      }
-      if (!ok) break;
-
-      // ---- epilogue: O is final once the segment's last P.V completes ----
-      if (!warp_wait(&bars->pv_done, (i - 1) & 1, abort_flag, __LINE__)) break;
-      tc_fence_after();
-      bars->xsum[hf][r] = l_run;
-      if (!xsync()) break;
-      const float l_tot = (bars->xsum[0][r] + bars->xsum[1][r]) * (1.0f / C::kPScale);  // sum of p
-      const bool whole = (sg.lo == 0 && sg.hi == sg.n);
-      const float o_scale = kv_scale / C::kPScale;  // tensor-core units -> true units
-      const float f = whole ? ((l_tot > 0.f) ? o_scale / l_tot : 0.f) : o_scale;
-      const int col0 = part * C::kDvPart + hf * kOHalf;
-      const int slot = whole ? 0 : prm.num_splits[sg.b] + sg.split;
-#pragma unroll 1
-      for (int ch = 0; ch < kOHalf / 32; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + C::kTO + hf * kOHalf + ch * 32, o);
-        tmem_ld_wait();
-        if (r >= R) continue;
-        if (whole) {
-          uint4* dst = reinterpret_cast<uint4*>(prm.out + (static_cast<size_t>(sg.b) * R + r) * kDV + col0 + ch * 32);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
-            dst[c] = w;
-          }
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(prm.ws_o + (static_cast<size_t>(slot) * kRows + r) * kDV + col0 + ch * 32);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * f, __uint_as_float(o[8 * c + 1]) * f);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * f, __uint_as_float(o[8 * c + 3]) * f);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * f, __uint_as_float(o[8 * c + 5]) * f);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * f, __uint_as_float(o[8 * c + 7]) * f);
-            dst[c] = w;
-          }
-        }
-      }
-      if (r < R && hf == 0) {
-        const size_t row = static_cast<size_t>(sg.b) * R + r;
-        if (whole) {
-          if (part == 0) prm.lse[row] = (l_tot > 0.f) ? (m_run + lg2_approx(l_tot)) * kLn2 : kNegInf;
-        } else {
-          const size_t srow = static_cast<size_t>(slot) * kRows + r;
-          if (part == 0) prm.ws_ml[srow] = make_float2((l_tot > 0.f) ? m_run : kNegInf, l_tot);
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
 // ===========================================================================
-// FP8-dots kernel.
+// Decode kernel (both dot modes).
 //
 // Work unit = 2 CTAs, each owning one 256-wide dv slice.  The shared-memory
-// ring of 5 stages carries, in one order that every role walks, three Q slots
-// at the start of each segment (the segment's quantised Q: two latent halves
-// and the RoPE part) followed by the segment's KV pages, so no separate Q
-// buffer competes with the KV pages for shared memory.  TMEM: O 256 + two S
-// buffers of 64 + Q latent 128 columns.
+// ring (5 stages; 3 with two-term dots) carries, in one order that every role
+// walks, three Q slots at the start of each segment (the segment's quantised
+// Q: two latent halves and the RoPE part) followed by the segment's KV pages,
+// so no separate Q buffer competes with the KV pages for shared memory.
+// TMEM: O 256 + two S buffers of 64 + Q latent 128 columns.
+//
+// 16-bit dots run as two-term E4M3 dots: Q's latent part and P each enter as
+// hi + lo (hi = E4M3(x), lo = E4M3(x - hi), about bf16's 8 significant bits)
+// against the cache's own E4M3 K and V codes, so no page is converted and the
+// MMAs stay f8f6f4: Q.K^T takes 16 more MMAs (Q_lo from shared memory) and
+// P.V 2 more (P_lo).  Q_lo is formed from the bf16 Q by the softmax warps
+// when they copy the segment's Q.
 // ===========================================================================
 namespace f8 {
-constexpr int kStages = 5;
 // Test hook of the bounded waits (0 = off); set by mla_set_wait_test.
 __device__ int g_fault_page = 0;
 constexpr int kThreads = 384;
 constexpr int kOffRope8 = 4 * kLatBox;             // 64 tokens x 64 E4M3 RoPE bytes, no swizzle
 constexpr int kStageBytes = kOffRope8 + kPage * 64;
-// Shared memory after the ring: two buffers for a page's RoPE part as f16
+constexpr int kCvtBytes = kLatBox;
+constexpr int kQLoBlock = kRows * 128;             // one 128-byte column block of Q_lo (16 KB)
+// Shared memory: the ring, then two buffers for a page's RoPE part as f16
 // (64 keys x 128 B, 128-byte swizzle), Q's RoPE part (128 rows x 128 B f16,
 // 128-byte swizzle), and P (128 rows x 64 E4M3 keys) as 8-row x 16-byte core
 // matrices: row group g and 16-byte key chunk c at g * kPSbo + c * kPLbo.
-constexpr int kCvtBytes = kLatBox;
-constexpr int kOffCvt = kStages * kStageBytes;
-constexpr int kOffQRope = kOffCvt + 2 * kCvtBytes;
-constexpr int kOffP = kOffQRope + kRows * 128;
+// Two-term dots add P_lo (P's layout) and Q_lo: 128 rows x 512 E4M3 as four
+// column blocks of kQLoBlock, each 128-byte swizzled (the K page's layout).
+template <bool kTwoTerm>
+struct Layout {
+  static constexpr int kStages = kTwoTerm ? 3 : 5;
+  static constexpr int kOffCvt = kStages * kStageBytes;
+  static constexpr int kOffQRope = kOffCvt + 2 * kCvtBytes;
+  static constexpr int kOffP = kOffQRope + kRows * 128;
+  static constexpr int kOffPLo = kOffP + kRows * kPage;
+  static constexpr int kOffQLo = kOffPLo + (kTwoTerm ? kRows * kPage : 0);
+  static constexpr int kSmemData = kOffQLo + (kTwoTerm ? 4 * kQLoBlock : 0);
+  static_assert(kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0 && kOffPLo % 1024 == 0 &&
+                    kOffQLo % 1024 == 0,
+                "1 KB aligned tiles");
+};
 constexpr int kPLbo = 128, kPSbo = 512;
-constexpr int kSmemData = kOffP + kRows * kPage;
 constexpr float kPScale = 64.0f, kPLog2 = 6.0f;  // P is stored as E4M3(64 p)
 constexpr float kTau = 2.75f;                     // 64 * 2^2.75 = 430.5 < 448
-// TMEM columns: O slice, two S buffers (pages alternate), Q latent (E4M3).
+// TMEM columns: O slice, two S buffers (pages alternate), Q latent (E4M3; Q_hi with two-term dots).
 constexpr uint32_t kTO = 0, kTS = 256, kTQ = 384;
 // Quantised Q of a sequence, as three ring slots: slot h (h = 0, 1) holds per
 // row latent bytes [256 h, 256 h + 256) at a 272-byte pitch, slot 2 the RoPE
@@ -642,10 +199,10 @@ constexpr int kQLatSlotBytes = kRows * kQLatPitch;
 constexpr int kQRopeSlotBytes = kRows * kQRopePitch;
 static_assert(kQLatSlotBytes <= kStageBytes && kQRopeSlotBytes <= kStageBytes, "a Q slot fits one stage");
 static_assert(2 * kQLatSlotBytes + kQRopeSlotBytes == kMlaQBytes, "quantised-Q layout");
-static_assert(kStageBytes % 1024 == 0 && kOffCvt % 1024 == 0 && kOffQRope % 1024 == 0 && kOffP % 1024 == 0,
-              "1 KB aligned tiles");
+static_assert(kStageBytes % 1024 == 0, "1 KB aligned stages");
 static_assert(kStageBytes == static_cast<int>(kPageTxBytes), "a page fills one stage");
 
+template <int kStages>
 struct Bars {
   uint64_t kv_full[kStages];    // stage holds its page (TMA bytes) or its Q slot (Q warps' arrival)
   uint64_t kv_empty[kStages];   // stage may be refilled
@@ -661,8 +218,12 @@ struct Bars {
   alignas(16) float scl[kStages][3][kPage];
 };
 
-constexpr size_t smem_bytes() { return kSmemData + sizeof(Bars) + 1024; }
-static_assert(smem_bytes() <= 232448, "fits the 227 KB opt-in shared memory of a CTA");
+template <bool kTwoTerm>
+constexpr size_t smem_bytes() {
+  return Layout<kTwoTerm>::kSmemData + sizeof(Bars<Layout<kTwoTerm>::kStages>) + 1024;
+}
+static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448,
+              "fits the 227 KB opt-in shared memory of a CTA");
 
 // Quantises the Q rows of sequence b into the three Q slots: latent -> E4M3(q / qs),
 // RoPE -> f16(q / qs), qs = smallest power of two with amax <= 448 qs.  kTpr
@@ -762,15 +323,20 @@ __device__ __forceinline__ void lane_group_transpose(uint4 (&pc)[N], int lane) {
 }  // namespace f8
 
 // kRowScales: per-row KV scales (prm.kv_rows) instead of the per-tensor kv_scale.
-template <bool kRowScales>
+// kTwoTerm: 16-bit dots as two-term E4M3 dots (per-tensor kv_scale only).
+template <bool kRowScales, bool kTwoTerm>
 __global__ void __launch_bounds__(f8::kThreads, 1)
     mla_fp8_kernel(const __grid_constant__ CUtensorMap tm_lat, const __grid_constant__ CUtensorMap tm_rope,
                    const MlaParams prm) {
+  static_assert(!(kRowScales && kTwoTerm), "per-row scales run with FP8 dots only");
   using namespace f8;
+  using L = Layout<kTwoTerm>;
+  constexpr int kStages = L::kStages;
+  constexpr int kOffCvt = L::kOffCvt, kOffQRope = L::kOffQRope, kOffP = L::kOffP;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  Bars* bars = reinterpret_cast<Bars*>(smem + kSmemData);
+  Bars<kStages>* bars = reinterpret_cast<Bars<kStages>*>(smem + L::kSmemData);
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -903,7 +469,8 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     // until S buffer i % 2 was read out (page i - 2), Q.K^T as 16 E4M3 MMAs
     // (latent, Q from TMEM, K = 32) and 4 f16 MMAs (RoPE, Q from shared
     // memory, K = 16), then the P.V of page i - 1 (2 E4M3 MMAs, K = 32 keys,
-    // N = 256) once its P is written.
+    // N = 256) once its P is written.  Two-term dots add 16 Q_lo MMAs to each
+    // Q.K^T and 2 P_lo MMAs to each P.V.
     {
       constexpr uint32_t idesc8 = make_idesc(0, 0, 0, 0, 64, 128);    // e4m3 x e4m3, both K-major, N = 64
       constexpr uint32_t idesc16 = make_idesc(0, 0, 0, 0, 64, 128);   // f16 x f16 (E4M3 keys are exact in f16)
@@ -912,6 +479,8 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       const bool leader = elect_one();
       const uint64_t qd = make_sdesc(smem_u32(smem + kOffQRope), 16, 1024, SWIZZLE_128B);
       const uint64_t pd = make_sdesc(smem_u32(smem + kOffP), kPLbo, kPSbo, SWIZZLE_NONE);
+      const uint64_t pd_lo = make_sdesc(smem_u32(smem + L::kOffPLo), kPLbo, kPSbo, SWIZZLE_NONE);
+      const uint64_t qlo_d = make_sdesc(smem_u32(smem + L::kOffQLo), 16, 1024, SWIZZLE_128B);
       SegmentWalker walk(prm, unit);
       Segment sg;
       int i = 0, k = 0, seg = 0;
@@ -931,6 +500,11 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         for (int kk = 0; kk < 2; ++kk)
           mma_f8_ss_if(leader, t_o, pd + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv,
                        (first && kk == 0) ? 0u : 1u);
+        if constexpr (kTwoTerm) {  // + P_lo . V
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)
+            mma_f8_ss_if(leader, t_o, pd_lo + ((kk * 2 * kPLbo) >> 4), vd + ((kk * 4096) >> 4), idesc_pv, 1u);
+        }
         tc_commit_if(leader, &bars->pv_done);
         tc_commit_if(leader, &bars->kv_empty[st]);
         ++j;
@@ -970,6 +544,12 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           for (int kk = 0; kk < 16; ++kk)
             mma_f8_ts_if(leader, t_s, tmem + kTQ + kk * 8, kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4),
                          idesc8, kk > 0 ? 1u : 0u);
+          if constexpr (kTwoTerm) {  // + Q_lo . K^T, Q_lo from shared memory
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk)
+              mma_f8_ss_if(leader, t_s, qlo_d + ((((kk >> 2) * kQLoBlock) + (kk & 3) * 32) >> 4),
+                           kd + ((((kk >> 2) * kLatBox) + (kk & 3) * 32) >> 4), idesc8, 1u);
+          }
           const uint64_t rd = make_sdesc(smem_u32(smem + kOffCvt + sbuf * kCvtBytes), 16, 1024, SWIZZLE_128B);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
@@ -1120,7 +700,34 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         for (int c = 4 * hf; c < 4 * hf + 4; ++c) *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = rope[c];
       }
       qs_out = prm.qscale[static_cast<size_t>(b_seq) * kRows + r];
-      fence_proxy_async_smem();  // the Q RoPE tile is read by the MMAs, the slots refilled by TMA
+      if constexpr (kTwoTerm) {
+        // Q_lo = E4M3(x - E4M3(x)), x = q / qs, for this half's latent bytes [256 hf, +256) of the
+        // row, from the bf16 Q (the hi term recomputed with the prep kernel's rounding), into
+        // column block x / 128 of the 128-byte-swizzled Q_lo tile; rows past R stay zero
+        const float inv_qs = __uint_as_float((254u << 23) - __float_as_uint(qs_out));  // 1 / qs, a power of two
+        const bool live = r < R;
+        const uint4* qg =
+            reinterpret_cast<const uint4*>(prm.q + (static_cast<size_t>(b_seq) * R + (live ? r : 0)) * kD) + 32 * hf;
+        uint8_t* qlo = smem + L::kOffQLo + r * 128;
+#pragma unroll 4
+        for (int c = 0; c < 16; ++c) {  // 16 values = one 16-byte chunk of Q_lo
+          const uint4 a = live ? __ldg(qg + 2 * c) : make_uint4(0, 0, 0, 0);
+          const uint4 d = live ? __ldg(qg + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+          uint32_t hi, lo[4];
+          split_e4m3x4(bf16_lo(a.x) * inv_qs, bf16_hi(a.x) * inv_qs, bf16_lo(a.y) * inv_qs, bf16_hi(a.y) * inv_qs,
+                       hi, lo[0]);
+          split_e4m3x4(bf16_lo(a.z) * inv_qs, bf16_hi(a.z) * inv_qs, bf16_lo(a.w) * inv_qs, bf16_hi(a.w) * inv_qs,
+                       hi, lo[1]);
+          split_e4m3x4(bf16_lo(d.x) * inv_qs, bf16_hi(d.x) * inv_qs, bf16_lo(d.y) * inv_qs, bf16_hi(d.y) * inv_qs,
+                       hi, lo[2]);
+          split_e4m3x4(bf16_lo(d.z) * inv_qs, bf16_hi(d.z) * inv_qs, bf16_lo(d.w) * inv_qs, bf16_hi(d.w) * inv_qs,
+                       hi, lo[3]);
+          const int x = 256 * hf + 16 * c;
+          *reinterpret_cast<uint4*>(qlo + (x >> 7) * kQLoBlock + ((((x & 127) >> 4) ^ (r & 7)) << 4)) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      fence_proxy_async_smem();  // the Q RoPE (and Q_lo) tiles are read by the MMAs, the slots refilled by TMA
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(&bars->q_full);
@@ -1222,7 +829,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         }
         const float bias = (m_run == kNegInf) ? 0.f : (kPLog2 - m_run);
         float sum = 0.f;
-        uint32_t pk[8];
+        uint32_t pk[8], pk_lo[kTwoTerm ? 8 : 1];
         if constexpr (kRowScales) {
           // P' = 2^(u_j - m) (stored, times kPScale); the row sum takes P' / sigma_j = 2^(s_j c sigma_j - m)
           const float4* iv4 = reinterpret_cast<const float4*>(bars->scl[pst][2] + 32 * hf);
@@ -1244,7 +851,10 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
             const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), c_row, bias));
             const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), c_row, bias));
             sum += (p0 + p1) + (p2 + p3);
-            pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
+            if constexpr (kTwoTerm)
+              split_e4m3x4(p0, p1, p2, p3, pk[c / 4], pk_lo[c / 4]);
+            else
+              pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
           }
         }
         l_run = l_run * alpha + sum;
@@ -1274,6 +884,11 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
           uint8_t* prow = smem + kOffP + (r >> 3) * kPSbo + (r & 7) * 16;
           *reinterpret_cast<uint4*>(prow + (2 * hf) * kPLbo) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           *reinterpret_cast<uint4*>(prow + (2 * hf + 1) * kPLbo) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          if constexpr (kTwoTerm) {  // P_lo, same layout
+            uint8_t* plo = prow + (L::kOffPLo - kOffP);
+            *reinterpret_cast<uint4*>(plo + (2 * hf) * kPLbo) = make_uint4(pk_lo[0], pk_lo[1], pk_lo[2], pk_lo[3]);
+            *reinterpret_cast<uint4*>(plo + (2 * hf + 1) * kPLbo) = make_uint4(pk_lo[4], pk_lo[5], pk_lo[6], pk_lo[7]);
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -1345,43 +960,31 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
   }
 }
 
-cudaError_t launch_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
-                       cudaStream_t stream) {
+template <bool kRowScales, bool kTwoTerm>
+cudaError_t launch_instance(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
+                            int num_units, cudaStream_t stream) {
   static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
   const cudaError_t e = configure_once(configured, [] {
-    cudaError_t e2 = cudaFuncSetAttribute(mla_fp8_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(f8::smem_bytes()));
-    if (e2 != cudaSuccess) return e2;
-    return cudaFuncSetAttribute(mla_fp8_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(f8::smem_bytes()));
+    return cudaFuncSetAttribute(mla_fp8_kernel<kRowScales, kTwoTerm>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(f8::smem_bytes<kTwoTerm>()));
   });
   if (e != cudaSuccess) return e;
-  return launch_dependent(prm.kv_rows ? mla_fp8_kernel<true> : mla_fp8_kernel<false>, dim3(num_units * 2), dim3(f8::kThreads), f8::smem_bytes(), stream, tm_lat,
-                          tm_rope, prm);
-}
-
-cudaError_t launch_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm, int num_units,
-                         cudaStream_t stream) {
-  static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
-  const cudaError_t e = configure_once(configured, [] {
-    return cudaFuncSetAttribute(mla_decode_16bit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem_bytes16()));
-  });
-  if (e != cudaSuccess) return e;
-  return launch_dependent(mla_decode_16bit_kernel, dim3(num_units * Cfg16::kParts), dim3(Cfg16::kThreads),
-                          smem_bytes16(), stream, tm_lat, tm_rope, prm);
+  return launch_dependent(mla_fp8_kernel<kRowScales, kTwoTerm>, dim3(num_units * 2), dim3(f8::kThreads),
+                          f8::smem_bytes<kTwoTerm>(), stream, tm_lat, tm_rope, prm);
 }
 
 }  // namespace mla
 
 cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                   int num_units, cudaStream_t stream) {
-  return mla::launch_fp8(tm_lat, tm_rope, prm, num_units, stream);
+  return prm.kv_rows ? mla::launch_instance<true, false>(tm_lat, tm_rope, prm, num_units, stream)
+                     : mla::launch_instance<false, false>(tm_lat, tm_rope, prm, num_units, stream);
 }
 
 cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                     int num_units, cudaStream_t stream) {
-  return mla::launch_16bit(tm_lat, tm_rope, prm, num_units, stream);
+  if (prm.kv_rows) return cudaErrorInvalidValue;
+  return mla::launch_instance<false, true>(tm_lat, tm_rope, prm, num_units, stream);
 }
 
 cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream) {

@@ -18,8 +18,8 @@ struct MlaParams {
   const int32_t* num_splits;   // [b + 1]
   uint16_t* ws_o;              // [slots, 128, 512] partial accumulators as bf16 (true units)
   float2* ws_ml;               // [slots, 128] (m in log2 units, l)
-  uint8_t* qbuf;               // [b, kMlaQBytes] Q quantised for FP8 dots, in the kernel's slot layout
-  float* qscale;               // [b, 128] per-row power-of-two Q scale (FP8 dots)
+  uint8_t* qbuf;               // [b, kMlaQBytes] Q quantised to E4M3 (its hi term for 16-bit dots), in the kernel's slot layout
+  float* qscale;               // [b, 128] per-row power-of-two Q scale
   uint16_t* out;               // bf16 [b, s_q, h_q, 512]
   float* lse;                  // [b, s_q, h_q]
   float softmax_scale;
@@ -40,7 +40,8 @@ constexpr int kMlaQBytes = 88064;
 constexpr size_t kMetadataMaxSmem = 200 * 1024;  // the scheduler stages ~16 bytes per sequence and unit
 size_t metadata_smem_bytes(int b, int num_units);
 
-// dense MLA decode kernels (mla_decode.cu)
+// dense MLA decode kernels (mla_decode.cu): FP8 dots (per-tensor or per-row
+// scales), 16-bit dots as two-term E4M3 dots (per-tensor scale)
 cudaError_t launch_mla_decode_fp8(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                                   int num_units, cudaStream_t stream);
 cudaError_t launch_mla_decode_16bit(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
@@ -56,20 +57,21 @@ void mla_read_and_clear_timeout_site(uint32_t where[3]);
 // fault_page = p + 1 makes CTA 0 of work unit 0 skip the loads of its p-th page
 // (0 = off); wait_limit_ns replaces the wait limit (0 = the default).
 cudaError_t mla_set_wait_test(int fault_page, uint64_t wait_limit_ns);
-// Quantises every sequence's Q rows for FP8 dots into prm.qbuf / prm.qscale
-// (launched right before launch_mla_decode_fp8, as a programmatic dependent).
+// Quantises every sequence's Q rows into prm.qbuf / prm.qscale (launched
+// right before the decode kernel of either dot mode, as a programmatic dependent).
 cudaError_t launch_mla_qprep(const MlaParams& prm, cudaStream_t stream);
 
 // metadata + combine (metadata.cu)
 cudaError_t launch_mla_metadata(const int32_t* seqlens, int b, int num_units, int force_splits, int32_t* tile_sched,
                                 int32_t* num_splits, cudaStream_t stream);
-// Merges split partials into out / lse, and (FP8 dots: q, the bf16 queries,
-// and qscale, their per-row power-of-two scales, non-null) applies the
-// first-order Q-quantisation correction to every row's LSE from the finished
-// output row and q_hat - q, recomputed with the prep kernel's rounding.
+// Merges split partials into out / lse, and (q, the bf16 queries, and qscale,
+// their per-row power-of-two scales, non-null) applies the first-order
+// Q-quantisation correction to every row's LSE from the finished output row
+// and q_hat - q, recomputed with the decode kernel's rounding: one E4M3 term
+// (FP8 dots) or two (two_term, 16-bit dots).
 cudaError_t launch_mla_combine(const int32_t* num_splits, const uint16_t* ws_o, const float2* ws_ml,
-                               const uint16_t* q, const float* qscale, float softmax_scale, uint16_t* out,
-                               float* lse, int b, int rows, cudaStream_t stream);
+                               const uint16_t* q, const float* qscale, bool two_term, float softmax_scale,
+                               uint16_t* out, float* lse, int b, int rows, cudaStream_t stream);
 uint32_t metadata_read_and_clear_status();
 
 }  // namespace fp8mla

@@ -107,14 +107,13 @@ extern "C" fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
   prm.b = b;
   prm.s_q = s_q;
   prm.h_q = h_q;
-  cudaError_t e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_qprep(prm, s) : cudaSuccess;
+  cudaError_t e = launch_mla_qprep(prm, s);
   if (e == cudaSuccess)
     e = (dot_mode == FP8MLA_DOT_FP8) ? launch_mla_decode_fp8(tm_lat, tm_rope, prm, units, s)
                                      : launch_mla_decode_16bit(tm_lat, tm_rope, prm, units, s);
   if (e != cudaSuccess) return FP8MLA_ERR_CUDA;
-  if (launch_mla_combine(num_splits, nullptr, nullptr, dot_mode == FP8MLA_DOT_FP8 ? prm.q : nullptr,
-                         dot_mode == FP8MLA_DOT_FP8 ? qscale : nullptr, softmax_scale, prm.out, lse, b, s_q * h_q,
-                         s) != cudaSuccess)
+  if (launch_mla_combine(num_splits, nullptr, nullptr, prm.q, qscale, dot_mode == FP8MLA_DOT_16BIT, softmax_scale,
+                         prm.out, lse, b, s_q * h_q, s) != cudaSuccess)
     return FP8MLA_ERR_CUDA;
   return FP8MLA_OK;
 }

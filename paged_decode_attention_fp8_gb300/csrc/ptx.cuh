@@ -462,6 +462,15 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t x, uint32_t& lo, uint3
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 
+// Two-term E4M3 split of four floats: hi = E4M3(x), lo = E4M3(x - hi) (x - hi
+// is exact in f32).  hi + lo carries about 8 significant bits of x, bf16's
+// precision, for |x| >= 2^-6; below that the terms are E4M3 subnormals.
+__device__ __forceinline__ void split_e4m3x4(float a, float b, float c, float d, uint32_t& hi, uint32_t& lo) {
+  hi = pack_e4m3x4(a, b, c, d);
+  const uint32_t h01 = e4m3x2_to_f16x2(hi & 0xFFFFu), h23 = e4m3x2_to_f16x2(hi >> 16);
+  lo = pack_e4m3x4(a - f16_lo(h01), b - f16_hi(h01), c - f16_lo(h23), d - f16_hi(h23));
+}
+
 // 4-byte global -> shared copy that does not go through registers; completes
 // for this thread at cp_async_wait_all
 __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
