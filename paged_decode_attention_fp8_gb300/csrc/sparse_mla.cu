@@ -176,6 +176,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   griddep_wait();  // inputs may come from the previous kernel in the stream
+  // The first step's indices (gather warps) and Q (softmax warps) are loaded
+  // before the block-wide barrier, so their latency overlaps it.
+  const int32_t* idx_t = prm.idx + static_cast<size_t>(t) * prm.topk;
+  auto load_idx = [&](int ch, int (&v)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = (c0 + ch) * kKeys + 4 * lane + q;
+      v[q] = k < prm.topk ? __ldg(idx_t + k) : -1;
+    }
+  };
+  int raw[4] = {-1, -1, -1, -1};
+  if ((warp == 0 || warp == 2 || warp == 3) && nchunks > 0) load_idx(0, raw);
+  uint4 qv[8];
+  if (warp >= 4) {
+    const int qh = (threadIdx.x - 128) / 8, qj = (threadIdx.x - 128) % 8;
+    const uint4* qsrc = reinterpret_cast<const uint4*>(prm.q + (static_cast<size_t>(t) * prm.h_q + qh) * kD + qj * 64);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) qv[c] = qh < prm.h_q ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -195,16 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cw = warp - 2;  // copy warp 0 or 1 (warp 0: the TMA warp)
     const int cb = lane / 8, cc = lane % 8;
     if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_rows);
-    const int32_t* idx_t = prm.idx + static_cast<size_t>(t) * prm.topk;
-    auto load_idx = [&](int ch, int (&v)[4]) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int k = (c0 + ch) * kKeys + 4 * lane + q;
-        v[q] = k < prm.topk ? __ldg(idx_t + k) : -1;
-      }
-    };
-    int raw[4] = {-1, -1, -1, -1};
-    if (nchunks > 0) load_idx(0, raw);
     int i = 0;
     for (; i < nchunks; ++i) {
       const int st = i % kStages, use = i / kStages;
@@ -310,17 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       return ok;
     };
     const float kv_scale = *prm.kv_scale;
-    const uint16_t* qtok = prm.q + static_cast<size_t>(t) * prm.h_q * kD;
 
-    // Q: thread (head qh, eighth qj) quantises dims [64 qj, 64 qj + 64).
+    // Q: thread (head qh, eighth qj) quantises dims [64 qj, 64 qj + 64) (loaded above).
     {
       const int qh = r / 8, qj = r % 8;
-      uint4 v[8];
+      const uint4* v = qv;
       float amax = 0.f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        v[c] = qh < prm.h_q ? __ldg(reinterpret_cast<const uint4*>(qtok + qh * kD + qj * 64) + c)
-                            : make_uint4(0, 0, 0, 0);
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v[c].x)), fabsf(bf16_hi(v[c].x))),
                                  fmaxf(fabsf(bf16_lo(v[c].y)), fabsf(bf16_hi(v[c].y)))));
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v[c].z)), fabsf(bf16_hi(v[c].z))),

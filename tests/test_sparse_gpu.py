@@ -72,6 +72,32 @@ def test_skipped_and_ragged_indices():
     assert fm.last_device_error() == 0
 
 
+@pytest.mark.parametrize("splits", [2, 3, 5, 8, 9, 16])
+def test_split_counts(splits):
+    # every split count up to one per 128-key chunk, counts that do not
+    # divide the 16 chunks evenly included
+    inp = syn.sparse_inputs(14, 2)
+    out, lse = run(inp, num_splits=splits)
+    ro, rl = ref(inp)
+    m = compare(out, lse, ro, rl, "fp8")
+    record(f"sparse_sq2_splits{splits}_counts", m)
+    assert_close(m, "fp8")
+    assert fm.last_device_error() == 0
+
+
+def test_split_merge_empty_shards_and_fewer_heads():
+    # 4 splits where one token has no key at all and another has keys in its
+    # first shard only, with 5 heads
+    inp = syn.sparse_inputs(15, 3, h_q=5, num_tokens=6000, topk=512)
+    idx = inp.topk_idx.clone()
+    idx[0, :] = -1
+    idx[1, 128:] = -1
+    out, lse = run(inp, num_splits=4, idx=idx)
+    ro, rl = ref(inp, idx)
+    assert_close(compare(out, lse, ro, rl, "fp8"), "fp8")
+    assert fm.last_device_error() == 0
+
+
 @pytest.mark.parametrize("s_q,splits", [(38, 4), (48, 4), (3, 24)])
 def test_split_merge_more_tokens_and_many_splits(s_q, splits):
     # more CTAs than SMs (48 x 4), and more than 16 splits per token (the
