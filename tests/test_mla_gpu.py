@@ -218,10 +218,12 @@ def test_bad_page_index_is_reported_not_faulted():
     assert fm.last_device_error() == 0   # read-and-clear
 
 
-def test_q_written_just_before_the_call_is_seen():
+@pytest.mark.parametrize("mode", MODES)
+def test_q_written_just_before_the_call_is_seen(mode):
     # Q is produced by a torch kernel on the same stream right before the
-    # FP8-dot call (as a projection GEMM would leave it): the call's first
-    # kernel must wait for that write before it reads Q
+    # call (as a projection GEMM would leave it): the call's first kernel
+    # must wait for that write before it reads Q, and the decode kernel
+    # (which reads the bf16 Q again for 16-bit dots) after it
     inp = syn.mla_inputs(14, 8, 2, 64, syn.uniform_seqlens(14, 8, 100, 3000), causal=True)
     d = to_dev(inp)
     src = d["q"].clone()
@@ -232,6 +234,6 @@ def test_q_written_just_before_the_call_is_seen():
         torch.cuda.synchronize()
         q.add_(src * 1.0)  # two torch kernels, enqueued just ahead of the decode
         out, lse = fm.decode(q, d["kv"], d["bt"], d["sl"], d["scale"], inp.softmax_scale, True, ts, ns,
-                             dot_mode="fp8")
+                             dot_mode=mode)
         torch.cuda.synchronize()
-        assert_close(compare(out, lse, ro, rl, "fp8"), "fp8")
+        assert_close(compare(out, lse, ro, rl, mode), mode)
