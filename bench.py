@@ -602,10 +602,11 @@ def leg_gqa(dev, peaks, steps, warmup, variant="plain"):
         cfg.update(dot="e4m3 operands, Q and P as two E4M3 terms", scales="per tensor")
         what = "bs=32, 32/8 heads, hd 128, ctx U[1024,16384]"
     elif variant == "rows":
-        cfg.update(dot="f16", scales="per row [num_blocks, h_kv, 16], base 2^U[-2,2]")
+        cfg.update(dot="e4m3 operands, Q and P as two E4M3 terms", scales="per row [num_blocks, h_kv, 16], base 2^U[-2,2]")
         what = "bs=32, 32/8 heads, hd 128, ctx U[1024,16384], per-row KV scales"
     else:
-        cfg.update(dot="f16", scales="per tensor", q_len=q_len, mask="seeded block mask", window=window,
+        cfg.update(dot="e4m3 operands, Q and P as two E4M3 terms", scales="per tensor", q_len=q_len,
+                   mask="seeded block mask", window=window,
                    sinks="seeded logits U[-2,6]")
         what = "bs=32, 32/8 heads, hd 128, ctx U[1024,16384], 4-token speculative block, window 4096, sinks"
     return _leg_result(f"paged GQA decode us/call ({what})", avg, ms, nbytes, 0.0, flops, peaks, cfg,

@@ -138,8 +138,12 @@ struct Smem {
   uint32_t tmem_base, abort_flag;
   float qs[kN];
   uint16_t vis_block[kN];  // per query token: bit c = key c of the speculative block visible
-  float red[2][4][kN];     // per-warp partial maxima, double-buffered by step parity
+  // per-warp partial maxima; written only in a step whose vote passed, between that step's
+  // two exchanges, so every reader of an earlier step is done with it (one buffer)
+  float red[4][kN];
   float red2[4][kN];
+  uint32_t grow[2][4];     // per warp: a score above its column's reference + tau (by step parity:
+                           // a step without a second exchange leaves no barrier before the next vote)
 };
 
 constexpr size_t kSmemBytes = kStages * kRawStageBytes + kQBytes + 2 * kPBytes + sizeof(Smem) + 1024;
@@ -199,8 +203,8 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < x2::kStages; ++s) {
-      mbar_init(&sm->raw_full[s], 1);
-      mbar_init(&sm->raw_empty[s], 1);  // the P.V that read the step's V
+      mbar_init(&sm->raw_full[s], kRows ? 33 : 1);  // the TMA bytes' arrival (+ per-row scales: one per lane)
+      mbar_init(&sm->raw_empty[s], 1);             // the P.V that read the step's V
     }
     for (int bf = 0; bf < 2; ++bf) {
       mbar_init(&sm->s_full[bf], 1);
@@ -252,26 +256,35 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       int rows[kPagesPerStep];
 #pragma unroll
       for (int p = 0; p < kPagesPerStep; ++p) rows[p] = (__shfl_sync(0xffffffffu, mine, p) * prm.h_kv + kvh) * kPage;
+      const int scale_row = (__shfl_sync(0xffffffffu, mine, lane / 4) * prm.h_kv + kvh) * kPage;  // page lane / 4
       bool ok = true;
       if (lane == 0) {
         ok = use == 0 || wait_bounded(&sm->raw_empty[st], (use - 1) & 1, abort_flag, &g_status_gqa);
         if (ok) {
-          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd + (kRows ? 2u * np * kPage * 4u : 0u));
+          mbar_arrive_expect_tx(&sm->raw_full[st], 2u * np * kPage * kHd);
           uint8_t* sb = smem + st * kRawStageBytes;
 #pragma unroll
           for (int p = 0; p < kPagesPerStep; ++p) {
             if (p >= np) break;
             tma_load_3d(sb + kOffRawK + p * kPage * kHd, &tm_k, &sm->raw_full[st], 0, rows[p], 0);
             tma_load_3d(sb + kOffRawV + p * kPage * kHd, &tm_v, &sm->raw_full[st], 0, rows[p], 0);
-            if constexpr (kRows) {  // the page's 16 row scales of K and of V (rows are the scales' index too)
-              bulk_load(&sm->row_scale[st][0][p * kPage], prm.k_scale + rows[p], kPage * 4u, &sm->raw_full[st]);
-              bulk_load(&sm->row_scale[st][1][p * kPage], prm.v_scale + rows[p], kPage * 4u, &sm->raw_full[st]);
-            }
           }
         }
       }
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      if constexpr (kRows) {
+        // the step's row scales (rows are the scales' index too), 16 bytes a lane by cp.async
+        // rather than 16 small bulk copies through the TMA unit: lane l copies scales
+        // [4 (l % 4), +4) of page l / 4, of K and of V, and arrives once they land
+        const int p = lane / 4, c = lane % 4;
+        if (p < np) {
+          cp_async16(smem_u32(&sm->row_scale[st][0][p * kPage + 4 * c]), prm.k_scale + scale_row + 4 * c, 16u);
+          cp_async16(smem_u32(&sm->row_scale[st][1][p * kPage + 4 * c]), prm.v_scale + scale_row + 4 * c, 16u);
+        }
+        cp_async_mbar_arrive(&sm->raw_full[st]);
+      }
     }
+    if constexpr (kRows) cp_async_wait_all();  // this lane's copies have landed before the CTA can exit
     if (lane == 0)
       for (int j = max(0, i - x2::kStages); j < i; ++j)
         wait_bounded(&sm->raw_full[j % x2::kStages], (j / x2::kStages) & 1, nullptr, &g_status_gqa);
@@ -448,13 +461,14 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       for (int h = 0; h < kG; ++h)
         v[h] = ((colvis >> h) & 1u) ? (__uint_as_float(s[h]) + __uint_as_float(s[kN + h])) * c_h[h] * sk + lsv
                                     : kNegInf;
+      // The reference m_h of a column moves only when a score passes it by more
+      // than tau, so one vote decides whether the column maxima are needed at
+      // all: most steps after a CTA's first skip the per-column reductions.
+      bool grow = false;
 #pragma unroll
-      for (int h = 0; h < kG; ++h) {
-        float x = v[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (lane == 0) sm->red[i & 1][w][h] = x;
-      }
+      for (int h = 0; h < kG; ++h) grow |= v[h] > m_h[h] + x2::kTau;
+      grow = __any_sync(0xffffffffu, grow);
+      if (lane == 0) sm->grow[i & 1][w] = grow ? 1u : 0u;
       if (!xsync()) {
         ok = false;
         break;
@@ -462,14 +476,28 @@ __global__ void __launch_bounds__(x2::kThreads, 2)
       float alpha[kG];
       bool any_rescale = false;
 #pragma unroll
-      for (int h = 0; h < kG; ++h) {
-        const float* rm = &sm->red[i & 1][0][0];
-        const float mx = fmaxf(fmaxf(rm[h], rm[kN + h]), fmaxf(rm[2 * kN + h], rm[3 * kN + h]));
-        alpha[h] = 1.f;
-        if (mx > m_h[h] + x2::kTau) {
-          alpha[h] = ex2_approx(m_h[h] - mx);
-          any_rescale |= (i > 0);
-          m_h[h] = mx;
+      for (int h = 0; h < kG; ++h) alpha[h] = 1.f;
+      if ((sm->grow[i & 1][0] | sm->grow[i & 1][1] | sm->grow[i & 1][2] | sm->grow[i & 1][3]) != 0u) {
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+          float x = v[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+          if (lane == 0) sm->red[w][h] = x;
+        }
+        if (!xsync()) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+          const float* rm = &sm->red[0][0];
+          const float mx = fmaxf(fmaxf(rm[h], rm[kN + h]), fmaxf(rm[2 * kN + h], rm[3 * kN + h]));
+          if (mx > m_h[h] + x2::kTau) {
+            alpha[h] = ex2_approx(m_h[h] - mx);
+            any_rescale |= (i > 0);
+            m_h[h] = mx;
+          }
         }
       }
       uint8_t phi[kG], plo[kG];
