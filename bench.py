@@ -370,7 +370,6 @@ def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, worl
     ts = torch.empty((units, 8), dtype=torch.int32, device=dev)
     ns = torch.empty((b + 1,), dtype=torch.int32, device=dev)
     ws = torch.empty((fm.workspace_bytes(b, s_q, h_q, units),), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
     h2d_s = torch.cuda.Stream(dev)
     d2h_s = torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(nbuf)]    # a slot's inputs are on the device
@@ -378,18 +377,18 @@ def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, worl
     ev_out = [torch.cuda.Event() for _ in range(nbuf)]   # a slot's results are back on the host
     steps = max(args.steps // 10, 20)
 
-    def step(i):
+    def step(i, stream, first):
         k = i % nbuf
         _, kv = sets[i % len(sets)]
         with torch.cuda.stream(h2d_s):
-            if i >= nbuf:
+            if not first:
                 h2d_s.wait_event(ev_done[k])  # the decode two steps back has read this slot
             q_d[k].copy_(q_h, non_blocking=True)
             bt_d[k].copy_(bt_h, non_blocking=True)
             sl_d[k].copy_(sl_h, non_blocking=True)
             ev_in[k].record(h2d_s)
         stream.wait_event(ev_in[k])
-        if i >= nbuf:
+        if not first:
             stream.wait_event(ev_out[k])  # this slot's previous results have left the device
         fm.get_metadata(sl_d[k], h_q, s_q, num_units=units, tile_sched=ts, num_splits=ns)
         fm.decode(q_d[k], kv, bt_d[k], sl_d[k], scale, inp.softmax_scale, True, ts, ns, dot_mode=args.dot,
@@ -401,27 +400,63 @@ def measure_e2e(args, inp, seqlens, sets, bt, sl, scale, dev, units, flops, worl
             lse_h[k].copy_(lse[k], non_blocking=True)
             ev_out[k].record(d2h_s)
 
+    def timed(run, n_steps, stream):
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        h2d_s.wait_event(t0)
+        d2h_s.wait_event(t0)
+        host0 = time.perf_counter()
+        run()
+        host_us = (time.perf_counter() - host0) * 1e6 / n_steps
+        stream.wait_stream(h2d_s)  # the timed region ends when the last results are on the host
+        stream.wait_stream(d2h_s)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return slowest_rank_ms(t0.elapsed_time(t1), world, dev) / n_steps, host_us
+
+    # eager: every step's copies, calls and events enqueued from Python
+    stream = torch.cuda.current_stream(dev)
     for i in range(3):
-        step(i)
-    torch.cuda.synchronize()
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    h2d_s.wait_event(t0)
-    for i in range(steps):
-        step(i)
-    for k in range(nbuf):  # the timed region ends when the last results are on the host
-        stream.wait_event(ev_out[k])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    ms = slowest_rank_ms(t0.elapsed_time(t1), world, dev) / steps
+        step(i, stream, i < nbuf)
+    eager_ms, eager_host_us = timed(lambda: [step(i, stream, False) for i in range(steps)], steps, stream)
+
+    # graph: the same calls captured once as a chain of `per_graph` steps and replayed, so
+    # that Python's per-call cost leaves the loop (every step still copies its own inputs in
+    # and its own results out); consecutive replays run one after another
+    per_graph = 50
+    replays = max(1, steps // per_graph)
+    graph_ms = graph_host_us = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            h2d_s.wait_stream(cap)
+            d2h_s.wait_stream(cap)
+            for i in range(per_graph):
+                step(i, cap, i < nbuf)
+            cap.wait_stream(h2d_s)
+            cap.wait_stream(d2h_s)
+        for _ in range(2):
+            g.replay()
+        graph_ms, graph_host_us = timed(lambda: [g.replay() for _ in range(replays)], replays * per_graph, stream)
+    except Exception as exc:  # capture unsupported here: report the eager loop alone
+        print(f"e2e graph capture failed: {exc!r}", file=sys.stderr)
+    use_graph = graph_ms is not None and graph_ms < eager_ms
+    ms = graph_ms if use_graph else eager_ms
     h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
     d2h = out_h[0].numel() * 2 + lse_h[0].numel() * 4
     return dict(value=round(whole_job_tflops(world, flops, ms), 2), unit="TFLOPS", ms_per_step=round(ms, 5),
-                h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h), steps=steps,
+                h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
+                steps=replays * per_graph if use_graph else steps,
+                launch="cuda graph of %d steps, replayed" % per_graph if use_graph else "eager",
+                eager_ms_per_step=round(eager_ms, 5), eager_host_us_per_step=round(eager_host_us, 1),
+                graph_ms_per_step=None if graph_ms is None else round(graph_ms, 5),
                 note="KV cache resident in HBM; per-step Q/block table/seqlens in, out/lse back, on two copy "
                      "streams overlapping the neighbouring steps' compute (double-buffered)")
 
