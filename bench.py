@@ -246,8 +246,10 @@ def run_ours(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
+    host0 = time.perf_counter()
     for i in range(args.steps):
         step(i)
+    host_us = (time.perf_counter() - host0) * 1e6 / args.steps  # below the step time: the loop is GPU-bound
     t1.record(stream)
     torch.cuda.synchronize()
     # The decode call's own duration: the same steps again with events around
@@ -323,6 +325,7 @@ def run_ours(args):
                        parallelism=f"replicas x{world}"),
         "us_per_call": round(dec_avg_ms * 1e3, 2),
         "us_per_step": round(ms_per_step * 1e3, 2),
+        "host_enqueue_us_per_step": round(host_us, 1),
         "tflops_decode_call": round(flops / (dec_avg_ms * 1e-3) / 1e12, 1),
         "kv_gbs": round(kv_bytes / (dec_avg_ms * 1e-3) / 1e9, 1),
         "roofline": roofline,
