@@ -490,7 +490,38 @@ def _time_calls(call, steps, warmup, stream):
     torch.cuda.synchronize()
     assert fm.last_device_error() == 0
     ms = sorted(a.elapsed_time(b) for a, b in evs)
+    _graph_time.last = _graph_replay_ms(call, warmup + steps, stream)
     return sum(ms) / len(ms), ms
+
+
+def _graph_replay_ms(call, base, stream, per_graph=20, replays=10):
+    """Per-call device time of `per_graph` calls captured as one CUDA graph and replayed
+    back to back (no host enqueue in the timed region), or None if capture fails here."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(per_graph):
+                call(base + i)
+        g.replay()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / (per_graph * replays)
+    except Exception as exc:
+        print(f"graph timing unavailable: {exc!r}", file=sys.stderr)
+        return None
+
+
+class _graph_time:  # the last _time_calls' graph-replayed per-call time (ms), for _leg_result
+    last = None
 
 
 def _leg_result(metric, avg_ms, ms, nbytes, flops_fp8, flops_16, peaks, cfg, launches):
@@ -500,6 +531,7 @@ def _leg_result(metric, avg_ms, ms, nbytes, flops_fp8, flops_16, peaks, cfg, lau
     achieved = nbytes / (avg_ms * 1e-3) / 1e9
     return {
         "metric": metric, "value": round(avg_ms * 1e3, 2), "unit": "us/call", "higher_is_better": False,
+        "graph_us_per_call": None if _graph_time.last is None else round(_graph_time.last * 1e3, 2),
         "config": cfg, "p10_us": round(ms[len(ms) // 10] * 1e3, 2),
         "p90_us": round(ms[(9 * len(ms)) // 10] * 1e3, 2), "calls": len(ms),
         "tflops": round(flops / (avg_ms * 1e-3) / 1e12, 2) if flops else None,
