@@ -389,6 +389,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
       tma_prefetch_desc(&tm_lat);
       tma_prefetch_desc(&tm_rope);
     }
+    const uint64_t kv_policy = l2_evict_first_policy();
     // bounded-wait test hook: CTA 0 of unit 0 never loads its page (g_fault_page - 1) of the unit
     const int fault = (unit == 0 && part == 0) ? *reinterpret_cast<volatile int*>(&g_fault_page) : 0;
     int upg = 0;  // the unit's pages so far
@@ -439,8 +440,12 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
               uint8_t* sb = smem + st * kStageBytes;
               mbar_arrive_expect_tx(&bars->kv_full[st], kPageTxBytes + (kRowScales ? kPage * 4u : 0u));
 #pragma unroll
-              for (int q = 0; q < 4; ++q) tma_load_3d(sb + q * kLatBox, &tm_lat, &bars->kv_full[st], q * 128, 0, phys);
-              tma_load_3d(sb + kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys);
+              // pages are streamed once (the unit's other CTA reads them at about the same time): evict
+              // them first, keeping Q, the quantised Q and the split partials in L2 for the other kernels
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                tma_load_3d_hint(sb + q * kLatBox, &tm_lat, &bars->kv_full[st], q * 128, 0, phys, kv_policy);
+              tma_load_3d_hint(sb + kOffRope8, &tm_rope, &bars->kv_full[st], kDLat, 0, phys, kv_policy);
               if constexpr (kRowScales)  // the page's 64 row scales (256 bytes)
                 bulk_load(&bars->scl[st][0][0], prm.kv_rows + static_cast<size_t>(phys) * kPage, kPage * 4u,
                           &bars->kv_full[st]);
