@@ -171,9 +171,10 @@ constexpr int kQLoBlock = kRows * 128;             // one 128-byte column block 
 // matrices: row group g and 16-byte key chunk c at g * kPSbo + c * kPLbo.
 // Two-term dots add P_lo (P's layout) and Q_lo: 128 rows x 512 E4M3 as four
 // column blocks of kQLoBlock, each 128-byte swizzled (the K page's layout).
-template <bool kTwoTerm>
+template <bool kTwoTerm, bool kRowScales = false>
 struct Layout {
-  static constexpr int kStages = kTwoTerm ? 3 : 5;
+  // per-row scales give up a stage for the partner-maximum exchange (PairExchange)
+  static constexpr int kStages = kTwoTerm ? 3 : (kRowScales ? 4 : 5);
   static constexpr int kOffCvt = kStages * kStageBytes;
   static constexpr int kOffQRope = kOffCvt + 2 * kCvtBytes;
   static constexpr int kOffP = kOffQRope + kRows * 128;
@@ -202,8 +203,19 @@ static_assert(2 * kQLatSlotBytes + kQRopeSlotBytes == kMlaQBytes, "quantised-Q l
 static_assert(kStageBytes % 1024 == 0, "1 KB aligned stages");
 static_assert(kStageBytes == static_cast<int>(kPageTxBytes), "a page fills one stage");
 
-template <int kStages>
-struct Bars {
+// Per-row scales: the two threads of a query row (warps w and w + 4) swap the
+// maximum of their half of a page's scaled scores instead of each scaling the
+// other half too.
+template <bool kOn>
+struct PairExchange {};
+template <>
+struct PairExchange<true> {
+  uint64_t pair[4];         // per row block: both warps of a row block published their half's maximum
+  float pmax[2][2][kRows];  // by page parity, half, row
+};
+
+template <int kStages, bool kPair = false>
+struct Bars : PairExchange<kPair> {
   uint64_t kv_full[kStages];    // stage holds its page (TMA bytes) or its Q slot (Q warps' arrival)
   uint64_t kv_empty[kStages];   // stage may be refilled
   uint64_t cvt_ready[kStages];  // the page's RoPE part is converted and its dead rows zeroed
@@ -218,11 +230,12 @@ struct Bars {
   alignas(16) float scl[kStages][3][kPage];
 };
 
-template <bool kTwoTerm>
+template <bool kTwoTerm, bool kRowScales = false>
 constexpr size_t smem_bytes() {
-  return Layout<kTwoTerm>::kSmemData + sizeof(Bars<Layout<kTwoTerm>::kStages>) + 1024;
+  return Layout<kTwoTerm, kRowScales>::kSmemData + sizeof(Bars<Layout<kTwoTerm, kRowScales>::kStages, kRowScales>) +
+         1024;
 }
-static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448,
+static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448 && smem_bytes<false, true>() <= 232448,
               "fits the 227 KB opt-in shared memory of a CTA");
 
 // Quantises the Q rows of sequence b into the three Q slots: latent -> E4M3(q / qs),
@@ -330,13 +343,13 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
                    const MlaParams prm) {
   static_assert(!(kRowScales && kTwoTerm), "per-row scales run with FP8 dots only");
   using namespace f8;
-  using L = Layout<kTwoTerm>;
+  using L = Layout<kTwoTerm, kRowScales>;
   constexpr int kStages = L::kStages;
   constexpr int kOffCvt = L::kOffCvt, kOffQRope = L::kOffQRope, kOffP = L::kOffP;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  Bars<kStages>* bars = reinterpret_cast<Bars<kStages>*>(smem + L::kSmemData);
+  Bars<kStages, kRowScales>* bars = reinterpret_cast<Bars<kStages, kRowScales>*>(smem + L::kSmemData);
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x / 32;
@@ -356,6 +369,8 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
     mbar_init(&bars->q_full, kSoftmaxThreads / 32);
     mbar_init(&bars->final_mma, 1);
     mbar_init(&bars->xchg, kSoftmaxThreads / 32);
+    if constexpr (kRowScales)
+      for (int w4 = 0; w4 < 4; ++w4) mbar_init(&bars->pair[w4], 2);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
@@ -767,9 +782,9 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
         tc_fence_after();
         // Both halves of the row are read: the other half only for the row max,
         // so each warp takes the max of all 64 keys without waiting on its partner.
-        uint32_t s[32], so[32];
+        uint32_t s[32], so[kRowScales ? 1 : 32];
         tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * hf, s);
-        tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * (1 - hf), so);
+        if constexpr (!kRowScales) tmem_ld32(lane_base + kTS + sbuf * kPage + 32 * (1 - hf), so);
         // per-row scales: the page's stage (its slot follows the segment's three Q slots); its
         // conversion barrier covers the scale arrays, and its phase is this page's (the stage is
         // refilled only after this page's P.V)
@@ -788,9 +803,11 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             if (base + c >= visible) s[c] = __float_as_uint(kNegInf);
-            if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
+            if constexpr (!kRowScales)
+              if (base_o + c >= visible) so[c] = __float_as_uint(kNegInf);
           }
         }
+        float mx;
         if constexpr (kRowScales) {
           // u_j = s_j c sigma_j + log2 sigma_j: the key's score with its K scale, plus its V scale's
           // log, so that P' = 2^(u_j - m) carries sigma_j (masked keys stay -inf)
@@ -804,27 +821,41 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
             v[3] = __float_as_uint(fmaf(__uint_as_float(v[3]), c_row * g.w, l.w));
           };
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            scale4(s + 4 * c4, sg4[8 * hf + c4], lg4[8 * hf + c4]);
-            scale4(so + 4 * c4, sg4[8 * (1 - hf) + c4], lg4[8 * (1 - hf) + c4]);
+          for (int c4 = 0; c4 < 8; ++c4) scale4(s + 4 * c4, sg4[8 * hf + c4], lg4[8 * hf + c4]);
+          // this half's maximum, swapped with the row's other thread (warp w + 4 or w - 4) through the
+          // pair barrier; both then take the same row maximum
+          float m11[11];
+#pragma unroll
+          for (int c = 0; c < 10; ++c)
+            m11[c] = fmax3(__uint_as_float(s[3 * c]), __uint_as_float(s[3 * c + 1]), __uint_as_float(s[3 * c + 2]));
+          m11[10] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
+          const float m_own = fmax3(fmax3(m11[0], m11[1], m11[2]), fmax3(m11[3], m11[4], m11[5]),
+                                    fmax3(fmax3(m11[6], m11[7], m11[8]), m11[9], m11[10]));
+          bars->pmax[i & 1][hf][r] = m_own;
+          warp_arrive(&bars->pair[warp % 4]);
+          if (!warp_spin(&bars->pair[warp % 4], i & 1, abort_flag, __LINE__)) {
+            ok = false;
+            break;
           }
-        }
-        // row max of the 64 scores as a tree of three-way maxima
-        float m22[22];
+          mx = fmaxf(m_own, bars->pmax[i & 1][1 - hf][r]);
+        } else {
+          // row max of the 64 scores as a tree of three-way maxima
+          float m22[22];
 #pragma unroll
-        for (int c = 0; c < 10; ++c) {
-          m22[c] = fmax3(__uint_as_float(s[3 * c]), __uint_as_float(s[3 * c + 1]), __uint_as_float(s[3 * c + 2]));
-          m22[10 + c] =
-              fmax3(__uint_as_float(so[3 * c]), __uint_as_float(so[3 * c + 1]), __uint_as_float(so[3 * c + 2]));
-        }
-        m22[20] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
-        m22[21] = fmaxf(__uint_as_float(so[30]), __uint_as_float(so[31]));
-        float m8[8];
+          for (int c = 0; c < 10; ++c) {
+            m22[c] = fmax3(__uint_as_float(s[3 * c]), __uint_as_float(s[3 * c + 1]), __uint_as_float(s[3 * c + 2]));
+            m22[10 + c] =
+                fmax3(__uint_as_float(so[3 * c]), __uint_as_float(so[3 * c + 1]), __uint_as_float(so[3 * c + 2]));
+          }
+          m22[20] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
+          m22[21] = fmaxf(__uint_as_float(so[30]), __uint_as_float(so[31]));
+          float m8[8];
 #pragma unroll
-        for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
-        m8[7] = m22[21];
-        const float m3a = fmax3(m8[0], m8[1], m8[2]), m3b = fmax3(m8[3], m8[4], m8[5]);
-        const float mx = fmax3(m3a, m3b, fmaxf(m8[6], m8[7])) * (kRowScales ? 1.f : c_row);  // c_row > 0; both warps agree
+          for (int c = 0; c < 7; ++c) m8[c] = fmax3(m22[3 * c], m22[3 * c + 1], m22[3 * c + 2]);
+          m8[7] = m22[21];
+          const float m3a = fmax3(m8[0], m8[1], m8[2]), m3b = fmax3(m8[3], m8[4], m8[5]);
+          mx = fmax3(m3a, m3b, fmaxf(m8[6], m8[7])) * c_row;  // c_row > 0; both warps agree
+        }
         float alpha = 1.f;
         bool rescale = false;
         if (mx > m_run + kTau) {
@@ -845,7 +876,7 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
             const float p2 = ex2_approx(__uint_as_float(s[c + 2]) + bias);
             const float p3 = ex2_approx(__uint_as_float(s[c + 3]) + bias);
             const float4 iv = iv4[c / 4];
-            sum += (p0 * iv.x + p1 * iv.y) + (p2 * iv.z + p3 * iv.w);
+            sum = fmaf(p3, iv.w, fmaf(p2, iv.z, fmaf(p1, iv.y, fmaf(p0, iv.x, sum))));
             pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
           }
         } else {
@@ -968,14 +999,15 @@ __global__ void __launch_bounds__(f8::kThreads, 1)
 template <bool kRowScales, bool kTwoTerm>
 cudaError_t launch_instance(const CUtensorMap& tm_lat, const CUtensorMap& tm_rope, const MlaParams& prm,
                             int num_units, cudaStream_t stream) {
+  constexpr size_t kBytes = f8::smem_bytes<kTwoTerm, kRowScales>();
   static std::atomic<uint64_t> configured{0};  // per device: CUDA keeps the limit per device
   const cudaError_t e = configure_once(configured, [] {
     return cudaFuncSetAttribute(mla_fp8_kernel<kRowScales, kTwoTerm>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(f8::smem_bytes<kTwoTerm>()));
+                                static_cast<int>(kBytes));
   });
   if (e != cudaSuccess) return e;
-  return launch_dependent(mla_fp8_kernel<kRowScales, kTwoTerm>, dim3(num_units * 2), dim3(f8::kThreads),
-                          f8::smem_bytes<kTwoTerm>(), stream, tm_lat, tm_rope, prm);
+  return launch_dependent(mla_fp8_kernel<kRowScales, kTwoTerm>, dim3(num_units * 2), dim3(f8::kThreads), kBytes,
+                          stream, tm_lat, tm_rope, prm);
 }
 
 }  // namespace mla
