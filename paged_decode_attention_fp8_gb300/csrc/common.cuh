@@ -36,37 +36,15 @@ __device__ __forceinline__ void record_timeout_site(uint32_t site) {
   }
 }
 
-// Probes poll with the CTA-scope form (cheap); a wait on a barrier that
-// other CTAs arrive on (kCluster) takes one cluster-scope acquire fence after
-// the phase is seen complete, instead of an acquire at cluster scope on every poll.
-template <bool kCluster>
-__device__ __forceinline__ bool mbar_probe_try(uint64_t* bar, uint32_t parity) {
-  const bool ok = mbar_try_wait(bar, parity);
-  if constexpr (kCluster)
-    if (ok) fence_acq_rel_cluster();
-  return ok;
-}
-
-template <bool kCluster>
-__device__ __forceinline__ bool mbar_probe_test(uint64_t* bar, uint32_t parity) {
-  const bool ok = mbar_test_wait(bar, parity);
-  if constexpr (kCluster)
-    if (ok) fence_acq_rel_cluster();
-  return ok;
-}
-
 // Bounded wait on an mbarrier phase.  Returns false (without waiting further)
 // once *abort_flag is set by any thread of the CTA, or after the limit, in
-// which case it sets the flag and the status bit itself.  kCluster: the
-// barrier receives arrivals from other CTAs of the cluster, and completing
-// the wait acquires their released writes at cluster scope.
-template <bool kCluster = false>
+// which case it sets the flag and the status bit itself.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                              uint32_t* status, uint32_t site = 0) {
-  if (mbar_probe_try<kCluster>(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_probe_try<kCluster>(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
       if (it > kWaitMinPolls && globaltimer_ns() - t0 > *(volatile uint64_t*)&g_wait_limit_ns) {
@@ -81,13 +59,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, vol
 
 // The same contract as wait_bounded, but polling with the non-blocking probe:
 // for waits on the critical path, where a suspended thread wakes up late.
-template <bool kCluster = false>
 __device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                           uint32_t* status, uint32_t site = 0) {
-  if (mbar_probe_test<kCluster>(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_probe_test<kCluster>(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (abort_flag != nullptr && *abort_flag) return false;
       if (it > kWaitMinPolls && globaltimer_ns() - t0 > *(volatile uint64_t*)&g_wait_limit_ns) {

@@ -108,18 +108,16 @@ struct SegmentWalker {
 };
 
 // site: a source line recorded if the wait runs out
-template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                           uint32_t site = 0) {
-  const bool ok = wait_bounded<kCluster>(bar, parity, abort_flag, &g_status_mla, site);
+  const bool ok = wait_bounded(bar, parity, abort_flag, &g_status_mla, site);
   return __all_sync(0xffffffffu, ok);
 }
 
 // warp_wait polling without suspension, for the waits on the per-page critical path
-template <bool kCluster = false>
 __device__ __forceinline__ bool warp_spin(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                           uint32_t site = 0) {
-  const bool ok = wait_spin<kCluster>(bar, parity, abort_flag, &g_status_mla, site);
+  const bool ok = wait_spin(bar, parity, abort_flag, &g_status_mla, site);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -80,83 +80,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// ------------------------------------------------------------- cluster ----
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Address in the cluster's shared window of the same offset in CTA `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_u32(uint32_t caddr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-
-// Arrive `count` times on an mbarrier in any CTA of the cluster (cluster
-// address), releasing this thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr, uint32_t count) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(caddr), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-// Probes whose completion also acquires, at cluster scope, what the remote
-// arrivers released (for barriers that other CTAs of the cluster arrive on).
-__device__ __forceinline__ bool mbar_test_wait_cl(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\tselp.u32 "
-      "%0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\tselp.u32 "
-      "%0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Acquire-release fence at cluster scope: after a wait observed an mbarrier
-// phase that threads of another CTA completed with release arrivals, their
-// earlier writes are visible to this thread.
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-// Generic-proxy writes to shared memory anywhere in the cluster -> visible to the async proxy.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
 // ----------------------------------------------------------------- TMA ----
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -209,32 +132,8 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
-// 1-D bulk copy from this CTA's shared memory to shared memory of another CTA
-// of the cluster (cluster address), completing `bytes` of the transaction
-// count of the mbarrier at cluster address `bar` (in the destination CTA).
-// Both addresses and the size are multiples of 16 B.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   dst),
-               "r"(smem_u32(src)), "r"(bytes), "r"(bar)
-               : "memory");
-}
 
-// Asynchronous remote stores into shared memory of a CTA of the cluster
-// (cluster addresses): each completes its byte count on the mbarrier at
-// cluster address `bar` (in the destination CTA) when it lands; the storing
-// thread does not wait for them.
-__device__ __forceinline__ void st_async_v4(uint32_t dst, uint4 v, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
-               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
-               : "memory");
-}
 
-__device__ __forceinline__ void st_async_f32(uint32_t dst, float v, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
-               "r"(__float_as_uint(v)), "r"(bar)
-               : "memory");
-}
 
 // -------------------------------------------------- dependent launches ----
 
@@ -278,15 +177,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Arrive (once) on the mbarrier at the same shared-memory offset in every CTA
-// of `cta_mask` (cluster ranks) when this thread's tcgen05 ops so far complete.
-__device__ __forceinline__ void tc_commit_mc_if(bool issue, uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::"
-      "cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
-      "h"(cta_mask), "r"(issue ? 1u : 0u)
-      : "memory");
-}
 
 // Predicated forms for a converged warp: every lane executes the instruction
 // and only the lanes with `issue` set perform it (one elected lane), so the
@@ -317,14 +207,6 @@ __device__ __forceinline__ void mma_f8_ts_if(bool issue, uint32_t d_tmem, uint32
       : "memory");
 }
 
-__device__ __forceinline__ void mma_f16_ts_if(bool issue, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t@q tcgen05.mma.cta_group::1."
-      "kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue ? 1u : 0u)
-      : "memory");
-}
 
 __device__ __forceinline__ void mma_f16_ss_if(bool issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
@@ -335,14 +217,6 @@ __device__ __forceinline__ void mma_f16_ss_if(bool issue, uint32_t d_tmem, uint6
       : "memory");
 }
 
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, "
-      "p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 // Instruction descriptor (kind::f16 / kind::f8f6f4, dense):
 //   [4,6) D format (1 = f32), [7,10) A format, [10,13) B format,
@@ -469,13 +343,6 @@ __device__ __forceinline__ float f16_hi(uint32_t x) {
   return f;
 }
 
-// Four E4M3 bytes -> two bf16x2 words (exact).
-__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t x, uint32_t& lo, uint32_t& hi) {
-  uint32_t a = e4m3x2_to_f16x2(x & 0xFFFFu);
-  uint32_t b = e4m3x2_to_f16x2(x >> 16);
-  lo = pack_bf16x2(f16_lo(a), f16_hi(a));
-  hi = pack_bf16x2(f16_lo(b), f16_hi(b));
-}
 
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
@@ -489,13 +356,6 @@ __device__ __forceinline__ void split_e4m3x4(float a, float b, float c, float d,
   lo = pack_e4m3x4(a - f16_lo(h01), b - f16_hi(h01), c - f16_lo(h23), d - f16_hi(h23));
 }
 
-// 4-byte global -> shared copy that does not go through registers; completes
-// for this thread at cp_async_wait_all
-__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)),
-               "l"(reinterpret_cast<uint64_t>(src))
-               : "memory");
-}
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
@@ -513,13 +373,7 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
-}
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
-}
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
