@@ -645,8 +645,9 @@ def leg_gqa(dev, peaks, steps, warmup, variant="plain"):
     q = (syn.gqa_block_q(5, bs, q_len, h_q) if variant == "xqa" else inp.q.unsqueeze(1)).to(dev)
     mask = syn.spec_mask(5, bs, q_len).to(dev) if variant == "xqa" else None
     sinks = syn.sink_logits(5, h_q).to(dev) if variant == "xqa" else None
-    longest = min(bt.shape[1] * 16, window + q_len - 1 + 128) if window else bt.shape[1] * 16
-    splits = fm.gqa_num_splits(bs, h_kv, longest)
+    # the split count each entry point will choose (the extended one is window-aware)
+    splits = (fm.gqa_num_splits(bs, h_kv, bt.shape[1] * 16) if variant == "plain"
+              else fm.gqa_ext_num_splits(bs, h_kv, bt.shape[1] * 16, q_len, window))
     ws = torch.empty((max(fm.gqa_workspace_bytes(bs, h_q, hd, splits), 256),), dtype=torch.uint8, device=dev)
     out = torch.empty((bs, q_len, h_q, hd), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((bs, q_len, h_q), dtype=torch.float32, device=dev)

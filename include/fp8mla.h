@@ -234,8 +234,11 @@ FP8MLA_API size_t sparse_mla_workspace_bytes(int s_q, int h_q, int topk, int num
  *   v_cache      E4M3 bytes [num_blocks, h_kv, page_size, head_dim]
  *   k_scale, v_scale  float32 [1] each (device), NULL refused
  *   block_table  int32 [bs, max_blocks]; seqlens int32 [bs]
- *   num_splits   0 = auto (no split while bs * h_kv fills the GPU, else
- *                enough key shards to fill it, at most 16); k >= 1 forced
+ *   num_splits   0 = auto: when bs * h_kv CTAs already fill the GPU, every
+ *                sequence is cut into a few key shards (about six CTAs per
+ *                SM, at least 8 steps of 128 keys each, at most 16) so that
+ *                unequal lengths balance; otherwise the fewest shards that
+ *                fill the waves; k >= 1 forced
  *   workspace    >= paged_gqa_workspace_bytes(bs, h_q, head_dim, splits)
  *   out          bf16 [bs, h_q, head_dim]; lse float32 [bs, h_q]
  * Requires head_dim == 128, page_size == 16, h_q % h_kv == 0, h_q / h_kv <= 16. */
@@ -265,7 +268,10 @@ FP8MLA_API fp8mla_status_t paged_gqa_decode(const void* q, const void* k_cache, 
  *   out          bf16 [bs, q_len, h_q, head_dim]; lse float32 [bs, q_len, h_q]
  * A row that sees no key gets out = 0 and lse = its sink (-inf without one).
  * Requires q_len >= 1 and q_len * (h_q / h_kv) <= 16, window >= 0, and the
- * other requirements of paged_gqa_decode; workspace as paged_gqa_decode's. */
+ * other requirements of paged_gqa_decode; workspace as paged_gqa_decode's.
+ * Auto splits: paged_gqa_ext_num_splits (with a window, a grid that fills the
+ * GPU is not split; never more shards than paged_gqa_num_splits gives, so its
+ * workspace size suffices). */
 FP8MLA_API fp8mla_status_t paged_gqa_decode_ext(const void* q, const void* k_cache, const void* v_cache,
                                                 fp8mla_kv_dtype_t kv_dtype, int num_blocks, const float* k_scale,
                                                 const float* v_scale, int scale_per_row, const int32_t* block_table,
@@ -280,6 +286,15 @@ FP8MLA_API size_t paged_gqa_workspace_bytes(int bs, int h_q, int head_dim, int m
 /* Number of key shards paged_gqa_decode will use for these arguments
  * (num_splits as passed: 0 = auto).  Host-only, no device access. */
 FP8MLA_API int paged_gqa_num_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_splits);
+
+/* Number of key shards paged_gqa_decode_ext will use: paged_gqa_num_splits's
+ * rule, except that with a window (window > 0) max_seqlen is taken as the
+ * keys the window spans (window + q_len - 1 + 128 at most) and a grid of
+ * bs * h_kv CTAs that already fills the GPU is not split (the window makes
+ * the sequences' work nearly equal); never more than paged_gqa_num_splits
+ * gives for the same arguments.  Host-only. */
+FP8MLA_API int paged_gqa_ext_num_splits(int bs, int h_kv, int max_seqlen, int q_len, int window, int num_sms,
+                                        int num_splits);
 
 /* ---------------------------------------------------------- cache write ---
  * fp8_paged_cache_write -- quantise-on-write of new K or V rows into an E4M3

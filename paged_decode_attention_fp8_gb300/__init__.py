@@ -64,6 +64,7 @@ _SIGNATURES = {
                                   _P, _P, _I, _I, _I, _I, _I, _P]),
     "paged_gqa_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "paged_gqa_num_splits": (_I, [_I, _I, _I, _I, _I]),
+    "paged_gqa_ext_num_splits": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "fp8mla_decode_no_alloc": (_I, [_P, _P, _I, _I, _P, _I, _P, _P, _F, _I, _P, _P, _I, _I, _I, _I, _P]),
     "fp8_paged_cache_write": (_I, [_P, ctypes.c_int64, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "fp8mla_get_last_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -297,6 +298,13 @@ def gqa_num_splits(bs: int, h_kv: int, max_seqlen: int, num_splits: int = 0, sms
     return lib().paged_gqa_num_splits(bs, h_kv, max_seqlen, num_sms() if sms is None else sms, num_splits)
 
 
+def gqa_ext_num_splits(bs: int, h_kv: int, max_seqlen: int, q_len: int = 1, window: int = 0, num_splits: int = 0,
+                       sms: int | None = None) -> int:
+    """The key shards paged_gqa_decode_ext uses (window-aware; never more than gqa_num_splits)."""
+    return lib().paged_gqa_ext_num_splits(bs, h_kv, max_seqlen, q_len, window, num_sms() if sms is None else sms,
+                                          num_splits)
+
+
 def gqa_workspace_bytes(bs: int, h_q: int, head_dim: int, max_splits: int) -> int:
     return lib().paged_gqa_workspace_bytes(bs, h_q, head_dim, max_splits)
 
@@ -379,9 +387,7 @@ def paged_gqa_decode_ext(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
         softmax_scale = 1.0 / math.sqrt(hd)
     if max_seqlen is None:
         max_seqlen = block_table.shape[1] * page
-    if window > 0:  # a window bounds the keys any sequence reads (plus one step of alignment)
-        max_seqlen = min(max_seqlen, window + q_len - 1 + 128)
-    splits = gqa_num_splits(bs, h_kv, max_seqlen, num_splits)
+    splits = gqa_ext_num_splits(bs, h_kv, max_seqlen, q_len, window, num_splits)
     if out is None:
         out = torch.empty((bs, q_len, h_q, hd), dtype=torch.bfloat16, device=q.device)
     if lse is None:

@@ -351,6 +351,12 @@ int paged_gqa_num_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_
   return gqa_choose_splits(bs, h_kv, max_seqlen, num_sms, num_splits);
 }
 
+int paged_gqa_ext_num_splits(int bs, int h_kv, int max_seqlen, int q_len, int window, int num_sms, int num_splits) {
+  long long longest = max_seqlen;
+  if (window > 0) longest = std::min(longest, static_cast<long long>(window) + std::max(q_len, 1) - 1 + 128);
+  return gqa_choose_splits(bs, h_kv, static_cast<int>(longest), num_sms, num_splits, window > 0);
+}
+
 fp8mla_status_t paged_gqa_decode(const void* q, const void* k_cache, const void* v_cache,
                                  fp8mla_kv_dtype_t kv_dtype, int num_blocks, const float* k_scale,
                                  const float* v_scale, const int32_t* block_table, int max_blocks,

@@ -11,7 +11,9 @@
 namespace fp8mla {
 
 size_t gqa_workspace_bytes(int bs, int h_q, int head_dim, int max_splits);
-int gqa_choose_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_splits);
+// capped: a sliding window bounds every sequence's keys (pieces need no balancing: a
+// grid that fills the GPU is not split)
+int gqa_choose_splits(int bs, int h_kv, int max_seqlen, int num_sms, int num_splits, bool capped = false);
 // q_len query tokens per sequence (the last q_len cache positions) under spec_mask
 // [bs, q_len, q_len] (null: causal inside the block), a sliding window (0: off) and
 // sink logits [h_q] (null: none); scale_rows: k_scale / v_scale per cached row

@@ -263,3 +263,9 @@ def test_gqa_split_rule_on_the_host():
     # and 8 s / 152 >= 0.85 * 128 / 152 first at s = 14
     assert lib.paged_gqa_num_splits(1, 8, 16384, 152, 0) == 14
     assert lib.paged_gqa_num_splits(1, 8, 128, 152, 0) == 1        # one step: nothing to split
+    # the extended entry with a window: nearly equal pieces need no balancing, so a grid that
+    # fills the GPU (256 CTAs) is not split; a small grid still splits to fill its wave
+    assert lib.paged_gqa_ext_num_splits(32, 8, 16384, 4, 4096, 152, 0) == 1
+    assert lib.paged_gqa_ext_num_splits(32, 8, 16384, 4, 0, 152, 0) == 4   # no window: the plain rule
+    assert lib.paged_gqa_ext_num_splits(1, 8, 16384, 4, 4096, 152, 0) == 14  # a small grid: waves
+    assert lib.paged_gqa_ext_num_splits(32, 8, 16384, 4, 4096, 152, 3) == 3  # forced
