@@ -19,8 +19,10 @@
 //     softmax adds a column's two S values, the epilogue its two O values.
 //     Q carries a per-column power-of-two scale; P is stored x64 with the
 //     lazy reference raised only past 2.75 (64 * 2^2.75 < 448).
-//   * Softmax across TMEM lanes (one thread per token: per-column max by
-//     shuffles + a 4-warp exchange; each thread keeps partial sums).  Tokens
+//   * Softmax across TMEM lanes (one thread per token; each thread keeps
+//     partial sums).  A step first votes whether any score passes its
+//     column's reference by more than 2.75; only then are the per-column
+//     maxima taken (shuffles + a 4-warp exchange).  Tokens
 //     past the end are masked by select, and their V rows zeroed in shared
 //     memory before P.V reads the tile.
 //   * ~113 KB of shared memory and 128 TMEM columns per CTA: two CTAs share
@@ -29,9 +31,11 @@
 //     grids the split count follows the FA2-style "waves" rule, the smallest
 //     count within 85% of the best wave efficiency (InfiniCore page,
 //     Summary: the "auto" heuristic); a grid that already fills the GPU is
-//     still cut into about six CTAs per SM so unequal contexts balance.
+//     still cut into about six CTAs per SM so unequal contexts balance,
+//     unless a sliding window caps every piece (then it is not split).
 //   * Per-row scales [num_blocks, h_kv, 16] (InfiniCore page, Summary): each
-//     page's 16 K and 16 V scales arrive by bulk copy with its tiles; a
+//     page's 16 K and 16 V scales arrive by the producer lanes' cp.async
+//     with its tiles, on the same barrier; a
 //     token's K scale multiplies its scores in fp32, and its V scale enters
 //     the weights: u = score + log2 sigma_v, P' = 2^(u - m) carries sigma_v
 //     into P.V on the raw codes, and the row sums take P' / sigma_v.

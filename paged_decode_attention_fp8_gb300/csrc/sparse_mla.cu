@@ -39,7 +39,8 @@
 //     partial columns, so the merge is one round trip and has no barrier.
 //     (Merging inside a cooperatively launched decode grid was tried: the
 //     cooperative launch alone cost ~4.6 us per call at s_q = 2, more than
-//     the combine kernel.)  Because V = K, the first-order LSE error of Q's
+//     the combine kernel; so was merging inside thread-block clusters over
+//     distributed shared memory: slower at s_q = 2 and 16.)  Because V = K, the first-order LSE error of Q's
 //     quantisation is scale * (q_hat - q) . out, which the epilogue (or the
 //     combine) subtracts.
 #include <cuda.h>
