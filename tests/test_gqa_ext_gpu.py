@@ -157,3 +157,29 @@ def test_xqa_options(case):
     assert np.array_equal(np.isneginf(l_gpu), np.isneginf(rl))
     assert_close(compare(out, lse, ro, rl, "bf16"), "bf16")
     assert fm.last_device_error() == 0
+
+
+def test_window_on_a_full_grid_runs_unsplit():
+    """With a window, a grid that fills the GPU (16 sequences x 8 KV heads) is not split: the
+    library's choice is 1, and the unsplit call matches the oracle and a forced 4-way split."""
+    h_kv, group, q_len, window = 8, 4, 4, 256
+    seqlens = [int(x) for x in np.random.default_rng(45).integers(200, 1400, 16)]
+    inp = syn.gqa_inputs(45, len(seqlens), seqlens, h_q=h_kv * group, h_kv=h_kv, spare_blocks=4)
+    assert fm.gqa_ext_num_splits(len(seqlens), h_kv, inp.block_table.shape[1] * 16, q_len, window) == 1
+    d = _dev_inputs(inp)
+    q = syn.gqa_block_q(45, len(seqlens), q_len, h_kv * group)
+    mask = syn.spec_mask(45, len(seqlens), q_len)
+    sinks = syn.sink_logits(45, h_kv * group)
+    ks = torch.tensor([inp.k_scale], dtype=torch.float32, device=DEV)
+    vs = torch.tensor([inp.v_scale], dtype=torch.float32, device=DEV)
+    runs = {}
+    for splits in (0, 4):
+        runs[splits] = fm.paged_gqa_decode_ext(q.to(DEV), d["kc"], d["vc"], d["bt"], d["sl"], ks, vs,
+                                               inp.softmax_scale, spec_mask=mask.to(DEV), window=window,
+                                               sinks=sinks.to(DEV), num_splits=splits)
+    torch.cuda.synchronize()
+    ro, rl = gqa_decode_ext(q, inp.k_cache, inp.v_cache, inp.block_table, inp.seqlens, inp.k_scale, inp.v_scale,
+                            inp.softmax_scale, spec_mask=mask.numpy(), window=window, sinks=sinks.numpy())
+    for splits, (out, lse) in runs.items():
+        assert_close(compare(out, lse, ro, rl, "bf16"), "bf16")
+    assert fm.last_device_error() == 0
