@@ -3,7 +3,9 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <mutex>
 #include <utility>
 
 #include "fp8mla.h"
@@ -11,6 +13,43 @@
 #include "ptx.cuh"
 
 namespace fp8mla {
+
+// The last N tensor maps an entry point encoded, by (base pointer, extent,
+// device): a map depends on nothing else (its boxes and strides are fixed per
+// entry point), so a call on the same cache skips the host-side encoding.
+template <int N>
+class TensorMapCache {
+ public:
+  template <typename Encode>
+  bool get(const void* base, long long extent, CUtensorMap* out, Encode&& encode) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu_);
+    for (const Entry& e : entries_)
+      if (e.used && e.base == base && e.extent == extent && e.device == dev) {
+        *out = e.map;
+        return true;
+      }
+    CUtensorMap m;
+    if (!encode(&m)) return false;
+    entries_[next_] = Entry{base, extent, dev, true, m};
+    next_ = (next_ + 1) % N;
+    *out = m;
+    return true;
+  }
+
+ private:
+  struct Entry {
+    const void* base;
+    long long extent;
+    int device;
+    bool used;
+    CUtensorMap map;
+  };
+  std::mutex mu_;
+  Entry entries_[N] = {};
+  int next_ = 0;
+};
 
 // A wait that has not completed after this long is treated as a hang: the
 // kernel records FP8MLA_DEV_WAIT_TIMEOUT and stops instead of spinning on.

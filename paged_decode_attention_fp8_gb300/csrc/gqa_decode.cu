@@ -776,7 +776,10 @@ fp8mla_status_t gqa_decode_entry(const void* q, const void* k_cache, const void*
   }
   const long long rows = static_cast<long long>(num_blocks) * h_kv * gqa::kPage;
   CUtensorMap tk, tv;
-  if (!gqa::encode_pages(&tk, k_cache, rows) || !gqa::encode_pages(&tv, v_cache, rows)) return FP8MLA_ERR_CUDA;
+  static TensorMapCache<16> maps;
+  if (!maps.get(k_cache, rows, &tk, [&](CUtensorMap* m) { return gqa::encode_pages(m, k_cache, rows); }) ||
+      !maps.get(v_cache, rows, &tv, [&](CUtensorMap* m) { return gqa::encode_pages(m, v_cache, rows); }))
+    return FP8MLA_ERR_CUDA;
   gqa::Params prm;
   prm.q = static_cast<const uint16_t*>(q);
   prm.block_table = block_table;

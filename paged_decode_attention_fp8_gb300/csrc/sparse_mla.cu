@@ -739,7 +739,9 @@ fp8mla_status_t sparse_decode_entry(const void* q, const void* kv_cache, int64_t
     return workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) ? FP8MLA_ERR_INVALID_ARG
                                                                                  : FP8MLA_ERR_WORKSPACE_TOO_SMALL;
   CUtensorMap tm;
-  if (!sparse::encode_rows(&tm, kv_cache, num_tokens)) return FP8MLA_ERR_CUDA;
+  static TensorMapCache<8> maps;
+  if (!maps.get(kv_cache, num_tokens, &tm, [&](CUtensorMap* m) { return sparse::encode_rows(m, kv_cache, num_tokens); }))
+    return FP8MLA_ERR_CUDA;
   sparse::Params prm;
   char* ws = static_cast<char*>(workspace);
   prm.q = static_cast<const uint16_t*>(q);
