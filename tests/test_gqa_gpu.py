@@ -90,3 +90,16 @@ def test_bad_block_reported():
     inp.block_table[0, 1] = 10 ** 6
     run(inp, 1)
     assert fm.last_device_error() & fm.DEV_BAD_PAGE
+
+
+def test_alternating_caches_use_their_own_tensor_maps():
+    # encoded tensor maps are kept by (base pointer, extent, device): alternating K/V caches of
+    # one shape, and caches of another pool size, each read their own
+    a = syn.gqa_inputs(61, 3, [300, 17, 900], spare_blocks=2)
+    b = syn.gqa_inputs(62, 3, [300, 17, 900], spare_blocks=2)
+    c = syn.gqa_inputs(63, 3, [64, 1000, 5], spare_blocks=9)
+    for inp in (a, b, a, c, b):
+        out, lse = run(inp, 0)
+        ro, rl = ref(inp)
+        assert_close(compare(out, lse, ro, rl, "bf16"), "bf16")
+    assert fm.last_device_error() == 0

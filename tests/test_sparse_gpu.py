@@ -146,3 +146,16 @@ def test_prefill_scale_sampled():
     record("sparse_prefill_sq16384_sampled", m)
     assert_close(m, "fp8")
     assert fm.last_device_error() == 0
+
+
+def test_alternating_caches_use_their_own_tensor_maps():
+    # the entry point keeps encoded tensor maps by (base pointer, extent, device): calls that
+    # alternate between two caches of one shape, and a third of another size, each read their own
+    a = syn.sparse_inputs(16, 2, num_tokens=4096, topk=512)
+    b = syn.sparse_inputs(17, 2, num_tokens=4096, topk=512)
+    c = syn.sparse_inputs(18, 2, num_tokens=6000, topk=512)
+    for inp in (a, b, a, c, b):
+        out, lse = run(inp)
+        ro, rl = ref(inp)
+        assert_close(compare(out, lse, ro, rl, "fp8"), "fp8")
+    assert fm.last_device_error() == 0
