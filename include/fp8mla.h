@@ -142,9 +142,9 @@ FP8MLA_API fp8mla_status_t fp8mla_get_metadata(const int32_t* cache_seqlens, int
                                     fp8mla_stream_t stream);
 
 /* Workspace of fp8mla_decode: (b + num_units) split-KV partial slots of
- * 128 x 512 bf16 accumulators plus 128 (m, l) pairs each, then (FP8 dots) per
- * sequence its quantised Q (88 064 bytes: the decode kernel's Q slots) and
- * 128 Q scales. */
+ * 128 x 512 bf16 accumulators plus 128 (m, l) pairs each, then per sequence
+ * its quantised Q, the E4M3 hi term in both dot modes (88 064 bytes: the
+ * decode kernel's Q slots), and 128 Q scales. */
 FP8MLA_API size_t fp8mla_workspace_bytes(int b, int s_q, int h_q, int num_units);
 
 /* fp8mla_decode -- dense MLA decode over the paged E4M3 cache.
@@ -369,7 +369,7 @@ FP8MLA_API fp8mla_status_t fp8mla_decode_no_alloc(const void* q, const void* kv_
 
 /* Stage timing of fp8mla_decode, a measurement aid (off by default).  While
  * enabled, fp8mla_decode records CUDA events before and after each of its
- * kernels (Q quantisation for FP8 dots, the decode kernel, the combine);
+ * kernels (Q quantisation, the decode kernel, the combine);
  * those events keep the kernels from overlapping one another, so time the
  * call itself with timing off.  One timer per process, used by one thread at
  * a time: a decode call that times holds it for the call.  Enabling or

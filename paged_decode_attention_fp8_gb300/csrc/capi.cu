@@ -115,7 +115,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [partial O | partial (m, l) | quantised Q (FP8 dots) | per-row Q scale]
+// Workspace: [partial O | partial (m, l) | quantised Q (E4M3 hi term) | per-row Q scale]
 struct MlaWorkspace {
   size_t o, ml, qbuf, qscale, total;
 };

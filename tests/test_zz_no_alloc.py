@@ -2,8 +2,8 @@
 allocate device memory.
 
 Such callers pass only inputs and outputs; the library keeps the tile
-schedule, the split counts and (FP8 dots) the quantised Q with its per-row
-scales in a fixed device array of its own.  It
+schedule, the split counts and the quantised Q (its E4M3 hi term, in both dot
+modes) with its per-row scales in a fixed device array of its own.  It
 schedules one unit per sequence, so fp8mla_decode with one unit per sequence
 (force_splits=1) runs the same kernels on the same schedule: the results must
 be bit-identical.  Two different batches are decoded in a row, so the second
