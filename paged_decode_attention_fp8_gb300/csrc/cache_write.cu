@@ -20,9 +20,9 @@
 //
 // HBM-bound streaming.  A group of L lanes (the largest power of two up to 32
 // that the row's 16-byte chunks fill) owns a row; each warp walks its rows in
-// a grid-stride loop, R rows per group per step (R x chunks per lane <= 4),
-// with the next step's 16-byte loads issued before the current step is
-// worked on.  A step reduces each row's amax across its group with shuffles;
+// a grid-stride loop (four CTAs per SM), R rows per group per step (R = 2
+// when a lane holds one chunk of a row, else 1), with the next step's 16-byte
+// loads issued before the current step is worked on.  A step reduces each row's amax across its group with shuffles;
 // lane r of the group divides for row r and hands the reciprocal round by
 // shuffle (and stores row r's scale), so a lane does one division per step;
 // then each lane stores 8 codes per chunk.  Integer division by h_kv and the
@@ -72,10 +72,13 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
   return f.d == 1 ? n : (__umulhi(n, f.m) >> f.s);
 }
 
-// Rows per group per step: R x (chunks per lane) <= 4 loads in flight per lane.
+// Rows per group per step.  With four CTAs per SM, two rows of one chunk per
+// lane measured fastest on the 128-wide rows of a GQA cache: more rows or more
+// CTAs in flight make the scattered 128-byte stores slower, fewer leave HBM
+// idle.
 template <int kC>
 __host__ __device__ constexpr int rows_per_step() {
-  return kC >= 4 ? 1 : 4 / kC;
+  return kC >= 2 ? 1 : 2;
 }
 
 template <int kR, int kC>
@@ -85,7 +88,7 @@ struct CwStep {
 };
 
 template <int kL, int kC>
-__global__ void __launch_bounds__(kCwThreads, 3) cache_write_kernel(
+__global__ void __launch_bounds__(kCwThreads, 4) cache_write_kernel(
     const uint16_t* __restrict__ x, int64_t x_token_stride, const int32_t* __restrict__ slot_mapping,
     uint32_t n_rows, FastDiv div_h, int head_dim, FastDiv div_page, uint32_t num_slots, uint8_t* __restrict__ cache,
     const float* __restrict__ tensor_scale, float* __restrict__ token_scales) {
@@ -257,7 +260,7 @@ cudaError_t launch_cw(const CacheWriteArgs& a, cudaStream_t stream) {
   constexpr int kBlockRows = (kCwThreads / 32) * (32 / kL) * rows_per_step<kC>();
   const int64_t rows = static_cast<int64_t>(a.n_tokens) * a.h_kv;
   const int64_t need = (rows + kBlockRows - 1) / kBlockRows;
-  const int64_t cap = static_cast<int64_t>(device_sms()) * 3;  // one wave of resident CTAs
+  const int64_t cap = static_cast<int64_t>(device_sms()) * 4;  // one wave of resident CTAs
   const int64_t blocks = need < cap ? need : cap;
   cache_write_kernel<kL, kC><<<static_cast<unsigned>(blocks), kCwThreads, 0, stream>>>(
       a.x, a.x_token_stride, a.slot_mapping, static_cast<uint32_t>(rows), make_fast_div(a.h_kv), a.head_dim,
