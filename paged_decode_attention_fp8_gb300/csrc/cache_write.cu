@@ -18,11 +18,14 @@
 // (block s / page, offset s % page); a negative slot skips the token, a slot
 // past the cache sets FP8MLA_DEV_BAD_SLOT and skips it.
 //
-// HBM-bound streaming.  A group of L lanes (the largest power of two up to 32
-// that the row's 16-byte chunks fill) owns a row; each warp walks its rows in
-// a grid-stride loop (four CTAs per SM), R rows per group per step (R = 2
-// when a lane holds one chunk of a row, else 1), with the next step's 16-byte
-// loads issued before the current step is worked on.  A step reduces each row's amax across its group with shuffles;
+// HBM-bound streaming.  A group of L lanes owns a row: the fewest (a power of
+// two, at most 32) that leave each lane at most three of the row's 16-byte
+// chunks, so a lane holds two chunks of a power-of-two row and the row's
+// index arithmetic, done by every lane of the group, is spread over 32 bytes
+// or more.  Each warp walks its rows in a grid-stride loop (four CTAs per SM),
+// R rows per group per step (R = 2 when a lane holds one or two chunks of a
+// row, else 1), with the next step's 16-byte loads issued before the current
+// step is worked on.  A step reduces each row's amax across its group with shuffles;
 // lane r of the group divides for row r and hands the reciprocal round by
 // shuffle (and stores row r's scale), so a lane does one division per step;
 // then each lane stores 8 codes per chunk.  Integer division by h_kv and the
@@ -72,13 +75,11 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
   return f.d == 1 ? n : (__umulhi(n, f.m) >> f.s);
 }
 
-// Rows per group per step.  With four CTAs per SM, two rows of one chunk per
-// lane measured fastest on the 128-wide rows of a GQA cache: more rows or more
-// CTAs in flight make the scattered 128-byte stores slower, fewer leave HBM
-// idle.
+// Rows per group per step: two while a lane holds at most two chunks of a
+// row (four 16-byte loads in flight per lane), else one.
 template <int kC>
 __host__ __device__ constexpr int rows_per_step() {
-  return kC >= 2 ? 1 : 2;
+  return kC >= 3 ? 1 : 2;
 }
 
 template <int kR, int kC>
@@ -274,7 +275,7 @@ cudaError_t launch_cw(const CacheWriteArgs& a, cudaStream_t stream) {
 int cache_write_group_lanes(int head_dim) {
   const int chunks = head_dim / 8;
   int l = 1;
-  while (l * 2 <= chunks && l < 32) l *= 2;
+  while (l < 32 && (chunks + l - 1) / l > 3) l *= 2;
   return l;
 }
 
@@ -293,19 +294,20 @@ fp8mla_status_t cache_write_entry(const CacheWriteArgs& a, cudaStream_t stream) 
       (a.token_scales != nullptr && reinterpret_cast<uintptr_t>(a.token_scales) % 4 != 0))
     return FP8MLA_ERR_INVALID_ARG;
   const int l = cache_write_group_lanes(a.head_dim);
-  const int c = (a.head_dim / 8 + l - 1) / l;  // chunks per lane: <= 2 below 32 lanes, <= 4 at 32
+  const int c = (a.head_dim / 8 + l - 1) / l;  // chunks per lane: <= 3 below 32 lanes, <= 4 at 32
   cudaError_t e;
   switch (l * 8 + c) {
     case 1 * 8 + 1: e = launch_cw<1, 1>(a, stream); break;
-    case 2 * 8 + 1: e = launch_cw<2, 1>(a, stream); break;
+    case 1 * 8 + 2: e = launch_cw<1, 2>(a, stream); break;
+    case 1 * 8 + 3: e = launch_cw<1, 3>(a, stream); break;
     case 2 * 8 + 2: e = launch_cw<2, 2>(a, stream); break;
-    case 4 * 8 + 1: e = launch_cw<4, 1>(a, stream); break;
+    case 2 * 8 + 3: e = launch_cw<2, 3>(a, stream); break;
     case 4 * 8 + 2: e = launch_cw<4, 2>(a, stream); break;
-    case 8 * 8 + 1: e = launch_cw<8, 1>(a, stream); break;
+    case 4 * 8 + 3: e = launch_cw<4, 3>(a, stream); break;
     case 8 * 8 + 2: e = launch_cw<8, 2>(a, stream); break;
-    case 16 * 8 + 1: e = launch_cw<16, 1>(a, stream); break;
+    case 8 * 8 + 3: e = launch_cw<8, 3>(a, stream); break;
     case 16 * 8 + 2: e = launch_cw<16, 2>(a, stream); break;
-    case 32 * 8 + 1: e = launch_cw<32, 1>(a, stream); break;
+    case 16 * 8 + 3: e = launch_cw<16, 3>(a, stream); break;
     case 32 * 8 + 2: e = launch_cw<32, 2>(a, stream); break;
     case 32 * 8 + 3: e = launch_cw<32, 3>(a, stream); break;
     case 32 * 8 + 4: e = launch_cw<32, 4>(a, stream); break;

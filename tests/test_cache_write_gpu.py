@@ -45,7 +45,10 @@ def _ref(inp, x, per_row=True, tensor_scale=None):
     return ref_write(x, inp.slot_mapping, cache, inp.page, tensor_scale=tensor_scale)
 
 
-@pytest.mark.parametrize("hd", [8, 16, 24, 64, 128, 200, 256, 512, 576, 1024])
+# every lane-group shape the kernel has: one to three chunks of 8 values per
+# lane at 1 lane, two or three at 2-16 lanes, two to four at 32; 40, 80, 200
+# and 328 leave some lanes of each group without a chunk
+@pytest.mark.parametrize("hd", [8, 16, 24, 32, 40, 64, 80, 128, 192, 200, 256, 328, 512, 576, 1024])
 def test_per_row_head_dims(hd):
     # ragged lengths (partial last blocks), padding slots, several row groups per warp
     inp = syn.cache_write_inputs(21, [37, 5, 70], h_kv=2, hd=hd, page=16, base_tokens=64, spare_blocks=3,
