@@ -119,6 +119,8 @@ def test_zero_rows_and_extreme_magnitudes():
     x[8] *= 2.0 ** -100
     x[9, 0, :] = 0.0
     x[9, 0, 17] = -2.0 ** -120                   # one tiny nonzero value in a row
+    x[10, 1, :] = 0.0
+    x[10, 1, 40] = 2.0 ** -130                   # a bf16 subnormal: the row's amax must keep it
     x = x.to(torch.bfloat16)
     got, gs = _run(inp, x)
     want, ws = _ref(inp, x)
