@@ -46,8 +46,8 @@ def _ref(inp, x, per_row=True, tensor_scale=None):
 
 
 # every lane-group shape the kernel has: one to three chunks of 8 values per
-# lane at 1 lane, two or three at 2-16 lanes, two to four at 32; 40, 80, 200
-# and 328 leave some lanes of each group without a chunk
+# lane at 1 lane, two or three at 2-16 lanes, two to four at 32; 40, 80, 200,
+# 328 and 576 leave some lanes of each group without a chunk
 @pytest.mark.parametrize("hd", [8, 16, 24, 32, 40, 64, 80, 128, 192, 200, 256, 328, 512, 576, 1024])
 def test_per_row_head_dims(hd):
     # ragged lengths (partial last blocks), padding slots, several row groups per warp
